@@ -1,0 +1,122 @@
+"""Pins for the oracle's Markov-head block draft.
+
+Sources: DSpark explainer (papers.franksyz.com mainline topic 31) section 6
+(parallel backbone gives base logits, a light sequential head conditions on
+the anchor and the sampled in-block prefix) and section 7 (drafter logits =
+U_k + B_k; the Markov head looks only at the previous token through a low-rank
+factorisation); llama.cpp PR 25173 description (anchor-first block, bias(prev)
+= markov_w2 . markov_w1[prev], sampled left to right).
+"""
+import numpy as np
+import pytest
+from scipy import stats
+
+from speculative_decoding_dspark_gb300 import inputs
+
+
+def _bf16_decode(b):
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_markov_bias_is_gemv(orc, dtype):
+    """b = W2 @ W1[prev] (rows of both factors are rank-vectors), against numpy."""
+    w = inputs.workload("batched_sampling", R=2, V=333, gamma=2, rank=24, w_dtype=dtype)
+    d = inputs.draft_inputs(w)
+    dec = _bf16_decode if dtype == "bf16" else (lambda a: a.astype(np.float64))
+    W1, W2 = dec(d["W1"]), dec(d["W2"])
+    for prev in [0, 7, 332]:
+        ref = W2 @ W1[prev]
+        np.testing.assert_allclose(orc.markov_bias(d["W1"], d["W2"], prev), ref, rtol=1e-12, atol=1e-15)
+        # the transposed reading (W1 @ W2[prev]) is a different vector
+        assert not np.allclose(W1 @ W2[prev], ref)
+    assert np.all(orc.markov_bias(d["W1"], d["W2"], -1) == 0.0)
+
+
+def test_logsumexp_closed_forms(orc):
+    for V in [1, 64, 151936]:
+        assert orc.logsumexp(np.full(V, 2.5)) == pytest.approx(2.5 + np.log(V), rel=1e-13)
+    x = np.array([1000.0, -np.inf, 1000.0])
+    assert orc.logsumexp(x) == pytest.approx(1000.0 + np.log(2.0), rel=1e-15)
+    s = orc.softmax(np.array([0.0, np.log(3.0)]))
+    np.testing.assert_allclose(s, [0.25, 0.75], rtol=1e-14)
+
+
+def _draft_numpy_greedy(d, W1, W2, U):
+    R, gamma, V = U.shape
+    y = np.zeros((R, gamma), np.int64)
+    for r in range(R):
+        prev = int(d["anchor"][r])
+        for k in range(gamma):
+            s = U[r, k] + (W2 @ W1[prev] if prev >= 0 else 0.0)
+            y[r, k] = int(np.argmax(s))
+            prev = y[r, k]
+    return y
+
+
+def test_greedy_draft_is_semi_autoregressive_argmax(orc):
+    """T = 0: y_k = argmax(U_k + W2 W1[y_{k-1}]), y_{-1} = anchor."""
+    w = inputs.workload("qwen3_8b_greedy", R=4, V=700, gamma=6, rank=32, w_sigma=0.4)
+    d = inputs.draft_inputs(w)
+    out = orc.markov_draft(d["U"], d["W1"], d["W2"], d["anchor"], d["seeds"], 0, 0.0)
+    ref = _draft_numpy_greedy(d, _bf16_decode(d["W1"]), _bf16_decode(d["W2"]), _bf16_decode(d["U"]))
+    assert (out["y"] == ref).all()
+    # the chain really depends on the previous token: a different anchor changes position 0
+    d2 = dict(d, anchor=(d["anchor"] + 1) % w["V"])
+    out2 = orc.markov_draft(d["U"], d["W1"], d["W2"], d2["anchor"], d["seeds"], 0, 0.0)
+    assert not np.array_equal(out["q_logits"][:, 0], out2["q_logits"][:, 0])
+
+
+def test_draft_logits_and_stats(orc):
+    """q_logits = (U_k + bias(prev)) * invT, q_lse = logsumexp, q_tok = q(y)."""
+    w = inputs.workload("batched_sampling", R=3, V=257, gamma=4, rank=16, w_sigma=0.3)
+    d = inputs.draft_inputs(w)
+    T = float(w["temperature"])
+    invT = float(np.float32(1.0) / np.float32(T))
+    out = orc.markov_draft(d["U"], d["W1"], d["W2"], d["anchor"], d["seeds"], 5, T)
+    W1, W2, U = _bf16_decode(d["W1"]), _bf16_decode(d["W2"]), _bf16_decode(d["U"])
+    for r in range(3):
+        prev = int(d["anchor"][r])
+        for k in range(4):
+            s = (U[r, k] + W2 @ W1[prev]) * invT
+            np.testing.assert_allclose(out["q_logits"][r, k], s, rtol=1e-12, atol=1e-12)
+            lse = np.log(np.exp(s - s.max()).sum()) + s.max()
+            assert out["q_lse"][r, k] == pytest.approx(lse, rel=1e-12)
+            y = out["y"][r, k]
+            assert out["q_tok"][r, k] == pytest.approx(np.exp(s[y] - lse), rel=1e-12)
+            prev = int(y)
+    # anchor < 0: no bias at position 0
+    out0 = orc.markov_draft(d["U"], d["W1"], d["W2"], np.full(3, -1), d["seeds"], 5, T)
+    np.testing.assert_allclose(out0["q_logits"][:, 0], U[:, 0] * invT, rtol=1e-13)
+
+
+def test_gumbel_max_draws_follow_softmax(orc):
+    """At T = 0.7 the drafted token's frequencies over 6000 cycles match
+    softmax(U * invT) (chi-square on 12 symbols); the draws change with the
+    cycle index and the request seed."""
+    V = 12
+    g = np.random.default_rng(11)
+    U = g.normal(0, 1.5, (1, 1, V)).astype(np.float32)
+    W = np.zeros((V, 4), np.float32)
+    T = 0.7
+    invT = float(np.float32(1.0) / np.float32(T))
+    ys = np.array([orc.markov_draft(U, W, W, [-1], [123], c, T, want_logits=False)["y"][0, 0]
+                   for c in range(6000)])
+    counts = np.bincount(ys, minlength=V)
+    p = orc.softmax(U[0, 0].astype(np.float64) * invT)
+    chi2 = ((counts - 6000 * p) ** 2 / (6000 * p)).sum()
+    assert stats.chi2.sf(chi2, V - 1) > 1e-3, chi2
+    # a sign error in the noise (argmin-like sampling) would favour the least likely token
+    assert counts[np.argmax(p)] > counts[np.argmin(p)]
+
+
+def test_request_subset_replays_batch(orc):
+    """req_ids lets a subset of requests be replayed with the batch's random counters."""
+    w = inputs.workload("batched_sampling", R=5, V=200, gamma=3, rank=8)
+    d = inputs.draft_inputs(w)
+    full = orc.markov_draft(d["U"], d["W1"], d["W2"], d["anchor"], d["seeds"], 2, 0.7)
+    sub = [1, 4]
+    part = orc.markov_draft(d["U"][sub], d["W1"], d["W2"], d["anchor"][sub], d["seeds"][sub], 2, 0.7,
+                            req_ids=sub)
+    assert (part["y"] == full["y"][sub]).all()
+    np.testing.assert_array_equal(part["q_lse"], full["q_lse"][sub])

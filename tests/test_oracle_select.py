@@ -1,0 +1,156 @@
+"""Pins for the oracle's survival, capacity and prefix-closed selection.
+
+Sources: DSpark explainer (papers.franksyz.com mainline topic 31) section 5
+(a suffix position is worth the product of the conditional acceptance rates),
+section 8 (survival a[r,k] from the confidences c[r,k]), section 9 (global
+prefix-closed selection maximising predicted output times SPS(B); the causal
+greedy stops when Theta stops improving) and section 10 (capacity K from the
+confidences of two steps earlier, top-K of the current a within it).
+"""
+import itertools
+
+import numpy as np
+import pytest
+
+from speculative_decoding_dspark_gb300 import inputs
+
+
+def _brute_best(a, n):
+    """max over prefix-closed sets of size n of sum(a); exhaustive over (l_0..l_{R-1})."""
+    R, gamma = a.shape
+    best = -1.0
+    for ls in itertools.product(range(gamma + 1), repeat=R):
+        if sum(ls) != n:
+            continue
+        s = sum(float(a[r, :ls[r]].astype(np.float64).sum()) for r in range(R))
+        best = max(best, s)
+    return best
+
+
+def _conf(R, gamma, seed):
+    w = inputs.workload("confidence_scheduled", seed_offset=seed, R=R, gamma=gamma)
+    return inputs.confidence_inputs(w)
+
+
+def test_survival_is_cumprod(orc):
+    ci = _conf(64, 5, 0)
+    out = orc.select_prefix(ci["c"], None, None, None, K_cap=64 * 6, mode=0)
+    # numpy's float32 cumprod multiplies left to right in float32: bit-identical
+    np.testing.assert_array_equal(out["a"], np.cumprod(ci["c"], axis=1, dtype=np.float32))
+    assert (np.diff(out["a"], axis=1) <= 0).all()
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_topk_is_prefix_closed_and_optimal(orc, seed):
+    R, gamma = 3, 3
+    ci = _conf(R, gamma, seed)
+    for n in range(R * gamma + 1):
+        out = orc.select_prefix(ci["c"], None, None, None, K_cap=R + n, mode=0)
+        assert out["status"] == 0
+        l = out["l"]
+        assert l.sum() == n and out["K_used"] == R + n
+        assert (l >= 0).all() and (l <= gamma).all()
+        np.testing.assert_array_equal(out["cu_seqlens"], inputs.cu_from_lengths(l))
+        chosen = sum(float(out["a"][r, :l[r]].astype(np.float64).sum()) for r in range(R))
+        assert chosen == pytest.approx(_brute_best(out["a"], n), rel=1e-12, abs=1e-15)
+
+
+def _theta_table(a, sizes, sps, R, gamma, K_cap):
+    th = []
+    for S, v in zip(sizes, sps):
+        if S < R:
+            continue
+        n = min(min(S, K_cap) - R, R * gamma)
+        th.append((float(v) * (R + _brute_best(a, n)), S, n))
+    return th
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_capacity_planning_is_exhaustive_argmax(orc, seed):
+    R, gamma = 3, 3
+    ci = _conf(R, gamma, seed)
+    sizes = np.array([2, 3, 4, 6, 8, 12], np.int32)
+    # a staircase steep enough that the best size varies with the confidences
+    sps = (1.0 / (0.010 + 0.0016 * sizes)).astype(np.float32)
+    for mode, plan_c in [(1, ci["c_hist"]), (2, ci["c"])]:
+        for K_cap in [3, 7, 12]:
+            out = orc.select_prefix(ci["c"], ci["c_hist"], sizes, sps, K_cap, mode)
+            a_plan = np.cumprod(plan_c, axis=1, dtype=np.float32)
+            table = _theta_table(a_plan, sizes, sps, R, gamma, K_cap)
+            best = max(table, key=lambda t: (t[0], -t[1]))
+            assert out["K_used"] == R + best[2], (mode, K_cap, table)
+            # the selection itself always ranks the current a
+            chosen = sum(float(out["a"][r, :out["l"][r]].astype(np.float64).sum()) for r in range(R))
+            assert chosen == pytest.approx(_brute_best(out["a"], best[2]), rel=1e-12, abs=1e-15)
+
+
+def test_first_stop_greedy(orc):
+    """Mode 3 adds candidates in order of a while Theta strictly grows."""
+    for seed in range(6):
+        R, gamma = 3, 3
+        ci = _conf(R, gamma, seed)
+        sizes = np.array([3, 4, 5, 6, 8, 12], np.int32)
+        sps = (1.0 / (0.010 + 0.0009 * sizes)).astype(np.float32)
+        out = orc.select_prefix(ci["c"], None, sizes, sps, 12, 3)
+        a = out["a"]
+        n = 0
+        pad = lambda B: min([i for i in range(len(sizes)) if sizes[i] >= B], key=lambda i: sizes[i])
+        theta = float(sps[pad(R)]) * R
+        while n < R * gamma:
+            nxt = float(sps[pad(R + n + 1)]) * (R + _brute_best(a, n + 1))
+            if not nxt > theta:
+                break
+            theta, n = nxt, n + 1
+        assert out["K_used"] == R + n
+
+
+def test_staircase_edge_selects_nothing_when_first_stop(orc):
+    """At R = 512 (a capture-size edge) the first extra row doubles the padded
+    batch, so the first-stop greedy verifies nothing, while the fixed capacity
+    K = 1024 verifies the 512 best prefixes."""
+    ci = _conf(512, 5, 0)
+    g = orc.select_prefix(ci["c"], None, ci["capture_sizes"], ci["sps"], 1024, 3)
+    assert g["K_used"] == 512 and (g["l"] == 0).all()
+    f = orc.select_prefix(ci["c"], None, ci["capture_sizes"], ci["sps"], 1024, 0)
+    assert f["K_used"] == 1024 and f["l"].sum() == 512
+    h = orc.select_prefix(ci["c"], ci["c_hist"], ci["capture_sizes"], ci["sps"], 1024, 1)
+    assert h["status"] == 0 and h["K_used"] in (512, 1024)
+
+
+def test_tie_order_k_then_r(orc):
+    """Equal survival values are taken in order of position, then request."""
+    c = np.ones((3, 2), np.float32)
+    out = orc.select_prefix(c, None, None, None, K_cap=3 + 4, mode=0)
+    # order: (k0,r0),(k0,r1),(k0,r2),(k1,r0) -> l = [2,1,1]
+    assert list(out["l"]) == [2, 1, 1]
+    # position before request: a = [[1,1],[1,0.5]], two picks -> (k0,r0),(k0,r1)
+    c = np.array([[1.0, 1.0], [1.0, 0.5]], np.float32)
+    assert list(orc.select_prefix(c, None, None, None, K_cap=2 + 2, mode=0)["l"]) == [1, 1]
+    # lower request first among equal (a, k)
+    c = np.array([[0.7, 0.1], [0.7, 0.1], [0.7, 0.1]], np.float32)
+    assert list(orc.select_prefix(c, None, None, None, K_cap=3 + 2, mode=0)["l"]) == [1, 1, 0]
+
+
+def test_select_errors(orc):
+    c = np.full((4, 3), 0.5, np.float32)
+    assert orc.select_prefix(c, None, None, None, K_cap=3, mode=0)["status"] == -3
+    bad = c.copy(); bad[1, 2] = 1.5
+    assert orc.select_prefix(bad, None, None, None, K_cap=16, mode=0)["status"] == -6
+    bad[1, 2] = np.nan
+    assert orc.select_prefix(bad, None, None, None, K_cap=16, mode=0)["status"] == -6
+    assert orc.select_prefix(c, None, [4, 8], [1.0, 2.0], 16, 1)["status"] == -1
+
+
+def test_commit_lengths(orc):
+    n_acc = np.array([0, 3, 5, 2], np.int32)
+    l = np.array([2, 3, 5, 4], np.int32)
+    out = orc.commit_lengths(n_acc, l, 5)
+    assert out["status"] == 0
+    assert list(out["commit_len"]) == [1, 4, 6, 3]
+    assert list(out["cu_commit"]) == [0, 1, 5, 11, 14]
+    assert list(out["discard"]) == [2, 0, 0, 2]
+    assert out["total"] == 14
+    out = orc.commit_lengths(n_acc, None, 5)
+    assert list(out["discard"]) == [5, 2, 0, 3]
+    bad = orc.commit_lengths(np.array([4], np.int32), np.array([3], np.int32), 5)
+    assert bad["status"] == -6
