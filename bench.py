@@ -1,0 +1,369 @@
+"""Throughput of the DSpark decode-cycle hot path on GB300.
+
+One step = one whole decode cycle of the workload through the library's C ABI:
+prefix selection -> Markov-head block draft -> lossless verify -> commit
+lengths, on seeded synthetic inputs already resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload batched_sampling]
+
+Prints one JSON line.  For N > 1 it runs under torch.distributed.run, one
+rank per GPU; every rank runs its own replica of the workload (requests are
+independent, no collective is needed), the time is the max over ranks and
+`value` counts the cycles of all ranks.  `--impl reference` times the CPU
+oracle (single-threaded C++) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from speculative_decoding_dspark_gb300 import inputs  # noqa: E402
+
+METRIC = "draft+verify cycles/s"
+UNIT = "cycles/s"
+DEFAULT_WORKLOAD = "batched_sampling"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_config(w):
+    return {"workload": w["name"], "R": w["R"], "V": w["V"], "gamma": w["gamma"],
+            "rank": w["rank"], "temperature": float(w["temperature"]),
+            "l2": "inputs larger than L2 (no flush): W2/U/target/q_logits stream > 1 GB per step"}
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_sample(w, d, full, n_req, cycle):
+    """Time the oracle on n_req requests of the workload (draft all gamma
+    positions + verify); returns (seconds per request, sample text)."""
+    import oracle
+    oracle.build()
+    R, gamma = w["R"], w["gamma"]
+    T = float(w["temperature"])
+    rows = list(np.linspace(0, R - 1, n_req).astype(int))
+    l = np.full(len(rows), gamma, np.int32)
+    t0 = time.perf_counter()
+    o = oracle.markov_draft(d["U"][rows], d["W1"], d["W2"], d["anchor"][rows], d["seeds"][rows],
+                            cycle, T, req_ids=rows)
+    oracle.verify(inputs.pack_rows(full[rows], l), inputs.cu_from_lengths(l), o["y"], o["q_logits"],
+                  d["seeds"][rows], cycle, T, req_ids=rows)
+    oracle.commit_lengths(np.zeros(len(rows), np.int32), l, gamma)
+    dt = time.perf_counter() - t0
+    return dt / len(rows), f"{len(rows)} of {R} requests, whole cycle each (draft {gamma} positions + verify), scaled x{R}"
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = inputs.workload(args.workload)
+    d = inputs.draft_inputs(w)
+    full = inputs.target_full(w, d["U"])
+    per_req = []
+    sample = ""
+    for step in range(args.warmup + args.steps):
+        s, sample = oracle_sample(w, d, full, 1, step)
+        if step >= args.warmup:
+            per_req.append(s)
+    cyc_s = 1.0 / (statistics.mean(per_req) * w["R"])
+    line = {"metric": METRIC, "value": cyc_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000.0 / cyc_s, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w), "impl": "reference",
+            "cpu_baseline": {"value": cyc_s, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "each step: " + sample.replace("1 of", "1 request of")},
+            "e2e": {"value": cyc_s, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.idx = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1])); mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        top = max(mx)
+        loaded = [s for s in sm if s > 0.5 * top] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": top, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU arm
+def source_digest(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def traffic_from_profile(kernel, digest):
+    """dram bytes per launch recorded for this kernel's current source, or None."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        f = line.split()
+        if len(f) >= 3 and not line.startswith("#") and f[0] == kernel and f[1] == digest:
+            return float(f[2])
+    return None
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from speculative_decoding_dspark_gb300 import binding as B
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    w = inputs.workload(args.workload)
+    R, V, gamma, rank_r = w["R"], w["V"], w["gamma"], w["rank"]
+    T = float(w["temperature"])
+    d = inputs.draft_inputs(w)
+    full = inputs.target_full(w, d["U"])
+    ci = inputs.confidence_inputs(w)
+    if w.get("confidence"):
+        K_cap, mode = ci["K_cap"], B.DSPARK_SELECT_HISTORY
+    else:  # fixed-length workloads: the capacity admits every draft position
+        K_cap, mode = R * (gamma + 1), B.DSPARK_SELECT_FIXED
+    max_rows = min(K_cap, R * (gamma + 1))
+
+    def dev(x):
+        x = np.ascontiguousarray(x)
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+        if x.dtype == np.uint64:
+            return torch.from_numpy(x.view(np.int64)).cuda()
+        return torch.from_numpy(x).cuda()
+
+    U, W1, W2 = dev(d["U"]), dev(d["W1"]), dev(d["W2"])
+    anchor, seeds = dev(d["anchor"]), dev(d["seeds"])
+    c, c_hist = dev(ci["c"]), dev(ci["c_hist"])
+    sizes, sps = dev(ci["capture_sizes"]), dev(ci["sps"])
+    # target rows in full [R, gamma+1, V]; with every position selected the packed
+    # layout equals it, otherwise the first max_rows rows of the buffer are read
+    target = dev(full.reshape(R * (gamma + 1), V))
+    del full
+    i32 = dict(dtype=torch.int32, device="cuda")
+    y = torch.empty((R, gamma), **i32)
+    q_lse = torch.empty((R, gamma), device="cuda")
+    q_tok = torch.empty((R, gamma), device="cuda")
+    q_logits = torch.empty((R, gamma, V), device="cuda") if T > 0 else None
+    a = torch.empty((R, gamma), device="cuda")
+    l = torch.empty(R, **i32)
+    cu = torch.empty(R + 1, **i32)
+    K_used = torch.empty(1, **i32)
+    n_acc = torch.empty(R, **i32)
+    out = torch.empty((R, gamma + 1), **i32)
+    p_tok = torch.empty((R, gamma), device="cuda")
+    cl = torch.empty(R, **i32)
+    cuc = torch.empty(R + 1, **i32)
+    disc = torch.empty(R, **i32)
+    tot = torch.empty(1, **i32)
+    status = torch.zeros(1, **i32)
+    ws_d = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_DRAFT, R, gamma, V, rank_r, 0, B.DSPARK_BF16))
+    ws_v = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_VERIFY, R, gamma, V, 0, max_rows))
+    stream = torch.cuda.current_stream()
+    uses_tc = B.dspark_markov_draft_uses_tensor_cores(B.DSPARK_BF16, B.DSPARK_BF16, R, V, rank_r)
+
+    def step(cycle, ev=None):
+        if ev is not None: ev[0].record(stream)
+        B.dspark_select_prefix(c, c_hist, sizes, sps, K_cap, mode, a, l, cu, K_used, None, status)
+        if ev is not None: ev[1].record(stream)
+        B.dspark_markov_draft(U, W1, W2, anchor, seeds, cycle, T, y, q_lse, q_tok, q_logits, ws_d, status)
+        if ev is not None: ev[2].record(stream)
+        B.dspark_verify(target, cu, y, q_logits, q_lse, q_tok, seeds, cycle, T, max_rows, n_acc, out,
+                        p_tok, ws_v, status)
+        if ev is not None: ev[3].record(stream)
+        B.dspark_commit_lengths(n_acc, l, gamma, cl, cuc, disc, tot, status)
+        if ev is not None: ev[4].record(stream)
+
+    # launches of this library per step
+    draft_launches = gamma if uses_tc else 1 + 2 * gamma
+    launches_per_step = 1 + draft_launches + (3 if T > 0 else 2) + 1
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    start.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i, evs[i])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    ms = start.elapsed_time(stop)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    per = {k: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+           for j, k in enumerate(["select", "draft", "verify", "commit"])}
+    ms_step = ms / args.steps
+    value = world * args.steps / (ms / 1000.0)
+
+    # roofline of the dominant kernel: one Markov draft step (one vocabulary pass)
+    draft_step_ms = per["draft"] / gamma
+    step_bytes = V * rank_r * 2 + R * V * 2 + (R * V * 4 if q_logits is not None else 0)
+    peaks = {}
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        peaks = json.load(open(pk))
+    hbm = peaks.get("hbm_gbs")
+    peak_src = "measured" if hbm else "fallback"
+    hbm = hbm or 6800.0
+    achieved = step_bytes / (draft_step_ms / 1000.0) / 1e9
+    kname = "draft_step_tc" if uses_tc else "draft_bias_simt+draft_sample"
+    digest = source_digest(["speculative_decoding_dspark_gb300/csrc/draft_tc.cu" if uses_tc else
+                            "speculative_decoding_dspark_gb300/csrc/draft_simt.cu",
+                            "speculative_decoding_dspark_gb300/csrc/common.cuh"])
+    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+            "traffic": traffic_from_profile(kname, digest), "kernel": kname,
+            "algorithmic_bytes_per_launch": step_bytes, "launch_ms": draft_step_ms,
+            "peak_source": peak_src}
+
+    # end to end through the public API from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        hU = U.cpu().pin_memory(); htgt = target.cpu().pin_memory(); hc = c.cpu().pin_memory()
+        hch = c_hist.cpu().pin_memory(); ha = anchor.cpu().pin_memory(); hs = seeds.cpu().pin_memory()
+        h_out = torch.empty((R, gamma + 1), dtype=torch.int32).pin_memory()
+        h_n = torch.empty(R, dtype=torch.int32).pin_memory()
+        h_cl = torch.empty(R + 1, dtype=torch.int32).pin_memory()
+        bi = sum(t.numel() * t.element_size() for t in (hU, htgt, hc, hch, ha, hs))
+        bo = sum(t.numel() * t.element_size() for t in (h_out, h_n, h_cl))
+
+        def e2e_step(cycle):
+            U.copy_(hU, non_blocking=True); target.copy_(htgt, non_blocking=True)
+            c.copy_(hc, non_blocking=True); c_hist.copy_(hch, non_blocking=True)
+            anchor.copy_(ha, non_blocking=True); seeds.copy_(hs, non_blocking=True)
+            step(cycle)
+            h_out.copy_(out, non_blocking=True); h_n.copy_(n_acc, non_blocking=True)
+            h_cl.copy_(cuc, non_blocking=True)
+
+        n_e2e = max(3, min(args.steps, 20))
+        for i in range(2):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for i in range(n_e2e):
+            e2e_step(100 + i)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = s0.elapsed_time(s1)
+        if world > 1:
+            t = torch.tensor([e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * n_e2e / (e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": bi,
+               "d2h_bytes_per_step": bo, "steps": n_e2e}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        per_req, sample = oracle_sample(w, d, inputs.target_full(w, d["U"]), 4, 0)
+        cpu = {"value": 1.0 / (per_req * R), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16 GEMM (fp32 accumulate) + fp32 softmax/verify",
+                "data": "synthetic (seeded; shapes and laws of the workload)",
+                "config": dict(workload_config(w), parallelism=f"replicas x{world}"),
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+                "gpu_launches": launches_per_step * args.steps,
+                "stage_ms": per, "logits_gb_s": (R * (gamma + 1) * V * 4 + R * gamma * V * 2) /
+                (ms_step / 1000.0) / 1e9, "draft_path": "tcgen05" if uses_tc else "simt"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,240 @@
+/*
+ * dspark.h -- C ABI of the DSpark decode-cycle hot path on one GB300 GPU.
+ *
+ * One DSpark decode cycle, as the pages describe it:
+ *   1. draft   -- the Markov-head block draft: per position k the drafter's
+ *                 logits are the backbone's base logits U_k plus a low-rank
+ *                 bias of the previous sampled token, sampled left to right
+ *                 ("DSpark explainer", papers.franksyz.com topic 31, sections
+ *                 6-7; llama.cpp PR 25173 "spec: add DSpark speculative
+ *                 decoding", description: anchor-first block,
+ *                 bias(prev) = markov_w2 . markov_w1[prev]);
+ *   2. select  -- survival a = cumulative product of the confidences and a
+ *                 prefix-closed choice of verify lengths within a physical
+ *                 capacity (explainer sections 5, 8, 9, 10);
+ *   3. verify  -- left-to-right acceptance min(1, p/q), residual
+ *                 max(0, p - q) on the first rejection, a bonus token when
+ *                 every draft is accepted (explainer sections 2-3), over
+ *                 target rows packed back to back (section 13);
+ *   4. commit  -- lengths of what each request commits and rolls back
+ *                 (sections 2 and 11).
+ *
+ * Conventions shared by every call:
+ *   - Every array argument is a DEVICE pointer owned by the caller; the
+ *     library allocates no memory and keeps no state between calls.  Scratch
+ *     lives in a caller-provided workspace of dspark_workspace_size() bytes
+ *     (any 256-byte aligned device buffer; its contents need no
+ *     initialisation and are clobbered).
+ *   - Arrays are row-major and densely packed; the shapes are given beside
+ *     each argument.  Token ids and lengths are int32.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream), never synchronises and never throws.  It
+ *     returns DSPARK_OK once its kernels are enqueued, or a negative status
+ *     after a host-side check failed, in which case nothing was enqueued.
+ *   - Errors found by the kernels (a token id outside [0, V), a verify
+ *     length outside [0, gamma], a confidence outside [0, 1], a bounded
+ *     device wait that expired) are written asynchronously to *dev_status
+ *     (an int32 the caller zeroes; first error wins) when dev_status is not
+ *     NULL, and the affected request's outputs are set to -1.
+ *   - Random numbers: counter-based Philox4x32-10 keyed by the request's
+ *     64-bit seed, counter (vocab index / 4, block position, request index,
+ *     cycle << 4 | purpose), purposes 0 draft noise, 1 acceptance, 2
+ *     residual noise, 3 bonus noise; the uniform from a 32-bit word x is
+ *     ((x >> 9) + 0.5) * 2^-23.  cycle must be < 2^28.  Reusing (seed,
+ *     cycle) reproduces a cycle exactly.
+ *   - temperature == 0 means greedy decoding on both sides; otherwise the
+ *     logits are multiplied by invT = 1.0f / temperature computed in fp32.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t; declared opaquely so that this header needs no CUDA header. */
+typedef struct CUstream_st* dspark_stream_t;
+
+/* ---- status codes ---------------------------------------------------------- */
+#define DSPARK_OK 0
+#define DSPARK_ERR_INVALID_ARG (-1)  /* NULL pointer, bad size, gamma > 16, T < 0 ...  */
+#define DSPARK_ERR_UNSUPPORTED (-2)  /* a shape or dtype no kernel here handles        */
+#define DSPARK_ERR_CAPACITY (-3)     /* R > K_cap, or more rows than max_rows          */
+#define DSPARK_ERR_CUDA (-4)         /* a CUDA launch or driver call failed            */
+#define DSPARK_ERR_TIMEOUT (-5)      /* device side: a bounded wait gave up            */
+#define DSPARK_ERR_DEVICE_INPUT (-6) /* device side: bad token id / length / confidence */
+#define DSPARK_ERR_WORKSPACE (-7)    /* workspace NULL, misaligned or too small        */
+
+/* ---- element types ------------------------------------------------------- */
+#define DSPARK_F32 0
+#define DSPARK_BF16 1
+
+/* ---- workspace owners ------------------------------------------------------ */
+#define DSPARK_OP_DRAFT 0
+#define DSPARK_OP_VERIFY 1
+#define DSPARK_OP_SELECT 2
+
+/* ---- dspark_markov_draft flags ---------------------------------------------- */
+#define DSPARK_DRAFT_FORCE_SIMT 1u   /* use the CUDA-core kernels even where the
+                                        tensor-core kernel applies (testing) */
+
+/* ---- selection modes --------------------------------------------------------- */
+#define DSPARK_SELECT_FIXED 0      /* capacity K = K_cap                              */
+#define DSPARK_SELECT_HISTORY 1    /* capacity from c_hist (the confidences of an
+                                      earlier cycle), explainer section 10            */
+#define DSPARK_SELECT_CURRENT 2    /* capacity from the current c; it looks at values
+                                      that admission must not see (section 4), kept
+                                      only to study the planner                       */
+#define DSPARK_SELECT_FIRST_STOP 3 /* the theoretical greedy of section 9: add the best
+                                      remaining candidate while Theta strictly grows  */
+
+/* Static text for a status code. */
+const char* dspark_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int dspark_version(void);
+
+/* Bytes of workspace one call of `op` needs for these sizes (0 on bad
+ * arguments).  For DSPARK_OP_DRAFT pass the weights' element type and the
+ * draft flags; for DSPARK_OP_VERIFY, max_rows bounds cu_seqlens[R]; other
+ * arguments may be 0 where unused. */
+size_t dspark_workspace_size(int op, int R, int gamma, int V, int rank, int max_rows,
+                             int w_dtype, unsigned flags);
+
+/* 1 if dspark_markov_draft would use the tcgen05 tensor-core kernel for these
+ * arguments, 0 for the CUDA-core kernels. */
+int dspark_markov_draft_uses_tensor_cores(int u_dtype, int w_dtype, int R, int V, int rank,
+                                          unsigned flags);
+
+/*
+ * dspark_philox4x32_10 -- the generator every random draw of the cycle comes
+ * from (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
+ * 1, 2, 3", SC'11), exposed so that callers and tests can reproduce draws.
+ *   ctr [n, 4] uint32 counters, keys [n] uint64, out [n, 4] uint32 (device).
+ */
+int dspark_philox4x32_10(const uint32_t* ctr, const uint64_t* keys, int n, uint32_t* out,
+                         dspark_stream_t stream);
+
+/*
+ * dspark_markov_draft -- semi-autoregressive Markov-head block draft
+ * (explainer sections 6-7; PR 25173 description, draft-dspark bullet).
+ *
+ * For k = 0 .. gamma-1, for every request r:
+ *   prev = anchor[r] at k = 0 (anchor < 0: no bias at k = 0), else y[r][k-1]
+ *   s_v  = (U[r][k][v] + sum_j W2[v][j] * W1[prev][j]) * invT   (T > 0)
+ *   s_v  =  U[r][k][v] + sum_j W2[v][j] * W1[prev][j]           (T = 0)
+ *   y[r][k] = argmax_v (s_v + Gumbel(u_v)) with u from purpose 0 at position k
+ *             (T = 0: argmax_v s_v); ties go to the lowest v
+ *   q_lse[r][k] = log sum_v exp(s_v),  q_tok[r][k] = exp(s_y - q_lse)   (T > 0 only)
+ *   q_logits[r][k][v] = s_v                                            (if not NULL)
+ * The steps run in order on `stream`; step k reads the tokens of step k-1.
+ *
+ *   U          [R, gamma, V]  u_dtype (F32 or BF16)
+ *   W1, W2     [V, rank]      w_dtype (F32 or BF16), the Markov factors
+ *   anchor     [R] int32      last committed token of each request
+ *   seeds      [R] uint64     per-request Philox keys (may be NULL iff T == 0)
+ *   draft_tokens [R, gamma] int32 out
+ *   q_lse, q_tok [R, gamma] fp32 out (may be NULL iff T == 0)
+ *   q_logits   [R, gamma, V] fp32 out; NULL skips it (needed by dspark_verify at T > 0)
+ *   ws, ws_bytes  workspace of dspark_workspace_size(DSPARK_OP_DRAFT, R, gamma, V,
+ *                 rank, 0, w_dtype, flags) bytes
+ * Limits: 1 <= gamma <= 16, R >= 1, V >= 1, rank >= 1.  The tensor-core kernel
+ * applies to BF16 U and weights with rank % 64 == 0, rank <= 1024 and
+ * V % 8 == 0; everything else runs on the CUDA-core kernels.
+ */
+int dspark_markov_draft(const void* U, int u_dtype, const void* W1, const void* W2,
+                        int w_dtype, const int32_t* anchor, const uint64_t* seeds,
+                        uint32_t cycle, float temperature, int R, int gamma, int V,
+                        int rank, int32_t* draft_tokens, float* q_lse, float* q_tok,
+                        float* q_logits, unsigned flags, void* ws, size_t ws_bytes,
+                        int32_t* dev_status, dspark_stream_t stream);
+
+/*
+ * dspark_verify -- lossless left-to-right verification (explainer sections
+ * 2, 3 and 13).
+ *
+ * Request r owns target rows cu_seqlens[r] .. cu_seqlens[r+1]-1, that is
+ * l_r + 1 rows with 0 <= l_r <= gamma: rows for the l_r drafts to check and
+ * the row after them.  With t = row * invT (T = 0: the row itself),
+ * p = softmax(t) and the drafter's q = softmax(q_logits[r][j]):
+ *   draft j is accepted iff u_j < p(y_j) / q_tok[r][j], u_j from purpose 1 at
+ *   position j (T = 0: iff y_j == argmax of row j); checking stops at the first
+ *   rejection.  n_accepted[r] = number accepted.
+ *   After a rejection at j the extra token is drawn from max(0, p - q) of row j
+ *   by Gumbel-max over log weights (purpose 2, position j); if that residual
+ *   is empty in fp32 it is drawn from p with the same noise.  If every draft is
+ *   accepted the extra token is drawn from p of row l_r (purpose 3, position
+ *   l_r).  T = 0: the extra token is the argmax of row n_accepted.
+ *   out_tokens[r] = y[r][0 .. n-1], extra token, then -1 up to gamma + 1 entries.
+ *   p_tok[r][j] = p(y_j) for the drafts examined (T = 0: 1 if y_j is the row's
+ *   argmax else 0); entries not examined are left untouched.
+ *
+ *   target_logits [cu_seqlens[R], V] fp32, packed rows without padding
+ *   cu_seqlens   [R + 1] int32, cu_seqlens[0] = 0, non-decreasing
+ *   draft_tokens [R, gamma] int32;  q_tok, q_lse [R, gamma] fp32 (T > 0)
+ *   q_logits     [R, gamma, V] fp32 from dspark_markov_draft (T > 0)
+ *   seeds        [R] uint64 (T > 0)
+ *   n_accepted [R], out_tokens [R, gamma + 1] int32 out; p_tok [R, gamma] fp32 out or NULL
+ *   ws, ws_bytes  dspark_workspace_size(DSPARK_OP_VERIFY, R, gamma, V, 0, max_rows, 0, 0)
+ *                 with max_rows >= cu_seqlens[R]
+ *   max_rows     the host's bound on cu_seqlens[R] (<= R * (gamma + 1))
+ */
+int dspark_verify(const float* target_logits, const int32_t* cu_seqlens,
+                  const int32_t* draft_tokens, const float* q_logits, const float* q_lse,
+                  const float* q_tok, const uint64_t* seeds, uint32_t cycle,
+                  float temperature, int R, int gamma, int V, int max_rows,
+                  int32_t* n_accepted, int32_t* out_tokens, float* p_tok, void* ws,
+                  size_t ws_bytes, int32_t* dev_status, dspark_stream_t stream);
+
+/*
+ * dspark_select_prefix -- survival, capacity and prefix-closed top-K
+ * (explainer sections 5, 8, 9 and 10).
+ *
+ *   a[r][k] = a[r][k-1] * c[r][k] in fp32, a[r][0] = c[r][0]
+ *   candidates (r, k) are ranked by a descending, then k ascending, then r
+ *   ascending; a is non-increasing in k, so every top-n set is prefix-closed.
+ *   Theta(n) = SPS(B) * (R + sum of the n best a), B = R + n physical rows; for
+ *   a capture size S the step rate is sps[i] for the smallest S_i >= B.
+ *   n = min(K_cap - R, R*gamma)                                      (FIXED)
+ *   n = n_S of the capture size S >= R maximising
+ *       sps_S * (R + sum of the n_S best a_plan), n_S = min(min(S, K_cap) - R, R*gamma),
+ *       ties to the smaller S; a_plan from c_hist (HISTORY) or c (CURRENT)
+ *   n = the first-stop greedy of section 9, at most K_cap - R         (FIRST_STOP)
+ *   l[r] = selected positions of request r; cu_seqlens[r+1] = cu_seqlens[r] + l[r] + 1
+ *   K_used[0] = R + n (the physical rows the verify step will see)
+ *
+ *   c, c_hist    [R, gamma] fp32 in [0, 1]; c_hist may be NULL except in HISTORY mode
+ *   capture_sizes [n_steps] int32, sps [n_steps] fp32 (unused in FIXED mode)
+ *   a [R, gamma] fp32 out; l [R], cu_seqlens [R + 1], K_used [1] int32 out
+ * Limits: R * gamma <= 8192, n_steps <= 64.
+ */
+int dspark_select_prefix(const float* c, const float* c_hist, const int32_t* capture_sizes,
+                         const float* sps, int n_steps, int K_cap, int mode, int R, int gamma,
+                         float* a, int32_t* l, int32_t* cu_seqlens, int32_t* K_used,
+                         void* ws, size_t ws_bytes, int32_t* dev_status,
+                         dspark_stream_t stream);
+
+/*
+ * dspark_commit_lengths -- per-request commit and rollback counts
+ * (explainer sections 2 and 11: the accepted prefix plus one target-correct
+ * token is committed, the rest of what was verified is rolled back).
+ *
+ *   commit_len[r] = n_accepted[r] + 1
+ *   cu_commit[0] = 0, cu_commit[r+1] = cu_commit[r] + commit_len[r]
+ *   discard[r] = l[r] - n_accepted[r]  (l == NULL: every request verified gamma)
+ *   total[0] = cu_commit[R]
+ * A request with n_accepted outside [0, l] commits 0 and is reported through
+ * dev_status.
+ */
+int dspark_commit_lengths(const int32_t* n_accepted, const int32_t* l, int R, int gamma,
+                          int32_t* commit_len, int32_t* cu_commit, int32_t* discard,
+                          int32_t* total, int32_t* dev_status, dspark_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */

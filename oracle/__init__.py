@@ -62,6 +62,7 @@ def lib():
             vp, i32, u32, u64, f32, dbl = (ctypes.c_void_p, ctypes.c_int, ctypes.c_uint32,
                                            ctypes.c_uint64, ctypes.c_float, ctypes.c_double)
             L.orc_philox4x32_10.argtypes = [vp, u64, vp]
+            L.orc_philox4x32_10_batch.argtypes = [vp, vp, i32, vp]
             L.orc_uniform_from_bits.argtypes = [u32]
             L.orc_uniform_from_bits.restype = dbl
             L.orc_uniform_vocab.argtypes = [u64, u32, i32, i32, i32, i32]
@@ -106,6 +107,15 @@ def philox4x32_10(ctr, seed: int) -> np.ndarray:
     ctr = _c(ctr, np.uint32)
     out = np.zeros(4, np.uint32)
     lib().orc_philox4x32_10(_p(ctr), ctypes.c_uint64(seed), _p(out))
+    return out
+
+
+def philox4x32_10_batch(ctr, keys) -> np.ndarray:
+    """ctr [n, 4] uint32, keys [n] uint64 -> [n, 4] uint32."""
+    ctr = _c(ctr, np.uint32)
+    keys = _c(keys, np.uint64)
+    out = np.zeros_like(ctr)
+    lib().orc_philox4x32_10_batch(_p(ctr), _p(keys), keys.size, _p(out))
     return out
 
 

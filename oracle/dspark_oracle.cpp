@@ -159,6 +159,12 @@ void orc_philox4x32_10(const uint32_t ctr[4], uint64_t seed, uint32_t out[4]) {
     philox4x32_10(ctr, (uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32), out);
 }
 
+void orc_philox4x32_10_batch(const uint32_t* ctr, const uint64_t* keys, int n, uint32_t* out) {
+    for (int i = 0; i < n; ++i)
+        philox4x32_10(ctr + 4 * (size_t)i, (uint32_t)(keys[i] & 0xFFFFFFFFu),
+                      (uint32_t)(keys[i] >> 32), out + 4 * (size_t)i);
+}
+
 double orc_uniform_from_bits(uint32_t x) { return uniform_from_bits(x); }
 
 double orc_uniform_vocab(uint64_t seed, uint32_t cycle, int purpose, int req,

@@ -1,0 +1,231 @@
+// abi.cu -- the library's extern "C" entry points (declared in dspark.h).
+//
+// Host-side argument checks, workspace carving and kernel dispatch only; every
+// step of the cycle runs in the kernels.  No call allocates memory, keeps
+// state, synchronises or throws.
+#include <cstring>
+
+#include "kernels.cuh"
+#include "draft_tc.cuh"
+
+namespace {
+
+using namespace dspark;
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA; }
+
+// ---- workspace layouts (the size query and the calls share them) ------------
+struct DraftSimtLayout {
+    size_t cnt, parts, bias, total;
+};
+DraftSimtLayout draft_simt_layout(int R, int V) {
+    DraftSimtLayout L;
+    const int nchunk = (V + kDraftChunk - 1) / kDraftChunk;
+    size_t off = 0;
+    L.cnt = off; off += align_up(sizeof(int) * (size_t)R);
+    L.parts = off; off += align_up(sizeof(DraftPartial) * (size_t)R * nchunk);
+    L.bias = off; off += align_up(sizeof(float) * (size_t)R * V);
+    L.total = off;
+    return L;
+}
+
+struct VerifyLayout {
+    size_t ok, valid, cnt1, cnt2, stats, jobs, parts, total;
+};
+VerifyLayout verify_layout(int R, int V, int max_rows) {
+    VerifyLayout L;
+    const int nchunk = (V + kVerifyChunk - 1) / kVerifyChunk;
+    size_t off = 0;
+    L.ok = off; off += align_up(sizeof(int));
+    L.valid = off; off += align_up(sizeof(int) * (size_t)R);
+    L.cnt1 = off; off += align_up(sizeof(int) * (size_t)R);
+    L.cnt2 = off; off += align_up(sizeof(int) * (size_t)R);
+    L.stats = off; off += align_up(sizeof(RowStat) * (size_t)max_rows * nchunk);
+    L.jobs = off; off += align_up(sizeof(VerifyJob) * (size_t)R);
+    L.parts = off; off += align_up(sizeof(SamplePartial) * (size_t)R * nchunk);
+    L.total = off;
+    return L;
+}
+
+template <typename T>
+T* carve(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<unsigned char*>(ws) + off);
+}
+
+bool tc_applies(int u_dtype, int w_dtype, int R, int V, int rank, unsigned flags) {
+    if (flags & DSPARK_DRAFT_FORCE_SIMT) return false;
+    return draft_tc_supported(u_dtype, w_dtype, R, V, rank);
+}
+
+bool valid_dtype(int d) { return d == DSPARK_F32 || d == DSPARK_BF16; }
+
+}  // namespace
+
+extern "C" {
+
+const char* dspark_status_string(int status) {
+    switch (status) {
+        case DSPARK_OK: return "ok";
+        case DSPARK_ERR_INVALID_ARG: return "invalid argument";
+        case DSPARK_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case DSPARK_ERR_CAPACITY: return "capacity exceeded";
+        case DSPARK_ERR_CUDA: return "CUDA error";
+        case DSPARK_ERR_TIMEOUT: return "device wait timed out";
+        case DSPARK_ERR_DEVICE_INPUT: return "bad device-side input (token id, length or confidence)";
+        case DSPARK_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        default: return "unknown status";
+    }
+}
+
+int dspark_version(void) { return 100; }
+
+int dspark_markov_draft_uses_tensor_cores(int u_dtype, int w_dtype, int R, int V, int rank,
+                                          unsigned flags) {
+    return tc_applies(u_dtype, w_dtype, R, V, rank, flags) ? 1 : 0;
+}
+
+size_t dspark_workspace_size(int op, int R, int gamma, int V, int rank, int max_rows,
+                             int w_dtype, unsigned flags) {
+    if (R <= 0) return 0;
+    switch (op) {
+        case DSPARK_OP_DRAFT:
+            if (V <= 0 || rank <= 0 || gamma <= 0) return 0;
+            if (tc_applies(w_dtype, w_dtype, R, V, rank, flags)) return draft_tc_workspace(R, V, rank);
+            return draft_simt_layout(R, V).total;
+        case DSPARK_OP_VERIFY:
+            if (V <= 0 || max_rows < 0) return 0;
+            return verify_layout(R, V, max_rows).total;
+        case DSPARK_OP_SELECT:
+            return 0;
+        default:
+            return 0;
+    }
+}
+
+int dspark_markov_draft(const void* U, int u_dtype, const void* W1, const void* W2,
+                        int w_dtype, const int32_t* anchor, const uint64_t* seeds,
+                        uint32_t cycle, float temperature, int R, int gamma, int V,
+                        int rank, int32_t* draft_tokens, float* q_lse, float* q_tok,
+                        float* q_logits, unsigned flags, void* ws, size_t ws_bytes,
+                        int32_t* dev_status, dspark_stream_t stream) {
+    if (!U || !W1 || !W2 || !anchor || !draft_tokens) return DSPARK_ERR_INVALID_ARG;
+    if (!valid_dtype(u_dtype) || !valid_dtype(w_dtype)) return DSPARK_ERR_INVALID_ARG;
+    if (R <= 0 || V <= 0 || rank <= 0 || gamma <= 0 || gamma > 16) return DSPARK_ERR_INVALID_ARG;
+    if (!(temperature >= 0.0f) || temperature == INFINITY) return DSPARK_ERR_INVALID_ARG;
+    if (cycle >= (1u << 28)) return DSPARK_ERR_INVALID_ARG;
+    const bool greedy = temperature == 0.0f;
+    if (!greedy && (!seeds || !q_lse || !q_tok)) return DSPARK_ERR_INVALID_ARG;
+    if ((flags & ~DSPARK_DRAFT_FORCE_SIMT) != 0) return DSPARK_ERR_INVALID_ARG;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return DSPARK_ERR_WORKSPACE;
+    const float invT = greedy ? 1.0f : 1.0f / temperature;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    if (tc_applies(u_dtype, w_dtype, R, V, rank, flags)) {
+        if (ws_bytes < draft_tc_workspace(R, V, rank)) return DSPARK_ERR_WORKSPACE;
+        if (!aligned16(U) || !aligned16(W1) || !aligned16(W2)) return DSPARK_ERR_UNSUPPORTED;
+        DraftTcArgs a;
+        a.U = U; a.W1 = W1; a.W2 = W2; a.anchor = anchor; a.seeds = seeds; a.cycle = cycle;
+        a.invT = invT; a.greedy = greedy; a.R = R; a.gamma = gamma; a.V = V; a.rank = rank;
+        a.y = draft_tokens; a.q_lse = q_lse; a.q_tok = q_tok; a.q_logits = q_logits;
+        a.dev_status = dev_status; a.ws = ws;
+        return launch_draft_tc(a, s);
+    }
+
+    const DraftSimtLayout L = draft_simt_layout(R, V);
+    if (ws_bytes < L.total) return DSPARK_ERR_WORKSPACE;
+    DraftParams p;
+    p.U = U; p.u_dtype = u_dtype; p.W1 = W1; p.W2 = W2; p.w_dtype = w_dtype;
+    p.anchor = anchor; p.seeds = seeds; p.cycle = cycle; p.invT = invT; p.greedy = greedy;
+    p.R = R; p.gamma = gamma; p.V = V; p.rank = rank;
+    p.nchunk = (V + kDraftChunk - 1) / kDraftChunk;
+    p.y = draft_tokens; p.q_lse = q_lse; p.q_tok = q_tok; p.q_logits = q_logits;
+    p.dev_status = dev_status;
+    p.cnt = carve<int>(ws, L.cnt);
+    p.parts = carve<DraftPartial>(ws, L.parts);
+    p.bias = carve<float>(ws, L.bias);
+    return cuda_status(launch_draft_simt(p, s));
+}
+
+int dspark_verify(const float* target_logits, const int32_t* cu_seqlens,
+                  const int32_t* draft_tokens, const float* q_logits, const float* q_lse,
+                  const float* q_tok, const uint64_t* seeds, uint32_t cycle,
+                  float temperature, int R, int gamma, int V, int max_rows,
+                  int32_t* n_accepted, int32_t* out_tokens, float* p_tok, void* ws,
+                  size_t ws_bytes, int32_t* dev_status, dspark_stream_t stream) {
+    if (!target_logits || !cu_seqlens || !draft_tokens || !n_accepted || !out_tokens)
+        return DSPARK_ERR_INVALID_ARG;
+    if (R <= 0 || V <= 0 || gamma <= 0 || gamma > 16) return DSPARK_ERR_INVALID_ARG;
+    if (max_rows < R || (long long)max_rows > (long long)R * (gamma + 1)) return DSPARK_ERR_INVALID_ARG;
+    if (!(temperature >= 0.0f) || temperature == INFINITY) return DSPARK_ERR_INVALID_ARG;
+    if (cycle >= (1u << 28)) return DSPARK_ERR_INVALID_ARG;
+    const bool greedy = temperature == 0.0f;
+    if (!greedy && (!q_logits || !q_lse || !q_tok || !seeds)) return DSPARK_ERR_INVALID_ARG;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return DSPARK_ERR_WORKSPACE;
+    const VerifyLayout L = verify_layout(R, V, max_rows);
+    if (ws_bytes < L.total) return DSPARK_ERR_WORKSPACE;
+    const int nchunk = (V + kVerifyChunk - 1) / kVerifyChunk;
+    if ((long long)max_rows * nchunk >= (1LL << 31) || (long long)R * nchunk >= (1LL << 31))
+        return DSPARK_ERR_UNSUPPORTED;
+
+    VerifyParams p;
+    p.target = target_logits; p.cu = cu_seqlens; p.y = draft_tokens; p.q_logits = q_logits;
+    p.q_lse = q_lse; p.q_tok = q_tok; p.seeds = seeds; p.cycle = cycle;
+    p.invT = greedy ? 1.0f : 1.0f / temperature; p.greedy = greedy;
+    p.R = R; p.gamma = gamma; p.V = V; p.max_rows = max_rows; p.nchunk = nchunk;
+    p.n_acc = n_accepted; p.out_tokens = out_tokens; p.p_tok = p_tok; p.dev_status = dev_status;
+    p.ok = carve<int>(ws, L.ok);
+    p.valid = carve<int>(ws, L.valid);
+    p.cnt1 = carve<int>(ws, L.cnt1);
+    p.cnt2 = carve<int>(ws, L.cnt2);
+    p.stats = carve<RowStat>(ws, L.stats);
+    p.jobs = carve<VerifyJob>(ws, L.jobs);
+    p.parts = carve<SamplePartial>(ws, L.parts);
+    return cuda_status(launch_verify(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dspark_select_prefix(const float* c, const float* c_hist, const int32_t* capture_sizes,
+                         const float* sps, int n_steps, int K_cap, int mode, int R, int gamma,
+                         float* a, int32_t* l, int32_t* cu_seqlens, int32_t* K_used,
+                         void* ws, size_t ws_bytes, int32_t* dev_status,
+                         dspark_stream_t stream) {
+    (void)ws; (void)ws_bytes;
+    if (!c || !a || !l || !cu_seqlens || !K_used) return DSPARK_ERR_INVALID_ARG;
+    if (R <= 0 || gamma <= 0 || gamma > 16) return DSPARK_ERR_INVALID_ARG;
+    if (mode < DSPARK_SELECT_FIXED || mode > DSPARK_SELECT_FIRST_STOP) return DSPARK_ERR_INVALID_ARG;
+    if (mode == DSPARK_SELECT_HISTORY && !c_hist) return DSPARK_ERR_INVALID_ARG;
+    if (mode != DSPARK_SELECT_FIXED &&
+        (n_steps <= 0 || n_steps > kSelectMaxSteps || !capture_sizes || !sps))
+        return DSPARK_ERR_INVALID_ARG;
+    if ((long long)R * gamma > kSelectMaxItems) return DSPARK_ERR_UNSUPPORTED;
+    if (K_cap < R) return DSPARK_ERR_CAPACITY;
+    SelectParams p;
+    p.c = c; p.c_hist = c_hist; p.capture_sizes = capture_sizes; p.sps = sps;
+    p.n_steps = mode == DSPARK_SELECT_FIXED ? 0 : n_steps;
+    p.K_cap = K_cap; p.mode = mode; p.R = R; p.gamma = gamma;
+    p.a = a; p.l = l; p.cu = cu_seqlens; p.K_used = K_used; p.dev_status = dev_status;
+    return cuda_status(launch_select(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dspark_philox4x32_10(const uint32_t* ctr, const uint64_t* keys, int n, uint32_t* out,
+                         dspark_stream_t stream) {
+    if (n < 0 || (n > 0 && (!ctr || !keys || !out))) return DSPARK_ERR_INVALID_ARG;
+    if (n > 0 && (!aligned16(ctr) || !aligned16(out))) return DSPARK_ERR_INVALID_ARG;
+    return cuda_status(launch_philox_batch(ctr, keys, n, out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dspark_commit_lengths(const int32_t* n_accepted, const int32_t* l, int R, int gamma,
+                          int32_t* commit_len, int32_t* cu_commit, int32_t* discard,
+                          int32_t* total, int32_t* dev_status, dspark_stream_t stream) {
+    if (!n_accepted || !commit_len || !cu_commit || !discard) return DSPARK_ERR_INVALID_ARG;
+    if (R <= 0 || gamma <= 0 || gamma > 16) return DSPARK_ERR_INVALID_ARG;
+    return cuda_status(launch_commit(n_accepted, l, R, gamma, commit_len, cu_commit, discard,
+                                     total, dev_status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,120 @@
+// common.cuh -- device helpers shared by the library's kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "dspark.h"
+
+namespace dspark {
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As
+// Easy as 1, 2, 3", SC'11): ten rounds of two 32x32->64 multiplies on counter
+// words 0 and 2, the high halves xor-ed with the other two words and the
+// round key, the key advanced by two Weyl increments between rounds.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int i = 0; i < 10; ++i) {
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// Precomputed round keys of one 64-bit seed (the key schedule does not depend
+// on the counter, so a thread drawing many numbers for one request keeps it).
+struct PhiloxKey {
+    uint32_t k0[10], k1[10];
+};
+
+__device__ __forceinline__ PhiloxKey philox_key(uint64_t seed) {
+    PhiloxKey K;
+    uint32_t a = (uint32_t)(seed & 0xFFFFFFFFu), b = (uint32_t)(seed >> 32);
+#pragma unroll
+    for (int i = 0; i < 10; ++i) {
+        K.k0[i] = a; K.k1[i] = b;
+        a += 0x9E3779B9u; b += 0xBB67AE85u;
+    }
+    return K;
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKey& K) {
+#pragma unroll
+    for (int i = 0; i < 10; ++i) {
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+        c = make_uint4(hi1 ^ c.y ^ K.k0[i], lo1, hi0 ^ c.w ^ K.k1[i], lo0);
+    }
+    return c;
+}
+
+enum Purpose : uint32_t { kDraftGumbel = 0, kAccept = 1, kResidualGumbel = 2, kBonusGumbel = 3 };
+
+__device__ __forceinline__ uint32_t ctr_word3(uint32_t cycle, uint32_t purpose) {
+    return (cycle << 4) | purpose;
+}
+
+// ((x >> 9) + 0.5) * 2^-23, exactly: the top 23 bits become the mantissa of a
+// float in [1, 2); subtracting 1 is exact (both in [1, 2)), and adding 2^-24
+// to a multiple of 2^-23 below 1 needs at most 24 significant bits.
+__device__ __forceinline__ float uniform_from_bits(uint32_t x) {
+    const float f = __uint_as_float((x >> 9) | 0x3F800000u);
+    return __fadd_rn(__fsub_rn(f, 1.0f), 0x1p-24f);
+}
+
+// Standard Gumbel noise -log(-log u), with CUDA's accurate logf (no fast math).
+__device__ __forceinline__ float gumbel_from_uniform(float u) {
+    return -logf(-logf(u));
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+    return __uint_as_float(((uint32_t)b) << 16);
+}
+
+__device__ __forceinline__ float load_elem(const void* base, int dtype, size_t idx) {
+    return dtype == DSPARK_F32 ? __ldg((const float*)base + idx)
+                               : bf16_bits_to_float(__ldg((const uint16_t*)base + idx));
+}
+
+// First device error wins.
+__device__ __forceinline__ void report(int32_t* dev_status, int code) {
+    if (dev_status) atomicCAS(dev_status, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// Reductions.
+// ---------------------------------------------------------------------------
+// (max, sum of exp(x - max)) pairs, merged.
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+    if (m2 > m) {
+        s = s * expf(m - m2) + s2;  // expf(-inf) = 0 covers an empty side
+        m = m2;
+    } else if (m2 != -INFINITY) {
+        s = s + s2 * expf(m2 - m);
+    }
+}
+
+// (score, index) with the larger score winning and the lower index breaking ties.
+__device__ __forceinline__ bool better(float sa, int ia, float sb, int ib) {
+    return sa > sb || (sa == sb && ia < ib);
+}
+
+template <typename T>
+__device__ __forceinline__ T shfl_xor(T v, int m) {
+    return __shfl_xor_sync(0xFFFFFFFFu, v, m);
+}
+
+// Global-time based bound for device spin waits (nanoseconds).
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+}  // namespace dspark

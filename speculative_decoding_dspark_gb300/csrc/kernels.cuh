@@ -1,0 +1,128 @@
+// kernels.cuh -- launch parameters and entry points of the library's kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace dspark {
+
+// ----------------------------------------------------------------------------
+// Verify
+// ----------------------------------------------------------------------------
+constexpr int kVerifyThreads = 256;
+constexpr int kVerifyChunk = 8192;  // target-row elements per CTA unit
+
+struct RowStat {  // per (row, chunk): max and sum of exp(t - max), first argmax
+    float m, s;
+    int idx, pad;
+};
+struct VerifyJob {  // per request: the row the extra token comes from
+    int row, pos, mode, pad;  // mode 0: none, 1: residual, 2: bonus
+    float lse;
+    float pad2[3];
+};
+struct SamplePartial {  // per (request, chunk) of a Gumbel-max draw
+    float best;
+    int idx;
+    float best_alt;  // noise on p instead of the residual (empty-residual fallback)
+    int idx_alt;
+    float mass;      // residual mass seen
+    float pad[3];
+};
+
+struct VerifyParams {
+    const float* target;
+    const int32_t* cu;
+    const int32_t* y;
+    const float* q_logits;
+    const float* q_lse;
+    const float* q_tok;
+    const uint64_t* seeds;
+    uint32_t cycle;
+    float invT;
+    int greedy;
+    int R, gamma, V, max_rows, nchunk;
+    int32_t* n_acc;
+    int32_t* out_tokens;
+    float* p_tok;
+    int32_t* dev_status;
+    // workspace
+    int* ok;        // [1] cu_seqlens well formed
+    int* valid;     // [R]
+    int* cnt1;      // [R]
+    int* cnt2;      // [R]
+    RowStat* stats; // [max_rows * nchunk]
+    VerifyJob* jobs;        // [R]
+    SamplePartial* parts;   // [R * nchunk]
+};
+
+cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream);
+
+// ----------------------------------------------------------------------------
+// Draft (CUDA-core path)
+// ----------------------------------------------------------------------------
+constexpr int kDraftThreads = 256;
+constexpr int kDraftChunk = 8192;
+
+struct DraftPartial {
+    float score;
+    int idx;
+    float s_at;  // the logit s of the chosen index
+    float m, sum;
+    float pad[3];
+};
+
+struct DraftParams {
+    const void* U;
+    int u_dtype;
+    const void* W1;
+    const void* W2;
+    int w_dtype;
+    const int32_t* anchor;
+    const uint64_t* seeds;
+    uint32_t cycle;
+    float invT;
+    int greedy;
+    int R, gamma, V, rank, nchunk;
+    int32_t* y;
+    float* q_lse;
+    float* q_tok;
+    float* q_logits;
+    int32_t* dev_status;
+    // workspace
+    int* cnt;            // [R]
+    DraftPartial* parts; // [R * nchunk]
+    float* bias;         // [R * V]
+};
+
+cudaError_t launch_draft_simt(const DraftParams& p, cudaStream_t stream);
+
+// ----------------------------------------------------------------------------
+// Selection and commit
+// ----------------------------------------------------------------------------
+constexpr int kSelectThreads = 1024;
+constexpr int kSelectMaxItems = 8192;
+constexpr int kSelectMaxSteps = 64;
+
+struct SelectParams {
+    const float* c;
+    const float* c_hist;
+    const int32_t* capture_sizes;
+    const float* sps;
+    int n_steps, K_cap, mode, R, gamma;
+    float* a;
+    int32_t* l;
+    int32_t* cu;
+    int32_t* K_used;
+    int32_t* dev_status;
+};
+
+cudaError_t launch_select(const SelectParams& p, cudaStream_t stream);
+
+cudaError_t launch_philox_batch(const uint32_t* ctr, const uint64_t* keys, int n, uint32_t* out,
+                                cudaStream_t stream);
+
+cudaError_t launch_commit(const int32_t* n_acc, const int32_t* l, int R, int gamma,
+                          int32_t* commit_len, int32_t* cu_commit, int32_t* discard,
+                          int32_t* total, int32_t* dev_status, cudaStream_t stream);
+
+}  // namespace dspark

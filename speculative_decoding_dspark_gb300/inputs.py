@@ -168,7 +168,11 @@ def confidence_inputs(w: dict) -> dict:
     for the current cycle and, from an independent stream, for the cycle whose
     confidences fix the physical capacity."""
     R, gamma, seed = w["R"], w["gamma"], w["seed"]
-    tau = np.asarray(w.get("tau", [1.0] * gamma), np.float64)[:gamma]
+    # per-position calibration temperatures; positions past the given list
+    # continue the workload's +0.1 step
+    given = list(w.get("tau", []))
+    tau = np.asarray([given[k] if k < len(given) else 1.0 + 0.1 * k for k in range(gamma)],
+                     np.float64)
 
     def conf(stream):
         z = 1.0 + 1.5 * rng(seed, stream).standard_normal((R, gamma))

@@ -1,0 +1,182 @@
+"""Helpers for the GPU parity tests: run the CUDA library through its C ABI on
+seeded inputs and compare with the CPU oracle.
+
+Comparison rule: token ids, accepted counts, verify lengths and row offsets
+must agree exactly, except where the oracle itself records a rounding-level
+near tie -- the top two Gumbel (or greedy logit) scores of a draw within
+MARGIN, or |u - p/q| within MARGIN for an acceptance -- such decisions are
+counted as exempt and the rest of that request is left out; exempt decisions
+must stay under 0.1% of all decisions.  Probabilities (q(y), p(y)) agree to
+PROB_TOL absolute, log-normalisers to LSE_TOL relative.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from speculative_decoding_dspark_gb300 import binding as B
+from speculative_decoding_dspark_gb300 import inputs
+
+MARGIN = 1e-5
+PROB_TOL = 1e-5
+LSE_TOL = 1e-5
+EXEMPT_FRACTION = 1e-3
+
+
+def dev(x: np.ndarray) -> torch.Tensor:
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.uint16:
+        return torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    if x.dtype == np.uint64:
+        return torch.from_numpy(x.view(np.int64)).cuda()
+    if x.dtype == np.uint32:
+        return torch.from_numpy(x.view(np.int32)).cuda()
+    return torch.from_numpy(x).cuda()
+
+
+def host(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().numpy()
+
+
+def gpu_draft(d: dict, temperature: float, cycle: int, flags: int = 0, want_logits: bool = True):
+    U, W1, W2 = dev(d["U"]), dev(d["W1"]), dev(d["W2"])
+    R, gamma, V = U.shape
+    rank = W1.shape[1]
+    y = torch.full((R, gamma), -7, dtype=torch.int32, device="cuda")
+    q_lse = torch.full((R, gamma), float("nan"), device="cuda")
+    q_tok = torch.full((R, gamma), float("nan"), device="cuda")
+    q_logits = torch.empty((R, gamma, V), device="cuda") if want_logits else None
+    w_dtype = B.DSPARK_BF16 if W1.dtype == torch.bfloat16 else B.DSPARK_F32
+    ws = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_DRAFT, R, gamma, V, rank, 0, w_dtype, flags))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.dspark_markov_draft(U, W1, W2, dev(d["anchor"]), dev(d["seeds"]), cycle, temperature, y,
+                          q_lse, q_tok, q_logits, ws, status, flags=flags)
+    torch.cuda.synchronize()
+    out = dict(y=host(y), q_lse=host(q_lse), q_tok=host(q_tok), status=int(status.item()))
+    out["q_logits_dev"] = q_logits
+    out["q_lse_dev"], out["q_tok_dev"], out["y_dev"] = q_lse, q_tok, y
+    return out
+
+
+def gpu_verify(target, cu, y, q_logits, q_lse, q_tok, seeds, cycle, temperature, max_rows=None):
+    """All array arguments may be numpy (copied) or CUDA tensors (used as is)."""
+    t = lambda a: None if a is None else (a if isinstance(a, torch.Tensor) else dev(a))
+    target_d, cu_d, y_d = t(target), t(cu), t(y)
+    R, gamma = y_d.shape
+    V = target_d.shape[1]
+    max_rows = int(target_d.shape[0]) if max_rows is None else max_rows
+    n_acc = torch.full((R,), -7, dtype=torch.int32, device="cuda")
+    out = torch.full((R, gamma + 1), -7, dtype=torch.int32, device="cuda")
+    p_tok = torch.full((R, gamma), float("nan"), device="cuda")
+    ws = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_VERIFY, R, gamma, V, 0, max_rows))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.dspark_verify(target_d, cu_d, y_d, t(q_logits), t(q_lse), t(q_tok), t(seeds), cycle,
+                    temperature, max_rows, n_acc, out, p_tok, ws, status)
+    torch.cuda.synchronize()
+    return dict(n_acc=host(n_acc), out_tokens=host(out), p_tok=host(p_tok), status=int(status.item()))
+
+
+def gpu_select(c, c_hist, sizes, sps, K_cap, mode):
+    R, gamma = c.shape
+    a = torch.full((R, gamma), float("nan"), device="cuda")
+    l = torch.full((R,), -7, dtype=torch.int32, device="cuda")
+    cu = torch.full((R + 1,), -7, dtype=torch.int32, device="cuda")
+    K = torch.zeros(1, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t = lambda x: None if x is None else dev(x)
+    B.dspark_select_prefix(dev(c), t(c_hist), t(sizes), t(sps), K_cap, mode, a, l, cu, K, None, status)
+    torch.cuda.synchronize()
+    return dict(a=host(a), l=host(l), cu_seqlens=host(cu), K_used=int(K.item()), status=int(status.item()))
+
+
+def gpu_commit(n_acc, l, gamma):
+    R = len(n_acc)
+    cl = torch.full((R,), -7, dtype=torch.int32, device="cuda")
+    cu = torch.full((R + 1,), -7, dtype=torch.int32, device="cuda")
+    disc = torch.full((R,), -7, dtype=torch.int32, device="cuda")
+    tot = torch.zeros(1, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.dspark_commit_lengths(dev(np.asarray(n_acc, np.int32)), None if l is None else dev(np.asarray(l, np.int32)),
+                            gamma, cl, cu, disc, tot, status)
+    torch.cuda.synchronize()
+    return dict(commit_len=host(cl), cu_commit=host(cu), discard=host(disc), total=int(tot.item()),
+                status=int(status.item()))
+
+
+class Tally:
+    """Counts decisions and exempt near ties across a test."""
+
+    def __init__(self):
+        self.decisions = 0
+        self.exempt = 0
+        self.errors = []
+
+    def check(self):
+        assert not self.errors, self.errors[:10]
+        assert self.exempt <= max(1, EXEMPT_FRACTION * self.decisions) or self.decisions == 0, \
+            (self.exempt, self.decisions)
+
+
+def compare_draft(tally: Tally, g: dict, o: dict, temperature: float, rows=None):
+    """Returns the set of request rows whose drafts matched completely."""
+    R, gamma = o["y"].shape
+    clean = set()
+    for i in range(R):
+        gi = i if rows is None else rows[i]
+        ok = True
+        for k in range(gamma):
+            tally.decisions += 1
+            if g["y"][gi, k] != o["y"][i, k]:
+                if o["margin"][i, k] <= MARGIN:
+                    tally.exempt += 1
+                else:
+                    tally.errors.append(("draft token", gi, k, int(g["y"][gi, k]), int(o["y"][i, k]),
+                                         float(o["margin"][i, k])))
+                ok = False
+                break
+            if temperature > 0:
+                if abs(g["q_tok"][gi, k] - o["q_tok"][i, k]) > PROB_TOL:
+                    tally.errors.append(("q_tok", gi, k, float(g["q_tok"][gi, k]), float(o["q_tok"][i, k])))
+                lse = o["q_lse"][i, k]
+                if abs(g["q_lse"][gi, k] - lse) > LSE_TOL * max(1.0, abs(lse)):
+                    tally.errors.append(("q_lse", gi, k, float(g["q_lse"][gi, k]), float(lse)))
+        if ok:
+            clean.add(i)
+    return clean
+
+
+def compare_verify(tally: Tally, g: dict, o: dict, l, rows=None, only=None):
+    """Compare n_acc, out_tokens and p_tok of the oracle's requests (optionally a
+    subset); l = the verify length of each oracle request."""
+    R = len(o["n_acc"])
+    for i in range(R):
+        if only is not None and i not in only:
+            continue
+        gi = i if rows is None else rows[i]
+        n_o, n_g = int(o["n_acc"][i]), int(g["n_acc"][gi])
+        tally.decisions += max(n_o, 0) + 1
+        if n_o != n_g:
+            j = min(n_o, n_g)
+            if j >= 0 and o["accept_margin"][i, j] <= MARGIN:
+                tally.exempt += 1
+            else:
+                tally.errors.append(("n_acc", gi, n_g, n_o))
+            continue
+        if list(g["out_tokens"][gi]) != list(o["out_tokens"][i]):
+            if o["sample_margin"][i] <= MARGIN:
+                tally.exempt += 1
+            else:
+                tally.errors.append(("out_tokens", gi, list(g["out_tokens"][gi]), list(o["out_tokens"][i]),
+                                     float(o["sample_margin"][i])))
+            continue
+        if n_o < 0:
+            continue
+        for j in range(min(n_o + 1, int(l[i]))):  # the drafts examined
+            if abs(g["p_tok"][gi, j] - o["p_tok"][i, j]) > PROB_TOL:
+                tally.errors.append(("p_tok", gi, j, float(g["p_tok"][gi, j]), float(o["p_tok"][i, j])))
+
+
+def cycle_inputs(name: str, seed_offset: int = 0, **overrides):
+    w = inputs.workload(name, seed_offset=seed_offset, **overrides)
+    d = inputs.draft_inputs(w)
+    return w, d

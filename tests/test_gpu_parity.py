@@ -1,0 +1,272 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle on
+the same seeded inputs.
+
+Small cases compare every element; they span several vocabulary tiles and
+chunks with a ragged tail.  The full-size workloads run the whole batch on the
+GPU and replay a sample of requests on the oracle (the draft and verify of a
+request depend only on that request's inputs and counters), while the
+selection is compared on every candidate.
+"""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import parity_helpers as H  # noqa: E402
+from speculative_decoding_dspark_gb300 import inputs  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def B():
+    from speculative_decoding_dspark_gb300 import build
+    build.build()
+    from speculative_decoding_dspark_gb300 import binding
+    return binding
+
+
+# ------------------------------------------------------------------ generator
+def test_philox_bit_exact(B, orc):
+    g = np.random.default_rng(5)
+    n = 1 << 20
+    ctr = g.integers(0, 1 << 32, size=(n, 4), dtype=np.uint64).astype(np.uint32)
+    keys = g.integers(0, 1 << 63, size=n, dtype=np.uint64) * np.uint64(2) + np.uint64(1)
+    out = torch.zeros((n, 4), dtype=torch.int32, device="cuda")
+    B.dspark_philox4x32_10(H.dev(ctr).view(torch.int32), H.dev(keys), out)
+    torch.cuda.synchronize()
+    ref = orc.philox4x32_10_batch(ctr, keys)
+    np.testing.assert_array_equal(H.host(out).view(np.uint32), ref)
+
+
+# ------------------------------------------------------------------ draft
+DRAFT_CASES = [
+    # name, overrides, temperature, flags
+    ("tiny_exhaustive", {}, 1.0, 0),
+    ("tiny_exhaustive", {}, 0.0, 0),
+    ("batched_sampling", dict(R=6, V=17416, gamma=4, rank=64, w_sigma=0.2), 0.7, 1),
+    ("batched_sampling", dict(R=6, V=17416, gamma=4, rank=64, w_sigma=0.2), 0.7, 0),
+    ("batched_sampling", dict(R=3, V=9001, gamma=3, rank=40, w_sigma=0.2), 1.0, 0),
+    ("qwen3_8b_greedy", dict(R=5, V=20480, gamma=7, rank=128, w_sigma=0.2), 0.0, 0),
+    ("qwen3_8b_greedy", dict(R=5, V=20480, gamma=7, rank=128, w_sigma=0.2), 0.0, 1),
+    ("batched_sampling", dict(R=130, V=4096, gamma=2, rank=64, w_sigma=0.2), 0.7, 0),
+]
+
+
+@pytest.mark.parametrize("name,over,T,flags", DRAFT_CASES)
+def test_draft_parity_small(B, orc, name, over, T, flags):
+    w, d = H.cycle_inputs(name, **over)
+    tally = H.Tally()
+    for cycle in range(3):
+        g = H.gpu_draft(d, T, cycle, flags=flags)
+        o = orc.markov_draft(d["U"], d["W1"], d["W2"], d["anchor"], d["seeds"], cycle, T)
+        assert g["status"] == 0
+        clean = H.compare_draft(tally, g, o, T)
+        # q_logits: the scaled logits of every vocabulary entry
+        ql = H.host(g["q_logits_dev"])
+        for r in clean:
+            np.testing.assert_allclose(ql[r], o["q_logits"][r], rtol=2e-6, atol=2e-5)
+    tally.check()
+
+
+def test_draft_tiny_many_cycles(B, orc):
+    """The V=64 workload: 2000 cycles at T=1 and 2000 greedy."""
+    w, d = H.cycle_inputs("tiny_exhaustive")
+    for T in (1.0, 0.0):
+        tally = H.Tally()
+        for cycle in range(2000):
+            g = H.gpu_draft(d, T, cycle, want_logits=False)
+            o = orc.markov_draft(d["U"], d["W1"], d["W2"], d["anchor"], d["seeds"], cycle, T,
+                                 want_logits=False)
+            H.compare_draft(tally, g, o, T)
+        tally.check()
+
+
+# ------------------------------------------------------------------ verify
+def _oracle_draft_as_inputs(o):
+    return (o["y"].astype(np.int32), o["q_logits"].astype(np.float32),
+            o["q_lse"].astype(np.float32), o["q_tok"].astype(np.float32))
+
+
+VERIFY_CASES = [
+    ("tiny_exhaustive", {}, 1.0),
+    ("tiny_exhaustive", {}, 0.0),
+    ("batched_sampling", dict(R=7, V=20000, gamma=5, rank=16, w_sigma=0.3), 0.7),
+    ("varlen_verify", dict(R=24, V=10007, gamma=5, rank=16, w_sigma=0.3), 1.0),
+    ("qwen3_8b_greedy", dict(R=9, V=16390, gamma=7, rank=16, w_sigma=0.3), 0.0),
+]
+
+
+@pytest.mark.parametrize("name,over,T", VERIFY_CASES)
+def test_verify_parity_small(B, orc, name, over, T):
+    """Verify alone, fed the oracle's own draft (rounded to fp32)."""
+    w, d = H.cycle_inputs(name, **over)
+    full = inputs.target_full(w, d["U"])
+    l = inputs.verify_lengths(w)
+    cu = inputs.cu_from_lengths(l)
+    target = inputs.pack_rows(full, l)
+    tally = H.Tally()
+    for cycle in range(4):
+        o_d = orc.markov_draft(d["U"], d["W1"], d["W2"], d["anchor"], d["seeds"], cycle, T)
+        y, ql, qlse, qtok = _oracle_draft_as_inputs(o_d)
+        o_v = orc.verify(target, cu, y, o_d["q_logits"], d["seeds"], cycle, T)
+        g_v = H.gpu_verify(target, cu, y, ql if T > 0 else None, qlse if T > 0 else None,
+                           qtok if T > 0 else None, d["seeds"] if T > 0 else None, cycle, T)
+        assert g_v["status"] == 0 and o_v["status"] == 0
+        H.compare_verify(tally, g_v, o_v, l)
+    tally.check()
+
+
+def test_verify_tiny_many_cycles(B, orc):
+    """The V=64 workload, 2000 full cycles draft -> verify on the GPU vs the oracle."""
+    w, d = H.cycle_inputs("tiny_exhaustive")
+    full = inputs.target_full(w, d["U"])
+    l = inputs.verify_lengths(w)
+    cu = inputs.cu_from_lengths(l)
+    target = inputs.pack_rows(full, l)
+    tD, cuD, seedsD = H.dev(target), H.dev(cu), H.dev(d["seeds"])
+    for T in (1.0, 0.0):
+        tally = H.Tally()
+        for cycle in range(2000):
+            g = H.gpu_draft(d, T, cycle)
+            gv = H.gpu_verify(tD, cuD, g["y_dev"], g["q_logits_dev"] if T > 0 else None,
+                              g["q_lse_dev"] if T > 0 else None, g["q_tok_dev"] if T > 0 else None,
+                              seedsD if T > 0 else None, cycle, T)
+            o = orc.markov_draft(d["U"], d["W1"], d["W2"], d["anchor"], d["seeds"], cycle, T)
+            ov = orc.verify(target, cu, o["y"], o["q_logits"], d["seeds"], cycle, T)
+            clean = H.compare_draft(tally, g, o, T)
+            H.compare_verify(tally, gv, ov, l, only=clean)
+        tally.check()
+
+
+def test_verify_edge_cases(B, orc):
+    # every request plain decode (l = 0), V not a multiple of 4 (scalar path)
+    R, V, gamma = 5, 1001, 4
+    g = np.random.default_rng(2)
+    target = g.normal(0, 2, (R, V)).astype(np.float32)
+    cu = np.arange(R + 1, dtype=np.int32)
+    y = np.zeros((R, gamma), np.int32)
+    seeds = inputs.request_seeds(99, R)
+    ql = np.zeros((R, gamma, V), np.float32)
+    for T in (1.0, 0.0):
+        gv = H.gpu_verify(target, cu, y, ql, np.zeros((R, gamma), np.float32),
+                          np.ones((R, gamma), np.float32), seeds, 3, T)
+        ov = orc.verify(target, cu, y, ql.astype(np.float64), seeds, 3, T)
+        assert (gv["n_acc"] == 0).all()
+        np.testing.assert_array_equal(gv["out_tokens"], ov["out_tokens"])
+    # a bad draft token and a bad length are reported, the request outputs are -1
+    l = np.array([2, 3, 1, 0, 2], np.int32)
+    cu = inputs.cu_from_lengths(l)
+    target = g.normal(0, 2, (cu[-1], V)).astype(np.float32)
+    y = g.integers(0, V, (R, gamma)).astype(np.int32)
+    y[1, 1] = V + 3
+    gv = H.gpu_verify(target, cu, y, ql, np.zeros((R, gamma), np.float32),
+                      np.ones((R, gamma), np.float32), seeds, 0, 1.0)
+    assert gv["status"] == -6 and gv["n_acc"][1] == -1 and (gv["out_tokens"][1] == -1).all()
+    assert (gv["n_acc"][[0, 2, 3, 4]] >= 0).all()
+    bad_cu = cu.copy(); bad_cu[3] = bad_cu[2] - 1
+    gv = H.gpu_verify(target, bad_cu, y, ql, np.zeros((R, gamma), np.float32),
+                      np.ones((R, gamma), np.float32), seeds, 0, 1.0)
+    assert gv["status"] == -6 and (gv["n_acc"] == -1).all()
+
+
+# ------------------------------------------------------------------ select / commit
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+@pytest.mark.parametrize("R,gamma,seed", [(512, 5, 0), (3, 3, 1), (97, 7, 2), (1000, 8, 3)])
+def test_select_parity(B, orc, mode, R, gamma, seed):
+    w = inputs.workload("confidence_scheduled", seed_offset=seed, R=R, gamma=gamma)
+    ci = inputs.confidence_inputs(w)
+    sizes, sps = ci["capture_sizes"], ci["sps"]
+    if R < 64:
+        sizes = np.array([3, 4, 5, 6, 8, 12], np.int32)
+        sps = (1.0 / (0.010 + 0.0009 * sizes)).astype(np.float32)
+    for K_cap in sorted({R, R + (R * gamma) // 3, 2 * R, R * (gamma + 1)}):
+        o = orc.select_prefix(ci["c"], ci["c_hist"], sizes, sps, K_cap, mode)
+        g = H.gpu_select(ci["c"], ci["c_hist"], sizes, sps, K_cap, mode)
+        assert o["status"] == 0 and g["status"] == 0
+        np.testing.assert_array_equal(g["a"].view(np.uint32), o["a"].view(np.uint32))
+        if o["theta_gap"] > 1e-9:
+            np.testing.assert_array_equal(g["l"], o["l"])
+            np.testing.assert_array_equal(g["cu_seqlens"], o["cu_seqlens"])
+            assert g["K_used"] == o["K_used"]
+
+
+def test_select_ties_and_errors(B, orc):
+    c = np.array([[1.0, 1.0], [1.0, 0.5], [0.7, 0.7]], np.float32)
+    for K_cap in range(3, 10):
+        o = orc.select_prefix(c, None, None, None, K_cap, 0)
+        g = H.gpu_select(c, None, None, None, K_cap, 0)
+        np.testing.assert_array_equal(g["l"], o["l"])
+    bad = c.copy(); bad[2, 1] = np.nan
+    g = H.gpu_select(bad, None, None, None, 6, 0)
+    assert g["status"] == -6 and (g["l"] == -1).all()
+    with pytest.raises(B.DSparkError):
+        H.gpu_select(c, None, None, None, 2, 0)
+
+
+def test_commit_parity(B, orc):
+    g = np.random.default_rng(0)
+    for R, gamma in [(1, 5), (700, 7), (3000, 5)]:
+        l = g.integers(0, gamma + 1, R).astype(np.int32)
+        n_acc = (g.random(R) * (l + 1)).astype(np.int32)
+        for ll in (l, None):
+            o = orc.commit_lengths(n_acc if ll is not None else np.minimum(n_acc, gamma), ll, gamma)
+            gg = H.gpu_commit(n_acc if ll is not None else np.minimum(n_acc, gamma), ll, gamma)
+            for key in ("commit_len", "cu_commit", "discard"):
+                np.testing.assert_array_equal(gg[key], o[key])
+            assert gg["total"] == o["total"] and gg["status"] == 0
+
+
+# ------------------------------------------------------------------ full-size workloads
+FULL = [
+    ("qwen3_8b_greedy", 4, [0, 7, 15]),
+    ("batched_sampling", 1, [0, 77, 127]),
+    ("varlen_verify", 1, None),
+    ("confidence_scheduled", 1, [0, 300, 511]),
+]
+
+
+@pytest.mark.parametrize("name,cycles,sample", FULL)
+def test_full_size_cycle_sampled(B, orc, name, cycles, sample):
+    w, d = H.cycle_inputs(name)
+    T = float(w["temperature"])
+    full = inputs.target_full(w, d["U"])
+    R, gamma = w["R"], w["gamma"]
+    tally = H.Tally()
+    for cycle in range(cycles):
+        if w.get("confidence"):
+            ci = inputs.confidence_inputs(w)
+            o_s = orc.select_prefix(ci["c"], ci["c_hist"], ci["capture_sizes"], ci["sps"], ci["K_cap"], 1)
+            g_s = H.gpu_select(ci["c"], ci["c_hist"], ci["capture_sizes"], ci["sps"], ci["K_cap"], 1)
+            np.testing.assert_array_equal(g_s["l"], o_s["l"])
+            l = o_s["l"]
+        else:
+            l = inputs.verify_lengths(w)
+        cu = inputs.cu_from_lengths(l)
+        target = inputs.pack_rows(full, l)
+        g = H.gpu_draft(d, T, cycle)
+        gv = H.gpu_verify(target, cu, g["y_dev"], g["q_logits_dev"] if T > 0 else None,
+                          g["q_lse_dev"] if T > 0 else None, g["q_tok_dev"] if T > 0 else None,
+                          H.dev(d["seeds"]) if T > 0 else None, cycle, T)
+        assert g["status"] == 0 and gv["status"] == 0
+        rows = sample
+        if rows is None:  # include the shortest and longest verify lengths
+            rows = sorted({int(np.argmin(l)), int(np.argmax(l)), R // 2})
+        sub = dict(U=d["U"][rows], anchor=d["anchor"][rows], seeds=d["seeds"][rows])
+        o = orc.markov_draft(sub["U"], d["W1"], d["W2"], sub["anchor"], sub["seeds"], cycle, T,
+                             req_ids=rows)
+        lsub = l[rows]
+        ov = orc.verify(inputs.pack_rows(full[rows], lsub), inputs.cu_from_lengths(lsub), o["y"],
+                        o["q_logits"], sub["seeds"], cycle, T, req_ids=rows)
+        clean = H.compare_draft(tally, g, o, T, rows=rows)
+        H.compare_verify(tally, gv, ov, lsub, rows=rows, only=clean)
+        # properties that hold for every request of the batch
+        assert ((gv["n_acc"] >= 0) & (gv["n_acc"] <= l)).all()
+        for r in range(R):
+            n = gv["n_acc"][r]
+            assert (gv["out_tokens"][r, :n] == g["y"][r, :n]).all()
+            assert 0 <= gv["out_tokens"][r, n] < w["V"]
+            assert (gv["out_tokens"][r, n + 1:] == -1).all()
+    tally.check()
