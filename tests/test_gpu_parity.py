@@ -71,6 +71,25 @@ def test_draft_parity_small(B, orc, name, over, T, flags):
     tally.check()
 
 
+@pytest.mark.parametrize("R,rank,T", [(128, 64, 0.7), (256, 128, 1.0), (100, 64, 0.0)])
+def test_draft_multi_tile_elementwise(B, orc, R, rank, T):
+    """Full vocabulary with every request row of the tile active: each CTA walks
+    many vocabulary tiles, reusing its base-logit buffer and both accumulators.
+    The scaled logits of sampled requests match the oracle element by element."""
+    w, d = H.cycle_inputs("batched_sampling", R=R, V=151936, gamma=3, rank=rank, w_sigma=0.2)
+    g = H.gpu_draft(d, T, 1)
+    assert g["status"] == 0
+    ql = H.host(g["q_logits_dev"])
+    rows = [0, R // 2 + 1, R - 1]
+    o = orc.markov_draft(d["U"][rows], d["W1"], d["W2"], d["anchor"][rows], d["seeds"][rows], 1, T,
+                         req_ids=rows)
+    tally = H.Tally()
+    clean = H.compare_draft(tally, g, o, T, rows=rows)
+    tally.check()
+    for i in clean:
+        np.testing.assert_allclose(ql[rows[i]], o["q_logits"][i], rtol=2e-6, atol=2e-5)
+
+
 def test_draft_tiny_many_cycles(B, orc):
     """The V=64 workload: 2000 cycles at T=1 and 2000 greedy."""
     w, d = H.cycle_inputs("tiny_exhaustive")
