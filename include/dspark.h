@@ -190,6 +190,38 @@ int dspark_verify(const float* target_logits, const int32_t* cu_seqlens,
                   size_t ws_bytes, int32_t* dev_status, dspark_stream_t stream);
 
 /*
+ * dspark_verify_static_scratch -- dspark_verify for callers that cannot
+ * provide a workspace.  The pages have no counterpart of this call; it exists
+ * for callers that are not allowed to allocate device memory, such as a plugin
+ * inside a serving engine whose device memory is all owned and accounted by
+ * the engine's own pool (an extra cudaMalloc can synchronise the device and
+ * escapes that accounting), or code that has no spare buffer to pass down.
+ *
+ * Same arguments, results and status codes as dspark_verify, minus ws and
+ * ws_bytes.  The scratch is a static device array of
+ * DSPARK_VERIFY_STATIC_SCRATCH_BYTES (2 MiB) compiled into the library; every
+ * GPU that loads the library holds it until the process exits.  The call
+ * allocates nothing.  Sizes whose scratch need
+ * (dspark_workspace_size(DSPARK_OP_VERIFY, R, gamma, V, 0, max_rows, 0, 0))
+ * exceeds the array return DSPARK_ERR_CAPACITY and enqueue nothing.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture starts.  All calls on a device share the array
+ * and it keeps the last call's contents; the kernels reset their own counters
+ * at the start of every call.  Calls whose kernels overlap on the GPU (for
+ * example on two streams at once) race on the array: serialise them.
+ */
+#define DSPARK_VERIFY_STATIC_SCRATCH_BYTES (2u * 1024u * 1024u)
+
+int dspark_verify_static_scratch(const float* target_logits, const int32_t* cu_seqlens,
+                                 const int32_t* draft_tokens, const float* q_logits,
+                                 const float* q_lse, const float* q_tok, const uint64_t* seeds,
+                                 uint32_t cycle, float temperature, int R, int gamma, int V,
+                                 int max_rows, int32_t* n_accepted, int32_t* out_tokens,
+                                 float* p_tok, int32_t* dev_status, dspark_stream_t stream);
+
+/*
  * dspark_select_prefix -- survival, capacity and prefix-closed top-K
  * (explainer sections 5, 8, 9 and 10).
  *

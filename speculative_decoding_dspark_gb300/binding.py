@@ -33,7 +33,7 @@ DSPARK_SELECT_FIXED, DSPARK_SELECT_HISTORY, DSPARK_SELECT_CURRENT, DSPARK_SELECT
 
 EXPORTED = ["dspark_status_string", "dspark_version", "dspark_workspace_size", "dspark_philox4x32_10",
             "dspark_markov_draft_uses_tensor_cores", "dspark_markov_draft", "dspark_verify",
-            "dspark_select_prefix", "dspark_commit_lengths"]
+            "dspark_select_prefix", "dspark_commit_lengths", "dspark_verify_static_scratch"]
 
 
 class DSparkError(RuntimeError):
@@ -64,6 +64,9 @@ def _load():
     L.dspark_select_prefix.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp,
                                        vp, sz, vp, vp]
     L.dspark_select_prefix.restype = i32
+    L.dspark_verify_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, vp, u32, f32, i32, i32, i32,
+                                               i32, vp, vp, vp, vp, vp]
+    L.dspark_verify_static_scratch.restype = i32
     L.dspark_philox4x32_10.argtypes = [vp, vp, i32, vp, vp]
     L.dspark_philox4x32_10.restype = i32
     L.dspark_commit_lengths.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, vp]
@@ -188,6 +191,38 @@ def dspark_verify(target_logits, cu_seqlens, draft_tokens, q_logits, q_lse, q_to
                           gamma, V, int(max_rows), _ptr(n_accepted), _ptr(out_tokens), _ptr(p_tok),
                           _ptr(ws), ws.numel(), _ptr(dev_status), _stream(stream))
     _raise("dspark_verify", st)
+
+
+def dspark_verify_static_scratch(target_logits, cu_seqlens, draft_tokens, q_logits, q_lse, q_tok,
+                                 seeds, cycle, temperature, max_rows, n_accepted, out_tokens,
+                                 p_tok=None, dev_status=None, stream=None):
+    """dspark_verify without a workspace argument, for callers that are not
+    allowed to allocate device memory (for example a plugin inside a serving
+    engine whose device memory all belongs to the engine's pool).  The scratch
+    is a fixed 2 MiB array inside the library, shared by every call on a
+    device: calls must not overlap on the GPU, and the first call on a device
+    (which looks the array up) should happen before any stream capture."""
+    R, gamma = draft_tokens.shape
+    V = target_logits.shape[1]
+    _check(target_logits, "target_logits", torch.float32)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, (R + 1,))
+    _check(draft_tokens, "draft_tokens", torch.int32)
+    _check(q_logits, "q_logits", torch.float32, (R, gamma, V), allow_none=True)
+    _check(q_lse, "q_lse", torch.float32, (R, gamma), allow_none=True)
+    _check(q_tok, "q_tok", torch.float32, (R, gamma), allow_none=True)
+    _check(seeds, "seeds", torch.int64, (R,), allow_none=True)
+    _check(n_accepted, "n_accepted", torch.int32, (R,))
+    _check(out_tokens, "out_tokens", torch.int32, (R, gamma + 1))
+    _check(p_tok, "p_tok", torch.float32, (R, gamma), allow_none=True)
+    _check(dev_status, "dev_status", torch.int32, allow_none=True)
+    if target_logits.shape[0] < max_rows:
+        raise ValueError("target_logits has fewer rows than max_rows")
+    st = _L.dspark_verify_static_scratch(_ptr(target_logits), _ptr(cu_seqlens), _ptr(draft_tokens),
+                                         _ptr(q_logits), _ptr(q_lse), _ptr(q_tok), _ptr(seeds),
+                                         int(cycle), float(temperature), R, gamma, V, int(max_rows),
+                                         _ptr(n_accepted), _ptr(out_tokens), _ptr(p_tok),
+                                         _ptr(dev_status), _stream(stream))
+    _raise("dspark_verify_static_scratch", st)
 
 
 def dspark_select_prefix(c, c_hist, capture_sizes, sps, K_cap, mode, a, l, cu_seqlens, K_used,
