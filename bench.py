@@ -45,6 +45,10 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--stage", choices=["cycle", "draft", "verify"], default="cycle",
+                    help="time the whole cycle (default) or one call of it (profiling)")
+    ap.add_argument("--gamma", type=int, default=None, help="override the workload's block size")
+    ap.add_argument("--temperature", type=float, default=None, help="override the workload's T")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -183,7 +187,12 @@ def run_ours(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     torch.cuda.set_device(local)
-    w = inputs.workload(args.workload)
+    over = {}
+    if args.gamma is not None:
+        over["gamma"] = args.gamma
+    if args.temperature is not None:
+        over["temperature"] = args.temperature
+    w = inputs.workload(args.workload, **over)
     R, V, gamma, rank_r = w["R"], w["V"], w["gamma"], w["rank"]
     T = float(w["temperature"])
     d = inputs.draft_inputs(w)
@@ -233,21 +242,34 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     uses_tc = B.dspark_markov_draft_uses_tensor_cores(B.DSPARK_BF16, B.DSPARK_BF16, R, V, rank_r)
 
+    run_select = run_commit = args.stage == "cycle"
+    run_draft = args.stage in ("cycle", "draft")
+    run_verify = args.stage in ("cycle", "verify")
+    if args.stage == "verify":  # the verify stage needs lengths and a draft once
+        B.dspark_select_prefix(c, c_hist, sizes, sps, K_cap, mode, a, l, cu, K_used, None, status)
+        B.dspark_markov_draft(U, W1, W2, anchor, seeds, 0, T, y, q_lse, q_tok, q_logits, ws_d, status)
+
     def step(cycle, ev=None):
         if ev is not None: ev[0].record(stream)
-        B.dspark_select_prefix(c, c_hist, sizes, sps, K_cap, mode, a, l, cu, K_used, None, status)
+        if run_select:
+            B.dspark_select_prefix(c, c_hist, sizes, sps, K_cap, mode, a, l, cu, K_used, None, status)
         if ev is not None: ev[1].record(stream)
-        B.dspark_markov_draft(U, W1, W2, anchor, seeds, cycle, T, y, q_lse, q_tok, q_logits, ws_d, status)
+        if run_draft:
+            B.dspark_markov_draft(U, W1, W2, anchor, seeds, cycle, T, y, q_lse, q_tok, q_logits, ws_d,
+                                  status)
         if ev is not None: ev[2].record(stream)
-        B.dspark_verify(target, cu, y, q_logits, q_lse, q_tok, seeds, cycle, T, max_rows, n_acc, out,
-                        p_tok, ws_v, status)
+        if run_verify:
+            B.dspark_verify(target, cu, y, q_logits, q_lse, q_tok, seeds, cycle, T, max_rows, n_acc,
+                            out, p_tok, ws_v, status)
         if ev is not None: ev[3].record(stream)
-        B.dspark_commit_lengths(n_acc, l, gamma, cl, cuc, disc, tot, status)
+        if run_commit:
+            B.dspark_commit_lengths(n_acc, l, gamma, cl, cuc, disc, tot, status)
         if ev is not None: ev[4].record(stream)
 
     # launches of this library per step
     draft_launches = gamma if uses_tc else 1 + 2 * gamma
-    launches_per_step = 1 + draft_launches + (3 if T > 0 else 2) + 1
+    launches_per_step = (int(run_select) + draft_launches * int(run_draft) +
+                         (3 if T > 0 else 2) * int(run_verify) + int(run_commit))
 
     for i in range(args.warmup):
         step(i)
@@ -301,7 +323,7 @@ def run_ours(args):
 
     # end to end through the public API from pinned host buffers
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.stage == "cycle":
         hU = U.cpu().pin_memory(); htgt = target.cpu().pin_memory(); hc = c.cpu().pin_memory()
         hch = c_hist.cpu().pin_memory(); ha = anchor.cpu().pin_memory(); hs = seeds.cpu().pin_memory()
         h_out = torch.empty((R, gamma + 1), dtype=torch.int32).pin_memory()
@@ -337,7 +359,7 @@ def run_ours(args):
                "d2h_bytes_per_step": bo, "steps": n_e2e}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.stage == "cycle":
         per_req, sample = oracle_sample(w, d, inputs.target_full(w, d["U"]), 4, 0)
         cpu = {"value": 1.0 / (per_req * R), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
 
@@ -350,7 +372,7 @@ def run_ours(args):
                 "config": dict(workload_config(w), parallelism=f"replicas x{world}"),
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
                 "gpu_launches": launches_per_step * args.steps,
-                "stage_ms": per, "logits_gb_s": (R * (gamma + 1) * V * 4 + R * gamma * V * 2) /
+                "stage": args.stage, "stage_ms": per, "logits_gb_s": (R * (gamma + 1) * V * 4 + R * gamma * V * 2) /
                 (ms_step / 1000.0) / 1e9, "draft_path": "tcgen05" if uses_tc else "simt"}
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -14,15 +14,19 @@
 //     ring of 16 KB stages (64 rank elements per stage);
 //   D = A . B^T accumulated in fp32 in tensor memory, two 128-column buffers so
 //     the epilogue of one vocabulary tile overlaps the MMAs of the next;
-//   epilogue (8 warps, thread = one request x 64 vocabulary columns): adds the
-//     base logits U (TMA tile), scales by 1/T, adds Gumbel noise from Philox,
-//     keeps a running argmax and (max, sum of exp); optionally stores the
-//     scaled logits q_logits.
+//   epilogue (16 warps; thread = one request x 32 vocabulary columns, in two
+//     16-column passes): adds the base logits U (prefetched into L2 by TMA and
+//     read straight into registers), scales by 1/T, keeps (max, sum of exp) and
+//     draws the Gumbel-max sample in its exponential-race form: with
+//     w = exp(s - m) and E = -log(u), the largest s + Gumbel(u) = s - log(E) is
+//     the largest w / E, so a candidate replaces the best when
+//     w * E_best > w_best * E (one log and one exp per entry); optionally
+//     stores the scaled logits q_logits.
 // Each CTA leaves one partial per request; the last CTA to finish (atomic
 // counter, no spin) reduces them, one warp per request, into y, q_lse, q_tok.
 //
 // Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM owner),
-// warps 2-9 = gather + epilogue.  Every mbarrier wait is bounded (2 s); a
+// warps 2-17 = gather + epilogue.  Every mbarrier wait is bounded (2 s); a
 // timeout aborts the CTA cleanly and reports DSPARK_ERR_TIMEOUT.
 #include <cuda.h>
 
@@ -36,9 +40,9 @@ constexpr int kM = 128;                       // requests per CTA (MMA M)
 constexpr int kNV = 128;                      // vocabulary rows per tile (MMA N)
 constexpr int kKB = 64;                       // rank elements per stage (128-byte rows)
 constexpr int kTileBytes = 128 * kKB * 2;     // 16 KB: one operand k-block
-constexpr int kUBytes = kM * kNV * 2;         // 32 KB: base logits of one tile
-constexpr int kThreads = 320;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;
+constexpr int kThreads = 64 + kEpiWarps * 32;
+constexpr int kCols = 32;                     // vocabulary columns per epilogue thread
 constexpr int kMaxStages = 8;
 constexpr int kMaxP = 256;                    // partials per request (>= CTAs per block)
 constexpr uint32_t kTmemCols = 256;
@@ -53,6 +57,7 @@ struct TcPartial {
 };
 
 struct TcParams {
+    const uint16_t* U;
     const uint16_t* W1;
     const int32_t* anchor;
     const uint64_t* seeds;
@@ -73,7 +78,7 @@ struct TcParams {
 struct Bars {
     uint64_t full[kMaxStages], empty[kMaxStages];
     uint64_t tfull[2], tempty[2];
-    uint64_t ufull, uempty, afull, mma_done;
+    uint64_t afull, mma_done;
     uint32_t tmem_slot;
     int abort_flag;
     int last;
@@ -102,8 +107,7 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_con
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = sA + p.nkb * kTileBytes;
-    uint8_t* sU = sB + p.n_stages * kTileBytes;
-    Bars& bar = *reinterpret_cast<Bars*>(sU + kUBytes);
+    Bars& bar = *reinterpret_cast<Bars*>(sB + p.n_stages * kTileBytes);
     volatile int* abort_flag = &bar.abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -115,8 +119,6 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_con
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) { tc::mbar_init(&bar.full[s], 1); tc::mbar_init(&bar.empty[s], 1); }
         for (int a = 0; a < 2; ++a) { tc::mbar_init(&bar.tfull[a], 1); tc::mbar_init(&bar.tempty[a], kEpiWarps); }
-        tc::mbar_init(&bar.ufull, 1);
-        tc::mbar_init(&bar.uempty, kEpiWarps);
         tc::mbar_init(&bar.afull, kEpiWarps);
         tc::mbar_init(&bar.mma_done, 1);
         bar.abort_flag = 0;
@@ -137,7 +139,7 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_con
     const uint32_t tmem_base = bar.tmem_slot;
     const int n_local = cidx < p.n_tiles ? (p.n_tiles - 1 - cidx) / p.P + 1 : 0;
 
-    // per-request running partial (epilogue threads)
+    // per-request running partial of this thread (epilogue threads)
     float best = -INFINITY, s_at = 0.0f, mx = -INFINITY, sum = 0.0f;
     int bidx = INT_MAX;
 
@@ -148,10 +150,12 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_con
             uint32_t ph = 0;
             int last_phase[kMaxStages];
             for (int i = 0; i < kMaxStages; ++i) last_phase[i] = -1;
-            int u_issued = -1;
             bool ok = true;
             for (int i = 0; ok && i < n_local; ++i) {
                 const int t = cidx + i * p.P;
+                // base logits of this tile go to L2 while its W2 tile streams in
+                tc::tma_prefetch_l2_3d(&tm_u, t * kNV, p.k, row0);
+                tc::tma_prefetch_l2_3d(&tm_u, t * kNV + kKB, p.k, row0);
                 for (int kb = 0; kb < p.nkb; ++kb) {
                     if (!tc::mbar_wait(&bar.empty[s], ph ^ 1u, abort_flag, kWaitNs)) { ok = false; break; }
                     tc::mbar_arrive_expect_tx(&bar.full[s], kTileBytes);
@@ -159,12 +163,6 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_con
                     last_phase[s] = (int)ph;
                     if (++s == S) { s = 0; ph ^= 1u; }
                 }
-                if (!ok) break;
-                if (!tc::mbar_wait(&bar.uempty, (uint32_t)(i & 1) ^ 1u, abort_flag, kWaitNs)) { ok = false; break; }
-                tc::mbar_arrive_expect_tx(&bar.ufull, kUBytes);
-                tc::tma_load_3d(sU, &tm_u, &bar.ufull, t * kNV, p.k, row0);
-                tc::tma_load_3d(sU + kUBytes / 2, &tm_u, &bar.ufull, t * kNV + kKB, p.k, row0);
-                u_issued = i;
             }
             if (*abort_flag) {
                 // let the copies already in flight land before the CTA exits
@@ -172,7 +170,6 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_con
                 volatile int* no_abort = &dummy;
                 for (int q = 0; q < S; ++q)
                     if (last_phase[q] >= 0) tc::mbar_wait(&bar.full[q], (uint32_t)last_phase[q], no_abort, kWaitNs);
-                if (u_issued >= 0) tc::mbar_wait(&bar.ufull, (uint32_t)(u_issued & 1), no_abort, kWaitNs);
             }
         }
     } else if (warp == 1) {
@@ -212,22 +209,36 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_con
         }
     } else {
         // ------------------------------------------------------------ gather + epilogue
-        const int quad = warp & 3;
-        const int half = (warp - 2) >> 2;
+        const int ew = warp - 2;           // 0..15
+        const int quad = warp & 3;         // TMEM lane quadrant this warp may read
+        const int quarter = ew >> 2;       // which 32 of the tile's 128 columns
         const int m = quad * 32 + lane;
         const int rr = row0 + m;
         {
-            const int cpr = p.rank >> 3;  // 16-byte chunks per W1 row
+            // A = W1[prev] rows, 16-byte chunks, eight loads in flight per thread
+            const int cpr = p.rank >> 3;
             const int total = kM * cpr;
-            for (int e = threadIdx.x - 64; e < total; e += kEpiWarps * 32) {
-                const int row = e / cpr, c = e - row * cpr;
-                const int g = row0 + row;
-                const int prev = g < p.R ? prev_of(p, g) : -1;
-                uint4 val = make_uint4(0u, 0u, 0u, 0u);
-                if (prev >= 0) val = __ldg(reinterpret_cast<const uint4*>(p.W1 + (size_t)prev * p.rank) + c);
-                const int kb = c >> 3, cc = c & 7;
-                *reinterpret_cast<uint4*>(sA + kb * kTileBytes + (row >> 3) * 1024 + (row & 7) * 128 +
-                                          ((cc ^ (row & 7)) << 4)) = val;
+            const int et = threadIdx.x - 64;
+            for (int base = 0; base < total; base += 8 * kEpiWarps * 32) {
+                uint4 val[8];
+                int dst_off[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int e = base + et + u * kEpiWarps * 32;
+                    val[u] = make_uint4(0u, 0u, 0u, 0u);
+                    dst_off[u] = -1;
+                    if (e < total) {
+                        const int row = e / cpr, c = e - row * cpr;
+                        const int g = row0 + row;
+                        const int prev = g < p.R ? prev_of(p, g) : -1;
+                        if (prev >= 0) val[u] = __ldg(reinterpret_cast<const uint4*>(p.W1 + (size_t)prev * p.rank) + c);
+                        const int kb = c >> 3, cc = c & 7;
+                        dst_off[u] = kb * kTileBytes + (row >> 3) * 1024 + (row & 7) * 128 + ((cc ^ (row & 7)) << 4);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (dst_off[u] >= 0) *reinterpret_cast<uint4*>(sA + dst_off[u]) = val[u];
             }
             tc::fence_proxy_async_smem();
             __syncwarp();
@@ -237,96 +248,105 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_con
         PhiloxKey K;
         if (!p.greedy) K = philox_key(row_ok ? p.seeds[rr] : 0ull);
         const uint32_t w3 = ctr_word3(p.cycle, kDraftGumbel);
-        float* qrow = (p.q_logits && row_ok) ? p.q_logits + ((size_t)rr * p.gamma + p.k) * p.V : nullptr;
+        const size_t rk = (size_t)rr * p.gamma + p.k;
+        const uint16_t* urow = p.U + rk * p.V;
+        float* qrow = (p.q_logits && row_ok) ? p.q_logits + rk * p.V : nullptr;
+        // exponential race state: best candidate's w (relative to mx) and E
+        float bw = 0.0f, bE = 1.0f;
         for (int i = 0; i < n_local; ++i) {
             const int t = cidx + i * p.P;
             const int a = i & 1;
             const uint32_t use = (uint32_t)(i >> 1);
-            // warp-uniform waits: every lane waits (acquire), all leave together
+            const int vq = t * kNV + quarter * kCols;
+            // base logits of this thread's 32 columns (already in L2), two halves
+            uint32_t uwA[8], uwB[8];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const uint4 qa = (row_ok && 8 * j < p.V - vq) ? __ldg(reinterpret_cast<const uint4*>(urow + vq) + j)
+                                                              : make_uint4(0u, 0u, 0u, 0u);
+                const uint4 qb = (row_ok && 16 + 8 * j < p.V - vq)
+                                     ? __ldg(reinterpret_cast<const uint4*>(urow + vq) + 2 + j)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+                uwA[4 * j + 0] = qa.x; uwA[4 * j + 1] = qa.y; uwA[4 * j + 2] = qa.z; uwA[4 * j + 3] = qa.w;
+                uwB[4 * j + 0] = qb.x; uwB[4 * j + 1] = qb.y; uwB[4 * j + 2] = qb.z; uwB[4 * j + 3] = qb.w;
+            }
+            // warp-uniform wait: every lane waits (acquire), all leave together
             if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.tfull[a], use & 1u, abort_flag, kWaitNs))) break;
             tc::tc_fence_after();
-            float acc[64];
-            {
-                const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(a * kNV + half * 64);
-                tc::tmem_ld_32x32b_x32<0>(taddr, acc);
-                tc::tmem_ld_32x32b_x32<32>(taddr + 32, acc);
+            const uint32_t taddr =
+                tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(a * kNV + quarter * kCols);
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                float sv[16];
+                __syncwarp();  // lanes that skipped the previous pass rejoin before the aligned load
+                tc::tmem_ld_32x32b_x16<0>(taddr + 16u * h, sv);
                 tc::tmem_ld_wait();
-            }
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bar.tempty[a]);
-            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.ufull, (uint32_t)(i & 1), abort_flag, kWaitNs))) break;
-            uint32_t uw[32];  // 64 bf16 base logits of this thread's row, two per word
-            {
-                const uint8_t* ub = sU + half * (kUBytes / 2) + m * 128;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 q4 = *reinterpret_cast<const uint4*>(ub + ((c ^ (m & 7)) << 4));
-                    uw[4 * c + 0] = q4.x; uw[4 * c + 1] = q4.y; uw[4 * c + 2] = q4.z; uw[4 * c + 3] = q4.w;
+                if (h == 1) {  // both halves are in registers: hand the accumulator back
+                    tc::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&bar.tempty[a]);
                 }
-            }
-            // consume the loaded words before releasing the buffer: a shared
-            // load still in flight must not race the TMA that refills it
+                if (!row_ok) continue;
+                const int v0 = vq + 16 * h;
+                const int nvalid = min(16, p.V - v0);
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const uint32_t word = uw[c >> 1];
-                const float u = __uint_as_float((c & 1) ? (word & 0xFFFF0000u) : (word << 16));
-                const float sb = u + acc[c];
-                acc[c] = p.greedy ? sb : sb * p.invT;
-            }
-            tc::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bar.uempty);
-            if (!row_ok) continue;
-            const int v0 = t * kNV + half * 64;
-            const int nvalid = min(64, p.V - v0);
-            if (qrow) {
-                if (nvalid == 64) {
+                for (int c = 0; c < 16; ++c) {
+                    const uint32_t word = h ? uwB[c >> 1] : uwA[c >> 1];
+                    const float u = __uint_as_float((c & 1) ? (word & 0xFFFF0000u) : (word << 16));
+                    const float sb = u + sv[c];
+                    sv[c] = p.greedy ? sb : sb * p.invT;
+                }
+                if (qrow) {
 #pragma unroll
-                    for (int c = 0; c < 64; c += 4)
-                        *reinterpret_cast<float4*>(qrow + v0 + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+                    for (int c = 0; c < 16; c += 4)
+                        if (c < nvalid)
+                            *reinterpret_cast<float4*>(qrow + v0 + c) = make_float4(sv[c], sv[c + 1], sv[c + 2], sv[c + 3]);
+                }
+                if (p.greedy) {
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        if (c < nvalid && better(sv[c], v0 + c, best, bidx)) { best = sv[c]; bidx = v0 + c; s_at = sv[c]; }
                 } else {
+                    float cm = -INFINITY;
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        if (c < nvalid) qrow[v0 + c] = acc[c];
-                }
-            }
-            if (p.greedy) {
+                    for (int c = 0; c < 16; ++c) if (c < nvalid) cm = fmaxf(cm, sv[c]);
+                    if (cm > mx) {
+                        const float sc = expf(mx - cm);  // 0 while mx = -inf
+                        sum *= sc;
+                        bw *= sc;
+                        mx = cm;
+                    }
 #pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (c < nvalid && better(acc[c], v0 + c, best, bidx)) { best = acc[c]; bidx = v0 + c; s_at = acc[c]; }
-            } else {
-                float cm = -INFINITY;
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 wd = philox4x32_10(
+                            make_uint4((uint32_t)((v0 >> 2) + q), (uint32_t)p.k, (uint32_t)rr, w3), K);
+                        const uint32_t words[4] = {wd.x, wd.y, wd.z, wd.w};
 #pragma unroll
-                for (int c = 0; c < 64; ++c) if (c < nvalid) cm = fmaxf(cm, acc[c]);
-                if (cm > mx) { sum *= expf(mx - cm); mx = cm; }
-#pragma unroll
-                for (int c = 0; c < 64; ++c) if (c < nvalid) sum += expf(acc[c] - mx);
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const uint4 wd = philox4x32_10(
-                        make_uint4((uint32_t)((v0 >> 2) + q), (uint32_t)p.k, (uint32_t)rr, w3), K);
-                    const uint32_t words[4] = {wd.x, wd.y, wd.z, wd.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c = 4 * q + e;
-                        if (c < nvalid) {
-                            const float sc = acc[c] + gumbel_from_uniform(uniform_from_bits(words[e]));
-                            if (better(sc, v0 + c, best, bidx)) { best = sc; bidx = v0 + c; s_at = acc[c]; }
+                        for (int e = 0; e < 4; ++e) {
+                            const int c = 4 * q + e;
+                            if (c < nvalid) {
+                                const float w = expf(sv[c] - mx);
+                                sum += w;
+                                const float E = -logf(uniform_from_bits(words[e]));
+                                if (w * bE > bw * E) { bw = w; bE = E; bidx = v0 + c; s_at = sv[c]; }
+                            }
                         }
                     }
                 }
             }
         }
+        // the winner's Gumbel score s - log(E), for merging across threads and CTAs
+        if (!p.greedy && bidx != INT_MAX) best = s_at - logf(bE);
     }
 
     // ---------------------------------------------------------------- per-CTA partials
     __syncthreads();
-    TcPartial* scratch = reinterpret_cast<TcPartial*>(sU);  // U tile no longer needed
+    TcPartial* scratch = reinterpret_cast<TcPartial*>(sB);  // W2 stages are drained
     if (warp >= 6) {
         const int m = (warp & 3) * 32 + lane;
-        scratch[m].score = best; scratch[m].idx = bidx; scratch[m].s_at = s_at;
-        scratch[m].m = mx; scratch[m].sum = sum;
+        const int qtr = (warp - 2) >> 2;  // 1..3
+        TcPartial& o = scratch[(qtr - 1) * kM + m];
+        o.score = best; o.idx = bidx; o.s_at = s_at; o.m = mx; o.sum = sum;
     }
     __syncthreads();
     if (warp == 1) {
@@ -338,8 +358,11 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_con
         const int m = (warp & 3) * 32 + lane;
         const int rr = row0 + m;
         if (rr < p.R) {
-            const TcPartial o = scratch[m];
-            merge_partial(best, bidx, s_at, mx, sum, o.score, o.idx, o.s_at, o.m, o.sum);
+#pragma unroll
+            for (int q = 0; q < 3; ++q) {
+                const TcPartial o = scratch[q * kM + m];
+                merge_partial(best, bidx, s_at, mx, sum, o.score, o.idx, o.s_at, o.m, o.sum);
+            }
             TcPartial w;
             w.score = best; w.idx = bidx; w.s_at = s_at; w.m = mx; w.sum = sum;
             w.pad[0] = w.pad[1] = w.pad[2] = 0.0f;
@@ -446,10 +469,12 @@ int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream) {
         return DSPARK_ERR_CUDA;
 
     const int nkb = a.rank / kKB;
-    const size_t fixed = 1024 + (size_t)nkb * kTileBytes + kUBytes + sizeof(Bars);
+    const size_t fixed = 1024 + (size_t)nkb * kTileBytes + sizeof(Bars);
     if ((size_t)max_smem < fixed + 2 * kTileBytes) return DSPARK_ERR_UNSUPPORTED;
     const int n_stages = (int)std::min<size_t>(kMaxStages, ((size_t)max_smem - fixed) / kTileBytes);
     const size_t smem = fixed + (size_t)n_stages * kTileBytes;
+    // the end-of-launch partial exchange reuses the drained stages
+    if ((size_t)n_stages * kTileBytes < 3 * kM * sizeof(TcPartial)) return DSPARK_ERR_UNSUPPORTED;
 
     CUtensorMap tm_w2, tm_u;
     {
@@ -475,6 +500,7 @@ int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream) {
 
     const TcLayout L = tc_layout(a.R);
     TcParams p;
+    p.U = static_cast<const uint16_t*>(a.U);
     p.W1 = static_cast<const uint16_t*>(a.W1);
     p.anchor = a.anchor;
     p.seeds = a.seeds;

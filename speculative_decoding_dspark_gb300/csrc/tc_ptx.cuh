@@ -170,6 +170,36 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, float (&v)[N]
     v[OFF + 30] = __uint_as_float(r30); v[OFF + 31] = __uint_as_float(r31);
 }
 
+// 32 lanes x 16 consecutive 32-bit columns into v[OFF .. OFF+15].
+template <int OFF, int N>
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, float (&v)[N]) {
+    static_assert(OFF + 16 <= N, "destination too small");
+    uint32_t r0, r1, r2, r3, r4, r5, r6, r7, r8, r9, r10, r11, r12, r13, r14, r15;
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3), "=r"(r4), "=r"(r5), "=r"(r6), "=r"(r7), "=r"(r8),
+          "=r"(r9), "=r"(r10), "=r"(r11), "=r"(r12), "=r"(r13), "=r"(r14), "=r"(r15)
+        : "r"(taddr)
+        : "memory");
+    v[OFF + 0] = __uint_as_float(r0); v[OFF + 1] = __uint_as_float(r1);
+    v[OFF + 2] = __uint_as_float(r2); v[OFF + 3] = __uint_as_float(r3);
+    v[OFF + 4] = __uint_as_float(r4); v[OFF + 5] = __uint_as_float(r5);
+    v[OFF + 6] = __uint_as_float(r6); v[OFF + 7] = __uint_as_float(r7);
+    v[OFF + 8] = __uint_as_float(r8); v[OFF + 9] = __uint_as_float(r9);
+    v[OFF + 10] = __uint_as_float(r10); v[OFF + 11] = __uint_as_float(r11);
+    v[OFF + 12] = __uint_as_float(r12); v[OFF + 13] = __uint_as_float(r13);
+    v[OFF + 14] = __uint_as_float(r14); v[OFF + 15] = __uint_as_float(r15);
+}
+
+// Prefetch one TMA box of a 3-D tensor into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
