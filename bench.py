@@ -63,7 +63,7 @@ def dist_env():
 def workload_config(w):
     return {"workload": w["name"], "R": w["R"], "V": w["V"], "gamma": w["gamma"],
             "rank": w["rank"], "temperature": float(w["temperature"]),
-            "l2": "inputs larger than L2 (no flush): W2/U/target/q_logits stream > 1 GB per step"}
+            "l2": "inputs larger than L2 (no flush): W2, U and target logits stream ~2 GB per step"}
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -224,7 +224,9 @@ def run_ours(args):
     y = torch.empty((R, gamma), **i32)
     q_lse = torch.empty((R, gamma), device="cuda")
     q_tok = torch.empty((R, gamma), device="cuda")
-    q_logits = torch.empty((R, gamma, V), device="cuda") if T > 0 else None
+    # the verify recomputes the drafter's rejected rows from its factors, so the
+    # draft keeps no logits in memory
+    q_logits = None
     a = torch.empty((R, gamma), device="cuda")
     l = torch.empty(R, **i32)
     cu = torch.empty(R + 1, **i32)
@@ -238,7 +240,7 @@ def run_ours(args):
     tot = torch.empty(1, **i32)
     status = torch.zeros(1, **i32)
     ws_d = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_DRAFT, R, gamma, V, rank_r, 0, B.DSPARK_BF16))
-    ws_v = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_VERIFY, R, gamma, V, 0, max_rows))
+    ws_v = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_VERIFY_MARKOV, R, gamma, V, rank_r, max_rows))
     stream = torch.cuda.current_stream()
     uses_tc = B.dspark_markov_draft_uses_tensor_cores(B.DSPARK_BF16, B.DSPARK_BF16, R, V, rank_r)
 
@@ -259,17 +261,18 @@ def run_ours(args):
                                   status)
         if ev is not None: ev[2].record(stream)
         if run_verify:
-            B.dspark_verify(target, cu, y, q_logits, q_lse, q_tok, seeds, cycle, T, max_rows, n_acc,
-                            out, p_tok, ws_v, status)
+            B.dspark_verify_markov(target, cu, y, U, W1, W2, anchor, q_lse, q_tok, seeds, cycle, T,
+                                   max_rows, n_acc, out, p_tok, ws_v, status)
         if ev is not None: ev[3].record(stream)
         if run_commit:
             B.dspark_commit_lengths(n_acc, l, gamma, cl, cuc, disc, tot, status)
         if ev is not None: ev[4].record(stream)
 
     # launches of this library per step
-    draft_launches = gamma if uses_tc else 1 + 2 * gamma
+    draft_launches = 1 + gamma if uses_tc else 1 + 2 * gamma  # + the anchor-row gather
+    verify_launches = 4 if T > 0 else 2  # prologue, stats, (residual rows, residual draw)
     launches_per_step = (int(run_select) + draft_launches * int(run_draft) +
-                         (3 if T > 0 else 2) * int(run_verify) + int(run_commit))
+                         verify_launches * int(run_verify) + int(run_commit))
 
     for i in range(args.warmup):
         step(i)
@@ -312,7 +315,7 @@ def run_ours(args):
     peak_src = "measured" if hbm else "fallback"
     hbm = hbm or 6800.0
     achieved = step_bytes / (draft_step_ms / 1000.0) / 1e9
-    kname = "draft_step_tc" if uses_tc else "draft_bias_simt+draft_sample"
+    kname = "markov_tc_kernel<draft>" if uses_tc else "draft_bias_simt+draft_sample"
     digest = source_digest(["speculative_decoding_dspark_gb300/csrc/draft_tc.cu" if uses_tc else
                             "speculative_decoding_dspark_gb300/csrc/draft_simt.cu",
                             "speculative_decoding_dspark_gb300/csrc/common.cuh"])

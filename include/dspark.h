@@ -76,6 +76,7 @@ typedef struct CUstream_st* dspark_stream_t;
 #define DSPARK_OP_DRAFT 0
 #define DSPARK_OP_VERIFY 1
 #define DSPARK_OP_SELECT 2
+#define DSPARK_OP_VERIFY_MARKOV 3
 
 /* ---- dspark_markov_draft flags ---------------------------------------------- */
 #define DSPARK_DRAFT_FORCE_SIMT 1u   /* use the CUDA-core kernels even where the
@@ -188,6 +189,31 @@ int dspark_verify(const float* target_logits, const int32_t* cu_seqlens,
                   float temperature, int R, int gamma, int V, int max_rows,
                   int32_t* n_accepted, int32_t* out_tokens, float* p_tok, void* ws,
                   size_t ws_bytes, int32_t* dev_status, dspark_stream_t stream);
+
+/*
+ * dspark_verify_markov -- dspark_verify for a Markov-head drafter, without the
+ * drafter's logits in memory (explainer sections 2-3 and 7).
+ *
+ * Same decisions and outputs as dspark_verify.  Instead of q_logits it takes
+ * the drafter's own inputs -- U [R, gamma, V], W1 and W2 [V, rank] (bf16, the
+ * shapes dspark_markov_draft_uses_tensor_cores accepts) and anchor [R] -- and
+ * recomputes, on the tensor cores, the drafter's scaled logits
+ * s_v = (U[r][j][v] + W2[v] . W1[prev_j]) * invT of the one row j each request
+ * needs for its residual; q = exp(s - q_lse[r][j]).  One pass over W2 per
+ * verify replaces writing and re-reading R * gamma * V fp32 logits.  The
+ * draft call then passes q_logits = NULL.
+ *   ws, ws_bytes  dspark_workspace_size(DSPARK_OP_VERIFY_MARKOV, R, gamma, V, rank,
+ *                 max_rows, DSPARK_BF16, 0)
+ * Returns DSPARK_ERR_UNSUPPORTED for factor types or shapes the tensor-core
+ * kernel does not take (use dspark_verify with q_logits there).
+ */
+int dspark_verify_markov(const float* target_logits, const int32_t* cu_seqlens,
+                         const int32_t* draft_tokens, const void* U, const void* W1,
+                         const void* W2, const int32_t* anchor, int rank, const float* q_lse,
+                         const float* q_tok, const uint64_t* seeds, uint32_t cycle,
+                         float temperature, int R, int gamma, int V, int max_rows,
+                         int32_t* n_accepted, int32_t* out_tokens, float* p_tok, void* ws,
+                         size_t ws_bytes, int32_t* dev_status, dspark_stream_t stream);
 
 /*
  * dspark_verify_static_scratch -- dspark_verify for callers that cannot

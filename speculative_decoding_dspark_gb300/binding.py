@@ -27,13 +27,14 @@ DSPARK_ERR_DEVICE_INPUT = -6
 DSPARK_ERR_WORKSPACE = -7
 
 DSPARK_F32, DSPARK_BF16 = 0, 1
-DSPARK_OP_DRAFT, DSPARK_OP_VERIFY, DSPARK_OP_SELECT = 0, 1, 2
+DSPARK_OP_DRAFT, DSPARK_OP_VERIFY, DSPARK_OP_SELECT, DSPARK_OP_VERIFY_MARKOV = 0, 1, 2, 3
 DSPARK_DRAFT_FORCE_SIMT = 1
 DSPARK_SELECT_FIXED, DSPARK_SELECT_HISTORY, DSPARK_SELECT_CURRENT, DSPARK_SELECT_FIRST_STOP = 0, 1, 2, 3
 
 EXPORTED = ["dspark_status_string", "dspark_version", "dspark_workspace_size", "dspark_philox4x32_10",
             "dspark_markov_draft_uses_tensor_cores", "dspark_markov_draft", "dspark_verify",
-            "dspark_select_prefix", "dspark_commit_lengths", "dspark_verify_static_scratch"]
+            "dspark_select_prefix", "dspark_commit_lengths", "dspark_verify_static_scratch",
+            "dspark_verify_markov"]
 
 
 class DSparkError(RuntimeError):
@@ -64,6 +65,9 @@ def _load():
     L.dspark_select_prefix.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp,
                                        vp, sz, vp, vp]
     L.dspark_select_prefix.restype = i32
+    L.dspark_verify_markov.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, u32, f32, i32, i32,
+                                       i32, i32, vp, vp, vp, vp, sz, vp, vp]
+    L.dspark_verify_markov.restype = i32
     L.dspark_verify_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, vp, u32, f32, i32, i32, i32,
                                                i32, vp, vp, vp, vp, vp]
     L.dspark_verify_static_scratch.restype = i32
@@ -191,6 +195,37 @@ def dspark_verify(target_logits, cu_seqlens, draft_tokens, q_logits, q_lse, q_to
                           gamma, V, int(max_rows), _ptr(n_accepted), _ptr(out_tokens), _ptr(p_tok),
                           _ptr(ws), ws.numel(), _ptr(dev_status), _stream(stream))
     _raise("dspark_verify", st)
+
+
+def dspark_verify_markov(target_logits, cu_seqlens, draft_tokens, U, W1, W2, anchor, q_lse, q_tok, seeds,
+                         cycle, temperature, max_rows, n_accepted, out_tokens, p_tok=None, ws=None,
+                         dev_status=None, stream=None):
+    R, gamma = draft_tokens.shape
+    V = target_logits.shape[1]
+    rank = W1.shape[1]
+    _check(target_logits, "target_logits", torch.float32)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, (R + 1,))
+    _check(draft_tokens, "draft_tokens", torch.int32)
+    _check(U, "U", torch.bfloat16, (R, gamma, V))
+    _check(W1, "W1", torch.bfloat16, (V, rank))
+    _check(W2, "W2", torch.bfloat16, (V, rank))
+    _check(anchor, "anchor", torch.int32, (R,))
+    _check(q_lse, "q_lse", torch.float32, (R, gamma), allow_none=True)
+    _check(q_tok, "q_tok", torch.float32, (R, gamma), allow_none=True)
+    _check(seeds, "seeds", torch.int64, (R,), allow_none=True)
+    _check(n_accepted, "n_accepted", torch.int32, (R,))
+    _check(out_tokens, "out_tokens", torch.int32, (R, gamma + 1))
+    _check(p_tok, "p_tok", torch.float32, (R, gamma), allow_none=True)
+    _check(ws, "ws", torch.uint8)
+    _check(dev_status, "dev_status", torch.int32, allow_none=True)
+    if target_logits.shape[0] < max_rows:
+        raise ValueError("target_logits has fewer rows than max_rows")
+    st = _L.dspark_verify_markov(_ptr(target_logits), _ptr(cu_seqlens), _ptr(draft_tokens), _ptr(U), _ptr(W1),
+                                 _ptr(W2), _ptr(anchor), rank, _ptr(q_lse), _ptr(q_tok), _ptr(seeds),
+                                 int(cycle), float(temperature), R, gamma, V, int(max_rows),
+                                 _ptr(n_accepted), _ptr(out_tokens), _ptr(p_tok), _ptr(ws), ws.numel(),
+                                 _ptr(dev_status), _stream(stream))
+    _raise("dspark_verify_markov", st)
 
 
 def dspark_verify_static_scratch(target_logits, cu_seqlens, draft_tokens, q_logits, q_lse, q_tok,

@@ -101,6 +101,9 @@ size_t dspark_workspace_size(int op, int R, int gamma, int V, int rank, int max_
         case DSPARK_OP_VERIFY:
             if (V <= 0 || max_rows < 0) return 0;
             return verify_layout(R, V, max_rows).total;
+        case DSPARK_OP_VERIFY_MARKOV:
+            if (V <= 0 || max_rows < 0 || rank <= 0) return 0;
+            return align_up(verify_layout(R, V, max_rows).total) + residual_tc_workspace(R, rank);
         case DSPARK_OP_SELECT:
             return 0;
         default:
@@ -187,6 +190,57 @@ int dspark_verify(const float* target_logits, const int32_t* cu_seqlens,
     p.jobs = carve<VerifyJob>(ws, L.jobs);
     p.parts = carve<SamplePartial>(ws, L.parts);
     return cuda_status(launch_verify(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dspark_verify_markov(const float* target_logits, const int32_t* cu_seqlens,
+                         const int32_t* draft_tokens, const void* U, const void* W1,
+                         const void* W2, const int32_t* anchor, int rank, const float* q_lse,
+                         const float* q_tok, const uint64_t* seeds, uint32_t cycle,
+                         float temperature, int R, int gamma, int V, int max_rows,
+                         int32_t* n_accepted, int32_t* out_tokens, float* p_tok, void* ws,
+                         size_t ws_bytes, int32_t* dev_status, dspark_stream_t stream) {
+    if (!target_logits || !cu_seqlens || !draft_tokens || !n_accepted || !out_tokens)
+        return DSPARK_ERR_INVALID_ARG;
+    if (R <= 0 || V <= 0 || gamma <= 0 || gamma > 16 || rank <= 0) return DSPARK_ERR_INVALID_ARG;
+    if (max_rows < R || (long long)max_rows > (long long)R * (gamma + 1)) return DSPARK_ERR_INVALID_ARG;
+    if (!(temperature >= 0.0f) || temperature == INFINITY) return DSPARK_ERR_INVALID_ARG;
+    if (cycle >= (1u << 28)) return DSPARK_ERR_INVALID_ARG;
+    const bool greedy = temperature == 0.0f;
+    if (!greedy && (!U || !W1 || !W2 || !anchor || !q_lse || !q_tok || !seeds)) return DSPARK_ERR_INVALID_ARG;
+    if (!draft_tc_supported(DSPARK_BF16, DSPARK_BF16, R, V, rank)) return DSPARK_ERR_UNSUPPORTED;
+    if (!greedy && (!aligned16(U) || !aligned16(W1) || !aligned16(W2))) return DSPARK_ERR_UNSUPPORTED;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return DSPARK_ERR_WORKSPACE;
+    const VerifyLayout L = verify_layout(R, V, max_rows);
+    const size_t res_off = align_up(L.total);
+    if (ws_bytes < res_off + residual_tc_workspace(R, rank)) return DSPARK_ERR_WORKSPACE;
+    const int nchunk = (V + kVerifyChunk - 1) / kVerifyChunk;
+    if ((long long)max_rows * nchunk >= (1LL << 31)) return DSPARK_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    VerifyParams p;
+    p.target = target_logits; p.cu = cu_seqlens; p.y = draft_tokens; p.q_logits = nullptr;
+    p.q_lse = q_lse; p.q_tok = q_tok; p.seeds = seeds; p.cycle = cycle;
+    p.invT = greedy ? 1.0f : 1.0f / temperature; p.greedy = greedy;
+    p.R = R; p.gamma = gamma; p.V = V; p.max_rows = max_rows; p.nchunk = nchunk;
+    p.n_acc = n_accepted; p.out_tokens = out_tokens; p.p_tok = p_tok; p.dev_status = dev_status;
+    p.ok = carve<int>(ws, L.ok);
+    p.valid = carve<int>(ws, L.valid);
+    p.cnt1 = carve<int>(ws, L.cnt1);
+    p.cnt2 = carve<int>(ws, L.cnt2);
+    p.stats = carve<RowStat>(ws, L.stats);
+    p.jobs = carve<VerifyJob>(ws, L.jobs);
+    p.parts = carve<SamplePartial>(ws, L.parts);
+    const cudaError_t e = launch_verify_decide(p, s);
+    if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+    if (greedy) return DSPARK_OK;  // the decision pass already wrote the argmax token
+
+    ResidualTcArgs a;
+    a.U = U; a.W1 = W1; a.W2 = W2; a.anchor = anchor; a.y = draft_tokens; a.seeds = seeds;
+    a.cycle = cycle; a.invT = p.invT; a.R = R; a.gamma = gamma; a.V = V; a.rank = rank;
+    a.target = target_logits; a.q_lse = q_lse; a.jobs = p.jobs; a.valid = p.valid;
+    a.out_tokens = out_tokens; a.dev_status = dev_status;
+    a.ws = static_cast<unsigned char*>(ws) + res_off;
+    return launch_residual_tc(a, s);
 }
 
 int dspark_select_prefix(const float* c, const float* c_hist, const int32_t* capture_sizes,

@@ -1,7 +1,8 @@
-// draft_tc.cuh -- the tensor-core (tcgen05) Markov draft: interface.
+// draft_tc.cuh -- the tensor-core (tcgen05) Markov-head kernels: interface.
 #pragma once
 
 #include "common.cuh"
+#include "kernels.cuh"
 
 namespace dspark {
 
@@ -23,8 +24,32 @@ struct DraftTcArgs {
     void* ws;
 };
 
+// The extra token of every request after the verify decisions, with the
+// drafter's logits of the rejected row recomputed from its Markov factors.
+struct ResidualTcArgs {
+    const void* U;
+    const void* W1;
+    const void* W2;
+    const int32_t* anchor;
+    const int32_t* y;          // draft tokens [R, gamma]
+    const uint64_t* seeds;
+    uint32_t cycle;
+    float invT;
+    int R, gamma, V, rank;
+    const float* target;       // packed target rows
+    const float* q_lse;        // the drafter's log-normalisers [R, gamma]
+    const VerifyJob* jobs;     // per request: row, position and kind of the extra token
+    const int* valid;          // per request: inputs usable
+    int32_t* out_tokens;       // [R, gamma + 1]
+    int32_t* dev_status;
+    void* ws;
+};
+
 bool draft_tc_supported(int u_dtype, int w_dtype, int R, int V, int rank);
 size_t draft_tc_workspace(int R, int V, int rank);
 int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream);
+
+size_t residual_tc_workspace(int R, int rank);
+int launch_residual_tc(const ResidualTcArgs& a, cudaStream_t stream);
 
 }  // namespace dspark

@@ -56,6 +56,8 @@ struct VerifyParams {
 };
 
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream);
+// prologue + stats/decision passes only (the extra token is left to the caller)
+cudaError_t launch_verify_decide(const VerifyParams& p, cudaStream_t stream);
 
 // ----------------------------------------------------------------------------
 // Draft (CUDA-core path)

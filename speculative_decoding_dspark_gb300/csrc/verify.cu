@@ -336,13 +336,19 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_correct_kernel(VerifyPa
 
 }  // namespace
 
-cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream) {
+cudaError_t launch_verify_decide(const VerifyParams& p, cudaStream_t stream) {
     verify_prologue_kernel<<<1, 1024, 0, stream>>>(p);
     const long long grid1 = (long long)p.max_rows * p.nchunk;
     if (grid1 > 0) {
         if (p.greedy) verify_stats_kernel<true><<<(unsigned)grid1, kVerifyThreads, 0, stream>>>(p);
         else verify_stats_kernel<false><<<(unsigned)grid1, kVerifyThreads, 0, stream>>>(p);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream) {
+    const cudaError_t e = launch_verify_decide(p, stream);
+    if (e != cudaSuccess) return e;
     if (!p.greedy) {
         const long long grid2 = (long long)p.R * p.nchunk;
         verify_correct_kernel<<<(unsigned)grid2, kVerifyThreads, 0, stream>>>(p);

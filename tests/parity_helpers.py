@@ -76,6 +76,30 @@ def gpu_verify(target, cu, y, q_logits, q_lse, q_tok, seeds, cycle, temperature,
     return dict(n_acc=host(n_acc), out_tokens=host(out), p_tok=host(p_tok), status=int(status.item()))
 
 
+def gpu_verify_markov(target, cu, d, g, cycle, temperature, max_rows=None):
+    """dspark_verify_markov on the GPU draft g of inputs d (drafter logits recomputed)."""
+    t = lambda a: a if isinstance(a, torch.Tensor) else dev(a)
+    target_d, cu_d = t(target), t(cu)
+    y_d = g["y_dev"]
+    R, gamma = y_d.shape
+    V = target_d.shape[1]
+    W1 = dev(d["W1"])
+    rank = W1.shape[1]
+    max_rows = int(target_d.shape[0]) if max_rows is None else max_rows
+    n_acc = torch.full((R,), -7, dtype=torch.int32, device="cuda")
+    out = torch.full((R, gamma + 1), -7, dtype=torch.int32, device="cuda")
+    p_tok = torch.full((R, gamma), float("nan"), device="cuda")
+    ws = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_VERIFY_MARKOV, R, gamma, V, rank, max_rows))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    samp = temperature > 0
+    B.dspark_verify_markov(target_d, cu_d, y_d, dev(d["U"]), W1, dev(d["W2"]), dev(d["anchor"]),
+                           g["q_lse_dev"] if samp else None, g["q_tok_dev"] if samp else None,
+                           dev(d["seeds"]) if samp else None, cycle, temperature, max_rows, n_acc, out,
+                           p_tok, ws, status)
+    torch.cuda.synchronize()
+    return dict(n_acc=host(n_acc), out_tokens=host(out), p_tok=host(p_tok), status=int(status.item()))
+
+
 def gpu_select(c, c_hist, sizes, sps, K_cap, mode):
     R, gamma = c.shape
     a = torch.full((R, gamma), float("nan"), device="cuda")

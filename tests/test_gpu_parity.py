@@ -138,6 +138,41 @@ def test_verify_parity_small(B, orc, name, over, T):
     tally.check()
 
 
+MARKOV_CASES = [
+    ("batched_sampling", dict(R=7, V=20000, gamma=5, rank=64, w_sigma=0.3), 0.7),
+    ("varlen_verify", dict(R=24, V=10008, gamma=5, rank=64, w_sigma=0.3), 1.0),
+    ("batched_sampling", dict(R=130, V=4096, gamma=3, rank=128, w_sigma=0.3), 1.0),
+    ("qwen3_8b_greedy", dict(R=9, V=16392, gamma=7, rank=64, w_sigma=0.3), 0.0),
+]
+
+
+@pytest.mark.parametrize("name,over,T", MARKOV_CASES)
+def test_verify_markov_parity(B, orc, name, over, T):
+    """Verify with the drafter's logits recomputed on the tensor cores: against
+    the oracle, and identical to dspark_verify fed the stored logits."""
+    w, d = H.cycle_inputs(name, **over)
+    full = inputs.target_full(w, d["U"])
+    l = inputs.verify_lengths(w)
+    cu = inputs.cu_from_lengths(l)
+    target = inputs.pack_rows(full, l)
+    tD, cuD = H.dev(target), H.dev(cu)
+    tally = H.Tally()
+    for cycle in range(4):
+        g = H.gpu_draft(d, T, cycle)
+        gm = H.gpu_verify_markov(tD, cuD, d, g, cycle, T)
+        gv = H.gpu_verify(tD, cuD, g["y_dev"], g["q_logits_dev"] if T > 0 else None,
+                          g["q_lse_dev"] if T > 0 else None, g["q_tok_dev"] if T > 0 else None,
+                          H.dev(d["seeds"]) if T > 0 else None, cycle, T)
+        assert gm["status"] == 0 and gv["status"] == 0
+        np.testing.assert_array_equal(gm["n_acc"], gv["n_acc"])
+        np.testing.assert_array_equal(gm["out_tokens"], gv["out_tokens"])
+        o = orc.markov_draft(d["U"], d["W1"], d["W2"], d["anchor"], d["seeds"], cycle, T)
+        ov = orc.verify(target, cu, o["y"], o["q_logits"], d["seeds"], cycle, T)
+        clean = H.compare_draft(tally, g, o, T)
+        H.compare_verify(tally, gm, ov, l, only=clean)
+    tally.check()
+
+
 def test_verify_tiny_many_cycles(B, orc):
     """The V=64 workload, 2000 full cycles draft -> verify on the GPU vs the oracle."""
     w, d = H.cycle_inputs("tiny_exhaustive")
@@ -281,6 +316,11 @@ def test_full_size_cycle_sampled(B, orc, name, cycles, sample):
                         o["q_logits"], sub["seeds"], cycle, T, req_ids=rows)
         clean = H.compare_draft(tally, g, o, T, rows=rows)
         H.compare_verify(tally, gv, ov, lsub, rows=rows, only=clean)
+        # the same verify with the drafter's rejected rows recomputed from its factors
+        gm = H.gpu_verify_markov(H.dev(target), H.dev(cu), d, g, cycle, T)
+        assert gm["status"] == 0
+        np.testing.assert_array_equal(gm["n_acc"], gv["n_acc"])
+        np.testing.assert_array_equal(gm["out_tokens"], gv["out_tokens"])
         # properties that hold for every request of the batch
         assert ((gv["n_acc"] >= 0) & (gv["n_acc"] <= l)).all()
         for r in range(R):
