@@ -47,9 +47,11 @@ __device__ __forceinline__ PhiloxKey philox_key(uint64_t seed) {
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKey& K) {
 #pragma unroll
     for (int i = 0; i < 10; ++i) {
-        const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
-        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
-        c = make_uint4(hi1 ^ c.y ^ K.k0[i], lo1, hi0 ^ c.w ^ K.k1[i], lo0);
+        // one 32x32 -> 64-bit product each gives both halves
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
+        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ K.k0[i], (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ K.k1[i],
+                       (uint32_t)p0);
     }
     return c;
 }

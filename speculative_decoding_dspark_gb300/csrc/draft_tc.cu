@@ -62,6 +62,8 @@ constexpr int kGroup = 16;                    // CTAs per first-level reduction 
 constexpr int kMaxGroups = kMaxP / kGroup;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr float kLog2eF = 1.4426950408889634f;
+constexpr float kLn2F = 0.6931471805599453f;
 
 // Per-request partial.  Draft: (score, idx) of the Gumbel-max draw, s at it,
 // (max, sum of exp) of the logits.  Residual: (score, idx) over the residual,
@@ -169,6 +171,13 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x
                      reinterpret_cast<uint64_t>(map)),
                  "r"(x), "r"(y)
                  : "memory");
+}
+
+// Programmatic dependent launch: wait for the grids this one depends on to
+// complete (and their writes to be visible); allow dependents to start.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_l2(const void* p) {
@@ -303,13 +312,21 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
             int last_phase[kMaxStages];
             for (int i = 0; i < kMaxStages; ++i) last_phase[i] = -1;
             bool ok = true;
+            // The first tiles do not depend on the previous launch: pull them into
+            // L2 while that launch may still be finishing (programmatic launch).
+            for (int i = 0; i < 2 && i < n_local; ++i) {
+                const int t = cidx + i * p.P;
+                for (int q = 0; q < p.nkb; ++q) tma_prefetch_l2_2d(&tm_w2, q * kKB, t * kNV);
+                if (!kRes) {
+                    tc::tma_prefetch_l2_3d(&tm_u, t * kNV, p.k, row0);
+                    tc::tma_prefetch_l2_3d(&tm_u, t * kNV + kKB, p.k, row0);
+                }
+            }
+            // H (and everything else the previous launch wrote) is ready after this
+            griddep_wait();
             // A: the block's H rows, resident for the launch
             tc::mbar_arrive_expect_tx(&bar.afull, (uint32_t)(p.nkb * kTileBytes));
             for (int kb = 0; kb < p.nkb; ++kb) tc::tma_load_2d(sA + kb * kTileBytes, &tm_h, &bar.afull, kb * kKB, row0);
-            if (!kRes && n_local > 0) {
-                tc::tma_prefetch_l2_3d(&tm_u, cidx * kNV, p.k, row0);
-                tc::tma_prefetch_l2_3d(&tm_u, cidx * kNV + kKB, p.k, row0);
-            }
             for (int i = 0; ok && i < n_local; ++i) {
                 const int t = cidx + i * p.P;
                 for (int kb = 0; kb < p.nkb; ++kb) {
@@ -400,6 +417,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         float* qrow = (!kRes && p.q_logits && row_ok) ? p.q_logits + rk * p.V : nullptr;
         // exponential-race state: draft (bw, bE); residual (br, bEr) and (bp, bEp)
         float bw = 0.0f, bE = 1.0f, bp = 0.0f, bEp = 1.0f;
+        float rho2 = INFINITY;  // draft: E_best * log2(e) / w_best
         int ia = INT_MAX;
         for (int i = 0; i < n_local; ++i) {
             const int t = cidx + i * p.P;
@@ -474,24 +492,56 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                         }
                     continue;
                 }
-                float tv[16];
-                if (kRes) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float4 f = 4 * j < nvalid ? __ldg(reinterpret_cast<const float4*>(trow + v0) + j)
-                                                        : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                        tv[4 * j + 0] = f.x; tv[4 * j + 1] = f.y; tv[4 * j + 2] = f.z; tv[4 * j + 3] = f.w;
-                    }
-                } else {
+                if (!kRes) {
+                    // Sampling draft, base-2 units: s2 = s * log2(e), w = 2^(s2 - m2).
+                    // An entry can only replace the best when w * E_best > w_best * E,
+                    // i.e. u > exp(-w * E_best / w_best); that bound is tested first
+                    // (with a 2^-14 relative margin against the rounding of its
+                    // approximations) and the accurate log and exact comparison run
+                    // only for entries that pass it.
                     float cm = -INFINITY;
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) if (c < nvalid) cm = fmaxf(cm, sv[c]);
+                    for (int c = 0; c < 16; ++c) {
+                        sv[c] *= kLog2eF;
+                        if (c < nvalid) cm = fmaxf(cm, sv[c]);
+                    }
                     if (cm > part.m) {
-                        const float sc = expf(part.m - cm);  // 0 while the max is -inf
+                        const float sc = exp2f(part.m - cm);  // 0 while the max is -inf
                         part.sum *= sc;
                         bw *= sc;
                         part.m = cm;
+                        rho2 = bE * kLog2eF / bw;
                     }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 wd = philox4x32_10(
+                            make_uint4((uint32_t)((v0 >> 2) + q), (uint32_t)pos, (uint32_t)rr, w3), K);
+                        const uint32_t words[4] = {wd.x, wd.y, wd.z, wd.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int c = 4 * q + e;
+                            if (c < nvalid) {
+                                const float w = exp2f(sv[c] - part.m);
+                                part.sum += w;
+                                const float u = uniform_from_bits(words[e]);
+                                if (u > exp2f(-w * rho2) * (1.0f - 0x1p-14f)) {
+                                    const float E = -logf(u);
+                                    if (w * bE > bw * E) {
+                                        bw = w; bE = E; part.idx = v0 + c; part.s_at = sv[c];
+                                        rho2 = bE * kLog2eF / bw;
+                                    }
+                                }
+                            }
+                        }
+                    }
+                    continue;
+                }
+                float tv[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float4 f = 4 * j < nvalid ? __ldg(reinterpret_cast<const float4*>(trow + v0) + j)
+                                                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    tv[4 * j + 0] = f.x; tv[4 * j + 1] = f.y; tv[4 * j + 2] = f.z; tv[4 * j + 3] = f.w;
                 }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -503,20 +553,14 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                         const int c = 4 * q + e;
                         if (c < nvalid) {
                             const float E = -logf(uniform_from_bits(words[e]));
-                            if (kRes) {
-                                const float pv = expf(tv[c] * p.invT - rinfo.lse_p);
-                                if (pv * bEp > bp * E) { bp = pv; bEp = E; ia = v0 + c; }
-                                if (with_u) {
-                                    const float res = pv - expf(sv[c] - rinfo.q_lse);
-                                    if (res > 0.0f) {
-                                        part.sum += res;
-                                        if (res * bE > bw * E) { bw = res; bE = E; part.idx = v0 + c; }
-                                    }
+                            const float pv = expf(tv[c] * p.invT - rinfo.lse_p);
+                            if (pv * bEp > bp * E) { bp = pv; bEp = E; ia = v0 + c; }
+                            if (with_u) {
+                                const float res = pv - expf(sv[c] - rinfo.q_lse);
+                                if (res > 0.0f) {
+                                    part.sum += res;
+                                    if (res * bE > bw * E) { bw = res; bE = E; part.idx = v0 + c; }
                                 }
-                            } else {
-                                const float w = expf(sv[c] - part.m);
-                                part.sum += w;
-                                if (w * bE > bw * E) { bw = w; bE = E; part.idx = v0 + c; part.s_at = sv[c]; }
                             }
                         }
                     }
@@ -528,12 +572,19 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
             part.score = part.idx != INT_MAX ? logf(bw) - logf(bE) : -INFINITY;
             part.s_at = ia != INT_MAX ? logf(bp) - logf(bEp) : -INFINITY;
             part.m = __int_as_float(ia);
-        } else if (!p.greedy && part.idx != INT_MAX) {
-            part.score = part.s_at - logf(bE);
+        } else if (!p.greedy) {
+            // back to natural units: the max and the winner's logit
+            part.m *= kLn2F;
+            part.s_at *= kLn2F;
+            if (part.idx != INT_MAX) part.score = part.s_at - logf(bE);
         }
     }
 
     // ---------------------------------------------------------------- per-CTA partials
+    // The next launch may start on SMs this grid leaves; the workspace below is
+    // shared with the previous launch, so wait for it to have finished.
+    griddep_launch_dependents();
+    griddep_wait();
     __syncthreads();
     TcPartial* scratch = reinterpret_cast<TcPartial*>(sB);  // W2 stages are drained
     if (warp >= 6) {
@@ -800,9 +851,23 @@ int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream) {
         const int blocks = (int)std::min<long long>((chunks + 255) / 256, 4LL * n_sm);
         gather_anchor_rows_kernel<<<blocks, 256, 0, stream>>>(p.W1, a.anchor, a.R, a.V, a.rank, p.H);
     }
+    // Each step may start while the previous one finishes its reduction: the
+    // kernel prefetches its first tiles and waits (griddepcontrol) before it
+    // reads anything the previous launch wrote.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     for (int k = 0; k < a.gamma; ++k) {
         p.k = k;
-        markov_tc_kernel<false><<<grid, kThreads, smem, stream>>>(tm_w2, tm_u, tm_h, p);
+        if (cudaLaunchKernelEx(&cfg, markov_tc_kernel<false>, tm_w2, tm_u, tm_h, p) != cudaSuccess)
+            return DSPARK_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }

@@ -97,8 +97,11 @@ struct SelectSmem {
 
 // Fill keys from confidences (computing the survival products), sort, scan.
 // Returns false if a confidence is outside [0, 1].  Leaves the sorted ids in
-// buffer 0 and prefix sums in sm.prefix.
-__device__ bool survival_sort_scan(SelectSmem& sm, const float* c, float* a_out, int R, int gamma) {
+// buffer 0 and prefix sums in sm.prefix.  Without do_sort (the selection takes
+// every candidate or none, so order does not matter) it stops after the
+// products.
+__device__ bool survival_sort_scan(SelectSmem& sm, const float* c, float* a_out, int R, int gamma,
+                                   bool do_sort = true) {
     const int N = R * gamma;
     if (threadIdx.x == 0) sm.flag = 0;
     __syncthreads();
@@ -116,6 +119,7 @@ __device__ bool survival_sort_scan(SelectSmem& sm, const float* c, float* a_out,
     }
     __syncthreads();
     if (sm.flag) return false;
+    if (!do_sort) return true;
 
     // stable split passes, one per bit, ones (larger) first
     int src = 0;
@@ -177,7 +181,9 @@ __global__ void __launch_bounds__(kNT) select_kernel(SelectParams p) {
     if (p.mode == DSPARK_SELECT_HISTORY) {
         good = survival_sort_scan(sm, p.c_hist, nullptr, R, gamma);
     } else {
-        good = survival_sort_scan(sm, p.c, p.a, R, gamma);
+        const int n_fixed = min(p.K_cap - R, N);
+        const bool all_or_none = p.mode == DSPARK_SELECT_FIXED && (n_fixed == 0 || n_fixed == N);
+        good = survival_sort_scan(sm, p.c, p.a, R, gamma, !all_or_none);
     }
     if (good && (p.mode == DSPARK_SELECT_HISTORY || p.mode == DSPARK_SELECT_CURRENT)) {
         if (threadIdx.x == 0) {
@@ -194,7 +200,7 @@ __global__ void __launch_bounds__(kNT) select_kernel(SelectParams p) {
         }
         __syncthreads();
         n = sm.n_sel;
-        if (p.mode == DSPARK_SELECT_HISTORY) good = survival_sort_scan(sm, p.c, p.a, R, gamma);
+        if (p.mode == DSPARK_SELECT_HISTORY) good = survival_sort_scan(sm, p.c, p.a, R, gamma, n != 0 && n != N);
     } else if (good && p.mode == DSPARK_SELECT_FIRST_STOP) {
         // Theta(n) for every n in parallel; the answer is the first n whose
         // successor is not strictly better (or infeasible).

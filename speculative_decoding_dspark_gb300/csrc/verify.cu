@@ -66,7 +66,21 @@ __global__ void __launch_bounds__(1024) verify_prologue_kernel(VerifyParams p) {
     }
 }
 
-// Block-wide combine of (m, s, argmax) held by every thread; result in thread 0.
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// (max, sum of 2^(x - max)) pairs in base-2 units, merged.
+__device__ __forceinline__ void lse2_merge(float& m, float& s, float m2, float s2) {
+    if (m2 > m) {
+        s = s * exp2f(m - m2) + s2;  // exp2f(-inf) = 0 covers an empty side
+        m = m2;
+    } else if (m2 != -INFINITY) {
+        s = s + s2 * exp2f(m2 - m);
+    }
+}
+
+// Block-wide combine of (m, s, argmax) held by every thread (m, s in base-2
+// units); result in thread 0.
 __device__ __forceinline__ void block_rowstat(float& m, float& s, float& bm, int& bi) {
     __shared__ float sm_m[32], sm_s[32], sm_bm[32];
     __shared__ int sm_bi[32];
@@ -74,7 +88,7 @@ __device__ __forceinline__ void block_rowstat(float& m, float& s, float& bm, int
     for (int o = 16; o > 0; o >>= 1) {
         const float m2 = shfl_xor(m, o), s2 = shfl_xor(s, o), bm2 = shfl_xor(bm, o);
         const int bi2 = shfl_xor(bi, o);
-        lse_merge(m, s, m2, s2);
+        lse2_merge(m, s, m2, s2);
         if (better(bm2, bi2, bm, bi)) { bm = bm2; bi = bi2; }
     }
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -90,20 +104,22 @@ __device__ __forceinline__ void block_rowstat(float& m, float& s, float& bm, int
         for (int o = 16; o > 0; o >>= 1) {
             const float m2 = shfl_xor(m, o), s2 = shfl_xor(s, o), bm2 = shfl_xor(bm, o);
             const int bi2 = shfl_xor(bi, o);
-            lse_merge(m, s, m2, s2);
+            lse2_merge(m, s, m2, s2);
             if (better(bm2, bi2, bm, bi)) { bm = bm2; bi = bi2; }
         }
     }
 }
 
+// Greedy: running first argmax of the raw row.  Sampling: t2 = row * invT *
+// log2(e), running (max, sum of 2^(t2 - max)); the argmax is not needed.
 template <bool kGreedy>
-__device__ __forceinline__ void stat_elem(float x, int v, float invT, float& m, float& s,
-                                          float& bm, int& bi) {
-    const float t = kGreedy ? x : x * invT;
-    if (t > bm) { bm = t; bi = v; }
-    if (!kGreedy) {
-        if (t > m) { s = s * expf(m - t) + 1.0f; m = t; }
-        else s += expf(t - m);
+__device__ __forceinline__ void stat_elem(float x, int v, float c2, float& m, float& s, float& bm, int& bi) {
+    if (kGreedy) {
+        if (x > bm) { bm = x; bi = v; }
+    } else {
+        const float t = x * c2;
+        if (t > m) { s = s * exp2f(m - t) + 1.0f; m = t; }
+        else s += exp2f(t - m);
     }
 }
 
@@ -124,6 +140,7 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_stats_kernel(VerifyPara
     const int v0 = chunk * kVerifyChunk;
     const int v1 = min(V, v0 + kVerifyChunk);
     const float* base = p.target + (size_t)row * V;
+    const float c2 = p.invT * kLog2e;
     float m = -INFINITY, s = 0.0f, bm = -INFINITY;
     int bi = INT_MAX;
     if ((V & 3) == 0 && ((reinterpret_cast<uintptr_t>(p.target) & 15) == 0)) {
@@ -136,19 +153,34 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_stats_kernel(VerifyPara
             buf[i] = v < v1 ? __ldcs(reinterpret_cast<const float4*>(base + v))
                             : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         }
+        if (kGreedy) {
 #pragma unroll
-        for (int i = 0; i < kVec; ++i) {
-            const int v = v0 + 4 * (threadIdx.x + i * kVerifyThreads);
-            if (v < v1) {
-                stat_elem<kGreedy>(buf[i].x, v + 0, p.invT, m, s, bm, bi);
-                stat_elem<kGreedy>(buf[i].y, v + 1, p.invT, m, s, bm, bi);
-                stat_elem<kGreedy>(buf[i].z, v + 2, p.invT, m, s, bm, bi);
-                stat_elem<kGreedy>(buf[i].w, v + 3, p.invT, m, s, bm, bi);
+            for (int i = 0; i < kVec; ++i) {
+                const int v = v0 + 4 * (threadIdx.x + i * kVerifyThreads);
+                if (v < v1) {
+                    stat_elem<true>(buf[i].x, v + 0, c2, m, s, bm, bi);
+                    stat_elem<true>(buf[i].y, v + 1, c2, m, s, bm, bi);
+                    stat_elem<true>(buf[i].z, v + 2, c2, m, s, bm, bi);
+                    stat_elem<true>(buf[i].w, v + 3, c2, m, s, bm, bi);
+                }
+            }
+        } else {
+            // the thread's maximum first, then one pass of 2^(t - max); entries past
+            // the row end were loaded as -inf and add nothing
+#pragma unroll
+            for (int i = 0; i < kVec; ++i) {
+                buf[i].x *= c2; buf[i].y *= c2; buf[i].z *= c2; buf[i].w *= c2;
+                m = fmaxf(m, fmaxf(fmaxf(buf[i].x, buf[i].y), fmaxf(buf[i].z, buf[i].w)));
+            }
+            if (m != -INFINITY) {
+#pragma unroll
+                for (int i = 0; i < kVec; ++i)
+                    s += (exp2f(buf[i].x - m) + exp2f(buf[i].y - m)) + (exp2f(buf[i].z - m) + exp2f(buf[i].w - m));
             }
         }
     } else {
         for (int v = v0 + threadIdx.x; v < v1; v += kVerifyThreads)
-            stat_elem<kGreedy>(__ldg(base + v), v, p.invT, m, s, bm, bi);
+            stat_elem<kGreedy>(__ldg(base + v), v, c2, m, s, bm, bi);
     }
     block_rowstat(m, s, bm, bi);
     if (threadIdx.x == 0) {
@@ -179,9 +211,9 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_stats_kernel(VerifyPara
             const float m2 = __ldcg(&rs[c].m), s2 = __ldcg(&rs[c].s);
             const int i2 = __ldcg(&rs[c].idx);
             if (better(m2, i2, am, ai)) { am = m2; ai = i2; }
-            if (!kGreedy) lse_merge(cm, cs, m2, s2);
+            if (!kGreedy) lse2_merge(cm, cs, m2, s2);
         }
-        row_lse[threadIdx.x] = kGreedy ? 0.0f : cm + logf(cs);
+        row_lse[threadIdx.x] = kGreedy ? 0.0f : cm + log2f(cs);  // base-2 log-normaliser
         row_amax[threadIdx.x] = ai;
     }
     __syncthreads();
@@ -196,8 +228,7 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_stats_kernel(VerifyPara
                 accept = (yj == row_amax[j]);
                 pt = accept ? 1.0f : 0.0f;
             } else {
-                const float t = p.target[(size_t)(first + j) * p.V + yj] * p.invT;
-                pt = expf(t - row_lse[j]);
+                pt = exp2f(p.target[(size_t)(first + j) * p.V + yj] * c2 - row_lse[j]);
                 const float ratio = pt / p.q_tok[(size_t)r * g + j];
                 const uint4 w = philox4x32_10(
                     make_uint4(0u, (uint32_t)j, (uint32_t)r, ctr_word3(p.cycle, kAccept)),
@@ -221,7 +252,7 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_stats_kernel(VerifyPara
             job.pos = n;
             job.mode = (n < l) ? 1 : 2;
             job.pad = 0;
-            job.lse = row_lse[n];
+            job.lse = row_lse[n] * kLn2;  // natural log-normaliser of t = row * invT
             job.pad2[0] = job.pad2[1] = job.pad2[2] = 0.0f;
             p.jobs[r] = job;
         }
