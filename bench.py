@@ -269,8 +269,8 @@ def run_ours(args):
         if ev is not None: ev[4].record(stream)
 
     # launches of this library per step
-    draft_launches = 1 + gamma if uses_tc else 1 + 2 * gamma  # + the anchor-row gather
-    verify_launches = 4 if T > 0 else 2  # prologue, stats, (residual rows, residual draw)
+    draft_launches = gamma + 1 if uses_tc else 1 + 2 * gamma  # steps + finalize
+    verify_launches = 5 if T > 0 else 2  # prologue, stats, (residual rows, draw, finalize)
     launches_per_step = (int(run_select) + draft_launches * int(run_draft) +
                          verify_launches * int(run_verify) + int(run_commit))
 

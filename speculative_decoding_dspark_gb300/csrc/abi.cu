@@ -96,7 +96,7 @@ size_t dspark_workspace_size(int op, int R, int gamma, int V, int rank, int max_
     switch (op) {
         case DSPARK_OP_DRAFT:
             if (V <= 0 || rank <= 0 || gamma <= 0) return 0;
-            if (tc_applies(w_dtype, w_dtype, R, V, rank, flags)) return draft_tc_workspace(R, V, rank);
+            if (tc_applies(w_dtype, w_dtype, R, V, rank, flags)) return draft_tc_workspace(R, gamma, rank);
             return draft_simt_layout(R, V).total;
         case DSPARK_OP_VERIFY:
             if (V <= 0 || max_rows < 0) return 0;
@@ -130,7 +130,7 @@ int dspark_markov_draft(const void* U, int u_dtype, const void* W1, const void* 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     if (tc_applies(u_dtype, w_dtype, R, V, rank, flags)) {
-        if (ws_bytes < draft_tc_workspace(R, V, rank)) return DSPARK_ERR_WORKSPACE;
+        if (ws_bytes < draft_tc_workspace(R, gamma, rank)) return DSPARK_ERR_WORKSPACE;
         if (!aligned16(U) || !aligned16(W1) || !aligned16(W2)) return DSPARK_ERR_UNSUPPORTED;
         DraftTcArgs a;
         a.U = U; a.W1 = W1; a.W2 = W2; a.anchor = anchor; a.seeds = seeds; a.cycle = cycle;

@@ -11,7 +11,7 @@
 //
 // One pipeline, two epilogues:
 //   draft     one launch per position k: logits of every request, Gumbel-max
-//             sample, log-normaliser and q(y);
+//             sample and the pieces of its log-normaliser and q(y);
 //   residual  one launch per verify: for every request the drafter's logits of
 //             its rejected row are recomputed here (the residual needs q on the
 //             whole vocabulary, and recomputing one row per request costs one
@@ -20,10 +20,9 @@
 //             full acceptance.
 //
 // Persistent, one CTA per SM, 18 warps:
-//   A (M = 128 requests x K = rank) = rows W1[prev] gathered into a workspace
-//     matrix H (a small kernel for the anchors or the residual rows, the
-//     reducer of draft step k for step k + 1), loaded by TMA into
-//     128-byte-swizzled shared memory and resident for the launch;
+//   A (M = 128 requests x K = rank) = rows W1[prev], gathered by the epilogue
+//     warps straight into 128-byte-swizzled shared memory at the start of the
+//     launch and resident for it;
 //   B (N = 128 vocabulary rows x K = rank) = W2 tiles streamed by TMA through a
 //     ring of 16 KB stages; the next tile's boxes are prefetched into L2 one
 //     tile ahead so the ring only has to cover L2 latency;
@@ -33,14 +32,23 @@
 //     16-column passes): Gumbel-max draws use the exponential-race form: with
 //     weight w > 0 and E = -log(u), the largest log(w) + Gumbel(u) is the
 //     largest w / E, so a candidate replaces the best when
-//     w * E_best > w_best * E (one log per entry, no log of the weight).
-// Each CTA leaves one partial per request; reduction is two-level and never
-// spins: the last CTA of each group of kGroup CTAs (atomic counter) merges its
-// group, the last group of a request block merges the groups.
+//     w * E_best > w_best * E.  Since E >= 1 - u, an entry with
+//     1 - u >= w * E_best / w_best cannot win; that test needs no logarithm
+//     (1 - u comes exactly from the random bits), and only the entries that
+//     pass it take the accurate log and the exact comparison.
+//
+// Cross-CTA results need no merging pass: every CTA folds its winner into one
+// 64-bit key per request and step with atomicMax (order-preserving bits of
+// the score above the inverted index, so ties go to the lower index), and
+// stores its (max, sum of exp, winner logit) piece of the normaliser.  The
+// next draft step decodes its A rows' tokens from the keys (it is launched
+// as a programmatic dependent and waits for the previous step before reading
+// them, while its producer already streams W2), and one finalize kernel after
+// the last step turns keys and pieces into tokens, q_lse and q(y).
 //
 // Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM owner),
-// warps 2-17 = epilogue.  Every mbarrier wait is bounded (2 s); a timeout
-// aborts the CTA cleanly and reports DSPARK_ERR_TIMEOUT.
+// warps 2-17 = A gather, then epilogue.  Every mbarrier wait is bounded (2 s);
+// a timeout aborts the CTA cleanly and reports DSPARK_ERR_TIMEOUT.
 #include <cuda.h>
 
 #include "draft_tc.cuh"
@@ -54,20 +62,22 @@ constexpr int kNV = 128;                      // vocabulary rows per tile (MMA N
 constexpr int kKB = 64;                       // rank elements per stage (128-byte rows)
 constexpr int kTileBytes = 128 * kKB * 2;     // 16 KB: one operand k-block
 constexpr int kEpiWarps = 16;
-constexpr int kThreads = 64 + kEpiWarps * 32;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kCols = 32;                     // vocabulary columns per epilogue thread
 constexpr int kMaxStages = 8;
-constexpr int kMaxP = 256;                    // partials per request (>= CTAs per block)
-constexpr int kGroup = 16;                    // CTAs per first-level reduction group
-constexpr int kMaxGroups = kMaxP / kGroup;
+constexpr int kMaxP = 256;                    // CTAs per request block (pieces per request)
 constexpr uint32_t kTmemCols = 256;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2eF = 1.4426950408889634f;
 constexpr float kLn2F = 0.6931471805599453f;
+// Relative slack of the no-log race test, far above the rounding of the
+// quantities it compares (a few units in 2^-24).
+constexpr float kRaceSlack = 1.0f + 0x1p-10f;
 
-// Per-request partial.  Draft: (score, idx) of the Gumbel-max draw, s at it,
-// (max, sum of exp) of the logits.  Residual: (score, idx) over the residual,
-// (s_at, m-as-index) the draw over p, sum = residual mass seen.
+// Per-request partial of one thread or CTA.  Draft: (score, idx) of the
+// Gumbel-max draw, s at it, (max, sum of exp) of the logits.  Residual:
+// (score, idx) over the residual, (s_at, m-as-index) the draw over p.
 struct TcPartial {
     float score;
     int idx;
@@ -82,36 +92,28 @@ struct ResRow {
     int pos;       // block position of the row
     int trow;      // packed target row
     uint32_t w3;   // Philox counter word 3 (cycle and purpose)
-    float lse_p;   // target log-normaliser of the row (scaled logits)
-    float q_lse;   // drafter log-normaliser at pos (mode 1)
-    float pad[2];
+    float lse2_p;  // target log-normaliser of the row (scaled logits), base 2
+    float q_lse2;  // drafter log-normaliser at pos (mode 1), base 2
+    int prev;      // token whose W1 row is the A row (mode 1), else -1
+    float pad;
 };
 
 struct TcParams {
     const uint16_t* U;
     const uint16_t* W1;
-    uint16_t* H;           // [R, rank] the A rows
-    int* gcount;           // [nb * kMaxGroups] first-level counters
-    int* tcount;           // [nb] second-level counters
-    TcPartial* parts;      // [R * kMaxP]
-    TcPartial* gparts;     // [R * kMaxGroups]
+    unsigned long long* keys;  // draft [gamma][R]; residual [2][R] (residual race, p race)
+    float4* parts;             // draft [gamma][R][P]: (max, sum, winner logit, winner) per CTA
     const uint64_t* seeds;
     int32_t* dev_status;
     uint32_t cycle;
     float invT;
     int greedy;
     int R, gamma, V, rank, k;
-    int nb, P, n_groups, n_tiles, n_stages, nkb;
-    // draft
+    int nb, P, n_tiles, n_stages, nkb;
     const int32_t* anchor;
-    int32_t* y;
-    float* q_lse;
-    float* q_tok;
     float* q_logits;
-    // residual
     const float* target;
     const ResRow* rows;
-    int32_t* out_tokens;
 };
 
 struct Bars {
@@ -120,8 +122,7 @@ struct Bars {
     uint64_t afull, mma_done;
     uint32_t tmem_slot;
     int abort_flag;
-    int last;
-    int top;
+    int tok[kM];  // token of each A row: >= 0 a W1 row, -1 zero row, -2 zero row and no result
 };
 
 __device__ __forceinline__ void merge_draft(float& sc, int& ix, float& sa, float& m, float& su, float sc2, int ix2,
@@ -130,18 +131,17 @@ __device__ __forceinline__ void merge_draft(float& sc, int& ix, float& sa, float
     lse_merge(m, su, m2, su2);
 }
 
-__device__ __forceinline__ void merge_residual(float& sc, int& ix, float& sa, int& ia, float& su, float sc2, int ix2,
-                                               float sa2, int ia2, float su2) {
+__device__ __forceinline__ void merge_residual(float& sc, int& ix, float& sa, int& ia, float sc2, int ix2, float sa2,
+                                               int ia2) {
     if (better(sc2, ix2, sc, ix)) { sc = sc2; ix = ix2; }
     if (better(sa2, ia2, sa, ia)) { sa = sa2; ia = ia2; }
-    su += su2;
 }
 
 template <bool kRes>
 __device__ __forceinline__ void merge_any(TcPartial& a, const TcPartial& b) {
     if (kRes) {
         int ia = __float_as_int(a.m);
-        merge_residual(a.score, a.idx, a.s_at, ia, a.sum, b.score, b.idx, b.s_at, __float_as_int(b.m), b.sum);
+        merge_residual(a.score, a.idx, a.s_at, ia, b.score, b.idx, b.s_at, __float_as_int(b.m));
         a.m = __int_as_float(ia);
     } else {
         merge_draft(a.score, a.idx, a.s_at, a.m, a.sum, b.score, b.idx, b.s_at, b.m, b.sum);
@@ -157,13 +157,30 @@ __device__ __forceinline__ TcPartial identity_partial() {
     return w;
 }
 
-__device__ __forceinline__ int prev_of(const TcParams& p, int r) {  // -1 none, -2 bad
-    if (p.k == 0) {
-        const int a = p.anchor[r];
-        return a >= p.V ? -2 : (a < 0 ? -1 : a);
-    }
-    const int t = p.y[(size_t)r * p.gamma + p.k - 1];
-    return (t < 0 || t >= p.V) ? -2 : t;
+// (score, idx) as one integer whose unsigned order is better()'s order: the
+// score's bits made order-preserving (negative floats inverted, positive ones
+// with the sign bit set; -0 folded onto +0) above the inverted index.  A
+// published key is never 0.
+__device__ __forceinline__ unsigned long long winner_key(float score, int idx) {
+    uint32_t b = __float_as_uint(score + 0.0f);
+    b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return ((unsigned long long)b << 32) | (unsigned long long)(~(uint32_t)idx);
+}
+
+__device__ __forceinline__ int key_index(unsigned long long key) { return (int)~(uint32_t)key; }
+
+// 2^x on the special-function unit (relative error about 2^-22; the race
+// decisions and normalisers it feeds carry far larger margins).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// 1 + (1 - u) - 2^-24 for u = uniform_from_bits(x): the 23 kept bits inverted
+// under the exponent of 1.0 (exact).
+__device__ __forceinline__ float one_plus_complement(uint32_t x) {
+    return __uint_as_float((x >> 9) ^ 0x3FFFFFFFu);
 }
 
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
@@ -174,7 +191,7 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x
 }
 
 // Programmatic dependent launch: wait for the grids this one depends on to
-// complete (and their writes to be visible); allow dependents to start.
+// complete (and their writes to be visible); allow dependents to be scheduled.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -184,85 +201,38 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
-// Copies rows x n partials (row stride `stride`, first column `first`) into
-// shared memory with every load issued before any is used: one L2 round trip.
-__device__ __forceinline__ void stage_partials(TcPartial* dst, const TcPartial* src, size_t stride, int first,
-                                               int n, int rows) {
-    const int total = rows * n;
-    for (int e0 = threadIdx.x; e0 < total; e0 += 4 * kThreads) {
-        float4 lo[4], hi[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int e = e0 + u * kThreads;
-            if (e < total) {
-                const int r = e / n, j = e - r * n;
-                const float4* q = reinterpret_cast<const float4*>(src + (size_t)r * stride + first + j);
-                lo[u] = __ldcg(q);
-                hi[u] = __ldcg(q + 1);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int e = e0 + u * kThreads;
-            if (e < total) {
-                reinterpret_cast<float4*>(dst + e)[0] = lo[u];
-                reinterpret_cast<float4*>(dst + e)[1] = hi[u];
-            }
-        }
-    }
+__device__ __forceinline__ void epilogue_barrier() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
 }
 
-// H[r] = W1[anchor[r]] (zeros when there is no usable anchor): the A rows of draft step 0.
-__global__ void __launch_bounds__(256) gather_anchor_rows_kernel(const uint16_t* W1, const int32_t* anchor,
-                                                                 int R, int V, int rank, uint16_t* H) {
-    const int cpr = rank >> 3;  // 16-byte chunks per row
-    const long long total = (long long)R * cpr;
-    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
-         e += (long long)gridDim.x * blockDim.x) {
-        const int r = (int)(e / cpr), c = (int)(e - (long long)r * cpr);
-        const int a = anchor[r];
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (a >= 0 && a < V) v = __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)a * rank) + c);
-        reinterpret_cast<uint4*>(H + (size_t)r * rank)[c] = v;
+// Per request after the verify decisions: what the residual launch draws and
+// the token whose W1 row is its A row (the rejected position's predecessor).
+__global__ void __launch_bounds__(256) residual_prep_kernel(ResidualTcArgs a, ResRow* rows) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= a.R) return;
+    const VerifyJob job = a.jobs[r];
+    const int mode = a.valid[r] ? job.mode : 0;
+    int prev = -1;
+    if (mode == 1) {
+        prev = job.pos == 0 ? a.anchor[r] : a.y[(size_t)r * a.gamma + job.pos - 1];
+        if (prev >= a.V || prev < 0) prev = -1;
     }
-}
-
-// Per request after the verify decisions: what the residual launch draws, and
-// its A row W1[prev] of the rejected position (zeros for a bonus draw).
-__global__ void __launch_bounds__(256) residual_prep_kernel(ResidualTcArgs a, ResRow* rows, uint16_t* H) {
-    const int cpr = a.rank >> 3;
-    const long long total = (long long)a.R * cpr;
-    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
-         e += (long long)gridDim.x * blockDim.x) {
-        const int r = (int)(e / cpr), c = (int)(e - (long long)r * cpr);
-        const VerifyJob job = a.jobs[r];
-        const int mode = a.valid[r] ? job.mode : 0;
-        int prev = -1;
-        if (mode == 1) {
-            prev = job.pos == 0 ? a.anchor[r] : a.y[(size_t)r * a.gamma + job.pos - 1];
-            if (prev >= a.V) prev = -1;
-        }
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (prev >= 0) v = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.W1) + (size_t)prev * a.rank) + c);
-        reinterpret_cast<uint4*>(H + (size_t)r * a.rank)[c] = v;
-        if (c == 0) {
-            ResRow w;
-            w.mode = mode;
-            w.pos = job.pos;
-            w.trow = job.row;
-            w.w3 = ctr_word3(a.cycle, mode == 1 ? kResidualGumbel : kBonusGumbel);
-            w.lse_p = job.lse;
-            w.q_lse = mode == 1 ? a.q_lse[(size_t)r * a.gamma + job.pos] : 0.0f;
-            w.pad[0] = w.pad[1] = 0.0f;
-            rows[r] = w;
-        }
-    }
+    ResRow w;
+    w.mode = mode;
+    w.pos = job.pos;
+    w.trow = job.row;
+    w.w3 = ctr_word3(a.cycle, mode == 1 ? kResidualGumbel : kBonusGumbel);
+    w.lse2_p = job.lse * kLog2eF;
+    w.q_lse2 = mode == 1 ? a.q_lse[(size_t)r * a.gamma + job.pos] * kLog2eF : 0.0f;
+    w.prev = prev;
+    w.pad = 0.0f;
+    rows[r] = w;
 }
 
 template <bool kRes>
 __global__ void __launch_bounds__(kThreads, 1)
 markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_u,
-                 const __grid_constant__ CUtensorMap tm_h, const TcParams p) {
+                 const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
@@ -279,11 +249,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) { tc::mbar_init(&bar.full[s], 1); tc::mbar_init(&bar.empty[s], 1); }
         for (int a = 0; a < 2; ++a) { tc::mbar_init(&bar.tfull[a], 1); tc::mbar_init(&bar.tempty[a], kEpiWarps); }
-        tc::mbar_init(&bar.afull, 1);
+        tc::mbar_init(&bar.afull, kEpiWarps);
         tc::mbar_init(&bar.mma_done, 1);
         bar.abort_flag = 0;
-        bar.last = 0;
-        bar.top = 0;
         tc::fence_barrier_init();
     }
     if (warp == 1) {
@@ -293,27 +261,30 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
     if (warp == 0 && lane == 0) {
         tc::prefetch_tmap(&tm_w2);
         if (!kRes) tc::prefetch_tmap(&tm_u);
-        tc::prefetch_tmap(&tm_h);
     }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
+    // The next launch may be scheduled as SMs free up; it waits (griddepcontrol)
+    // before it reads anything this one writes.
+    griddep_launch_dependents();
     const uint32_t tmem_base = bar.tmem_slot;
     const int n_local = cidx < p.n_tiles ? (p.n_tiles - 1 - cidx) / p.P + 1 : 0;
 
     // this thread's running partial (epilogue threads)
     TcPartial part = identity_partial<kRes>();
+    bool row_ok = false;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        // W2 and U are inputs no launch of this library writes, so streaming
+        // them may start before the previous draft step has finished.
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 0;
             int last_phase[kMaxStages];
             for (int i = 0; i < kMaxStages; ++i) last_phase[i] = -1;
             bool ok = true;
-            // The first tiles do not depend on the previous launch: pull them into
-            // L2 while that launch may still be finishing (programmatic launch).
             for (int i = 0; i < 2 && i < n_local; ++i) {
                 const int t = cidx + i * p.P;
                 for (int q = 0; q < p.nkb; ++q) tma_prefetch_l2_2d(&tm_w2, q * kKB, t * kNV);
@@ -322,11 +293,6 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                     tc::tma_prefetch_l2_3d(&tm_u, t * kNV + kKB, p.k, row0);
                 }
             }
-            // H (and everything else the previous launch wrote) is ready after this
-            griddep_wait();
-            // A: the block's H rows, resident for the launch
-            tc::mbar_arrive_expect_tx(&bar.afull, (uint32_t)(p.nkb * kTileBytes));
-            for (int kb = 0; kb < p.nkb; ++kb) tc::tma_load_2d(sA + kb * kTileBytes, &tm_h, &bar.afull, kb * kKB, row0);
             for (int i = 0; ok && i < n_local; ++i) {
                 const int t = cidx + i * p.P;
                 for (int kb = 0; kb < p.nkb; ++kb) {
@@ -346,11 +312,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                     }
                 }
             }
-            // the copies this thread issued must land before the CTA exits
-            int dummy = 0;
-            volatile int* no_abort = &dummy;
-            tc::mbar_wait(&bar.afull, 0, no_abort, kWaitNs);
+            // after an abort, the copies this thread issued must land before the CTA exits
             if (*abort_flag) {
+                int dummy = 0;
+                volatile int* no_abort = &dummy;
                 for (int q = 0; q < S; ++q)
                     if (last_phase[q] >= 0) tc::mbar_wait(&bar.full[q], (uint32_t)last_phase[q], no_abort, kWaitNs);
             }
@@ -360,6 +325,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         if (lane == 0) {
             constexpr uint32_t idesc = tc::idesc_bf16_f32(kM, kNV);
             bool ok = tc::mbar_wait(&bar.afull, 0, abort_flag, kWaitNs);
+            tc::tc_fence_after();
             int s = 0;
             uint32_t ph = 0;
             const uint32_t a_base = tc::smem_u32(sA), b_base = tc::smem_u32(sB);
@@ -391,20 +357,73 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
             tc::mbar_wait(&bar.mma_done, 0, no_abort, kWaitNs);
         }
     } else {
+        // ------------------------------------------------------------ A gather
+        const int et = threadIdx.x - 64;  // 0..511
+        // the previous draft step's winners are read after this
+        griddep_wait();
+        if (et < kM) {
+            const int r = row0 + et;
+            int t = -1;
+            if (r < p.R) {
+                if (kRes) {
+                    const ResRow ri = p.rows[r];
+                    t = ri.mode == 0 ? -2 : ri.prev;
+                } else if (p.k == 0) {
+                    const int a = p.anchor[r];
+                    t = a >= p.V ? -2 : (a < 0 ? -1 : a);
+                } else {
+                    const unsigned long long key = __ldcg(p.keys + (size_t)(p.k - 1) * p.R + r);
+                    t = key ? key_index(key) : -2;
+                }
+            } else {
+                t = -2;
+            }
+            bar.tok[et] = t;
+        }
+        epilogue_barrier();
+        {
+            // A row m, k-block kb, 16-byte chunk j sits at chunk j ^ (m & 7) of its
+            // 128-byte row: the layout a 128-byte-swizzled TMA box would give.
+            const int cpr = p.rank >> 3;
+            const int total = kM * cpr;
+            for (int e0 = et; e0 < total; e0 += 8 * kEpiThreads) {
+                uint4 v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int e = e0 + u * kEpiThreads;
+                    v[u] = make_uint4(0u, 0u, 0u, 0u);
+                    if (e < total) {
+                        const int m = e / cpr, c = e - m * cpr;
+                        const int t = bar.tok[m];
+                        if (t >= 0) v[u] = __ldg(reinterpret_cast<const uint4*>(p.W1 + (size_t)t * p.rank) + c);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int e = e0 + u * kEpiThreads;
+                    if (e < total) {
+                        const int m = e / cpr, c = e - m * cpr;
+                        const int off = (c >> 3) * kTileBytes + m * 128 + (((c & 7) ^ (m & 7)) << 4);
+                        *reinterpret_cast<uint4*>(sA + off) = v[u];
+                    }
+                }
+            }
+        }
+        // the tensor cores read A through the async proxy
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bar.afull);
+
         // ------------------------------------------------------------ epilogue
         const int ew = warp - 2;           // 0..15
         const int quad = warp & 3;         // TMEM lane quadrant this warp may read
         const int quarter = ew >> 2;       // which 32 of the tile's 128 columns
         const int m = quad * 32 + lane;
         const int rr = row0 + m;
-        bool row_ok = rr < p.R;
-        // per-row constants of the two modes
+        row_ok = bar.tok[m] != -2;
         ResRow rinfo;
-        rinfo.mode = 0; rinfo.pos = 0; rinfo.trow = 0; rinfo.w3 = 0; rinfo.lse_p = 0.0f; rinfo.q_lse = 0.0f;
-        if (kRes && row_ok) {
-            rinfo = p.rows[rr];
-            row_ok = rinfo.mode != 0;
-        }
+        rinfo.mode = 0; rinfo.pos = 0; rinfo.trow = 0; rinfo.w3 = 0; rinfo.lse2_p = 0.0f; rinfo.q_lse2 = 0.0f;
+        if (kRes && row_ok) rinfo = p.rows[rr];
         const bool sampling = kRes || !p.greedy;
         PhiloxKey K;
         if (sampling) K = philox_key(row_ok ? p.seeds[rr] : 0ull);
@@ -415,9 +434,12 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         const uint16_t* urow = p.U + rk * p.V;
         const float* trow = kRes ? p.target + (size_t)rinfo.trow * p.V : nullptr;
         float* qrow = (!kRes && p.q_logits && row_ok) ? p.q_logits + rk * p.V : nullptr;
-        // exponential-race state: draft (bw, bE); residual (br, bEr) and (bp, bEp)
+        // logits are scaled to base 2 when sampling: s2 = s * log2(e) / T
+        const float c2 = sampling ? p.invT * kLog2eF : 1.0f;
+        // exponential-race state: draft / residual race (bw, bE, rho), p race (bp, bEp, rho_p);
+        // rho = E_best / w_best with the slack, the bound of the no-log test
         float bw = 0.0f, bE = 1.0f, bp = 0.0f, bEp = 1.0f;
-        float rho2 = INFINITY;  // draft: E_best * log2(e) / w_best
+        float rho = INFINITY, rho_p = INFINITY;
         int ia = INT_MAX;
         for (int i = 0; i < n_local; ++i) {
             const int t = cidx + i * p.P;
@@ -474,15 +496,16 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                     for (int c = 0; c < 16; ++c) {
                         const uint32_t word = (kRes || h == 0) ? uwA[c >> 1] : uwB[c >> 1];
                         const float u = __uint_as_float((c & 1) ? (word & 0xFFFF0000u) : (word << 16));
-                        const float sb = u + sv[c];
-                        sv[c] = (!kRes && p.greedy) ? sb : sb * p.invT;
+                        sv[c] = (u + sv[c]) * c2;
                     }
                 }
-                if (qrow) {
+                if (qrow) {  // natural units
+                    const float back = sampling ? kLn2F : 1.0f;
 #pragma unroll
                     for (int c = 0; c < 16; c += 4)
                         if (c < nvalid)
-                            *reinterpret_cast<float4*>(qrow + v0 + c) = make_float4(sv[c], sv[c + 1], sv[c + 2], sv[c + 3]);
+                            *reinterpret_cast<float4*>(qrow + v0 + c) =
+                                make_float4(sv[c] * back, sv[c + 1] * back, sv[c + 2] * back, sv[c + 3] * back);
                 }
                 if (!kRes && p.greedy) {
 #pragma unroll
@@ -492,25 +515,18 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                         }
                     continue;
                 }
-                if (!kRes) {
-                    // Sampling draft, base-2 units: s2 = s * log2(e), w = 2^(s2 - m2).
-                    // An entry can only replace the best when w * E_best > w_best * E,
-                    // i.e. u > exp(-w * E_best / w_best); that bound is tested first
-                    // (with a 2^-14 relative margin against the rounding of its
-                    // approximations) and the accurate log and exact comparison run
-                    // only for entries that pass it.
+                if constexpr (!kRes) {
+                    // sampling draft in base 2: w = 2^(s2 - m2) relative to the running max
                     float cm = -INFINITY;
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        sv[c] *= kLog2eF;
+                    for (int c = 0; c < 16; ++c)
                         if (c < nvalid) cm = fmaxf(cm, sv[c]);
-                    }
                     if (cm > part.m) {
-                        const float sc = exp2f(part.m - cm);  // 0 while the max is -inf
+                        const float sc = ex2(part.m - cm);  // 0 while the max is -inf
                         part.sum *= sc;
                         bw *= sc;
                         part.m = cm;
-                        rho2 = bE * kLog2eF / bw;
+                        rho = bE / bw * kRaceSlack;
                     }
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -521,45 +537,50 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                         for (int e = 0; e < 4; ++e) {
                             const int c = 4 * q + e;
                             if (c < nvalid) {
-                                const float w = exp2f(sv[c] - part.m);
+                                const float w = ex2(sv[c] - part.m);
                                 part.sum += w;
-                                const float u = uniform_from_bits(words[e]);
-                                if (u > exp2f(-w * rho2) * (1.0f - 0x1p-14f)) {
-                                    const float E = -logf(u);
+                                if (one_plus_complement(words[e]) < fmaf(w, rho, 1.0f)) {
+                                    const float E = -logf(uniform_from_bits(words[e]));
                                     if (w * bE > bw * E) {
                                         bw = w; bE = E; part.idx = v0 + c; part.s_at = sv[c];
-                                        rho2 = bE * kLog2eF / bw;
+                                        rho = bE / bw * kRaceSlack;
                                     }
                                 }
                             }
                         }
                     }
-                    continue;
-                }
-                float tv[16];
+                } else {
+                    float tv[16];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float4 f = 4 * j < nvalid ? __ldg(reinterpret_cast<const float4*>(trow + v0) + j)
-                                                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                    tv[4 * j + 0] = f.x; tv[4 * j + 1] = f.y; tv[4 * j + 2] = f.z; tv[4 * j + 3] = f.w;
-                }
+                    for (int j = 0; j < 4; ++j) {
+                        const float4 f = 4 * j < nvalid ? __ldg(reinterpret_cast<const float4*>(trow + v0) + j)
+                                                        : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                        tv[4 * j + 0] = f.x; tv[4 * j + 1] = f.y; tv[4 * j + 2] = f.z; tv[4 * j + 3] = f.w;
+                    }
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 wd = philox4x32_10(
-                        make_uint4((uint32_t)((v0 >> 2) + q), (uint32_t)pos, (uint32_t)rr, w3), K);
-                    const uint32_t words[4] = {wd.x, wd.y, wd.z, wd.w};
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 wd = philox4x32_10(
+                            make_uint4((uint32_t)((v0 >> 2) + q), (uint32_t)pos, (uint32_t)rr, w3), K);
+                        const uint32_t words[4] = {wd.x, wd.y, wd.z, wd.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c = 4 * q + e;
-                        if (c < nvalid) {
-                            const float E = -logf(uniform_from_bits(words[e]));
-                            const float pv = expf(tv[c] * p.invT - rinfo.lse_p);
-                            if (pv * bEp > bp * E) { bp = pv; bEp = E; ia = v0 + c; }
-                            if (with_u) {
-                                const float res = pv - expf(sv[c] - rinfo.q_lse);
-                                if (res > 0.0f) {
-                                    part.sum += res;
-                                    if (res * bE > bw * E) { bw = res; bE = E; part.idx = v0 + c; }
+                        for (int e = 0; e < 4; ++e) {
+                            const int c = 4 * q + e;
+                            if (c < nvalid) {
+                                const float pv = ex2(fmaf(tv[c], c2, -rinfo.lse2_p));
+                                const float res = with_u ? pv - ex2(sv[c] - rinfo.q_lse2) : 0.0f;
+                                const float f = one_plus_complement(words[e]);
+                                const bool try_p = f < fmaf(pv, rho_p, 1.0f);
+                                const bool try_r = res > 0.0f && f < fmaf(res, rho, 1.0f);
+                                if (try_p || try_r) {
+                                    const float E = -logf(uniform_from_bits(words[e]));
+                                    if (try_p && pv * bEp > bp * E) {
+                                        bp = pv; bEp = E; ia = v0 + c;
+                                        rho_p = bEp / bp * kRaceSlack;
+                                    }
+                                    if (try_r && res * bE > bw * E) {
+                                        bw = res; bE = E; part.idx = v0 + c;
+                                        rho = bE / bw * kRaceSlack;
+                                    }
                                 }
                             }
                         }
@@ -580,11 +601,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         }
     }
 
-    // ---------------------------------------------------------------- per-CTA partials
-    // The next launch may start on SMs this grid leaves; the workspace below is
-    // shared with the previous launch, so wait for it to have finished.
-    griddep_launch_dependents();
-    griddep_wait();
+    // ---------------------------------------------------------------- per-CTA result
     __syncthreads();
     TcPartial* scratch = reinterpret_cast<TcPartial*>(sB);  // W2 stages are drained
     if (warp >= 6) {
@@ -597,116 +614,102 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem_base, kTmemCols);
     }
-    const bool aborted = *abort_flag != 0;
-    if (warp >= 2 && warp < 6 && !aborted) {
+    if (*abort_flag) {
+        if (threadIdx.x == 0) report(p.dev_status, DSPARK_ERR_TIMEOUT);
+        return;
+    }
+    if (warp >= 2 && warp < 6 && row_ok) {
         const int m = (warp & 3) * 32 + lane;
         const int rr = row0 + m;
-        if (rr < p.R) {
 #pragma unroll
-            for (int q = 0; q < 3; ++q) merge_any<kRes>(part, scratch[q * kM + m]);
-            p.parts[(size_t)rr * p.P + cidx] = part;
-            __threadfence();
-        }
-    }
-    __syncthreads();
-    const int grp = cidx / kGroup;
-    const int gsize = min(kGroup, p.P - grp * kGroup);
-    int* gcnt = p.gcount + blk * kMaxGroups + grp;
-    if (threadIdx.x == 0) {
-        if (aborted) {
-            report(p.dev_status, DSPARK_ERR_TIMEOUT);
-        } else {
-            __threadfence();
-            bar.last = (atomicAdd(gcnt, 1) == gsize - 1);
-        }
-    }
-    __syncthreads();
-    if (!bar.last) return;
-    __threadfence();
-
-    // ------------------------------------------- last CTA of its group: merge the group
-    const int rows = min(kM, p.R - row0);
-    TcPartial* stage = reinterpret_cast<TcPartial*>(sB);
-    stage_partials(stage, p.parts + (size_t)row0 * p.P, p.P, grp * kGroup, gsize, rows);
-    __syncthreads();
-    for (int m = threadIdx.x; m < rows; m += kThreads) {
-        TcPartial w = identity_partial<kRes>();
-        for (int j = 0; j < gsize; ++j) merge_any<kRes>(w, stage[m * gsize + j]);
-        p.gparts[(size_t)(row0 + m) * kMaxGroups + grp] = w;
-    }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        *gcnt = 0;  // ready for the next launch
-        bar.top = (atomicAdd(p.tcount + blk, 1) == p.n_groups - 1);
-    }
-    __syncthreads();
-    if (!bar.top) return;
-    __threadfence();
-
-    // ------------------------------------------- last group of the block: final merge
-    stage_partials(stage, p.gparts + (size_t)row0 * kMaxGroups, kMaxGroups, 0, p.n_groups, rows);
-    __syncthreads();
-    for (int m = threadIdx.x; m < rows; m += kThreads) {
-        const int rr = row0 + m;
-        TcPartial w = identity_partial<kRes>();
-        for (int j = 0; j < p.n_groups; ++j) merge_any<kRes>(w, stage[m * p.n_groups + j]);
+        for (int q = 0; q < 3; ++q) merge_any<kRes>(part, scratch[q * kM + m]);
         if (kRes) {
-            const ResRow ri = p.rows[rr];
-            if (ri.mode == 0) continue;
-            const int alt = __float_as_int(w.m);
-            int tok = (ri.mode == 1 && w.sum > 0.0f) ? w.idx : alt;
-            if (tok < 0 || tok >= p.V) {  // no finite score (NaN logits)
-                tok = -1;
-                report(p.dev_status, DSPARK_ERR_DEVICE_INPUT);
-            }
-            p.out_tokens[(size_t)rr * (p.gamma + 1) + ri.pos] = tok;
+            if (part.idx != INT_MAX) atomicMax(p.keys + rr, winner_key(part.score, part.idx));
+            const int ia = __float_as_int(part.m);
+            if (ia != INT_MAX) atomicMax(p.keys + p.R + rr, winner_key(part.s_at, ia));
         } else {
-            const size_t rk = (size_t)rr * p.gamma + p.k;
-            const int prev = prev_of(p, rr);
-            if (prev == -2 || w.idx < 0 || w.idx >= p.V) {
-                p.y[rk] = -1;
-                if (p.q_lse) p.q_lse[rk] = NAN;
-                if (p.q_tok) p.q_tok[rk] = NAN;
-                report(p.dev_status, DSPARK_ERR_DEVICE_INPUT);
-            } else {
-                p.y[rk] = w.idx;
-                if (!p.greedy) {
-                    const float lse = w.m + logf(w.sum);
-                    if (p.q_lse) p.q_lse[rk] = lse;
-                    if (p.q_tok) p.q_tok[rk] = expf(w.s_at - lse);
-                }
-            }
+            const size_t slot = (size_t)p.k * p.R + rr;
+            if (!p.greedy)
+                p.parts[slot * p.P + cidx] = make_float4(part.m, part.sum, part.s_at, __int_as_float(part.idx));
+            if (part.idx != INT_MAX) atomicMax(p.keys + slot, winner_key(part.score, part.idx));
         }
     }
-    if (threadIdx.x == 0) p.tcount[blk] = 0;
-    if (!kRes && p.k + 1 < p.gamma) {
-        // the next step's A rows: H[r] = W1[y_k[r]] (zeros for an unusable request)
-        __syncthreads();
-        const int cpr = p.rank >> 3;
-        const int total = rows * cpr;
-        for (int e0 = threadIdx.x; e0 < total; e0 += 8 * kThreads) {
-            uint4 v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int e = e0 + u * kThreads;
-                v[u] = make_uint4(0u, 0u, 0u, 0u);
-                if (e < total) {
-                    const int m = e / cpr, c = e - m * cpr;
-                    const int tok = p.y[(size_t)(row0 + m) * p.gamma + p.k];
-                    if (tok >= 0 && tok < p.V) v[u] = __ldg(reinterpret_cast<const uint4*>(p.W1 + (size_t)tok * p.rank) + c);
-                }
+}
+
+struct DraftFinalize {
+    const unsigned long long* keys;
+    const float4* parts;
+    int R, gamma, P, greedy;
+    int32_t* y;
+    float* q_lse;
+    float* q_tok;
+    int32_t* dev_status;
+};
+
+// One warp per (position, request): the token from the step's winner key, the
+// log-normaliser from the CTAs' (max, sum) pieces, q(y) from the piece of the
+// CTA that held the winner.  A request without a key had an unusable anchor or
+// predecessor (or no finite logit): its token is -1 and its q values NaN.
+__global__ void __launch_bounds__(256) draft_finalize_kernel(DraftFinalize f) {
+    griddep_wait();
+    const int gw = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (gw >= f.R * f.gamma) return;
+    const int k = gw / f.R, r = gw - k * f.R;
+    const size_t slot = (size_t)k * f.R + r;
+    const size_t rk = (size_t)r * f.gamma + k;
+    const unsigned long long key = f.keys[slot];
+    if (key == 0) {
+        if (lane == 0) {
+            f.y[rk] = -1;
+            if (!f.greedy) {
+                if (f.q_lse) f.q_lse[rk] = NAN;
+                if (f.q_tok) f.q_tok[rk] = NAN;
             }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int e = e0 + u * kThreads;
-                if (e < total) {
-                    const int m = e / cpr, c = e - m * cpr;
-                    reinterpret_cast<uint4*>(p.H + (size_t)(row0 + m) * p.rank)[c] = v[u];
-                }
-            }
+            report(f.dev_status, DSPARK_ERR_DEVICE_INPUT);
         }
+        return;
     }
+    const int idx = key_index(key);
+    if (f.greedy) {
+        if (lane == 0) f.y[rk] = idx;
+        return;
+    }
+    float m = -INFINITY, s = 0.0f, sat = -INFINITY;
+    for (int j = lane; j < f.P; j += 32) {
+        const float4 q = f.parts[slot * f.P + j];
+        lse_merge(m, s, q.x, q.y);
+        if (__float_as_int(q.w) == idx) sat = q.z;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = shfl_xor(m, o), s2 = shfl_xor(s, o);
+        lse_merge(m, s, m2, s2);
+        sat = fmaxf(sat, shfl_xor(sat, o));
+    }
+    if (lane == 0) {
+        const float lse = m + logf(s);
+        f.y[rk] = idx;
+        if (f.q_lse) f.q_lse[rk] = lse;
+        if (f.q_tok) f.q_tok[rk] = expf(sat - lse);
+    }
+}
+
+// The extra token of every request: the residual winner when the residual has
+// mass (mode 1), else the winner over p.
+__global__ void __launch_bounds__(256) residual_finalize_kernel(const ResRow* rows, const unsigned long long* keys,
+                                                                int R, int gamma, int32_t* out_tokens,
+                                                                int32_t* dev_status) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= R) return;
+    const ResRow ri = rows[r];
+    if (ri.mode == 0) return;
+    const unsigned long long kr = keys[r], kp = keys[R + r];
+    int tok = -1;
+    if (ri.mode == 1 && kr) tok = key_index(kr);
+    else if (kp) tok = key_index(kp);
+    if (tok < 0) report(dev_status, DSPARK_ERR_DEVICE_INPUT);  // no finite score (NaN logits)
+    out_tokens[(size_t)r * (gamma + 1) + ri.pos] = tok;
 }
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -728,17 +731,17 @@ EncodeTiled encoder() {
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
+// Workspace: winner keys, then (draft) the per-CTA normaliser pieces or
+// (residual) the per-request rows.
 struct TcLayout {
-    size_t counters, parts, gparts, h, rows, total;
+    size_t keys, n_keys, parts, rows, total;
 };
-TcLayout tc_layout(int R, int rank, bool residual) {
-    const int nb = (R + kM - 1) / kM;
+TcLayout tc_layout(int R, int gamma, bool residual) {
     TcLayout L;
     size_t off = 0;
-    L.counters = off; off += up256(sizeof(int) * (size_t)nb * (kMaxGroups + 1));
-    L.parts = off; off += up256(sizeof(TcPartial) * (size_t)R * kMaxP);
-    L.gparts = off; off += up256(sizeof(TcPartial) * (size_t)R * kMaxGroups);
-    L.h = off; off += up256((size_t)R * rank * 2);
+    L.n_keys = residual ? 2 * (size_t)R : (size_t)gamma * R;
+    L.keys = off; off += up256(sizeof(unsigned long long) * L.n_keys);
+    L.parts = off; off += residual ? 0 : up256(sizeof(float4) * (size_t)gamma * R * kMaxP);
     L.rows = off; off += residual ? up256(sizeof(ResRow) * (size_t)R) : 0;
     L.total = off;
     return L;
@@ -757,8 +760,7 @@ bool encode_2d_bf16(EncodeTiled enc, CUtensorMap* m, const void* base, int inner
 // Shared launch setup of both modes: device limits, stage count, tensor maps,
 // the common parameter block.  Returns DSPARK_OK or an error status.
 int prepare(EncodeTiled enc, const void* U, const void* W1, const void* W2, int R, int gamma, int V, int rank,
-            void* ws, bool residual, TcParams& p, CUtensorMap& tm_w2, CUtensorMap& tm_u, CUtensorMap& tm_h,
-            int& grid, size_t& smem, int& n_sm) {
+            TcParams& p, CUtensorMap& tm_w2, CUtensorMap& tm_u, int& grid, size_t& smem, int& n_sm) {
     int dev = 0, max_smem = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DSPARK_ERR_CUDA;
@@ -769,14 +771,10 @@ int prepare(EncodeTiled enc, const void* U, const void* W1, const void* W2, int 
     if ((size_t)max_smem < fixed + 2 * kTileBytes) return DSPARK_ERR_UNSUPPORTED;
     const int n_stages = (int)std::min<size_t>(kMaxStages, ((size_t)max_smem - fixed) / kTileBytes);
     smem = fixed + (size_t)n_stages * kTileBytes;
-    // the end-of-launch partial exchange and merges reuse the drained stages
-    if ((size_t)n_stages * kTileBytes < (size_t)kM * kMaxGroups * sizeof(TcPartial)) return DSPARK_ERR_UNSUPPORTED;
+    // the end-of-launch exchange of the epilogue quarters reuses the drained stages
+    if ((size_t)n_stages * kTileBytes < (size_t)3 * kM * sizeof(TcPartial)) return DSPARK_ERR_UNSUPPORTED;
 
-    const TcLayout L = tc_layout(R, rank, residual);
-    unsigned char* w = static_cast<unsigned char*>(ws);
-    uint16_t* H = reinterpret_cast<uint16_t*>(w + L.h);
     if (!encode_2d_bf16(enc, &tm_w2, W2, rank, V, kNV)) return DSPARK_ERR_CUDA;
-    if (!encode_2d_bf16(enc, &tm_h, H, rank, R, kM)) return DSPARK_ERR_CUDA;
     {
         const cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)gamma, (cuuint64_t)R};
         const cuuint64_t strides[2] = {(cuuint64_t)V * 2, (cuuint64_t)gamma * V * 2};
@@ -790,19 +788,13 @@ int prepare(EncodeTiled enc, const void* U, const void* W1, const void* W2, int 
     p = TcParams();
     p.U = static_cast<const uint16_t*>(U);
     p.W1 = static_cast<const uint16_t*>(W1);
-    p.H = H;
-    p.parts = reinterpret_cast<TcPartial*>(w + L.parts);
-    p.gparts = reinterpret_cast<TcPartial*>(w + L.gparts);
     p.R = R;
     p.gamma = gamma;
     p.V = V;
     p.rank = rank;
     p.nb = (R + kM - 1) / kM;
-    p.gcount = reinterpret_cast<int*>(w + L.counters);
-    p.tcount = p.gcount + (size_t)p.nb * kMaxGroups;
     p.n_tiles = (V + kNV - 1) / kNV;
     p.P = std::max(1, std::min(std::min(n_sm / p.nb, p.n_tiles), kMaxP));
-    p.n_groups = (p.P + kGroup - 1) / kGroup;
     p.n_stages = n_stages;
     p.nkb = nkb;
     grid = p.P * p.nb;
@@ -816,26 +808,26 @@ bool draft_tc_supported(int u_dtype, int w_dtype, int R, int V, int rank) {
            rank <= 512 && V % 8 == 0 && V >= 8;
 }
 
-size_t draft_tc_workspace(int R, int, int rank) { return tc_layout(R, rank, false).total; }
+size_t draft_tc_workspace(int R, int gamma, int) { return tc_layout(R, gamma, false).total; }
 
-size_t residual_tc_workspace(int R, int rank) { return tc_layout(R, rank, true).total; }
+size_t residual_tc_workspace(int R, int) { return tc_layout(R, 0, true).total; }
 
 int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream) {
     EncodeTiled enc = encoder();
     if (!enc) return DSPARK_ERR_CUDA;
     if (a.q_logits && (reinterpret_cast<uintptr_t>(a.q_logits) & 15)) return DSPARK_ERR_UNSUPPORTED;
     TcParams p;
-    CUtensorMap tm_w2, tm_u, tm_h;
+    CUtensorMap tm_w2, tm_u;
     int grid = 0, n_sm = 0;
     size_t smem = 0;
-    const int st = prepare(enc, a.U, a.W1, a.W2, a.R, a.gamma, a.V, a.rank, a.ws, false, p, tm_w2, tm_u, tm_h, grid,
-                           smem, n_sm);
+    const int st = prepare(enc, a.U, a.W1, a.W2, a.R, a.gamma, a.V, a.rank, p, tm_w2, tm_u, grid, smem, n_sm);
     if (st != DSPARK_OK) return st;
+    const TcLayout L = tc_layout(a.R, a.gamma, false);
+    unsigned char* w = static_cast<unsigned char*>(a.ws);
+    p.keys = reinterpret_cast<unsigned long long*>(w + L.keys);
+    p.parts = reinterpret_cast<float4*>(w + L.parts);
     p.anchor = a.anchor;
     p.seeds = a.seeds;
-    p.y = a.y;
-    p.q_lse = a.q_lse;
-    p.q_tok = a.q_tok;
     p.q_logits = a.q_logits;
     p.dev_status = a.dev_status;
     p.cycle = a.cycle;
@@ -844,16 +836,12 @@ int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream) {
     if (cudaFuncSetAttribute(markov_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return DSPARK_ERR_CUDA;
-    if (cudaMemsetAsync(p.gcount, 0, sizeof(int) * (size_t)p.nb * (kMaxGroups + 1), stream) != cudaSuccess)
+    if (cudaMemsetAsync(p.keys, 0, sizeof(unsigned long long) * L.n_keys, stream) != cudaSuccess)
         return DSPARK_ERR_CUDA;
-    {
-        const long long chunks = (long long)a.R * (a.rank >> 3);
-        const int blocks = (int)std::min<long long>((chunks + 255) / 256, 4LL * n_sm);
-        gather_anchor_rows_kernel<<<blocks, 256, 0, stream>>>(p.W1, a.anchor, a.R, a.V, a.rank, p.H);
-    }
-    // Each step may start while the previous one finishes its reduction: the
-    // kernel prefetches its first tiles and waits (griddepcontrol) before it
-    // reads anything the previous launch wrote.
+    // Step 0 waits for everything before it on the stream.  Steps 1.. and the
+    // finalize are programmatic dependents of the launch before them: they may
+    // start as its CTAs retire and wait (griddepcontrol) before reading its
+    // results; the only data they touch earlier are W2 and U.
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -863,12 +851,30 @@ int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream) {
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
     for (int k = 0; k < a.gamma; ++k) {
         p.k = k;
-        if (cudaLaunchKernelEx(&cfg, markov_tc_kernel<false>, tm_w2, tm_u, tm_h, p) != cudaSuccess)
-            return DSPARK_ERR_CUDA;
+        cfg.numAttrs = k == 0 ? 0 : 1;
+        if (cudaLaunchKernelEx(&cfg, markov_tc_kernel<false>, tm_w2, tm_u, p) != cudaSuccess) return DSPARK_ERR_CUDA;
     }
+    DraftFinalize f;
+    f.keys = p.keys;
+    f.parts = p.parts;
+    f.R = a.R;
+    f.gamma = a.gamma;
+    f.P = p.P;
+    f.greedy = a.greedy;
+    f.y = a.y;
+    f.q_lse = a.q_lse;
+    f.q_tok = a.q_tok;
+    f.dev_status = a.dev_status;
+    cudaLaunchConfig_t fcfg = {};
+    const long long warps = (long long)a.R * a.gamma;
+    fcfg.gridDim = dim3((unsigned)((warps * 32 + 255) / 256));
+    fcfg.blockDim = dim3(256);
+    fcfg.stream = stream;
+    fcfg.attrs = attr;
+    fcfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&fcfg, draft_finalize_kernel, f) != cudaSuccess) return DSPARK_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 
@@ -876,16 +882,16 @@ int launch_residual_tc(const ResidualTcArgs& a, cudaStream_t stream) {
     EncodeTiled enc = encoder();
     if (!enc) return DSPARK_ERR_CUDA;
     TcParams p;
-    CUtensorMap tm_w2, tm_u, tm_h;
+    CUtensorMap tm_w2, tm_u;
     int grid = 0, n_sm = 0;
     size_t smem = 0;
-    const int st = prepare(enc, a.U, a.W1, a.W2, a.R, a.gamma, a.V, a.rank, a.ws, true, p, tm_w2, tm_u, tm_h, grid,
-                           smem, n_sm);
+    const int st = prepare(enc, a.U, a.W1, a.W2, a.R, a.gamma, a.V, a.rank, p, tm_w2, tm_u, grid, smem, n_sm);
     if (st != DSPARK_OK) return st;
-    const TcLayout L = tc_layout(a.R, a.rank, true);
-    ResRow* rows = reinterpret_cast<ResRow*>(static_cast<unsigned char*>(a.ws) + L.rows);
+    const TcLayout L = tc_layout(a.R, a.gamma, true);
+    unsigned char* w = static_cast<unsigned char*>(a.ws);
+    ResRow* rows = reinterpret_cast<ResRow*>(w + L.rows);
+    p.keys = reinterpret_cast<unsigned long long*>(w + L.keys);
     p.anchor = a.anchor;
-    p.y = const_cast<int32_t*>(a.y);
     p.seeds = a.seeds;
     p.dev_status = a.dev_status;
     p.cycle = a.cycle;
@@ -893,19 +899,16 @@ int launch_residual_tc(const ResidualTcArgs& a, cudaStream_t stream) {
     p.greedy = 0;
     p.target = a.target;
     p.rows = rows;
-    p.out_tokens = a.out_tokens;
+    p.k = 0;
     if (cudaFuncSetAttribute(markov_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return DSPARK_ERR_CUDA;
-    if (cudaMemsetAsync(p.gcount, 0, sizeof(int) * (size_t)p.nb * (kMaxGroups + 1), stream) != cudaSuccess)
+    if (cudaMemsetAsync(p.keys, 0, sizeof(unsigned long long) * L.n_keys, stream) != cudaSuccess)
         return DSPARK_ERR_CUDA;
-    {
-        const long long chunks = (long long)a.R * (a.rank >> 3);
-        const int blocks = (int)std::min<long long>((chunks + 255) / 256, 4LL * n_sm);
-        residual_prep_kernel<<<blocks, 256, 0, stream>>>(a, rows, p.H);
-    }
-    p.k = 0;
-    markov_tc_kernel<true><<<grid, kThreads, smem, stream>>>(tm_w2, tm_u, tm_h, p);
+    const int blocks = (a.R + 255) / 256;
+    residual_prep_kernel<<<blocks, 256, 0, stream>>>(a, rows);
+    markov_tc_kernel<true><<<grid, kThreads, smem, stream>>>(tm_w2, tm_u, p);
+    residual_finalize_kernel<<<blocks, 256, 0, stream>>>(rows, p.keys, a.R, a.gamma, a.out_tokens, a.dev_status);
     return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 

@@ -46,7 +46,7 @@ struct ResidualTcArgs {
 };
 
 bool draft_tc_supported(int u_dtype, int w_dtype, int R, int V, int rank);
-size_t draft_tc_workspace(int R, int V, int rank);
+size_t draft_tc_workspace(int R, int gamma, int rank);
 int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream);
 
 size_t residual_tc_workspace(int R, int rank);

@@ -48,19 +48,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete may be suspended
+// for up to hint_ns (it resumes as soon as the phase completes), so a long wait
+// does not keep the warp scheduler busy polling.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase of parity `parity` to complete, at most limit_ns.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           uint64_t limit_ns) {
+    constexpr uint32_t kSleepNs = 20000;
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63) == 0) {
-            if (*abort_flag) return false;
-            if (global_ns() - t0 > limit_ns) {
-                *abort_flag = 1;
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > limit_ns) {
+            *abort_flag = 1;
+            return false;
         }
     }
 }
