@@ -19,23 +19,31 @@
 //             then the extra token is drawn from max(0, p - q), or from p after
 //             full acceptance.
 //
-// Persistent, one CTA per SM, 18 warps:
-//   A (M = 128 requests x K = rank) = rows W1[prev], gathered by the epilogue
-//     warps straight into 128-byte-swizzled shared memory at the start of the
-//     launch and resident for it;
+// Persistent, one CTA per SM, 19 warps:
+//   A (M = 128 requests x K = rank) = rows W1[prev], gathered once per launch
+//     into a workspace matrix H by a small kernel (spread over many SMs: the
+//     rows are scattered over W1's pages), loaded by TMA into 128-byte-swizzled
+//     shared memory and resident for the launch;
 //   B (N = 128 vocabulary rows x K = rank) = W2 tiles streamed by TMA through a
 //     ring of 16 KB stages; the next tile's boxes are prefetched into L2 one
 //     tile ahead so the ring only has to cover L2 latency;
 //   D = A . B^T in fp32 tensor memory, two 128-column buffers so the epilogue
 //     of one vocabulary tile overlaps the MMAs of the next;
-//   epilogue (16 warps; thread = one request x 32 vocabulary columns, in two
-//     16-column passes): Gumbel-max draws use the exponential-race form: with
+//   U_k (draft) = the tile's base logits, by TMA into two 16 KB pass buffers
+//     (128 requests x 64 columns, 128-byte-swizzled) one pass ahead of the
+//     epilogue, which adds them to the accumulator;
+//   epilogue (16 warps; thread = one request x 32 vocabulary columns of a
+//     tile, in two 16-column passes, pass h over columns 64 h .. 64 h + 63 of
+//     the tile across the four warps of a lane quadrant): Gumbel-max draws
+//     use the exponential-race form: with
 //     weight w > 0 and E = -log(u), the largest log(w) + Gumbel(u) is the
 //     largest w / E, so a candidate replaces the best when
 //     w * E_best > w_best * E.  Since E >= 1 - u, an entry with
 //     1 - u >= w * E_best / w_best cannot win; that test needs no logarithm
 //     (1 - u comes exactly from the random bits), and only the entries that
-//     pass it take the accurate log and the exact comparison.
+//     pass it take the log (a short series in 1 - u near u = 1, the
+//     special-function log2 elsewhere; relative error about 2e-6) and the
+//     comparison.
 //
 // Cross-CTA results need no merging pass: every CTA folds its winner into one
 // 64-bit key per request and step with atomicMax (order-preserving bits of
@@ -44,10 +52,14 @@
 // next draft step decodes its A rows' tokens from the keys (it is launched
 // as a programmatic dependent and waits for the previous step before reading
 // them, while its producer already streams W2), and one finalize kernel after
-// the last step turns keys and pieces into tokens, q_lse and q(y).
+// the last step turns keys and pieces into tokens, q_lse and q(y).  The chain
+// gather -> step -> gather -> ... -> finalize is launched with programmatic
+// stream serialization: each launch starts as the previous one retires, its
+// producers pull its first W2 and U tiles into L2, and only reading H / the
+// keys waits for the previous launch to complete.
 //
-// Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM owner),
-// warps 2-17 = A gather, then epilogue.  Every mbarrier wait is bounded (2 s);
+// Warp roles: warp 0 = W2/A TMA producer, warp 1 = MMA issuer (and TMEM
+// owner), warp 2 = U TMA producer (draft), warps 3-18 = epilogue.  Every mbarrier wait is bounded (2 s);
 // a timeout aborts the CTA cleanly and reports DSPARK_ERR_TIMEOUT.
 #include <cuda.h>
 
@@ -63,8 +75,10 @@ constexpr int kKB = 64;                       // rank elements per stage (128-by
 constexpr int kTileBytes = 128 * kKB * 2;     // 16 KB: one operand k-block
 constexpr int kEpiWarps = 16;
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kThreads = 64 + kEpiThreads;
-constexpr int kCols = 32;                     // vocabulary columns per epilogue thread
+constexpr int kCtlWarps = 3;                  // W2 producer, MMA issuer, U producer
+constexpr int kThreads = kCtlWarps * 32 + kEpiThreads;
+constexpr int kPassCols = 16;                 // of which one pass handles
+constexpr int kUBufBytes = kM * 64 * 2;       // base logits of one pass: 128 requests x 64 columns
 constexpr int kMaxStages = 8;
 constexpr int kMaxP = 256;                    // CTAs per request block (pieces per request)
 constexpr uint32_t kTmemCols = 256;
@@ -102,6 +116,7 @@ struct TcParams {
     const uint16_t* U;
     const uint16_t* W1;
     unsigned long long* keys;  // draft [gamma][R]; residual [2][R] (residual race, p race)
+    const int32_t* toks;       // draft [R]: the A rows' tokens (-2: no usable predecessor)
     float4* parts;             // draft [gamma][R][P]: (max, sum, winner logit, winner) per CTA
     const uint64_t* seeds;
     int32_t* dev_status;
@@ -119,10 +134,10 @@ struct TcParams {
 struct Bars {
     uint64_t full[kMaxStages], empty[kMaxStages];
     uint64_t tfull[2], tempty[2];
+    uint64_t ufull[2], uempty[2];
     uint64_t afull, mma_done;
     uint32_t tmem_slot;
     int abort_flag;
-    int tok[kM];  // token of each A row: >= 0 a W1 row, -1 zero row, -2 zero row and no result
 };
 
 __device__ __forceinline__ void merge_draft(float& sc, int& ix, float& sa, float& m, float& su, float sc2, int ix2,
@@ -183,6 +198,23 @@ __device__ __forceinline__ float one_plus_complement(uint32_t x) {
     return __uint_as_float((x >> 9) ^ 0x3FFFFFFFu);
 }
 
+// E = -ln(u) for u = uniform_from_bits(x), with relative error below about
+// 2e-6, without a branch: for u near 1 from d = 1 - u (exact from the bits) by
+// the series d + d^2/2 + ... + d^5/5 (truncation below d^5 / 6 relative for
+// d < 1/16), else from the special-function unit's log2 (absolute error about
+// 2^-22 on |log2 u| >= 0.09).
+__device__ __forceinline__ float neg_log_uniform(uint32_t x) {
+    const float d = (__uint_as_float((x >> 9) ^ 0x3FFFFFFFu) - 1.0f) + 0x1p-24f;
+    const float series = d * fmaf(d, fmaf(d, fmaf(d, fmaf(d, 0.2f, 0.25f), 1.0f / 3.0f), 0.5f), 1.0f);
+    float l2;
+    asm("lg2.approx.f32 %0, %1;" : "=f"(l2) : "f"(uniform_from_bits(x)));
+    return d < 0.0625f ? series : -l2 * kLn2F;
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& x, int j) {
+    return j == 0 ? x.x : (j == 1 ? x.y : (j == 2 ? x.z : x.w));
+}
+
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                      reinterpret_cast<uint64_t>(map)),
@@ -201,14 +233,48 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
-__device__ __forceinline__ void epilogue_barrier() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+// Copies W1[t] (zeros for t < 0) into row r of H: one warp, 16-byte pieces.
+__device__ __forceinline__ void copy_w1_row(const uint16_t* W1, int t, int rank, uint16_t* H, int r, int lane) {
+    const int cpr = rank >> 3;
+    const uint4* src = reinterpret_cast<const uint4*>(W1 + (size_t)(t < 0 ? 0 : t) * rank);
+    uint4* dst = reinterpret_cast<uint4*>(H + (size_t)r * rank);
+    for (int c = lane; c < cpr; c += 32) dst[c] = t >= 0 ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
 }
 
-// Per request after the verify decisions: what the residual launch draws and
-// the token whose W1 row is its A row (the rejected position's predecessor).
-__global__ void __launch_bounds__(256) residual_prep_kernel(ResidualTcArgs a, ResRow* rows) {
-    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+// The A rows of draft step k, one small CTA per request (the rows lie on
+// scattered pages of W1; one row per SM keeps the address translations of the
+// gather in parallel): the predecessor token (the anchor at k = 0, else the
+// winner of step k - 1 decoded from its key; -1 no anchor, -2 unusable: the
+// step then computes nothing for the request) and its W1 row.
+constexpr int kGatherThreads = 64;
+__global__ void __launch_bounds__(kGatherThreads) gather_a_rows_kernel(const uint16_t* W1, const int32_t* anchor,
+                                                                       const unsigned long long* prev_keys, int k,
+                                                                       int R, int V, int rank, uint16_t* H,
+                                                                       int32_t* toks) {
+    griddep_launch_dependents();
+    griddep_wait();  // the previous step's keys
+    const int r = blockIdx.x;
+    int t;
+    if (k == 0) {
+        const int a = anchor[r];
+        t = a >= V ? -2 : (a < 0 ? -1 : a);
+    } else {
+        const unsigned long long key = prev_keys[r];
+        t = key ? key_index(key) : -2;
+    }
+    if (threadIdx.x == 0) toks[r] = t;
+    const int cpr = rank >> 3;
+    const uint4* src = reinterpret_cast<const uint4*>(W1 + (size_t)(t < 0 ? 0 : t) * rank);
+    uint4* dst = reinterpret_cast<uint4*>(H + (size_t)r * rank);
+    for (int c = threadIdx.x; c < cpr; c += kGatherThreads) dst[c] = t >= 0 ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Per request after the verify decisions: what the residual launch draws, and
+// its A row W1[prev] of the rejected position (zeros for a bonus draw).  One
+// warp per request.
+__global__ void __launch_bounds__(256) residual_prep_kernel(ResidualTcArgs a, ResRow* rows, uint16_t* H) {
+    const int r = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
     if (r >= a.R) return;
     const VerifyJob job = a.jobs[r];
     const int mode = a.valid[r] ? job.mode : 0;
@@ -226,17 +292,19 @@ __global__ void __launch_bounds__(256) residual_prep_kernel(ResidualTcArgs a, Re
     w.q_lse2 = mode == 1 ? a.q_lse[(size_t)r * a.gamma + job.pos] * kLog2eF : 0.0f;
     w.prev = prev;
     w.pad = 0.0f;
-    rows[r] = w;
+    if (lane == 0) rows[r] = w;
+    copy_w1_row(static_cast<const uint16_t*>(a.W1), prev, a.rank, H, r, lane);
 }
 
 template <bool kRes>
 __global__ void __launch_bounds__(kThreads, 1)
 markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_u,
-                 const TcParams p) {
+                 const __grid_constant__ CUtensorMap tm_h, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
-    uint8_t* sB = sA + p.nkb * kTileBytes;
+    uint8_t* sU = sA + p.nkb * kTileBytes;          // draft: two pass buffers of base logits
+    uint8_t* sB = sU + (kRes ? 0 : 2 * kUBufBytes);
     Bars& bar = *reinterpret_cast<Bars*>(sB + p.n_stages * kTileBytes);
     volatile int* abort_flag = &bar.abort_flag;
 
@@ -249,7 +317,8 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) { tc::mbar_init(&bar.full[s], 1); tc::mbar_init(&bar.empty[s], 1); }
         for (int a = 0; a < 2; ++a) { tc::mbar_init(&bar.tfull[a], 1); tc::mbar_init(&bar.tempty[a], kEpiWarps); }
-        tc::mbar_init(&bar.afull, kEpiWarps);
+        for (int a = 0; a < 2; ++a) { tc::mbar_init(&bar.ufull[a], 1); tc::mbar_init(&bar.uempty[a], kEpiWarps); }
+        tc::mbar_init(&bar.afull, 1);
         tc::mbar_init(&bar.mma_done, 1);
         bar.abort_flag = 0;
         tc::fence_barrier_init();
@@ -261,6 +330,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
     if (warp == 0 && lane == 0) {
         tc::prefetch_tmap(&tm_w2);
         if (!kRes) tc::prefetch_tmap(&tm_u);
+        tc::prefetch_tmap(&tm_h);
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -277,14 +347,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        // W2 and U are inputs no launch of this library writes, so streaming
-        // them may start before the previous draft step has finished.
+        // W2 and U are inputs no launch of this library writes: the first tiles
+        // are requested into L2 before waiting for the previous launch, which
+        // wrote H; A is loaded first, then the W2 ring.
         if (lane == 0) {
-            int s = 0;
-            uint32_t ph = 0;
-            int last_phase[kMaxStages];
-            for (int i = 0; i < kMaxStages; ++i) last_phase[i] = -1;
-            bool ok = true;
             for (int i = 0; i < 2 && i < n_local; ++i) {
                 const int t = cidx + i * p.P;
                 for (int q = 0; q < p.nkb; ++q) tma_prefetch_l2_2d(&tm_w2, q * kKB, t * kNV);
@@ -293,33 +359,45 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                     tc::tma_prefetch_l2_3d(&tm_u, t * kNV + kKB, p.k, row0);
                 }
             }
-            for (int i = 0; ok && i < n_local; ++i) {
+            const int n_loads = n_local * p.nkb;  // W2 stage loads, tile-major
+            int issued = 0;
+            bool ok = true;
+            // the stage of load l is l % S, used for the (l / S)-th time
+            auto issue = [&](int l) {
+                const int s = l % S, i = l / p.nkb, kb = l - i * p.nkb;
                 const int t = cidx + i * p.P;
-                for (int kb = 0; kb < p.nkb; ++kb) {
-                    if (!tc::mbar_wait(&bar.empty[s], ph ^ 1u, abort_flag, kWaitNs)) { ok = false; break; }
-                    tc::mbar_arrive_expect_tx(&bar.full[s], kTileBytes);
-                    tc::tma_load_2d(sB + s * kTileBytes, &tm_w2, &bar.full[s], kb * kKB, t * kNV);
-                    last_phase[s] = (int)ph;
-                    if (++s == S) { s = 0; ph ^= 1u; }
-                    // once this tile's first loads are out, pull the next tile into L2
-                    if (kb == min(S, p.nkb) - 1 && i + 1 < n_local) {
-                        const int tn = t + p.P;
-                        for (int q = 0; q < p.nkb; ++q) tma_prefetch_l2_2d(&tm_w2, q * kKB, tn * kNV);
-                        if (!kRes) {
-                            tc::tma_prefetch_l2_3d(&tm_u, tn * kNV, p.k, row0);
-                            tc::tma_prefetch_l2_3d(&tm_u, tn * kNV + kKB, p.k, row0);
-                        }
+                tc::mbar_arrive_expect_tx(&bar.full[s], kTileBytes);
+                tc::tma_load_2d(sB + s * kTileBytes, &tm_w2, &bar.full[s], kb * kKB, t * kNV);
+                // once a tile's first ring of loads is out, pull the next tile into L2
+                if (kb == min(S, p.nkb) - 1 && i + 1 < n_local) {
+                    const int tn = t + p.P;
+                    for (int q = 0; q < p.nkb; ++q) tma_prefetch_l2_2d(&tm_w2, q * kKB, tn * kNV);
+                    if (!kRes) {
+                        tc::tma_prefetch_l2_3d(&tm_u, tn * kNV, p.k, row0);
+                        tc::tma_prefetch_l2_3d(&tm_u, tn * kNV + kKB, p.k, row0);
                     }
                 }
+            };
+            griddep_wait();
+            // A: the block's H rows, resident for the launch
+            tc::mbar_arrive_expect_tx(&bar.afull, (uint32_t)(p.nkb * kTileBytes));
+            for (int kb = 0; kb < p.nkb; ++kb) tc::tma_load_2d(sA + kb * kTileBytes, &tm_h, &bar.afull, kb * kKB, row0);
+            for (; issued < n_loads; ++issued) {
+                const int s = issued % S;
+                const uint32_t ph = (uint32_t)((issued / S) & 1);
+                if (!tc::mbar_wait(&bar.empty[s], ph ^ 1u, abort_flag, kWaitNs)) { ok = false; break; }
+                issue(issued);
             }
-            // after an abort, the copies this thread issued must land before the CTA exits
-            if (*abort_flag) {
-                int dummy = 0;
-                volatile int* no_abort = &dummy;
-                for (int q = 0; q < S; ++q)
-                    if (last_phase[q] >= 0) tc::mbar_wait(&bar.full[q], (uint32_t)last_phase[q], no_abort, kWaitNs);
+            // the copies this thread issued must land before the CTA exits
+            int dummy = 0;
+            volatile int* no_abort = &dummy;
+            tc::mbar_wait(&bar.afull, 0, no_abort, kWaitNs);
+            if (!ok) {
+                for (int l = max(0, issued - S); l < issued; ++l)
+                    tc::mbar_wait(&bar.full[l % S], (uint32_t)((l / S) & 1), no_abort, kWaitNs);
             }
         }
+        __syncwarp();  // the warp reconverges before the CTA-wide barrier below
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -356,77 +434,47 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
             volatile int* no_abort = &dummy;
             tc::mbar_wait(&bar.mma_done, 0, no_abort, kWaitNs);
         }
-    } else {
-        // ------------------------------------------------------------ A gather
-        const int et = threadIdx.x - 64;  // 0..511
-        // the previous draft step's winners are read after this
-        griddep_wait();
-        if (et < kM) {
-            const int r = row0 + et;
-            int t = -1;
-            if (r < p.R) {
-                if (kRes) {
-                    const ResRow ri = p.rows[r];
-                    t = ri.mode == 0 ? -2 : ri.prev;
-                } else if (p.k == 0) {
-                    const int a = p.anchor[r];
-                    t = a >= p.V ? -2 : (a < 0 ? -1 : a);
-                } else {
-                    const unsigned long long key = __ldcg(p.keys + (size_t)(p.k - 1) * p.R + r);
-                    t = key ? key_index(key) : -2;
-                }
-            } else {
-                t = -2;
-            }
-            bar.tok[et] = t;
-        }
-        epilogue_barrier();
-        {
-            // A row m, k-block kb, 16-byte chunk j sits at chunk j ^ (m & 7) of its
-            // 128-byte row: the layout a 128-byte-swizzled TMA box would give.
-            const int cpr = p.rank >> 3;
-            const int total = kM * cpr;
-            for (int e0 = et; e0 < total; e0 += 8 * kEpiThreads) {
-                uint4 v[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int e = e0 + u * kEpiThreads;
-                    v[u] = make_uint4(0u, 0u, 0u, 0u);
-                    if (e < total) {
-                        const int m = e / cpr, c = e - m * cpr;
-                        const int t = bar.tok[m];
-                        if (t >= 0) v[u] = __ldg(reinterpret_cast<const uint4*>(p.W1 + (size_t)t * p.rank) + c);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int e = e0 + u * kEpiThreads;
-                    if (e < total) {
-                        const int m = e / cpr, c = e - m * cpr;
-                        const int off = (c >> 3) * kTileBytes + m * 128 + (((c & 7) ^ (m & 7)) << 4);
-                        *reinterpret_cast<uint4*>(sA + off) = v[u];
-                    }
-                }
-            }
-        }
-        // the tensor cores read A through the async proxy
-        tc::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&bar.afull);
-
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ U producer
+        // Draft: the base logits U_k of pass n (tile n / 2, columns 64 (n % 2) ..
+        // + 63 of the tile, all 128 requests) into pass buffer n % 2, one pass ahead
+        // of the epilogue; U is an input, so no wait on the previous launch.
+        if (!kRes && lane == 0) {
+            const int n_pass = 2 * n_local;
+            int n = 0;
+            for (; n < n_pass; ++n) {
+                const int b = n & 1;
+                const uint32_t use = (uint32_t)(n >> 1);
+                if (!tc::mbar_wait(&bar.uempty[b], (use & 1u) ^ 1u, abort_flag, kWaitNs)) break;
+                tc::mbar_arrive_expect_tx(&bar.ufull[b], (uint32_t)kUBufBytes);
+                tc::tma_load_3d(sU + b * kUBufBytes, &tm_u, &bar.ufull[b], (cidx + (n >> 1) * p.P) * kNV + 64 * b, p.k,
+                                row0);
+            }
+            // the copies this thread issued must land before the CTA exits
+            int dummy = 0;
+            volatile int* no_abort = &dummy;
+            for (int l = max(0, n - 2); l < n; ++l)
+                tc::mbar_wait(&bar.ufull[l & 1], (uint32_t)((l >> 1) & 1), no_abort, kWaitNs);
+        }
+        __syncwarp();
+    } else {
+        // the A rows' tokens (draft) were written by the previous launch
+        griddep_wait();
         // ------------------------------------------------------------ epilogue
-        const int ew = warp - 2;           // 0..15
+        const int ew = warp - kCtlWarps;   // 0..15
         const int quad = warp & 3;         // TMEM lane quadrant this warp may read
-        const int quarter = ew >> 2;       // which 32 of the tile's 128 columns
+        const int quarter = ew >> 2;       // pass h covers columns 64 h + 16 quarter .. + 15 of a tile
         const int m = quad * 32 + lane;
         const int rr = row0 + m;
-        row_ok = bar.tok[m] != -2;
+        if (kRes) row_ok = rr < p.R && p.rows[rr].mode != 0;
+        else row_ok = rr < p.R && p.toks[rr] != -2;
         ResRow rinfo;
         rinfo.mode = 0; rinfo.pos = 0; rinfo.trow = 0; rinfo.w3 = 0; rinfo.lse2_p = 0.0f; rinfo.q_lse2 = 0.0f;
         if (kRes && row_ok) rinfo = p.rows[rr];
         const bool sampling = kRes || !p.greedy;
-        PhiloxKey K;
-        if (sampling) K = philox_key(row_ok ? p.seeds[rr] : 0ull);
+        const uint64_t seed = (sampling && row_ok) ? p.seeds[rr] : 0ull;
+        const uint32_t key0 = (uint32_t)(seed & 0xFFFFFFFFu), key1 = (uint32_t)(seed >> 32);
         const uint32_t w3 = kRes ? rinfo.w3 : ctr_word3(p.cycle, kDraftGumbel);
         const int pos = kRes ? rinfo.pos : p.k;
         const bool with_u = !kRes || rinfo.mode == 1;
@@ -441,143 +489,188 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         float bw = 0.0f, bE = 1.0f, bp = 0.0f, bEp = 1.0f;
         float rho = INFINITY, rho_p = INFINITY;
         int ia = INT_MAX;
+        // residual: the 16 base logits (bf16 pairs) of the request's rejected row at v
+        auto load_u = [&](int v, uint32_t(&dst)[8]) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const uint4 q = (row_ok && v + 8 * j < p.V) ? __ldg(reinterpret_cast<const uint4*>(urow + v) + j)
+                                                             : make_uint4(0u, 0u, 0u, 0u);
+                dst[4 * j + 0] = q.x; dst[4 * j + 1] = q.y; dst[4 * j + 2] = q.z; dst[4 * j + 3] = q.w;
+            }
+        };
+        // draft: this thread's 32 bytes of a pass buffer (row m, 16-byte chunks
+        // 2 quarter and 2 quarter + 1 of the 128-byte-swizzled row)
+        const uint32_t u_off0 = (uint32_t)(m * 128 + (((2 * quarter) ^ (m & 7)) << 4));
+        const uint32_t u_off1 = (uint32_t)(m * 128 + (((2 * quarter + 1) ^ (m & 7)) << 4));
         for (int i = 0; i < n_local; ++i) {
             const int t = cidx + i * p.P;
             const int a = i & 1;
             const uint32_t use = (uint32_t)(i >> 1);
-            const int vq = t * kNV + quarter * kCols;
-            uint32_t uwA[8], uwB[8];
-            if (!kRes) {
-                // base logits of this thread's 32 columns (already in L2), two halves
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const uint4 qa = (row_ok && 8 * j < p.V - vq) ? __ldg(reinterpret_cast<const uint4*>(urow + vq) + j)
-                                                                  : make_uint4(0u, 0u, 0u, 0u);
-                    const uint4 qb = (row_ok && 16 + 8 * j < p.V - vq)
-                                         ? __ldg(reinterpret_cast<const uint4*>(urow + vq) + 2 + j)
-                                         : make_uint4(0u, 0u, 0u, 0u);
-                    uwA[4 * j + 0] = qa.x; uwA[4 * j + 1] = qa.y; uwA[4 * j + 2] = qa.z; uwA[4 * j + 3] = qa.w;
-                    uwB[4 * j + 0] = qb.x; uwB[4 * j + 1] = qb.y; uwB[4 * j + 2] = qb.z; uwB[4 * j + 3] = qb.w;
-                }
-            } else if (row_ok && vq < p.V) {
+            if (kRes && row_ok) {
                 // residual rows differ per request: pull this thread's pieces into L2 now
-                prefetch_l2(trow + vq);
-                if (with_u) prefetch_l2(urow + vq);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int v = t * kNV + 64 * h + kPassCols * quarter;
+                    if (v < p.V) {
+                        prefetch_l2(trow + v);
+                        if (with_u) prefetch_l2(urow + v);
+                    }
+                }
             }
             // warp-uniform wait: every lane waits (acquire), all leave together
             if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.tfull[a], use & 1u, abort_flag, kWaitNs))) break;
             tc::tc_fence_after();
             const uint32_t taddr =
-                tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(a * kNV + quarter * kCols);
+                tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(a * kNV + quarter * kPassCols);
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {
                 float sv[16];
                 __syncwarp();  // lanes that skipped the previous pass rejoin before the aligned load
-                tc::tmem_ld_32x32b_x16<0>(taddr + 16u * h, sv);
+                tc::tmem_ld_32x32b_x16<0>(taddr + 64u * h, sv);
+                uint32_t uw[8];
+                if (!kRes) {
+                    // this pass's base logits, then the buffer goes back to the U producer
+                    // pass buffer h is filled once per tile: its phase parity is i & 1
+                    if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.ufull[h], (uint32_t)(i & 1), abort_flag, kWaitNs))) {
+                        tc::tmem_ld_wait();
+                        break;
+                    }
+                    const uint4 q0 = *reinterpret_cast<const uint4*>(sU + h * kUBufBytes + u_off0);
+                    const uint4 q1 = *reinterpret_cast<const uint4*>(sU + h * kUBufBytes + u_off1);
+                    uw[0] = q0.x; uw[1] = q0.y; uw[2] = q0.z; uw[3] = q0.w;
+                    uw[4] = q1.x; uw[5] = q1.y; uw[6] = q1.z; uw[7] = q1.w;
+                }
                 tc::tmem_ld_wait();
                 if (h == 1) {  // both halves are in registers: hand the accumulator back
                     tc::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(&bar.tempty[a]);
                 }
-                if (!row_ok) continue;
-                const int v0 = vq + 16 * h;
-                const int nvalid = min(16, p.V - v0);
-                if (kRes && with_u) {
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const uint4 q4 = 8 * j < nvalid ? __ldg(reinterpret_cast<const uint4*>(urow + v0) + j)
-                                                        : make_uint4(0u, 0u, 0u, 0u);
-                        uwA[4 * j + 0] = q4.x; uwA[4 * j + 1] = q4.y; uwA[4 * j + 2] = q4.z; uwA[4 * j + 3] = q4.w;
-                    }
-                }
-                if (!kRes || with_u) {
+                const int v0 = t * kNV + 64 * h + kPassCols * quarter;
+                const int nvalid = min(16, p.V - v0);  // the same in the whole warp
+                if (!kRes) {
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
-                        const uint32_t word = (kRes || h == 0) ? uwA[c >> 1] : uwB[c >> 1];
+                        const uint32_t word = uw[c >> 1];
                         const float u = __uint_as_float((c & 1) ? (word & 0xFFFF0000u) : (word << 16));
                         sv[c] = (u + sv[c]) * c2;
                     }
+                    // the values are in registers: the async proxy may overwrite the buffer
+                    tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&bar.uempty[h]);
                 }
-                if (qrow) {  // natural units
-                    const float back = sampling ? kLn2F : 1.0f;
+                if (row_ok && nvalid > 0) {
+                    if constexpr (!kRes) {
+                        if (qrow) {  // natural units
+                            const float back = sampling ? kLn2F : 1.0f;
 #pragma unroll
-                    for (int c = 0; c < 16; c += 4)
-                        if (c < nvalid)
-                            *reinterpret_cast<float4*>(qrow + v0 + c) =
-                                make_float4(sv[c] * back, sv[c + 1] * back, sv[c + 2] * back, sv[c + 3] * back);
-                }
-                if (!kRes && p.greedy) {
-#pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        if (c < nvalid && better(sv[c], v0 + c, part.score, part.idx)) {
-                            part.score = sv[c]; part.idx = v0 + c; part.s_at = sv[c];
+                            for (int c = 0; c < 16; c += 4)
+                                if (c < nvalid)
+                                    *reinterpret_cast<float4*>(qrow + v0 + c) = make_float4(
+                                        sv[c] * back, sv[c + 1] * back, sv[c + 2] * back, sv[c + 3] * back);
                         }
-                    continue;
-                }
-                if constexpr (!kRes) {
-                    // sampling draft in base 2: w = 2^(s2 - m2) relative to the running max
-                    float cm = -INFINITY;
+                        if (p.greedy) {
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        if (c < nvalid) cm = fmaxf(cm, sv[c]);
-                    if (cm > part.m) {
-                        const float sc = ex2(part.m - cm);  // 0 while the max is -inf
-                        part.sum *= sc;
-                        bw *= sc;
-                        part.m = cm;
-                        rho = bE / bw * kRaceSlack;
-                    }
+                            for (int c = 0; c < 16; ++c)
+                                if (c < nvalid && better(sv[c], v0 + c, part.score, part.idx)) {
+                                    part.score = sv[c]; part.idx = v0 + c; part.s_at = sv[c];
+                                }
+                        } else {
+                            // columns past the row end weigh 2^-inf = 0 and never pass the race test
+                            if (nvalid < 16) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint4 wd = philox4x32_10(
-                            make_uint4((uint32_t)((v0 >> 2) + q), (uint32_t)pos, (uint32_t)rr, w3), K);
-                        const uint32_t words[4] = {wd.x, wd.y, wd.z, wd.w};
+                                for (int c = 0; c < 16; ++c)
+                                    if (c >= nvalid) sv[c] = -INFINITY;
+                            }
+                            // sampling draft in base 2: w = 2^(s2 - m2) relative to the running max
+                            float cm = sv[0];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int c = 4 * q + e;
-                            if (c < nvalid) {
+                            for (int c = 1; c < 16; ++c) cm = fmaxf(cm, sv[c]);
+                            if (cm > part.m) {
+                                const float sc = ex2(part.m - cm);  // 0 while the max is -inf
+                                part.sum *= sc;
+                                bw *= sc;
+                                part.m = cm;
+                                rho = bE / bw * kRaceSlack;
+                            }
+                            uint4 x[4];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                x[q] = make_uint4((uint32_t)((v0 >> 2) + q), (uint32_t)pos, (uint32_t)rr, w3);
+                            philox4x32_10_x4(x, key0, key1);
+                            // every weight into the normaliser; entries that may beat the
+                            // running winner marked for the exact test
+                            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                            uint32_t cand = 0;
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) {
+                                const uint32_t wd = word_of(x[c >> 2], c & 3);
                                 const float w = ex2(sv[c] - part.m);
-                                part.sum += w;
-                                if (one_plus_complement(words[e]) < fmaf(w, rho, 1.0f)) {
-                                    const float E = -logf(uniform_from_bits(words[e]));
-                                    if (w * bE > bw * E) {
-                                        bw = w; bE = E; part.idx = v0 + c; part.s_at = sv[c];
-                                        rho = bE / bw * kRaceSlack;
+                                acc[c & 3] += w;
+                                cand |= (one_plus_complement(wd) < fmaf(w, rho, 1.0f)) ? (1u << c) : 0u;
+                            }
+                            part.sum += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                            if (cand) {
+#pragma unroll
+                                for (int c = 0; c < 16; ++c) {
+                                    if (cand & (1u << c)) {
+                                        const float w = ex2(sv[c] - part.m);
+                                        const float E = neg_log_uniform(word_of(x[c >> 2], c & 3));
+                                        if (w * bE > bw * E) {
+                                            bw = w; bE = E; part.idx = v0 + c; part.s_at = sv[c];
+                                            rho = bE / bw * kRaceSlack;
+                                        }
                                     }
                                 }
                             }
                         }
-                    }
-                } else {
-                    float tv[16];
+                    } else {
+                        // residual: target logits (past the row end -inf: p = 0) and,
+                        // for a rejected row, the drafter's base logits
+                        float tv[16];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float4 f = 4 * j < nvalid ? __ldg(reinterpret_cast<const float4*>(trow + v0) + j)
-                                                        : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                        tv[4 * j + 0] = f.x; tv[4 * j + 1] = f.y; tv[4 * j + 2] = f.z; tv[4 * j + 3] = f.w;
-                    }
+                        for (int j = 0; j < 4; ++j) {
+                            const float4 f = 4 * j < nvalid ? __ldg(reinterpret_cast<const float4*>(trow + v0) + j)
+                                                            : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                            tv[4 * j + 0] = f.x; tv[4 * j + 1] = f.y; tv[4 * j + 2] = f.z; tv[4 * j + 3] = f.w;
+                        }
+                        if (with_u) {
+                            uint32_t uw[8];
+                            load_u(v0, uw);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint4 wd = philox4x32_10(
-                            make_uint4((uint32_t)((v0 >> 2) + q), (uint32_t)pos, (uint32_t)rr, w3), K);
-                        const uint32_t words[4] = {wd.x, wd.y, wd.z, wd.w};
+                            for (int c = 0; c < 16; ++c) {
+                                const uint32_t word = uw[c >> 1];
+                                const float u = __uint_as_float((c & 1) ? (word & 0xFFFF0000u) : (word << 16));
+                                sv[c] = (u + sv[c]) * c2;
+                            }
+                        }
+                        uint4 x[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int c = 4 * q + e;
-                            if (c < nvalid) {
-                                const float pv = ex2(fmaf(tv[c], c2, -rinfo.lse2_p));
-                                const float res = with_u ? pv - ex2(sv[c] - rinfo.q_lse2) : 0.0f;
-                                const float f = one_plus_complement(words[e]);
-                                const bool try_p = f < fmaf(pv, rho_p, 1.0f);
-                                const bool try_r = res > 0.0f && f < fmaf(res, rho, 1.0f);
-                                if (try_p || try_r) {
-                                    const float E = -logf(uniform_from_bits(words[e]));
-                                    if (try_p && pv * bEp > bp * E) {
+                        for (int q = 0; q < 4; ++q)
+                            x[q] = make_uint4((uint32_t)((v0 >> 2) + q), (uint32_t)pos, (uint32_t)rr, w3);
+                        philox4x32_10_x4(x, key0, key1);
+                        uint32_t cand_p = 0, cand_r = 0;
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const float f = one_plus_complement(word_of(x[c >> 2], c & 3));
+                            const float pv = ex2(fmaf(tv[c], c2, -rinfo.lse2_p));
+                            const float res = with_u ? pv - ex2(sv[c] - rinfo.q_lse2) : 0.0f;
+                            cand_p |= (f < fmaf(pv, rho_p, 1.0f)) ? (1u << c) : 0u;
+                            cand_r |= (res > 0.0f && f < fmaf(res, rho, 1.0f)) ? (1u << c) : 0u;
+                        }
+                        if (cand_p | cand_r) {
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) {
+                                if ((cand_p | cand_r) & (1u << c)) {
+                                    const float pv = ex2(fmaf(tv[c], c2, -rinfo.lse2_p));
+                                    const float res = with_u ? pv - ex2(sv[c] - rinfo.q_lse2) : 0.0f;
+                                    const float E = neg_log_uniform(word_of(x[c >> 2], c & 3));
+                                    if ((cand_p & (1u << c)) && pv * bEp > bp * E) {
                                         bp = pv; bEp = E; ia = v0 + c;
                                         rho_p = bEp / bp * kRaceSlack;
                                     }
-                                    if (try_r && res * bE > bw * E) {
+                                    if ((cand_r & (1u << c)) && res * bE > bw * E) {
                                         bw = res; bE = E; part.idx = v0 + c;
                                         rho = bE / bw * kRaceSlack;
                                     }
@@ -604,9 +697,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
     // ---------------------------------------------------------------- per-CTA result
     __syncthreads();
     TcPartial* scratch = reinterpret_cast<TcPartial*>(sB);  // W2 stages are drained
-    if (warp >= 6) {
+    if (warp >= kCtlWarps + 4) {
         const int m = (warp & 3) * 32 + lane;
-        const int qtr = (warp - 2) >> 2;  // 1..3
+        const int qtr = (warp - kCtlWarps) >> 2;  // 1..3
         scratch[(qtr - 1) * kM + m] = part;
     }
     __syncthreads();
@@ -618,7 +711,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         if (threadIdx.x == 0) report(p.dev_status, DSPARK_ERR_TIMEOUT);
         return;
     }
-    if (warp >= 2 && warp < 6 && row_ok) {
+    if (warp >= kCtlWarps && warp < kCtlWarps + 4 && row_ok) {
         const int m = (warp & 3) * 32 + lane;
         const int rr = row0 + m;
 #pragma unroll
@@ -731,16 +824,18 @@ EncodeTiled encoder() {
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Workspace: winner keys, then (draft) the per-CTA normaliser pieces or
-// (residual) the per-request rows.
+// Workspace: winner keys, the A matrix H, then (draft) the A rows' tokens and
+// the per-CTA normaliser pieces or (residual) the per-request rows.
 struct TcLayout {
-    size_t keys, n_keys, parts, rows, total;
+    size_t keys, n_keys, h, toks, parts, rows, total;
 };
-TcLayout tc_layout(int R, int gamma, bool residual) {
+TcLayout tc_layout(int R, int gamma, int rank, bool residual) {
     TcLayout L;
     size_t off = 0;
     L.n_keys = residual ? 2 * (size_t)R : (size_t)gamma * R;
     L.keys = off; off += up256(sizeof(unsigned long long) * L.n_keys);
+    L.h = off; off += up256((size_t)R * rank * 2);
+    L.toks = off; off += residual ? 0 : up256(sizeof(int32_t) * (size_t)R);
     L.parts = off; off += residual ? 0 : up256(sizeof(float4) * (size_t)gamma * R * kMaxP);
     L.rows = off; off += residual ? up256(sizeof(ResRow) * (size_t)R) : 0;
     L.total = off;
@@ -759,15 +854,16 @@ bool encode_2d_bf16(EncodeTiled enc, CUtensorMap* m, const void* base, int inner
 
 // Shared launch setup of both modes: device limits, stage count, tensor maps,
 // the common parameter block.  Returns DSPARK_OK or an error status.
-int prepare(EncodeTiled enc, const void* U, const void* W1, const void* W2, int R, int gamma, int V, int rank,
-            TcParams& p, CUtensorMap& tm_w2, CUtensorMap& tm_u, int& grid, size_t& smem, int& n_sm) {
+int prepare(EncodeTiled enc, const void* U, const void* W1, const void* W2, const void* H, int R, int gamma, int V,
+            int rank, bool residual, TcParams& p, CUtensorMap& tm_w2, CUtensorMap& tm_u, CUtensorMap& tm_h,
+            int& grid, size_t& smem, int& n_sm) {
     int dev = 0, max_smem = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return DSPARK_ERR_CUDA;
     const int nkb = rank / kKB;
-    const size_t fixed = 1024 + (size_t)nkb * kTileBytes + sizeof(Bars);
+    const size_t fixed = 1024 + (size_t)nkb * kTileBytes + (residual ? 0 : 2 * (size_t)kUBufBytes) + sizeof(Bars);
     if ((size_t)max_smem < fixed + 2 * kTileBytes) return DSPARK_ERR_UNSUPPORTED;
     const int n_stages = (int)std::min<size_t>(kMaxStages, ((size_t)max_smem - fixed) / kTileBytes);
     smem = fixed + (size_t)n_stages * kTileBytes;
@@ -775,6 +871,7 @@ int prepare(EncodeTiled enc, const void* U, const void* W1, const void* W2, int 
     if ((size_t)n_stages * kTileBytes < (size_t)3 * kM * sizeof(TcPartial)) return DSPARK_ERR_UNSUPPORTED;
 
     if (!encode_2d_bf16(enc, &tm_w2, W2, rank, V, kNV)) return DSPARK_ERR_CUDA;
+    if (!encode_2d_bf16(enc, &tm_h, H, rank, R, kM)) return DSPARK_ERR_CUDA;
     {
         const cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)gamma, (cuuint64_t)R};
         const cuuint64_t strides[2] = {(cuuint64_t)V * 2, (cuuint64_t)gamma * V * 2};
@@ -808,23 +905,27 @@ bool draft_tc_supported(int u_dtype, int w_dtype, int R, int V, int rank) {
            rank <= 512 && V % 8 == 0 && V >= 8;
 }
 
-size_t draft_tc_workspace(int R, int gamma, int) { return tc_layout(R, gamma, false).total; }
+size_t draft_tc_workspace(int R, int gamma, int rank) { return tc_layout(R, gamma, rank, false).total; }
 
-size_t residual_tc_workspace(int R, int) { return tc_layout(R, 0, true).total; }
+size_t residual_tc_workspace(int R, int rank) { return tc_layout(R, 0, rank, true).total; }
 
 int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream) {
     EncodeTiled enc = encoder();
     if (!enc) return DSPARK_ERR_CUDA;
     if (a.q_logits && (reinterpret_cast<uintptr_t>(a.q_logits) & 15)) return DSPARK_ERR_UNSUPPORTED;
+    const TcLayout L = tc_layout(a.R, a.gamma, a.rank, false);
+    unsigned char* w = static_cast<unsigned char*>(a.ws);
+    uint16_t* H = reinterpret_cast<uint16_t*>(w + L.h);
+    int32_t* toks = reinterpret_cast<int32_t*>(w + L.toks);
     TcParams p;
-    CUtensorMap tm_w2, tm_u;
+    CUtensorMap tm_w2, tm_u, tm_h;
     int grid = 0, n_sm = 0;
     size_t smem = 0;
-    const int st = prepare(enc, a.U, a.W1, a.W2, a.R, a.gamma, a.V, a.rank, p, tm_w2, tm_u, grid, smem, n_sm);
+    const int st =
+        prepare(enc, a.U, a.W1, a.W2, H, a.R, a.gamma, a.V, a.rank, false, p, tm_w2, tm_u, tm_h, grid, smem, n_sm);
     if (st != DSPARK_OK) return st;
-    const TcLayout L = tc_layout(a.R, a.gamma, false);
-    unsigned char* w = static_cast<unsigned char*>(a.ws);
     p.keys = reinterpret_cast<unsigned long long*>(w + L.keys);
+    p.toks = toks;
     p.parts = reinterpret_cast<float4*>(w + L.parts);
     p.anchor = a.anchor;
     p.seeds = a.seeds;
@@ -838,10 +939,10 @@ int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream) {
         return DSPARK_ERR_CUDA;
     if (cudaMemsetAsync(p.keys, 0, sizeof(unsigned long long) * L.n_keys, stream) != cudaSuccess)
         return DSPARK_ERR_CUDA;
-    // Step 0 waits for everything before it on the stream.  Steps 1.. and the
-    // finalize are programmatic dependents of the launch before them: they may
-    // start as its CTAs retire and wait (griddepcontrol) before reading its
-    // results; the only data they touch earlier are W2 and U.
+    // gather 0 waits for everything before it on the stream.  Every later launch
+    // is a programmatic dependent of the one before: it may start as that one
+    // retires and waits (griddepcontrol) before reading its results; the only
+    // data read earlier are W2 and U.
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -851,10 +952,21 @@ int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream) {
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchConfig_t gcfg = {};
+    gcfg.gridDim = dim3((unsigned)a.R);
+    gcfg.blockDim = dim3(kGatherThreads);
+    gcfg.stream = stream;
+    gcfg.attrs = attr;
     for (int k = 0; k < a.gamma; ++k) {
+        gcfg.numAttrs = k == 0 ? 0 : 1;
+        const unsigned long long* prev_keys = k == 0 ? nullptr : p.keys + (size_t)(k - 1) * a.R;
+        if (cudaLaunchKernelEx(&gcfg, gather_a_rows_kernel, p.W1, a.anchor, prev_keys, k, a.R, a.V, a.rank, H,
+                               toks) != cudaSuccess)
+            return DSPARK_ERR_CUDA;
         p.k = k;
-        cfg.numAttrs = k == 0 ? 0 : 1;
-        if (cudaLaunchKernelEx(&cfg, markov_tc_kernel<false>, tm_w2, tm_u, p) != cudaSuccess) return DSPARK_ERR_CUDA;
+        if (cudaLaunchKernelEx(&cfg, markov_tc_kernel<false>, tm_w2, tm_u, tm_h, p) != cudaSuccess)
+            return DSPARK_ERR_CUDA;
     }
     DraftFinalize f;
     f.keys = p.keys;
@@ -881,14 +993,16 @@ int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream) {
 int launch_residual_tc(const ResidualTcArgs& a, cudaStream_t stream) {
     EncodeTiled enc = encoder();
     if (!enc) return DSPARK_ERR_CUDA;
+    const TcLayout L = tc_layout(a.R, a.gamma, a.rank, true);
+    unsigned char* w = static_cast<unsigned char*>(a.ws);
+    uint16_t* H = reinterpret_cast<uint16_t*>(w + L.h);
     TcParams p;
-    CUtensorMap tm_w2, tm_u;
+    CUtensorMap tm_w2, tm_u, tm_h;
     int grid = 0, n_sm = 0;
     size_t smem = 0;
-    const int st = prepare(enc, a.U, a.W1, a.W2, a.R, a.gamma, a.V, a.rank, p, tm_w2, tm_u, grid, smem, n_sm);
+    const int st =
+        prepare(enc, a.U, a.W1, a.W2, H, a.R, a.gamma, a.V, a.rank, true, p, tm_w2, tm_u, tm_h, grid, smem, n_sm);
     if (st != DSPARK_OK) return st;
-    const TcLayout L = tc_layout(a.R, a.gamma, true);
-    unsigned char* w = static_cast<unsigned char*>(a.ws);
     ResRow* rows = reinterpret_cast<ResRow*>(w + L.rows);
     p.keys = reinterpret_cast<unsigned long long*>(w + L.keys);
     p.anchor = a.anchor;
@@ -905,10 +1019,10 @@ int launch_residual_tc(const ResidualTcArgs& a, cudaStream_t stream) {
         return DSPARK_ERR_CUDA;
     if (cudaMemsetAsync(p.keys, 0, sizeof(unsigned long long) * L.n_keys, stream) != cudaSuccess)
         return DSPARK_ERR_CUDA;
-    const int blocks = (a.R + 255) / 256;
-    residual_prep_kernel<<<blocks, 256, 0, stream>>>(a, rows);
-    markov_tc_kernel<true><<<grid, kThreads, smem, stream>>>(tm_w2, tm_u, p);
-    residual_finalize_kernel<<<blocks, 256, 0, stream>>>(rows, p.keys, a.R, a.gamma, a.out_tokens, a.dev_status);
+    residual_prep_kernel<<<(unsigned)((a.R * 32LL + 255) / 256), 256, 0, stream>>>(a, rows, H);
+    markov_tc_kernel<true><<<grid, kThreads, smem, stream>>>(tm_w2, tm_u, tm_h, p);
+    residual_finalize_kernel<<<(a.R + 255) / 256, 256, 0, stream>>>(rows, p.keys, a.R, a.gamma, a.out_tokens,
+                                                                     a.dev_status);
     return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 
