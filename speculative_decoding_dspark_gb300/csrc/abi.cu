@@ -46,7 +46,8 @@ VerifyLayout verify_layout(int R, int V, int max_rows) {
     L.valid = off; off += align_up(sizeof(int) * (size_t)R);
     L.cnt1 = off; off += align_up(sizeof(int) * (size_t)R);
     L.cnt2 = off; off += align_up(sizeof(int) * (size_t)R);
-    L.stats = off; off += align_up(sizeof(RowStat) * (size_t)max_rows * nchunk);
+    const int nsub = (V + kStatChunk - 1) / kStatChunk;
+    L.stats = off; off += align_up(sizeof(RowStat) * (size_t)max_rows * nsub);
     L.jobs = off; off += align_up(sizeof(VerifyJob) * (size_t)R);
     L.parts = off; off += align_up(sizeof(SamplePartial) * (size_t)R * nchunk);
     L.total = off;
@@ -173,7 +174,8 @@ int dspark_verify(const float* target_logits, const int32_t* cu_seqlens,
     const VerifyLayout L = verify_layout(R, V, max_rows);
     if (ws_bytes < L.total) return DSPARK_ERR_WORKSPACE;
     const int nchunk = (V + kVerifyChunk - 1) / kVerifyChunk;
-    if ((long long)max_rows * nchunk >= (1LL << 31) || (long long)R * nchunk >= (1LL << 31))
+    if ((long long)max_rows * ((V + kStatChunk - 1) / kStatChunk) >= (1LL << 31) ||
+        (long long)R * nchunk >= (1LL << 31))
         return DSPARK_ERR_UNSUPPORTED;
 
     VerifyParams p;
@@ -181,6 +183,7 @@ int dspark_verify(const float* target_logits, const int32_t* cu_seqlens,
     p.q_lse = q_lse; p.q_tok = q_tok; p.seeds = seeds; p.cycle = cycle;
     p.invT = greedy ? 1.0f : 1.0f / temperature; p.greedy = greedy;
     p.R = R; p.gamma = gamma; p.V = V; p.max_rows = max_rows; p.nchunk = nchunk;
+    p.nsub = (V + kStatChunk - 1) / kStatChunk;
     p.n_acc = n_accepted; p.out_tokens = out_tokens; p.p_tok = p_tok; p.dev_status = dev_status;
     p.ok = carve<int>(ws, L.ok);
     p.valid = carve<int>(ws, L.valid);
@@ -214,7 +217,7 @@ int dspark_verify_markov(const float* target_logits, const int32_t* cu_seqlens,
     const size_t res_off = align_up(L.total);
     if (ws_bytes < res_off + residual_tc_workspace(R, rank)) return DSPARK_ERR_WORKSPACE;
     const int nchunk = (V + kVerifyChunk - 1) / kVerifyChunk;
-    if ((long long)max_rows * nchunk >= (1LL << 31)) return DSPARK_ERR_UNSUPPORTED;
+    if ((long long)max_rows * ((V + kStatChunk - 1) / kStatChunk) >= (1LL << 31)) return DSPARK_ERR_UNSUPPORTED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     VerifyParams p;
@@ -222,6 +225,7 @@ int dspark_verify_markov(const float* target_logits, const int32_t* cu_seqlens,
     p.q_lse = q_lse; p.q_tok = q_tok; p.seeds = seeds; p.cycle = cycle;
     p.invT = greedy ? 1.0f : 1.0f / temperature; p.greedy = greedy;
     p.R = R; p.gamma = gamma; p.V = V; p.max_rows = max_rows; p.nchunk = nchunk;
+    p.nsub = (V + kStatChunk - 1) / kStatChunk;
     p.n_acc = n_accepted; p.out_tokens = out_tokens; p.p_tok = p_tok; p.dev_status = dev_status;
     p.ok = carve<int>(ws, L.ok);
     p.valid = carve<int>(ws, L.valid);

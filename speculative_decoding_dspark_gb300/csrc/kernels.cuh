@@ -9,7 +9,8 @@ namespace dspark {
 // Verify
 // ----------------------------------------------------------------------------
 constexpr int kVerifyThreads = 256;
-constexpr int kVerifyChunk = 8192;  // target-row elements per CTA unit
+constexpr int kVerifyChunk = 8192;  // target-row elements per CTA unit of the extra-token draw
+constexpr int kStatChunk = 1024;    // target-row elements per warp unit of the row statistics
 
 struct RowStat {  // per (row, chunk): max and sum of exp(t - max), first argmax
     float m, s;
@@ -40,7 +41,7 @@ struct VerifyParams {
     uint32_t cycle;
     float invT;
     int greedy;
-    int R, gamma, V, max_rows, nchunk;
+    int R, gamma, V, max_rows, nchunk, nsub;
     int32_t* n_acc;
     int32_t* out_tokens;
     float* p_tok;
@@ -50,7 +51,7 @@ struct VerifyParams {
     int* valid;     // [R]
     int* cnt1;      // [R]
     int* cnt2;      // [R]
-    RowStat* stats; // [max_rows * nchunk]
+    RowStat* stats; // [max_rows * nsub] per (row, kStatChunk-element unit)
     VerifyJob* jobs;        // [R]
     SamplePartial* parts;   // [R * nchunk]
 };

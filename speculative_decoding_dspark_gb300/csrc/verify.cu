@@ -6,13 +6,16 @@
 // min(1, p/q), correct from max(0, p - q); section 13: the verified rows of
 // all requests are packed back to back, delimited by cu_seqlens.
 //
-// Three launches:
+// Four launches:
 //   verify_prologue  one CTA: checks cu_seqlens and the draft ids, clears the
 //                    per-request counters, fills the outputs of bad requests;
-//   verify_stats     one CTA per (row, 8192-element chunk): a streaming pass
-//                    computing max, sum of exp and the first argmax of
-//                    t = row * invT.  The last CTA of a request (counter, no
-//                    spin) combines its rows and makes the accept decisions;
+//   verify_stats     a streaming pass over (row, 1024-element) units, every
+//                    warp on its own sequence of units with the next one's
+//                    loads in flight while it reduces the current one: max,
+//                    sum of exp and the first argmax of t = row * invT per
+//                    unit; no block barrier, fence or atomic in the stream;
+//   verify_decide    one CTA per request: combines its rows' units and
+//                    makes the accept decisions, one thread per position;
 //   verify_correct   (T > 0) one CTA per (request, chunk) of the row the extra
 //                    token comes from: Gumbel-max over log max(0, p - q) or
 //                    over p; the last CTA of the request writes the token.
@@ -20,16 +23,6 @@
 
 namespace dspark {
 namespace {
-
-__device__ __forceinline__ int request_of_row(const int32_t* cu, int R, int row) {
-    // largest r with cu[r] <= row (cu non-decreasing, checked by the prologue)
-    int lo = 0, hi = R - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(cu + mid) <= row) lo = mid; else hi = mid - 1;
-    }
-    return lo;
-}
 
 __global__ void __launch_bounds__(1024) verify_prologue_kernel(VerifyParams p) {
     __shared__ int bad_cu;
@@ -79,37 +72,6 @@ __device__ __forceinline__ void lse2_merge(float& m, float& s, float m2, float s
     }
 }
 
-// Block-wide combine of (m, s, argmax) held by every thread (m, s in base-2
-// units); result in thread 0.
-__device__ __forceinline__ void block_rowstat(float& m, float& s, float& bm, int& bi) {
-    __shared__ float sm_m[32], sm_s[32], sm_bm[32];
-    __shared__ int sm_bi[32];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = shfl_xor(m, o), s2 = shfl_xor(s, o), bm2 = shfl_xor(bm, o);
-        const int bi2 = shfl_xor(bi, o);
-        lse2_merge(m, s, m2, s2);
-        if (better(bm2, bi2, bm, bi)) { bm = bm2; bi = bi2; }
-    }
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) { sm_m[w] = m; sm_s[w] = s; sm_bm[w] = bm; sm_bi[w] = bi; }
-    __syncthreads();
-    if (w == 0) {
-        const int nw = blockDim.x >> 5;
-        m = lane < nw ? sm_m[lane] : -INFINITY;
-        s = lane < nw ? sm_s[lane] : 0.0f;
-        bm = lane < nw ? sm_bm[lane] : -INFINITY;
-        bi = lane < nw ? sm_bi[lane] : INT_MAX;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float m2 = shfl_xor(m, o), s2 = shfl_xor(s, o), bm2 = shfl_xor(bm, o);
-            const int bi2 = shfl_xor(bi, o);
-            lse2_merge(m, s, m2, s2);
-            if (better(bm2, bi2, bm, bi)) { bm = bm2; bi = bi2; }
-        }
-    }
-}
-
 // Greedy: running first argmax of the raw row.  Sampling: t2 = row * invT *
 // log2(e), running (max, sum of 2^(t2 - max)); the argmax is not needed.
 template <bool kGreedy>
@@ -123,125 +85,157 @@ __device__ __forceinline__ void stat_elem(float x, int v, float c2, float& m, fl
     }
 }
 
-template <bool kGreedy>
-__global__ void __launch_bounds__(kVerifyThreads) verify_stats_kernel(VerifyParams p) {
-    __shared__ int s_req, s_last;
-    const int row = blockIdx.x / p.nchunk;
-    const int chunk = blockIdx.x - row * p.nchunk;
-    if (!p.ok[0]) return;
-    const int n_rows = p.cu[p.R];
-    if (row >= n_rows) return;
-    if (threadIdx.x == 0) s_req = request_of_row(p.cu, p.R, row);
-    __syncthreads();
-    const int r = s_req;
-    if (!p.valid[r]) return;
+constexpr int kStatVec = kStatChunk / 4 / 32;  // float4 per lane and unit
+constexpr int kStatThreads = 256;
 
+// 16-byte loads of unit u = (row, 1024-element piece) of the packed target
+// rows, lane-interleaved (a warp reads 512 contiguous bytes per load); entries
+// past the row end read as -inf and add nothing.
+__device__ __forceinline__ void load_unit(const VerifyParams& p, int u, int lane, float4 (&b)[kStatVec]) {
+    const int row = u / p.nsub, sub = u - row * p.nsub;
+    const int v0 = sub * kStatChunk, v1 = min(p.V, v0 + kStatChunk);
+    const float* base = p.target + (size_t)row * p.V;
+#pragma unroll
+    for (int i = 0; i < kStatVec; ++i) {
+        const int v = v0 + 4 * (lane + 32 * i);
+        b[i] = v < v1 ? __ldcs(reinterpret_cast<const float4*>(base + v))
+                      : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+}
+
+template <bool kGreedy>
+__global__ void __launch_bounds__(kStatThreads) verify_stats_kernel(VerifyParams p) {
+    if (!p.ok[0]) return;
     const int V = p.V;
-    const int v0 = chunk * kVerifyChunk;
-    const int v1 = min(V, v0 + kVerifyChunk);
-    const float* base = p.target + (size_t)row * V;
+    const int n_units = p.cu[p.R] * p.nsub;
+    const int lane = threadIdx.x & 31;
+    const int w0 = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+    const int nw = (int)((gridDim.x * (size_t)blockDim.x) >> 5);
+    const bool vec = (V & 3) == 0 && ((reinterpret_cast<uintptr_t>(p.target) & 15) == 0);
     const float c2 = p.invT * kLog2e;
-    float m = -INFINITY, s = 0.0f, bm = -INFINITY;
-    int bi = INT_MAX;
-    if ((V & 3) == 0 && ((reinterpret_cast<uintptr_t>(p.target) & 15) == 0)) {
-        // 8 independent 16-byte loads per thread, then the arithmetic
-        constexpr int kVec = kVerifyChunk / 4 / kVerifyThreads;
-        float4 buf[kVec];
+    float4 buf[kStatVec];
+    if (vec && w0 < n_units) load_unit(p, w0, lane, buf);
+    for (int u = w0; u < n_units; u += nw) {
+        const int row = u / p.nsub;
+        const int sub = u - row * p.nsub;
+        const int v0 = sub * kStatChunk;
+        // the next unit's loads go out before this one is reduced
+        float4 nxt[kStatVec];
+        if (vec && u + nw < n_units) load_unit(p, u + nw, lane, nxt);
+        float m = -INFINITY, s = 0.0f, bm = -INFINITY;
+        int bi = INT_MAX;
+        if (vec) {
+            if (kGreedy) {
 #pragma unroll
-        for (int i = 0; i < kVec; ++i) {
-            const int v = v0 + 4 * (threadIdx.x + i * kVerifyThreads);
-            buf[i] = v < v1 ? __ldcs(reinterpret_cast<const float4*>(base + v))
-                            : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        }
-        if (kGreedy) {
-#pragma unroll
-            for (int i = 0; i < kVec; ++i) {
-                const int v = v0 + 4 * (threadIdx.x + i * kVerifyThreads);
-                if (v < v1) {
+                for (int i = 0; i < kStatVec; ++i) {
+                    const int v = v0 + 4 * (lane + 32 * i);
                     stat_elem<true>(buf[i].x, v + 0, c2, m, s, bm, bi);
                     stat_elem<true>(buf[i].y, v + 1, c2, m, s, bm, bi);
                     stat_elem<true>(buf[i].z, v + 2, c2, m, s, bm, bi);
                     stat_elem<true>(buf[i].w, v + 3, c2, m, s, bm, bi);
                 }
+            } else {
+                // the lane's maximum first, then one pass of 2^(t - max)
+#pragma unroll
+                for (int i = 0; i < kStatVec; ++i) {
+                    buf[i].x *= c2; buf[i].y *= c2; buf[i].z *= c2; buf[i].w *= c2;
+                    m = fmaxf(m, fmaxf(fmaxf(buf[i].x, buf[i].y), fmaxf(buf[i].z, buf[i].w)));
+                }
+                if (m != -INFINITY) {
+#pragma unroll
+                    for (int i = 0; i < kStatVec; ++i)
+                        s += (exp2f(buf[i].x - m) + exp2f(buf[i].y - m)) + (exp2f(buf[i].z - m) + exp2f(buf[i].w - m));
+                }
             }
         } else {
-            // the thread's maximum first, then one pass of 2^(t - max); entries past
-            // the row end were loaded as -inf and add nothing
-#pragma unroll
-            for (int i = 0; i < kVec; ++i) {
-                buf[i].x *= c2; buf[i].y *= c2; buf[i].z *= c2; buf[i].w *= c2;
-                m = fmaxf(m, fmaxf(fmaxf(buf[i].x, buf[i].y), fmaxf(buf[i].z, buf[i].w)));
-            }
-            if (m != -INFINITY) {
-#pragma unroll
-                for (int i = 0; i < kVec; ++i)
-                    s += (exp2f(buf[i].x - m) + exp2f(buf[i].y - m)) + (exp2f(buf[i].z - m) + exp2f(buf[i].w - m));
-            }
+            const int v1 = min(V, v0 + kStatChunk);
+            const float* base = p.target + (size_t)row * V;
+            for (int v = v0 + lane; v < v1; v += 32) stat_elem<kGreedy>(__ldg(base + v), v, c2, m, s, bm, bi);
         }
-    } else {
-        for (int v = v0 + threadIdx.x; v < v1; v += kVerifyThreads)
-            stat_elem<kGreedy>(__ldg(base + v), v, c2, m, s, bm, bi);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float m2 = shfl_xor(m, o), s2 = shfl_xor(s, o), bm2 = shfl_xor(bm, o);
+            const int bi2 = shfl_xor(bi, o);
+            lse2_merge(m, s, m2, s2);
+            if (better(bm2, bi2, bm, bi)) { bm = bm2; bi = bi2; }
+        }
+        if (lane == 0) {
+            RowStat st;
+            st.m = kGreedy ? bm : m;
+            st.s = s;
+            st.idx = bi;
+            st.pad = 0;
+            p.stats[(size_t)row * p.nsub + sub] = st;
+        }
+#pragma unroll
+        for (int i = 0; i < kStatVec; ++i) buf[i] = nxt[i];
     }
-    block_rowstat(m, s, bm, bi);
-    if (threadIdx.x == 0) {
-        RowStat st;
-        st.m = kGreedy ? bm : m;
-        st.s = s;
-        st.idx = bi;
-        st.pad = 0;
-        p.stats[(size_t)row * p.nchunk + chunk] = st;
-        __threadfence();
-        const int total = (p.cu[r + 1] - p.cu[r]) * p.nchunk;
-        s_last = (atomicAdd(p.cnt1 + r, 1) == total - 1);
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
+}
 
-    // ---- last CTA of request r: combine its rows, decide left to right ----
+// One CTA per request: each row's units combined by a warp, then the drafts
+// decided left to right (one thread per position; the first rejection wins).
+template <bool kGreedy>
+__global__ void __launch_bounds__(kStatThreads) verify_decide_kernel(VerifyParams p) {
     __shared__ float row_lse[17];
     __shared__ int row_amax[17];
+    __shared__ float s_pt[16];
+    __shared__ int s_acc[16];
+    const int r = blockIdx.x;
+    if (!p.ok[0] || !p.valid[r]) return;
     const int first = p.cu[r];
     const int l = p.cu[r + 1] - first - 1;
-    if (threadIdx.x <= l) {
-        const RowStat* rs = p.stats + (size_t)(first + threadIdx.x) * p.nchunk;
+    const int g = p.gamma;
+    const float c2 = p.invT * kLog2e;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int j = warp; j <= l; j += kStatThreads / 32) {
+        const RowStat* rs = p.stats + (size_t)(first + j) * p.nsub;
         float cm = -INFINITY, cs = 0.0f, am = -INFINITY;
         int ai = INT_MAX;
-        for (int c = 0; c < p.nchunk; ++c) {
-            const float m2 = __ldcg(&rs[c].m), s2 = __ldcg(&rs[c].s);
-            const int i2 = __ldcg(&rs[c].idx);
-            if (better(m2, i2, am, ai)) { am = m2; ai = i2; }
-            if (!kGreedy) lse2_merge(cm, cs, m2, s2);
+        for (int c = lane; c < p.nsub; c += 32) {
+            const RowStat q = rs[c];
+            if (better(q.m, q.idx, am, ai)) { am = q.m; ai = q.idx; }
+            if (!kGreedy) lse2_merge(cm, cs, q.m, q.s);
         }
-        row_lse[threadIdx.x] = kGreedy ? 0.0f : cm + log2f(cs);  // base-2 log-normaliser
-        row_amax[threadIdx.x] = ai;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float m2 = shfl_xor(cm, o), s2 = shfl_xor(cs, o), am2 = shfl_xor(am, o);
+            const int ai2 = shfl_xor(ai, o);
+            lse2_merge(cm, cs, m2, s2);
+            if (better(am2, ai2, am, ai)) { am = am2; ai = ai2; }
+        }
+        if (lane == 0) {
+            row_lse[j] = kGreedy ? 0.0f : cm + log2f(cs);  // base-2 log-normaliser
+            row_amax[j] = ai;
+        }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        const int g = p.gamma;
-        int n = l;
-        for (int j = 0; j < l; ++j) {
-            const int yj = p.y[(size_t)r * g + j];
-            bool accept;
-            float pt;
-            if (kGreedy) {
-                accept = (yj == row_amax[j]);
-                pt = accept ? 1.0f : 0.0f;
-            } else {
-                pt = exp2f(p.target[(size_t)(first + j) * p.V + yj] * c2 - row_lse[j]);
-                const float ratio = pt / p.q_tok[(size_t)r * g + j];
-                const uint4 w = philox4x32_10(
-                    make_uint4(0u, (uint32_t)j, (uint32_t)r, ctr_word3(p.cycle, kAccept)),
-                    (uint32_t)(p.seeds[r] & 0xFFFFFFFFu), (uint32_t)(p.seeds[r] >> 32));
-                accept = uniform_from_bits(w.x) < ratio;
-            }
-            if (p.p_tok) p.p_tok[(size_t)r * g + j] = pt;
-            if (!accept) { n = j; break; }
+    const int j = threadIdx.x;
+    if (j < l) {
+        const int yj = p.y[(size_t)r * g + j];
+        bool accept;
+        float pt;
+        if (kGreedy) {
+            accept = (yj == row_amax[j]);
+            pt = accept ? 1.0f : 0.0f;
+        } else {
+            pt = exp2f(p.target[(size_t)(first + j) * p.V + yj] * c2 - row_lse[j]);
+            const float ratio = pt / p.q_tok[(size_t)r * g + j];
+            const uint4 w = philox4x32_10(make_uint4(0u, (uint32_t)j, (uint32_t)r, ctr_word3(p.cycle, kAccept)),
+                                          (uint32_t)(p.seeds[r] & 0xFFFFFFFFu), (uint32_t)(p.seeds[r] >> 32));
+            accept = uniform_from_bits(w.x) < ratio;
         }
+        s_pt[j] = pt;
+        s_acc[j] = accept;
+    }
+    __syncthreads();
+    int n = l;  // accepted drafts: up to the first rejection
+    for (int i = 0; i < l; ++i)
+        if (!s_acc[i]) { n = i; break; }
+    if (j < l && j <= n && p.p_tok) p.p_tok[(size_t)r * g + j] = s_pt[j];
+    int32_t* out = p.out_tokens + (size_t)r * (g + 1);
+    if (j <= g && j != n) out[j] = j < n ? p.y[(size_t)r * g + j] : -1;
+    if (j == 0) {
         p.n_acc[r] = n;
-        int32_t* out = p.out_tokens + (size_t)r * (g + 1);
-        for (int j = 0; j < n; ++j) out[j] = p.y[(size_t)r * g + j];
-        for (int j = n + 1; j <= g; ++j) out[j] = -1;
         if (kGreedy) {
             const int tok = row_amax[n];
             out[n] = (tok >= 0 && tok < p.V) ? tok : -1;
@@ -369,10 +363,22 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_correct_kernel(VerifyPa
 
 cudaError_t launch_verify_decide(const VerifyParams& p, cudaStream_t stream) {
     verify_prologue_kernel<<<1, 1024, 0, stream>>>(p);
-    const long long grid1 = (long long)p.max_rows * p.nchunk;
-    if (grid1 > 0) {
-        if (p.greedy) verify_stats_kernel<true><<<(unsigned)grid1, kVerifyThreads, 0, stream>>>(p);
-        else verify_stats_kernel<false><<<(unsigned)grid1, kVerifyThreads, 0, stream>>>(p);
+    const long long units = (long long)p.max_rows * p.nsub;  // at most: the rows in use are read on the device
+    if (units > 0) {
+        int dev = 0, n_sm = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return cudaGetLastError();
+        // enough resident warps to keep each SM's share of the stream in flight
+        const long long warps = std::min<long long>(units, 24LL * n_sm);
+        const unsigned grid1 = (unsigned)((warps * 32 + kStatThreads - 1) / kStatThreads);
+        if (p.greedy) {
+            verify_stats_kernel<true><<<grid1, kStatThreads, 0, stream>>>(p);
+            verify_decide_kernel<true><<<p.R, kStatThreads, 0, stream>>>(p);
+        } else {
+            verify_stats_kernel<false><<<grid1, kStatThreads, 0, stream>>>(p);
+            verify_decide_kernel<false><<<p.R, kStatThreads, 0, stream>>>(p);
+        }
     }
     return cudaGetLastError();
 }
