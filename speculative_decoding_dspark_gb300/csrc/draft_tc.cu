@@ -91,7 +91,7 @@ constexpr float kRaceSlack = 1.0f + 0x1p-10f;
 
 // Per-request partial of one thread or CTA.  Draft: (score, idx) of the
 // Gumbel-max draw, s at it, (max, sum of exp) of the logits.  Residual:
-// (score, idx) over the residual, (s_at, m-as-index) the draw over p.
+// (score, idx) of the draw.
 struct TcPartial {
     float score;
     int idx;
@@ -115,7 +115,7 @@ struct ResRow {
 struct TcParams {
     const uint16_t* U;
     const uint16_t* W1;
-    unsigned long long* keys;  // draft [gamma][R]; residual [2][R] (residual race, p race)
+    unsigned long long* keys;  // draft [gamma][R]; residual [R]
     const int32_t* toks;       // draft [R]: the A rows' tokens (-2: no usable predecessor)
     float4* parts;             // draft [gamma][R][P]: (max, sum, winner logit, winner) per CTA
     const uint64_t* seeds;
@@ -146,18 +146,10 @@ __device__ __forceinline__ void merge_draft(float& sc, int& ix, float& sa, float
     lse_merge(m, su, m2, su2);
 }
 
-__device__ __forceinline__ void merge_residual(float& sc, int& ix, float& sa, int& ia, float sc2, int ix2, float sa2,
-                                               int ia2) {
-    if (better(sc2, ix2, sc, ix)) { sc = sc2; ix = ix2; }
-    if (better(sa2, ia2, sa, ia)) { sa = sa2; ia = ia2; }
-}
-
 template <bool kRes>
 __device__ __forceinline__ void merge_any(TcPartial& a, const TcPartial& b) {
     if (kRes) {
-        int ia = __float_as_int(a.m);
-        merge_residual(a.score, a.idx, a.s_at, ia, b.score, b.idx, b.s_at, __float_as_int(b.m));
-        a.m = __int_as_float(ia);
+        if (better(b.score, b.idx, a.score, a.idx)) { a.score = b.score; a.idx = b.idx; }
     } else {
         merge_draft(a.score, a.idx, a.s_at, a.m, a.sum, b.score, b.idx, b.s_at, b.m, b.sum);
     }
@@ -166,8 +158,8 @@ __device__ __forceinline__ void merge_any(TcPartial& a, const TcPartial& b) {
 template <bool kRes>
 __device__ __forceinline__ TcPartial identity_partial() {
     TcPartial w;
-    w.score = -INFINITY; w.idx = INT_MAX; w.s_at = kRes ? -INFINITY : 0.0f;
-    w.m = kRes ? __int_as_float(INT_MAX) : -INFINITY; w.sum = 0.0f;
+    w.score = -INFINITY; w.idx = INT_MAX; w.s_at = 0.0f;
+    w.m = -INFINITY; w.sum = 0.0f;
     w.pad[0] = w.pad[1] = w.pad[2] = 0.0f;
     return w;
 }
@@ -190,6 +182,13 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// E_best / w_best with the slack of the no-log test.  An approximate quotient
+// (a few units in 2^-24) is far inside the 2^-10 slack; w_best = 0 gives +inf
+// (every entry with w > 0 is then a candidate).
+__device__ __forceinline__ float race_bound(float e_best, float w_best) {
+    return __fdividef(e_best, w_best) * kRaceSlack;
 }
 
 // 1 + (1 - u) - 2^-24 for u = uniform_from_bits(x): the 23 kept bits inverted
@@ -484,11 +483,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         float* qrow = (!kRes && p.q_logits && row_ok) ? p.q_logits + rk * p.V : nullptr;
         // logits are scaled to base 2 when sampling: s2 = s * log2(e) / T
         const float c2 = sampling ? p.invT * kLog2eF : 1.0f;
-        // exponential-race state: draft / residual race (bw, bE, rho), p race (bp, bEp, rho_p);
-        // rho = E_best / w_best with the slack, the bound of the no-log test
-        float bw = 0.0f, bE = 1.0f, bp = 0.0f, bEp = 1.0f;
-        float rho = INFINITY, rho_p = INFINITY;
-        int ia = INT_MAX;
+        // exponential-race state (bw, bE) and rho = E_best / w_best with the
+        // slack, the bound of the no-log test
+        float bw = 0.0f, bE = 1.0f;
+        float rho = INFINITY;
         // residual: the 16 base logits (bf16 pairs) of the request's rejected row at v
         auto load_u = [&](int v, uint32_t(&dst)[8]) {
 #pragma unroll
@@ -507,13 +505,16 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
             const int a = i & 1;
             const uint32_t use = (uint32_t)(i >> 1);
             if (kRes && row_ok) {
-                // residual rows differ per request: pull this thread's pieces into L2 now
+                // residual rows differ per request: pull this thread's pieces of the
+                // next tile (of this one too, at the start) into L2
+                for (int tt = (i == 0 ? t : t + p.P); tt <= t + p.P && tt < p.n_tiles; tt += p.P) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int v = t * kNV + 64 * h + kPassCols * quarter;
-                    if (v < p.V) {
-                        prefetch_l2(trow + v);
-                        if (with_u) prefetch_l2(urow + v);
+                    for (int h = 0; h < 2; ++h) {
+                        const int v = tt * kNV + 64 * h + kPassCols * quarter;
+                        if (v < p.V) {
+                            prefetch_l2(trow + v);
+                            if (with_u) prefetch_l2(urow + v);
+                        }
                     }
                 }
             }
@@ -524,10 +525,27 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                 tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(a * kNV + quarter * kPassCols);
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {
+                const int v0 = t * kNV + 64 * h + kPassCols * quarter;
+                const int nvalid = min(16, p.V - v0);  // the same in the whole warp
                 float sv[16];
+                uint32_t uw[8];
+                float tv[16];
+                if constexpr (kRes) {
+                    // residual: target logits (past the row end -inf: p = 0) and, for a
+                    // rejected row, the drafter's base logits; requested before the
+                    // accumulator is read
+                    if (row_ok && nvalid > 0) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float4 f = 4 * j < nvalid ? __ldg(reinterpret_cast<const float4*>(trow + v0) + j)
+                                                            : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                            tv[4 * j + 0] = f.x; tv[4 * j + 1] = f.y; tv[4 * j + 2] = f.z; tv[4 * j + 3] = f.w;
+                        }
+                        if (with_u) load_u(v0, uw);
+                    }
+                }
                 __syncwarp();  // lanes that skipped the previous pass rejoin before the aligned load
                 tc::tmem_ld_32x32b_x16<0>(taddr + 64u * h, sv);
-                uint32_t uw[8];
                 if (!kRes) {
                     // this pass's base logits, then the buffer goes back to the U producer
                     // pass buffer h is filled once per tile: its phase parity is i & 1
@@ -546,8 +564,6 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(&bar.tempty[a]);
                 }
-                const int v0 = t * kNV + 64 * h + kPassCols * quarter;
-                const int nvalid = min(16, p.V - v0);  // the same in the whole warp
                 if (!kRes) {
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
@@ -592,7 +608,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                                 part.sum *= sc;
                                 bw *= sc;
                                 part.m = cm;
-                                rho = bE / bw * kRaceSlack;
+                                rho = race_bound(bE, bw);
                             }
                             uint4 x[4];
 #pragma unroll
@@ -619,25 +635,16 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                                         const float E = neg_log_uniform(word_of(x[c >> 2], c & 3));
                                         if (w * bE > bw * E) {
                                             bw = w; bE = E; part.idx = v0 + c; part.s_at = sv[c];
-                                            rho = bE / bw * kRaceSlack;
+                                            rho = race_bound(bE, bw);
                                         }
                                     }
                                 }
                             }
                         }
                     } else {
-                        // residual: target logits (past the row end -inf: p = 0) and,
-                        // for a rejected row, the drafter's base logits
-                        float tv[16];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const float4 f = 4 * j < nvalid ? __ldg(reinterpret_cast<const float4*>(trow + v0) + j)
-                                                            : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-                            tv[4 * j + 0] = f.x; tv[4 * j + 1] = f.y; tv[4 * j + 2] = f.z; tv[4 * j + 3] = f.w;
-                        }
+                        // one race per request: over max(0, p - q) for a rejected row,
+                        // over p for a bonus draw (q = 0 there)
                         if (with_u) {
-                            uint32_t uw[8];
-                            load_u(v0, uw);
 #pragma unroll
                             for (int c = 0; c < 16; ++c) {
                                 const uint32_t word = uw[c >> 1];
@@ -650,29 +657,25 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                         for (int q = 0; q < 4; ++q)
                             x[q] = make_uint4((uint32_t)((v0 >> 2) + q), (uint32_t)pos, (uint32_t)rr, w3);
                         philox4x32_10_x4(x, key0, key1);
-                        uint32_t cand_p = 0, cand_r = 0;
+                        uint32_t cand = 0;
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
-                            const float f = one_plus_complement(word_of(x[c >> 2], c & 3));
                             const float pv = ex2(fmaf(tv[c], c2, -rinfo.lse2_p));
-                            const float res = with_u ? pv - ex2(sv[c] - rinfo.q_lse2) : 0.0f;
-                            cand_p |= (f < fmaf(pv, rho_p, 1.0f)) ? (1u << c) : 0u;
-                            cand_r |= (res > 0.0f && f < fmaf(res, rho, 1.0f)) ? (1u << c) : 0u;
+                            const float wgt = with_u ? pv - ex2(sv[c] - rinfo.q_lse2) : pv;
+                            tv[c] = wgt;
+                            cand |= (wgt > 0.0f && one_plus_complement(word_of(x[c >> 2], c & 3)) <
+                                                       fmaf(wgt, rho, 1.0f))
+                                        ? (1u << c)
+                                        : 0u;
                         }
-                        if (cand_p | cand_r) {
+                        if (cand) {
 #pragma unroll
                             for (int c = 0; c < 16; ++c) {
-                                if ((cand_p | cand_r) & (1u << c)) {
-                                    const float pv = ex2(fmaf(tv[c], c2, -rinfo.lse2_p));
-                                    const float res = with_u ? pv - ex2(sv[c] - rinfo.q_lse2) : 0.0f;
+                                if (cand & (1u << c)) {
                                     const float E = neg_log_uniform(word_of(x[c >> 2], c & 3));
-                                    if ((cand_p & (1u << c)) && pv * bEp > bp * E) {
-                                        bp = pv; bEp = E; ia = v0 + c;
-                                        rho_p = bEp / bp * kRaceSlack;
-                                    }
-                                    if ((cand_r & (1u << c)) && res * bE > bw * E) {
-                                        bw = res; bE = E; part.idx = v0 + c;
-                                        rho = bE / bw * kRaceSlack;
+                                    if (tv[c] * bE > bw * E) {
+                                        bw = tv[c]; bE = E; part.idx = v0 + c;
+                                        rho = race_bound(bE, bw);
                                     }
                                 }
                             }
@@ -684,8 +687,6 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         // scores of the winners in log form, for merging across threads and CTAs
         if (kRes) {
             part.score = part.idx != INT_MAX ? logf(bw) - logf(bE) : -INFINITY;
-            part.s_at = ia != INT_MAX ? logf(bp) - logf(bEp) : -INFINITY;
-            part.m = __int_as_float(ia);
         } else if (!p.greedy) {
             // back to natural units: the max and the winner's logit
             part.m *= kLn2F;
@@ -718,8 +719,6 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         for (int q = 0; q < 3; ++q) merge_any<kRes>(part, scratch[q * kM + m]);
         if (kRes) {
             if (part.idx != INT_MAX) atomicMax(p.keys + rr, winner_key(part.score, part.idx));
-            const int ia = __float_as_int(part.m);
-            if (ia != INT_MAX) atomicMax(p.keys + p.R + rr, winner_key(part.s_at, ia));
         } else {
             const size_t slot = (size_t)p.k * p.R + rr;
             if (!p.greedy)
@@ -788,21 +787,48 @@ __global__ void __launch_bounds__(256) draft_finalize_kernel(DraftFinalize f) {
     }
 }
 
-// The extra token of every request: the residual winner when the residual has
-// mass (mode 1), else the winner over p.
+// The extra token of every request, one CTA each: the race's winner (over
+// max(0, p - q) for a rejected row, over p for a bonus draw).  When a rejected
+// row's residual has no positive mass (p <= q everywhere), the CTA draws from
+// p of the row with the same noise.
 __global__ void __launch_bounds__(256) residual_finalize_kernel(const ResRow* rows, const unsigned long long* keys,
-                                                                int R, int gamma, int32_t* out_tokens,
+                                                                const float* target, const uint64_t* seeds,
+                                                                float invT, int gamma, int V, int32_t* out_tokens,
                                                                 int32_t* dev_status) {
-    const int r = blockIdx.x * blockDim.x + threadIdx.x;
-    if (r >= R) return;
+    __shared__ unsigned long long s_key;
+    const int r = blockIdx.x;
     const ResRow ri = rows[r];
     if (ri.mode == 0) return;
-    const unsigned long long kr = keys[r], kp = keys[R + r];
-    int tok = -1;
-    if (ri.mode == 1 && kr) tok = key_index(kr);
-    else if (kp) tok = key_index(kp);
-    if (tok < 0) report(dev_status, DSPARK_ERR_DEVICE_INPUT);  // no finite score (NaN logits)
-    out_tokens[(size_t)r * (gamma + 1) + ri.pos] = tok;
+    unsigned long long key = keys[r];
+    if (key == 0 && ri.mode == 1) {
+        if (threadIdx.x == 0) s_key = 0;
+        __syncthreads();
+        const float c2 = invT * kLog2eF;
+        const float* trow = target + (size_t)ri.trow * V;
+        const uint64_t seed = seeds[r];
+        float bw = 0.0f, bE = 1.0f;
+        int bi = INT_MAX;
+        for (int v4 = threadIdx.x; 4 * v4 < V; v4 += blockDim.x) {
+            const uint4 x = philox4x32_10(make_uint4((uint32_t)v4, (uint32_t)ri.pos, (uint32_t)r, ri.w3),
+                                          (uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int v = 4 * v4 + e;
+                if (v >= V) break;
+                const float pv = ex2(fmaf(__ldg(trow + v), c2, -ri.lse2_p));
+                const float E = neg_log_uniform(word_of(x, e));
+                if (pv * bE > bw * E) { bw = pv; bE = E; bi = v; }
+            }
+        }
+        if (bi != INT_MAX) atomicMax(&s_key, winner_key(logf(bw) - logf(bE), bi));
+        __syncthreads();
+        key = s_key;
+    }
+    if (threadIdx.x == 0) {
+        const int tok = key ? key_index(key) : -1;
+        if (tok < 0) report(dev_status, DSPARK_ERR_DEVICE_INPUT);  // no finite score (NaN logits)
+        out_tokens[(size_t)r * (gamma + 1) + ri.pos] = tok;
+    }
 }
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -832,7 +858,7 @@ struct TcLayout {
 TcLayout tc_layout(int R, int gamma, int rank, bool residual) {
     TcLayout L;
     size_t off = 0;
-    L.n_keys = residual ? 2 * (size_t)R : (size_t)gamma * R;
+    L.n_keys = residual ? (size_t)R : (size_t)gamma * R;
     L.keys = off; off += up256(sizeof(unsigned long long) * L.n_keys);
     L.h = off; off += up256((size_t)R * rank * 2);
     L.toks = off; off += residual ? 0 : up256(sizeof(int32_t) * (size_t)R);
@@ -1021,8 +1047,8 @@ int launch_residual_tc(const ResidualTcArgs& a, cudaStream_t stream) {
         return DSPARK_ERR_CUDA;
     residual_prep_kernel<<<(unsigned)((a.R * 32LL + 255) / 256), 256, 0, stream>>>(a, rows, H);
     markov_tc_kernel<true><<<grid, kThreads, smem, stream>>>(tm_w2, tm_u, tm_h, p);
-    residual_finalize_kernel<<<(a.R + 255) / 256, 256, 0, stream>>>(rows, p.keys, a.R, a.gamma, a.out_tokens,
-                                                                     a.dev_status);
+    residual_finalize_kernel<<<a.R, 256, 0, stream>>>(rows, p.keys, a.target, a.seeds, a.invT, a.gamma, a.V,
+                                                      a.out_tokens, a.dev_status);
     return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 
