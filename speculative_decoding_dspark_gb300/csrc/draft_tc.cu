@@ -138,6 +138,9 @@ struct Bars {
     uint64_t afull, mma_done;
     uint32_t tmem_slot;
     int abort_flag;
+    // per request row and epilogue quarter: the best race record so far as
+    // log2(w / E) in absolute units (-inf: none), read by the row's other quarters
+    float g_share[4][kM];
 };
 
 __device__ __forceinline__ void merge_draft(float& sc, int& ix, float& sa, float& m, float& su, float sc2, int ix2,
@@ -189,6 +192,21 @@ __device__ __forceinline__ float ex2(float x) {
 // (every entry with w > 0 is then a candidate).
 __device__ __forceinline__ float race_bound(float e_best, float w_best) {
     return __fdividef(e_best, w_best) * kRaceSlack;
+}
+
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// log2 of the ratio w / E encoded in a published winner key (natural-log
+// score in the high word); -inf when nothing is published yet.
+__device__ __forceinline__ float key_log2_ratio(unsigned long long key) {
+    if (key == 0) return -INFINITY;
+    const uint32_t hi = (uint32_t)(key >> 32);
+    const uint32_t bits = (hi & 0x80000000u) ? (hi & 0x7FFFFFFFu) : ~hi;
+    return __uint_as_float(bits) * kLog2eF;
 }
 
 // 1 + (1 - u) - 2^-24 for u = uniform_from_bits(x): the 23 kept bits inverted
@@ -313,6 +331,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
     const int row0 = blk * kM;
     const int S = p.n_stages;
 
+    for (int e = threadIdx.x; e < 4 * kM; e += kThreads) (&bar.g_share[0][0])[e] = -INFINITY;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) { tc::mbar_init(&bar.full[s], 1); tc::mbar_init(&bar.empty[s], 1); }
         for (int a = 0; a < 2; ++a) { tc::mbar_init(&bar.tfull[a], 1); tc::mbar_init(&bar.tempty[a], kEpiWarps); }
@@ -484,9 +503,20 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         // logits are scaled to base 2 when sampling: s2 = s * log2(e) / T
         const float c2 = sampling ? p.invT * kLog2eF : 1.0f;
         // exponential-race state (bw, bE) and rho = E_best / w_best with the
-        // slack, the bound of the no-log test
+        // slack, the bound of the no-log test.  Residual: an entry that cannot
+        // beat the best record of any thread racing over the same request
+        // cannot be the request's winner either, so rho is taken from the best
+        // of this thread's record, the row's other three quarters in this CTA
+        // (shared memory, every pass) and the request's published key (global,
+        // read a tile late), each as g = log2(w / E) in absolute units.  (The
+        // draft's races gain too little from this to pay for the atomics.)
         float bw = 0.0f, bE = 1.0f;
         float rho = INFINITY;
+        float g_own = -INFINITY, g_pub = -INFINITY, g_glob = -INFINITY;
+        unsigned long long gkey = 0;
+        const bool share = kRes && row_ok;
+        unsigned long long* my_key = kRes ? p.keys + rr : p.keys + (size_t)p.k * p.R + rr;
+        volatile float* gsh = &bar.g_share[0][m];  // the row's four quarter records, written by other warps
         // residual: the 16 base logits (bf16 pairs) of the request's rejected row at v
         auto load_u = [&](int v, uint32_t(&dst)[8]) {
 #pragma unroll
@@ -517,6 +547,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                         }
                     }
                 }
+            }
+            if (share) {
+                if (i > 0) g_glob = key_log2_ratio(gkey);
+                gkey = *reinterpret_cast<volatile unsigned long long*>(my_key);
             }
             // warp-uniform wait: every lane waits (acquire), all leave together
             if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.tfull[a], use & 1u, abort_flag, kWaitNs))) break;
@@ -608,8 +642,8 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                                 part.sum *= sc;
                                 bw *= sc;
                                 part.m = cm;
-                                rho = race_bound(bE, bw);
                             }
+                            rho = race_bound(bE, bw);
                             uint4 x[4];
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
@@ -657,6 +691,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                         for (int q = 0; q < 4; ++q)
                             x[q] = make_uint4((uint32_t)((v0 >> 2) + q), (uint32_t)pos, (uint32_t)rr, w3);
                         philox4x32_10_x4(x, key0, key1);
+                        {
+                            const float g = fmaxf(fmaxf(g_own, g_glob),
+                                                  fmaxf(fmaxf(gsh[0], gsh[kM]), fmaxf(gsh[2 * kM], gsh[3 * kM])));
+                            rho = fminf(race_bound(bE, bw), ex2(-g) * kRaceSlack);
+                        }
                         uint32_t cand = 0;
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
@@ -669,19 +708,33 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                                         : 0u;
                         }
                         if (cand) {
+                            bool rec = false;
 #pragma unroll
                             for (int c = 0; c < 16; ++c) {
                                 if (cand & (1u << c)) {
                                     const float E = neg_log_uniform(word_of(x[c >> 2], c & 3));
                                     if (tv[c] * bE > bw * E) {
                                         bw = tv[c]; bE = E; part.idx = v0 + c;
-                                        rho = race_bound(bE, bw);
+                                        rho = fminf(rho, race_bound(bE, bw));
+                                        rec = true;
                                     }
                                 }
+                            }
+                            if (rec) {
+                                g_own = lg2(bw) - lg2(bE);
+                                gsh[quarter * kM] = g_own;
                             }
                         }
                     }
                 }
+            }
+            // this thread's record, if it beats the request's best seen so far, for the
+            // other CTAs racing over it (few threads qualify after the first tiles:
+            // same-address atomics serialise)
+            if (share && g_own > fmaxf(g_pub, g_glob)) {
+                const float sc = kRes ? logf(bw) - logf(bE) : part.s_at * kLn2F - logf(bE);
+                atomicMax(my_key, winner_key(sc, part.idx));
+                g_pub = g_own;
             }
         }
         // scores of the winners in log form, for merging across threads and CTAs
