@@ -68,6 +68,10 @@ typedef struct CUstream_st* dspark_stream_t;
 #define DSPARK_ERR_DEVICE_INPUT (-6) /* device side: bad token id / length / confidence */
 #define DSPARK_ERR_WORKSPACE (-7)    /* workspace NULL, misaligned or too small        */
 
+/* Largest R the verify calls accept (their per-round request list is kept in
+ * shared memory). */
+#define DSPARK_VERIFY_MAX_R 16384
+
 /* ---- element types ------------------------------------------------------- */
 #define DSPARK_F32 0
 #define DSPARK_BF16 1
@@ -172,6 +176,8 @@ int dspark_markov_draft(const void* U, int u_dtype, const void* W1, const void* 
  *   out_tokens[r] = y[r][0 .. n-1], extra token, then -1 up to gamma + 1 entries.
  *   p_tok[r][j] = p(y_j) for the drafts examined (T = 0: 1 if y_j is the row's
  *   argmax else 0); entries not examined are left untouched.
+ *   Rows after a request's first rejection are not read.  R <= DSPARK_VERIFY_MAX_R
+ *   (else DSPARK_ERR_UNSUPPORTED).
  *
  *   target_logits [cu_seqlens[R], V] fp32, packed rows without padding
  *   cu_seqlens   [R + 1] int32, cu_seqlens[0] = 0, non-decreasing

@@ -36,7 +36,7 @@ DraftSimtLayout draft_simt_layout(int R, int V) {
 }
 
 struct VerifyLayout {
-    size_t ok, valid, cnt1, cnt2, stats, jobs, parts, total;
+    size_t ok, valid, cnt1, cnt2, act, lazy, stats, jobs, parts, total;
 };
 VerifyLayout verify_layout(int R, int V, int max_rows) {
     VerifyLayout L;
@@ -46,8 +46,10 @@ VerifyLayout verify_layout(int R, int V, int max_rows) {
     L.valid = off; off += align_up(sizeof(int) * (size_t)R);
     L.cnt1 = off; off += align_up(sizeof(int) * (size_t)R);
     L.cnt2 = off; off += align_up(sizeof(int) * (size_t)R);
+    L.act = off; off += align_up(sizeof(int) * 2 * (size_t)R);
+    L.lazy = off; off += align_up(sizeof(int) * 8);
     const int nsub = (V + kStatChunk - 1) / kStatChunk;
-    L.stats = off; off += align_up(sizeof(RowStat) * (size_t)max_rows * nsub);
+    L.stats = off; off += align_up(sizeof(RowStat) * (size_t)R * nsub);
     L.jobs = off; off += align_up(sizeof(VerifyJob) * (size_t)R);
     L.parts = off; off += align_up(sizeof(SamplePartial) * (size_t)R * nchunk);
     L.total = off;
@@ -165,6 +167,7 @@ int dspark_verify(const float* target_logits, const int32_t* cu_seqlens,
     if (!target_logits || !cu_seqlens || !draft_tokens || !n_accepted || !out_tokens)
         return DSPARK_ERR_INVALID_ARG;
     if (R <= 0 || V <= 0 || gamma <= 0 || gamma > 16) return DSPARK_ERR_INVALID_ARG;
+    if (R > DSPARK_VERIFY_MAX_R) return DSPARK_ERR_UNSUPPORTED;
     if (max_rows < R || (long long)max_rows > (long long)R * (gamma + 1)) return DSPARK_ERR_INVALID_ARG;
     if (!(temperature >= 0.0f) || temperature == INFINITY) return DSPARK_ERR_INVALID_ARG;
     if (cycle >= (1u << 28)) return DSPARK_ERR_INVALID_ARG;
@@ -189,6 +192,8 @@ int dspark_verify(const float* target_logits, const int32_t* cu_seqlens,
     p.valid = carve<int>(ws, L.valid);
     p.cnt1 = carve<int>(ws, L.cnt1);
     p.cnt2 = carve<int>(ws, L.cnt2);
+    p.act = carve<int>(ws, L.act);
+    p.lazy = carve<int>(ws, L.lazy);
     p.stats = carve<RowStat>(ws, L.stats);
     p.jobs = carve<VerifyJob>(ws, L.jobs);
     p.parts = carve<SamplePartial>(ws, L.parts);
@@ -205,6 +210,7 @@ int dspark_verify_markov(const float* target_logits, const int32_t* cu_seqlens,
     if (!target_logits || !cu_seqlens || !draft_tokens || !n_accepted || !out_tokens)
         return DSPARK_ERR_INVALID_ARG;
     if (R <= 0 || V <= 0 || gamma <= 0 || gamma > 16 || rank <= 0) return DSPARK_ERR_INVALID_ARG;
+    if (R > DSPARK_VERIFY_MAX_R) return DSPARK_ERR_UNSUPPORTED;
     if (max_rows < R || (long long)max_rows > (long long)R * (gamma + 1)) return DSPARK_ERR_INVALID_ARG;
     if (!(temperature >= 0.0f) || temperature == INFINITY) return DSPARK_ERR_INVALID_ARG;
     if (cycle >= (1u << 28)) return DSPARK_ERR_INVALID_ARG;
@@ -231,6 +237,8 @@ int dspark_verify_markov(const float* target_logits, const int32_t* cu_seqlens,
     p.valid = carve<int>(ws, L.valid);
     p.cnt1 = carve<int>(ws, L.cnt1);
     p.cnt2 = carve<int>(ws, L.cnt2);
+    p.act = carve<int>(ws, L.act);
+    p.lazy = carve<int>(ws, L.lazy);
     p.stats = carve<RowStat>(ws, L.stats);
     p.jobs = carve<VerifyJob>(ws, L.jobs);
     p.parts = carve<SamplePartial>(ws, L.parts);

@@ -51,7 +51,10 @@ struct VerifyParams {
     int* valid;     // [R]
     int* cnt1;      // [R]
     int* cnt2;      // [R]
-    RowStat* stats; // [max_rows * nsub] per (row, kStatChunk-element unit)
+    int* act;       // [2][R] requests still drafting-accepted, per round parity
+    int* lazy;      // [8] round state of the verify pass: barrier count and generation,
+                    // next-round counts (2), abort flag
+    RowStat* stats; // [R * nsub] per (request, kStatChunk-element unit of its first row)
     VerifyJob* jobs;        // [R]
     SamplePartial* parts;   // [R * nchunk]
 };

@@ -6,16 +6,21 @@
 // min(1, p/q), correct from max(0, p - q); section 13: the verified rows of
 // all requests are packed back to back, delimited by cu_seqlens.
 //
-// Four launches:
+// Three launches:
 //   verify_prologue  one CTA: checks cu_seqlens and the draft ids, clears the
 //                    per-request counters, fills the outputs of bad requests;
-//   verify_stats     a streaming pass over (row, 1024-element) units, every
-//                    warp on its own sequence of units with the next one's
-//                    loads in flight while it reduces the current one: max,
-//                    sum of exp and the first argmax of t = row * invT per
-//                    unit; no block barrier, fence or atomic in the stream;
-//   verify_decide    one CTA per request: combines its rows' units and
-//                    makes the accept decisions, one thread per position;
+//   verify_rounds    one cooperative launch, rounds j = 0, 1, ... over the
+//                    block positions.  Round j streams row j of every request
+//                    whose drafts 0..j-1 were all accepted: every warp walks
+//                    its own sequence of 1024-element units with the next
+//                    unit's loads in flight while it reduces the current one
+//                    (max, sum of exp, first argmax of t = row * invT); after
+//                    a grid barrier one warp per such request merges its units
+//                    and decides draft j (or, at j = l, takes the bonus row);
+//                    accepted requests go on to round j + 1.  Rows after the
+//                    first rejection are never read: with a weak drafter a
+//                    request needs about one row, with a strong one every
+//                    round still streams at the full rate of the grid.
 //   verify_correct   (T > 0) one CTA per (request, chunk) of the row the extra
 //                    token comes from: Gumbel-max over log max(0, p - q) or
 //                    over p; the last CTA of the request writes the token.
@@ -35,6 +40,7 @@ __global__ void __launch_bounds__(1024) verify_prologue_kernel(VerifyParams p) {
     }
     __syncthreads();
     const int ok = !bad_cu;
+    if (threadIdx.x < 8) p.lazy[threadIdx.x] = 0;
     if (threadIdx.x == 0) {
         p.ok[0] = ok;
         if (!ok) report(p.dev_status, DSPARK_ERR_DEVICE_INPUT);
@@ -52,6 +58,8 @@ __global__ void __launch_bounds__(1024) verify_prologue_kernel(VerifyParams p) {
             if (!valid) report(p.dev_status, DSPARK_ERR_DEVICE_INPUT);
         }
         p.valid[r] = valid;
+        p.act[r] = 0;
+        p.act[p.R + r] = 0;
         if (!valid) {
             p.n_acc[r] = -1;
             for (int j = 0; j <= p.gamma; ++j) p.out_tokens[(size_t)r * (p.gamma + 1) + j] = -1;
@@ -86,13 +94,11 @@ __device__ __forceinline__ void stat_elem(float x, int v, float c2, float& m, fl
 }
 
 constexpr int kStatVec = kStatChunk / 4 / 32;  // float4 per lane and unit
-constexpr int kStatThreads = 256;
 
-// 16-byte loads of unit u = (row, 1024-element piece) of the packed target
-// rows, lane-interleaved (a warp reads 512 contiguous bytes per load); entries
-// past the row end read as -inf and add nothing.
-__device__ __forceinline__ void load_unit(const VerifyParams& p, int u, int lane, float4 (&b)[kStatVec]) {
-    const int row = u / p.nsub, sub = u - row * p.nsub;
+// 16-byte loads of 1024-element piece `sub` of target row `row`,
+// lane-interleaved (a warp reads 512 contiguous bytes per load); entries past
+// the row end read as -inf and add nothing.
+__device__ __forceinline__ void load_unit(const VerifyParams& p, int row, int sub, int lane, float4 (&b)[kStatVec]) {
     const int v0 = sub * kStatChunk, v1 = min(p.V, v0 + kStatChunk);
     const float* base = p.target + (size_t)row * p.V;
 #pragma unroll
@@ -103,154 +109,250 @@ __device__ __forceinline__ void load_unit(const VerifyParams& p, int u, int lane
     }
 }
 
+// Round state in the workspace (zeroed by the prologue).
+enum : int { kBarCount = 0, kBarGen = 1, kAbort = 2 };
+constexpr uint64_t kBarrierNs = 2000000000ull;
+
+// Grid-wide barrier of a cooperative launch (every CTA is resident): the last
+// CTA to arrive resets the count and advances the generation; the others wait
+// for it, at most kBarrierNs, after which the round state's abort flag is set.
+// Returns false when the pass is aborted.
+__device__ __forceinline__ bool grid_barrier(int* st, unsigned& gen) {
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        const unsigned target = gen + 1;
+        __threadfence();
+        if (atomicAdd(reinterpret_cast<unsigned*>(st + kBarCount), 1u) == gridDim.x - 1) {
+            st[kBarCount] = 0;
+            __threadfence();
+            atomicExch(reinterpret_cast<unsigned*>(st + kBarGen), target);
+        } else {
+            const uint64_t t0 = global_ns();
+            for (unsigned it = 1; *reinterpret_cast<volatile unsigned*>(st + kBarGen) != target; ++it) {
+                if ((it & 31) == 0 &&
+                    (*reinterpret_cast<volatile int*>(st + kAbort) || global_ns() - t0 > kBarrierNs)) {
+                    atomicExch(st + kAbort, 1);
+                    ok = 0;
+                    break;
+                }
+            }
+        }
+        __threadfence();
+        s_ok = ok && !*reinterpret_cast<volatile int*>(st + kAbort);
+    }
+    __syncthreads();
+    gen += 1;
+    return s_ok != 0;
+}
+
+constexpr int kRoundThreads = 768;  // one CTA per SM: 24 warps, a grid barrier of n_sm arrivals
+constexpr size_t kMaxListBytes = sizeof(int) * DSPARK_VERIFY_MAX_R;  // the round's request list in shared memory
+
 template <bool kGreedy>
-__global__ void __launch_bounds__(kStatThreads) verify_stats_kernel(VerifyParams p) {
-    if (!p.ok[0]) return;
-    const int V = p.V;
-    const int n_units = p.cu[p.R] * p.nsub;
+__global__ void __launch_bounds__(kRoundThreads, 1) verify_rounds_kernel(VerifyParams p) {
+    extern __shared__ int s_list[];  // [R] the requests active in the current round
+    __shared__ int s_nact;
+    if (!p.ok[0]) return;  // the same for every CTA
+    const int V = p.V, g = p.gamma;
     const int lane = threadIdx.x & 31;
     const int w0 = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
     const int nw = (int)((gridDim.x * (size_t)blockDim.x) >> 5);
     const bool vec = (V & 3) == 0 && ((reinterpret_cast<uintptr_t>(p.target) & 15) == 0);
     const float c2 = p.invT * kLog2e;
-    float4 buf[kStatVec];
-    if (vec && w0 < n_units) load_unit(p, w0, lane, buf);
-    for (int u = w0; u < n_units; u += nw) {
-        const int row = u / p.nsub;
-        const int sub = u - row * p.nsub;
-        const int v0 = sub * kStatChunk;
-        // the next unit's loads go out before this one is reduced
-        float4 nxt[kStatVec];
-        if (vec && u + nw < n_units) load_unit(p, u + nw, lane, nxt);
-        float m = -INFINITY, s = 0.0f, bm = -INFINITY;
-        int bi = INT_MAX;
-        if (vec) {
-            if (kGreedy) {
-#pragma unroll
-                for (int i = 0; i < kStatVec; ++i) {
-                    const int v = v0 + 4 * (lane + 32 * i);
-                    stat_elem<true>(buf[i].x, v + 0, c2, m, s, bm, bi);
-                    stat_elem<true>(buf[i].y, v + 1, c2, m, s, bm, bi);
-                    stat_elem<true>(buf[i].z, v + 2, c2, m, s, bm, bi);
-                    stat_elem<true>(buf[i].w, v + 3, c2, m, s, bm, bi);
-                }
-            } else {
-                // the lane's maximum first, then one pass of 2^(t - max)
-#pragma unroll
-                for (int i = 0; i < kStatVec; ++i) {
-                    buf[i].x *= c2; buf[i].y *= c2; buf[i].z *= c2; buf[i].w *= c2;
-                    m = fmaxf(m, fmaxf(fmaxf(buf[i].x, buf[i].y), fmaxf(buf[i].z, buf[i].w)));
-                }
-                if (m != -INFINITY) {
-#pragma unroll
-                    for (int i = 0; i < kStatVec; ++i)
-                        s += (exp2f(buf[i].x - m) + exp2f(buf[i].y - m)) + (exp2f(buf[i].z - m) + exp2f(buf[i].w - m));
+    int* st = p.lazy;
+    unsigned gen = 0;
+    int n_act = p.R;           // round 0: every request (the bad ones are skipped when deciding)
+    bool all = true;           // round 0: request a is a
+    for (int j = 0; j <= g && n_act > 0; ++j) {
+        auto act_at = [&](int a) { return all ? a : s_list[a]; };
+        // the warp that decides for an active request fetches what the decision
+        // needs besides the row statistics now, so it is in registers after the stream
+        int d_r = -1, d_first = 0, d_l = 0, d_y = 0, d_valid = 0;
+        float d_t = 0.0f, d_q = 1.0f;
+        uint64_t d_seed = 0;
+        if (w0 < n_act && lane == 0) {
+            d_r = act_at(w0);
+            d_valid = p.valid[d_r];
+            d_first = p.cu[d_r];
+            d_l = p.cu[d_r + 1] - d_first - 1;
+            if (d_valid && j < d_l) {
+                d_y = p.y[(size_t)d_r * g + j];
+                if (!kGreedy) {
+                    d_t = __ldg(p.target + (size_t)(d_first + j) * V + d_y);
+                    d_q = p.q_tok[(size_t)d_r * g + j];
+                    d_seed = p.seeds[d_r];
                 }
             }
-        } else {
-            const int v1 = min(V, v0 + kStatChunk);
-            const float* base = p.target + (size_t)row * V;
-            for (int v = v0 + lane; v < v1; v += 32) stat_elem<kGreedy>(__ldg(base + v), v, c2, m, s, bm, bi);
         }
+        // ---- row j of every active request: unit statistics
+        const int n_units = n_act * p.nsub;
+        auto unit_row = [&](int u, int& r, int& sub) {
+            const int a = u / p.nsub;
+            sub = u - a * p.nsub;
+            r = act_at(a);
+            return __ldg(p.cu + r) + j;
+        };
+        float4 buf[kStatVec];
+        if (vec && w0 < n_units) {
+            int r0, sub0;
+            const int row0 = unit_row(w0, r0, sub0);
+            load_unit(p, row0, sub0, lane, buf);
+        }
+        for (int u = w0; u < n_units; u += nw) {
+            int r, sub;
+            const int row = unit_row(u, r, sub);
+            const int v0 = sub * kStatChunk;
+            // the next unit's loads go out before this one is reduced
+            float4 nxt[kStatVec];
+            if (vec && u + nw < n_units) {
+                int r1, sub1;
+                const int row1 = unit_row(u + nw, r1, sub1);
+                load_unit(p, row1, sub1, lane, nxt);
+            }
+            float m = -INFINITY, s = 0.0f, bm = -INFINITY;
+            int bi = INT_MAX;
+            if (vec) {
+                if (kGreedy) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float m2 = shfl_xor(m, o), s2 = shfl_xor(s, o), bm2 = shfl_xor(bm, o);
-            const int bi2 = shfl_xor(bi, o);
-            lse2_merge(m, s, m2, s2);
-            if (better(bm2, bi2, bm, bi)) { bm = bm2; bi = bi2; }
-        }
-        if (lane == 0) {
-            RowStat st;
-            st.m = kGreedy ? bm : m;
-            st.s = s;
-            st.idx = bi;
-            st.pad = 0;
-            p.stats[(size_t)row * p.nsub + sub] = st;
-        }
+                    for (int i = 0; i < kStatVec; ++i) {
+                        const int v = v0 + 4 * (lane + 32 * i);
+                        stat_elem<true>(buf[i].x, v + 0, c2, m, s, bm, bi);
+                        stat_elem<true>(buf[i].y, v + 1, c2, m, s, bm, bi);
+                        stat_elem<true>(buf[i].z, v + 2, c2, m, s, bm, bi);
+                        stat_elem<true>(buf[i].w, v + 3, c2, m, s, bm, bi);
+                    }
+                } else {
+                    // the lane's maximum first, then one pass of 2^(t - max)
 #pragma unroll
-        for (int i = 0; i < kStatVec; ++i) buf[i] = nxt[i];
-    }
-}
-
-// One CTA per request: each row's units combined by a warp, then the drafts
-// decided left to right (one thread per position; the first rejection wins).
-template <bool kGreedy>
-__global__ void __launch_bounds__(kStatThreads) verify_decide_kernel(VerifyParams p) {
-    __shared__ float row_lse[17];
-    __shared__ int row_amax[17];
-    __shared__ float s_pt[16];
-    __shared__ int s_acc[16];
-    const int r = blockIdx.x;
-    if (!p.ok[0] || !p.valid[r]) return;
-    const int first = p.cu[r];
-    const int l = p.cu[r + 1] - first - 1;
-    const int g = p.gamma;
-    const float c2 = p.invT * kLog2e;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int j = warp; j <= l; j += kStatThreads / 32) {
-        const RowStat* rs = p.stats + (size_t)(first + j) * p.nsub;
-        float cm = -INFINITY, cs = 0.0f, am = -INFINITY;
-        int ai = INT_MAX;
-        for (int c = lane; c < p.nsub; c += 32) {
-            const RowStat q = rs[c];
-            if (better(q.m, q.idx, am, ai)) { am = q.m; ai = q.idx; }
-            if (!kGreedy) lse2_merge(cm, cs, q.m, q.s);
-        }
+                    for (int i = 0; i < kStatVec; ++i) {
+                        buf[i].x *= c2; buf[i].y *= c2; buf[i].z *= c2; buf[i].w *= c2;
+                        m = fmaxf(m, fmaxf(fmaxf(buf[i].x, buf[i].y), fmaxf(buf[i].z, buf[i].w)));
+                    }
+                    if (m != -INFINITY) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float m2 = shfl_xor(cm, o), s2 = shfl_xor(cs, o), am2 = shfl_xor(am, o);
-            const int ai2 = shfl_xor(ai, o);
-            lse2_merge(cm, cs, m2, s2);
-            if (better(am2, ai2, am, ai)) { am = am2; ai = ai2; }
+                        for (int i = 0; i < kStatVec; ++i)
+                            s += (exp2f(buf[i].x - m) + exp2f(buf[i].y - m)) + (exp2f(buf[i].z - m) + exp2f(buf[i].w - m));
+                    }
+                }
+            } else {
+                const int v1 = min(V, v0 + kStatChunk);
+                const float* base = p.target + (size_t)row * V;
+                for (int v = v0 + lane; v < v1; v += 32) stat_elem<kGreedy>(__ldg(base + v), v, c2, m, s, bm, bi);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float m2 = shfl_xor(m, o), s2 = shfl_xor(s, o), bm2 = shfl_xor(bm, o);
+                const int bi2 = shfl_xor(bi, o);
+                lse2_merge(m, s, m2, s2);
+                if (better(bm2, bi2, bm, bi)) { bm = bm2; bi = bi2; }
+            }
+            if (lane == 0) {
+                RowStat stt;
+                stt.m = kGreedy ? bm : m;
+                stt.s = s;
+                stt.idx = bi;
+                stt.pad = 0;
+                p.stats[(size_t)r * p.nsub + sub] = stt;
+            }
+#pragma unroll
+            for (int i = 0; i < kStatVec; ++i) buf[i] = nxt[i];
         }
-        if (lane == 0) {
-            row_lse[j] = kGreedy ? 0.0f : cm + log2f(cs);  // base-2 log-normaliser
-            row_amax[j] = ai;
+        if (!grid_barrier(st, gen)) break;
+        // ---- one warp per active request: merge its units, decide draft j
+        for (int a = w0; a < n_act; a += nw) {
+            // a == w0 was prefetched at the round start (lane 0)
+            const bool pre = (a == w0);
+            const int r = pre ? __shfl_sync(0xFFFFFFFFu, d_r, 0) : act_at(a);
+            const int valid = pre ? __shfl_sync(0xFFFFFFFFu, d_valid, 0) : p.valid[r];
+            if (!valid) continue;
+            const int first = pre ? __shfl_sync(0xFFFFFFFFu, d_first, 0) : p.cu[r];
+            const int l = pre ? __shfl_sync(0xFFFFFFFFu, d_l, 0) : p.cu[r + 1] - first - 1;
+            const RowStat* rs = p.stats + (size_t)r * p.nsub;
+            float cm = -INFINITY, cs = 0.0f, am = -INFINITY;
+            int ai = INT_MAX;
+            for (int c = lane; c < p.nsub; c += 32) {
+                // written by other CTAs in this launch: read from L2, not a stale L1 line
+                const float4 q4 = __ldcg(reinterpret_cast<const float4*>(rs + c));
+                RowStat q;
+                q.m = q4.x; q.s = q4.y; q.idx = __float_as_int(q4.z); q.pad = 0;
+                if (better(q.m, q.idx, am, ai)) { am = q.m; ai = q.idx; }
+                if (!kGreedy) lse2_merge(cm, cs, q.m, q.s);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float m2 = shfl_xor(cm, o), s2 = shfl_xor(cs, o), am2 = shfl_xor(am, o);
+                const int ai2 = shfl_xor(ai, o);
+                lse2_merge(cm, cs, m2, s2);
+                if (better(am2, ai2, am, ai)) { am = am2; ai = ai2; }
+            }
+            const float lse2 = kGreedy ? 0.0f : cm + log2f(cs);  // base-2 log-normaliser of row j
+            int n = -1;  // the request's number of accepted drafts once decided
+            if (j == l) {
+                n = l;  // every draft accepted: the extra token comes from this row
+            } else if (lane == 0) {
+                const int yj = pre ? d_y : p.y[(size_t)r * g + j];
+                bool accept;
+                float pt;
+                if (kGreedy) {
+                    accept = (yj == ai);
+                    pt = accept ? 1.0f : 0.0f;
+                } else {
+                    const float tv = pre ? d_t : p.target[(size_t)(first + j) * V + yj];
+                    const float qv = pre ? d_q : p.q_tok[(size_t)r * g + j];
+                    const uint64_t seed = pre ? d_seed : p.seeds[r];
+                    pt = exp2f(tv * c2 - lse2);
+                    const float ratio = pt / qv;
+                    const uint4 w = philox4x32_10(make_uint4(0u, (uint32_t)j, (uint32_t)r, ctr_word3(p.cycle, kAccept)),
+                                                  (uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32));
+                    accept = uniform_from_bits(w.x) < ratio;
+                }
+                if (p.p_tok) p.p_tok[(size_t)r * g + j] = pt;
+                if (accept) p.act[r] = j + 1;  // goes on to round j + 1
+                else n = j;
+            }
+            n = __shfl_sync(0xFFFFFFFFu, n, 0);
+            if (n < 0) continue;
+            int32_t* out = p.out_tokens + (size_t)r * (g + 1);
+            for (int jj = lane; jj <= g; jj += 32)
+                if (jj != n) out[jj] = jj < n ? p.y[(size_t)r * g + jj] : -1;
+            if (lane == 0) {
+                p.n_acc[r] = n;
+                if (kGreedy) {
+                    out[n] = (ai >= 0 && ai < V) ? ai : -1;
+                    if (out[n] < 0) report(p.dev_status, DSPARK_ERR_DEVICE_INPUT);  // NaN row
+                } else {
+                    VerifyJob job;
+                    job.row = first + n;
+                    job.pos = n;
+                    job.mode = (n < l) ? 1 : 2;
+                    job.pad = 0;
+                    job.lse = lse2 * kLn2;  // natural log-normaliser of t = row * invT
+                    job.pad2[0] = job.pad2[1] = job.pad2[2] = 0.0f;
+                    p.jobs[r] = job;
+                }
+            }
         }
+        if (!grid_barrier(st, gen)) break;
+        // every CTA lists the requests accepted in this round (flags written by
+        // other CTAs: read from L2)
+        if (threadIdx.x < 32) {
+            int cnt = 0;
+            for (int base = 0; base < p.R; base += 32) {
+                const bool f = base + lane < p.R && __ldcg(p.act + base + lane) == j + 1;
+                const unsigned m = __ballot_sync(0xFFFFFFFFu, f);
+                if (f) s_list[cnt + __popc(m & ((1u << lane) - 1u))] = base + lane;
+                cnt += __popc(m);
+            }
+            if (lane == 0) s_nact = cnt;
+        }
+        __syncthreads();
+        n_act = s_nact;
+        all = false;
     }
-    __syncthreads();
-    const int j = threadIdx.x;
-    if (j < l) {
-        const int yj = p.y[(size_t)r * g + j];
-        bool accept;
-        float pt;
-        if (kGreedy) {
-            accept = (yj == row_amax[j]);
-            pt = accept ? 1.0f : 0.0f;
-        } else {
-            pt = exp2f(p.target[(size_t)(first + j) * p.V + yj] * c2 - row_lse[j]);
-            const float ratio = pt / p.q_tok[(size_t)r * g + j];
-            const uint4 w = philox4x32_10(make_uint4(0u, (uint32_t)j, (uint32_t)r, ctr_word3(p.cycle, kAccept)),
-                                          (uint32_t)(p.seeds[r] & 0xFFFFFFFFu), (uint32_t)(p.seeds[r] >> 32));
-            accept = uniform_from_bits(w.x) < ratio;
-        }
-        s_pt[j] = pt;
-        s_acc[j] = accept;
-    }
-    __syncthreads();
-    int n = l;  // accepted drafts: up to the first rejection
-    for (int i = 0; i < l; ++i)
-        if (!s_acc[i]) { n = i; break; }
-    if (j < l && j <= n && p.p_tok) p.p_tok[(size_t)r * g + j] = s_pt[j];
-    int32_t* out = p.out_tokens + (size_t)r * (g + 1);
-    if (j <= g && j != n) out[j] = j < n ? p.y[(size_t)r * g + j] : -1;
-    if (j == 0) {
-        p.n_acc[r] = n;
-        if (kGreedy) {
-            const int tok = row_amax[n];
-            out[n] = (tok >= 0 && tok < p.V) ? tok : -1;
-            if (out[n] < 0) report(p.dev_status, DSPARK_ERR_DEVICE_INPUT);  // NaN row
-        } else {
-            VerifyJob job;
-            job.row = first + n;
-            job.pos = n;
-            job.mode = (n < l) ? 1 : 2;
-            job.pad = 0;
-            job.lse = row_lse[n] * kLn2;  // natural log-normaliser of t = row * invT
-            job.pad2[0] = job.pad2[1] = job.pad2[2] = 0.0f;
-            p.jobs[r] = job;
-        }
-    }
+    if (blockIdx.x == 0 && threadIdx.x == 0 && *reinterpret_cast<volatile int*>(st + kAbort))
+        report(p.dev_status, DSPARK_ERR_TIMEOUT);
 }
 
 __device__ __forceinline__ void block_sample(float& best, int& idx, float& best2, int& idx2,
@@ -363,23 +465,25 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_correct_kernel(VerifyPa
 
 cudaError_t launch_verify_decide(const VerifyParams& p, cudaStream_t stream) {
     verify_prologue_kernel<<<1, 1024, 0, stream>>>(p);
-    const long long units = (long long)p.max_rows * p.nsub;  // at most: the rows in use are read on the device
-    if (units > 0) {
-        int dev = 0, n_sm = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return cudaGetLastError();
-        // enough resident warps to keep each SM's share of the stream in flight
-        const long long warps = std::min<long long>(units, 24LL * n_sm);
-        const unsigned grid1 = (unsigned)((warps * 32 + kStatThreads - 1) / kStatThreads);
-        if (p.greedy) {
-            verify_stats_kernel<true><<<grid1, kStatThreads, 0, stream>>>(p);
-            verify_decide_kernel<true><<<p.R, kStatThreads, 0, stream>>>(p);
-        } else {
-            verify_stats_kernel<false><<<grid1, kStatThreads, 0, stream>>>(p);
-            verify_decide_kernel<false><<<p.R, kStatThreads, 0, stream>>>(p);
-        }
-    }
+    int dev = 0, n_sm = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaGetLastError();
+    const void* fn = p.greedy ? reinterpret_cast<const void*>(verify_rounds_kernel<true>)
+                              : reinterpret_cast<const void*>(verify_rounds_kernel<false>);
+    if ((size_t)p.R * sizeof(int) > kMaxListBytes) return cudaErrorInvalidValue;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxListBytes) != cudaSuccess)
+        return cudaGetLastError();
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kRoundThreads, sizeof(int) * p.R);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+    // every CTA resident at once (cooperative launch): the rounds meet at grid barriers
+    const int grid = n_sm;
+    const size_t smem = sizeof(int) * (size_t)p.R;
+    VerifyParams arg = p;
+    void* args[] = {&arg};
+    e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kRoundThreads), args, smem, stream);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
