@@ -361,6 +361,23 @@ def run_ours(args):
         e2e = {"value": world * n_e2e / (e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo, "steps": n_e2e}
 
+    # verify reads target rows only up to each request's first rejection: its
+    # data-dependent algorithmic bytes (those rows, plus for T > 0 the residual
+    # draw's W2 pass and one target row and one U row per request) per verify call
+    verify_roof = None
+    if run_verify:
+        n_h = n_acc.cpu().numpy().astype(np.int64)
+        l_h = l.cpu().numpy().astype(np.int64)
+        ok = n_h >= 0
+        rows_read = int((np.minimum(n_h[ok], l_h[ok]) + 1).sum())
+        vbytes = rows_read * V * 4
+        if T > 0:
+            vbytes += V * rank_r * 2 + int(ok.sum()) * V * (4 + 2)
+        v_ms = per["verify"]
+        verify_roof = {"bound": "hbm", "achieved": vbytes / (v_ms / 1000.0) / 1e9, "peak": hbm, "unit": "GB/s",
+                       "frac": vbytes / (v_ms / 1000.0) / 1e9 / hbm, "algorithmic_bytes_per_call": vbytes,
+                       "rows_read": rows_read, "rows_presented": int((l_h + 1).sum()), "call_ms": v_ms}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.stage == "cycle":
         per_req, sample = oracle_sample(w, d, inputs.target_full(w, d["U"]), 4, 0)
@@ -373,7 +390,7 @@ def run_ours(args):
                 "dtype": "bf16 GEMM (fp32 accumulate) + fp32 softmax/verify",
                 "data": "synthetic (seeded; shapes and laws of the workload)",
                 "config": dict(workload_config(w), parallelism=f"replicas x{world}"),
-                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+                "roofline": roof, "verify_roofline": verify_roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
                 "gpu_launches": launches_per_step * args.steps,
                 "stage": args.stage, "stage_ms": per, "logits_gb_s": (R * (gamma + 1) * V * 4 + R * gamma * V * 2) /
                 (ms_step / 1000.0) / 1e9, "draft_path": "tcgen05" if uses_tc else "simt"}
