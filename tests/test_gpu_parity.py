@@ -253,6 +253,13 @@ def test_select_ties_and_errors(B, orc):
         o = orc.select_prefix(c, None, None, None, K_cap, 0)
         g = H.gpu_select(c, None, None, None, K_cap, 0)
         np.testing.assert_array_equal(g["l"], o["l"])
+    # a confidence of -0 is a survival of 0: it ties with +0 (position, then request order)
+    cz = np.array([[-0.0, 0.5], [0.0, 1.0], [0.3, -0.0], [0.0, 0.0]], np.float32)
+    for K_cap in range(4, 13):
+        o = orc.select_prefix(cz, None, None, None, K_cap, 0)
+        g = H.gpu_select(cz, None, None, None, K_cap, 0)
+        np.testing.assert_array_equal(g["l"], o["l"])
+        np.testing.assert_array_equal(g["cu_seqlens"], o["cu_seqlens"])
     bad = c.copy(); bad[2, 1] = np.nan
     g = H.gpu_select(bad, None, None, None, 6, 0)
     assert g["status"] == -6 and (g["l"] == -1).all()
