@@ -10,8 +10,9 @@
 // row after the block.
 //
 // One pipeline, two epilogues:
-//   draft     one launch per position k: logits of every request, Gumbel-max
-//             sample and the pieces of its log-normaliser and q(y);
+//   draft     one launch for the whole block: at each position k the logits of
+//             every request, the Gumbel-max sample and the pieces of its
+//             log-normaliser and q(y);
 //   residual  one launch per verify: for every request the drafter's logits of
 //             its rejected row are recomputed here (the residual needs q on the
 //             whole vocabulary, and recomputing one row per request costs one
@@ -20,10 +21,10 @@
 //             full acceptance.
 //
 // Persistent, one CTA per SM, 19 warps:
-//   A (M = 128 requests x K = rank) = rows W1[prev], gathered once per launch
-//     into a workspace matrix H by a small kernel (spread over many SMs: the
-//     rows are scattered over W1's pages), loaded by TMA into 128-byte-swizzled
-//     shared memory and resident for the launch;
+//   A (M = 128 requests x K = rank) = rows W1[prev], copied by the epilogue
+//     warps into 128-byte-swizzled shared memory at the start of each step
+//     (prev: the anchor at k = 0, else the step's predecessor decoded from the
+//     previous step's winner keys) and resident for the step;
 //   B (N = 128 vocabulary rows x K = rank) = W2 tiles streamed by TMA through a
 //     ring of 16 KB stages; the next tile's boxes are prefetched into L2 one
 //     tile ahead so the ring only has to cover L2 latency;
@@ -49,18 +50,19 @@
 // 64-bit key per request and step with atomicMax (order-preserving bits of
 // the score above the inverted index, so ties go to the lower index), and
 // stores its (max, sum of exp, winner logit) piece of the normaliser.  The
-// next draft step decodes its A rows' tokens from the keys (it is launched
-// as a programmatic dependent and waits for the previous step before reading
-// them, while its producer already streams W2), and one finalize kernel after
-// the last step turns keys and pieces into tokens, q_lse and q(y).  The chain
-// gather -> step -> gather -> ... -> finalize is launched with programmatic
-// stream serialization: each launch starts as the previous one retires, its
-// producers pull its first W2 and U tiles into L2, and only reading H / the
-// keys waits for the previous launch to complete.
+// draft's steps run in one cooperative launch: after step k every CTA passes
+// a grid barrier (a counter per step, bounded spin) and only then decodes the
+// next A rows from the keys of step k.  Nothing else waits: the W2 ring and
+// the U passes do not depend on the draws and stream on into the next step
+// while the epilogue finishes the current one, and tensor memory, barriers
+// and the ring are set up once per block instead of once per position.  One
+// finalize kernel after the last step (a programmatic dependent) turns keys
+// and pieces into tokens, q_lse and q(y).
 //
-// Warp roles: warp 0 = W2/A TMA producer, warp 1 = MMA issuer (and TMEM
-// owner), warp 2 = U TMA producer (draft), warps 3-18 = epilogue.  Every mbarrier wait is bounded (2 s);
-// a timeout aborts the CTA cleanly and reports DSPARK_ERR_TIMEOUT.
+// Warp roles: warp 0 = W2 TMA producer, warp 1 = MMA issuer (and TMEM
+// owner), warp 2 = U TMA producer (draft), warps 3-18 = epilogue (and the A
+// rows).  Every mbarrier wait and the grid barrier are bounded (2 s); a timeout
+// aborts every CTA cleanly and reports DSPARK_ERR_TIMEOUT.
 #include <cuda.h>
 
 #include "draft_tc.cuh"
@@ -116,14 +118,14 @@ struct TcParams {
     const uint16_t* U;
     const uint16_t* W1;
     unsigned long long* keys;  // draft [gamma][R]; residual [R]
-    const int32_t* toks;       // draft [R]: the A rows' tokens (-2: no usable predecessor)
+    unsigned* step_done;       // draft [gamma]: CTAs done with step k; then one abort word
     float4* parts;             // draft [gamma][R][P]: (max, sum, winner logit, winner) per CTA
     const uint64_t* seeds;
     int32_t* dev_status;
     uint32_t cycle;
     float invT;
     int greedy;
-    int R, gamma, V, rank, k;
+    int R, gamma, V, rank;
     int nb, P, n_tiles, n_stages, nkb;
     const int32_t* anchor;
     float* q_logits;
@@ -135,13 +137,15 @@ struct Bars {
     uint64_t full[kMaxStages], empty[kMaxStages];
     uint64_t tfull[2], tempty[2];
     uint64_t ufull[2], uempty[2];
-    uint64_t afull, mma_done;
+    uint64_t afull, mma_done;  // afull: the step's A rows are in shared memory (one arrival per epilogue warp)
     uint32_t tmem_slot;
     int abort_flag;
-    // per request row and epilogue quarter: the best race record so far as
-    // log2(w / E) in absolute units (-inf: none), read by the row's other quarters
-    float g_share[4][kM];
+    int step_ok;               // the grid barrier after a step passed (read by every epilogue warp)
+    int a_tok[kM];             // the step's A rows' tokens: -1 zero row, -2 nothing to compute for the request
 };
+// Residual: per request row and epilogue quarter, the best race record so far
+// as log2(w / E) in absolute units (-inf: none), read by the row's other quarters.
+constexpr size_t kShareBytes = 4 * kM * sizeof(float);
 
 __device__ __forceinline__ void merge_draft(float& sc, int& ix, float& sa, float& m, float& su, float sc2, int ix2,
                                             float sa2, float m2, float su2) {
@@ -250,48 +254,45 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
-// Copies W1[t] (zeros for t < 0) into row r of H: one warp, 16-byte pieces.
-__device__ __forceinline__ void copy_w1_row(const uint16_t* W1, int t, int rank, uint16_t* H, int r, int lane) {
-    const int cpr = rank >> 3;
-    const uint4* src = reinterpret_cast<const uint4*>(W1 + (size_t)(t < 0 ? 0 : t) * rank);
-    uint4* dst = reinterpret_cast<uint4*>(H + (size_t)r * rank);
-    for (int c = lane; c < cpr; c += 32) dst[c] = t >= 0 ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+// 16 bytes global -> shared without registers; zeros when !valid (nothing read).
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(tc::smem_u32(dst)), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
 }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// The A rows of draft step k, one small CTA per request (the rows lie on
-// scattered pages of W1; one row per SM keeps the address translations of the
-// gather in parallel): the predecessor token (the anchor at k = 0, else the
-// winner of step k - 1 decoded from its key; -1 no anchor, -2 unusable: the
-// step then computes nothing for the request) and its W1 row.
-constexpr int kGatherThreads = 64;
-__global__ void __launch_bounds__(kGatherThreads) gather_a_rows_kernel(const uint16_t* W1, const int32_t* anchor,
-                                                                       const unsigned long long* prev_keys, int k,
-                                                                       int R, int V, int rank, uint16_t* H,
-                                                                       int32_t* toks) {
-    griddep_launch_dependents();
-    griddep_wait();  // the previous step's keys
-    const int r = blockIdx.x;
-    int t;
-    if (k == 0) {
-        const int a = anchor[r];
-        t = a >= V ? -2 : (a < 0 ? -1 : a);
-    } else {
-        const unsigned long long key = prev_keys[r];
-        t = key ? key_index(key) : -2;
+// The 16 epilogue warps alone (named barrier 1; barrier 0 is the CTA's).
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); }
+
+// Between two draft steps, one thread per CTA: every CTA's winner keys of the
+// step are published (its threads passed a CTA barrier after their atomics)
+// before any CTA reads them.  done counts the CTAs through the step (zeroed
+// with the keys before the launch, used once).  Bounded: gives up after the
+// wait limit or when another CTA gave up (abort word), raising the abort word
+// itself on a timeout.
+__device__ __forceinline__ bool step_barrier(unsigned* done, int* abort_word, unsigned n_cta) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(done) : "memory");
+    const uint64_t t0 = global_ns();
+    for (unsigned it = 1;; ++it) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(done) : "memory");
+        if (v >= n_cta) break;
+        if ((it & 15) == 0) {
+            if (*reinterpret_cast<volatile int*>(abort_word)) return false;
+            if (global_ns() - t0 > kWaitNs) {
+                atomicExch(abort_word, 1);
+                return false;
+            }
+        }
     }
-    if (threadIdx.x == 0) toks[r] = t;
-    const int cpr = rank >> 3;
-    const uint4* src = reinterpret_cast<const uint4*>(W1 + (size_t)(t < 0 ? 0 : t) * rank);
-    uint4* dst = reinterpret_cast<uint4*>(H + (size_t)r * rank);
-    for (int c = threadIdx.x; c < cpr; c += kGatherThreads) dst[c] = t >= 0 ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+    return true;
 }
 
-// Per request after the verify decisions: what the residual launch draws, and
-// its A row W1[prev] of the rejected position (zeros for a bonus draw).  One
-// warp per request.
-__global__ void __launch_bounds__(256) residual_prep_kernel(ResidualTcArgs a, ResRow* rows, uint16_t* H) {
-    const int r = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
-    const int lane = threadIdx.x & 31;
+// Per request after the verify decisions: what the residual launch draws and
+// the token whose W1 row is its A row.  One thread per request.
+__global__ void __launch_bounds__(256) residual_prep_kernel(ResidualTcArgs a, ResRow* rows) {
+    const int r = (int)(blockIdx.x * (size_t)blockDim.x + threadIdx.x);
     if (r >= a.R) return;
     const VerifyJob job = a.jobs[r];
     const int mode = a.valid[r] ? job.mode : 0;
@@ -309,20 +310,22 @@ __global__ void __launch_bounds__(256) residual_prep_kernel(ResidualTcArgs a, Re
     w.q_lse2 = mode == 1 ? a.q_lse[(size_t)r * a.gamma + job.pos] * kLog2eF : 0.0f;
     w.prev = prev;
     w.pad = 0.0f;
-    if (lane == 0) rows[r] = w;
-    copy_w1_row(static_cast<const uint16_t*>(a.W1), prev, a.rank, H, r, lane);
+    rows[r] = w;
 }
 
 template <bool kRes>
 __global__ void __launch_bounds__(kThreads, 1)
-markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_u,
-                 const __grid_constant__ CUtensorMap tm_h, const TcParams p) {
+markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_u, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sU = sA + p.nkb * kTileBytes;          // draft: two pass buffers of base logits
     uint8_t* sB = sU + (kRes ? 0 : 2 * kUBufBytes);
     Bars& bar = *reinterpret_cast<Bars*>(sB + p.n_stages * kTileBytes);
+    float* g_share = reinterpret_cast<float*>(&bar + 1);  // residual: [4][kM]
+    // the quarters' exchange at the end of a step ([3][kM]) uses the A rows' space:
+    // the step's MMAs have completed and the next step's rows are not written yet
+    TcPartial* scratch = reinterpret_cast<TcPartial*>(sA);
     volatile int* abort_flag = &bar.abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -330,13 +333,15 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
     const int cidx = blockIdx.x / p.nb;
     const int row0 = blk * kM;
     const int S = p.n_stages;
+    const int n_steps = kRes ? 1 : p.gamma;
 
-    for (int e = threadIdx.x; e < 4 * kM; e += kThreads) (&bar.g_share[0][0])[e] = -INFINITY;
+    if (kRes)
+        for (int e = threadIdx.x; e < 4 * kM; e += kThreads) g_share[e] = -INFINITY;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) { tc::mbar_init(&bar.full[s], 1); tc::mbar_init(&bar.empty[s], 1); }
         for (int a = 0; a < 2; ++a) { tc::mbar_init(&bar.tfull[a], 1); tc::mbar_init(&bar.tempty[a], kEpiWarps); }
         for (int a = 0; a < 2; ++a) { tc::mbar_init(&bar.ufull[a], 1); tc::mbar_init(&bar.uempty[a], kEpiWarps); }
-        tc::mbar_init(&bar.afull, 1);
+        tc::mbar_init(&bar.afull, kEpiWarps);
         tc::mbar_init(&bar.mma_done, 1);
         bar.abort_flag = 0;
         tc::fence_barrier_init();
@@ -348,16 +353,16 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
     if (warp == 0 && lane == 0) {
         tc::prefetch_tmap(&tm_w2);
         if (!kRes) tc::prefetch_tmap(&tm_u);
-        tc::prefetch_tmap(&tm_h);
     }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    // The next launch may be scheduled as SMs free up; it waits (griddepcontrol)
-    // before it reads anything this one writes.
+    // the launch after this one (the finalize) may be scheduled early; it waits
+    // (griddepcontrol) for this one to complete before reading its results
     griddep_launch_dependents();
     const uint32_t tmem_base = bar.tmem_slot;
     const int n_local = cidx < p.n_tiles ? (p.n_tiles - 1 - cidx) / p.P + 1 : 0;
+    const int n_tl = n_steps * n_local;  // tiles of this CTA over the launch: step-major
 
     // this thread's running partial (epilogue threads)
     TcPartial part = identity_partial<kRes>();
@@ -365,52 +370,39 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        // W2 and U are inputs no launch of this library writes: the first tiles
-        // are requested into L2 before waiting for the previous launch, which
-        // wrote H; A is loaded first, then the W2 ring.
+        // The W2 ring, tile-major over every step of the launch (the tiles are the
+        // same at each step): nothing here depends on the draws, so the ring runs
+        // into the next step while the epilogue finishes the current one.
         if (lane == 0) {
-            for (int i = 0; i < 2 && i < n_local; ++i) {
-                const int t = cidx + i * p.P;
-                for (int q = 0; q < p.nkb; ++q) tma_prefetch_l2_2d(&tm_w2, q * kKB, t * kNV);
+            // L2 prefetch of global tile g (W2 boxes and, draft, the step's U passes)
+            auto prefetch_tile = [&](int g) {
+                const int tn = cidx + (g % n_local) * p.P;
+                for (int q = 0; q < p.nkb; ++q) tma_prefetch_l2_2d(&tm_w2, q * kKB, tn * kNV);
                 if (!kRes) {
-                    tc::tma_prefetch_l2_3d(&tm_u, t * kNV, p.k, row0);
-                    tc::tma_prefetch_l2_3d(&tm_u, t * kNV + kKB, p.k, row0);
-                }
-            }
-            const int n_loads = n_local * p.nkb;  // W2 stage loads, tile-major
-            int issued = 0;
-            bool ok = true;
-            // the stage of load l is l % S, used for the (l / S)-th time
-            auto issue = [&](int l) {
-                const int s = l % S, i = l / p.nkb, kb = l - i * p.nkb;
-                const int t = cidx + i * p.P;
-                tc::mbar_arrive_expect_tx(&bar.full[s], kTileBytes);
-                tc::tma_load_2d(sB + s * kTileBytes, &tm_w2, &bar.full[s], kb * kKB, t * kNV);
-                // once a tile's first ring of loads is out, pull the next tile into L2
-                if (kb == min(S, p.nkb) - 1 && i + 1 < n_local) {
-                    const int tn = t + p.P;
-                    for (int q = 0; q < p.nkb; ++q) tma_prefetch_l2_2d(&tm_w2, q * kKB, tn * kNV);
-                    if (!kRes) {
-                        tc::tma_prefetch_l2_3d(&tm_u, tn * kNV, p.k, row0);
-                        tc::tma_prefetch_l2_3d(&tm_u, tn * kNV + kKB, p.k, row0);
-                    }
+                    tc::tma_prefetch_l2_3d(&tm_u, tn * kNV, g / n_local, row0);
+                    tc::tma_prefetch_l2_3d(&tm_u, tn * kNV + kKB, g / n_local, row0);
                 }
             };
-            griddep_wait();
-            // A: the block's H rows, resident for the launch
-            tc::mbar_arrive_expect_tx(&bar.afull, (uint32_t)(p.nkb * kTileBytes));
-            for (int kb = 0; kb < p.nkb; ++kb) tc::tma_load_2d(sA + kb * kTileBytes, &tm_h, &bar.afull, kb * kKB, row0);
+            for (int g = 0; g < 2 && g < n_tl; ++g) prefetch_tile(g);
+            const int n_loads = n_tl * p.nkb;  // W2 stage loads
+            int issued = 0;
+            bool ok = true;
             for (; issued < n_loads; ++issued) {
+                // load l goes to stage l % S, used for the (l / S)-th time
                 const int s = issued % S;
                 const uint32_t ph = (uint32_t)((issued / S) & 1);
                 if (!tc::mbar_wait(&bar.empty[s], ph ^ 1u, abort_flag, kWaitNs)) { ok = false; break; }
-                issue(issued);
+                const int g = issued / p.nkb, kb = issued - g * p.nkb;
+                const int t = cidx + (g % n_local) * p.P;
+                tc::mbar_arrive_expect_tx(&bar.full[s], kTileBytes);
+                tc::tma_load_2d(sB + s * kTileBytes, &tm_w2, &bar.full[s], kb * kKB, t * kNV);
+                // once a tile's first ring of loads is out, pull the next tile into L2
+                if (kb == min(S, p.nkb) - 1 && g + 1 < n_tl) prefetch_tile(g + 1);
             }
             // the copies this thread issued must land before the CTA exits
-            int dummy = 0;
-            volatile int* no_abort = &dummy;
-            tc::mbar_wait(&bar.afull, 0, no_abort, kWaitNs);
             if (!ok) {
+                int dummy = 0;
+                volatile int* no_abort = &dummy;
                 for (int l = max(0, issued - S); l < issued; ++l)
                     tc::mbar_wait(&bar.full[l % S], (uint32_t)((l / S) & 1), no_abort, kWaitNs);
             }
@@ -420,31 +412,35 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = tc::idesc_bf16_f32(kM, kNV);
-            bool ok = tc::mbar_wait(&bar.afull, 0, abort_flag, kWaitNs);
-            tc::tc_fence_after();
+            bool ok = true;
             int s = 0;
             uint32_t ph = 0;
             const uint32_t a_base = tc::smem_u32(sA), b_base = tc::smem_u32(sB);
-            for (int i = 0; ok && i < n_local; ++i) {
-                const int a = i & 1;
-                const uint32_t use = (uint32_t)(i >> 1);
-                if (!tc::mbar_wait(&bar.tempty[a], (use & 1u) ^ 1u, abort_flag, kWaitNs)) { ok = false; break; }
+            for (int k = 0; ok && k < n_steps; ++k) {
+                // the step's A rows, written by the epilogue warps
+                if (!tc::mbar_wait(&bar.afull, (uint32_t)(k & 1), abort_flag, kWaitNs)) { ok = false; break; }
                 tc::tc_fence_after();
-                const uint32_t d = tmem_base + (uint32_t)(a * kNV);
-                for (int kb = 0; kb < p.nkb; ++kb) {
-                    if (!tc::mbar_wait(&bar.full[s], ph, abort_flag, kWaitNs)) { ok = false; break; }
+                for (int i = 0; ok && i < n_local; ++i) {
+                    const int g = k * n_local + i;
+                    const int a = g & 1;
+                    const uint32_t use = (uint32_t)(g >> 1);
+                    if (!tc::mbar_wait(&bar.tempty[a], (use & 1u) ^ 1u, abort_flag, kWaitNs)) { ok = false; break; }
                     tc::tc_fence_after();
-                    const uint32_t aa = a_base + (uint32_t)(kb * kTileBytes);
-                    const uint32_t bb = b_base + (uint32_t)(s * kTileBytes);
+                    const uint32_t d = tmem_base + (uint32_t)(a * kNV);
+                    for (int kb = 0; kb < p.nkb; ++kb) {
+                        if (!tc::mbar_wait(&bar.full[s], ph, abort_flag, kWaitNs)) { ok = false; break; }
+                        tc::tc_fence_after();
+                        const uint32_t aa = a_base + (uint32_t)(kb * kTileBytes);
+                        const uint32_t bb = b_base + (uint32_t)(s * kTileBytes);
 #pragma unroll
-                    for (int j = 0; j < kKB / 16; ++j)
-                        tc::umma_bf16(d, tc::smem_desc_sw128(aa + 32u * j), tc::smem_desc_sw128(bb + 32u * j), idesc,
-                                      (kb | j) != 0);
-                    tc::umma_commit(&bar.empty[s]);
-                    if (++s == S) { s = 0; ph ^= 1u; }
+                        for (int j = 0; j < kKB / 16; ++j)
+                            tc::umma_bf16(d, tc::smem_desc_sw128(aa + 32u * j), tc::smem_desc_sw128(bb + 32u * j), idesc,
+                                          (kb | j) != 0);
+                        tc::umma_commit(&bar.empty[s]);
+                        if (++s == S) { s = 0; ph ^= 1u; }
+                    }
+                    if (ok) tc::umma_commit(&bar.tfull[a]);
                 }
-                if (!ok) break;
-                tc::umma_commit(&bar.tfull[a]);
             }
             // every MMA issued has completed before anyone frees tensor memory
             tc::umma_commit(&bar.mma_done);
@@ -455,19 +451,19 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         __syncwarp();
     } else if (warp == 2) {
         // ------------------------------------------------------------ U producer
-        // Draft: the base logits U_k of pass n (tile n / 2, columns 64 (n % 2) ..
-        // + 63 of the tile, all 128 requests) into pass buffer n % 2, one pass ahead
-        // of the epilogue; U is an input, so no wait on the previous launch.
+        // Draft: the base logits U_k of pass n (global tile n / 2, columns 64 (n % 2)
+        // .. + 63 of the tile, all 128 requests) into pass buffer n % 2, one pass
+        // ahead of the epilogue, across the steps of the launch.
         if (!kRes && lane == 0) {
-            const int n_pass = 2 * n_local;
+            const int n_pass = 2 * n_tl;
             int n = 0;
             for (; n < n_pass; ++n) {
-                const int b = n & 1;
-                const uint32_t use = (uint32_t)(n >> 1);
+                const int b = n & 1, g = n >> 1;
+                const uint32_t use = (uint32_t)g;
                 if (!tc::mbar_wait(&bar.uempty[b], (use & 1u) ^ 1u, abort_flag, kWaitNs)) break;
                 tc::mbar_arrive_expect_tx(&bar.ufull[b], (uint32_t)kUBufBytes);
-                tc::tma_load_3d(sU + b * kUBufBytes, &tm_u, &bar.ufull[b], (cidx + (n >> 1) * p.P) * kNV + 64 * b, p.k,
-                                row0);
+                tc::tma_load_3d(sU + b * kUBufBytes, &tm_u, &bar.ufull[b], (cidx + (g % n_local) * p.P) * kNV + 64 * b,
+                                g / n_local, row0);
             }
             // the copies this thread issued must land before the CTA exits
             int dummy = 0;
@@ -477,308 +473,363 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         }
         __syncwarp();
     } else {
-        // the A rows' tokens (draft) were written by the previous launch
-        griddep_wait();
         // ------------------------------------------------------------ epilogue
+        const int e = threadIdx.x - kCtlWarps * 32;  // 0..511
         const int ew = warp - kCtlWarps;   // 0..15
         const int quad = warp & 3;         // TMEM lane quadrant this warp may read
         const int quarter = ew >> 2;       // pass h covers columns 64 h + 16 quarter .. + 15 of a tile
         const int m = quad * 32 + lane;
         const int rr = row0 + m;
-        if (kRes) row_ok = rr < p.R && p.rows[rr].mode != 0;
-        else row_ok = rr < p.R && p.toks[rr] != -2;
         ResRow rinfo;
         rinfo.mode = 0; rinfo.pos = 0; rinfo.trow = 0; rinfo.w3 = 0; rinfo.lse2_p = 0.0f; rinfo.q_lse2 = 0.0f;
-        if (kRes && row_ok) rinfo = p.rows[rr];
+        if (kRes && rr < p.R) rinfo = p.rows[rr];
         const bool sampling = kRes || !p.greedy;
-        const uint64_t seed = (sampling && row_ok) ? p.seeds[rr] : 0ull;
+        const uint64_t seed = (sampling && rr < p.R) ? p.seeds[rr] : 0ull;
         const uint32_t key0 = (uint32_t)(seed & 0xFFFFFFFFu), key1 = (uint32_t)(seed >> 32);
         const uint32_t w3 = kRes ? rinfo.w3 : ctr_word3(p.cycle, kDraftGumbel);
-        const int pos = kRes ? rinfo.pos : p.k;
         const bool with_u = !kRes || rinfo.mode == 1;
-        const size_t rk = (size_t)rr * p.gamma + pos;
-        const uint16_t* urow = p.U + rk * p.V;
         const float* trow = kRes ? p.target + (size_t)rinfo.trow * p.V : nullptr;
-        float* qrow = (!kRes && p.q_logits && row_ok) ? p.q_logits + rk * p.V : nullptr;
         // logits are scaled to base 2 when sampling: s2 = s * log2(e) / T
         const float c2 = sampling ? p.invT * kLog2eF : 1.0f;
-        // exponential-race state (bw, bE) and rho = E_best / w_best with the
-        // slack, the bound of the no-log test.  Residual: an entry that cannot
-        // beat the best record of any thread racing over the same request
-        // cannot be the request's winner either, so rho is taken from the best
-        // of this thread's record, the row's other three quarters in this CTA
-        // (shared memory, every pass) and the request's published key (global,
-        // read a tile late), each as g = log2(w / E) in absolute units.  (The
-        // draft's races gain too little from this to pay for the atomics.)
-        float bw = 0.0f, bE = 1.0f;
-        float rho = INFINITY;
-        float g_own = -INFINITY, g_pub = -INFINITY, g_glob = -INFINITY;
-        unsigned long long gkey = 0;
-        const bool share = kRes && row_ok;
-        unsigned long long* my_key = kRes ? p.keys + rr : p.keys + (size_t)p.k * p.R + rr;
-        volatile float* gsh = &bar.g_share[0][m];  // the row's four quarter records, written by other warps
-        // residual: the 16 base logits (bf16 pairs) of the request's rejected row at v
-        auto load_u = [&](int v, uint32_t(&dst)[8]) {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const uint4 q = (row_ok && v + 8 * j < p.V) ? __ldg(reinterpret_cast<const uint4*>(urow + v) + j)
-                                                             : make_uint4(0u, 0u, 0u, 0u);
-                dst[4 * j + 0] = q.x; dst[4 * j + 1] = q.y; dst[4 * j + 2] = q.z; dst[4 * j + 3] = q.w;
-            }
-        };
         // draft: this thread's 32 bytes of a pass buffer (row m, 16-byte chunks
         // 2 quarter and 2 quarter + 1 of the 128-byte-swizzled row)
         const uint32_t u_off0 = (uint32_t)(m * 128 + (((2 * quarter) ^ (m & 7)) << 4));
         const uint32_t u_off1 = (uint32_t)(m * 128 + (((2 * quarter + 1) ^ (m & 7)) << 4));
-        for (int i = 0; i < n_local; ++i) {
-            const int t = cidx + i * p.P;
-            const int a = i & 1;
-            const uint32_t use = (uint32_t)(i >> 1);
-            if (kRes && row_ok) {
-                // residual rows differ per request: pull this thread's pieces of the
-                // next tile (of this one too, at the start) into L2
-                for (int tt = (i == 0 ? t : t + p.P); tt <= t + p.P && tt < p.n_tiles; tt += p.P) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int v = tt * kNV + 64 * h + kPassCols * quarter;
-                        if (v < p.V) {
-                            prefetch_l2(trow + v);
-                            if (with_u) prefetch_l2(urow + v);
-                        }
+        const int cpr = p.rank >> 3;  // 16-byte pieces of a W1 row (at most 64)
+
+        for (int k = 0; k < n_steps; ++k) {
+            // ---- the step's A rows: tokens (the anchor at k = 0, else the previous
+            // step's winner, decoded from its key; residual: the rejected
+            // position's predecessor), then W1 rows into the 128-byte-swizzled
+            // K-major layout the MMA descriptors describe: 16-byte piece c of row j
+            // at k-block c / 8, row j, piece (c % 8) ^ (j % 8)
+            if (e < kM) {
+                const int r = row0 + e;
+                int t = -2;
+                if (r < p.R) {
+                    if constexpr (kRes) {
+                        const ResRow& rw = p.rows[r];
+                        t = rw.mode == 0 ? -2 : rw.prev;
+                    } else if (k == 0) {
+                        const int an = p.anchor[r];
+                        t = an >= p.V ? -2 : (an < 0 ? -1 : an);
+                    } else {
+                        // published by every CTA's atomics before the step barrier: read from L2
+                        const unsigned long long key = __ldcg(p.keys + (size_t)(k - 1) * p.R + r);
+                        t = key ? key_index(key) : -2;
                     }
                 }
+                bar.a_tok[e] = t;
             }
-            if (share) {
-                if (i > 0) g_glob = key_log2_ratio(gkey);
-                gkey = *reinterpret_cast<volatile unsigned long long*>(my_key);
-            }
-            // warp-uniform wait: every lane waits (acquire), all leave together
-            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.tfull[a], use & 1u, abort_flag, kWaitNs))) break;
-            tc::tc_fence_after();
-            const uint32_t taddr =
-                tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(a * kNV + quarter * kPassCols);
+            epi_sync();
+            // warp ew copies rows 8 ew .. 8 ew + 7, every piece in flight at once
 #pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                const int v0 = t * kNV + 64 * h + kPassCols * quarter;
-                const int nvalid = min(16, p.V - v0);  // the same in the whole warp
-                float sv[16];
-                uint32_t uw[8];
-                float tv[16];
-                if constexpr (kRes) {
-                    // residual: target logits (past the row end -inf: p = 0) and, for a
-                    // rejected row, the drafter's base logits; requested before the
-                    // accumulator is read
+            for (int q = 0; q < 8; ++q) {
+                const int j = 8 * ew + q;
+                const int t = bar.a_tok[j];
+                const uint4* src = reinterpret_cast<const uint4*>(p.W1 + (size_t)(t < 0 ? 0 : t) * p.rank);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int c = lane + 32 * h;
+                    if (c < cpr)
+                        cp_async_16(sA + (c >> 3) * kTileBytes + j * 128 + (((c & 7) ^ (j & 7)) << 4), src + c, t >= 0);
+                }
+            }
+            cp_async_wait_all();
+            // the rows are read by the tensor cores (async proxy)
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bar.afull);
+
+            row_ok = rr < p.R && bar.a_tok[m] != -2;
+            if (kRes) row_ok = row_ok && rinfo.mode != 0;
+            const int pos = kRes ? rinfo.pos : k;
+            const size_t rk = (size_t)rr * p.gamma + pos;
+            const uint16_t* urow = p.U + rk * p.V;
+            float* qrow = (!kRes && p.q_logits && row_ok) ? p.q_logits + rk * p.V : nullptr;
+            part = identity_partial<kRes>();
+            // exponential-race state (bw, bE) and rho = E_best / w_best with the
+            // slack, the bound of the no-log test.  Residual: an entry that cannot
+            // beat the best record of any thread racing over the same request
+            // cannot be the request's winner either, so rho is taken from the best
+            // of this thread's record, the row's other three quarters in this CTA
+            // (shared memory, every pass) and the request's published key (global,
+            // read a tile late), each as g = log2(w / E) in absolute units.  (The
+            // draft's races gain too little from this to pay for the atomics.)
+            float bw = 0.0f, bE = 1.0f;
+            float rho = INFINITY;
+            float g_own = -INFINITY, g_pub = -INFINITY, g_glob = -INFINITY;
+            unsigned long long gkey = 0;
+            const bool share = kRes && row_ok;
+            unsigned long long* my_key = kRes ? p.keys + rr : p.keys + (size_t)k * p.R + rr;
+            volatile float* gsh = g_share + m;  // the row's four quarter records, written by other warps
+            // residual: the 16 base logits (bf16 pairs) of the request's rejected row at v
+            auto load_u = [&](int v, uint32_t(&dst)[8]) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const uint4 q = (row_ok && v + 8 * j < p.V) ? __ldg(reinterpret_cast<const uint4*>(urow + v) + j)
+                                                                 : make_uint4(0u, 0u, 0u, 0u);
+                    dst[4 * j + 0] = q.x; dst[4 * j + 1] = q.y; dst[4 * j + 2] = q.z; dst[4 * j + 3] = q.w;
+                }
+            };
+            for (int i = 0; i < n_local; ++i) {
+                const int t = cidx + i * p.P;
+                const int g = k * n_local + i;  // global tile of the launch: TMEM buffer, U pass phases
+                const int a = g & 1;
+                const uint32_t use = (uint32_t)(g >> 1);
+                if (kRes && row_ok) {
+                    // residual rows differ per request: pull this thread's pieces of the
+                    // next tile (of this one too, at the start) into L2
+                    for (int tt = (i == 0 ? t : t + p.P); tt <= t + p.P && tt < p.n_tiles; tt += p.P) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int v = tt * kNV + 64 * h + kPassCols * quarter;
+                            if (v < p.V) {
+                                prefetch_l2(trow + v);
+                                if (with_u) prefetch_l2(urow + v);
+                            }
+                        }
+                    }
+                }
+                if (share) {
+                    if (i > 0) g_glob = key_log2_ratio(gkey);
+                    gkey = *reinterpret_cast<volatile unsigned long long*>(my_key);
+                }
+                // warp-uniform wait: every lane waits (acquire), all leave together
+                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.tfull[a], use & 1u, abort_flag, kWaitNs))) break;
+                tc::tc_fence_after();
+                const uint32_t taddr =
+                    tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(a * kNV + quarter * kPassCols);
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    const int v0 = t * kNV + 64 * h + kPassCols * quarter;
+                    const int nvalid = min(16, p.V - v0);  // the same in the whole warp
+                    float sv[16];
+                    uint32_t uw[8];
+                    float tv[16];
+                    if constexpr (kRes) {
+                        // residual: target logits (past the row end -inf: p = 0) and, for a
+                        // rejected row, the drafter's base logits; requested before the
+                        // accumulator is read
+                        if (row_ok && nvalid > 0) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float4 f = 4 * j < nvalid ? __ldg(reinterpret_cast<const float4*>(trow + v0) + j)
+                                                                : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                                tv[4 * j + 0] = f.x; tv[4 * j + 1] = f.y; tv[4 * j + 2] = f.z; tv[4 * j + 3] = f.w;
+                            }
+                            if (with_u) load_u(v0, uw);
+                        }
+                    }
+                    __syncwarp();  // lanes that skipped the previous pass rejoin before the aligned load
+                    tc::tmem_ld_32x32b_x16<0>(taddr + 64u * h, sv);
+                    if (!kRes) {
+                        // this pass's base logits, then the buffer goes back to the U producer
+                        // pass buffer h is filled once per tile: its phase parity is g & 1
+                        if (!__all_sync(0xFFFFFFFFu,
+                                        tc::mbar_wait(&bar.ufull[h], (uint32_t)(g & 1), abort_flag, kWaitNs))) {
+                            tc::tmem_ld_wait();
+                            break;
+                        }
+                        const uint4 q0 = *reinterpret_cast<const uint4*>(sU + h * kUBufBytes + u_off0);
+                        const uint4 q1 = *reinterpret_cast<const uint4*>(sU + h * kUBufBytes + u_off1);
+                        uw[0] = q0.x; uw[1] = q0.y; uw[2] = q0.z; uw[3] = q0.w;
+                        uw[4] = q1.x; uw[5] = q1.y; uw[6] = q1.z; uw[7] = q1.w;
+                    }
+                    tc::tmem_ld_wait();
+                    if (h == 1) {  // both halves are in registers: hand the accumulator back
+                        tc::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&bar.tempty[a]);
+                    }
+                    if (!kRes) {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const uint32_t word = uw[c >> 1];
+                            const float u = __uint_as_float((c & 1) ? (word & 0xFFFF0000u) : (word << 16));
+                            sv[c] = (u + sv[c]) * c2;
+                        }
+                        // the values are in registers: the async proxy may overwrite the buffer
+                        tc::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&bar.uempty[h]);
+                    }
                     if (row_ok && nvalid > 0) {
+                        if constexpr (!kRes) {
+                            if (qrow) {  // natural units
+                                const float back = sampling ? kLn2F : 1.0f;
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const float4 f = 4 * j < nvalid ? __ldg(reinterpret_cast<const float4*>(trow + v0) + j)
-                                                            : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-                            tv[4 * j + 0] = f.x; tv[4 * j + 1] = f.y; tv[4 * j + 2] = f.z; tv[4 * j + 3] = f.w;
-                        }
-                        if (with_u) load_u(v0, uw);
-                    }
-                }
-                __syncwarp();  // lanes that skipped the previous pass rejoin before the aligned load
-                tc::tmem_ld_32x32b_x16<0>(taddr + 64u * h, sv);
-                if (!kRes) {
-                    // this pass's base logits, then the buffer goes back to the U producer
-                    // pass buffer h is filled once per tile: its phase parity is i & 1
-                    if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.ufull[h], (uint32_t)(i & 1), abort_flag, kWaitNs))) {
-                        tc::tmem_ld_wait();
-                        break;
-                    }
-                    const uint4 q0 = *reinterpret_cast<const uint4*>(sU + h * kUBufBytes + u_off0);
-                    const uint4 q1 = *reinterpret_cast<const uint4*>(sU + h * kUBufBytes + u_off1);
-                    uw[0] = q0.x; uw[1] = q0.y; uw[2] = q0.z; uw[3] = q0.w;
-                    uw[4] = q1.x; uw[5] = q1.y; uw[6] = q1.z; uw[7] = q1.w;
-                }
-                tc::tmem_ld_wait();
-                if (h == 1) {  // both halves are in registers: hand the accumulator back
-                    tc::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&bar.tempty[a]);
-                }
-                if (!kRes) {
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const uint32_t word = uw[c >> 1];
-                        const float u = __uint_as_float((c & 1) ? (word & 0xFFFF0000u) : (word << 16));
-                        sv[c] = (u + sv[c]) * c2;
-                    }
-                    // the values are in registers: the async proxy may overwrite the buffer
-                    tc::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&bar.uempty[h]);
-                }
-                if (row_ok && nvalid > 0) {
-                    if constexpr (!kRes) {
-                        if (qrow) {  // natural units
-                            const float back = sampling ? kLn2F : 1.0f;
-#pragma unroll
-                            for (int c = 0; c < 16; c += 4)
-                                if (c < nvalid)
-                                    *reinterpret_cast<float4*>(qrow + v0 + c) = make_float4(
-                                        sv[c] * back, sv[c + 1] * back, sv[c + 2] * back, sv[c + 3] * back);
-                        }
-                        if (p.greedy) {
-#pragma unroll
-                            for (int c = 0; c < 16; ++c)
-                                if (c < nvalid && better(sv[c], v0 + c, part.score, part.idx)) {
-                                    part.score = sv[c]; part.idx = v0 + c; part.s_at = sv[c];
-                                }
-                        } else {
-                            // columns past the row end weigh 2^-inf = 0 and never pass the race test
-                            if (nvalid < 16) {
+                                for (int c = 0; c < 16; c += 4)
+                                    if (c < nvalid)
+                                        *reinterpret_cast<float4*>(qrow + v0 + c) = make_float4(
+                                            sv[c] * back, sv[c + 1] * back, sv[c + 2] * back, sv[c + 3] * back);
+                            }
+                            if (p.greedy) {
 #pragma unroll
                                 for (int c = 0; c < 16; ++c)
-                                    if (c >= nvalid) sv[c] = -INFINITY;
-                            }
-                            // sampling draft in base 2: w = 2^(s2 - m2) relative to the running max
-                            float cm = sv[0];
+                                    if (c < nvalid && better(sv[c], v0 + c, part.score, part.idx)) {
+                                        part.score = sv[c]; part.idx = v0 + c; part.s_at = sv[c];
+                                    }
+                            } else {
+                                // columns past the row end weigh 2^-inf = 0 and never pass the race test
+                                if (nvalid < 16) {
 #pragma unroll
-                            for (int c = 1; c < 16; ++c) cm = fmaxf(cm, sv[c]);
-                            if (cm > part.m) {
-                                const float sc = ex2(part.m - cm);  // 0 while the max is -inf
-                                part.sum *= sc;
-                                bw *= sc;
-                                part.m = cm;
+                                    for (int c = 0; c < 16; ++c)
+                                        if (c >= nvalid) sv[c] = -INFINITY;
+                                }
+                                // sampling draft in base 2: w = 2^(s2 - m2) relative to the running max
+                                float cm = sv[0];
+#pragma unroll
+                                for (int c = 1; c < 16; ++c) cm = fmaxf(cm, sv[c]);
+                                if (cm > part.m) {
+                                    const float sc = ex2(part.m - cm);  // 0 while the max is -inf
+                                    part.sum *= sc;
+                                    bw *= sc;
+                                    part.m = cm;
+                                }
+                                rho = race_bound(bE, bw);
+                                uint4 x[4];
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    x[q] = make_uint4((uint32_t)((v0 >> 2) + q), (uint32_t)pos, (uint32_t)rr, w3);
+                                philox4x32_10_x4(x, key0, key1);
+                                // every weight into the normaliser; entries that may beat the
+                                // running winner marked for the exact test
+                                float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                                uint32_t cand = 0;
+#pragma unroll
+                                for (int c = 0; c < 16; ++c) {
+                                    const uint32_t wd = word_of(x[c >> 2], c & 3);
+                                    const float w = ex2(sv[c] - part.m);
+                                    acc[c & 3] += w;
+                                    cand |= (one_plus_complement(wd) < fmaf(w, rho, 1.0f)) ? (1u << c) : 0u;
+                                }
+                                part.sum += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                                if (cand) {
+#pragma unroll
+                                    for (int c = 0; c < 16; ++c) {
+                                        if (cand & (1u << c)) {
+                                            const float w = ex2(sv[c] - part.m);
+                                            const float E = neg_log_uniform(word_of(x[c >> 2], c & 3));
+                                            if (w * bE > bw * E) {
+                                                bw = w; bE = E; part.idx = v0 + c; part.s_at = sv[c];
+                                                rho = race_bound(bE, bw);
+                                            }
+                                        }
+                                    }
+                                }
                             }
-                            rho = race_bound(bE, bw);
+                        } else {
+                            // one race per request: over max(0, p - q) for a rejected row,
+                            // over p for a bonus draw (q = 0 there)
+                            if (with_u) {
+#pragma unroll
+                                for (int c = 0; c < 16; ++c) {
+                                    const uint32_t word = uw[c >> 1];
+                                    const float u = __uint_as_float((c & 1) ? (word & 0xFFFF0000u) : (word << 16));
+                                    sv[c] = (u + sv[c]) * c2;
+                                }
+                            }
                             uint4 x[4];
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
                                 x[q] = make_uint4((uint32_t)((v0 >> 2) + q), (uint32_t)pos, (uint32_t)rr, w3);
                             philox4x32_10_x4(x, key0, key1);
-                            // every weight into the normaliser; entries that may beat the
-                            // running winner marked for the exact test
-                            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                            {
+                                const float gq = fmaxf(fmaxf(g_own, g_glob),
+                                                       fmaxf(fmaxf(gsh[0], gsh[kM]), fmaxf(gsh[2 * kM], gsh[3 * kM])));
+                                rho = fminf(race_bound(bE, bw), ex2(-gq) * kRaceSlack);
+                            }
                             uint32_t cand = 0;
 #pragma unroll
                             for (int c = 0; c < 16; ++c) {
-                                const uint32_t wd = word_of(x[c >> 2], c & 3);
-                                const float w = ex2(sv[c] - part.m);
-                                acc[c & 3] += w;
-                                cand |= (one_plus_complement(wd) < fmaf(w, rho, 1.0f)) ? (1u << c) : 0u;
+                                const float pv = ex2(fmaf(tv[c], c2, -rinfo.lse2_p));
+                                const float wgt = with_u ? pv - ex2(sv[c] - rinfo.q_lse2) : pv;
+                                tv[c] = wgt;
+                                cand |= (wgt > 0.0f && one_plus_complement(word_of(x[c >> 2], c & 3)) <
+                                                           fmaf(wgt, rho, 1.0f))
+                                            ? (1u << c)
+                                            : 0u;
                             }
-                            part.sum += (acc[0] + acc[1]) + (acc[2] + acc[3]);
                             if (cand) {
+                                bool rec = false;
 #pragma unroll
                                 for (int c = 0; c < 16; ++c) {
                                     if (cand & (1u << c)) {
-                                        const float w = ex2(sv[c] - part.m);
                                         const float E = neg_log_uniform(word_of(x[c >> 2], c & 3));
-                                        if (w * bE > bw * E) {
-                                            bw = w; bE = E; part.idx = v0 + c; part.s_at = sv[c];
-                                            rho = race_bound(bE, bw);
+                                        if (tv[c] * bE > bw * E) {
+                                            bw = tv[c]; bE = E; part.idx = v0 + c;
+                                            rho = fminf(rho, race_bound(bE, bw));
+                                            rec = true;
                                         }
                                     }
                                 }
-                            }
-                        }
-                    } else {
-                        // one race per request: over max(0, p - q) for a rejected row,
-                        // over p for a bonus draw (q = 0 there)
-                        if (with_u) {
-#pragma unroll
-                            for (int c = 0; c < 16; ++c) {
-                                const uint32_t word = uw[c >> 1];
-                                const float u = __uint_as_float((c & 1) ? (word & 0xFFFF0000u) : (word << 16));
-                                sv[c] = (u + sv[c]) * c2;
-                            }
-                        }
-                        uint4 x[4];
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            x[q] = make_uint4((uint32_t)((v0 >> 2) + q), (uint32_t)pos, (uint32_t)rr, w3);
-                        philox4x32_10_x4(x, key0, key1);
-                        {
-                            const float g = fmaxf(fmaxf(g_own, g_glob),
-                                                  fmaxf(fmaxf(gsh[0], gsh[kM]), fmaxf(gsh[2 * kM], gsh[3 * kM])));
-                            rho = fminf(race_bound(bE, bw), ex2(-g) * kRaceSlack);
-                        }
-                        uint32_t cand = 0;
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            const float pv = ex2(fmaf(tv[c], c2, -rinfo.lse2_p));
-                            const float wgt = with_u ? pv - ex2(sv[c] - rinfo.q_lse2) : pv;
-                            tv[c] = wgt;
-                            cand |= (wgt > 0.0f && one_plus_complement(word_of(x[c >> 2], c & 3)) <
-                                                       fmaf(wgt, rho, 1.0f))
-                                        ? (1u << c)
-                                        : 0u;
-                        }
-                        if (cand) {
-                            bool rec = false;
-#pragma unroll
-                            for (int c = 0; c < 16; ++c) {
-                                if (cand & (1u << c)) {
-                                    const float E = neg_log_uniform(word_of(x[c >> 2], c & 3));
-                                    if (tv[c] * bE > bw * E) {
-                                        bw = tv[c]; bE = E; part.idx = v0 + c;
-                                        rho = fminf(rho, race_bound(bE, bw));
-                                        rec = true;
-                                    }
+                                if (rec) {
+                                    g_own = lg2(bw) - lg2(bE);
+                                    gsh[quarter * kM] = g_own;
                                 }
-                            }
-                            if (rec) {
-                                g_own = lg2(bw) - lg2(bE);
-                                gsh[quarter * kM] = g_own;
                             }
                         }
                     }
                 }
+                // this thread's record, if it beats the request's best seen so far, for the
+                // other CTAs racing over it (few threads qualify after the first tiles:
+                // same-address atomics serialise)
+                if (share && g_own > fmaxf(g_pub, g_glob)) {
+                    const float sc = kRes ? logf(bw) - logf(bE) : part.s_at * kLn2F - logf(bE);
+                    atomicMax(my_key, winner_key(sc, part.idx));
+                    g_pub = g_own;
+                }
             }
-            // this thread's record, if it beats the request's best seen so far, for the
-            // other CTAs racing over it (few threads qualify after the first tiles:
-            // same-address atomics serialise)
-            if (share && g_own > fmaxf(g_pub, g_glob)) {
-                const float sc = kRes ? logf(bw) - logf(bE) : part.s_at * kLn2F - logf(bE);
-                atomicMax(my_key, winner_key(sc, part.idx));
-                g_pub = g_own;
+            // scores of the winners in log form, for merging across threads and CTAs
+            if (kRes) {
+                part.score = part.idx != INT_MAX ? logf(bw) - logf(bE) : -INFINITY;
+            } else if (!p.greedy) {
+                // back to natural units: the max and the winner's logit
+                part.m *= kLn2F;
+                part.s_at *= kLn2F;
+                if (part.idx != INT_MAX) part.score = part.s_at - logf(bE);
             }
-        }
-        // scores of the winners in log form, for merging across threads and CTAs
-        if (kRes) {
-            part.score = part.idx != INT_MAX ? logf(bw) - logf(bE) : -INFINITY;
-        } else if (!p.greedy) {
-            // back to natural units: the max and the winner's logit
-            part.m *= kLn2F;
-            part.s_at *= kLn2F;
-            if (part.idx != INT_MAX) part.score = part.s_at - logf(bE);
+
+            // ---- the CTA's result of the step: the row's four quarters merged by
+            // quarter 0, which publishes the winner key and (draft) the normaliser piece
+            if (quarter != 0) scratch[(quarter - 1) * kM + m] = part;
+            epi_sync();
+            if (quarter == 0 && row_ok && !*abort_flag) {
+#pragma unroll
+                for (int q = 0; q < 3; ++q) merge_any<kRes>(part, scratch[q * kM + m]);
+                if (kRes) {
+                    if (part.idx != INT_MAX) atomicMax(p.keys + rr, winner_key(part.score, part.idx));
+                } else {
+                    const size_t slot = (size_t)k * p.R + rr;
+                    if (!p.greedy)
+                        p.parts[slot * p.P + cidx] = make_float4(part.m, part.sum, part.s_at, __int_as_float(part.idx));
+                    if (part.idx != INT_MAX) atomicMax(p.keys + slot, winner_key(part.score, part.idx));
+                }
+            }
+            if (k + 1 < n_steps) {
+                // ---- every CTA's keys of step k before any CTA reads them (the scratch
+                // is free again after this too)
+                epi_sync();
+                if (e == 0) {
+                    bool ok = !*abort_flag;
+                    if (ok) ok = step_barrier(p.step_done + k, reinterpret_cast<int*>(p.step_done + p.gamma), gridDim.x);
+                    else atomicExch(reinterpret_cast<int*>(p.step_done + p.gamma), 1);
+                    if (!ok) *abort_flag = 1;  // the control warps stop too
+                    bar.step_ok = ok ? 1 : 0;
+                }
+                epi_sync();
+                if (!bar.step_ok) break;
+            }
         }
     }
 
-    // ---------------------------------------------------------------- per-CTA result
-    __syncthreads();
-    TcPartial* scratch = reinterpret_cast<TcPartial*>(sB);  // W2 stages are drained
-    if (warp >= kCtlWarps + 4) {
-        const int m = (warp & 3) * 32 + lane;
-        const int qtr = (warp - kCtlWarps) >> 2;  // 1..3
-        scratch[(qtr - 1) * kM + m] = part;
-    }
     __syncthreads();
     if (warp == 1) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem_base, kTmemCols);
     }
-    if (*abort_flag) {
-        if (threadIdx.x == 0) report(p.dev_status, DSPARK_ERR_TIMEOUT);
-        return;
-    }
-    if (warp >= kCtlWarps && warp < kCtlWarps + 4 && row_ok) {
-        const int m = (warp & 3) * 32 + lane;
-        const int rr = row0 + m;
-#pragma unroll
-        for (int q = 0; q < 3; ++q) merge_any<kRes>(part, scratch[q * kM + m]);
-        if (kRes) {
-            if (part.idx != INT_MAX) atomicMax(p.keys + rr, winner_key(part.score, part.idx));
-        } else {
-            const size_t slot = (size_t)p.k * p.R + rr;
-            if (!p.greedy)
-                p.parts[slot * p.P + cidx] = make_float4(part.m, part.sum, part.s_at, __int_as_float(part.idx));
-            if (part.idx != INT_MAX) atomicMax(p.keys + slot, winner_key(part.score, part.idx));
-        }
-    }
+    if (*abort_flag && threadIdx.x == 0) report(p.dev_status, DSPARK_ERR_TIMEOUT);
 }
 
 struct DraftFinalize {
@@ -903,18 +954,20 @@ EncodeTiled encoder() {
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Workspace: winner keys, the A matrix H, then (draft) the A rows' tokens and
-// the per-CTA normaliser pieces or (residual) the per-request rows.
+// Workspace: winner keys, (draft) the step counters and the abort word of the
+// launch's grid barrier, zeroed with the keys, then (draft) the per-CTA
+// normaliser pieces or (residual) the per-request rows.
 struct TcLayout {
-    size_t keys, n_keys, h, toks, parts, rows, total;
+    size_t keys, n_keys, step_done, zero_bytes, parts, rows, total;
 };
-TcLayout tc_layout(int R, int gamma, int rank, bool residual) {
+TcLayout tc_layout(int R, int gamma, bool residual) {
     TcLayout L;
     size_t off = 0;
     L.n_keys = residual ? (size_t)R : (size_t)gamma * R;
-    L.keys = off; off += up256(sizeof(unsigned long long) * L.n_keys);
-    L.h = off; off += up256((size_t)R * rank * 2);
-    L.toks = off; off += residual ? 0 : up256(sizeof(int32_t) * (size_t)R);
+    L.keys = off; off += sizeof(unsigned long long) * L.n_keys;
+    L.step_done = off; off += residual ? 0 : sizeof(unsigned) * ((size_t)gamma + 1);
+    L.zero_bytes = off;
+    off = up256(off);
     L.parts = off; off += residual ? 0 : up256(sizeof(float4) * (size_t)gamma * R * kMaxP);
     L.rows = off; off += residual ? up256(sizeof(ResRow) * (size_t)R) : 0;
     L.total = off;
@@ -933,24 +986,23 @@ bool encode_2d_bf16(EncodeTiled enc, CUtensorMap* m, const void* base, int inner
 
 // Shared launch setup of both modes: device limits, stage count, tensor maps,
 // the common parameter block.  Returns DSPARK_OK or an error status.
-int prepare(EncodeTiled enc, const void* U, const void* W1, const void* W2, const void* H, int R, int gamma, int V,
-            int rank, bool residual, TcParams& p, CUtensorMap& tm_w2, CUtensorMap& tm_u, CUtensorMap& tm_h,
-            int& grid, size_t& smem, int& n_sm) {
+int prepare(EncodeTiled enc, const void* U, const void* W1, const void* W2, int R, int gamma, int V, int rank,
+            bool residual, TcParams& p, CUtensorMap& tm_w2, CUtensorMap& tm_u, int& grid, size_t& smem, int& n_sm) {
     int dev = 0, max_smem = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return DSPARK_ERR_CUDA;
     const int nkb = rank / kKB;
-    const size_t fixed = 1024 + (size_t)nkb * kTileBytes + (residual ? 0 : 2 * (size_t)kUBufBytes) + sizeof(Bars);
+    const size_t fixed = 1024 + (size_t)nkb * kTileBytes + (residual ? kShareBytes : 2 * (size_t)kUBufBytes) +
+                         sizeof(Bars);
+    // the end-of-step exchange of the epilogue quarters reuses the A rows' space
+    if ((size_t)nkb * kTileBytes < 3 * kM * sizeof(TcPartial)) return DSPARK_ERR_UNSUPPORTED;
     if ((size_t)max_smem < fixed + 2 * kTileBytes) return DSPARK_ERR_UNSUPPORTED;
     const int n_stages = (int)std::min<size_t>(kMaxStages, ((size_t)max_smem - fixed) / kTileBytes);
     smem = fixed + (size_t)n_stages * kTileBytes;
-    // the end-of-launch exchange of the epilogue quarters reuses the drained stages
-    if ((size_t)n_stages * kTileBytes < (size_t)3 * kM * sizeof(TcPartial)) return DSPARK_ERR_UNSUPPORTED;
 
     if (!encode_2d_bf16(enc, &tm_w2, W2, rank, V, kNV)) return DSPARK_ERR_CUDA;
-    if (!encode_2d_bf16(enc, &tm_h, H, rank, R, kM)) return DSPARK_ERR_CUDA;
     {
         const cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)gamma, (cuuint64_t)R};
         const cuuint64_t strides[2] = {(cuuint64_t)V * 2, (cuuint64_t)gamma * V * 2};
@@ -984,27 +1036,24 @@ bool draft_tc_supported(int u_dtype, int w_dtype, int R, int V, int rank) {
            rank <= 512 && V % 8 == 0 && V >= 8;
 }
 
-size_t draft_tc_workspace(int R, int gamma, int rank) { return tc_layout(R, gamma, rank, false).total; }
+size_t draft_tc_workspace(int R, int gamma, int /*rank*/) { return tc_layout(R, gamma, false).total; }
 
-size_t residual_tc_workspace(int R, int rank) { return tc_layout(R, 0, rank, true).total; }
+size_t residual_tc_workspace(int R, int /*rank*/) { return tc_layout(R, 0, true).total; }
 
 int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream) {
     EncodeTiled enc = encoder();
     if (!enc) return DSPARK_ERR_CUDA;
     if (a.q_logits && (reinterpret_cast<uintptr_t>(a.q_logits) & 15)) return DSPARK_ERR_UNSUPPORTED;
-    const TcLayout L = tc_layout(a.R, a.gamma, a.rank, false);
+    const TcLayout L = tc_layout(a.R, a.gamma, false);
     unsigned char* w = static_cast<unsigned char*>(a.ws);
-    uint16_t* H = reinterpret_cast<uint16_t*>(w + L.h);
-    int32_t* toks = reinterpret_cast<int32_t*>(w + L.toks);
     TcParams p;
-    CUtensorMap tm_w2, tm_u, tm_h;
+    CUtensorMap tm_w2, tm_u;
     int grid = 0, n_sm = 0;
     size_t smem = 0;
-    const int st =
-        prepare(enc, a.U, a.W1, a.W2, H, a.R, a.gamma, a.V, a.rank, false, p, tm_w2, tm_u, tm_h, grid, smem, n_sm);
+    const int st = prepare(enc, a.U, a.W1, a.W2, a.R, a.gamma, a.V, a.rank, false, p, tm_w2, tm_u, grid, smem, n_sm);
     if (st != DSPARK_OK) return st;
     p.keys = reinterpret_cast<unsigned long long*>(w + L.keys);
-    p.toks = toks;
+    p.step_done = reinterpret_cast<unsigned*>(w + L.step_done);
     p.parts = reinterpret_cast<float4*>(w + L.parts);
     p.anchor = a.anchor;
     p.seeds = a.seeds;
@@ -1016,37 +1065,27 @@ int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream) {
     if (cudaFuncSetAttribute(markov_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return DSPARK_ERR_CUDA;
-    if (cudaMemsetAsync(p.keys, 0, sizeof(unsigned long long) * L.n_keys, stream) != cudaSuccess)
-        return DSPARK_ERR_CUDA;
-    // gather 0 waits for everything before it on the stream.  Every later launch
-    // is a programmatic dependent of the one before: it may start as that one
-    // retires and waits (griddepcontrol) before reading its results; the only
-    // data read earlier are W2 and U.
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    // keys, step counters and abort word in one piece
+    if (cudaMemsetAsync(w, 0, L.zero_bytes, stream) != cudaSuccess) return DSPARK_ERR_CUDA;
+    // All gamma steps in one launch whose CTAs wait for one another between
+    // steps: a cooperative launch, so that every CTA is resident (one per SM,
+    // grid <= SM count) or the launch fails.
+    cudaLaunchAttribute coop[1];
+    coop[0].id = cudaLaunchAttributeCooperative;
+    coop[0].val.cooperative = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cfg.attrs = attr;
+    cfg.attrs = coop;
     cfg.numAttrs = 1;
-    cudaLaunchConfig_t gcfg = {};
-    gcfg.gridDim = dim3((unsigned)a.R);
-    gcfg.blockDim = dim3(kGatherThreads);
-    gcfg.stream = stream;
-    gcfg.attrs = attr;
-    for (int k = 0; k < a.gamma; ++k) {
-        gcfg.numAttrs = k == 0 ? 0 : 1;
-        const unsigned long long* prev_keys = k == 0 ? nullptr : p.keys + (size_t)(k - 1) * a.R;
-        if (cudaLaunchKernelEx(&gcfg, gather_a_rows_kernel, p.W1, a.anchor, prev_keys, k, a.R, a.V, a.rank, H,
-                               toks) != cudaSuccess)
-            return DSPARK_ERR_CUDA;
-        p.k = k;
-        if (cudaLaunchKernelEx(&cfg, markov_tc_kernel<false>, tm_w2, tm_u, tm_h, p) != cudaSuccess)
-            return DSPARK_ERR_CUDA;
-    }
+    if (cudaLaunchKernelEx(&cfg, markov_tc_kernel<false>, tm_w2, tm_u, p) != cudaSuccess) return DSPARK_ERR_CUDA;
+    // the finalize is a programmatic dependent: it may start as the steps
+    // retire and waits (griddepcontrol) before reading their results
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     DraftFinalize f;
     f.keys = p.keys;
     f.parts = p.parts;
@@ -1072,15 +1111,13 @@ int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream) {
 int launch_residual_tc(const ResidualTcArgs& a, cudaStream_t stream) {
     EncodeTiled enc = encoder();
     if (!enc) return DSPARK_ERR_CUDA;
-    const TcLayout L = tc_layout(a.R, a.gamma, a.rank, true);
+    const TcLayout L = tc_layout(a.R, a.gamma, true);
     unsigned char* w = static_cast<unsigned char*>(a.ws);
-    uint16_t* H = reinterpret_cast<uint16_t*>(w + L.h);
     TcParams p;
-    CUtensorMap tm_w2, tm_u, tm_h;
+    CUtensorMap tm_w2, tm_u;
     int grid = 0, n_sm = 0;
     size_t smem = 0;
-    const int st =
-        prepare(enc, a.U, a.W1, a.W2, H, a.R, a.gamma, a.V, a.rank, true, p, tm_w2, tm_u, tm_h, grid, smem, n_sm);
+    const int st = prepare(enc, a.U, a.W1, a.W2, a.R, a.gamma, a.V, a.rank, true, p, tm_w2, tm_u, grid, smem, n_sm);
     if (st != DSPARK_OK) return st;
     ResRow* rows = reinterpret_cast<ResRow*>(w + L.rows);
     p.keys = reinterpret_cast<unsigned long long*>(w + L.keys);
@@ -1092,14 +1129,13 @@ int launch_residual_tc(const ResidualTcArgs& a, cudaStream_t stream) {
     p.greedy = 0;
     p.target = a.target;
     p.rows = rows;
-    p.k = 0;
     if (cudaFuncSetAttribute(markov_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return DSPARK_ERR_CUDA;
     if (cudaMemsetAsync(p.keys, 0, sizeof(unsigned long long) * L.n_keys, stream) != cudaSuccess)
         return DSPARK_ERR_CUDA;
-    residual_prep_kernel<<<(unsigned)((a.R * 32LL + 255) / 256), 256, 0, stream>>>(a, rows, H);
-    markov_tc_kernel<true><<<grid, kThreads, smem, stream>>>(tm_w2, tm_u, tm_h, p);
+    residual_prep_kernel<<<(unsigned)((a.R + 255) / 256), 256, 0, stream>>>(a, rows);
+    markov_tc_kernel<true><<<grid, kThreads, smem, stream>>>(tm_w2, tm_u, p);
     residual_finalize_kernel<<<a.R, 256, 0, stream>>>(rows, p.keys, a.target, a.seeds, a.invT, a.gamma, a.V,
                                                       a.out_tokens, a.dev_status);
     return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
