@@ -211,7 +211,9 @@ int dspark_verify(const float* target_logits, const int32_t* cu_seqlens,
  *   ws, ws_bytes  dspark_workspace_size(DSPARK_OP_VERIFY_MARKOV, R, gamma, V, rank,
  *                 max_rows, DSPARK_BF16, 0)
  * Returns DSPARK_ERR_UNSUPPORTED for factor types or shapes the tensor-core
- * kernel does not take (use dspark_verify with q_logits there).
+ * kernel does not take (use dspark_verify with q_logits there), and at
+ * temperature > 0 when target_logits, U, W1 or W2 is not 16-byte aligned (the
+ * residual kernel reads the rows in 16-byte pieces).
  */
 int dspark_verify_markov(const float* target_logits, const int32_t* cu_seqlens,
                          const int32_t* draft_tokens, const void* U, const void* W1,

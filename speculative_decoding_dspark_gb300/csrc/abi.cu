@@ -217,7 +217,8 @@ int dspark_verify_markov(const float* target_logits, const int32_t* cu_seqlens,
     const bool greedy = temperature == 0.0f;
     if (!greedy && (!U || !W1 || !W2 || !anchor || !q_lse || !q_tok || !seeds)) return DSPARK_ERR_INVALID_ARG;
     if (!draft_tc_supported(DSPARK_BF16, DSPARK_BF16, R, V, rank)) return DSPARK_ERR_UNSUPPORTED;
-    if (!greedy && (!aligned16(U) || !aligned16(W1) || !aligned16(W2))) return DSPARK_ERR_UNSUPPORTED;
+    if (!greedy && (!aligned16(U) || !aligned16(W1) || !aligned16(W2) || !aligned16(target_logits)))
+        return DSPARK_ERR_UNSUPPORTED;
     if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return DSPARK_ERR_WORKSPACE;
     const VerifyLayout L = verify_layout(R, V, max_rows);
     const size_t res_off = align_up(L.total);

@@ -56,14 +56,15 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKey& K) {
     return c;
 }
 
-// Four counters under one key, round by round: the four chains are
-// independent (their multiplies overlap) and share the key schedule, which is
-// advanced in place instead of being kept as twenty round keys.
-__device__ __forceinline__ void philox4x32_10_x4(uint4 (&c)[4], uint32_t k0, uint32_t k1) {
+// N counters under one key, round by round: the N chains are independent
+// (their multiplies overlap) and share the key schedule, which is advanced in
+// place instead of being kept as twenty round keys.
+template <int N>
+__device__ __forceinline__ void philox4x32_10_xn(uint4 (&c)[N], uint32_t k0, uint32_t k1) {
 #pragma unroll
     for (int i = 0; i < 10; ++i) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < N; ++j) {
             const uint64_t p0 = (uint64_t)0xD2511F53u * c[j].x;
             const uint64_t p1 = (uint64_t)0xCD9E8D57u * c[j].z;
             c[j] = make_uint4((uint32_t)(p1 >> 32) ^ c[j].y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c[j].w ^ k1,
@@ -72,6 +73,10 @@ __device__ __forceinline__ void philox4x32_10_x4(uint4 (&c)[4], uint32_t k0, uin
         k0 += 0x9E3779B9u;
         k1 += 0xBB67AE85u;
     }
+}
+
+__device__ __forceinline__ void philox4x32_10_x4(uint4 (&c)[4], uint32_t k0, uint32_t k1) {
+    philox4x32_10_xn<4>(c, k0, k1);
 }
 
 enum Purpose : uint32_t { kDraftGumbel = 0, kAccept = 1, kResidualGumbel = 2, kBonusGumbel = 3 };

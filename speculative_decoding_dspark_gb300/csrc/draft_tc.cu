@@ -81,9 +81,19 @@ constexpr int kCtlWarps = 3;                  // W2 producer, MMA issuer, U prod
 constexpr int kThreads = kCtlWarps * 32 + kEpiThreads;
 constexpr int kPassCols = 16;                 // of which one pass handles
 constexpr int kUBufBytes = kM * 64 * 2;       // base logits of one pass: 128 requests x 64 columns
+// residual staging of one 32-column pass for the 128 requests: target logits
+// (fp32, 128-byte rows) and base logits (bf16, 64-byte rows), copied in
+// 16-byte pieces by the epilogue threads a few passes ahead
+constexpr int kResCols = 32;
+constexpr int kResTBytes = kM * kResCols * 4;  // 16 KB
+constexpr int kResUBytes = kM * kResCols * 2;  // 8 KB
+constexpr int kResBufs = 6;                    // staging buffers
+constexpr int kResAhead = kResBufs - 2;        // passes whose copies are issued ahead of the one computed
 constexpr int kMaxStages = 8;
 constexpr int kMaxP = 256;                    // CTAs per request block (pieces per request)
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 256;     // draft: two 128-column accumulators
+constexpr uint32_t kTmemColsRes = 512;  // residual: the accumulators, then the A rows (at most 256 columns)
+constexpr uint32_t kAcol = 256;         // residual: first tensor-memory column of A
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2eF = 1.4426950408889634f;
 constexpr float kLn2F = 0.6931471805599453f;
@@ -137,15 +147,24 @@ struct Bars {
     uint64_t full[kMaxStages], empty[kMaxStages];
     uint64_t tfull[2], tempty[2];
     uint64_t ufull[2], uempty[2];
+    uint64_t sfull[kResBufs], sempty[kResBufs];  // residual staging buffers
     uint64_t afull, mma_done;  // afull: the step's A rows are in shared memory (one arrival per epilogue warp)
     uint32_t tmem_slot;
     int abort_flag;
     int step_ok;               // the grid barrier after a step passed (read by every epilogue warp)
     int a_tok[kM];             // the step's A rows' tokens: -1 zero row, -2 nothing to compute for the request
 };
-// Residual: per request row and epilogue quarter, the best race record so far
-// as log2(w / E) in absolute units (-inf: none), read by the row's other quarters.
-constexpr size_t kShareBytes = 4 * kM * sizeof(float);
+// Residual-only shared memory after the barriers: per request row and epilogue
+// quarter the best race record so far as log2(w / E) in absolute units (-inf:
+// none), read by the row's other quarters; then each request's target row and
+// U row (-1 when not needed), from which every epilogue thread takes the rows
+// of its staging copies.
+struct ResShared {
+    float g_share[4][kM];
+    int trow[kM];
+    int urow[kM];
+};
+constexpr size_t kShareBytes = sizeof(ResShared);
 
 __device__ __forceinline__ void merge_draft(float& sc, int& ix, float& sa, float& m, float& su, float sc2, int ix2,
                                             float sa2, float m2, float su2) {
@@ -250,9 +269,6 @@ __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
 
 // 16 bytes global -> shared without registers; zeros when !valid (nothing read).
 __device__ __forceinline__ void cp_async_16(void* dst, const void* src, bool valid) {
@@ -261,6 +277,10 @@ __device__ __forceinline__ void cp_async_16(void* dst, const void* src, bool val
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// One arrival on bar once every cp.async this thread issued so far has landed.
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+}
 
 // The 16 epilogue warps alone (named barrier 1; barrier 0 is the CTA's).
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); }
@@ -318,14 +338,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_u, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // draft: A rows | two U pass buffers | W2 ring; residual (A in tensor
+    // memory): target staging buffers | base-logit staging buffers | W2 ring
     uint8_t* sA = smem;
-    uint8_t* sU = sA + p.nkb * kTileBytes;          // draft: two pass buffers of base logits
-    uint8_t* sB = sU + (kRes ? 0 : 2 * kUBufBytes);
+    uint8_t* sU = kRes ? smem : sA + p.nkb * kTileBytes;
+    uint8_t* sRT = sU;
+    uint8_t* sRU = sU + kResBufs * kResTBytes;
+    uint8_t* sB = sU + (kRes ? kResBufs * (kResTBytes + kResUBytes) : 2 * kUBufBytes);
     Bars& bar = *reinterpret_cast<Bars*>(sB + p.n_stages * kTileBytes);
-    float* g_share = reinterpret_cast<float*>(&bar + 1);  // residual: [4][kM]
-    // the quarters' exchange at the end of a step ([3][kM]) uses the A rows' space:
-    // the step's MMAs have completed and the next step's rows are not written yet
-    TcPartial* scratch = reinterpret_cast<TcPartial*>(sA);
+    ResShared& rsh = *reinterpret_cast<ResShared*>(&bar + 1);  // residual only
+    float* g_share = &rsh.g_share[0][0];
+    // the quarters' exchange at the end of a step ([3][kM]): draft, the A rows'
+    // space (the step's MMAs have completed and the next step's rows are not
+    // written yet); residual, the W2 ring (drained when the last tile's
+    // accumulator has been seen)
+    TcPartial* scratch = reinterpret_cast<TcPartial*>(kRes ? sB : sA);
     volatile int* abort_flag = &bar.abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -341,13 +368,17 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         for (int s = 0; s < S; ++s) { tc::mbar_init(&bar.full[s], 1); tc::mbar_init(&bar.empty[s], 1); }
         for (int a = 0; a < 2; ++a) { tc::mbar_init(&bar.tfull[a], 1); tc::mbar_init(&bar.tempty[a], kEpiWarps); }
         for (int a = 0; a < 2; ++a) { tc::mbar_init(&bar.ufull[a], 1); tc::mbar_init(&bar.uempty[a], kEpiWarps); }
+        for (int a = 0; a < kResBufs; ++a) {
+            tc::mbar_init(&bar.sfull[a], kEpiThreads);  // one cp.async arrival per epilogue thread
+            tc::mbar_init(&bar.sempty[a], kEpiWarps);
+        }
         tc::mbar_init(&bar.afull, kEpiWarps);
         tc::mbar_init(&bar.mma_done, 1);
         bar.abort_flag = 0;
         tc::fence_barrier_init();
     }
     if (warp == 1) {
-        tc::tmem_alloc(&bar.tmem_slot, kTmemCols);
+        tc::tmem_alloc(&bar.tmem_slot, kRes ? kTmemColsRes : kTmemCols);
         tc::tmem_relinquish();
     }
     if (warp == 0 && lane == 0) {
@@ -433,9 +464,14 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                         const uint32_t aa = a_base + (uint32_t)(kb * kTileBytes);
                         const uint32_t bb = b_base + (uint32_t)(s * kTileBytes);
 #pragma unroll
-                        for (int j = 0; j < kKB / 16; ++j)
-                            tc::umma_bf16(d, tc::smem_desc_sw128(aa + 32u * j), tc::smem_desc_sw128(bb + 32u * j), idesc,
-                                          (kb | j) != 0);
+                        for (int j = 0; j < kKB / 16; ++j) {
+                            if constexpr (kRes)  // A in tensor memory: K elements 64 kb + 16 j .. at column 32 kb + 8 j
+                                tc::umma_bf16_ta(d, tmem_base + kAcol + (uint32_t)(32 * kb + 8 * j),
+                                                 tc::smem_desc_sw128(bb + 32u * j), idesc, (kb | j) != 0);
+                            else
+                                tc::umma_bf16(d, tc::smem_desc_sw128(aa + 32u * j), tc::smem_desc_sw128(bb + 32u * j),
+                                              idesc, (kb | j) != 0);
+                        }
                         tc::umma_commit(&bar.empty[s]);
                         if (++s == S) { s = 0; ph ^= 1u; }
                     }
@@ -488,7 +524,6 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         const uint32_t key0 = (uint32_t)(seed & 0xFFFFFFFFu), key1 = (uint32_t)(seed >> 32);
         const uint32_t w3 = kRes ? rinfo.w3 : ctr_word3(p.cycle, kDraftGumbel);
         const bool with_u = !kRes || rinfo.mode == 1;
-        const float* trow = kRes ? p.target + (size_t)rinfo.trow * p.V : nullptr;
         // logits are scaled to base 2 when sampling: s2 = s * log2(e) / T
         const float c2 = sampling ? p.invT * kLog2eF : 1.0f;
         // draft: this thread's 32 bytes of a pass buffer (row m, 16-byte chunks
@@ -500,9 +535,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         for (int k = 0; k < n_steps; ++k) {
             // ---- the step's A rows: tokens (the anchor at k = 0, else the previous
             // step's winner, decoded from its key; residual: the rejected
-            // position's predecessor), then W1 rows into the 128-byte-swizzled
-            // K-major layout the MMA descriptors describe: 16-byte piece c of row j
-            // at k-block c / 8, row j, piece (c % 8) ^ (j % 8)
+            // position's predecessor), then W1 rows: draft, into the 128-byte-
+            // swizzled K-major layout the MMA descriptors describe (16-byte piece c
+            // of row j at k-block c / 8, row j, piece (c % 8) ^ (j % 8)); residual,
+            // into tensor memory
             if (e < kM) {
                 const int r = row0 + e;
                 int t = -2;
@@ -510,6 +546,8 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                     if constexpr (kRes) {
                         const ResRow& rw = p.rows[r];
                         t = rw.mode == 0 ? -2 : rw.prev;
+                        rsh.trow[e] = rw.mode != 0 ? rw.trow : -1;
+                        rsh.urow[e] = rw.mode == 1 ? r * p.gamma + rw.pos : -1;
                     } else if (k == 0) {
                         const int an = p.anchor[r];
                         t = an >= p.V ? -2 : (an < 0 ? -1 : an);
@@ -520,32 +558,94 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                     }
                 }
                 bar.a_tok[e] = t;
+                if (kRes && r >= p.R) { rsh.trow[e] = -1; rsh.urow[e] = -1; }
             }
             epi_sync();
-            // warp ew copies rows 8 ew .. 8 ew + 7, every piece in flight at once
+            // Residual staging: thread e copies target pieces e and e + 512 (piece c of
+            // row m: c = piece % 8, m = piece / 8) and base-logit piece e (c = e % 4,
+            // m = e / 4) of every pass, so that one warp instruction moves four whole
+            // 128-byte target rows or eight 64-byte U rows; pieces past the row end,
+            // and rows without a draw, are zero-filled without a read.  The copies
+            // of pass n go out kResAhead passes before it is computed.
+            const int n_res = kRes ? 4 * n_local : 0;
+            const int stc = e & 7, stm0 = e >> 3, stm1 = stm0 + 64, suc = e & 3, sum_ = e >> 2;
+            const int st_t0 = kRes ? rsh.trow[stm0] : -1, st_t1 = kRes ? rsh.trow[stm1] : -1;
+            const int st_u = kRes ? rsh.urow[sum_] : -1;
+            const uint32_t st_d0 = (uint32_t)(stm0 * 128 + ((stc ^ (stm0 & 7)) << 4));
+            const uint32_t st_d1 = (uint32_t)(stm1 * 128 + ((stc ^ (stm1 & 7)) << 4));
+            const uint32_t st_du = (uint32_t)(sum_ * 64 + ((suc ^ ((sum_ >> 1) & 3)) << 4));
+            // false when the wait for a free buffer gave up
+            auto stage_issue = [&](int n) -> bool {
+                const int b = n % kResBufs;
+                const uint32_t use = (uint32_t)(n / kResBufs);
+                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.sempty[b], (use & 1u) ^ 1u, abort_flag, kWaitNs)))
+                    return false;
+                const int v = (cidx + (n >> 2) * p.P) * kNV + kResCols * (n & 3);
+                const int ct = v + 4 * stc, cu = v + 8 * suc;
+                const bool i0 = st_t0 >= 0 && ct < p.V, i1 = st_t1 >= 0 && ct < p.V, iu = st_u >= 0 && cu < p.V;
+                cp_async_16(sRT + b * kResTBytes + st_d0, p.target + (i0 ? (size_t)st_t0 * p.V + ct : 0), i0);
+                cp_async_16(sRT + b * kResTBytes + st_d1, p.target + (i1 ? (size_t)st_t1 * p.V + ct : 0), i1);
+                cp_async_16(sRU + b * kResUBytes + st_du, p.U + (iu ? (size_t)st_u * p.V + cu : 0), iu);
+                cp_async_arrive(&bar.sfull[b]);
+                return true;
+            };
+            bool staged = true;
+            if constexpr (kRes)
+                for (int n = 0; staged && n < kResAhead && n < n_res; ++n) staged = stage_issue(n);
+            if constexpr (kRes) {
+                // residual: A in tensor memory from column kAcol (lane = request row,
+                // two bf16 per column); thread (row m, quarter) writes row m's K
+                // elements rank/4 * quarter .. + rank/4 - 1, eight columns per store
+                const int t = bar.a_tok[m];
+                const int kq = p.rank >> 2;  // a multiple of 16
+                const uint4* src =
+                    reinterpret_cast<const uint4*>(p.W1 + (size_t)(t < 0 ? 0 : t) * p.rank + (size_t)quarter * kq);
+                const uint32_t tq =
+                    tmem_base + ((uint32_t)(quad * 32) << 16) + kAcol + (uint32_t)(quarter * (kq >> 1));
+                const int n16 = kq >> 3;  // 16-byte pieces of the quarter row (at most 16)
 #pragma unroll 1
-            for (int q = 0; q < 8; ++q) {
-                const int j = 8 * ew + q;
-                const int t = bar.a_tok[j];
-                const uint4* src = reinterpret_cast<const uint4*>(p.W1 + (size_t)(t < 0 ? 0 : t) * p.rank);
+                for (int c0 = 0; c0 < n16; c0 += 8) {
+                    uint4 v[8];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int c = lane + 32 * h;
-                    if (c < cpr)
-                        cp_async_16(sA + (c >> 3) * kTileBytes + j * 128 + (((c & 7) ^ (j & 7)) << 4), src + c, t >= 0);
+                    for (int c = 0; c < 8; ++c)
+                        v[c] = (t >= 0 && c0 + c < n16) ? __ldg(src + c0 + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                    for (int c = 0; c < 8; c += 2) {
+                        if (c0 + c < n16) {  // warp-uniform
+                            const uint32_t w[8] = {v[c].x, v[c].y, v[c].z, v[c].w,
+                                                   v[c + 1].x, v[c + 1].y, v[c + 1].z, v[c + 1].w};
+                            tc::tmem_st_32x32b_x8(tq + (uint32_t)(4 * (c0 + c)), w);
+                        }
+                    }
                 }
+                tc::tmem_st_wait();
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&bar.afull);
+            } else {
+                // warp ew copies rows 8 ew .. 8 ew + 7, every piece in flight at once
+#pragma unroll 1
+                for (int q = 0; q < 8; ++q) {
+                    const int j = 8 * ew + q;
+                    const int t = bar.a_tok[j];
+                    const uint4* src = reinterpret_cast<const uint4*>(p.W1 + (size_t)(t < 0 ? 0 : t) * p.rank);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int c = lane + 32 * h;
+                        if (c < cpr)
+                            cp_async_16(sA + (c >> 3) * kTileBytes + j * 128 + (((c & 7) ^ (j & 7)) << 4), src + c, t >= 0);
+                    }
+                }
+                cp_async_wait_all();
+                // the rows are read by the tensor cores (async proxy)
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&bar.afull);
             }
-            cp_async_wait_all();
-            // the rows are read by the tensor cores (async proxy)
-            tc::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bar.afull);
-
             row_ok = rr < p.R && bar.a_tok[m] != -2;
             if (kRes) row_ok = row_ok && rinfo.mode != 0;
             const int pos = kRes ? rinfo.pos : k;
             const size_t rk = (size_t)rr * p.gamma + pos;
-            const uint16_t* urow = p.U + rk * p.V;
             float* qrow = (!kRes && p.q_logits && row_ok) ? p.q_logits + rk * p.V : nullptr;
             part = identity_partial<kRes>();
             // exponential-race state (bw, bE) and rho = E_best / w_best with the
@@ -563,38 +663,14 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
             const bool share = kRes && row_ok;
             unsigned long long* my_key = kRes ? p.keys + rr : p.keys + (size_t)k * p.R + rr;
             volatile float* gsh = g_share + m;  // the row's four quarter records, written by other warps
-            // residual: the 16 base logits (bf16 pairs) of the request's rejected row at v
-            auto load_u = [&](int v, uint32_t(&dst)[8]) {
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const uint4 q = (row_ok && v + 8 * j < p.V) ? __ldg(reinterpret_cast<const uint4*>(urow + v) + j)
-                                                                 : make_uint4(0u, 0u, 0u, 0u);
-                    dst[4 * j + 0] = q.x; dst[4 * j + 1] = q.y; dst[4 * j + 2] = q.z; dst[4 * j + 3] = q.w;
-                }
-            };
+            if constexpr (!kRes) {
+            // ---- draft: thread = request row m x 32 columns of a tile, two
+            // 16-column passes (pass h covers columns 64 h + 16 quarter .. + 15)
             for (int i = 0; i < n_local; ++i) {
                 const int t = cidx + i * p.P;
                 const int g = k * n_local + i;  // global tile of the launch: TMEM buffer, U pass phases
                 const int a = g & 1;
                 const uint32_t use = (uint32_t)(g >> 1);
-                if (kRes && row_ok) {
-                    // residual rows differ per request: pull this thread's pieces of the
-                    // next tile (of this one too, at the start) into L2
-                    for (int tt = (i == 0 ? t : t + p.P); tt <= t + p.P && tt < p.n_tiles; tt += p.P) {
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int v = tt * kNV + 64 * h + kPassCols * quarter;
-                            if (v < p.V) {
-                                prefetch_l2(trow + v);
-                                if (with_u) prefetch_l2(urow + v);
-                            }
-                        }
-                    }
-                }
-                if (share) {
-                    if (i > 0) g_glob = key_log2_ratio(gkey);
-                    gkey = *reinterpret_cast<volatile unsigned long long*>(my_key);
-                }
                 // warp-uniform wait: every lane waits (acquire), all leave together
                 if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.tfull[a], use & 1u, abort_flag, kWaitNs))) break;
                 tc::tc_fence_after();
@@ -606,180 +682,232 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                     const int nvalid = min(16, p.V - v0);  // the same in the whole warp
                     float sv[16];
                     uint32_t uw[8];
-                    float tv[16];
-                    if constexpr (kRes) {
-                        // residual: target logits (past the row end -inf: p = 0) and, for a
-                        // rejected row, the drafter's base logits; requested before the
-                        // accumulator is read
-                        if (row_ok && nvalid > 0) {
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const float4 f = 4 * j < nvalid ? __ldg(reinterpret_cast<const float4*>(trow + v0) + j)
-                                                                : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-                                tv[4 * j + 0] = f.x; tv[4 * j + 1] = f.y; tv[4 * j + 2] = f.z; tv[4 * j + 3] = f.w;
-                            }
-                            if (with_u) load_u(v0, uw);
-                        }
-                    }
                     __syncwarp();  // lanes that skipped the previous pass rejoin before the aligned load
                     tc::tmem_ld_32x32b_x16<0>(taddr + 64u * h, sv);
-                    if (!kRes) {
-                        // this pass's base logits, then the buffer goes back to the U producer
-                        // pass buffer h is filled once per tile: its phase parity is g & 1
-                        if (!__all_sync(0xFFFFFFFFu,
-                                        tc::mbar_wait(&bar.ufull[h], (uint32_t)(g & 1), abort_flag, kWaitNs))) {
-                            tc::tmem_ld_wait();
-                            break;
-                        }
-                        const uint4 q0 = *reinterpret_cast<const uint4*>(sU + h * kUBufBytes + u_off0);
-                        const uint4 q1 = *reinterpret_cast<const uint4*>(sU + h * kUBufBytes + u_off1);
-                        uw[0] = q0.x; uw[1] = q0.y; uw[2] = q0.z; uw[3] = q0.w;
-                        uw[4] = q1.x; uw[5] = q1.y; uw[6] = q1.z; uw[7] = q1.w;
+                    // this pass's base logits, then the buffer goes back to the U producer
+                    // pass buffer h is filled once per tile: its phase parity is g & 1
+                    if (!__all_sync(0xFFFFFFFFu,
+                                    tc::mbar_wait(&bar.ufull[h], (uint32_t)(g & 1), abort_flag, kWaitNs))) {
+                        tc::tmem_ld_wait();
+                        break;
                     }
+                    const uint4 q0 = *reinterpret_cast<const uint4*>(sU + h * kUBufBytes + u_off0);
+                    const uint4 q1 = *reinterpret_cast<const uint4*>(sU + h * kUBufBytes + u_off1);
+                    uw[0] = q0.x; uw[1] = q0.y; uw[2] = q0.z; uw[3] = q0.w;
+                    uw[4] = q1.x; uw[5] = q1.y; uw[6] = q1.z; uw[7] = q1.w;
                     tc::tmem_ld_wait();
                     if (h == 1) {  // both halves are in registers: hand the accumulator back
                         tc::tc_fence_before();
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&bar.tempty[a]);
                     }
-                    if (!kRes) {
 #pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            const uint32_t word = uw[c >> 1];
-                            const float u = __uint_as_float((c & 1) ? (word & 0xFFFF0000u) : (word << 16));
-                            sv[c] = (u + sv[c]) * c2;
-                        }
-                        // the values are in registers: the async proxy may overwrite the buffer
-                        tc::fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(&bar.uempty[h]);
+                    for (int c = 0; c < 16; ++c) {
+                        const uint32_t word = uw[c >> 1];
+                        const float u = __uint_as_float((c & 1) ? (word & 0xFFFF0000u) : (word << 16));
+                        sv[c] = (u + sv[c]) * c2;
                     }
+                    // the values are in registers: the async proxy may overwrite the buffer
+                    tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&bar.uempty[h]);
                     if (row_ok && nvalid > 0) {
-                        if constexpr (!kRes) {
-                            if (qrow) {  // natural units
-                                const float back = sampling ? kLn2F : 1.0f;
+                        if (qrow) {  // natural units
+                            const float back = sampling ? kLn2F : 1.0f;
 #pragma unroll
-                                for (int c = 0; c < 16; c += 4)
-                                    if (c < nvalid)
-                                        *reinterpret_cast<float4*>(qrow + v0 + c) = make_float4(
-                                            sv[c] * back, sv[c + 1] * back, sv[c + 2] * back, sv[c + 3] * back);
-                            }
-                            if (p.greedy) {
+                            for (int c = 0; c < 16; c += 4)
+                                if (c < nvalid)
+                                    *reinterpret_cast<float4*>(qrow + v0 + c) = make_float4(
+                                        sv[c] * back, sv[c + 1] * back, sv[c + 2] * back, sv[c + 3] * back);
+                        }
+                        if (p.greedy) {
+#pragma unroll
+                            for (int c = 0; c < 16; ++c)
+                                if (c < nvalid && better(sv[c], v0 + c, part.score, part.idx)) {
+                                    part.score = sv[c]; part.idx = v0 + c; part.s_at = sv[c];
+                                }
+                        } else {
+                            // columns past the row end weigh 2^-inf = 0 and never pass the race test
+                            if (nvalid < 16) {
 #pragma unroll
                                 for (int c = 0; c < 16; ++c)
-                                    if (c < nvalid && better(sv[c], v0 + c, part.score, part.idx)) {
-                                        part.score = sv[c]; part.idx = v0 + c; part.s_at = sv[c];
-                                    }
-                            } else {
-                                // columns past the row end weigh 2^-inf = 0 and never pass the race test
-                                if (nvalid < 16) {
-#pragma unroll
-                                    for (int c = 0; c < 16; ++c)
-                                        if (c >= nvalid) sv[c] = -INFINITY;
-                                }
-                                // sampling draft in base 2: w = 2^(s2 - m2) relative to the running max
-                                float cm = sv[0];
-#pragma unroll
-                                for (int c = 1; c < 16; ++c) cm = fmaxf(cm, sv[c]);
-                                if (cm > part.m) {
-                                    const float sc = ex2(part.m - cm);  // 0 while the max is -inf
-                                    part.sum *= sc;
-                                    bw *= sc;
-                                    part.m = cm;
-                                }
-                                rho = race_bound(bE, bw);
-                                uint4 x[4];
-#pragma unroll
-                                for (int q = 0; q < 4; ++q)
-                                    x[q] = make_uint4((uint32_t)((v0 >> 2) + q), (uint32_t)pos, (uint32_t)rr, w3);
-                                philox4x32_10_x4(x, key0, key1);
-                                // every weight into the normaliser; entries that may beat the
-                                // running winner marked for the exact test
-                                float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                                uint32_t cand = 0;
-#pragma unroll
-                                for (int c = 0; c < 16; ++c) {
-                                    const uint32_t wd = word_of(x[c >> 2], c & 3);
-                                    const float w = ex2(sv[c] - part.m);
-                                    acc[c & 3] += w;
-                                    cand |= (one_plus_complement(wd) < fmaf(w, rho, 1.0f)) ? (1u << c) : 0u;
-                                }
-                                part.sum += (acc[0] + acc[1]) + (acc[2] + acc[3]);
-                                if (cand) {
-#pragma unroll
-                                    for (int c = 0; c < 16; ++c) {
-                                        if (cand & (1u << c)) {
-                                            const float w = ex2(sv[c] - part.m);
-                                            const float E = neg_log_uniform(word_of(x[c >> 2], c & 3));
-                                            if (w * bE > bw * E) {
-                                                bw = w; bE = E; part.idx = v0 + c; part.s_at = sv[c];
-                                                rho = race_bound(bE, bw);
-                                            }
-                                        }
-                                    }
-                                }
+                                    if (c >= nvalid) sv[c] = -INFINITY;
                             }
-                        } else {
-                            // one race per request: over max(0, p - q) for a rejected row,
-                            // over p for a bonus draw (q = 0 there)
-                            if (with_u) {
+                            // sampling draft in base 2: w = 2^(s2 - m2) relative to the running max
+                            float cm = sv[0];
 #pragma unroll
-                                for (int c = 0; c < 16; ++c) {
-                                    const uint32_t word = uw[c >> 1];
-                                    const float u = __uint_as_float((c & 1) ? (word & 0xFFFF0000u) : (word << 16));
-                                    sv[c] = (u + sv[c]) * c2;
-                                }
+                            for (int c = 1; c < 16; ++c) cm = fmaxf(cm, sv[c]);
+                            if (cm > part.m) {
+                                const float sc = ex2(part.m - cm);  // 0 while the max is -inf
+                                part.sum *= sc;
+                                bw *= sc;
+                                part.m = cm;
                             }
+                            rho = race_bound(bE, bw);
                             uint4 x[4];
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
                                 x[q] = make_uint4((uint32_t)((v0 >> 2) + q), (uint32_t)pos, (uint32_t)rr, w3);
                             philox4x32_10_x4(x, key0, key1);
-                            {
-                                const float gq = fmaxf(fmaxf(g_own, g_glob),
-                                                       fmaxf(fmaxf(gsh[0], gsh[kM]), fmaxf(gsh[2 * kM], gsh[3 * kM])));
-                                rho = fminf(race_bound(bE, bw), ex2(-gq) * kRaceSlack);
-                            }
+                            // every weight into the normaliser; entries that may beat the
+                            // running winner marked for the exact test
+                            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                             uint32_t cand = 0;
 #pragma unroll
                             for (int c = 0; c < 16; ++c) {
-                                const float pv = ex2(fmaf(tv[c], c2, -rinfo.lse2_p));
-                                const float wgt = with_u ? pv - ex2(sv[c] - rinfo.q_lse2) : pv;
-                                tv[c] = wgt;
-                                cand |= (wgt > 0.0f && one_plus_complement(word_of(x[c >> 2], c & 3)) <
-                                                           fmaf(wgt, rho, 1.0f))
-                                            ? (1u << c)
-                                            : 0u;
+                                const uint32_t wd = word_of(x[c >> 2], c & 3);
+                                const float w = ex2(sv[c] - part.m);
+                                acc[c & 3] += w;
+                                cand |= (one_plus_complement(wd) < fmaf(w, rho, 1.0f)) ? (1u << c) : 0u;
                             }
+                            part.sum += (acc[0] + acc[1]) + (acc[2] + acc[3]);
                             if (cand) {
-                                bool rec = false;
 #pragma unroll
                                 for (int c = 0; c < 16; ++c) {
                                     if (cand & (1u << c)) {
+                                        const float w = ex2(sv[c] - part.m);
                                         const float E = neg_log_uniform(word_of(x[c >> 2], c & 3));
-                                        if (tv[c] * bE > bw * E) {
-                                            bw = tv[c]; bE = E; part.idx = v0 + c;
-                                            rho = fminf(rho, race_bound(bE, bw));
-                                            rec = true;
+                                        if (w * bE > bw * E) {
+                                            bw = w; bE = E; part.idx = v0 + c; part.s_at = sv[c];
+                                            rho = race_bound(bE, bw);
                                         }
                                     }
-                                }
-                                if (rec) {
-                                    g_own = lg2(bw) - lg2(bE);
-                                    gsh[quarter * kM] = g_own;
                                 }
                             }
                         }
                     }
                 }
+            }
+            } else {
+            // ---- residual: one race per request, over max(0, p - q) for a rejected
+            // row and over p for a bonus draw (q = 0 there).  Thread = request row
+            // m x 8 columns of each 32-column pass (pass h covers columns
+            // 32 h + 8 quarter .. + 7 of a tile), four passes per tile.  The row's
+            // target logits and base logits of the pass come from the staging
+            // buffers (target rows:
+            // 16-byte piece c of row m at m * 128 + (c ^ (m % 8)) * 16; base logits:
+            // piece c of row m at m * 64 + (c ^ (m / 2 % 4)) * 16, so a warp's 32
+            // rows read without bank conflicts).
+            const int vq = 8 * quarter;
+            const uint32_t t_off0 = (uint32_t)(m * 128 + (((2 * quarter) ^ (m & 7)) << 4));
+            const uint32_t t_off1 = (uint32_t)(m * 128 + (((2 * quarter + 1) ^ (m & 7)) << 4));
+            const uint32_t ru_off = (uint32_t)(m * 64 + ((quarter ^ ((m >> 1) & 3)) << 4));
+            // pass n's 8 target logits (past the row end: zeros from the copy, read
+            // as -inf: p = 0) and 8 base logits (bf16 pairs); the buffer then goes
+            // back to the producer.  V % 8 == 0 and v % 8 == 0: a piece is wholly
+            // inside or wholly past the row.  False when the wait gave up.
+            auto take_piece = [&](int n, float (&tp)[8], uint32_t (&up)[4]) -> bool {
+                const int b = n % kResBufs;
+                if (!__all_sync(0xFFFFFFFFu,
+                                tc::mbar_wait(&bar.sfull[b], (uint32_t)((n / kResBufs) & 1), abort_flag, kWaitNs)))
+                    return false;
+                const float4 f0 = *reinterpret_cast<const float4*>(sRT + b * kResTBytes + t_off0);
+                const float4 f1 = *reinterpret_cast<const float4*>(sRT + b * kResTBytes + t_off1);
+                const uint4 q = *reinterpret_cast<const uint4*>(sRU + b * kResUBytes + ru_off);
+                tp[0] = f0.x; tp[1] = f0.y; tp[2] = f0.z; tp[3] = f0.w;
+                tp[4] = f1.x; tp[5] = f1.y; tp[6] = f1.z; tp[7] = f1.w;
+                up[0] = q.x; up[1] = q.y; up[2] = q.z; up[3] = q.w;
+                // the values are in registers: the async proxy may overwrite the buffer
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&bar.sempty[b]);
+                return true;
+            };
+            // one pass: the accumulator's 8 columns at col, the piece at v0; last
+            // hands the tile's accumulator back after reading it
+            auto pass = [&](int v0, uint32_t col, bool last, int a, const float (&tp)[8],
+                            const uint32_t (&up)[4]) {
+                float sv[8];
+                __syncwarp();  // lanes that skipped the previous pass rejoin before the aligned load
+                tc::tmem_ld_32x32b_x8<0>(col, sv);
+                tc::tmem_ld_wait();
+                if (last) {
+                    tc::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&bar.tempty[a]);
+                }
+                if (!(row_ok && v0 < p.V)) return;
+                if (with_u) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t word = up[c >> 1];
+                        const float u = __uint_as_float((c & 1) ? (word & 0xFFFF0000u) : (word << 16));
+                        sv[c] = (u + sv[c]) * c2;
+                    }
+                }
+                uint4 x[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                    x[q] = make_uint4((uint32_t)((v0 >> 2) + q), (uint32_t)pos, (uint32_t)rr, w3);
+                philox4x32_10_xn<2>(x, key0, key1);
+                {
+                    const float gq = fmaxf(fmaxf(g_own, g_glob),
+                                           fmaxf(fmaxf(gsh[0], gsh[kM]), fmaxf(gsh[2 * kM], gsh[3 * kM])));
+                    rho = fminf(race_bound(bE, bw), ex2(-gq) * kRaceSlack);
+                }
+                float wv[8];
+                uint32_t cand = 0;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const float pv = ex2(fmaf(tp[c], c2, -rinfo.lse2_p));
+                    const float wgt = with_u ? pv - ex2(sv[c] - rinfo.q_lse2) : pv;
+                    wv[c] = wgt;
+                    cand |= (wgt > 0.0f && one_plus_complement(word_of(x[c >> 2], c & 3)) < fmaf(wgt, rho, 1.0f))
+                                ? (1u << c)
+                                : 0u;
+                }
+                if (cand) {
+                    bool rec = false;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        if (cand & (1u << c)) {
+                            const float E = neg_log_uniform(word_of(x[c >> 2], c & 3));
+                            if (wv[c] * bE > bw * E) {
+                                bw = wv[c]; bE = E; part.idx = v0 + c;
+                                rho = fminf(rho, race_bound(bE, bw));
+                                rec = true;
+                            }
+                        }
+                    }
+                    if (rec) {
+                        g_own = lg2(bw) - lg2(bE);
+                        gsh[quarter * kM] = g_own;
+                    }
+                }
+            };
+            for (int i = 0; staged && i < n_local; ++i) {
+                const int t = cidx + i * p.P;
+                const int a = i & 1;  // one step: the launch's tile index is i
+                const uint32_t use = (uint32_t)(i >> 1);
+                if (share) {
+                    if (i > 0) g_glob = key_log2_ratio(gkey);
+                    gkey = *reinterpret_cast<volatile unsigned long long*>(my_key);
+                }
+                // warp-uniform wait: every lane waits (acquire), all leave together
+                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.tfull[a], use & 1u, abort_flag, kWaitNs))) break;
+                tc::tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(a * kNV + vq);
+                const int vt = t * kNV + vq;
+#pragma unroll 1
+                for (int h = 0; h < 4; ++h) {
+                    float tp[8];
+                    uint32_t up[4];
+                    const int n = 4 * i + h;
+                    if (n + kResAhead < n_res && !stage_issue(n + kResAhead)) { staged = false; break; }
+                    if (!take_piece(n, tp, up)) { staged = false; break; }
+                    pass(vt + kResCols * h, taddr + (uint32_t)(kResCols * h), h == 3, a, tp, up);
+                }
+                if (!staged) break;
                 // this thread's record, if it beats the request's best seen so far, for the
                 // other CTAs racing over it (few threads qualify after the first tiles:
                 // same-address atomics serialise)
                 if (share && g_own > fmaxf(g_pub, g_glob)) {
-                    const float sc = kRes ? logf(bw) - logf(bE) : part.s_at * kLn2F - logf(bE);
-                    atomicMax(my_key, winner_key(sc, part.idx));
+                    atomicMax(my_key, winner_key(logf(bw) - logf(bE), part.idx));
                     g_pub = g_own;
                 }
+            }
+            // staging copies still in flight (after an abort) land before the CTA exits
+            cp_async_wait_all();
             }
             // scores of the winners in log form, for merging across threads and CTAs
             if (kRes) {
@@ -827,7 +955,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
     __syncthreads();
     if (warp == 1) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tmem_base, kTmemCols);
+        tc::tmem_dealloc(tmem_base, kRes ? kTmemColsRes : kTmemCols);
     }
     if (*abort_flag && threadIdx.x == 0) report(p.dev_status, DSPARK_ERR_TIMEOUT);
 }
@@ -994,16 +1122,21 @@ int prepare(EncodeTiled enc, const void* U, const void* W1, const void* W2, int 
     if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return DSPARK_ERR_CUDA;
     const int nkb = rank / kKB;
-    const size_t fixed = 1024 + (size_t)nkb * kTileBytes + (residual ? kShareBytes : 2 * (size_t)kUBufBytes) +
-                         sizeof(Bars);
+    // residual: A lives in tensor memory, the staging buffers in shared memory
+    const size_t fixed =
+        1024 + sizeof(Bars) +
+        (residual ? kShareBytes + (size_t)kResBufs * (kResTBytes + kResUBytes)
+                  : (size_t)nkb * kTileBytes + 2 * (size_t)kUBufBytes);
     // the end-of-step exchange of the epilogue quarters reuses the A rows' space
-    if ((size_t)nkb * kTileBytes < 3 * kM * sizeof(TcPartial)) return DSPARK_ERR_UNSUPPORTED;
+    // (draft) or the drained W2 ring (residual, at least two stages)
+    if (!residual && (size_t)nkb * kTileBytes < 3 * kM * sizeof(TcPartial)) return DSPARK_ERR_UNSUPPORTED;
+    static_assert(2 * kTileBytes >= 3 * kM * sizeof(TcPartial), "exchange larger than two ring stages");
     if ((size_t)max_smem < fixed + 2 * kTileBytes) return DSPARK_ERR_UNSUPPORTED;
     const int n_stages = (int)std::min<size_t>(kMaxStages, ((size_t)max_smem - fixed) / kTileBytes);
     smem = fixed + (size_t)n_stages * kTileBytes;
 
     if (!encode_2d_bf16(enc, &tm_w2, W2, rank, V, kNV)) return DSPARK_ERR_CUDA;
-    {
+    if (!residual) {
         const cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)gamma, (cuuint64_t)R};
         const cuuint64_t strides[2] = {(cuuint64_t)V * 2, (cuuint64_t)gamma * V * 2};
         const cuuint32_t box[3] = {kKB, 1, kM};
@@ -1012,6 +1145,8 @@ int prepare(EncodeTiled enc, const void* U, const void* W1, const void* W2, int 
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return DSPARK_ERR_CUDA;
+    } else {
+        tm_u = tm_w2;  // unused by the residual
     }
     p = TcParams();
     p.U = static_cast<const uint16_t*>(U);

@@ -206,6 +206,45 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, float (&v)[N]
     v[OFF + 14] = __uint_as_float(r14); v[OFF + 15] = __uint_as_float(r15);
 }
 
+// D (+)= A . B^T with A in tensor memory (M lanes, K along the columns, two
+// bf16 per 32-bit column) and B described in shared memory.
+__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 8 consecutive 32-bit columns of this warp's 32 lanes from v[0..7] (thread i
+// of the warp writes lane quadrant base + i).
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 8 consecutive 32-bit columns into v[OFF .. OFF+7].
+template <int OFF, int N>
+__device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, float (&v)[N]) {
+    static_assert(OFF + 8 <= N, "destination too small");
+    uint32_t r0, r1, r2, r3, r4, r5, r6, r7;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3), "=r"(r4), "=r"(r5), "=r"(r6), "=r"(r7)
+                 : "r"(taddr)
+                 : "memory");
+    v[OFF + 0] = __uint_as_float(r0); v[OFF + 1] = __uint_as_float(r1);
+    v[OFF + 2] = __uint_as_float(r2); v[OFF + 3] = __uint_as_float(r3);
+    v[OFF + 4] = __uint_as_float(r4); v[OFF + 5] = __uint_as_float(r5);
+    v[OFF + 6] = __uint_as_float(r6); v[OFF + 7] = __uint_as_float(r7);
+}
+
 // Prefetch one TMA box of a 3-D tensor into L2 (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
     asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(

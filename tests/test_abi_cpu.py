@@ -114,6 +114,21 @@ def test_host_argument_checks(lib):
     a = list(base); a[17] = 100
     assert v(*a) == -7          # workspace too small
 
+    mk = lib.dspark_verify_markov
+    mk.restype = ctypes.c_int
+    mk.argtypes = [vp] * 7 + [ctypes.c_int] + [vp] * 3 + [ctypes.c_uint32, ctypes.c_float] + \
+        [ctypes.c_int] * 4 + [vp] * 4 + [ctypes.c_size_t, vp, vp]
+    # target, cu, y, U, W1, W2, anchor, rank, q_lse, q_tok, seeds, cycle, T, R, gamma, V, max_rows,
+    # n_acc, out, p_tok, ws, ws_bytes, status, stream
+    base = [fake] * 7 + [64] + [fake] * 3 + [0, 1.0, 4, 5, 1024, 24] + [fake] * 3 + \
+        [vp(256 * 64), 1 << 30, None, None]
+    a = list(base); a[0] = vp(4096 + 4)
+    assert mk(*a) == -2         # target logits not 16-byte aligned (sampling)
+    a = list(base); a[3] = vp(4096 + 8)
+    assert mk(*a) == -2         # U not 16-byte aligned
+    a = list(base); a[7] = 100
+    assert mk(*a) == -2         # rank not a multiple of 64
+
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     """The Python binding refuses to import when the shared library is absent."""
