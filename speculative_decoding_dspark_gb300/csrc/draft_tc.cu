@@ -331,6 +331,12 @@ __global__ void __launch_bounds__(256) residual_prep_kernel(ResidualTcArgs a, Re
     w.prev = prev;
     w.pad = 0.0f;
     rows[r] = w;
+    // the residual launch reads this W1 row first (its A row): request it into L2 now
+    if (prev >= 0)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(static_cast<const uint16_t*>(a.W1) +
+                                                                        (size_t)prev * a.rank),
+                     "r"((uint32_t)a.rank * 2u)
+                     : "memory");
 }
 
 template <bool kRes>
@@ -590,38 +596,49 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                 return true;
             };
             bool staged = true;
-            if constexpr (kRes)
-                for (int n = 0; staged && n < kResAhead && n < n_res; ++n) staged = stage_issue(n);
             if constexpr (kRes) {
                 // residual: A in tensor memory from column kAcol (lane = request row,
-                // two bf16 per column); thread (row m, quarter) writes row m's K
-                // elements rank/4 * quarter .. + rank/4 - 1, eight columns per store
-                const int t = bar.a_tok[m];
-                const int kq = p.rank >> 2;  // a multiple of 16
-                const uint4* src =
-                    reinterpret_cast<const uint4*>(p.W1 + (size_t)(t < 0 ? 0 : t) * p.rank + (size_t)quarter * kq);
-                const uint32_t tq =
-                    tmem_base + ((uint32_t)(quad * 32) << 16) + kAcol + (uint32_t)(quarter * (kq >> 1));
-                const int n16 = kq >> 3;  // 16-byte pieces of the quarter row (at most 16)
+                // two bf16 per column).  The rows first pass through the staging
+                // buffers (not in use yet): warp ew copies rows 8 ew .. 8 ew + 7 whole
+                // with cp.async (16-byte piece c of row j at j * rank * 2 +
+                // (c ^ (j % 8)) * 16, zeros for a negative token), so that each
+                // warp instruction reads one row; then thread (row m, quarter) moves
+                // row m's K elements rank/4 * quarter .. + rank/4 - 1 into tensor
+                // memory, eight columns per store, its 32 rows' pieces on distinct banks.
+                const int rowb = p.rank * 2;
 #pragma unroll 1
-                for (int c0 = 0; c0 < n16; c0 += 8) {
-                    uint4 v[8];
+                for (int q = 0; q < 8; ++q) {
+                    const int j = 8 * ew + q;
+                    const int t = bar.a_tok[j];
+                    const uint4* src = reinterpret_cast<const uint4*>(p.W1 + (size_t)(t < 0 ? 0 : t) * p.rank);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        v[c] = (t >= 0 && c0 + c < n16) ? __ldg(src + c0 + c) : make_uint4(0u, 0u, 0u, 0u);
+                    for (int h = 0; h < 2; ++h) {
+                        const int c = lane + 32 * h;
+                        if (c < cpr) cp_async_16(sRT + j * rowb + ((c ^ (j & 7)) << 4), src + c, t >= 0);
+                    }
+                }
+                cp_async_wait_all();
+                epi_sync();
+                const int n16 = cpr >> 2;  // 16-byte pieces of a quarter row (at most 16)
+                const uint32_t tq =
+                    tmem_base + ((uint32_t)(quad * 32) << 16) + kAcol + (uint32_t)(quarter * (n16 * 4));
 #pragma unroll
-                    for (int c = 0; c < 8; c += 2) {
-                        if (c0 + c < n16) {  // warp-uniform
-                            const uint32_t w[8] = {v[c].x, v[c].y, v[c].z, v[c].w,
-                                                   v[c + 1].x, v[c + 1].y, v[c + 1].z, v[c + 1].w};
-                            tc::tmem_st_32x32b_x8(tq + (uint32_t)(4 * (c0 + c)), w);
-                        }
+                for (int c = 0; c < 16; c += 2) {
+                    if (c < n16) {  // warp-uniform
+                        const int pc = quarter * n16 + c;
+                        const uint4 v0 = *reinterpret_cast<const uint4*>(sRT + m * rowb + ((pc ^ (m & 7)) << 4));
+                        const uint4 v1 = *reinterpret_cast<const uint4*>(sRT + m * rowb + (((pc + 1) ^ (m & 7)) << 4));
+                        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                        tc::tmem_st_32x32b_x8(tq + (uint32_t)(4 * c), w);
                     }
                 }
                 tc::tmem_st_wait();
                 tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&bar.afull);
+                // every thread has read its A pieces before the staging copies reuse the space
+                epi_sync();
+                for (int n = 0; staged && n < kResAhead && n < n_res; ++n) staged = stage_issue(n);
             } else {
                 // warp ew copies rows 8 ew .. 8 ew + 7, every piece in flight at once
 #pragma unroll 1

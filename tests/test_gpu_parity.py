@@ -143,6 +143,8 @@ MARKOV_CASES = [
     ("varlen_verify", dict(R=24, V=10008, gamma=5, rank=64, w_sigma=0.3), 1.0),
     ("batched_sampling", dict(R=130, V=4096, gamma=3, rank=128, w_sigma=0.3), 1.0),
     ("qwen3_8b_greedy", dict(R=9, V=16392, gamma=7, rank=64, w_sigma=0.3), 0.0),
+    # rank 192: 24 sixteen-byte pieces per W1 row (not a power of two); V % 32 != 0
+    ("batched_sampling", dict(R=11, V=12008, gamma=4, rank=192, w_sigma=0.3), 0.8),
 ]
 
 
