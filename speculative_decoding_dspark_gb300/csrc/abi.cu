@@ -49,7 +49,7 @@ VerifyLayout verify_layout(int R, int V, int max_rows) {
     L.act = off; off += align_up(sizeof(int) * 2 * (size_t)R);
     L.lazy = off; off += align_up(sizeof(int) * 8);
     const int nsub = (V + kStatChunk - 1) / kStatChunk;
-    L.stats = off; off += align_up(sizeof(RowStat) * (size_t)R * nsub);
+    L.stats = off; off += align_up(sizeof(RowStat) * 2 * (size_t)R * nsub);  // two rounds in flight
     L.jobs = off; off += align_up(sizeof(VerifyJob) * (size_t)R);
     L.parts = off; off += align_up(sizeof(SamplePartial) * (size_t)R * nchunk);
     L.total = off;

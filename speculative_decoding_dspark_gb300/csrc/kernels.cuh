@@ -54,7 +54,7 @@ struct VerifyParams {
     int* act;       // [2][R] requests still drafting-accepted, per round parity
     int* lazy;      // [8] round state of the verify pass: barrier count and generation,
                     // next-round counts (2), abort flag
-    RowStat* stats; // [R * nsub] per (request, kStatChunk-element unit of its first row)
+    RowStat* stats; // [2][R * nsub] per (round parity, request, kStatChunk-element unit of its row)
     VerifyJob* jobs;        // [R]
     SamplePartial* parts;   // [R * nchunk]
 };

@@ -17,7 +17,10 @@
 //                    (max, sum of exp, first argmax of t = row * invT); after
 //                    a grid barrier one warp per such request merges its units
 //                    and decides draft j (or, at j = l, takes the bonus row);
-//                    accepted requests go on to round j + 1.  Rows after the
+//                    accepted requests go on to round j + 1 (published by a
+//                    second grid barrier; when at most 24 requests are active,
+//                    every CTA decides all of them itself instead and only the
+//                    owner of a request writes its outputs).  Rows after the
 //                    first rejection are never read: with a weak drafter a
 //                    request needs about one row, with a strong one every
 //                    round still streams at the full rate of the grid.
@@ -148,15 +151,124 @@ __device__ __forceinline__ bool grid_barrier(int* st, unsigned& gen) {
 }
 
 constexpr int kRoundThreads = 768;  // one CTA per SM: 24 warps, a grid barrier of n_sm arrivals
+constexpr int kRoundWarps = kRoundThreads / 32;
 constexpr size_t kMaxListBytes = sizeof(int) * DSPARK_VERIFY_MAX_R;  // the round's request list in shared memory
+
+// What the decision of request r at position j needs besides its row's
+// statistics, fetched early so that it is in registers when they are merged.
+struct DecideInputs {
+    int r = -1, first = 0, l = 0, y = 0, valid = 0;
+    float t = 0.0f, q = 1.0f;
+    uint64_t seed = 0;
+};
+
+template <bool kGreedy>
+__device__ __forceinline__ DecideInputs decide_inputs(const VerifyParams& p, int r, int j) {
+    DecideInputs d;
+    d.r = r;
+    d.valid = p.valid[r];
+    d.first = p.cu[r];
+    d.l = p.cu[r + 1] - d.first - 1;
+    if (d.valid && j < d.l) {
+        d.y = p.y[(size_t)r * p.gamma + j];
+        if (!kGreedy) {
+            d.t = __ldg(p.target + (size_t)(d.first + j) * p.V + d.y);
+            d.q = p.q_tok[(size_t)r * p.gamma + j];
+            d.seed = p.seeds[r];
+        }
+    }
+    return d;
+}
+
+// One warp: merge request d.r's unit statistics of row j (stj, written by other
+// CTAs in this launch: read from L2), decide draft j (or take the bonus row at
+// j = l) and, when `write`, store the outputs.  Returns the number of accepted
+// drafts once decided, -1 when draft j was accepted (the request goes on to
+// round j + 1), -2 for a request with bad inputs.  Every lane returns the same.
+template <bool kGreedy>
+__device__ __forceinline__ int decide_request(const VerifyParams& p, const RowStat* stj, const DecideInputs& d,
+                                              int j, float c2, bool write) {
+    const int lane = threadIdx.x & 31;
+    const int r = d.r, g = p.gamma;
+    if (!d.valid) return -2;
+    const RowStat* rs = stj + (size_t)r * p.nsub;
+    float cm = -INFINITY, cs = 0.0f, am = -INFINITY;
+    int ai = INT_MAX;
+    // four statistics per lane in flight at a time
+    for (int c0 = 0; c0 < p.nsub; c0 += 128) {
+        float4 q4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int c = c0 + lane + 32 * i;
+            q4[i] = c < p.nsub ? __ldcg(reinterpret_cast<const float4*>(rs + c))
+                               : make_float4(-INFINITY, 0.0f, __int_as_float(INT_MAX), 0.0f);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int qi = __float_as_int(q4[i].z);
+            if (better(q4[i].x, qi, am, ai)) { am = q4[i].x; ai = qi; }
+            if (!kGreedy) lse2_merge(cm, cs, q4[i].x, q4[i].y);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = shfl_xor(cm, o), s2 = shfl_xor(cs, o), am2 = shfl_xor(am, o);
+        const int ai2 = shfl_xor(ai, o);
+        lse2_merge(cm, cs, m2, s2);
+        if (better(am2, ai2, am, ai)) { am = am2; ai = ai2; }
+    }
+    const float lse2 = kGreedy ? 0.0f : cm + log2f(cs);  // base-2 log-normaliser of row j
+    int n = -1;  // the request's number of accepted drafts once decided
+    if (j == d.l) {
+        n = d.l;  // every draft accepted: the extra token comes from this row
+    } else if (lane == 0) {
+        bool accept;
+        float pt;
+        if (kGreedy) {
+            accept = (d.y == ai);
+            pt = accept ? 1.0f : 0.0f;
+        } else {
+            pt = exp2f(d.t * c2 - lse2);
+            const float ratio = pt / d.q;
+            const uint4 w = philox4x32_10(make_uint4(0u, (uint32_t)j, (uint32_t)r, ctr_word3(p.cycle, kAccept)),
+                                          (uint32_t)(d.seed & 0xFFFFFFFFu), (uint32_t)(d.seed >> 32));
+            accept = uniform_from_bits(w.x) < ratio;
+        }
+        if (write && p.p_tok) p.p_tok[(size_t)r * g + j] = pt;
+        if (!accept) n = j;
+    }
+    n = __shfl_sync(0xFFFFFFFFu, n, 0);
+    if (n < 0 || !write) return n;
+    int32_t* out = p.out_tokens + (size_t)r * (g + 1);
+    for (int jj = lane; jj <= g; jj += 32)
+        if (jj != n) out[jj] = jj < n ? p.y[(size_t)r * g + jj] : -1;
+    if (lane == 0) {
+        p.n_acc[r] = n;
+        if (kGreedy) {
+            out[n] = (ai >= 0 && ai < p.V) ? ai : -1;
+            if (out[n] < 0) report(p.dev_status, DSPARK_ERR_DEVICE_INPUT);  // NaN row
+        } else {
+            VerifyJob job;
+            job.row = d.first + n;
+            job.pos = n;
+            job.mode = (n < d.l) ? 1 : 2;
+            job.pad = 0;
+            job.lse = lse2 * kLn2;  // natural log-normaliser of t = row * invT
+            job.pad2[0] = job.pad2[1] = job.pad2[2] = 0.0f;
+            p.jobs[r] = job;
+        }
+    }
+    return n;
+}
 
 template <bool kGreedy>
 __global__ void __launch_bounds__(kRoundThreads, 1) verify_rounds_kernel(VerifyParams p) {
     extern __shared__ int s_list[];  // [R] the requests active in the current round
     __shared__ int s_nact;
+    __shared__ int s_next[kRoundWarps];
     if (!p.ok[0]) return;  // the same for every CTA
     const int V = p.V, g = p.gamma;
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
     const int w0 = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
     const int nw = (int)((gridDim.x * (size_t)blockDim.x) >> 5);
     const bool vec = (V & 3) == 0 && ((reinterpret_cast<uintptr_t>(p.target) & 15) == 0);
@@ -167,25 +279,19 @@ __global__ void __launch_bounds__(kRoundThreads, 1) verify_rounds_kernel(VerifyP
     bool all = true;           // round 0: request a is a
     for (int j = 0; j <= g && n_act > 0; ++j) {
         auto act_at = [&](int a) { return all ? a : s_list[a]; };
-        // the warp that decides for an active request fetches what the decision
-        // needs besides the row statistics now, so it is in registers after the stream
-        int d_r = -1, d_first = 0, d_l = 0, d_y = 0, d_valid = 0;
-        float d_t = 0.0f, d_q = 1.0f;
-        uint64_t d_seed = 0;
-        if (w0 < n_act && lane == 0) {
-            d_r = act_at(w0);
-            d_valid = p.valid[d_r];
-            d_first = p.cu[d_r];
-            d_l = p.cu[d_r + 1] - d_first - 1;
-            if (d_valid && j < d_l) {
-                d_y = p.y[(size_t)d_r * g + j];
-                if (!kGreedy) {
-                    d_t = __ldg(p.target + (size_t)(d_first + j) * V + d_y);
-                    d_q = p.q_tok[(size_t)d_r * g + j];
-                    d_seed = p.seeds[d_r];
-                }
-            }
-        }
+        // statistics of round j: two buffers by round parity, so that a CTA
+        // already streaming round j + 1 never overwrites what another CTA still
+        // merges for round j
+        RowStat* stj = p.stats + (size_t)(j & 1) * p.R * p.nsub;
+        // Few active requests: every CTA decides all of them itself (one warp
+        // each, the same result everywhere; outputs written by one owner CTA)
+        // and needs no second grid barrier.  Otherwise one warp of the grid per
+        // request decides, and a barrier publishes the accept flags.
+        const bool local = n_act <= kRoundWarps;
+        const int dw = local ? wl : w0;  // the warp that will decide active request dw
+        // its decision inputs now, so they are in registers after the stream
+        DecideInputs din;
+        if (dw < n_act && lane == 0) din = decide_inputs<kGreedy>(p, act_at(dw), j);
         // ---- row j of every active request: unit statistics
         const int n_units = n_act * p.nsub;
         auto unit_row = [&](int u, int& r, int& sub) {
@@ -254,100 +360,57 @@ __global__ void __launch_bounds__(kRoundThreads, 1) verify_rounds_kernel(VerifyP
                 stt.s = s;
                 stt.idx = bi;
                 stt.pad = 0;
-                p.stats[(size_t)r * p.nsub + sub] = stt;
+                stj[(size_t)r * p.nsub + sub] = stt;
             }
 #pragma unroll
             for (int i = 0; i < kStatVec; ++i) buf[i] = nxt[i];
         }
         if (!grid_barrier(st, gen)) break;
-        // ---- one warp per active request: merge its units, decide draft j
-        for (int a = w0; a < n_act; a += nw) {
-            // a == w0 was prefetched at the round start (lane 0)
-            const bool pre = (a == w0);
-            const int r = pre ? __shfl_sync(0xFFFFFFFFu, d_r, 0) : act_at(a);
-            const int valid = pre ? __shfl_sync(0xFFFFFFFFu, d_valid, 0) : p.valid[r];
-            if (!valid) continue;
-            const int first = pre ? __shfl_sync(0xFFFFFFFFu, d_first, 0) : p.cu[r];
-            const int l = pre ? __shfl_sync(0xFFFFFFFFu, d_l, 0) : p.cu[r + 1] - first - 1;
-            const RowStat* rs = p.stats + (size_t)r * p.nsub;
-            float cm = -INFINITY, cs = 0.0f, am = -INFINITY;
-            int ai = INT_MAX;
-            for (int c = lane; c < p.nsub; c += 32) {
-                // written by other CTAs in this launch: read from L2, not a stale L1 line
-                const float4 q4 = __ldcg(reinterpret_cast<const float4*>(rs + c));
-                RowStat q;
-                q.m = q4.x; q.s = q4.y; q.idx = __float_as_int(q4.z); q.pad = 0;
-                if (better(q.m, q.idx, am, ai)) { am = q.m; ai = q.idx; }
-                if (!kGreedy) lse2_merge(cm, cs, q.m, q.s);
+        // the decision inputs fetched by lane 0, for the whole warp
+        din.r = __shfl_sync(0xFFFFFFFFu, din.r, 0);
+        din.valid = __shfl_sync(0xFFFFFFFFu, din.valid, 0);
+        din.first = __shfl_sync(0xFFFFFFFFu, din.first, 0);
+        din.l = __shfl_sync(0xFFFFFFFFu, din.l, 0);
+        if (local) {
+            // ---- every CTA: warp a decides active request a; the owner CTA writes
+            int nx = -1;
+            if (wl < n_act) {
+                const int r = din.r;
+                const int n = decide_request<kGreedy>(p, stj, din, j, c2, r % (int)gridDim.x == (int)blockIdx.x);
+                nx = n == -1 ? r : -1;
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float m2 = shfl_xor(cm, o), s2 = shfl_xor(cs, o), am2 = shfl_xor(am, o);
-                const int ai2 = shfl_xor(ai, o);
-                lse2_merge(cm, cs, m2, s2);
-                if (better(am2, ai2, am, ai)) { am = am2; ai = ai2; }
+            if (lane == 0) s_next[wl] = nx;
+            __syncthreads();
+            if (threadIdx.x < 32) {
+                const int v = lane < n_act ? s_next[lane] : -1;  // n_act <= kRoundWarps <= 32
+                const unsigned msk = __ballot_sync(0xFFFFFFFFu, v >= 0);
+                if (v >= 0) s_list[__popc(msk & ((1u << lane) - 1u))] = v;
+                if (lane == 0) s_nact = __popc(msk);
             }
-            const float lse2 = kGreedy ? 0.0f : cm + log2f(cs);  // base-2 log-normaliser of row j
-            int n = -1;  // the request's number of accepted drafts once decided
-            if (j == l) {
-                n = l;  // every draft accepted: the extra token comes from this row
-            } else if (lane == 0) {
-                const int yj = pre ? d_y : p.y[(size_t)r * g + j];
-                bool accept;
-                float pt;
-                if (kGreedy) {
-                    accept = (yj == ai);
-                    pt = accept ? 1.0f : 0.0f;
-                } else {
-                    const float tv = pre ? d_t : p.target[(size_t)(first + j) * V + yj];
-                    const float qv = pre ? d_q : p.q_tok[(size_t)r * g + j];
-                    const uint64_t seed = pre ? d_seed : p.seeds[r];
-                    pt = exp2f(tv * c2 - lse2);
-                    const float ratio = pt / qv;
-                    const uint4 w = philox4x32_10(make_uint4(0u, (uint32_t)j, (uint32_t)r, ctr_word3(p.cycle, kAccept)),
-                                                  (uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32));
-                    accept = uniform_from_bits(w.x) < ratio;
+            __syncthreads();
+        } else {
+            // ---- one warp of the grid per active request: decide draft j
+            for (int a = w0; a < n_act; a += nw) {
+                // a == w0 was fetched at the round start (lane 0)
+                const DecideInputs d = (a == w0) ? din : decide_inputs<kGreedy>(p, act_at(a), j);
+                const int n = decide_request<kGreedy>(p, stj, d, j, c2, true);
+                if (n == -1 && lane == 0) p.act[d.r] = j + 1;  // goes on to round j + 1
+            }
+            if (!grid_barrier(st, gen)) break;
+            // every CTA lists the requests accepted in this round (flags written by
+            // other CTAs: read from L2)
+            if (threadIdx.x < 32) {
+                int cnt = 0;
+                for (int base = 0; base < p.R; base += 32) {
+                    const bool f = base + lane < p.R && __ldcg(p.act + base + lane) == j + 1;
+                    const unsigned m = __ballot_sync(0xFFFFFFFFu, f);
+                    if (f) s_list[cnt + __popc(m & ((1u << lane) - 1u))] = base + lane;
+                    cnt += __popc(m);
                 }
-                if (p.p_tok) p.p_tok[(size_t)r * g + j] = pt;
-                if (accept) p.act[r] = j + 1;  // goes on to round j + 1
-                else n = j;
+                if (lane == 0) s_nact = cnt;
             }
-            n = __shfl_sync(0xFFFFFFFFu, n, 0);
-            if (n < 0) continue;
-            int32_t* out = p.out_tokens + (size_t)r * (g + 1);
-            for (int jj = lane; jj <= g; jj += 32)
-                if (jj != n) out[jj] = jj < n ? p.y[(size_t)r * g + jj] : -1;
-            if (lane == 0) {
-                p.n_acc[r] = n;
-                if (kGreedy) {
-                    out[n] = (ai >= 0 && ai < V) ? ai : -1;
-                    if (out[n] < 0) report(p.dev_status, DSPARK_ERR_DEVICE_INPUT);  // NaN row
-                } else {
-                    VerifyJob job;
-                    job.row = first + n;
-                    job.pos = n;
-                    job.mode = (n < l) ? 1 : 2;
-                    job.pad = 0;
-                    job.lse = lse2 * kLn2;  // natural log-normaliser of t = row * invT
-                    job.pad2[0] = job.pad2[1] = job.pad2[2] = 0.0f;
-                    p.jobs[r] = job;
-                }
-            }
+            __syncthreads();
         }
-        if (!grid_barrier(st, gen)) break;
-        // every CTA lists the requests accepted in this round (flags written by
-        // other CTAs: read from L2)
-        if (threadIdx.x < 32) {
-            int cnt = 0;
-            for (int base = 0; base < p.R; base += 32) {
-                const bool f = base + lane < p.R && __ldcg(p.act + base + lane) == j + 1;
-                const unsigned m = __ballot_sync(0xFFFFFFFFu, f);
-                if (f) s_list[cnt + __popc(m & ((1u << lane) - 1u))] = base + lane;
-                cnt += __popc(m);
-            }
-            if (lane == 0) s_nact = cnt;
-        }
-        __syncthreads();
         n_act = s_nact;
         all = false;
     }
