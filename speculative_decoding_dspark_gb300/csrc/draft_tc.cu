@@ -722,20 +722,20 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                     for (int c = 0; c < 16; ++c) {
                         const uint32_t word = uw[c >> 1];
                         const float u = __uint_as_float((c & 1) ? (word & 0xFFFF0000u) : (word << 16));
-                        sv[c] = (u + sv[c]) * c2;
+                        sv[c] = u + sv[c];  // the logit before the temperature
                     }
                     // the values are in registers: the async proxy may overwrite the buffer
                     tc::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(&bar.uempty[h]);
                     if (row_ok && nvalid > 0) {
-                        if (qrow) {  // natural units
-                            const float back = sampling ? kLn2F : 1.0f;
+                        if (qrow) {  // scaled logits s = (U + B) / T
+                            const float sc = sampling ? p.invT : 1.0f;
 #pragma unroll
                             for (int c = 0; c < 16; c += 4)
                                 if (c < nvalid)
-                                    *reinterpret_cast<float4*>(qrow + v0 + c) = make_float4(
-                                        sv[c] * back, sv[c + 1] * back, sv[c + 2] * back, sv[c + 3] * back);
+                                    *reinterpret_cast<float4*>(qrow + v0 + c) =
+                                        make_float4(sv[c] * sc, sv[c + 1] * sc, sv[c + 2] * sc, sv[c + 3] * sc);
                         }
                         if (p.greedy) {
 #pragma unroll
@@ -750,43 +750,87 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                                 for (int c = 0; c < 16; ++c)
                                     if (c >= nvalid) sv[c] = -INFINITY;
                             }
-                            // sampling draft in base 2: w = 2^(s2 - m2) relative to the running max
-                            float cm = sv[0];
+                            // Sampling draft in base 2: w = 2^(s * c2 - m2) with m2 a reference
+                            // for the step's weights: the maximum of its first values, moved
+                            // only when a pass's weights sum past 2^32 (an entry more than
+                            // about 28 above it), so most passes need no maximum.  (max, sum)
+                            // stays a valid log-sum-exp piece whatever the reference.
+                            auto pass_max2 = [&]() {
+                                float cm = sv[0];
 #pragma unroll
-                            for (int c = 1; c < 16; ++c) cm = fmaxf(cm, sv[c]);
-                            if (cm > part.m) {
-                                const float sc = ex2(part.m - cm);  // 0 while the max is -inf
-                                part.sum *= sc;
-                                bw *= sc;
-                                part.m = cm;
-                            }
-                            rho = race_bound(bE, bw);
+                                for (int c = 1; c < 16; ++c) cm = fmaxf(cm, sv[c]);
+                                return cm * c2;
+                            };
                             uint4 x[4];
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
                                 x[q] = make_uint4((uint32_t)((v0 >> 2) + q), (uint32_t)pos, (uint32_t)rr, w3);
                             philox4x32_10_x4(x, key0, key1);
-                            // every weight into the normaliser; entries that may beat the
-                            // running winner marked for the exact test
-                            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                            uint32_t cand = 0;
+                            if (part.m == -INFINITY) {
+                                // the step's first values: their largest is the reference and
+                                // seeds the race (a real entry, so the winner is unchanged; it
+                                // replaces nothing when it is tested again), which spares the
+                                // no-log test the empty record's unbounded rho
+                                int cb = -1;
+                                float sb = -INFINITY;
+                                uint32_t wb = 0;
 #pragma unroll
-                            for (int c = 0; c < 16; ++c) {
-                                const uint32_t wd = word_of(x[c >> 2], c & 3);
-                                const float w = ex2(sv[c] - part.m);
-                                acc[c & 3] += w;
-                                cand |= (one_plus_complement(wd) < fmaf(w, rho, 1.0f)) ? (1u << c) : 0u;
+                                for (int c = 0; c < 16; ++c)  // a NaN is never chosen
+                                    if (sv[c] > sb) { sb = sv[c]; cb = c; wb = word_of(x[c >> 2], c & 3); }
+                                part.m = sb * c2;
+                                if (cb >= 0 && part.m != -INFINITY) {
+                                    bw = ex2(fmaf(sb, c2, -part.m));
+                                    bE = neg_log_uniform(wb);
+                                    part.idx = v0 + cb;
+                                    part.s_at = sb * c2;
+                                } else {
+                                    part.m = -INFINITY;  // nothing finite yet
+                                }
                             }
-                            part.sum += (acc[0] + acc[1]) + (acc[2] + acc[3]);
-                            if (cand) {
+                            if (part.m != -INFINITY) {                     // else nothing finite yet
+                                rho = race_bound(bE, bw);
+                                // every weight into the normaliser; entries that may beat the
+                                // running winner marked for the exact test
+                                float ps;
+                                uint32_t cand;
+                                auto weigh = [&]() {
+                                    const float nm = -part.m;
+                                    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                                    cand = 0;
 #pragma unroll
-                                for (int c = 0; c < 16; ++c) {
-                                    if (cand & (1u << c)) {
-                                        const float w = ex2(sv[c] - part.m);
-                                        const float E = neg_log_uniform(word_of(x[c >> 2], c & 3));
-                                        if (w * bE > bw * E) {
-                                            bw = w; bE = E; part.idx = v0 + c; part.s_at = sv[c];
-                                            rho = race_bound(bE, bw);
+                                    for (int c = 0; c < 16; ++c) {
+                                        const uint32_t wd = word_of(x[c >> 2], c & 3);
+                                        const float w = ex2(fmaf(sv[c], c2, nm));
+                                        acc[c & 3] += w;
+                                        cand |= (one_plus_complement(wd) < fmaf(w, rho, 1.0f)) ? (1u << c) : 0u;
+                                    }
+                                    ps = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                                };
+                                weigh();
+                                if (!(ps <= 0x1p32f)) {
+                                    // far above the reference (or a NaN): re-reference on this pass
+                                    const float cm = pass_max2();
+                                    if (cm > part.m) {
+                                        const float sc = ex2(part.m - cm);
+                                        part.sum *= sc;
+                                        bw *= sc;
+                                        part.m = cm;
+                                        rho = race_bound(bE, bw);
+                                        weigh();
+                                    }
+                                }
+                                part.sum += ps;
+                                if (cand) {
+                                    const float nm = -part.m;
+#pragma unroll
+                                    for (int c = 0; c < 16; ++c) {
+                                        if (cand & (1u << c)) {
+                                            const float w = ex2(fmaf(sv[c], c2, nm));
+                                            const float E = neg_log_uniform(word_of(x[c >> 2], c & 3));
+                                            if (w * bE > bw * E) {
+                                                bw = w; bE = E; part.idx = v0 + c; part.s_at = sv[c] * c2;
+                                                rho = race_bound(bE, bw);
+                                            }
                                         }
                                     }
                                 }
