@@ -271,9 +271,9 @@ def run_ours(args):
         if ev is not None: ev[4].record(stream)
 
     # launches of this library per step
-    # tensor cores: every position in one launch, then the finalize; CUDA cores:
+    # tensor cores: every position and the finalize in one launch; CUDA cores:
     # counter reset, then bias and sample kernels per position
-    draft_launches = 2 if uses_tc else 1 + 2 * gamma
+    draft_launches = 1 if uses_tc else 1 + 2 * gamma
     verify_launches = 5 if T > 0 else 2  # prologue, stats, (residual rows, draw, finalize)
     launches_per_step = (int(run_select) + draft_launches * int(run_draft) +
                          verify_launches * int(run_verify) + int(run_commit))
@@ -311,8 +311,8 @@ def run_ours(args):
     # roofline of the dominant kernel.  Algorithmic bytes of one Markov draft
     # step (one vocabulary pass): W2 once, U_k once, q_logits if written.  The
     # tensor-core kernel runs all gamma steps in one launch, timed as the whole
-    # draft call (which adds the workspace reset and the finalize, so the
-    # fraction is a lower bound); the CUDA-core path is timed per step.
+    # draft call (which adds the workspace reset, so the fraction is a lower
+    # bound); the CUDA-core path is timed per step.
     step_bytes = V * rank_r * 2 + R * V * 2 + (R * V * 4 if q_logits is not None else 0)
     steps_per_launch = gamma if uses_tc else 1
     launch_bytes = step_bytes * steps_per_launch

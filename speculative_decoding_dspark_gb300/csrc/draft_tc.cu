@@ -55,9 +55,9 @@
 // next A rows from the keys of step k.  Nothing else waits: the W2 ring and
 // the U passes do not depend on the draws and stream on into the next step
 // while the epilogue finishes the current one, and tensor memory, barriers
-// and the ring are set up once per block instead of once per position.  One
-// finalize kernel after the last step (a programmatic dependent) turns keys
-// and pieces into tokens, q_lse and q(y).
+// and the ring are set up once per block instead of once per position.  After
+// one more grid barrier past the last step, the epilogue warps of the grid
+// turn keys and pieces into tokens, q_lse and q(y).
 //
 // Warp roles: warp 0 = W2 TMA producer, warp 1 = MMA issuer (and TMEM
 // owner), warp 2 = U TMA producer (draft), warps 3-18 = epilogue (and the A
@@ -139,6 +139,9 @@ struct TcParams {
     int nb, P, n_tiles, n_stages, nkb;
     const int32_t* anchor;
     float* q_logits;
+    int32_t* y;                // draft outputs [R][gamma]
+    float* q_lse;
+    float* q_tok;
     const float* target;
     const ResRow* rows;
 };
@@ -262,12 +265,6 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x
                  : "memory");
 }
 
-// Programmatic dependent launch: wait for the grids this one depends on to
-// complete (and their writes to be visible); allow dependents to be scheduled.
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void griddep_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
 
 
 // 16 bytes global -> shared without registers; zeros when !valid (nothing read).
@@ -394,9 +391,6 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    // the launch after this one (the finalize) may be scheduled early; it waits
-    // (griddepcontrol) for this one to complete before reading its results
-    griddep_launch_dependents();
     const uint32_t tmem_base = bar.tmem_slot;
     const int n_local = cidx < p.n_tiles ? (p.n_tiles - 1 - cidx) / p.P + 1 : 0;
     const int n_tl = n_steps * n_local;  // tiles of this CTA over the launch: step-major
@@ -1011,6 +1005,69 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                 if (!bar.step_ok) break;
             }
         }
+        if constexpr (!kRes) {
+            // ---- after the last position: every CTA's keys and pieces are
+            // published (the last counter) before any CTA reads them, then each
+            // epilogue warp of the grid finalizes (position, request) pairs: the
+            // token from the winner key, the log-normaliser from the CTAs' (max,
+            // sum) pieces, q(y) from the piece of the CTA that held the winner.  A
+            // request without a key had an unusable anchor or predecessor (or no
+            // finite logit): its token is -1 and its q values NaN.
+            epi_sync();
+            if (e == 0) {
+                int* abort_word = reinterpret_cast<int*>(p.step_done + p.gamma);
+                bool ok = !*abort_flag;
+                if (ok) ok = step_barrier(p.step_done + (p.gamma - 1), abort_word, gridDim.x);
+                else atomicExch(abort_word, 1);
+                if (!ok) *abort_flag = 1;
+                bar.step_ok = ok ? 1 : 0;
+            }
+            epi_sync();
+            if (bar.step_ok) {
+                const int n_pairs = p.gamma * p.R;
+                const int gw_stride = (int)gridDim.x * kEpiWarps;
+                for (int pr = (int)blockIdx.x * kEpiWarps + ew; pr < n_pairs; pr += gw_stride) {
+                    const int k = pr / p.R, r = pr - k * p.R;
+                    const size_t slot = (size_t)k * p.R + r;
+                    const size_t rk = (size_t)r * p.gamma + k;
+                    const unsigned long long key = __ldcg(p.keys + slot);
+                    if (key == 0) {
+                        if (lane == 0) {
+                            p.y[rk] = -1;
+                            if (!p.greedy) {
+                                if (p.q_lse) p.q_lse[rk] = NAN;
+                                if (p.q_tok) p.q_tok[rk] = NAN;
+                            }
+                            report(p.dev_status, DSPARK_ERR_DEVICE_INPUT);
+                        }
+                        continue;
+                    }
+                    const int idx = key_index(key);
+                    if (p.greedy) {
+                        if (lane == 0) p.y[rk] = idx;
+                        continue;
+                    }
+                    float fm = -INFINITY, fs = 0.0f, sat = -INFINITY;
+                    for (int j = lane; j < p.P; j += 32) {
+                        const float4 q = __ldcg(p.parts + slot * p.P + j);
+                        lse_merge(fm, fs, q.x, q.y);
+                        if (__float_as_int(q.w) == idx) sat = q.z;
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const float m2 = shfl_xor(fm, o), s2 = shfl_xor(fs, o);
+                        lse_merge(fm, fs, m2, s2);
+                        sat = fmaxf(sat, shfl_xor(sat, o));
+                    }
+                    if (lane == 0) {
+                        const float lse = fm + logf(fs);
+                        p.y[rk] = idx;
+                        if (p.q_lse) p.q_lse[rk] = lse;
+                        if (p.q_tok) p.q_tok[rk] = expf(sat - lse);
+                    }
+                }
+            }
+        }
     }
 
     __syncthreads();
@@ -1019,65 +1076,6 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         tc::tmem_dealloc(tmem_base, kRes ? kTmemColsRes : kTmemCols);
     }
     if (*abort_flag && threadIdx.x == 0) report(p.dev_status, DSPARK_ERR_TIMEOUT);
-}
-
-struct DraftFinalize {
-    const unsigned long long* keys;
-    const float4* parts;
-    int R, gamma, P, greedy;
-    int32_t* y;
-    float* q_lse;
-    float* q_tok;
-    int32_t* dev_status;
-};
-
-// One warp per (position, request): the token from the step's winner key, the
-// log-normaliser from the CTAs' (max, sum) pieces, q(y) from the piece of the
-// CTA that held the winner.  A request without a key had an unusable anchor or
-// predecessor (or no finite logit): its token is -1 and its q values NaN.
-__global__ void __launch_bounds__(256) draft_finalize_kernel(DraftFinalize f) {
-    griddep_wait();
-    const int gw = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
-    const int lane = threadIdx.x & 31;
-    if (gw >= f.R * f.gamma) return;
-    const int k = gw / f.R, r = gw - k * f.R;
-    const size_t slot = (size_t)k * f.R + r;
-    const size_t rk = (size_t)r * f.gamma + k;
-    const unsigned long long key = f.keys[slot];
-    if (key == 0) {
-        if (lane == 0) {
-            f.y[rk] = -1;
-            if (!f.greedy) {
-                if (f.q_lse) f.q_lse[rk] = NAN;
-                if (f.q_tok) f.q_tok[rk] = NAN;
-            }
-            report(f.dev_status, DSPARK_ERR_DEVICE_INPUT);
-        }
-        return;
-    }
-    const int idx = key_index(key);
-    if (f.greedy) {
-        if (lane == 0) f.y[rk] = idx;
-        return;
-    }
-    float m = -INFINITY, s = 0.0f, sat = -INFINITY;
-    for (int j = lane; j < f.P; j += 32) {
-        const float4 q = f.parts[slot * f.P + j];
-        lse_merge(m, s, q.x, q.y);
-        if (__float_as_int(q.w) == idx) sat = q.z;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = shfl_xor(m, o), s2 = shfl_xor(s, o);
-        lse_merge(m, s, m2, s2);
-        sat = fmaxf(sat, shfl_xor(sat, o));
-    }
-    if (lane == 0) {
-        const float lse = m + logf(s);
-        f.y[rk] = idx;
-        if (f.q_lse) f.q_lse[rk] = lse;
-        if (f.q_tok) f.q_tok[rk] = expf(sat - lse);
-    }
 }
 
 // The extra token of every request, one CTA each: the race's winner (over
@@ -1254,6 +1252,9 @@ int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream) {
     p.anchor = a.anchor;
     p.seeds = a.seeds;
     p.q_logits = a.q_logits;
+    p.y = a.y;
+    p.q_lse = a.q_lse;
+    p.q_tok = a.q_tok;
     p.dev_status = a.dev_status;
     p.cycle = a.cycle;
     p.invT = a.invT;
@@ -1277,30 +1278,6 @@ int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream) {
     cfg.attrs = coop;
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, markov_tc_kernel<false>, tm_w2, tm_u, p) != cudaSuccess) return DSPARK_ERR_CUDA;
-    // the finalize is a programmatic dependent: it may start as the steps
-    // retire and waits (griddepcontrol) before reading their results
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    DraftFinalize f;
-    f.keys = p.keys;
-    f.parts = p.parts;
-    f.R = a.R;
-    f.gamma = a.gamma;
-    f.P = p.P;
-    f.greedy = a.greedy;
-    f.y = a.y;
-    f.q_lse = a.q_lse;
-    f.q_tok = a.q_tok;
-    f.dev_status = a.dev_status;
-    cudaLaunchConfig_t fcfg = {};
-    const long long warps = (long long)a.R * a.gamma;
-    fcfg.gridDim = dim3((unsigned)((warps * 32 + 255) / 256));
-    fcfg.blockDim = dim3(256);
-    fcfg.stream = stream;
-    fcfg.attrs = attr;
-    fcfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&fcfg, draft_finalize_kernel, f) != cudaSuccess) return DSPARK_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 
