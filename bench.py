@@ -274,7 +274,7 @@ def run_ours(args):
     # tensor cores: every position and the finalize in one launch; CUDA cores:
     # counter reset, then bias and sample kernels per position
     draft_launches = 1 if uses_tc else 1 + 2 * gamma
-    verify_launches = 5 if T > 0 else 2  # prologue, stats, (residual rows, draw, finalize)
+    verify_launches = 4 if T > 0 else 2  # prologue, rounds, (residual draw, finalize)
     launches_per_step = (int(run_select) + draft_launches * int(run_draft) +
                          verify_launches * int(run_verify) + int(run_commit))
 

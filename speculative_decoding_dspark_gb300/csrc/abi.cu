@@ -243,14 +243,21 @@ int dspark_verify_markov(const float* target_logits, const int32_t* cu_seqlens,
     p.stats = carve<RowStat>(ws, L.stats);
     p.jobs = carve<VerifyJob>(ws, L.jobs);
     p.parts = carve<SamplePartial>(ws, L.parts);
+    if (!greedy) {  // the decisions write the residual draw's per-request rows
+        p.res_rows = residual_tc_rows(static_cast<unsigned char*>(ws) + res_off, R);
+        p.res_keys = residual_tc_keys(static_cast<unsigned char*>(ws) + res_off, R);
+        p.anchor = anchor;
+        p.W1 = static_cast<const uint16_t*>(W1);
+        p.rank = rank;
+    }
     const cudaError_t e = launch_verify_decide(p, s);
     if (e != cudaSuccess) return DSPARK_ERR_CUDA;
     if (greedy) return DSPARK_OK;  // the decision pass already wrote the argmax token
 
     ResidualTcArgs a;
-    a.U = U; a.W1 = W1; a.W2 = W2; a.anchor = anchor; a.y = draft_tokens; a.seeds = seeds;
+    a.U = U; a.W1 = W1; a.W2 = W2; a.seeds = seeds;
     a.cycle = cycle; a.invT = p.invT; a.R = R; a.gamma = gamma; a.V = V; a.rank = rank;
-    a.target = target_logits; a.q_lse = q_lse; a.jobs = p.jobs; a.valid = p.valid;
+    a.target = target_logits;
     a.out_tokens = out_tokens; a.dev_status = dev_status;
     a.ws = static_cast<unsigned char*>(ws) + res_off;
     return launch_residual_tc(a, s);

@@ -112,17 +112,6 @@ struct TcPartial {
     float pad[3];
 };
 
-// Per-request description of the residual launch.
-struct ResRow {
-    int mode;      // 0: nothing to draw, 1: residual of row pos, 2: bonus from p of row pos
-    int pos;       // block position of the row
-    int trow;      // packed target row
-    uint32_t w3;   // Philox counter word 3 (cycle and purpose)
-    float lse2_p;  // target log-normaliser of the row (scaled logits), base 2
-    float q_lse2;  // drafter log-normaliser at pos (mode 1), base 2
-    int prev;      // token whose W1 row is the A row (mode 1), else -1
-    float pad;
-};
 
 struct TcParams {
     const uint16_t* U;
@@ -306,35 +295,6 @@ __device__ __forceinline__ bool step_barrier(unsigned* done, int* abort_word, un
     return true;
 }
 
-// Per request after the verify decisions: what the residual launch draws and
-// the token whose W1 row is its A row.  One thread per request.
-__global__ void __launch_bounds__(256) residual_prep_kernel(ResidualTcArgs a, ResRow* rows) {
-    const int r = (int)(blockIdx.x * (size_t)blockDim.x + threadIdx.x);
-    if (r >= a.R) return;
-    const VerifyJob job = a.jobs[r];
-    const int mode = a.valid[r] ? job.mode : 0;
-    int prev = -1;
-    if (mode == 1) {
-        prev = job.pos == 0 ? a.anchor[r] : a.y[(size_t)r * a.gamma + job.pos - 1];
-        if (prev >= a.V || prev < 0) prev = -1;
-    }
-    ResRow w;
-    w.mode = mode;
-    w.pos = job.pos;
-    w.trow = job.row;
-    w.w3 = ctr_word3(a.cycle, mode == 1 ? kResidualGumbel : kBonusGumbel);
-    w.lse2_p = job.lse * kLog2eF;
-    w.q_lse2 = mode == 1 ? a.q_lse[(size_t)r * a.gamma + job.pos] * kLog2eF : 0.0f;
-    w.prev = prev;
-    w.pad = 0.0f;
-    rows[r] = w;
-    // the residual launch reads this W1 row first (its A row): request it into L2 now
-    if (prev >= 0)
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(static_cast<const uint16_t*>(a.W1) +
-                                                                        (size_t)prev * a.rank),
-                     "r"((uint32_t)a.rank * 2u)
-                     : "memory");
-}
 
 template <bool kRes>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -1234,6 +1194,14 @@ size_t draft_tc_workspace(int R, int gamma, int /*rank*/) { return tc_layout(R, 
 
 size_t residual_tc_workspace(int R, int /*rank*/) { return tc_layout(R, 0, true).total; }
 
+ResRow* residual_tc_rows(void* ws, int R) {
+    return reinterpret_cast<ResRow*>(static_cast<unsigned char*>(ws) + tc_layout(R, 0, true).rows);
+}
+
+unsigned long long* residual_tc_keys(void* ws, int R) {
+    return reinterpret_cast<unsigned long long*>(static_cast<unsigned char*>(ws) + tc_layout(R, 0, true).keys);
+}
+
 int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream) {
     EncodeTiled enc = encoder();
     if (!enc) return DSPARK_ERR_CUDA;
@@ -1293,8 +1261,7 @@ int launch_residual_tc(const ResidualTcArgs& a, cudaStream_t stream) {
     const int st = prepare(enc, a.U, a.W1, a.W2, a.R, a.gamma, a.V, a.rank, true, p, tm_w2, tm_u, grid, smem, n_sm);
     if (st != DSPARK_OK) return st;
     ResRow* rows = reinterpret_cast<ResRow*>(w + L.rows);
-    p.keys = reinterpret_cast<unsigned long long*>(w + L.keys);
-    p.anchor = a.anchor;
+    p.keys = reinterpret_cast<unsigned long long*>(w + L.keys);  // zeroed by the verify prologue
     p.seeds = a.seeds;
     p.dev_status = a.dev_status;
     p.cycle = a.cycle;
@@ -1305,9 +1272,6 @@ int launch_residual_tc(const ResidualTcArgs& a, cudaStream_t stream) {
     if (cudaFuncSetAttribute(markov_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return DSPARK_ERR_CUDA;
-    if (cudaMemsetAsync(p.keys, 0, sizeof(unsigned long long) * L.n_keys, stream) != cudaSuccess)
-        return DSPARK_ERR_CUDA;
-    residual_prep_kernel<<<(unsigned)((a.R + 255) / 256), 256, 0, stream>>>(a, rows);
     markov_tc_kernel<true><<<grid, kThreads, smem, stream>>>(tm_w2, tm_u, p);
     residual_finalize_kernel<<<a.R, 256, 0, stream>>>(rows, p.keys, a.target, a.seeds, a.invT, a.gamma, a.V,
                                                       a.out_tokens, a.dev_status);

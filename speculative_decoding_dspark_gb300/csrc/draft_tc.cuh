@@ -26,20 +26,17 @@ struct DraftTcArgs {
 
 // The extra token of every request after the verify decisions, with the
 // drafter's logits of the rejected row recomputed from its Markov factors.
+// The per-request rows (residual_tc_rows of the workspace) are written by the
+// verify decisions and the keys (residual_tc_keys) zeroed by its prologue.
 struct ResidualTcArgs {
     const void* U;
     const void* W1;
     const void* W2;
-    const int32_t* anchor;
-    const int32_t* y;          // draft tokens [R, gamma]
     const uint64_t* seeds;
     uint32_t cycle;
     float invT;
     int R, gamma, V, rank;
     const float* target;       // packed target rows
-    const float* q_lse;        // the drafter's log-normalisers [R, gamma]
-    const VerifyJob* jobs;     // per request: row, position and kind of the extra token
-    const int* valid;          // per request: inputs usable
     int32_t* out_tokens;       // [R, gamma + 1]
     int32_t* dev_status;
     void* ws;
@@ -50,6 +47,10 @@ size_t draft_tc_workspace(int R, int gamma, int rank);
 int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream);
 
 size_t residual_tc_workspace(int R, int rank);
+// the per-request rows and winner keys inside the residual workspace (both
+// prepared by the verify kernels: rows as requests are decided, keys zeroed)
+ResRow* residual_tc_rows(void* ws, int R);
+unsigned long long* residual_tc_keys(void* ws, int R);
 int launch_residual_tc(const ResidualTcArgs& a, cudaStream_t stream);
 
 }  // namespace dspark

@@ -30,6 +30,19 @@ struct SamplePartial {  // per (request, chunk) of a Gumbel-max draw
     float pad[3];
 };
 
+// Per request after the verify decisions, for the residual draw of
+// dspark_verify_markov: what it draws and the A row of its recomputed logits.
+struct ResRow {
+    int mode;      // 0: nothing to draw, 1: residual of row pos, 2: bonus from p of row pos
+    int pos;       // block position of the row
+    int trow;      // packed target row
+    uint32_t w3;   // Philox counter word 3 (cycle and purpose)
+    float lse2_p;  // target log-normaliser of the row (scaled logits), base 2
+    float q_lse2;  // drafter log-normaliser at pos (mode 1), base 2
+    int prev;      // token whose W1 row is the A row (mode 1), else -1
+    float pad;
+};
+
 struct VerifyParams {
     const float* target;
     const int32_t* cu;
@@ -57,6 +70,13 @@ struct VerifyParams {
     RowStat* stats; // [2][R * nsub] per (round parity, request, kStatChunk-element unit of its row)
     VerifyJob* jobs;        // [R]
     SamplePartial* parts;   // [R * nchunk]
+    // dspark_verify_markov only (else NULL): the residual rows, written as the
+    // requests are decided, and what they need
+    ResRow* res_rows = nullptr;       // [R]
+    unsigned long long* res_keys = nullptr;  // [R] the residual draw's winner keys, zeroed by the prologue
+    const int32_t* anchor = nullptr;  // [R]
+    const uint16_t* W1 = nullptr;     // [V, rank] bf16: each predecessor's row is requested into L2
+    int rank = 0;
 };
 
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream);

@@ -63,6 +63,12 @@ __global__ void __launch_bounds__(1024) verify_prologue_kernel(VerifyParams p) {
         p.valid[r] = valid;
         p.act[r] = 0;
         p.act[p.R + r] = 0;
+        if (p.res_rows) {  // nothing to draw until the request is decided
+            ResRow w;
+            w.mode = 0; w.pos = 0; w.trow = 0; w.w3 = 0; w.lse2_p = 0.0f; w.q_lse2 = 0.0f; w.prev = -1; w.pad = 0.0f;
+            p.res_rows[r] = w;
+            p.res_keys[r] = 0ull;
+        }
         if (!valid) {
             p.n_acc[r] = -1;
             for (int j = 0; j <= p.gamma; ++j) p.out_tokens[(size_t)r * (p.gamma + 1) + j] = -1;
@@ -256,6 +262,31 @@ __device__ __forceinline__ int decide_request(const VerifyParams& p, const RowSt
             job.lse = lse2 * kLn2;  // natural log-normaliser of t = row * invT
             job.pad2[0] = job.pad2[1] = job.pad2[2] = 0.0f;
             p.jobs[r] = job;
+            if (p.res_rows) {
+                // the residual draw's row: a rejection at n draws from max(0, p - q) of
+                // row n, whose drafter logits come from W1 of the token before
+                // position n (the anchor at n = 0); full acceptance draws from p
+                int prev = -1;
+                if (job.mode == 1) {
+                    prev = n == 0 ? p.anchor[r] : p.y[(size_t)r * g + n - 1];
+                    if (prev >= p.V || prev < 0) prev = -1;
+                }
+                ResRow w;
+                w.mode = job.mode;
+                w.pos = n;
+                w.trow = job.row;
+                w.w3 = ctr_word3(p.cycle, job.mode == 1 ? kResidualGumbel : kBonusGumbel);
+                w.lse2_p = lse2;
+                w.q_lse2 = job.mode == 1 ? p.q_lse[(size_t)r * g + n] * kLog2e : 0.0f;
+                w.prev = prev;
+                w.pad = 0.0f;
+                p.res_rows[r] = w;
+                // the residual launch reads this W1 row first (its A row)
+                if (prev >= 0)
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.W1 + (size_t)prev * p.rank),
+                                 "r"((uint32_t)p.rank * 2u)
+                                 : "memory");
+            }
         }
     }
     return n;
