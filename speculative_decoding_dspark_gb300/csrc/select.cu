@@ -23,7 +23,6 @@ namespace dspark {
 namespace {
 
 constexpr int kNT = kSelectThreads;
-constexpr int kIPT = kSelectMaxItems / kNT;  // items per thread (blocked layout)
 
 // Exclusive scan of one int per thread over the CTA; returns the total in *tot.
 __device__ __forceinline__ int block_exclusive_scan(int x, int* tot, int* warp_sums) {
@@ -106,9 +105,15 @@ __device__ bool survival_sort_scan(SelectSmem& sm, const float* c, float* a_out,
     if (threadIdx.x == 0) sm.flag = 0;
     __syncthreads();
     for (int r = threadIdx.x; r < R; r += kNT) {
+        // the request's confidences, all loads in flight at once (gamma <= 16)
+        float cv[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) cv[k] = k < gamma ? c[(size_t)r * gamma + k] : 1.0f;
         float run = 1.0f;
-        for (int k = 0; k < gamma; ++k) {
-            const float ck = c[(size_t)r * gamma + k];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            if (k >= gamma) break;
+            const float ck = cv[k];
             if (!(ck >= 0.0f && ck <= 1.0f)) atomicOr(&sm.flag, 1);
             run = (k == 0) ? ck : run * ck;
             const int idn = k * R + r;
@@ -121,9 +126,11 @@ __device__ bool survival_sort_scan(SelectSmem& sm, const float* c, float* a_out,
     if (sm.flag) return false;
     if (!do_sort) return true;
 
-    // stable split passes, one per bit, ones (larger) first
+    // stable split passes, one per bit, ones (larger) first; blocked layout over
+    // all threads (thread t holds candidates t * ipt .. + ipt - 1, in order)
     int src = 0;
-    const int lo = min(N, threadIdx.x * kIPT), hi = min(N, lo + kIPT);
+    const int ipt = (N + kNT - 1) / kNT;
+    const int lo = min(N, threadIdx.x * ipt), hi = min(N, lo + ipt);
     for (int bit = 0; bit < 31; ++bit) {
         int ones = 0;
         for (int i = lo; i < hi; ++i) ones += (sm.key[src][i] >> bit) & 1u;

@@ -53,10 +53,13 @@ __global__ void __launch_bounds__(1024) verify_prologue_kernel(VerifyParams p) {
         p.cnt2[r] = 0;
         int valid = ok;
         if (ok) {
-            const int l = p.cu[r + 1] - p.cu[r] - 1;
-            for (int j = 0; j < l; ++j) {
-                const int yj = p.y[(size_t)r * p.gamma + j];
-                if (yj < 0 || yj >= p.V) valid = 0;
+            const int l = p.cu[r + 1] - p.cu[r] - 1;  // 0 <= l <= gamma <= 16 here
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {  // independent loads, all in flight
+                if (j < l) {
+                    const int yj = p.y[(size_t)r * p.gamma + j];
+                    if (yj < 0 || yj >= p.V) valid = 0;
+                }
             }
             if (!valid) report(p.dev_status, DSPARK_ERR_DEVICE_INPUT);
         }
