@@ -110,7 +110,10 @@ size_t dspark_workspace_size(int op, int R, int gamma, int V, int rank, int max_
                              int w_dtype, unsigned flags);
 
 /* 1 if dspark_markov_draft would use the tcgen05 tensor-core kernel for these
- * arguments, 0 for the CUDA-core kernels. */
+ * arguments, 0 for the CUDA-core kernels.  The tensor-core kernel takes bf16 U
+ * and factors, rank a multiple of 64 up to 512, V a multiple of 8, and at most
+ * 128 requests per SM of the current device (all positions run in one launch
+ * whose CTAs are resident together). */
 int dspark_markov_draft_uses_tensor_cores(int u_dtype, int w_dtype, int R, int V, int rank,
                                           unsigned flags);
 

@@ -63,7 +63,7 @@ T* carve(void* ws, size_t off) {
 
 bool tc_applies(int u_dtype, int w_dtype, int R, int V, int rank, unsigned flags) {
     if (flags & DSPARK_DRAFT_FORCE_SIMT) return false;
-    return draft_tc_supported(u_dtype, w_dtype, R, V, rank);
+    return draft_tc_supported(u_dtype, w_dtype, R, V, rank) && draft_tc_fits(R);
 }
 
 bool valid_dtype(int d) { return d == DSPARK_F32 || d == DSPARK_BF16; }

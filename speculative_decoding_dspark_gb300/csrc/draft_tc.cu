@@ -1185,6 +1185,13 @@ int prepare(EncodeTiled enc, const void* U, const void* W1, const void* W2, int 
 
 }  // namespace
 
+bool draft_tc_fits(int R) {
+    int dev = 0, n_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    return (R + kM - 1) / kM <= n_sm;
+}
+
 bool draft_tc_supported(int u_dtype, int w_dtype, int R, int V, int rank) {
     return u_dtype == DSPARK_BF16 && w_dtype == DSPARK_BF16 && R >= 1 && rank % kKB == 0 && rank >= kKB &&
            rank <= 512 && V % 8 == 0 && V >= 8;

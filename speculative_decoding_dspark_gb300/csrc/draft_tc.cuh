@@ -43,6 +43,8 @@ struct ResidualTcArgs {
 };
 
 bool draft_tc_supported(int u_dtype, int w_dtype, int R, int V, int rank);
+// the draft's one cooperative launch needs a CTA per SM for every 128 requests
+bool draft_tc_fits(int R);
 size_t draft_tc_workspace(int R, int gamma, int rank);
 int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream);
 

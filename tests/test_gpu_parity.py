@@ -71,6 +71,17 @@ def test_draft_parity_small(B, orc, name, over, T, flags):
     tally.check()
 
 
+def test_draft_path_choice_resident_limit(B):
+    """The tensor-core draft runs every position in one launch whose CTAs are
+    resident together (one per SM per 128 requests): above that many requests
+    the draft takes the CUDA-core kernels instead of failing to launch."""
+    import torch
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    bf = B.DSPARK_BF16
+    assert B.dspark_markov_draft_uses_tensor_cores(bf, bf, 128 * n_sm, 151936, 512)
+    assert not B.dspark_markov_draft_uses_tensor_cores(bf, bf, 128 * n_sm + 1, 151936, 512)
+
+
 @pytest.mark.parametrize("R,rank,T", [(128, 64, 0.7), (256, 128, 1.0), (100, 64, 0.0)])
 def test_draft_multi_tile_elementwise(B, orc, R, rank, T):
     """Full vocabulary with every request row of the tile active: each CTA walks
