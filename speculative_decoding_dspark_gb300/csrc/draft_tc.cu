@@ -45,6 +45,12 @@
 //     pass it take the log (a short series in 1 - u near u = 1, the
 //     special-function log2 elsewhere; relative error about 2e-6) and the
 //     comparison.
+//   The residual launch differs: its epilogue also needs each request's own
+//     target row and U row (128 scattered rows), so A lives in tensor memory
+//     (columns 256-511, written with tcgen05.st) and the shared memory it frees
+//     holds six staging buffers, each one 32-column pass of those rows, filled
+//     by the epilogue threads' own cp.async copies four passes ahead; the
+//     epilogue works in four 32-column passes per tile, 8 columns per thread.
 //
 // Cross-CTA results need no merging pass: every CTA folds its winner into one
 // 64-bit key per request and step with atomicMax (order-preserving bits of
@@ -64,6 +70,7 @@
 // rows).  Every mbarrier wait and the grid barrier are bounded (2 s); a timeout
 // aborts every CTA cleanly and reports DSPARK_ERR_TIMEOUT.
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include "draft_tc.cuh"
 #include "tc_ptx.cuh"
@@ -157,6 +164,13 @@ struct ResShared {
     int urow[kM];
 };
 constexpr size_t kShareBytes = sizeof(ResShared);
+// Draft-only shared memory after the barriers: per request row, the best race
+// record of each epilogue quarter as G = log2(w / E) in absolute base-2 units
+// (the record's scaled logit minus log2 E), rounded down to half precision: a
+// smaller G is a looser bound, so still a valid one; -inf when none yet.
+struct DraftShared {
+    __half g[kM][4];
+};
 
 __device__ __forceinline__ void merge_draft(float& sc, int& ix, float& sa, float& m, float& su, float sc2, int ix2,
                                             float sa2, float m2, float su2) {
@@ -243,6 +257,20 @@ __device__ __forceinline__ float neg_log_uniform(uint32_t x) {
     return d < 0.0625f ? series : -l2 * kLn2F;
 }
 
+// a[c] for a register array and a lane-varying c in [0, 16): a tree of
+// selects on the bits of c (register arrays cannot be indexed at run time
+// without a trip through local memory)
+template <typename T>
+__device__ __forceinline__ T pick16(const T (&a)[16], int c) {
+    T l1[8], l2[4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) l1[i] = (c & 1) ? a[2 * i + 1] : a[2 * i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) l2[i] = (c & 2) ? l1[2 * i + 1] : l1[2 * i];
+    const T l3a = (c & 4) ? l2[1] : l2[0], l3b = (c & 4) ? l2[3] : l2[2];
+    return (c & 8) ? l3b : l3a;
+}
+
 __device__ __forceinline__ uint32_t word_of(const uint4& x, int j) {
     return j == 0 ? x.x : (j == 1 ? x.y : (j == 2 ? x.z : x.w));
 }
@@ -310,6 +338,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
     uint8_t* sB = sU + (kRes ? kResBufs * (kResTBytes + kResUBytes) : 2 * kUBufBytes);
     Bars& bar = *reinterpret_cast<Bars*>(sB + p.n_stages * kTileBytes);
     ResShared& rsh = *reinterpret_cast<ResShared*>(&bar + 1);  // residual only
+    DraftShared& dsh = *reinterpret_cast<DraftShared*>(&bar + 1);  // draft only
     float* g_share = &rsh.g_share[0][0];
     // the quarters' exchange at the end of a step ([3][kM]): draft, the A rows'
     // space (the step's MMAs have completed and the next step's rows are not
@@ -493,6 +522,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         const int cpr = p.rank >> 3;  // 16-byte pieces of a W1 row (at most 64)
 
         for (int k = 0; k < n_steps; ++k) {
+            // no race record of this step yet (the previous step's readers are past
+            // the barriers at its end; this step's read after the one below)
+            if (!kRes) *reinterpret_cast<volatile unsigned short*>(&dsh.g[m][quarter]) = 0xFC00u;
             // ---- the step's A rows: tokens (the anchor at k = 0, else the previous
             // step's winner, decoded from its key; residual: the rejected
             // position's predecessor), then W1 rows: draft, into the 128-byte-
@@ -720,6 +752,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                             for (int q = 0; q < 4; ++q)
                                 x[q] = make_uint4((uint32_t)((v0 >> 2) + q), (uint32_t)pos, (uint32_t)rr, w3);
                             philox4x32_10_x4(x, key0, key1);
+                            bool rec = false;  // this thread's record moved: publish it
                             if (part.m == -INFINITY) {
                                 // the step's first values: their largest is the reference and
                                 // seeds the race (a real entry, so the winner is unchanged; it
@@ -737,12 +770,27 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                                     bE = neg_log_uniform(wb);
                                     part.idx = v0 + cb;
                                     part.s_at = sb * c2;
+                                    rec = true;
                                 } else {
                                     part.m = -INFINITY;  // nothing finite yet
                                 }
                             }
                             if (part.m != -INFINITY) {                     // else nothing finite yet
-                                rho = race_bound(bE, bw);
+                                // rho bounds E / w of the row's winner in this thread's units
+                                // (w = 2^(s c2 - m)): this thread's record, or the best
+                                // record G of the row's four quarters, E / w = 2^(m - G)
+                                float gq;
+                                {
+                                    const unsigned long long raw =
+                                        *reinterpret_cast<const volatile unsigned long long*>(&dsh.g[m][0]);
+                                    const __half2 g01 = __halves2half2(__ushort_as_half((unsigned short)raw),
+                                                                       __ushort_as_half((unsigned short)(raw >> 16)));
+                                    const __half2 g23 = __halves2half2(__ushort_as_half((unsigned short)(raw >> 32)),
+                                                                       __ushort_as_half((unsigned short)(raw >> 48)));
+                                    const __half2 gm = __hmax2(g01, g23);
+                                    gq = fmaxf(__low2float(gm), __high2float(gm));
+                                }
+                                rho = fminf(race_bound(bE, bw), ex2(part.m - gq) * kRaceSlack);
                                 // every weight into the normaliser; entries that may beat the
                                 // running winner marked for the exact test
                                 float ps;
@@ -769,26 +817,36 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                                         part.sum *= sc;
                                         bw *= sc;
                                         part.m = cm;
-                                        rho = race_bound(bE, bw);
+                                        rho = fminf(race_bound(bE, bw), ex2(part.m - gq) * kRaceSlack);
                                         weigh();
                                     }
                                 }
                                 part.sum += ps;
+                                // this lane's candidates one at a time, lowest column first
+                                // (the warp runs as many rounds as its busiest lane needs,
+                                // instead of one branch per column any lane marked)
                                 if (cand) {
                                     const float nm = -part.m;
+                                    uint32_t words[16];
 #pragma unroll
-                                    for (int c = 0; c < 16; ++c) {
-                                        if (cand & (1u << c)) {
-                                            const float w = ex2(fmaf(sv[c], c2, nm));
-                                            const float E = neg_log_uniform(word_of(x[c >> 2], c & 3));
-                                            if (w * bE > bw * E) {
-                                                bw = w; bE = E; part.idx = v0 + c; part.s_at = sv[c] * c2;
-                                                rho = race_bound(bE, bw);
-                                            }
+                                    for (int c = 0; c < 16; ++c) words[c] = word_of(x[c >> 2], c & 3);
+                                    do {
+                                        const int c = __ffs(cand) - 1;
+                                        cand &= cand - 1u;
+                                        const float sc = pick16(sv, c);
+                                        const float w = ex2(fmaf(sc, c2, nm));
+                                        const float E = neg_log_uniform(pick16(words, c));
+                                        if (w * bE > bw * E) {
+                                            bw = w; bE = E; part.idx = v0 + c; part.s_at = sc * c2;
+                                            rho = fminf(rho, race_bound(bE, bw));
+                                            rec = true;
                                         }
-                                    }
+                                    } while (cand);
                                 }
                             }
+                            if (rec)
+                                *reinterpret_cast<volatile unsigned short*>(&dsh.g[m][quarter]) =
+                                    __half_as_ushort(__float2half_rd(part.s_at - lg2(bE)));
                         }
                     }
                 }
@@ -1145,7 +1203,7 @@ int prepare(EncodeTiled enc, const void* U, const void* W1, const void* W2, int 
     const size_t fixed =
         1024 + sizeof(Bars) +
         (residual ? kShareBytes + (size_t)kResBufs * (kResTBytes + kResUBytes)
-                  : (size_t)nkb * kTileBytes + 2 * (size_t)kUBufBytes);
+                  : sizeof(DraftShared) + (size_t)nkb * kTileBytes + 2 * (size_t)kUBufBytes);
     // the end-of-step exchange of the epilogue quarters reuses the A rows' space
     // (draft) or the drained W2 ring (residual, at least two stages)
     if (!residual && (size_t)nkb * kTileBytes < 3 * kM * sizeof(TcPartial)) return DSPARK_ERR_UNSUPPORTED;
