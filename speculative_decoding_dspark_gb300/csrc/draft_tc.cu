@@ -403,7 +403,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                     tc::tma_prefetch_l2_3d(&tm_u, tn * kNV + kKB, g / n_local, row0);
                 }
             };
-            for (int g = 0; g < 2 && g < n_tl; ++g) prefetch_tile(g);
+            // prefetched up to (not including) global tile pf_next: one tile ahead,
+            // and two at a step's first tile, so that HBM keeps streaming the
+            // step's next tiles while the grid waits between steps
+            int pf_next = 0;
+            for (; pf_next < 2 && pf_next < n_tl; ++pf_next) prefetch_tile(pf_next);
             const int n_loads = n_tl * p.nkb;  // W2 stage loads
             int issued = 0;
             bool ok = true;
@@ -416,8 +420,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                 const int t = cidx + (g % n_local) * p.P;
                 tc::mbar_arrive_expect_tx(&bar.full[s], kTileBytes);
                 tc::tma_load_2d(sB + s * kTileBytes, &tm_w2, &bar.full[s], kb * kKB, t * kNV);
-                // once a tile's first ring of loads is out, pull the next tile into L2
-                if (kb == min(S, p.nkb) - 1 && g + 1 < n_tl) prefetch_tile(g + 1);
+                // once a tile's first ring of loads is out, pull the next tile(s) into L2
+                if (kb == min(S, p.nkb) - 1) {
+                    const int horizon = min(n_tl - 1, g + (g % n_local == 0 ? 2 : 1));
+                    for (; pf_next <= horizon; ++pf_next) prefetch_tile(pf_next);
+                }
             }
             // the copies this thread issued must land before the CTA exits
             if (!ok) {
