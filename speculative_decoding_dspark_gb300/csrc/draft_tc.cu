@@ -257,18 +257,18 @@ __device__ __forceinline__ float neg_log_uniform(uint32_t x) {
     return d < 0.0625f ? series : -l2 * kLn2F;
 }
 
-// a[c] for a register array and a lane-varying c in [0, 16): a tree of
-// selects on the bits of c (register arrays cannot be indexed at run time
-// without a trip through local memory)
-template <typename T>
-__device__ __forceinline__ T pick16(const T (&a)[16], int c) {
-    T l1[8], l2[4];
+// a[c] for a register array of N (a power of two) and a lane-varying c in
+// [0, N): a tree of selects on the bits of c, lowest bit first (register
+// arrays cannot be indexed at run time without a trip through local memory)
+template <int N, typename T>
+__device__ __forceinline__ T pick(const T (&a)[N], int c) {
+    T l[N / 2];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) l1[i] = (c & 1) ? a[2 * i + 1] : a[2 * i];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) l2[i] = (c & 2) ? l1[2 * i + 1] : l1[2 * i];
-    const T l3a = (c & 4) ? l2[1] : l2[0], l3b = (c & 4) ? l2[3] : l2[2];
-    return (c & 8) ? l3b : l3a;
+    for (int i = 0; i < N / 2; ++i) l[i] = (c & 1) ? a[2 * i + 1] : a[2 * i];
+    if constexpr (N == 2)
+        return l[0];
+    else
+        return pick<N / 2>(l, c >> 1);
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4& x, int j) {
@@ -840,9 +840,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                                     do {
                                         const int c = __ffs(cand) - 1;
                                         cand &= cand - 1u;
-                                        const float sc = pick16(sv, c);
+                                        const float sc = pick<16>(sv, c);
                                         const float w = ex2(fmaf(sc, c2, nm));
-                                        const float E = neg_log_uniform(pick16(words, c));
+                                        const float E = neg_log_uniform(pick<16>(words, c));
                                         if (w * bE > bw * E) {
                                             bw = w; bE = E; part.idx = v0 + c; part.s_at = sc * c2;
                                             rho = fminf(rho, race_bound(bE, bw));
@@ -937,18 +937,20 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                                 : 0u;
                 }
                 if (cand) {
+                    // this lane's candidates one at a time, lowest column first
                     bool rec = false;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        if (cand & (1u << c)) {
-                            const float E = neg_log_uniform(word_of(x[c >> 2], c & 3));
-                            if (wv[c] * bE > bw * E) {
-                                bw = wv[c]; bE = E; part.idx = v0 + c;
-                                rho = fminf(rho, race_bound(bE, bw));
-                                rec = true;
-                            }
+                    const uint32_t words[8] = {x[0].x, x[0].y, x[0].z, x[0].w, x[1].x, x[1].y, x[1].z, x[1].w};
+                    do {
+                        const int c = __ffs(cand) - 1;
+                        cand &= cand - 1u;
+                        const float w = pick<8>(wv, c);
+                        const float E = neg_log_uniform(pick<8>(words, c));
+                        if (w * bE > bw * E) {
+                            bw = w; bE = E; part.idx = v0 + c;
+                            rho = fminf(rho, race_bound(bE, bw));
+                            rec = true;
                         }
-                    }
+                    } while (cand);
                     if (rec) {
                         g_own = lg2(bw) - lg2(bE);
                         gsh[quarter * kM] = g_own;
