@@ -27,7 +27,8 @@
 //     previous step's winner keys) and resident for the step;
 //   B (N = 128 vocabulary rows x K = rank) = W2 tiles streamed by TMA through a
 //     ring of 16 KB stages; the next tile's boxes are prefetched into L2 one
-//     tile ahead so the ring only has to cover L2 latency;
+//     tile ahead (two at a step's first tile, while the grid waits between
+//     steps) so the ring only has to cover L2 latency;
 //   D = A . B^T in fp32 tensor memory, two 128-column buffers so the epilogue
 //     of one vocabulary tile overlaps the MMAs of the next;
 //   U_k (draft) = the tile's base logits, by TMA into two 16 KB pass buffers
@@ -44,7 +45,9 @@
 //     (1 - u comes exactly from the random bits), and only the entries that
 //     pass it take the log (a short series in 1 - u near u = 1, the
 //     special-function log2 elsewhere; relative error about 2e-6) and the
-//     comparison.
+//     comparison, one candidate per lane at a time.  The four threads racing
+//     over a request row in a CTA (one per quarter) share their best records
+//     through shared memory, so each test uses the strongest of the four.
 //   The residual launch differs: its epilogue also needs each request's own
 //     target row and U row (128 scattered rows), so A lives in tensor memory
 //     (columns 256-511, written with tcgen05.st) and the shared memory it frees
