@@ -114,6 +114,31 @@ def test_draft_tiny_many_cycles(B, orc):
         tally.check()
 
 
+def test_draft_extreme_logit_scale(B, orc):
+    """Logits far outside the usual range on the tensor-core draft: with
+    u_sigma = 60 and T = 0.02 or 0.001 the base-2 scaled logits reach about 1.7e4
+    and 3.5e5, so the weights of later passes sum past 2^32 (the race's reference
+    moves) and at T = 0.001 the race records shared between a row's four threads
+    saturate their half-precision slot (a looser bound, still a bound).  The
+    tokens must match the oracle exactly (the draws are all but deterministic at
+    this scale) and the log-normalisers to fp32 relative precision; q(y) is not
+    compared here, since exp of the difference of two fp32 values near 1e5
+    carries an absolute error of about 1e-2."""
+    w, d = H.cycle_inputs("batched_sampling", R=6, V=17416, gamma=4, rank=64, w_sigma=0.2, u_sigma=60.0)
+    assert B.dspark_markov_draft_uses_tensor_cores(B.DSPARK_BF16, B.DSPARK_BF16, 6, 17416, 64)
+    for T in (0.02, 0.001):
+        tally = H.Tally()
+        for cycle in range(2):
+            g = H.gpu_draft(d, T, cycle, want_logits=False)
+            o = orc.markov_draft(d["U"], d["W1"], d["W2"], d["anchor"], d["seeds"], cycle, T,
+                                 want_logits=False)
+            assert g["status"] == 0
+            clean = H.compare_draft(tally, g, o, 0.0)  # tokens only
+            for r in clean:
+                np.testing.assert_allclose(g["q_lse"][r], o["q_lse"][r], rtol=1e-5)
+        tally.check()
+
+
 # ------------------------------------------------------------------ verify
 def _oracle_draft_as_inputs(o):
     return (o["y"].astype(np.int32), o["q_logits"].astype(np.float32),
