@@ -38,7 +38,8 @@ DraftSimtLayout draft_simt_layout(int R, int V) {
 struct VerifyLayout {
     size_t ok, valid, cnt1, cnt2, act, lazy, stats, jobs, parts, total;
 };
-VerifyLayout verify_layout(int R, int V, int max_rows) {
+// (The rows are streamed lazily, so the scratch does not grow with max_rows.)
+VerifyLayout verify_layout(int R, int V) {
     VerifyLayout L;
     const int nchunk = (V + kVerifyChunk - 1) / kVerifyChunk;
     size_t off = 0;
@@ -103,10 +104,10 @@ size_t dspark_workspace_size(int op, int R, int gamma, int V, int rank, int max_
             return draft_simt_layout(R, V).total;
         case DSPARK_OP_VERIFY:
             if (V <= 0 || max_rows < 0) return 0;
-            return verify_layout(R, V, max_rows).total;
+            return verify_layout(R, V).total;
         case DSPARK_OP_VERIFY_MARKOV:
             if (V <= 0 || max_rows < 0 || rank <= 0) return 0;
-            return align_up(verify_layout(R, V, max_rows).total) + residual_tc_workspace(R, rank);
+            return align_up(verify_layout(R, V).total) + residual_tc_workspace(R, rank);
         case DSPARK_OP_SELECT:
             return 0;
         default:
@@ -174,7 +175,7 @@ int dspark_verify(const float* target_logits, const int32_t* cu_seqlens,
     const bool greedy = temperature == 0.0f;
     if (!greedy && (!q_logits || !q_lse || !q_tok || !seeds)) return DSPARK_ERR_INVALID_ARG;
     if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return DSPARK_ERR_WORKSPACE;
-    const VerifyLayout L = verify_layout(R, V, max_rows);
+    const VerifyLayout L = verify_layout(R, V);
     if (ws_bytes < L.total) return DSPARK_ERR_WORKSPACE;
     const int nchunk = (V + kVerifyChunk - 1) / kVerifyChunk;
     if ((long long)max_rows * ((V + kStatChunk - 1) / kStatChunk) >= (1LL << 31) ||
@@ -220,7 +221,7 @@ int dspark_verify_markov(const float* target_logits, const int32_t* cu_seqlens,
     if (!greedy && (!aligned16(U) || !aligned16(W1) || !aligned16(W2) || !aligned16(target_logits)))
         return DSPARK_ERR_UNSUPPORTED;
     if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return DSPARK_ERR_WORKSPACE;
-    const VerifyLayout L = verify_layout(R, V, max_rows);
+    const VerifyLayout L = verify_layout(R, V);
     const size_t res_off = align_up(L.total);
     if (ws_bytes < res_off + residual_tc_workspace(R, rank)) return DSPARK_ERR_WORKSPACE;
     const int nchunk = (V + kVerifyChunk - 1) / kVerifyChunk;
