@@ -60,6 +60,24 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x, world, device="cuda"):
+    """The largest x over the ranks of the job (its slowest replica's time);
+    x itself when the job has one rank."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, ms):
+    """Units per second of the whole job: every rank processed units_per_rank
+    in at most ms milliseconds."""
+    return world * units_per_rank / (ms / 1000.0)
+
+
 def workload_config(w):
     return {"workload": w["name"], "R": w["R"], "V": w["V"], "gamma": w["gamma"],
             "rank": w["rank"], "temperature": float(w["temperature"]),
@@ -298,15 +316,11 @@ def run_ours(args):
     clk = clocks.stop()
     if world > 1:
         dist.barrier()
-    ms = start.elapsed_time(stop)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(stop), world)
     per = {k: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
            for j, k in enumerate(["select", "draft", "verify", "commit"])}
     ms_step = ms / args.steps
-    value = world * args.steps / (ms / 1000.0)
+    value = whole_job_rate(args.steps, world, ms)
 
     # roofline of the dominant kernel.  Algorithmic bytes of one Markov draft
     # step (one vocabulary pass): W2 once, U_k once, q_logits if written.  The
@@ -402,12 +416,8 @@ def run_ours(args):
         e2e_run(n_e2e, 100, s0)
         s1.record(stream)
         torch.cuda.synchronize()
-        e_ms = s0.elapsed_time(s1)
-        if world > 1:
-            t = torch.tensor([e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * n_e2e / (e_ms / 1000.0), "unit": UNIT,
+        e_ms = max_over_ranks(s0.elapsed_time(s1), world)
+        e2e = {"value": whole_job_rate(n_e2e, world, e_ms), "unit": UNIT,
                "h2d_gb_s": bi * n_e2e / (e_ms / 1000.0) / 1e9, "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo, "steps": n_e2e}
 
