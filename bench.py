@@ -78,10 +78,23 @@ def whole_job_rate(units_per_rank, world, ms):
     return world * units_per_rank / (ms / 1000.0)
 
 
+L2_BYTES = 129 * 2**20  # GB300 L2
+
+
+def input_bytes(w):
+    """Input bytes of one cycle: W2 once per draft position, U, and the presented
+    target rows (fp32; verify reads them only up to each first rejection)."""
+    R, V, gamma, rank = w["R"], w["V"], w["gamma"], w["rank"]
+    return gamma * V * rank * 2 + R * gamma * V * 2 + R * (gamma + 1) * V * 4
+
+
 def workload_config(w):
+    nb = input_bytes(w)
+    l2 = (f"inputs larger than L2 (no flush): W2 per draft position, U and the presented target "
+          f"logits total ~{nb / 1e9:.2f} GB per step"
+          if nb > L2_BYTES else f"inputs ({nb / 1e6:.1f} MB per step) fit in L2: not a bench workload")
     return {"workload": w["name"], "R": w["R"], "V": w["V"], "gamma": w["gamma"],
-            "rank": w["rank"], "temperature": float(w["temperature"]),
-            "l2": "inputs larger than L2 (no flush): W2, U and target logits stream ~2 GB per step"}
+            "rank": w["rank"], "temperature": float(w["temperature"]), "l2": l2}
 
 
 # ---------------------------------------------------------------- CPU oracle
