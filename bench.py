@@ -10,15 +10,27 @@ lengths, on seeded synthetic inputs already resident in HBM.
 Prints one JSON line.  For N > 1 it runs under torch.distributed.run, one
 rank per GPU; every rank runs its own replica of the workload (requests are
 independent, no collective is needed), the time is the max over ranks and
-`value` counts the cycles of all ranks.  `--impl reference` times the CPU
-oracle (single-threaded C++) on a bounded sample of the same workload.
+`value` counts the cycles of all ranks.
+
+Timing: after W warm-up steps, blocks of exactly K steps are timed with CUDA
+events on the launching stream, one block after another until about a second
+has passed; `value` comes from the median block.  The line also carries the
+other workloads of the pages (`workloads`: the DeepSeek-style R=512, gamma=5,
+rank-512 confidence-scheduled cycle with its tensor-core fraction, the
+variable-length verify timed alone, the greedy Qwen3-8B-shaped cycle).
+
+`--impl reference` times the CPU oracle (single-threaded C++, one request per
+task) over a pool of host processes, one per core: each timed step is one
+whole cycle of every request of the workload.
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
 import json
+import multiprocessing as mp
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -35,9 +47,11 @@ from speculative_decoding_dspark_gb300 import inputs  # noqa: E402
 METRIC = "draft+verify cycles/s"
 UNIT = "cycles/s"
 DEFAULT_WORKLOAD = "batched_sampling"
+BLOCK_SECONDS = 1.0  # timed blocks of K steps are repeated until this much time has passed
+SIDE_SECONDS = 0.3   # the same for each side workload
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
@@ -50,7 +64,11 @@ def parse():
     ap.add_argument("--gamma", type=int, default=None, help="override the workload's block size")
     ap.add_argument("--temperature", type=float, default=None, help="override the workload's T")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--no-side-workloads", action="store_true",
+                    help="skip the other workloads (profiling runs)")
+    ap.add_argument("--blocks", type=int, default=None,
+                    help="timed blocks of K steps (default: repeat for about a second)")
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -88,33 +106,85 @@ def input_bytes(w):
     return gamma * V * rank * 2 + R * gamma * V * 2 + R * (gamma + 1) * V * 4
 
 
-def workload_config(w):
+def workload_config(w, world=1):
+    """The `config` object; both arms print the same one."""
     nb = input_bytes(w)
     l2 = (f"inputs larger than L2 (no flush): W2 per draft position, U and the presented target "
           f"logits total ~{nb / 1e9:.2f} GB per step"
           if nb > L2_BYTES else f"inputs ({nb / 1e6:.1f} MB per step) fit in L2: not a bench workload")
     return {"workload": w["name"], "R": w["R"], "V": w["V"], "gamma": w["gamma"],
-            "rank": w["rank"], "temperature": float(w["temperature"]), "l2": l2}
+            "rank": w["rank"], "temperature": float(w["temperature"]), "l2": l2,
+            "parallelism": f"replicas x{world}"}
+
+
+def host_cpu():
+    """CPU model and the number of cores this process may use."""
+    model = platform.processor() or platform.machine()
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        n = len(os.sched_getaffinity(0))
+    except AttributeError:
+        n = os.cpu_count() or 1
+    return model, n
 
 
 # ---------------------------------------------------------------- CPU oracle
-def oracle_sample(w, d, full, n_req, cycle):
-    """Time the oracle on n_req requests of the workload (draft all gamma
-    positions + verify); returns (seconds per request, sample text)."""
+# The oracle is single-threaded; the requests of a cycle are independent (their
+# draws are addressed by request index), so a pool of worker processes, one per
+# host core, each replays whole requests.  The pool is forked before this
+# process makes any CUDA call, after the inputs exist, so the workers share the
+# input arrays instead of copying them.
+_ORC = {}
+
+
+def _oracle_request(job):
+    """Draft all gamma positions and verify one request on the oracle; returns
+    its number of accepted drafts."""
+    r, cycle = job
     import oracle
-    oracle.build()
-    R, gamma = w["R"], w["gamma"]
-    T = float(w["temperature"])
-    rows = list(np.linspace(0, R - 1, n_req).astype(int))
-    l = np.full(len(rows), gamma, np.int32)
-    t0 = time.perf_counter()
+    w, d, full = _ORC["w"], _ORC["d"], _ORC["full"]
+    gamma, T = w["gamma"], float(w["temperature"])
+    rows = [r]
+    l = np.full(1, gamma, np.int32)
     o = oracle.markov_draft(d["U"][rows], d["W1"], d["W2"], d["anchor"][rows], d["seeds"][rows],
                             cycle, T, req_ids=rows)
-    oracle.verify(inputs.pack_rows(full[rows], l), inputs.cu_from_lengths(l), o["y"], o["q_logits"],
-                  d["seeds"][rows], cycle, T, req_ids=rows)
-    oracle.commit_lengths(np.zeros(len(rows), np.int32), l, gamma)
-    dt = time.perf_counter() - t0
-    return dt / len(rows), f"{len(rows)} of {R} requests, whole cycle each (draft {gamma} positions + verify), scaled x{R}"
+    v = oracle.verify(inputs.pack_rows(full[rows], l), inputs.cu_from_lengths(l), o["y"], o["q_logits"],
+                      d["seeds"][rows], cycle, T, req_ids=rows)
+    return int(v["n_acc"][0])
+
+
+class OraclePool:
+    """Worker processes for the CPU oracle (fork: create it before any CUDA call)."""
+
+    def __init__(self, w, d, full, n_proc):
+        import oracle
+        oracle.build()
+        _ORC.update(w=w, d=d, full=full)
+        self.n = max(1, min(n_proc, w["R"]))
+        self.pool = mp.get_context("fork").Pool(self.n)
+        self.w = w
+
+    def cycle(self, cycle, requests=None):
+        """One cycle of the given requests (default: all), with the whole-batch
+        steps (commit lengths) in this process; returns the seconds it took."""
+        import oracle
+        R, gamma = self.w["R"], self.w["gamma"]
+        reqs = list(range(R)) if requests is None else list(requests)
+        t0 = time.perf_counter()
+        n_acc = self.pool.map(_oracle_request, [(r, cycle) for r in reqs], chunksize=1)
+        oracle.commit_lengths(np.asarray(n_acc, np.int32), np.full(len(reqs), gamma, np.int32), gamma)
+        return time.perf_counter() - t0
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
 
 
 def run_reference(args):
@@ -124,19 +194,26 @@ def run_reference(args):
     w = inputs.workload(args.workload)
     d = inputs.draft_inputs(w)
     full = inputs.target_full(w, d["U"])
-    per_req = []
-    sample = ""
-    for step in range(args.warmup + args.steps):
-        s, sample = oracle_sample(w, d, full, 1, step)
-        if step >= args.warmup:
-            per_req.append(s)
-    cyc_s = 1.0 / (statistics.mean(per_req) * w["R"])
+    model, ncpu = host_cpu()
+    pool = OraclePool(w, d, full, ncpu)
+    R = w["R"]
+    try:
+        # warm-up steps: one request per worker (untimed); timed steps: whole cycles
+        for step in range(args.warmup):
+            pool.cycle(step, [(step * pool.n + i) % R for i in range(pool.n)])
+        secs = [pool.cycle(args.warmup + step) for step in range(args.steps)]
+    finally:
+        pool.close()
+    ms_step = 1000.0 * statistics.mean(secs)
+    cyc_s = 1000.0 / ms_step
+    sample = (f"each timed step: one whole cycle of all {R} requests (draft {w['gamma']} positions + "
+              f"verify + commit), requests spread over {pool.n} worker processes")
     line = {"metric": METRIC, "value": cyc_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": 1000.0 / cyc_s, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(w), "impl": "reference",
-            "cpu_baseline": {"value": cyc_s, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": "each step: " + sample.replace("1 of", "1 request of")},
+            "config": workload_config(w, world), "impl": "reference",
+            "cpu_baseline": {"value": cyc_s, "unit": UNIT, "cores": pool.n, "kind": "oracle",
+                             "sample": sample, "cpu_model": model, "nproc": ncpu},
             "e2e": {"value": cyc_s, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -153,7 +230,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
@@ -209,267 +286,443 @@ def traffic_from_profile(kernel, digest):
     return None
 
 
+def load_peaks():
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    return json.load(open(pk)) if os.path.exists(pk) else {}
+
+
+class Cycle:
+    """Device tensors and the launch sequence of one workload's decode cycle."""
+
+    def __init__(self, w, host, stage="cycle"):
+        import torch
+        from speculative_decoding_dspark_gb300 import binding as B
+        self.B, self.torch, self.w, self.stage = B, torch, w, stage
+        d, full, ci = host["d"], host["full"], host["ci"]
+        R, V, gamma, rank = w["R"], w["V"], w["gamma"], w["rank"]
+        self.R, self.V, self.gamma, self.rank = R, V, gamma, rank
+        self.T = float(w["temperature"])
+        if w.get("confidence"):
+            self.K_cap, self.mode = ci["K_cap"], B.DSPARK_SELECT_HISTORY
+        else:  # fixed-length workloads: the capacity admits every draft position
+            self.K_cap, self.mode = R * (gamma + 1), B.DSPARK_SELECT_FIXED
+        self.max_rows = min(self.K_cap, R * (gamma + 1))
+        self.varlen = bool(w.get("varlen"))
+
+        def dev(x):
+            x = np.ascontiguousarray(x)
+            if x.dtype == np.uint16:
+                return torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+            if x.dtype == np.uint64:
+                return torch.from_numpy(x.view(np.int64)).cuda()
+            return torch.from_numpy(x).cuda()
+
+        self.U, self.W1, self.W2 = dev(d["U"]), dev(d["W1"]), dev(d["W2"])
+        self.anchor, self.seeds = dev(d["anchor"]), dev(d["seeds"])
+        self.c, self.c_hist = dev(ci["c"]), dev(ci["c_hist"])
+        self.sizes, self.sps = dev(ci["capture_sizes"]), dev(ci["sps"])
+        i32 = dict(dtype=torch.int32, device="cuda")
+        if self.varlen:
+            # variable verify lengths drawn by the workload: packed rows and fixed
+            # cu_seqlens (no selection step)
+            l = inputs.verify_lengths(w)
+            self.target = dev(inputs.pack_rows(full, l))
+            self.l = dev(l)
+            self.cu = dev(inputs.cu_from_lengths(l))
+            self.max_rows = int(self.target.shape[0])
+        else:
+            # target rows in full [R, gamma+1, V]; with every position selected the
+            # packed layout equals it, otherwise the first max_rows rows are read
+            self.target = dev(full.reshape(R * (gamma + 1), V))
+            self.l = torch.empty(R, **i32)
+            self.cu = torch.empty(R + 1, **i32)
+        self.y = torch.empty((R, gamma), **i32)
+        self.q_lse = torch.empty((R, gamma), device="cuda")
+        self.q_tok = torch.empty((R, gamma), device="cuda")
+        self.a = torch.empty((R, gamma), device="cuda")
+        self.K_used = torch.empty(1, **i32)
+        self.n_acc = torch.empty(R, **i32)
+        self.out = torch.empty((R, gamma + 1), **i32)
+        self.p_tok = torch.empty((R, gamma), device="cuda")
+        self.cl = torch.empty(R, **i32)
+        self.cuc = torch.empty(R + 1, **i32)
+        self.disc = torch.empty(R, **i32)
+        self.tot = torch.empty(1, **i32)
+        self.status = torch.zeros(1, **i32)
+        self.ws_d = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_DRAFT, R, gamma, V, rank, 0,
+                                                        B.DSPARK_BF16))
+        self.ws_v = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_VERIFY_MARKOV, R, gamma, V, rank,
+                                                        self.max_rows))
+        self.stream = torch.cuda.current_stream()
+        self.uses_tc = B.dspark_markov_draft_uses_tensor_cores(B.DSPARK_BF16, B.DSPARK_BF16, R, V, rank)
+        self.run_select = stage == "cycle" and not self.varlen
+        self.run_commit = stage == "cycle"
+        self.run_draft = stage in ("cycle", "draft")
+        self.run_verify = stage in ("cycle", "verify")
+        if not self.run_draft or not self.run_select:  # lengths and a draft exist once
+            if not self.varlen:
+                self._select()
+            if not self.run_draft:
+                self._draft(0, self.U, self.anchor, self.seeds)
+        # launches of this library per step: tensor cores, every position and the
+        # finalize in one launch; CUDA cores, counter reset then bias and sample
+        # kernels per position.  Verify: prologue, rounds (residual draw, finalize).
+        draft_launches = 1 if self.uses_tc else 1 + 2 * gamma
+        verify_launches = 4 if self.T > 0 else 2
+        self.launches_per_step = (int(self.run_select) + draft_launches * int(self.run_draft) +
+                                  verify_launches * int(self.run_verify) + int(self.run_commit))
+
+    def _select(self, c=None, ch=None):
+        self.B.dspark_select_prefix(self.c if c is None else c, self.c_hist if ch is None else ch, self.sizes,
+                                    self.sps, self.K_cap, self.mode, self.a, self.l, self.cu, self.K_used,
+                                    None, self.status)
+
+    def _draft(self, cycle, U, anchor, seeds):
+        self.B.dspark_markov_draft(U, self.W1, self.W2, anchor, seeds, cycle, self.T, self.y, self.q_lse,
+                                   self.q_tok, None, self.ws_d, self.status)
+
+    def step(self, cycle, ev=None, inp=None):
+        # inp: the per-cycle inputs (U, target, c, c_hist, anchor, seeds); default the resident ones
+        U_, tgt_, c_, ch_, anc_, sd_ = inp if inp is not None else (self.U, self.target, self.c, self.c_hist,
+                                                                    self.anchor, self.seeds)
+        s = self.stream
+        if ev is not None: ev[0].record(s)
+        if self.run_select:
+            self._select(c_, ch_)
+        if ev is not None: ev[1].record(s)
+        if self.run_draft:
+            self._draft(cycle, U_, anc_, sd_)
+        if ev is not None: ev[2].record(s)
+        if self.run_verify:
+            self.B.dspark_verify_markov(tgt_, self.cu, self.y, U_, self.W1, self.W2, anc_, self.q_lse, self.q_tok,
+                                        sd_, cycle, self.T, self.max_rows, self.n_acc, self.out, self.p_tok,
+                                        self.ws_v, self.status)
+        if ev is not None: ev[3].record(s)
+        if self.run_commit:
+            self.B.dspark_commit_lengths(self.n_acc, self.l, self.gamma, self.cl, self.cuc, self.disc, self.tot,
+                                         self.status)
+        if ev is not None: ev[4].record(s)
+
+    def timed_blocks(self, steps, first_cycle, seconds, n_blocks=None):
+        """Blocks of exactly `steps` steps, each bracketed by CUDA events on the
+        launching stream, repeated until `seconds` have passed (or n_blocks).
+        Returns (per-block ms, per-stage mean ms, steps run)."""
+        torch = self.torch
+        blocks, evs_all, cyc = [], [], first_cycle
+        t_end = time.perf_counter() + seconds
+        while (n_blocks is None and (not blocks or time.perf_counter() < t_end)) or \
+                (n_blocks is not None and len(blocks) < n_blocks):
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b0.record(self.stream)
+            for i in range(steps):
+                self.step(cyc, evs[i])
+                cyc += 1
+            b1.record(self.stream)
+            torch.cuda.synchronize()
+            blocks.append(b0.elapsed_time(b1))
+            evs_all.extend(evs)
+        per = {k: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs_all)
+               for j, k in enumerate(["select", "draft", "verify", "commit"])}
+        return blocks, per, cyc - first_cycle
+
+    def rows_read(self):
+        """Target rows the last verify read: up to each request's first rejection."""
+        n_h = self.n_acc.cpu().numpy().astype(np.int64)
+        l_h = self.l.cpu().numpy().astype(np.int64)
+        ok = n_h >= 0
+        return int((np.minimum(n_h[ok], l_h[ok]) + 1).sum()), int((l_h + 1).sum()), int(ok.sum())
+
+    def verify_bytes(self):
+        """Data-dependent algorithmic bytes of the last verify call: the rows read,
+        plus for T > 0 the residual draw's W2 pass and one target row and one U
+        row per request."""
+        rows, presented, n_ok = self.rows_read()
+        b = rows * self.V * 4
+        if self.T > 0:
+            b += self.V * self.rank * 2 + n_ok * self.V * (4 + 2)
+        return b, rows, presented
+
+    def draft_bytes(self):
+        """Algorithmic bytes of one draft call: W2 and U_k once per position."""
+        return self.gamma * (self.V * self.rank * 2 + self.R * self.V * 2)
+
+    def draft_flops(self):
+        return 2.0 * self.R * self.V * self.rank * self.gamma
+
+
+def host_inputs(w):
+    d = inputs.draft_inputs(w)
+    return dict(d=d, full=inputs.target_full(w, d["U"]), ci=inputs.confidence_inputs(w))
+
+
+def side_workload(name, args, peaks):
+    """One of the pages' other workloads, measured on its own: cycles/s, the
+    draft's HBM and tensor fractions, and the verify call's HBM fraction (for
+    the variable-length workload, verify timed alone)."""
+    import torch
+    w = inputs.workload(name)
+    host = host_inputs(w)
+    verify_alone = bool(w.get("varlen"))
+    cyc = Cycle(w, host, stage="verify" if verify_alone else "cycle")
+    del host
+    for i in range(args.warmup):
+        cyc.step(i)
+    torch.cuda.synchronize()
+    assert int(cyc.status.item()) == 0, f"{name}: device status {int(cyc.status.item())}"
+    blocks, per, n = cyc.timed_blocks(args.steps, args.warmup, SIDE_SECONDS)
+    ms_block = statistics.median(blocks)
+    hbm = peaks.get("hbm_gbs") or 6800.0
+    tens = peaks.get("bf16_tflops_sustained") or 1700.0
+    out = {"R": w["R"], "V": w["V"], "gamma": w["gamma"], "rank": w["rank"],
+           "temperature": float(w["temperature"]), "blocks": len(blocks), "steps_per_block": args.steps,
+           "stage_ms": per}
+    vb, rows, presented = cyc.verify_bytes()
+    v_ms = per["verify"]
+    out["verify"] = {"ms": v_ms, "algorithmic_bytes": vb, "rows_read": rows, "rows_presented": presented,
+                     "achieved_gbs": vb / (v_ms / 1e3) / 1e9, "frac_hbm": vb / (v_ms / 1e3) / 1e9 / hbm}
+    if verify_alone:
+        out["metric"] = "verify calls/s (verify timed alone)"
+        out["value"] = 1000.0 * args.steps / ms_block
+    else:
+        out["metric"] = METRIC
+        out["value"] = 1000.0 * args.steps / ms_block
+        d_ms = per["draft"]
+        fl = cyc.draft_flops()
+        out["draft"] = {"ms": d_ms, "algorithmic_bytes": cyc.draft_bytes(),
+                        "achieved_gbs": cyc.draft_bytes() / (d_ms / 1e3) / 1e9,
+                        "frac_hbm": cyc.draft_bytes() / (d_ms / 1e3) / 1e9 / hbm,
+                        "flops": fl, "achieved_tflops": fl / (d_ms / 1e3) / 1e12,
+                        "frac_tensor": fl / (d_ms / 1e3) / 1e12 / tens,
+                        "tensor_peak_tflops": tens, "tensor_peak": "bf16_tflops_sustained (measured)",
+                        "path": "tcgen05" if cyc.uses_tc else "simt"}
+        if w.get("confidence"):
+            out["K_used"] = int(cyc.K_used.item())
+    out["peak_hbm_gbs"] = hbm
+    del cyc
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
-    from speculative_decoding_dspark_gb300 import binding as B
 
     rank, world, local = dist_env()
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    torch.cuda.set_device(local)
     over = {}
     if args.gamma is not None:
         over["gamma"] = args.gamma
     if args.temperature is not None:
         over["temperature"] = args.temperature
     w = inputs.workload(args.workload, **over)
+    host = host_inputs(w)
     R, V, gamma, rank_r = w["R"], w["V"], w["gamma"], w["rank"]
     T = float(w["temperature"])
-    d = inputs.draft_inputs(w)
-    full = inputs.target_full(w, d["U"])
-    ci = inputs.confidence_inputs(w)
-    if w.get("confidence"):
-        K_cap, mode = ci["K_cap"], B.DSPARK_SELECT_HISTORY
-    else:  # fixed-length workloads: the capacity admits every draft position
-        K_cap, mode = R * (gamma + 1), B.DSPARK_SELECT_FIXED
-    max_rows = min(K_cap, R * (gamma + 1))
+    # the oracle's worker pool is forked now, before this process touches CUDA
+    pool = None
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline and args.stage == "cycle"
+    model, ncpu = host_cpu()
+    if want_cpu:
+        pool = OraclePool(w, host["d"], host["full"], ncpu)
 
-    def dev(x):
-        x = np.ascontiguousarray(x)
-        if x.dtype == np.uint16:
-            return torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
-        if x.dtype == np.uint64:
-            return torch.from_numpy(x.view(np.int64)).cuda()
-        return torch.from_numpy(x).cuda()
-
-    U, W1, W2 = dev(d["U"]), dev(d["W1"]), dev(d["W2"])
-    anchor, seeds = dev(d["anchor"]), dev(d["seeds"])
-    c, c_hist = dev(ci["c"]), dev(ci["c_hist"])
-    sizes, sps = dev(ci["capture_sizes"]), dev(ci["sps"])
-    # target rows in full [R, gamma+1, V]; with every position selected the packed
-    # layout equals it, otherwise the first max_rows rows of the buffer are read
-    target = dev(full.reshape(R * (gamma + 1), V))
-    del full
-    i32 = dict(dtype=torch.int32, device="cuda")
-    y = torch.empty((R, gamma), **i32)
-    q_lse = torch.empty((R, gamma), device="cuda")
-    q_tok = torch.empty((R, gamma), device="cuda")
-    # the verify recomputes the drafter's rejected rows from its factors, so the
-    # draft keeps no logits in memory
-    q_logits = None
-    a = torch.empty((R, gamma), device="cuda")
-    l = torch.empty(R, **i32)
-    cu = torch.empty(R + 1, **i32)
-    K_used = torch.empty(1, **i32)
-    n_acc = torch.empty(R, **i32)
-    out = torch.empty((R, gamma + 1), **i32)
-    p_tok = torch.empty((R, gamma), device="cuda")
-    cl = torch.empty(R, **i32)
-    cuc = torch.empty(R + 1, **i32)
-    disc = torch.empty(R, **i32)
-    tot = torch.empty(1, **i32)
-    status = torch.zeros(1, **i32)
-    ws_d = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_DRAFT, R, gamma, V, rank_r, 0, B.DSPARK_BF16))
-    ws_v = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_VERIFY_MARKOV, R, gamma, V, rank_r, max_rows))
-    stream = torch.cuda.current_stream()
-    uses_tc = B.dspark_markov_draft_uses_tensor_cores(B.DSPARK_BF16, B.DSPARK_BF16, R, V, rank_r)
-
-    run_select = run_commit = args.stage == "cycle"
-    run_draft = args.stage in ("cycle", "draft")
-    run_verify = args.stage in ("cycle", "verify")
-    if args.stage == "verify":  # the verify stage needs lengths and a draft once
-        B.dspark_select_prefix(c, c_hist, sizes, sps, K_cap, mode, a, l, cu, K_used, None, status)
-        B.dspark_markov_draft(U, W1, W2, anchor, seeds, 0, T, y, q_lse, q_tok, q_logits, ws_d, status)
-
-    def step(cycle, ev=None, inp=None):
-        # inp: the per-cycle inputs (U, target, c, c_hist, anchor, seeds); default the resident ones
-        U_, tgt_, c_, ch_, anc_, sd_ = inp if inp is not None else (U, target, c, c_hist, anchor, seeds)
-        if ev is not None: ev[0].record(stream)
-        if run_select:
-            B.dspark_select_prefix(c_, ch_, sizes, sps, K_cap, mode, a, l, cu, K_used, None, status)
-        if ev is not None: ev[1].record(stream)
-        if run_draft:
-            B.dspark_markov_draft(U_, W1, W2, anc_, sd_, cycle, T, y, q_lse, q_tok, q_logits, ws_d,
-                                  status)
-        if ev is not None: ev[2].record(stream)
-        if run_verify:
-            B.dspark_verify_markov(tgt_, cu, y, U_, W1, W2, anc_, q_lse, q_tok, sd_, cycle, T,
-                                   max_rows, n_acc, out, p_tok, ws_v, status)
-        if ev is not None: ev[3].record(stream)
-        if run_commit:
-            B.dspark_commit_lengths(n_acc, l, gamma, cl, cuc, disc, tot, status)
-        if ev is not None: ev[4].record(stream)
-
-    # launches of this library per step
-    # tensor cores: every position and the finalize in one launch; CUDA cores:
-    # counter reset, then bias and sample kernels per position
-    draft_launches = 1 if uses_tc else 1 + 2 * gamma
-    verify_launches = 4 if T > 0 else 2  # prologue, rounds, (residual draw, finalize)
-    launches_per_step = (int(run_select) + draft_launches * int(run_draft) +
-                         verify_launches * int(run_verify) + int(run_commit))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    cyc = Cycle(w, host, stage=args.stage)
+    stream = cyc.stream
 
     for i in range(args.warmup):
-        step(i)
+        cyc.step(i)
     torch.cuda.synchronize()
-    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    assert int(cyc.status.item()) == 0, f"device status {int(cyc.status.item())}"
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
     time.sleep(0.3)
-    start.record(stream)
-    for i in range(args.steps):
-        step(args.warmup + i, evs[i])
-    stop.record(stream)
-    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    blocks, per, n_timed = cyc.timed_blocks(args.steps, args.warmup, BLOCK_SECONDS, args.blocks)
+    wall = time.perf_counter() - t0
     clk = clocks.stop()
     if world > 1:
         dist.barrier()
-    ms = max_over_ranks(start.elapsed_time(stop), world)
-    per = {k: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
-           for j, k in enumerate(["select", "draft", "verify", "commit"])}
+    ms_block = statistics.median(blocks)
+    ms = max_over_ranks(ms_block, world)
     ms_step = ms / args.steps
     value = whole_job_rate(args.steps, world, ms)
+    if clk is not None:
+        clk["timed_region_s"] = wall
+        clk["sm_mhz_x_ms_per_step"] = clk["sm_mhz"] * ms_step
 
     # roofline of the dominant kernel.  Algorithmic bytes of one Markov draft
-    # step (one vocabulary pass): W2 once, U_k once, q_logits if written.  The
-    # tensor-core kernel runs all gamma steps in one launch, timed as the whole
-    # draft call (which adds the workspace reset, so the fraction is a lower
-    # bound); the CUDA-core path is timed per step.
-    step_bytes = V * rank_r * 2 + R * V * 2 + (R * V * 4 if q_logits is not None else 0)
-    steps_per_launch = gamma if uses_tc else 1
+    # step (one vocabulary pass): W2 once, U_k once.  The tensor-core kernel
+    # runs all gamma steps in one launch, timed as the whole draft call (which
+    # adds the workspace reset, so the fraction is a lower bound); the CUDA-core
+    # path is timed per step.
+    step_bytes = V * rank_r * 2 + R * V * 2
+    steps_per_launch = gamma if cyc.uses_tc else 1
     launch_bytes = step_bytes * steps_per_launch
     launch_ms = per["draft"] / gamma * steps_per_launch
-    peaks = {}
-    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(pk):
-        peaks = json.load(open(pk))
+    peaks = load_peaks()
     hbm = peaks.get("hbm_gbs")
     peak_src = "measured" if hbm else "fallback"
     hbm = hbm or 6800.0
     achieved = launch_bytes / (launch_ms / 1000.0) / 1e9
-    kname = "markov_tc_kernel<draft>" if uses_tc else "draft_bias_simt+draft_sample"
-    digest = source_digest(["speculative_decoding_dspark_gb300/csrc/draft_tc.cu" if uses_tc else
+    kname = "markov_tc_kernel<draft>" if cyc.uses_tc else "draft_bias_simt+draft_sample"
+    digest = source_digest(["speculative_decoding_dspark_gb300/csrc/draft_tc.cu" if cyc.uses_tc else
                             "speculative_decoding_dspark_gb300/csrc/draft_simt.cu",
                             "speculative_decoding_dspark_gb300/csrc/common.cuh"])
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
             "traffic": traffic_from_profile(kname, digest), "kernel": kname,
             "algorithmic_bytes_per_launch": launch_bytes, "steps_per_launch": steps_per_launch,
-            "launch_ms": launch_ms,
-            "peak_source": peak_src}
+            "launch_ms": launch_ms, "peak_source": peak_src}
+    tens = peaks.get("bf16_tflops_sustained") or 1700.0
+    fl = cyc.draft_flops()
+    roof["tensor"] = {"achieved_tflops": fl / (launch_ms / 1e3) / 1e12, "peak_tflops": tens,
+                      "frac": fl / (launch_ms / 1e3) / 1e12 / tens, "peak": "bf16_tflops_sustained"}
 
     # end to end through the public API from pinned host buffers
     e2e = None
     if not args.no_e2e and args.stage == "cycle":
-        hU = U.cpu().pin_memory(); htgt = target.cpu().pin_memory(); hc = c.cpu().pin_memory()
-        hch = c_hist.cpu().pin_memory(); ha = anchor.cpu().pin_memory(); hs = seeds.cpu().pin_memory()
-        h_out = torch.empty((R, gamma + 1), dtype=torch.int32).pin_memory()
-        h_n = torch.empty(R, dtype=torch.int32).pin_memory()
-        h_cl = torch.empty(R + 1, dtype=torch.int32).pin_memory()
-        bi = sum(t.numel() * t.element_size() for t in (hU, htgt, hc, hch, ha, hs))
-        bo = sum(t.numel() * t.element_size() for t in (h_out, h_n, h_cl))
+        e2e = measure_e2e(cyc, args, world)
 
-        # Each cycle's inputs go host -> device as chunks spread over four copy
-        # streams (several copy engines), into one of two device input sets, so
-        # the copies of cycle i + 1 overlap the kernels of cycle i; the kernels
-        # of a cycle wait for its own copies, and a set is refilled only after
-        # the cycle that read it has finished.
-        copy_streams = [torch.cuda.Stream() for _ in range(4)]
-        sets = [(U, target, c, c_hist, anchor, seeds),
-                tuple(torch.empty_like(t) for t in (U, target, c, c_hist, anchor, seeds))]
-        hosts = (hU, htgt, hc, hch, ha, hs)
-        freed = [None, None]
-
-        def issue_copies(b, after):
-            for cs in copy_streams:
-                if after is not None: cs.wait_event(after)
-                if freed[b] is not None: cs.wait_event(freed[b])
-            k = 0
-            for dst, src in zip(sets[b], hosts):
-                fd, fs = dst.view(-1), src.view(-1)
-                n = fd.numel()
-                pieces = max(1, min(16, (n * dst.element_size()) >> 25))  # ~32 MB pieces
-                per = (n + pieces - 1) // pieces
-                for j in range(pieces):
-                    with torch.cuda.stream(copy_streams[k % len(copy_streams)]):
-                        fd[j * per:(j + 1) * per].copy_(fs[j * per:(j + 1) * per], non_blocking=True)
-                    k += 1
-            done = []
-            for cs in copy_streams:
-                e = torch.cuda.Event()
-                e.record(cs)
-                done.append(e)
-            return done
-
-        def e2e_run(n, first_cycle, start_ev=None):
-            pending = issue_copies(0, start_ev)
-            for i in range(n):
-                b = i & 1
-                for e in pending:
-                    stream.wait_event(e)
-                if i + 1 < n:
-                    pending = issue_copies((i + 1) & 1, None)
-                step(first_cycle + i, inp=sets[b])
-                fe = torch.cuda.Event()
-                fe.record(stream)
-                freed[b] = fe
-                h_out.copy_(out, non_blocking=True); h_n.copy_(n_acc, non_blocking=True)
-                h_cl.copy_(cuc, non_blocking=True)
-
-        n_e2e = max(3, min(args.steps, 20))
-        e2e_run(2, 0)
-        torch.cuda.synchronize()
-        freed[0] = freed[1] = None
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
-        e2e_run(n_e2e, 100, s0)
-        s1.record(stream)
-        torch.cuda.synchronize()
-        e_ms = max_over_ranks(s0.elapsed_time(s1), world)
-        e2e = {"value": whole_job_rate(n_e2e, world, e_ms), "unit": UNIT,
-               "h2d_gb_s": bi * n_e2e / (e_ms / 1000.0) / 1e9, "h2d_bytes_per_step": bi,
-               "d2h_bytes_per_step": bo, "steps": n_e2e}
-
-    # verify reads target rows only up to each request's first rejection: its
-    # data-dependent algorithmic bytes (those rows, plus for T > 0 the residual
-    # draw's W2 pass and one target row and one U row per request) per verify call
     verify_roof = None
-    if run_verify:
-        n_h = n_acc.cpu().numpy().astype(np.int64)
-        l_h = l.cpu().numpy().astype(np.int64)
-        ok = n_h >= 0
-        rows_read = int((np.minimum(n_h[ok], l_h[ok]) + 1).sum())
-        vbytes = rows_read * V * 4
-        if T > 0:
-            vbytes += V * rank_r * 2 + int(ok.sum()) * V * (4 + 2)
+    if cyc.run_verify:
+        vbytes, rows_read, rows_presented = cyc.verify_bytes()
         v_ms = per["verify"]
         verify_roof = {"bound": "hbm", "achieved": vbytes / (v_ms / 1000.0) / 1e9, "peak": hbm, "unit": "GB/s",
                        "frac": vbytes / (v_ms / 1000.0) / 1e9 / hbm, "algorithmic_bytes_per_call": vbytes,
-                       "rows_read": rows_read, "rows_presented": int((l_h + 1).sum()), "call_ms": v_ms}
+                       "rows_read": rows_read, "rows_presented": rows_presented, "call_ms": v_ms}
+    else:
+        rows_read = rows_presented = 0
+
+    side = None
+    if rank == 0 and args.stage == "cycle" and not args.no_side_workloads and args.workload == DEFAULT_WORKLOAD:
+        del cyc
+        torch.cuda.empty_cache()
+        side = {name: side_workload(name, args, peaks)
+                for name in ("confidence_scheduled", "varlen_verify", "qwen3_8b_greedy")}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.stage == "cycle":
-        per_req, sample = oracle_sample(w, d, inputs.target_full(w, d["U"]), 4, 0)
-        cpu = {"value": 1.0 / (per_req * R), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
+    if pool is not None:
+        secs = pool.cycle(0)
+        pool.close()
+        cpu = {"value": 1.0 / secs, "unit": UNIT, "cores": pool.n, "kind": "oracle",
+               "sample": f"one whole cycle of all {R} requests (draft {gamma} positions + verify + commit), "
+                         f"requests spread over {pool.n} worker processes",
+               "cpu_model": model, "nproc": ncpu}
 
     if rank == 0:
+        logits_read = rows_read * V * 4 + R * gamma * V * 2
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16 GEMM (fp32 accumulate) + fp32 softmax/verify",
                 "data": "synthetic (seeded; shapes and laws of the workload)",
-                "config": dict(workload_config(w), parallelism=f"replicas x{world}"),
+                "config": workload_config(w, world),
+                "timing": {"blocks": len(blocks), "steps_per_block": args.steps,
+                           "block_ms_min_median_max": [min(blocks), ms_block, max(blocks)],
+                           "rule": "median of timed blocks of exactly K steps, repeated for about "
+                                   f"{BLOCK_SECONDS:g} s"},
                 "roofline": roof, "verify_roofline": verify_roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-                "gpu_launches": launches_per_step * args.steps,
-                "stage": args.stage, "stage_ms": per, "logits_gb_s": (R * (gamma + 1) * V * 4 + R * gamma * V * 2) /
-                (ms_step / 1000.0) / 1e9, "draft_path": "tcgen05" if uses_tc else "simt"}
+                "gpu_launches": cyc_launches(args, w) * n_timed,
+                "stage": args.stage, "stage_ms": per,
+                "logits_gb_s": logits_read / (ms_step / 1000.0) / 1e9,
+                "logits_gb_s_rule": "target rows verify read (up to each first rejection) + U, per cycle",
+                "presented_logits_gb_s": (R * (gamma + 1) * V * 4 + R * gamma * V * 2) / (ms_step / 1000.0) / 1e9,
+                "draft_path": "tcgen05" if roof["kernel"].startswith("markov_tc") else "simt",
+                "workloads": side}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def cyc_launches(args, w):
+    """Launches of this library per step of the headline workload (recomputed
+    after the side workloads freed its tensors)."""
+    from speculative_decoding_dspark_gb300 import binding as B
+    R, V, gamma, rank = w["R"], w["V"], w["gamma"], w["rank"]
+    uses_tc = B.dspark_markov_draft_uses_tensor_cores(B.DSPARK_BF16, B.DSPARK_BF16, R, V, rank)
+    draft = (1 if uses_tc else 1 + 2 * gamma) * int(args.stage in ("cycle", "draft"))
+    verify = (4 if float(w["temperature"]) > 0 else 2) * int(args.stage in ("cycle", "verify"))
+    varlen = bool(w.get("varlen"))
+    return int(args.stage == "cycle" and not varlen) + draft + verify + int(args.stage == "cycle")
+
+
+def measure_e2e(cyc, args, world):
+    """The cycle end to end: every step copies its inputs from pinned host
+    memory and reads its results back, inside the timed region."""
+    import torch
+    stream = cyc.stream
+    R, gamma = cyc.R, cyc.gamma
+    dev_in = (cyc.U, cyc.target, cyc.c, cyc.c_hist, cyc.anchor, cyc.seeds)
+    hosts = tuple(t.cpu().pin_memory() for t in dev_in)
+    h_out = torch.empty((R, gamma + 1), dtype=torch.int32).pin_memory()
+    h_n = torch.empty(R, dtype=torch.int32).pin_memory()
+    h_cl = torch.empty(R + 1, dtype=torch.int32).pin_memory()
+    bi = sum(t.numel() * t.element_size() for t in hosts)
+    bo = sum(t.numel() * t.element_size() for t in (h_out, h_n, h_cl))
+
+    # Each cycle's inputs go host -> device as chunks spread over four copy
+    # streams (several copy engines), into one of two device input sets, so
+    # the copies of cycle i + 1 overlap the kernels of cycle i; the kernels
+    # of a cycle wait for its own copies, and a set is refilled only after
+    # the cycle that read it has finished.
+    copy_streams = [torch.cuda.Stream() for _ in range(4)]
+    sets = [dev_in, tuple(torch.empty_like(t) for t in dev_in)]
+    freed = [None, None]
+
+    def issue_copies(b, after):
+        for cs in copy_streams:
+            if after is not None: cs.wait_event(after)
+            if freed[b] is not None: cs.wait_event(freed[b])
+        k = 0
+        for dst, src in zip(sets[b], hosts):
+            fd, fs = dst.view(-1), src.view(-1)
+            n = fd.numel()
+            pieces = max(1, min(16, (n * dst.element_size()) >> 25))  # ~32 MB pieces
+            per = (n + pieces - 1) // pieces
+            for j in range(pieces):
+                with torch.cuda.stream(copy_streams[k % len(copy_streams)]):
+                    fd[j * per:(j + 1) * per].copy_(fs[j * per:(j + 1) * per], non_blocking=True)
+                k += 1
+        done = []
+        for cs in copy_streams:
+            e = torch.cuda.Event()
+            e.record(cs)
+            done.append(e)
+        return done
+
+    def e2e_run(n, first_cycle, start_ev=None):
+        pending = issue_copies(0, start_ev)
+        for i in range(n):
+            b = i & 1
+            for e in pending:
+                stream.wait_event(e)
+            if i + 1 < n:
+                pending = issue_copies((i + 1) & 1, None)
+            cyc.step(first_cycle + i, inp=sets[b])
+            fe = torch.cuda.Event()
+            fe.record(stream)
+            freed[b] = fe
+            h_out.copy_(cyc.out, non_blocking=True); h_n.copy_(cyc.n_acc, non_blocking=True)
+            h_cl.copy_(cyc.cuc, non_blocking=True)
+
+    n_e2e = max(3, min(args.steps, 20))
+    e2e_run(2, 0)
+    torch.cuda.synchronize()
+    freed[0] = freed[1] = None
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    e2e_run(n_e2e, 100000, s0)
+    s1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = max_over_ranks(s0.elapsed_time(s1), world)
+    del sets
+    return {"value": whole_job_rate(n_e2e, world, e_ms), "unit": UNIT,
+            "h2d_gb_s": bi * n_e2e / (e_ms / 1000.0) / 1e9, "h2d_bytes_per_step": bi,
+            "d2h_bytes_per_step": bo, "steps": n_e2e}
 
 
 def main():

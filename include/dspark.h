@@ -21,7 +21,9 @@
  *
  * Conventions shared by every call:
  *   - Every array argument is a DEVICE pointer owned by the caller; the
- *     library allocates no memory and keeps no state between calls.  Scratch
+ *     library allocates no memory and keeps no state between calls (apart
+ *     from the two process-wide wait settings of dspark_set_wait_limit_ns and
+ *     dspark_set_fault_injection, which default to "off").  Scratch
  *     lives in a caller-provided workspace of dspark_workspace_size() bytes
  *     (any 256-byte aligned device buffer; its contents need no
  *     initialisation and are clobbered).
@@ -113,7 +115,10 @@ size_t dspark_workspace_size(int op, int R, int gamma, int V, int rank, int max_
  * arguments, 0 for the CUDA-core kernels.  The tensor-core kernel takes bf16 U
  * and factors, rank a multiple of 64 up to 512, V a multiple of 8, and at most
  * 128 requests per SM of the current device (all positions run in one launch
- * whose CTAs are resident together). */
+ * whose CTAs are resident together).  Everything else -- fp32 operands, rank
+ * 576 .. 1024, rank not a multiple of 64, V % 8 != 0, more requests -- runs on
+ * the CUDA-core kernels, about 40x slower at the R = 128, V = 151936, rank 512
+ * shape. */
 int dspark_markov_draft_uses_tensor_cores(int u_dtype, int w_dtype, int R, int V, int rank,
                                           unsigned flags);
 
@@ -150,8 +155,10 @@ int dspark_philox4x32_10(const uint32_t* ctr, const uint64_t* keys, int n, uint3
  *   ws, ws_bytes  workspace of dspark_workspace_size(DSPARK_OP_DRAFT, R, gamma, V,
  *                 rank, 0, w_dtype, flags) bytes
  * Limits: 1 <= gamma <= 16, R >= 1, V >= 1, rank >= 1.  The tensor-core kernel
- * applies to BF16 U and weights with rank % 64 == 0, rank <= 1024 and
- * V % 8 == 0; everything else runs on the CUDA-core kernels.
+ * applies to BF16 U and weights with rank % 64 == 0, rank <= 512, V % 8 == 0
+ * and R <= 128 x the SM count (dspark_markov_draft_uses_tensor_cores says
+ * which); everything else runs on the CUDA-core kernels (a per-position bias
+ * GEMV and a sampling pass; correct, but far slower).
  */
 int dspark_markov_draft(const void* U, int u_dtype, const void* W1, const void* W2,
                         int w_dtype, const int32_t* anchor, const uint64_t* seeds,
@@ -236,20 +243,26 @@ int dspark_verify_markov(const float* target_logits, const int32_t* cu_seqlens,
  *
  * Same arguments, results and status codes as dspark_verify, minus ws and
  * ws_bytes.  The scratch is a static device array of
- * DSPARK_VERIFY_STATIC_SCRATCH_BYTES (2 MiB) compiled into the library; every
+ * DSPARK_VERIFY_STATIC_SCRATCH_BYTES (4 MiB) compiled into the library; every
  * GPU that loads the library holds it until the process exits.  The call
  * allocates nothing.  Sizes whose scratch need
- * (dspark_workspace_size(DSPARK_OP_VERIFY, R, gamma, V, 0, max_rows, 0, 0))
- * exceeds the array return DSPARK_ERR_CAPACITY and enqueue nothing.
+ * (dspark_workspace_size(DSPARK_OP_VERIFY, R, gamma, V, 0, max_rows, 0, 0),
+ * about R * (32 * ceil(V / 1024) + 32 * ceil(V / 8192) + 56) bytes) exceeds the
+ * array return DSPARK_ERR_CAPACITY and enqueue nothing: R <= 772 at
+ * V = 151936, R <= 905 at V = 129280, R <= 3482 at V = 32000.
  *
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture starts.  All calls on a device share the array
- * and it keeps the last call's contents; the kernels reset their own counters
- * at the start of every call.  Calls whose kernels overlap on the GPU (for
- * example on two streams at once) race on the array: serialise them.
+ * (cudaGetSymbolAddress, with that device current) and keeps it for the life
+ * of the process; make that first call before any stream capture starts.  The
+ * kept address belongs to the device's primary context: do not call this
+ * function again after cudaDeviceReset() (the module is then loaded anew,
+ * possibly at another address).  All calls on a device share the array and it
+ * keeps the last call's contents; the kernels reset their own counters, flags
+ * and per-request rows at the start of every call, so nothing has to be
+ * cleared beforehand.  Calls whose kernels overlap on the GPU (for example on
+ * two streams at once) race on the array: serialise them.
  */
-#define DSPARK_VERIFY_STATIC_SCRATCH_BYTES (2u * 1024u * 1024u)
+#define DSPARK_VERIFY_STATIC_SCRATCH_BYTES (4u * 1024u * 1024u)
 
 int dspark_verify_static_scratch(const float* target_logits, const int32_t* cu_seqlens,
                                  const int32_t* draft_tokens, const float* q_logits,
@@ -257,6 +270,37 @@ int dspark_verify_static_scratch(const float* target_logits, const int32_t* cu_s
                                  uint32_t cycle, float temperature, int R, int gamma, int V,
                                  int max_rows, int32_t* n_accepted, int32_t* out_tokens,
                                  float* p_tok, int32_t* dev_status, dspark_stream_t stream);
+
+/*
+ * ---- failure handling: the grid-wide waits --------------------------------
+ * The verify rounds (every verify call) and the tensor-core draft (all block
+ * positions in one launch) run as cooperative launches whose CTAs meet at
+ * grid-wide barriers: between verify rounds, and between draft positions.
+ * Every such wait is bounded (explainer section 16: a fault must fall back to
+ * target-only decoding, not hang the engine): when it runs out the kernel
+ * raises an abort word, every CTA drains the asynchronous copies and tensor-
+ * core operations it has in flight and exits, DSPARK_ERR_TIMEOUT is written to
+ * *dev_status, and the CUDA context stays usable.  Outputs of a call that
+ * reported DSPARK_ERR_TIMEOUT are invalid (requests decided before the wait
+ * ran out may have been written; the others are left untouched).  The waits
+ * of a CTA on its own asynchronous copies (mbarriers) keep a fixed 2 s limit.
+ *
+ * dspark_set_wait_limit_ns sets the limit of the grid-wide waits for every
+ * later call of this process (0 or anything above 2 s: the default, 2 s) and
+ * returns the previous limit.
+ *
+ * dspark_set_fault_injection is for tests of this failure path: with
+ * DSPARK_INJECT_VERIFY_BARRIER the verify rounds' barriers, with
+ * DSPARK_INJECT_DRAFT_BARRIER the draft's position barriers, count one
+ * arrival more than the grid has, so that no CTA is ever released and every
+ * wait runs out after the limit above.  Returns the previous mask; 0 turns
+ * injection off.  Both settings are read when a call is enqueued.
+ */
+#define DSPARK_INJECT_VERIFY_BARRIER 1u
+#define DSPARK_INJECT_DRAFT_BARRIER 2u
+
+uint64_t dspark_set_wait_limit_ns(uint64_t limit_ns);
+unsigned dspark_set_fault_injection(unsigned mask);
 
 /*
  * dspark_select_prefix -- survival, capacity and prefix-closed top-K

@@ -30,11 +30,12 @@ DSPARK_F32, DSPARK_BF16 = 0, 1
 DSPARK_OP_DRAFT, DSPARK_OP_VERIFY, DSPARK_OP_SELECT, DSPARK_OP_VERIFY_MARKOV = 0, 1, 2, 3
 DSPARK_DRAFT_FORCE_SIMT = 1
 DSPARK_SELECT_FIXED, DSPARK_SELECT_HISTORY, DSPARK_SELECT_CURRENT, DSPARK_SELECT_FIRST_STOP = 0, 1, 2, 3
+DSPARK_INJECT_VERIFY_BARRIER, DSPARK_INJECT_DRAFT_BARRIER = 1, 2
 
 EXPORTED = ["dspark_status_string", "dspark_version", "dspark_workspace_size", "dspark_philox4x32_10",
             "dspark_markov_draft_uses_tensor_cores", "dspark_markov_draft", "dspark_verify",
             "dspark_select_prefix", "dspark_commit_lengths", "dspark_verify_static_scratch",
-            "dspark_verify_markov"]
+            "dspark_verify_markov", "dspark_set_wait_limit_ns", "dspark_set_fault_injection"]
 
 
 class DSparkError(RuntimeError):
@@ -75,6 +76,10 @@ def _load():
     L.dspark_philox4x32_10.restype = i32
     L.dspark_commit_lengths.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, vp]
     L.dspark_commit_lengths.restype = i32
+    L.dspark_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    L.dspark_set_wait_limit_ns.restype = ctypes.c_uint64
+    L.dspark_set_fault_injection.argtypes = [ctypes.c_uint]
+    L.dspark_set_fault_injection.restype = ctypes.c_uint
     return L
 
 
@@ -141,6 +146,18 @@ def dspark_workspace_size(op, R, gamma, V, rank=0, max_rows=0, w_dtype=DSPARK_BF
 
 def dspark_markov_draft_uses_tensor_cores(u_dtype, w_dtype, R, V, rank, flags=0) -> bool:
     return bool(_L.dspark_markov_draft_uses_tensor_cores(u_dtype, w_dtype, R, V, rank, flags))
+
+
+def dspark_set_wait_limit_ns(limit_ns: int) -> int:
+    """Limit of the grid-wide device waits for later calls (0: the 2 s default);
+    returns the previous limit."""
+    return int(_L.dspark_set_wait_limit_ns(int(limit_ns)))
+
+
+def dspark_set_fault_injection(mask: int) -> int:
+    """Test hook: make the named grid-wide waits run out (see dspark.h); returns
+    the previous mask."""
+    return int(_L.dspark_set_fault_injection(int(mask)))
 
 
 def workspace(nbytes: int, device=None) -> torch.Tensor:
@@ -234,9 +251,10 @@ def dspark_verify_static_scratch(target_logits, cu_seqlens, draft_tokens, q_logi
     """dspark_verify without a workspace argument, for callers that are not
     allowed to allocate device memory (for example a plugin inside a serving
     engine whose device memory all belongs to the engine's pool).  The scratch
-    is a fixed 2 MiB array inside the library, shared by every call on a
-    device: calls must not overlap on the GPU, and the first call on a device
-    (which looks the array up) should happen before any stream capture."""
+    is a fixed 4 MiB array inside the library, shared by every call on a
+    device: calls must not overlap on the GPU, the first call on a device
+    (which looks the array up) should happen before any stream capture, and
+    the entry point must not be used after a cudaDeviceReset."""
     R, gamma = draft_tokens.shape
     V = target_logits.shape[1]
     _check(target_logits, "target_logits", torch.float32)

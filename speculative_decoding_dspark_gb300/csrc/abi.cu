@@ -1,8 +1,10 @@
 // abi.cu -- the library's extern "C" entry points (declared in dspark.h).
 //
 // Host-side argument checks, workspace carving and kernel dispatch only; every
-// step of the cycle runs in the kernels.  No call allocates memory, keeps
-// state, synchronises or throws.
+// step of the cycle runs in the kernels.  No call allocates memory,
+// synchronises or throws; the only state is the pair of process-wide wait
+// settings (limit of the grid-wide waits, test injection), read at each call.
+#include <atomic>
 #include <cstring>
 
 #include "kernels.cuh"
@@ -69,9 +71,28 @@ bool tc_applies(int u_dtype, int w_dtype, int R, int V, int rank, unsigned flags
 
 bool valid_dtype(int d) { return d == DSPARK_F32 || d == DSPARK_BF16; }
 
+// Process-wide settings of the grid-wide waits (see dspark_set_wait_limit_ns).
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+std::atomic<unsigned> g_inject{0u};
+
 }  // namespace
 
+namespace dspark {
+unsigned long long grid_wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+unsigned fault_injection_mask() { return g_inject.load(std::memory_order_relaxed); }
+}  // namespace dspark
+
 extern "C" {
+
+uint64_t dspark_set_wait_limit_ns(uint64_t limit_ns) {
+    if (limit_ns == 0 || limit_ns > kDefaultWaitNs) limit_ns = kDefaultWaitNs;
+    return g_wait_ns.exchange(limit_ns);
+}
+
+unsigned dspark_set_fault_injection(unsigned mask) {
+    return g_inject.exchange(mask & (DSPARK_INJECT_VERIFY_BARRIER | DSPARK_INJECT_DRAFT_BARRIER));
+}
 
 const char* dspark_status_string(int status) {
     switch (status) {

@@ -143,6 +143,10 @@ struct TcParams {
     float* q_tok;
     const float* target;
     const ResRow* rows;
+    // draft: the grid barriers between positions wait at most wait_ns; their
+    // arrival count is the grid's plus phantom (1 only in the timeout test)
+    unsigned long long wait_ns;
+    unsigned phantom;
 };
 
 struct Bars {
@@ -305,10 +309,11 @@ __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n
 // Between two draft steps, one thread per CTA: every CTA's winner keys of the
 // step are published (its threads passed a CTA barrier after their atomics)
 // before any CTA reads them.  done counts the CTAs through the step (zeroed
-// with the keys before the launch, used once).  Bounded: gives up after the
-// wait limit or when another CTA gave up (abort word), raising the abort word
+// with the keys before the launch, used once).  Bounded: gives up after
+// wait_ns or when another CTA gave up (abort word), raising the abort word
 // itself on a timeout.
-__device__ __forceinline__ bool step_barrier(unsigned* done, int* abort_word, unsigned n_cta) {
+__device__ __forceinline__ bool step_barrier(unsigned* done, int* abort_word, unsigned n_cta,
+                                             unsigned long long wait_ns) {
     asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(done) : "memory");
     const uint64_t t0 = global_ns();
     for (unsigned it = 1;; ++it) {
@@ -317,7 +322,7 @@ __device__ __forceinline__ bool step_barrier(unsigned* done, int* abort_word, un
         if (v >= n_cta) break;
         if ((it & 15) == 0) {
             if (*reinterpret_cast<volatile int*>(abort_word)) return false;
-            if (global_ns() - t0 > kWaitNs) {
+            if (global_ns() - t0 > wait_ns) {
                 atomicExch(abort_word, 1);
                 return false;
             }
@@ -1026,7 +1031,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                 epi_sync();
                 if (e == 0) {
                     bool ok = !*abort_flag;
-                    if (ok) ok = step_barrier(p.step_done + k, reinterpret_cast<int*>(p.step_done + p.gamma), gridDim.x);
+                    if (ok)
+                        ok = step_barrier(p.step_done + k, reinterpret_cast<int*>(p.step_done + p.gamma),
+                                          gridDim.x + p.phantom, p.wait_ns);
                     else atomicExch(reinterpret_cast<int*>(p.step_done + p.gamma), 1);
                     if (!ok) *abort_flag = 1;  // the control warps stop too
                     bar.step_ok = ok ? 1 : 0;
@@ -1047,7 +1054,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
             if (e == 0) {
                 int* abort_word = reinterpret_cast<int*>(p.step_done + p.gamma);
                 bool ok = !*abort_flag;
-                if (ok) ok = step_barrier(p.step_done + (p.gamma - 1), abort_word, gridDim.x);
+                if (ok) ok = step_barrier(p.step_done + (p.gamma - 1), abort_word, gridDim.x + p.phantom, p.wait_ns);
                 else atomicExch(abort_word, 1);
                 if (!ok) *abort_flag = 1;
                 bar.step_ok = ok ? 1 : 0;
@@ -1304,6 +1311,8 @@ int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream) {
     p.cycle = a.cycle;
     p.invT = a.invT;
     p.greedy = a.greedy;
+    p.wait_ns = grid_wait_limit_ns();
+    p.phantom = (fault_injection_mask() & DSPARK_INJECT_DRAFT_BARRIER) ? 1u : 0u;
     if (cudaFuncSetAttribute(markov_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return DSPARK_ERR_CUDA;
@@ -1346,6 +1355,8 @@ int launch_residual_tc(const ResidualTcArgs& a, cudaStream_t stream) {
     p.greedy = 0;
     p.target = a.target;
     p.rows = rows;
+    p.wait_ns = kWaitNs;  // no grid barrier in the residual launch
+    p.phantom = 0;
     if (cudaFuncSetAttribute(markov_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return DSPARK_ERR_CUDA;

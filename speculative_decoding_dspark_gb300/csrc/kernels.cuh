@@ -77,6 +77,10 @@ struct VerifyParams {
     const int32_t* anchor = nullptr;  // [R]
     const uint16_t* W1 = nullptr;     // [V, rank] bf16: each predecessor's row is requested into L2
     int rank = 0;
+    // the grid barriers between rounds: wait limit, and an arrival count one
+    // above the grid's when the barrier-timeout test injection is on
+    unsigned long long wait_ns = 2000000000ull;
+    int phantom = 0;
 };
 
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream);
@@ -146,6 +150,11 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t stream);
 
 cudaError_t launch_philox_batch(const uint32_t* ctr, const uint64_t* keys, int n, uint32_t* out,
                                 cudaStream_t stream);
+
+// Process-wide settings of the grid-wide waits (dspark_set_wait_limit_ns,
+// dspark_set_fault_injection), read by each call when it is enqueued.
+unsigned long long grid_wait_limit_ns();
+unsigned fault_injection_mask();
 
 cudaError_t launch_commit(const int32_t* n_acc, const int32_t* l, int R, int gamma,
                           int32_t* commit_len, int32_t* cu_commit, int32_t* discard,

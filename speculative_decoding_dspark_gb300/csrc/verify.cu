@@ -64,6 +64,10 @@ __global__ void __launch_bounds__(1024) verify_prologue_kernel(VerifyParams p) {
             if (!valid) report(p.dev_status, DSPARK_ERR_DEVICE_INPUT);
         }
         p.valid[r] = valid;
+        VerifyJob job;  // no extra token until the request is decided
+        job.row = 0; job.pos = 0; job.mode = 0; job.pad = 0; job.lse = 0.0f;
+        job.pad2[0] = job.pad2[1] = job.pad2[2] = 0.0f;
+        p.jobs[r] = job;
         p.act[r] = 0;
         p.act[p.R + r] = 0;
         if (p.res_rows) {  // nothing to draw until the request is decided
@@ -123,20 +127,21 @@ __device__ __forceinline__ void load_unit(const VerifyParams& p, int row, int su
 
 // Round state in the workspace (zeroed by the prologue).
 enum : int { kBarCount = 0, kBarGen = 1, kAbort = 2 };
-constexpr uint64_t kBarrierNs = 2000000000ull;
 
 // Grid-wide barrier of a cooperative launch (every CTA is resident): the last
 // CTA to arrive resets the count and advances the generation; the others wait
-// for it, at most kBarrierNs, after which the round state's abort flag is set.
-// Returns false when the pass is aborted.
-__device__ __forceinline__ bool grid_barrier(int* st, unsigned& gen) {
+// for it, at most p.wait_ns, after which the round state's abort flag is set.
+// (p.phantom = 1 counts one arrival more than the grid has, so that nobody is
+// last and every CTA's wait runs out: the timeout test.)  Returns false when
+// the pass is aborted.
+__device__ __forceinline__ bool grid_barrier(const VerifyParams& p, int* st, unsigned& gen) {
     __shared__ int s_ok;
     __syncthreads();
     if (threadIdx.x == 0) {
         int ok = 1;
         const unsigned target = gen + 1;
         __threadfence();
-        if (atomicAdd(reinterpret_cast<unsigned*>(st + kBarCount), 1u) == gridDim.x - 1) {
+        if (atomicAdd(reinterpret_cast<unsigned*>(st + kBarCount), 1u) == gridDim.x - 1u + (unsigned)p.phantom) {
             st[kBarCount] = 0;
             __threadfence();
             atomicExch(reinterpret_cast<unsigned*>(st + kBarGen), target);
@@ -144,7 +149,7 @@ __device__ __forceinline__ bool grid_barrier(int* st, unsigned& gen) {
             const uint64_t t0 = global_ns();
             for (unsigned it = 1; *reinterpret_cast<volatile unsigned*>(st + kBarGen) != target; ++it) {
                 if ((it & 31) == 0 &&
-                    (*reinterpret_cast<volatile int*>(st + kAbort) || global_ns() - t0 > kBarrierNs)) {
+                    (*reinterpret_cast<volatile int*>(st + kAbort) || global_ns() - t0 > p.wait_ns)) {
                     atomicExch(st + kAbort, 1);
                     ok = 0;
                     break;
@@ -399,7 +404,7 @@ __global__ void __launch_bounds__(kRoundThreads, 1) verify_rounds_kernel(VerifyP
 #pragma unroll
             for (int i = 0; i < kStatVec; ++i) buf[i] = nxt[i];
         }
-        if (!grid_barrier(st, gen)) break;
+        if (!grid_barrier(p, st, gen)) break;
         // the decision inputs fetched by lane 0, for the whole warp
         din.r = __shfl_sync(0xFFFFFFFFu, din.r, 0);
         din.valid = __shfl_sync(0xFFFFFFFFu, din.valid, 0);
@@ -430,7 +435,7 @@ __global__ void __launch_bounds__(kRoundThreads, 1) verify_rounds_kernel(VerifyP
                 const int n = decide_request<kGreedy>(p, stj, d, j, c2, true);
                 if (n == -1 && lane == 0) p.act[d.r] = j + 1;  // goes on to round j + 1
             }
-            if (!grid_barrier(st, gen)) break;
+            if (!grid_barrier(p, st, gen)) break;
             // every CTA lists the requests accepted in this round (flags written by
             // other CTAs: read from L2)
             if (threadIdx.x < 32) {
@@ -490,7 +495,11 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_correct_kernel(VerifyPa
     const int r = blockIdx.x / p.nchunk;
     const int chunk = blockIdx.x - r * p.nchunk;
     if (!p.ok[0] || !p.valid[r]) return;
+    // a decision pass that gave up (a grid barrier's wait ran out) leaves
+    // requests undecided: nothing to draw for them
+    if (*reinterpret_cast<volatile int*>(p.lazy + kAbort)) return;
     const VerifyJob job = p.jobs[r];
+    if (job.mode == 0) return;
     const int V = p.V;
     const int v0 = chunk * kVerifyChunk;
     const int v1 = min(V, v0 + kVerifyChunk);
@@ -578,6 +587,8 @@ cudaError_t launch_verify_decide(const VerifyParams& p, cudaStream_t stream) {
     const int grid = n_sm;
     const size_t smem = sizeof(int) * (size_t)p.R;
     VerifyParams arg = p;
+    arg.wait_ns = grid_wait_limit_ns();
+    arg.phantom = (fault_injection_mask() & DSPARK_INJECT_VERIFY_BARRIER) ? 1 : 0;
     void* args[] = {&arg};
     e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kRoundThreads), args, smem, stream);
     if (e != cudaSuccess) return e;

@@ -9,8 +9,9 @@
 // loads the library holds the array until the process exits.
 //
 // The array is shared by every call on a device and keeps whatever the last
-// call left in it; the verify kernels clear their own counters and flags at
-// the start of each call, so nothing has to be zeroed beforehand.  Two calls
+// call left in it; the verify prologue clears the counters, flags and
+// per-request rows at the start of each call, so nothing has to be zeroed
+// beforehand.  Two calls
 // whose kernels overlap on the GPU (for example on two streams) use the same
 // array and race: serialise them.
 #include <mutex>
@@ -27,7 +28,10 @@ __device__ __align__(256) unsigned char g_verify_scratch[DSPARK_VERIFY_STATIC_SC
 
 // Device addresses of the array, looked up once per device.  In host code the
 // array's name only stands in for the device object, so the address has to
-// come from cudaGetSymbolAddress with the device current.
+// come from cudaGetSymbolAddress with the device current.  The address kept
+// here belongs to the device's primary context; after cudaDeviceReset the
+// module is loaded anew (possibly elsewhere), which is why the header asks
+// callers not to use this entry point across a reset.
 void* g_scratch_addr[kMaxDevices] = {};
 std::mutex g_scratch_mutex;
 

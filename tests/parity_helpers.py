@@ -8,6 +8,9 @@ MARGIN, or |u - p/q| within MARGIN for an acceptance -- such decisions are
 counted as exempt and the rest of that request is left out; exempt decisions
 must stay under 0.1% of all decisions.  Probabilities (q(y), p(y)) agree to
 PROB_TOL absolute, log-normalisers to LSE_TOL relative.
+
+Every output and workspace passed to the library is surrounded by guard bytes
+that are checked after the call (no write outside a buffer).
 """
 from __future__ import annotations
 
@@ -21,6 +24,47 @@ MARGIN = 1e-5
 PROB_TOL = 1e-5
 LSE_TOL = 1e-5
 EXEMPT_FRACTION = 1e-3
+
+
+# ---------------------------------------------------------------- guard words
+# Every output and workspace the helpers hand to the library sits between two
+# 256-byte guard regions filled with GUARD_BYTE; after each call the guards are
+# compared, so a kernel writing past either end of a buffer fails the test.
+GUARD_BYTES = 256
+GUARD_BYTE = 0xA5
+
+
+class Guarded:
+    """Outputs and workspaces of one library call, each between guard regions."""
+
+    def __init__(self):
+        self.raw = []
+
+    def _alloc(self, nbytes):
+        nbytes = int(nbytes)
+        raw = torch.empty(GUARD_BYTES + nbytes + GUARD_BYTES, dtype=torch.uint8, device="cuda")
+        raw.fill_(GUARD_BYTE)
+        self.raw.append((raw, nbytes))
+        return raw[GUARD_BYTES:GUARD_BYTES + nbytes]
+
+    def out(self, shape, dtype, fill):
+        """A contiguous tensor of `shape` filled with `fill` (its data 256-byte aligned)."""
+        n = int(np.prod(shape))
+        item = torch.empty((), dtype=dtype).element_size()
+        t = self._alloc(max(n, 1) * item).view(dtype)[:n].view(shape)
+        t.fill_(fill)
+        return t
+
+    def workspace(self, nbytes):
+        return self._alloc(max(int(nbytes), 256))
+
+    def check(self):
+        """Call after the device has finished the call."""
+        for raw, nbytes in self.raw:
+            head = raw[:GUARD_BYTES]
+            tail = raw[GUARD_BYTES + nbytes:]
+            assert bool((head == GUARD_BYTE).all()), "write before the start of an output or workspace"
+            assert bool((tail == GUARD_BYTE).all()), "write past the end of an output or workspace"
 
 
 def dev(x: np.ndarray) -> torch.Tensor:
@@ -42,16 +86,18 @@ def gpu_draft(d: dict, temperature: float, cycle: int, flags: int = 0, want_logi
     U, W1, W2 = dev(d["U"]), dev(d["W1"]), dev(d["W2"])
     R, gamma, V = U.shape
     rank = W1.shape[1]
-    y = torch.full((R, gamma), -7, dtype=torch.int32, device="cuda")
-    q_lse = torch.full((R, gamma), float("nan"), device="cuda")
-    q_tok = torch.full((R, gamma), float("nan"), device="cuda")
-    q_logits = torch.empty((R, gamma, V), device="cuda") if want_logits else None
+    G = Guarded()
+    y = G.out((R, gamma), torch.int32, -7)
+    q_lse = G.out((R, gamma), torch.float32, float("nan"))
+    q_tok = G.out((R, gamma), torch.float32, float("nan"))
+    q_logits = G.out((R, gamma, V), torch.float32, float("nan")) if want_logits else None
     w_dtype = B.DSPARK_BF16 if W1.dtype == torch.bfloat16 else B.DSPARK_F32
-    ws = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_DRAFT, R, gamma, V, rank, 0, w_dtype, flags))
-    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = G.workspace(B.dspark_workspace_size(B.DSPARK_OP_DRAFT, R, gamma, V, rank, 0, w_dtype, flags))
+    status = G.out((1,), torch.int32, 0)
     B.dspark_markov_draft(U, W1, W2, dev(d["anchor"]), dev(d["seeds"]), cycle, temperature, y,
                           q_lse, q_tok, q_logits, ws, status, flags=flags)
     torch.cuda.synchronize()
+    G.check()
     out = dict(y=host(y), q_lse=host(q_lse), q_tok=host(q_tok), status=int(status.item()))
     out["q_logits_dev"] = q_logits
     out["q_lse_dev"], out["q_tok_dev"], out["y_dev"] = q_lse, q_tok, y
@@ -65,14 +111,16 @@ def gpu_verify(target, cu, y, q_logits, q_lse, q_tok, seeds, cycle, temperature,
     R, gamma = y_d.shape
     V = target_d.shape[1]
     max_rows = int(target_d.shape[0]) if max_rows is None else max_rows
-    n_acc = torch.full((R,), -7, dtype=torch.int32, device="cuda")
-    out = torch.full((R, gamma + 1), -7, dtype=torch.int32, device="cuda")
-    p_tok = torch.full((R, gamma), float("nan"), device="cuda")
-    ws = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_VERIFY, R, gamma, V, 0, max_rows))
-    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    G = Guarded()
+    n_acc = G.out((R,), torch.int32, -7)
+    out = G.out((R, gamma + 1), torch.int32, -7)
+    p_tok = G.out((R, gamma), torch.float32, float("nan"))
+    ws = G.workspace(B.dspark_workspace_size(B.DSPARK_OP_VERIFY, R, gamma, V, 0, max_rows))
+    status = G.out((1,), torch.int32, 0)
     B.dspark_verify(target_d, cu_d, y_d, t(q_logits), t(q_lse), t(q_tok), t(seeds), cycle,
                     temperature, max_rows, n_acc, out, p_tok, ws, status)
     torch.cuda.synchronize()
+    G.check()
     return dict(n_acc=host(n_acc), out_tokens=host(out), p_tok=host(p_tok), status=int(status.item()))
 
 
@@ -86,43 +134,51 @@ def gpu_verify_markov(target, cu, d, g, cycle, temperature, max_rows=None):
     W1 = dev(d["W1"])
     rank = W1.shape[1]
     max_rows = int(target_d.shape[0]) if max_rows is None else max_rows
-    n_acc = torch.full((R,), -7, dtype=torch.int32, device="cuda")
-    out = torch.full((R, gamma + 1), -7, dtype=torch.int32, device="cuda")
-    p_tok = torch.full((R, gamma), float("nan"), device="cuda")
-    ws = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_VERIFY_MARKOV, R, gamma, V, rank, max_rows))
-    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    G = Guarded()
+    n_acc = G.out((R,), torch.int32, -7)
+    out = G.out((R, gamma + 1), torch.int32, -7)
+    p_tok = G.out((R, gamma), torch.float32, float("nan"))
+    ws = G.workspace(B.dspark_workspace_size(B.DSPARK_OP_VERIFY_MARKOV, R, gamma, V, rank, max_rows))
+    status = G.out((1,), torch.int32, 0)
     samp = temperature > 0
     B.dspark_verify_markov(target_d, cu_d, y_d, dev(d["U"]), W1, dev(d["W2"]), dev(d["anchor"]),
                            g["q_lse_dev"] if samp else None, g["q_tok_dev"] if samp else None,
                            dev(d["seeds"]) if samp else None, cycle, temperature, max_rows, n_acc, out,
                            p_tok, ws, status)
     torch.cuda.synchronize()
+    G.check()
     return dict(n_acc=host(n_acc), out_tokens=host(out), p_tok=host(p_tok), status=int(status.item()))
 
 
 def gpu_select(c, c_hist, sizes, sps, K_cap, mode):
     R, gamma = c.shape
-    a = torch.full((R, gamma), float("nan"), device="cuda")
-    l = torch.full((R,), -7, dtype=torch.int32, device="cuda")
-    cu = torch.full((R + 1,), -7, dtype=torch.int32, device="cuda")
-    K = torch.zeros(1, dtype=torch.int32, device="cuda")
-    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    G = Guarded()
+    a = G.out((R, gamma), torch.float32, float("nan"))
+    l = G.out((R,), torch.int32, -7)
+    cu = G.out((R + 1,), torch.int32, -7)
+    K = G.out((1,), torch.int32, 0)
+    status = G.out((1,), torch.int32, 0)
     t = lambda x: None if x is None else dev(x)
-    B.dspark_select_prefix(dev(c), t(c_hist), t(sizes), t(sps), K_cap, mode, a, l, cu, K, None, status)
-    torch.cuda.synchronize()
+    try:
+        B.dspark_select_prefix(dev(c), t(c_hist), t(sizes), t(sps), K_cap, mode, a, l, cu, K, None, status)
+    finally:
+        torch.cuda.synchronize()
+        G.check()
     return dict(a=host(a), l=host(l), cu_seqlens=host(cu), K_used=int(K.item()), status=int(status.item()))
 
 
 def gpu_commit(n_acc, l, gamma):
     R = len(n_acc)
-    cl = torch.full((R,), -7, dtype=torch.int32, device="cuda")
-    cu = torch.full((R + 1,), -7, dtype=torch.int32, device="cuda")
-    disc = torch.full((R,), -7, dtype=torch.int32, device="cuda")
-    tot = torch.zeros(1, dtype=torch.int32, device="cuda")
-    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    G = Guarded()
+    cl = G.out((R,), torch.int32, -7)
+    cu = G.out((R + 1,), torch.int32, -7)
+    disc = G.out((R,), torch.int32, -7)
+    tot = G.out((1,), torch.int32, 0)
+    status = G.out((1,), torch.int32, 0)
     B.dspark_commit_lengths(dev(np.asarray(n_acc, np.int32)), None if l is None else dev(np.asarray(l, np.int32)),
                             gamma, cl, cu, disc, tot, status)
     torch.cuda.synchronize()
+    G.check()
     return dict(commit_len=host(cl), cu_commit=host(cu), discard=host(disc), total=int(tot.item()),
                 status=int(status.item()))
 

@@ -26,6 +26,12 @@ def test_reference_line_contract():
     assert line["config"]["workload"] == "tiny_exhaustive"
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == line["value"]
+    assert cb["nproc"] >= 1 and cb["cpu_model"]
+    # each timed step is one whole cycle: the rate and the step time agree
+    assert abs(line["value"] * line["ms_per_step"] - 1000.0) < 1e-6 * 1000.0
+    import bench
+    w = bench.inputs.workload("tiny_exhaustive")
+    assert line["config"] == bench.workload_config(w, 1)
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0

@@ -101,6 +101,59 @@ def test_draft_multi_tile_elementwise(B, orc, R, rank, T):
         np.testing.assert_allclose(ql[rows[i]], o["q_logits"][i], rtol=2e-6, atol=2e-5)
 
 
+def test_draft_rank512_every_request(B, orc):
+    """Rank 512 (the bench's Markov rank): A takes 128 KB of shared memory, so
+    the W2 ring has four 16 KB stages and each tile's eight k-blocks wrap the
+    ring inside the tile.  Factors at w_sigma 0.2 make the bias large enough to
+    move the draws (|b| about 0.9 against U's sigma of 3; checked below), so a
+    wrong k-block would change tokens and logits.  Every one of 128 requests
+    (all four tensor-memory lane quadrants) over 129 vocabulary tiles with a
+    ragged 8-column tail, called with q_logits (compared element by element)
+    and with q_logits = NULL (the call the bench times)."""
+    w, d = H.cycle_inputs("batched_sampling", R=128, V=16392, gamma=3, rank=512, w_sigma=0.2)
+    assert B.dspark_markov_draft_uses_tensor_cores(B.DSPARK_BF16, B.DSPARK_BF16, 128, 16392, 512)
+    bias = orc.markov_bias(d["W1"], d["W2"], int(d["anchor"][0]))
+    assert bias.std() > 0.5, bias.std()
+    T = 0.7
+    tally = H.Tally()
+    for cycle, want in ((0, True), (1, False)):
+        g = H.gpu_draft(d, T, cycle, want_logits=want)
+        assert g["status"] == 0
+        o = orc.markov_draft(d["U"], d["W1"], d["W2"], d["anchor"], d["seeds"], cycle, T,
+                             want_logits=want)
+        clean = H.compare_draft(tally, g, o, T)
+        assert len(clean) >= 120, len(clean)
+        if want:
+            ql = H.host(g["q_logits_dev"])
+            for r in clean:
+                np.testing.assert_allclose(ql[r], o["q_logits"][r], rtol=2e-6, atol=2e-5)
+    tally.check()
+    print(f"rank-512 draft: {tally.decisions} decisions, {tally.exempt} exempt near ties")
+
+
+def test_draft_rank512_full_vocab_sampled(B, orc):
+    """Rank 512 over the full 151936-entry vocabulary (each CTA walks about eight
+    tiles per position, so the four-stage ring also wraps across tiles and
+    positions), eight requests spread over the four lane quadrants compared with
+    the oracle, with q_logits element by element and with q_logits = NULL."""
+    w, d = H.cycle_inputs("batched_sampling", R=128, V=151936, gamma=2, rank=512, w_sigma=0.2)
+    T = 0.7
+    rows = [0, 9, 31, 32, 63, 64, 100, 127]
+    tally = H.Tally()
+    for cycle, want in ((0, True), (1, False)):
+        g = H.gpu_draft(d, T, cycle, want_logits=want)
+        assert g["status"] == 0
+        o = orc.markov_draft(d["U"][rows], d["W1"], d["W2"], d["anchor"][rows], d["seeds"][rows], cycle,
+                             T, req_ids=rows, want_logits=want)
+        clean = H.compare_draft(tally, g, o, T, rows=rows)
+        assert len(clean) >= 7, len(clean)
+        if want:
+            ql = H.host(g["q_logits_dev"])
+            for i in clean:
+                np.testing.assert_allclose(ql[rows[i]], o["q_logits"][i], rtol=2e-6, atol=2e-5)
+    tally.check()
+
+
 def test_draft_tiny_many_cycles(B, orc):
     """The V=64 workload: 2000 cycles at T=1 and 2000 greedy."""
     w, d = H.cycle_inputs("tiny_exhaustive")
@@ -175,17 +228,20 @@ def test_verify_parity_small(B, orc, name, over, T):
 
 
 MARKOV_CASES = [
-    ("batched_sampling", dict(R=7, V=20000, gamma=5, rank=64, w_sigma=0.3), 0.7),
-    ("varlen_verify", dict(R=24, V=10008, gamma=5, rank=64, w_sigma=0.3), 1.0),
-    ("batched_sampling", dict(R=130, V=4096, gamma=3, rank=128, w_sigma=0.3), 1.0),
-    ("qwen3_8b_greedy", dict(R=9, V=16392, gamma=7, rank=64, w_sigma=0.3), 0.0),
+    ("batched_sampling", dict(R=7, V=20000, gamma=5, rank=64, w_sigma=0.3), 0.7, 4),
+    ("varlen_verify", dict(R=24, V=10008, gamma=5, rank=64, w_sigma=0.3), 1.0, 4),
+    ("batched_sampling", dict(R=130, V=4096, gamma=3, rank=128, w_sigma=0.3), 1.0, 4),
+    ("qwen3_8b_greedy", dict(R=9, V=16392, gamma=7, rank=64, w_sigma=0.3), 0.0, 4),
     # rank 192: 24 sixteen-byte pieces per W1 row (not a power of two); V % 32 != 0
-    ("batched_sampling", dict(R=11, V=12008, gamma=4, rank=192, w_sigma=0.3), 0.8),
+    ("batched_sampling", dict(R=11, V=12008, gamma=4, rank=192, w_sigma=0.3), 0.8, 4),
+    # rank 512, the bench's: a four-stage W2 ring that wraps inside every tile,
+    # 128 requests (every lane quadrant), a ragged last tile
+    ("batched_sampling", dict(R=128, V=16392, gamma=3, rank=512, w_sigma=0.2), 0.7, 2),
 ]
 
 
-@pytest.mark.parametrize("name,over,T", MARKOV_CASES)
-def test_verify_markov_parity(B, orc, name, over, T):
+@pytest.mark.parametrize("name,over,T,cycles", MARKOV_CASES)
+def test_verify_markov_parity(B, orc, name, over, T, cycles):
     """Verify with the drafter's logits recomputed on the tensor cores: against
     the oracle, and identical to dspark_verify fed the stored logits."""
     w, d = H.cycle_inputs(name, **over)
@@ -195,7 +251,7 @@ def test_verify_markov_parity(B, orc, name, over, T):
     target = inputs.pack_rows(full, l)
     tD, cuD = H.dev(target), H.dev(cu)
     tally = H.Tally()
-    for cycle in range(4):
+    for cycle in range(cycles):
         g = H.gpu_draft(d, T, cycle)
         gm = H.gpu_verify_markov(tD, cuD, d, g, cycle, T)
         gv = H.gpu_verify(tD, cuD, g["y_dev"], g["q_logits_dev"] if T > 0 else None,
@@ -264,6 +320,59 @@ def test_verify_edge_cases(B, orc):
     assert gv["status"] == -6 and (gv["n_acc"] == -1).all()
 
 
+def _empty_residual_case(R=16, V=1032):
+    """Rows whose residual max(0, p - q) is empty in floating point although a
+    rejection is likely.  Drafter row: 1024 zeros, the drafted token y at -40,
+    seven entries at -inf; target row: the same but -41 at y, so p(y)/q(y) =
+    1/e (rejected when u >= 0.37).  Both log-normalisers round to ln 1024 (the
+    mass at y is 1e-18 of the total), so p == q on every other entry, in double
+    and in fp32 alike: the exact residual mass, (q(y) - p(y)) ~ 3e-21, is far
+    below either precision."""
+    s = np.zeros(V, np.float32)
+    s[1024] = -40.0
+    s[1025:] = -np.inf
+    t = s.copy()
+    t[1024] = -41.0
+    g = np.random.default_rng(11)
+    target = np.zeros((2 * R, V), np.float32)
+    target[0::2] = t
+    target[1::2] = 3.0 * g.standard_normal((R, V)).astype(np.float32)  # bonus rows
+    cu = inputs.cu_from_lengths(np.ones(R, np.int32))
+    y = np.full((R, 1), 1024, np.int32)
+    q_logits = np.broadcast_to(s, (R, 1, V)).copy()
+    return s, target, cu, y, q_logits
+
+
+def test_empty_residual_fallback(B, orc):
+    """The empty-residual branch (a rejection whose max(0, p - q) has no mass in
+    the working precision draws from p with the residual's noise): the oracle
+    takes it on these rows, and both GPU verify paths -- stored drafter logits
+    (dspark_verify) and recomputed ones (dspark_verify_markov: zero factors,
+    anchor -1, so the recomputed logits are U itself) -- commit the same tokens."""
+    R, V = 16, 1032
+    s, target, cu, y, q_logits = _empty_residual_case(R, V)
+    seeds = inputs.request_seeds(0x5EED0100, R)
+    lse = orc.logsumexp(s.astype(np.float64))
+    q_lse = np.full((R, 1), np.float32(lse), np.float32)
+    q_tok = np.full((R, 1), np.float32(np.exp(-40.0 - lse)), np.float32)
+    zeros_w = np.zeros((V, 64), np.uint16)
+    d = dict(U=inputs.bf16_bits(q_logits), W1=zeros_w, W2=zeros_w, anchor=np.full(R, -1, np.int32),
+             seeds=seeds)
+    tally = H.Tally()
+    empties = 0
+    for cycle in range(3):
+        ov = orc.verify(target, cu, y, q_logits.astype(np.float64), seeds, cycle, 1.0)
+        empties += int(ov["residual_empty"].sum())
+        gv = H.gpu_verify(target, cu, y, q_logits, q_lse, q_tok, seeds, cycle, 1.0)
+        g = dict(y_dev=H.dev(y), q_lse_dev=H.dev(q_lse), q_tok_dev=H.dev(q_tok))
+        gm = H.gpu_verify_markov(target, cu, d, g, cycle, 1.0)
+        assert gv["status"] == 0 and gm["status"] == 0
+        H.compare_verify(tally, gv, ov, np.ones(R, np.int32))
+        H.compare_verify(tally, gm, ov, np.ones(R, np.int32))
+    tally.check()
+    assert empties >= 10, empties  # about 63% of 48 draws are rejections
+
+
 # ------------------------------------------------------------------ select / commit
 @pytest.mark.parametrize("mode", [0, 1, 2, 3])
 @pytest.mark.parametrize("R,gamma,seed", [(512, 5, 0), (3, 3, 1), (97, 7, 2), (1000, 8, 3)])
@@ -320,15 +429,26 @@ def test_commit_parity(B, orc):
 
 # ------------------------------------------------------------------ full-size workloads
 FULL = [
-    ("qwen3_8b_greedy", 4, [0, 7, 15]),
-    ("batched_sampling", 1, [0, 77, 127]),
-    ("varlen_verify", 1, None),
-    ("confidence_scheduled", 1, [0, 300, 511]),
+    ("qwen3_8b_greedy", 4),
+    ("batched_sampling", 2),
+    ("varlen_verify", 1),
+    ("confidence_scheduled", 1),
 ]
 
 
-@pytest.mark.parametrize("name,cycles,sample", FULL)
-def test_full_size_cycle_sampled(B, orc, name, cycles, sample):
+def _sample_rows(R, cycle, l, n=8):
+    """n requests replayed on the oracle, drawn afresh each cycle, always with
+    the first and last request and, for variable lengths, the shortest and
+    longest verify length."""
+    g = np.random.default_rng(1000 + cycle)
+    rows = {0, R - 1, int(np.argmin(l)), int(np.argmax(l))}
+    rest = [r for r in g.permutation(R) if r not in rows]
+    rows.update(int(r) for r in rest[: max(0, n - len(rows))])
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("name,cycles", FULL)
+def test_full_size_cycle_sampled(B, orc, name, cycles):
     w, d = H.cycle_inputs(name)
     T = float(w["temperature"])
     full = inputs.target_full(w, d["U"])
@@ -350,9 +470,7 @@ def test_full_size_cycle_sampled(B, orc, name, cycles, sample):
                           g["q_lse_dev"] if T > 0 else None, g["q_tok_dev"] if T > 0 else None,
                           H.dev(d["seeds"]) if T > 0 else None, cycle, T)
         assert g["status"] == 0 and gv["status"] == 0
-        rows = sample
-        if rows is None:  # include the shortest and longest verify lengths
-            rows = sorted({int(np.argmin(l)), int(np.argmax(l)), R // 2})
+        rows = _sample_rows(R, cycle, l)
         sub = dict(U=d["U"][rows], anchor=d["anchor"][rows], seeds=d["seeds"][rows])
         o = orc.markov_draft(sub["U"], d["W1"], d["W2"], sub["anchor"], sub["seeds"], cycle, T,
                              req_ids=rows)

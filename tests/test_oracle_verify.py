@@ -237,3 +237,53 @@ def test_variable_lengths_and_bad_inputs(orc):
     assert vb["n_acc"][1] == -1
     if l[3] > 0:
         assert vb["n_acc"][3] == -1
+
+
+def test_empty_residual_falls_back_to_target(orc):
+    """The empty-residual branch (reading: when max(0, p - q) has no mass in the
+    working precision after a rejection, the token is drawn from p with the
+    residual's noise).  With exactly normalised p and q a rejection always
+    leaves positive residual mass, so only rounding can reach this branch; these
+    rows reach it.  Drafter row: 1024 zeros, the drafted token y at -40, seven
+    entries at -inf; target row the same with -41 at y, so p(y)/q(y) = 1/e.  The
+    true residual mass, q(y) - p(y) ~ (e^-40 - e^-41)/1024 ~ 2.6e-21, is below
+    the resolution of ln(1024 + e^-40) in double, so the oracle's p and q agree
+    bit for bit everywhere but y and its residual is empty."""
+    V, y_tok = 1032, 1024
+    s = np.zeros(V, np.float64)
+    s[y_tok] = -40.0
+    s[y_tok + 1:] = -np.inf
+    t = s.copy()
+    t[y_tok] = -41.0
+    p, q = orc.softmax(t), orc.softmax(s)
+    mask = np.arange(V) != y_tok
+    np.testing.assert_array_equal(p[mask], q[mask])
+    assert p[y_tok] < q[y_tok]
+    exact_mass = (np.exp(-40.0) - np.exp(-41.0)) / 1024.0
+    assert exact_mass > 0.0
+    assert orc.residual_weights(p, q)[1] == 0.0
+
+    target = np.stack([t, np.zeros(V)]).astype(np.float32)  # row 1: the bonus row
+    cu = np.array([0, 2], np.int32)
+    ql = s[None, None, :]
+    seeds = np.array([0x5EED0042], np.uint64)
+    rejections = distinct = 0
+    for cycle in range(40):
+        v = orc.verify(target, cu, np.array([[y_tok]], np.int32), ql, seeds, cycle, 1.0)
+        u0 = orc.uniform_single(int(seeds[0]), cycle, 1, 0, 0)
+        assert v["n_acc"][0] == (1 if u0 < np.exp(-1.0) else 0)
+        if v["n_acc"][0] == 1:
+            continue
+        rejections += 1
+        assert v["residual_empty"][0] == 1
+        # the token is the Gumbel-max draw from p with the residual's noise
+        # (purpose 2 at the rejected position), not the bonus noise (purpose 3)
+        g2 = np.array([-np.log(-np.log(orc.uniform_vocab(int(seeds[0]), cycle, 2, 0, 0, j)))
+                       for j in range(V)])
+        g3 = np.array([-np.log(-np.log(orc.uniform_vocab(int(seeds[0]), cycle, 3, 0, 0, j)))
+                       for j in range(V)])
+        assert v["out_tokens"][0, 0] == int(np.argmax(t + g2))
+        distinct += int(np.argmax(t + g2)) != int(np.argmax(t + g3))
+        assert v["out_tokens"][0, 1] == -1
+    assert rejections >= 15, rejections
+    assert distinct >= rejections - 1  # the two noises almost never pick the same token

@@ -63,13 +63,18 @@ def _verify_both(B, target, cu, g, seeds, cycle, T, max_rows):
 
 
 def test_static_scratch_matches_workspace_verify_twice(B):
-    for call, (seed, varlen, T) in enumerate([(0, False, 0.7), (1, True, 1.0)]):
+    # two sampling calls in a row, then a greedy one (which writes its tokens
+    # from the decision pass and skips the draw kernel) on the array the
+    # sampling calls left behind
+    for call, (seed, varlen, T) in enumerate([(0, False, 0.7), (1, True, 1.0), (2, True, 0.0)]):
         w, d, target, cu, rows = _case(seed, varlen)
         g = H.gpu_draft(d, T, call)
         ref, got = _verify_both(B, target, cu, g, H.dev(d["seeds"]), call, T, rows)
         assert ref["status"] == 0 and got["status"] == 0
         np.testing.assert_array_equal(got["n_acc"], ref["n_acc"])
         np.testing.assert_array_equal(got["out"], ref["out"])
+        if T == 0:
+            assert set(np.unique(got["p_tok"][~np.isnan(got["p_tok"])])) <= {0.0, 1.0}
         examined = ~np.isnan(ref["p_tok"])
         np.testing.assert_array_equal(examined, ~np.isnan(got["p_tok"]))
         np.testing.assert_allclose(got["p_tok"][examined], ref["p_tok"][examined], rtol=0, atol=H.PROB_TOL)
@@ -79,8 +84,12 @@ def test_static_scratch_matches_workspace_verify_twice(B):
 def test_static_scratch_rejects_oversized_requests(B):
     L = B.library()
     fake = ctypes.c_void_p(256)
-    # 4096 requests of 7 drafts over a 151936-entry vocabulary need far more than 2 MiB
+    # 4096 requests of 7 drafts over a 151936-entry vocabulary need far more than 4 MiB
     st = L.dspark_verify_static_scratch(fake, fake, fake, fake, fake, fake, fake, 0, 1.0, 4096, 7,
                                         151936, 4096 * 8, fake, fake, None, None, None)
     assert st == B.DSPARK_ERR_CAPACITY
-    assert B.dspark_workspace_size(B.DSPARK_OP_VERIFY, 4096, 7, 151936, 0, 4096 * 8) > 2 * 1024 * 1024
+    assert B.dspark_workspace_size(B.DSPARK_OP_VERIFY, 4096, 7, 151936, 0, 4096 * 8) > 4 * 1024 * 1024
+    # the largest batches that fit: 772 requests at V = 151936, 905 at V = 129280
+    for R, V in ((772, 151936), (905, 129280)):
+        assert B.dspark_workspace_size(B.DSPARK_OP_VERIFY, R, 7, V, 0, R * 8) <= 4 * 1024 * 1024
+        assert B.dspark_workspace_size(B.DSPARK_OP_VERIFY, R + 1, 7, V, 0, (R + 1) * 8) > 4 * 1024 * 1024
