@@ -97,11 +97,19 @@ typedef struct CUstream_st* dspark_stream_t;
                                       only to study the planner                       */
 #define DSPARK_SELECT_FIRST_STOP 3 /* the theoretical greedy of section 9: add the best
                                       remaining candidate while Theta strictly grows  */
+#define DSPARK_SELECT_CONF_CUTOFF 4     /* static per-request cutoff on the per-position
+                                           confidence: positions before the request's first
+                                           c[r][k] < conf_min (llama.cpp PR 25173's conf_min
+                                           pruning; the Strata plan's first milestone)     */
+#define DSPARK_SELECT_SURVIVAL_CUTOFF 5 /* static per-request cutoff on the survival:
+                                           positions with a[r][k] >= conf_min (the fixed
+                                           per-request threshold section 9 compares with)   */
 
 /* Static text for a status code. */
 const char* dspark_status_string(int status);
 
-/* Library version, major * 10000 + minor * 100 + patch. */
+/* Library version, major * 10000 + minor * 100 + patch (1.1.0: cutoff modes,
+ * conf_min in dspark_select_prefix, dspark_plan_cycles, the wait settings). */
 int dspark_version(void);
 
 /* Bytes of workspace one call of `op` needs for these sizes (0 on bad
@@ -316,19 +324,53 @@ unsigned dspark_set_fault_injection(unsigned mask);
  *       sps_S * (R + sum of the n_S best a_plan), n_S = min(min(S, K_cap) - R, R*gamma),
  *       ties to the smaller S; a_plan from c_hist (HISTORY) or c (CURRENT)
  *   n = the first-stop greedy of section 9, at most K_cap - R         (FIRST_STOP)
+ *   n = min(eligible, K_cap - R), the n best eligible candidates in the order above,
+ *       where request r is eligible up to its first position k with
+ *       c[r][k] < conf_min (CONF_CUTOFF) or a[r][k] < conf_min (SURVIVAL_CUTOFF)
  *   l[r] = selected positions of request r; cu_seqlens[r+1] = cu_seqlens[r] + l[r] + 1
  *   K_used[0] = R + n (the physical rows the verify step will see)
  *
  *   c, c_hist    [R, gamma] fp32 in [0, 1]; c_hist may be NULL except in HISTORY mode
- *   capture_sizes [n_steps] int32, sps [n_steps] fp32 (unused in FIXED mode)
+ *   capture_sizes [n_steps] int32, sps [n_steps] fp32 (read by HISTORY, CURRENT and
+ *                FIRST_STOP only)
+ *   conf_min     the cutoff of the two cutoff modes (not NaN; ignored otherwise)
  *   a [R, gamma] fp32 out; l [R], cu_seqlens [R + 1], K_used [1] int32 out
  * Limits: R * gamma <= 8192, n_steps <= 64.
  */
 int dspark_select_prefix(const float* c, const float* c_hist, const int32_t* capture_sizes,
-                         const float* sps, int n_steps, int K_cap, int mode, int R, int gamma,
-                         float* a, int32_t* l, int32_t* cu_seqlens, int32_t* K_used,
+                         const float* sps, int n_steps, int K_cap, int mode, float conf_min, int R,
+                         int gamma, float* a, int32_t* l, int32_t* cu_seqlens, int32_t* K_used,
                          void* ws, size_t ws_bytes, int32_t* dev_status,
                          dspark_stream_t stream);
+
+/*
+ * dspark_plan_cycles -- the scheduler over a run of consecutive cycles
+ * (explainer section 10: the physical capacity of cycle t is planned on the
+ * confidences of cycle t - lag, two steps back in the paper's implementation,
+ * while the top of cycle t's own survival fills it; section 15: watch the
+ * verify work wasted after first rejections).  One launch, one CTA per cycle.
+ *
+ * Cycle t runs dspark_select_prefix's selection on c_seq[t] in `mode`; in
+ * HISTORY mode its c_hist is c_seq[t - lag], and the first lag cycles (no
+ * history yet) use the capacity K_cap.  n_full[t][r] is how many leading
+ * drafts of request r the target would accept in cycle t (so the cycle accepts
+ * n_acc[r] = min(n_full[t][r], l[r])).  With B = K_used[t] and SPS the step
+ * rate of the smallest capture size >= B (0 if none):
+ *   stats[t][0] = SPS * (R + sum of the selected a)      predicted Theta
+ *   stats[t][1] = SPS * (R + sum_r n_acc[r])             achieved Theta (tokens/s)
+ *   stats[t][2] = sum_r n_acc[r]                         accepted drafts
+ *   stats[t][3] = sum_r (l[r] - n_acc[r])                wasted verify rows
+ * (stats[t][1..3] are 0 when n_full is NULL).
+ *
+ *   c_seq [n_cycles, R, gamma] fp32; n_full [n_cycles, R] int32 or NULL
+ *   capture_sizes [n_steps] int32, sps [n_steps] fp32 (always read)
+ *   l_seq [n_cycles, R] int32 out, K_seq [n_cycles] int32 out, stats [n_cycles, 4] fp64 out
+ * Limits as dspark_select_prefix; lag >= 1; n_cycles <= 2^20.
+ */
+int dspark_plan_cycles(const float* c_seq, const int32_t* n_full, const int32_t* capture_sizes,
+                       const float* sps, int n_steps, int K_cap, int mode, float conf_min, int lag,
+                       int n_cycles, int R, int gamma, int32_t* l_seq, int32_t* K_seq, double* stats,
+                       int32_t* dev_status, dspark_stream_t stream);
 
 /*
  * dspark_commit_lengths -- per-request commit and rollback counts

@@ -33,6 +33,7 @@ _lib = None
 F32, BF16 = 0, 1
 PURPOSE_DRAFT, PURPOSE_ACCEPT, PURPOSE_RESIDUAL, PURPOSE_BONUS = 0, 1, 2, 3
 MODE_FIXED, MODE_HISTORY, MODE_CURRENT, MODE_FIRST_STOP = 0, 1, 2, 3
+MODE_CONF_CUTOFF, MODE_SURVIVAL_CUTOFF = 4, 5
 
 
 def build(force: bool = False) -> str:
@@ -81,9 +82,12 @@ def lib():
             L.orc_verify.argtypes = [vp, vp, vp, vp, vp, vp, u32, f32, i32, i32, i32,
                                      vp, vp, vp, vp, vp, vp]
             L.orc_verify.restype = i32
-            L.orc_select_prefix.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32,
+            L.orc_select_prefix.argtypes = [vp, vp, vp, vp, i32, i32, i32, f32, i32, i32,
                                             vp, vp, vp, vp, vp]
             L.orc_select_prefix.restype = i32
+            L.orc_plan_cycles.argtypes = [vp, vp, vp, vp, i32, i32, i32, f32, i32, i32, i32, i32,
+                                          vp, vp, vp, vp]
+            L.orc_plan_cycles.restype = i32
             L.orc_commit_lengths.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp]
             L.orc_commit_lengths.restype = i32
             _lib = L
@@ -210,7 +214,7 @@ def verify(target, cu_seqlens, y, q_logits, seeds, cycle, temperature, req_ids=N
                 sample_margin=sm, residual_empty=empty)
 
 
-def select_prefix(c, c_hist, capture_sizes, sps, K_cap, mode):
+def select_prefix(c, c_hist, capture_sizes, sps, K_cap, mode, conf_min=0.0):
     c = _c(c, np.float32)
     R, gamma = c.shape
     ch = None if c_hist is None else _c(c_hist, np.float32)
@@ -222,9 +226,27 @@ def select_prefix(c, c_hist, capture_sizes, sps, K_cap, mode):
     cu = np.zeros(R + 1, np.int32)
     K_used = np.zeros(1, np.int32)
     gap = np.zeros(1, np.float64)
-    st = lib().orc_select_prefix(_p(c), _p(ch), _p(cs), _p(sp), n_steps, K_cap, mode, R, gamma,
-                                 _p(a), _p(l), _p(cu), _p(K_used), _p(gap))
+    st = lib().orc_select_prefix(_p(c), _p(ch), _p(cs), _p(sp), n_steps, K_cap, mode, conf_min, R,
+                                 gamma, _p(a), _p(l), _p(cu), _p(K_used), _p(gap))
     return dict(status=st, a=a, l=l, cu_seqlens=cu, K_used=int(K_used[0]), theta_gap=float(gap[0]))
+
+
+def plan_cycles(c_seq, n_full, capture_sizes, sps, K_cap, mode, conf_min=0.0, lag=2):
+    """A run of scheduling cycles: c_seq [n_cycles, R, gamma] float32, n_full
+    [n_cycles, R] int32 (leading drafts the target would accept) or None."""
+    c_seq = _c(c_seq, np.float32)
+    T, R, gamma = c_seq.shape
+    nf = None if n_full is None else _c(n_full, np.int32)
+    cs = _c(capture_sizes, np.int32)
+    sp = _c(sps, np.float32)
+    l_seq = np.zeros((T, R), np.int32)
+    K_seq = np.zeros(T, np.int32)
+    stats = np.zeros((T, 4), np.float64)
+    gap = np.zeros(T, np.float64)
+    st = lib().orc_plan_cycles(_p(c_seq), _p(nf), _p(cs), _p(sp), cs.size, K_cap, mode, conf_min, lag,
+                               T, R, gamma, _p(l_seq), _p(K_seq), _p(stats), _p(gap))
+    return dict(status=st, l=l_seq, K_used=K_seq, theta_pred=stats[:, 0], theta_real=stats[:, 1],
+                accepted=stats[:, 2].astype(np.int64), wasted=stats[:, 3].astype(np.int64), theta_gap=gap)
 
 
 def commit_lengths(n_acc, l, gamma):

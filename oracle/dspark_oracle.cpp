@@ -406,17 +406,27 @@ int orc_verify(const float* target, const int32_t* cu_seqlens, const int32_t* y,
 //   mode 2 (current)   : as mode 1 on the current a (anticipating; kept for study)
 //   mode 3 (first stop): from n = 0, add the next candidate while Theta strictly
 //                        grows, B <= K_cap and a capture size >= B exists
+//   mode 4 (confidence cutoff): the static per-request cutoff of the llama.cpp
+//                        PR's confidence pruning (conf_min) and of the Strata
+//                        plan's first scheduling milestone: request r is
+//                        eligible up to its first position with c[r][k] < conf_min
+//   mode 5 (survival cutoff): eligible where a[r][k] >= conf_min (a fixed
+//                        per-request threshold on the survival, the baseline
+//                        [EXPL] section 9 compares the global scheduler with)
+//                        modes 4 and 5: n = min(eligible, K_cap - R), the n best
+//                        eligible candidates in the same order
 // The n best current candidates are selected; l[r] counts them per request;
 // cu_seqlens[r+1] = cu_seqlens[r] + l[r] + 1; K_used = R + n.
 // theta_gap receives the relative gap between the best and second-best Theta
 // of the capacity choice (modes 1-3; +inf when there is no alternative).
 int orc_select_prefix(const float* c, const float* c_hist, const int32_t* capture_sizes,
-                      const float* sps, int n_steps, int K_cap, int mode, int R, int gamma,
-                      float* a, int32_t* l, int32_t* cu_seqlens, int32_t* K_used,
+                      const float* sps, int n_steps, int K_cap, int mode, float conf_min, int R,
+                      int gamma, float* a, int32_t* l, int32_t* cu_seqlens, int32_t* K_used,
                       double* theta_gap) {
-    if (R <= 0 || gamma <= 0 || !c || mode < 0 || mode > 3) return ORC_INVALID;
+    if (R <= 0 || gamma <= 0 || !c || mode < 0 || mode > 5) return ORC_INVALID;
     if (mode == 1 && !c_hist) return ORC_INVALID;
-    if (mode != 0 && (n_steps <= 0 || !capture_sizes || !sps)) return ORC_INVALID;
+    if (mode >= 1 && mode <= 3 && (n_steps <= 0 || !capture_sizes || !sps)) return ORC_INVALID;
+    if (mode >= 4 && !(conf_min == conf_min)) return ORC_INVALID;  // NaN cutoff
     if (K_cap < R) return ORC_CAPACITY;
     for (int i = 0; i < R * gamma; ++i) {
         if (!(c[i] >= 0.0f && c[i] <= 1.0f)) return ORC_DEVICE_INPUT;
@@ -458,12 +468,29 @@ int orc_select_prefix(const float* c, const float* c_hist, const int32_t* captur
     };
 
     survival(c, a);
-    const std::vector<int> ord = ordered(a);
+    std::vector<int> ord = ordered(a);
     const int n_all = R * gamma;
     int n = 0;
     double gap = std::numeric_limits<double>::infinity();
 
-    if (mode == 0) {
+    if (mode == 4 || mode == 5) {
+        // eligible: each request's leading positions passing the cutoff; the
+        // selection keeps the order above, restricted to eligible candidates
+        std::vector<char> elig(n_all, 0);
+        int n_elig = 0;
+        for (int r = 0; r < R; ++r)
+            for (int k = 0; k < gamma; ++k) {
+                const float v = (mode == 4) ? c[(size_t)r * gamma + k] : a[(size_t)r * gamma + k];
+                if (!(v >= conf_min)) break;
+                elig[(size_t)r * gamma + k] = 1;
+                ++n_elig;
+            }
+        std::vector<int> kept;
+        for (int i : ord)
+            if (elig[i]) kept.push_back(i);
+        ord.swap(kept);
+        n = std::min(n_elig, K_cap - R);
+    } else if (mode == 0) {
         n = std::min(K_cap - R, n_all);
     } else if (mode == 1 || mode == 2) {
         std::vector<float> ah(n_all);
@@ -515,6 +542,73 @@ int orc_select_prefix(const float* c, const float* c_hist, const int32_t* captur
     if (K_used) *K_used = R + n;
     if (theta_gap) *theta_gap = gap;
     return ORC_OK;
+}
+
+// A run of consecutive scheduling cycles ([EXPL] section 10: the physical
+// capacity of cycle t comes from the confidences of cycle t - lag (two steps
+// back in the paper's implementation), the top-K of cycle t's own survival
+// fills it; section 15 lists the wasted verify work among the metrics to
+// watch).  Every cycle is one orc_select_prefix call on c_seq[t]; in HISTORY
+// mode its c_hist is c_seq[t - lag], and the first lag cycles, which have no
+// history yet, use the capacity K_cap (FIXED).  With n_full[t][r] = the number
+// of leading drafts of request r that the target would accept in cycle t (a
+// property of the drafts, independent of how many are verified), the cycle's
+// outcome is n_acc[r] = min(n_full[t][r], l[r]), and per cycle:
+//   stats[t][0] = SPS(Bpad) * (R + sum of the selected a)   predicted Theta
+//   stats[t][1] = SPS(Bpad) * (R + sum_r n_acc[r])          achieved Theta
+//   stats[t][2] = sum_r n_acc[r]                            accepted drafts
+//   stats[t][3] = sum_r (l[r] - n_acc[r])                   wasted verify rows
+// with B = K_used physical rows and Bpad the smallest capture size >= B (SPS
+// = 0 when none is; stats[t][1..3] are 0 without n_full).
+int orc_plan_cycles(const float* c_seq, const int32_t* n_full, const int32_t* capture_sizes,
+                    const float* sps, int n_steps, int K_cap, int mode, float conf_min, int lag,
+                    int n_cycles, int R, int gamma, int32_t* l_seq, int32_t* K_seq, double* stats,
+                    double* theta_gap) {
+    if (n_cycles <= 0 || lag < 1 || R <= 0 || gamma <= 0) return ORC_INVALID;
+    if (n_steps <= 0 || !capture_sizes || !sps) return ORC_INVALID;
+    std::vector<float> a((size_t)R * gamma);
+    std::vector<int32_t> cu(R + 1);
+    int status = ORC_OK;
+    for (int t = 0; t < n_cycles; ++t) {
+        const float* ct = c_seq + (size_t)t * R * gamma;
+        int m = mode;
+        const float* hist = nullptr;
+        if (mode == 1) {
+            if (t >= lag) hist = c_seq + (size_t)(t - lag) * R * gamma;
+            else m = 0;
+        }
+        int32_t K = 0;
+        double gap = 0.0;
+        int32_t* lt = l_seq + (size_t)t * R;
+        const int st = orc_select_prefix(ct, hist, capture_sizes, sps, n_steps, K_cap, m, conf_min, R,
+                                         gamma, a.data(), lt, cu.data(), &K, &gap);
+        if (theta_gap) theta_gap[t] = gap;
+        K_seq[t] = K;
+        double* out = stats + (size_t)t * 4;
+        out[0] = out[1] = out[2] = out[3] = 0.0;
+        if (st != ORC_OK) { status = st; continue; }
+        int best = -1;  // smallest capture size >= K
+        for (int i = 0; i < n_steps; ++i)
+            if (capture_sizes[i] >= K && (best < 0 || capture_sizes[i] < capture_sizes[best])) best = i;
+        const double rate = best < 0 ? 0.0 : (double)sps[best];
+        double sel = 0.0;
+        long acc = 0, wasted = 0;
+        for (int r = 0; r < R; ++r) {
+            for (int k = 0; k < lt[r]; ++k) sel += (double)a[(size_t)r * gamma + k];
+            if (n_full) {
+                const int na = std::min((int)n_full[(size_t)t * R + r], (int)lt[r]);
+                acc += na;
+                wasted += lt[r] - na;
+            }
+        }
+        out[0] = rate * ((double)R + sel);
+        if (n_full) {
+            out[1] = rate * ((double)R + (double)acc);
+            out[2] = (double)acc;
+            out[3] = (double)wasted;
+        }
+    }
+    return status;
 }
 
 // Commit lengths ([EXPL] section 2: each cycle commits the accepted prefix

@@ -30,12 +30,14 @@ DSPARK_F32, DSPARK_BF16 = 0, 1
 DSPARK_OP_DRAFT, DSPARK_OP_VERIFY, DSPARK_OP_SELECT, DSPARK_OP_VERIFY_MARKOV = 0, 1, 2, 3
 DSPARK_DRAFT_FORCE_SIMT = 1
 DSPARK_SELECT_FIXED, DSPARK_SELECT_HISTORY, DSPARK_SELECT_CURRENT, DSPARK_SELECT_FIRST_STOP = 0, 1, 2, 3
+DSPARK_SELECT_CONF_CUTOFF, DSPARK_SELECT_SURVIVAL_CUTOFF = 4, 5
 DSPARK_INJECT_VERIFY_BARRIER, DSPARK_INJECT_DRAFT_BARRIER = 1, 2
 
 EXPORTED = ["dspark_status_string", "dspark_version", "dspark_workspace_size", "dspark_philox4x32_10",
             "dspark_markov_draft_uses_tensor_cores", "dspark_markov_draft", "dspark_verify",
             "dspark_select_prefix", "dspark_commit_lengths", "dspark_verify_static_scratch",
-            "dspark_verify_markov", "dspark_set_wait_limit_ns", "dspark_set_fault_injection"]
+            "dspark_verify_markov", "dspark_set_wait_limit_ns", "dspark_set_fault_injection",
+            "dspark_plan_cycles"]
 
 
 class DSparkError(RuntimeError):
@@ -63,9 +65,12 @@ def _load():
     L.dspark_verify.argtypes = [vp, vp, vp, vp, vp, vp, vp, u32, f32, i32, i32, i32, i32,
                                 vp, vp, vp, vp, sz, vp, vp]
     L.dspark_verify.restype = i32
-    L.dspark_select_prefix.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp,
+    L.dspark_select_prefix.argtypes = [vp, vp, vp, vp, i32, i32, i32, f32, i32, i32, vp, vp, vp, vp,
                                        vp, sz, vp, vp]
     L.dspark_select_prefix.restype = i32
+    L.dspark_plan_cycles.argtypes = [vp, vp, vp, vp, i32, i32, i32, f32, i32, i32, i32, i32, vp, vp, vp,
+                                     vp, vp]
+    L.dspark_plan_cycles.restype = i32
     L.dspark_verify_markov.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, u32, f32, i32, i32,
                                        i32, i32, vp, vp, vp, vp, sz, vp, vp]
     L.dspark_verify_markov.restype = i32
@@ -279,7 +284,7 @@ def dspark_verify_static_scratch(target_logits, cu_seqlens, draft_tokens, q_logi
 
 
 def dspark_select_prefix(c, c_hist, capture_sizes, sps, K_cap, mode, a, l, cu_seqlens, K_used,
-                         ws=None, dev_status=None, stream=None):
+                         ws=None, dev_status=None, stream=None, conf_min=0.0):
     R, gamma = c.shape
     _check(c, "c", torch.float32)
     _check(c_hist, "c_hist", torch.float32, (R, gamma), allow_none=True)
@@ -294,10 +299,27 @@ def dspark_select_prefix(c, c_hist, capture_sizes, sps, K_cap, mode, a, l, cu_se
     if sps is not None and sps.numel() != n_steps:
         raise ValueError("sps and capture_sizes differ in length")
     st = _L.dspark_select_prefix(_ptr(c), _ptr(c_hist), _ptr(capture_sizes), _ptr(sps), n_steps,
-                                 int(K_cap), int(mode), R, gamma, _ptr(a), _ptr(l),
+                                 int(K_cap), int(mode), float(conf_min), R, gamma, _ptr(a), _ptr(l),
                                  _ptr(cu_seqlens), _ptr(K_used), _ptr(ws),
                                  0 if ws is None else ws.numel(), _ptr(dev_status), _stream(stream))
     _raise("dspark_select_prefix", st)
+
+
+def dspark_plan_cycles(c_seq, n_full, capture_sizes, sps, K_cap, mode, l_seq, K_seq, stats, conf_min=0.0,
+                       lag=2, dev_status=None, stream=None):
+    T, R, gamma = c_seq.shape
+    _check(c_seq, "c_seq", torch.float32)
+    _check(n_full, "n_full", torch.int32, (T, R), allow_none=True)
+    _check(capture_sizes, "capture_sizes", torch.int32)
+    _check(sps, "sps", torch.float32, (capture_sizes.numel(),))
+    _check(l_seq, "l_seq", torch.int32, (T, R))
+    _check(K_seq, "K_seq", torch.int32, (T,))
+    _check(stats, "stats", torch.float64, (T, 4))
+    _check(dev_status, "dev_status", torch.int32, allow_none=True)
+    st = _L.dspark_plan_cycles(_ptr(c_seq), _ptr(n_full), _ptr(capture_sizes), _ptr(sps), capture_sizes.numel(),
+                               int(K_cap), int(mode), float(conf_min), int(lag), T, R, gamma, _ptr(l_seq),
+                               _ptr(K_seq), _ptr(stats), _ptr(dev_status), _stream(stream))
+    _raise("dspark_plan_cycles", st)
 
 
 def dspark_philox4x32_10(ctr, keys, out, stream=None):

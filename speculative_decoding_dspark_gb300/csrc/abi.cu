@@ -108,7 +108,7 @@ const char* dspark_status_string(int status) {
     }
 }
 
-int dspark_version(void) { return 100; }
+int dspark_version(void) { return 10100; }
 
 int dspark_markov_draft_uses_tensor_cores(int u_dtype, int w_dtype, int R, int V, int rank,
                                           unsigned flags) {
@@ -286,26 +286,47 @@ int dspark_verify_markov(const float* target_logits, const int32_t* cu_seqlens,
 }
 
 int dspark_select_prefix(const float* c, const float* c_hist, const int32_t* capture_sizes,
-                         const float* sps, int n_steps, int K_cap, int mode, int R, int gamma,
-                         float* a, int32_t* l, int32_t* cu_seqlens, int32_t* K_used,
+                         const float* sps, int n_steps, int K_cap, int mode, float conf_min, int R,
+                         int gamma, float* a, int32_t* l, int32_t* cu_seqlens, int32_t* K_used,
                          void* ws, size_t ws_bytes, int32_t* dev_status,
                          dspark_stream_t stream) {
     (void)ws; (void)ws_bytes;
     if (!c || !a || !l || !cu_seqlens || !K_used) return DSPARK_ERR_INVALID_ARG;
     if (R <= 0 || gamma <= 0 || gamma > 16) return DSPARK_ERR_INVALID_ARG;
-    if (mode < DSPARK_SELECT_FIXED || mode > DSPARK_SELECT_FIRST_STOP) return DSPARK_ERR_INVALID_ARG;
+    if (mode < DSPARK_SELECT_FIXED || mode > DSPARK_SELECT_SURVIVAL_CUTOFF) return DSPARK_ERR_INVALID_ARG;
     if (mode == DSPARK_SELECT_HISTORY && !c_hist) return DSPARK_ERR_INVALID_ARG;
-    if (mode != DSPARK_SELECT_FIXED &&
-        (n_steps <= 0 || n_steps > kSelectMaxSteps || !capture_sizes || !sps))
+    const bool planned = mode >= DSPARK_SELECT_HISTORY && mode <= DSPARK_SELECT_FIRST_STOP;
+    if (planned && (n_steps <= 0 || n_steps > kSelectMaxSteps || !capture_sizes || !sps))
         return DSPARK_ERR_INVALID_ARG;
+    if (mode >= DSPARK_SELECT_CONF_CUTOFF && !(conf_min == conf_min)) return DSPARK_ERR_INVALID_ARG;
     if ((long long)R * gamma > kSelectMaxItems) return DSPARK_ERR_UNSUPPORTED;
     if (K_cap < R) return DSPARK_ERR_CAPACITY;
     SelectParams p;
     p.c = c; p.c_hist = c_hist; p.capture_sizes = capture_sizes; p.sps = sps;
-    p.n_steps = mode == DSPARK_SELECT_FIXED ? 0 : n_steps;
-    p.K_cap = K_cap; p.mode = mode; p.R = R; p.gamma = gamma;
+    p.n_steps = planned ? n_steps : 0;
+    p.K_cap = K_cap; p.mode = mode; p.R = R; p.gamma = gamma; p.conf_min = conf_min;
     p.a = a; p.l = l; p.cu = cu_seqlens; p.K_used = K_used; p.dev_status = dev_status;
     return cuda_status(launch_select(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dspark_plan_cycles(const float* c_seq, const int32_t* n_full, const int32_t* capture_sizes,
+                       const float* sps, int n_steps, int K_cap, int mode, float conf_min, int lag,
+                       int n_cycles, int R, int gamma, int32_t* l_seq, int32_t* K_seq, double* stats,
+                       int32_t* dev_status, dspark_stream_t stream) {
+    if (!c_seq || !capture_sizes || !sps || !l_seq || !K_seq || !stats) return DSPARK_ERR_INVALID_ARG;
+    if (R <= 0 || gamma <= 0 || gamma > 16 || n_cycles <= 0 || lag < 1) return DSPARK_ERR_INVALID_ARG;
+    if (n_cycles > (1 << 20)) return DSPARK_ERR_UNSUPPORTED;
+    if (mode < DSPARK_SELECT_FIXED || mode > DSPARK_SELECT_SURVIVAL_CUTOFF) return DSPARK_ERR_INVALID_ARG;
+    if (n_steps <= 0 || n_steps > kSelectMaxSteps) return DSPARK_ERR_INVALID_ARG;
+    if (mode >= DSPARK_SELECT_CONF_CUTOFF && !(conf_min == conf_min)) return DSPARK_ERR_INVALID_ARG;
+    if ((long long)R * gamma > kSelectMaxItems) return DSPARK_ERR_UNSUPPORTED;
+    if (K_cap < R) return DSPARK_ERR_CAPACITY;
+    SelectParams p;
+    p.c = c_seq; p.c_hist = nullptr; p.capture_sizes = capture_sizes; p.sps = sps;
+    p.n_steps = n_steps; p.K_cap = K_cap; p.mode = mode; p.R = R; p.gamma = gamma; p.conf_min = conf_min;
+    p.a = nullptr; p.l = l_seq; p.cu = nullptr; p.K_used = K_seq; p.dev_status = dev_status;
+    p.lag = lag; p.n_full = n_full; p.stats = stats;
+    return cuda_status(launch_plan(p, n_cycles, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int dspark_philox4x32_10(const uint32_t* ctr, const uint64_t* keys, int n, uint32_t* out,

@@ -134,19 +134,25 @@ constexpr int kSelectMaxItems = 8192;
 constexpr int kSelectMaxSteps = 64;
 
 struct SelectParams {
-    const float* c;
+    const float* c;              // plan: c_seq [n_cycles, R, gamma]
     const float* c_hist;
     const int32_t* capture_sizes;
     const float* sps;
     int n_steps, K_cap, mode, R, gamma;
+    float conf_min;              // the cutoff modes' threshold
     float* a;
-    int32_t* l;
+    int32_t* l;                  // plan: [n_cycles, R]
     int32_t* cu;
-    int32_t* K_used;
+    int32_t* K_used;             // plan: [n_cycles]
     int32_t* dev_status;
+    // plan only
+    int lag = 0;
+    const int32_t* n_full = nullptr;  // [n_cycles, R] or NULL
+    double* stats = nullptr;          // [n_cycles, 4]
 };
 
 cudaError_t launch_select(const SelectParams& p, cudaStream_t stream);
+cudaError_t launch_plan(const SelectParams& p, int n_cycles, cudaStream_t stream);
 
 cudaError_t launch_philox_batch(const uint32_t* ctr, const uint64_t* keys, int n, uint32_t* out,
                                 cudaStream_t stream);

@@ -17,6 +17,12 @@
 //      a keep position-then-request order and every top-n set is prefix-closed;
 //   3. an inclusive fp64 scan of the sorted a gives sum-of-best-n for every n;
 //   4. the capacity rule picks n; positions < n of the sorted list are chosen.
+// The static cutoffs (modes CONF_CUTOFF and SURVIVAL_CUTOFF) mark each
+// request's leading positions that pass the cutoff in the key's top bit, so
+// one more split pass sorts the eligible candidates first, in the same order.
+// dspark_plan_cycles runs the same selection for many cycles at once, one CTA
+// per cycle, with the capacity of cycle t planned on the confidences of cycle
+// t - lag, and scores each cycle against the drafts the target would accept.
 #include "kernels.cuh"
 
 namespace dspark {
@@ -82,7 +88,7 @@ __device__ __forceinline__ double block_exclusive_scan_d(double x, double* tot, 
 }
 
 struct SelectSmem {
-    uint32_t key[2][kSelectMaxItems];  // float bits of a (non-negative: order-preserving)
+    uint32_t key[2][kSelectMaxItems];  // float bits of a (non-negative: order-preserving); top bit: eligible
     uint16_t id[2][kSelectMaxItems];   // candidate id = k * R + r
     double prefix[kSelectMaxItems + 1];  // prefix[n] = sum of the n best a
     int l[kSelectMaxItems];
@@ -92,17 +98,25 @@ struct SelectSmem {
     double warp_d[33];
     int flag;
     int n_sel;
+    int n_elig;
 };
+
+constexpr uint32_t kEligible = 0x80000000u;
+
+__device__ __forceinline__ bool cutoff_mode(int mode) {
+    return mode == DSPARK_SELECT_CONF_CUTOFF || mode == DSPARK_SELECT_SURVIVAL_CUTOFF;
+}
 
 // Fill keys from confidences (computing the survival products), sort, scan.
 // Returns false if a confidence is outside [0, 1].  Leaves the sorted ids in
 // buffer 0 and prefix sums in sm.prefix.  Without do_sort (the selection takes
 // every candidate or none, so order does not matter) it stops after the
-// products.
+// products.  cutoff (a CONF_CUTOFF or SURVIVAL_CUTOFF mode, else 0) marks the
+// eligible candidates, counted in sm.n_elig, and sorts them first.
 __device__ bool survival_sort_scan(SelectSmem& sm, const float* c, float* a_out, int R, int gamma,
-                                   bool do_sort = true) {
+                                   bool do_sort = true, int cutoff = 0, float conf_min = 0.0f) {
     const int N = R * gamma;
-    if (threadIdx.x == 0) sm.flag = 0;
+    if (threadIdx.x == 0) { sm.flag = 0; sm.n_elig = 0; }
     __syncthreads();
     for (int r = threadIdx.x; r < R; r += kNT) {
         // the request's confidences, all loads in flight at once (gamma <= 16)
@@ -110,17 +124,23 @@ __device__ bool survival_sort_scan(SelectSmem& sm, const float* c, float* a_out,
 #pragma unroll
         for (int k = 0; k < 16; ++k) cv[k] = k < gamma ? c[(size_t)r * gamma + k] : 1.0f;
         float run = 1.0f;
+        bool elig = cutoff != 0;
+        int n_e = 0;
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
             if (k >= gamma) break;
             const float ck = cv[k];
             if (!(ck >= 0.0f && ck <= 1.0f)) atomicOr(&sm.flag, 1);
             run = (k == 0) ? ck : run * ck;
+            // a request stays eligible up to its first position failing the cutoff
+            elig = elig && ((cutoff == DSPARK_SELECT_CONF_CUTOFF ? ck : run) >= conf_min);
+            n_e += elig ? 1 : 0;
             const int idn = k * R + r;
-            sm.key[0][idn] = __float_as_uint(run);
+            sm.key[0][idn] = __float_as_uint(run) | (elig ? kEligible : 0u);
             sm.id[0][idn] = (uint16_t)idn;
             if (a_out) a_out[(size_t)r * gamma + k] = run;
         }
+        if (n_e) atomicAdd(&sm.n_elig, n_e);
     }
     __syncthreads();
     if (sm.flag) return false;
@@ -131,7 +151,8 @@ __device__ bool survival_sort_scan(SelectSmem& sm, const float* c, float* a_out,
     int src = 0;
     const int ipt = (N + kNT - 1) / kNT;
     const int lo = min(N, threadIdx.x * ipt), hi = min(N, lo + ipt);
-    for (int bit = 0; bit < 31; ++bit) {
+    const int n_bits = cutoff ? 32 : 31;
+    for (int bit = 0; bit < n_bits; ++bit) {
         int ones = 0;
         for (int i = lo; i < hi; ++i) ones += (sm.key[src][i] >> bit) & 1u;
         int total1;
@@ -147,33 +168,49 @@ __device__ bool survival_sort_scan(SelectSmem& sm, const float* c, float* a_out,
         __syncthreads();
         src ^= 1;
     }
-    // 31 passes: the result sits in buffer 1; move it to buffer 0
-    for (int i = threadIdx.x; i < N; i += kNT) {
-        sm.key[0][i] = sm.key[1][i];
-        sm.id[0][i] = sm.id[1][i];
+    // an odd number of passes leaves the result in buffer 1; move it to buffer 0
+    if (src == 1) {
+        for (int i = threadIdx.x; i < N; i += kNT) {
+            sm.key[0][i] = sm.key[1][i];
+            sm.id[0][i] = sm.id[1][i];
+        }
+        __syncthreads();
     }
-    __syncthreads();
     // inclusive prefix sums of the sorted a in fp64, blocked per thread
     double local = 0.0;
-    for (int i = lo; i < hi; ++i) local += (double)__uint_as_float(sm.key[0][i]);
+    for (int i = lo; i < hi; ++i) local += (double)__uint_as_float(sm.key[0][i] & ~kEligible);
     double tot;
     double run = block_exclusive_scan_d(local, &tot, sm.warp_d);
     if (threadIdx.x == 0) sm.prefix[0] = 0.0;
     for (int i = lo; i < hi; ++i) {
-        run += (double)__uint_as_float(sm.key[0][i]);
+        run += (double)__uint_as_float(sm.key[0][i] & ~kEligible);
         sm.prefix[i + 1] = run;
     }
     __syncthreads();
     return true;
 }
 
-__global__ void __launch_bounds__(kNT) select_kernel(SelectParams p) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    SelectSmem& sm = *reinterpret_cast<SelectSmem*>(smem_raw);
+// Where one selection reads and writes: the current and the planning
+// confidences, the mode, and the outputs (a and cu may be NULL).
+struct SelectIo {
+    const float* c;
+    const float* c_hist;
+    int mode;
+    float* a;
+    int32_t* l;
+    int32_t* cu;
+    int32_t* K_used;
+};
+
+// The selection of one cycle by the whole CTA.  Leaves each request's length
+// in sm.l and returns the number of selected candidates n, or -1 after
+// reporting a bad confidence (the outputs are then -1).
+__device__ int select_body(SelectSmem& sm, const SelectParams& p, const SelectIo& io, bool sizes_loaded) {
     const int R = p.R, gamma = p.gamma, N = R * gamma;
+    const int mode = io.mode;
 
     // capture sizes sorted ascending (with their step rates)
-    if (threadIdx.x == 0 && p.mode != DSPARK_SELECT_FIXED) {
+    if (!sizes_loaded && threadIdx.x == 0 && mode >= DSPARK_SELECT_HISTORY && mode <= DSPARK_SELECT_FIRST_STOP) {
         for (int i = 0; i < p.n_steps; ++i) { sm.cs[i] = p.capture_sizes[i]; sm.sp[i] = p.sps[i]; }
         for (int i = 1; i < p.n_steps; ++i)
             for (int j = i; j > 0 && sm.cs[j - 1] > sm.cs[j]; --j) {
@@ -185,14 +222,18 @@ __global__ void __launch_bounds__(kNT) select_kernel(SelectParams p) {
 
     bool good = true;
     int n = 0;
-    if (p.mode == DSPARK_SELECT_HISTORY) {
-        good = survival_sort_scan(sm, p.c_hist, nullptr, R, gamma);
+    if (mode == DSPARK_SELECT_HISTORY) {
+        good = survival_sort_scan(sm, io.c_hist, nullptr, R, gamma);
+    } else if (cutoff_mode(mode)) {
+        good = survival_sort_scan(sm, io.c, io.a, R, gamma, true, mode, p.conf_min);
     } else {
         const int n_fixed = min(p.K_cap - R, N);
-        const bool all_or_none = p.mode == DSPARK_SELECT_FIXED && (n_fixed == 0 || n_fixed == N);
-        good = survival_sort_scan(sm, p.c, p.a, R, gamma, !all_or_none);
+        const bool all_or_none = mode == DSPARK_SELECT_FIXED && (n_fixed == 0 || n_fixed == N);
+        good = survival_sort_scan(sm, io.c, io.a, R, gamma, !all_or_none);
     }
-    if (good && (p.mode == DSPARK_SELECT_HISTORY || p.mode == DSPARK_SELECT_CURRENT)) {
+    if (good && cutoff_mode(mode)) {
+        n = min(sm.n_elig, p.K_cap - R);
+    } else if (good && (mode == DSPARK_SELECT_HISTORY || mode == DSPARK_SELECT_CURRENT)) {
         if (threadIdx.x == 0) {
             double best = -1.0;
             int best_S = -1, best_n = 0;
@@ -207,8 +248,8 @@ __global__ void __launch_bounds__(kNT) select_kernel(SelectParams p) {
         }
         __syncthreads();
         n = sm.n_sel;
-        if (p.mode == DSPARK_SELECT_HISTORY) good = survival_sort_scan(sm, p.c, p.a, R, gamma, n != 0 && n != N);
-    } else if (good && p.mode == DSPARK_SELECT_FIRST_STOP) {
+        if (mode == DSPARK_SELECT_HISTORY) good = survival_sort_scan(sm, io.c, io.a, R, gamma, n != 0 && n != N);
+    } else if (good && mode == DSPARK_SELECT_FIRST_STOP) {
         // Theta(n) for every n in parallel; the answer is the first n whose
         // successor is not strictly better (or infeasible).
         if (threadIdx.x == 0) sm.n_sel = INT_MAX;
@@ -242,10 +283,11 @@ __global__ void __launch_bounds__(kNT) select_kernel(SelectParams p) {
     }
     __syncthreads();
     if (!good) {
-        for (int r = threadIdx.x; r < R; r += kNT) p.l[r] = -1;
-        for (int r = threadIdx.x; r <= R; r += kNT) p.cu[r] = -1;
-        if (threadIdx.x == 0) { p.K_used[0] = -1; report(p.dev_status, DSPARK_ERR_DEVICE_INPUT); }
-        return;
+        for (int r = threadIdx.x; r < R; r += kNT) io.l[r] = -1;
+        if (io.cu)
+            for (int r = threadIdx.x; r <= R; r += kNT) io.cu[r] = -1;
+        if (threadIdx.x == 0) { io.K_used[0] = -1; report(p.dev_status, DSPARK_ERR_DEVICE_INPUT); }
+        return -1;
     }
     for (int r = threadIdx.x; r < R; r += kNT) sm.l[r] = 0;
     __syncthreads();
@@ -259,11 +301,96 @@ __global__ void __launch_bounds__(kNT) select_kernel(SelectParams p) {
     int tot;
     int run = block_exclusive_scan(local, &tot, sm.warp_i);
     for (int r = lo; r < hi; ++r) {
-        p.l[r] = sm.l[r];
-        p.cu[r] = run;
+        io.l[r] = sm.l[r];
+        if (io.cu) io.cu[r] = run;
         run += sm.l[r] + 1;
     }
-    if (threadIdx.x == 0) { p.cu[R] = tot; p.K_used[0] = R + n; }
+    if (threadIdx.x == 0) {
+        if (io.cu) io.cu[R] = tot;
+        io.K_used[0] = R + n;
+    }
+    return n;
+}
+
+__global__ void __launch_bounds__(kNT) select_kernel(SelectParams p) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    SelectSmem& sm = *reinterpret_cast<SelectSmem*>(smem_raw);
+    SelectIo io;
+    io.c = p.c; io.c_hist = p.c_hist; io.mode = p.mode;
+    io.a = p.a; io.l = p.l; io.cu = p.cu; io.K_used = p.K_used;
+    select_body(sm, p, io, false);
+}
+
+// One cycle of a planning run per CTA (blockIdx.x = cycle t): the selection
+// of c_seq[t] (capacity from c_seq[t - lag] in HISTORY mode; K_cap in the
+// first lag cycles), then the cycle's predicted and achieved Theta, accepted
+// drafts and wasted verify rows.
+__global__ void __launch_bounds__(kNT) plan_kernel(SelectParams p) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    SelectSmem& sm = *reinterpret_cast<SelectSmem*>(smem_raw);
+    const int t = blockIdx.x;
+    const int R = p.R, gamma = p.gamma;
+    const size_t rg = (size_t)R * gamma;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < p.n_steps; ++i) { sm.cs[i] = p.capture_sizes[i]; sm.sp[i] = p.sps[i]; }
+        for (int i = 1; i < p.n_steps; ++i)
+            for (int j = i; j > 0 && sm.cs[j - 1] > sm.cs[j]; --j) {
+                const int tt = sm.cs[j]; sm.cs[j] = sm.cs[j - 1]; sm.cs[j - 1] = tt;
+                const float f = sm.sp[j]; sm.sp[j] = sm.sp[j - 1]; sm.sp[j - 1] = f;
+            }
+    }
+    __syncthreads();
+    SelectIo io;
+    io.c = p.c + (size_t)t * rg;
+    io.mode = p.mode;
+    io.c_hist = nullptr;
+    if (p.mode == DSPARK_SELECT_HISTORY) {
+        if (t >= p.lag) io.c_hist = p.c + (size_t)(t - p.lag) * rg;
+        else io.mode = DSPARK_SELECT_FIXED;
+    }
+    io.a = nullptr;
+    io.l = p.l + (size_t)t * R;
+    io.cu = nullptr;
+    io.K_used = p.K_used + t;
+    const int n = select_body(sm, p, io, true);
+    double* out = p.stats + (size_t)t * 4;
+    if (n < 0) {
+        if (threadIdx.x < 4) out[threadIdx.x] = 0.0;
+        return;
+    }
+    // selected survival and the target's verdicts, per request (a recomputed
+    // with the same sequential fp32 products)
+    double sel = 0.0;
+    int acc = 0, wasted = 0;
+    for (int r = threadIdx.x; r < R; r += kNT) {
+        const int lr = sm.l[r];
+        float run = 1.0f;
+        for (int k = 0; k < lr; ++k) {
+            const float ck = io.c[(size_t)r * gamma + k];
+            run = (k == 0) ? ck : run * ck;
+            sel += (double)run;
+        }
+        if (p.n_full) {
+            const int na = min(p.n_full[(size_t)t * R + r], lr);
+            acc += na;
+            wasted += lr - na;
+        }
+    }
+    double sel_tot;
+    block_exclusive_scan_d(sel, &sel_tot, sm.warp_d);
+    int acc_tot, wasted_tot;
+    block_exclusive_scan(acc, &acc_tot, sm.warp_i);
+    block_exclusive_scan(wasted, &wasted_tot, sm.warp_i);
+    if (threadIdx.x == 0) {
+        const int B = R + n;
+        double rate = 0.0;  // the smallest capture size >= B
+        for (int i = 0; i < p.n_steps; ++i)
+            if (sm.cs[i] >= B) { rate = (double)sm.sp[i]; break; }
+        out[0] = rate * ((double)R + sel_tot);
+        out[1] = p.n_full ? rate * ((double)R + (double)acc_tot) : 0.0;
+        out[2] = p.n_full ? (double)acc_tot : 0.0;
+        out[3] = p.n_full ? (double)wasted_tot : 0.0;
+    }
 }
 
 __global__ void __launch_bounds__(1024) commit_kernel(const int32_t* n_acc, const int32_t* l, int R,
@@ -310,6 +437,14 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
                                          (int)smem);
     if (e != cudaSuccess) return e;
     select_kernel<<<1, kNT, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_plan(const SelectParams& p, int n_cycles, cudaStream_t stream) {
+    const size_t smem = sizeof(SelectSmem);
+    cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    plan_kernel<<<n_cycles, kNT, smem, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -180,4 +180,23 @@ def confidence_inputs(w: dict) -> dict:
 
     sizes = np.asarray(w.get("capture_sizes", [64, 128, 256, 512, 1024]), np.int32)
     return dict(c=conf(8), c_hist=conf(9), capture_sizes=sizes, sps=sps_staircase(sizes),
+                K_cap=int(w.get("K_cap", R * (gamma + 1))), tau=tau)
+
+
+def confidence_sequence(w: dict, n_cycles: int) -> dict:
+    """Confidences of n_cycles consecutive cycles of the same R request slots
+    ([n_cycles, R, gamma], each cycle drawn from the workload's law) and, as the
+    synthetic stand-in for the target's verdicts, n_full [n_cycles, R]: how many
+    leading drafts the target accepts, drawn so that draft k survives with
+    probability c[t, r, k] given the ones before it (the confidences are
+    calibrated conditional acceptance rates)."""
+    R, gamma, seed = w["R"], w["gamma"], w["seed"]
+    tau = confidence_inputs(w)["tau"]
+    z = 1.0 + 1.5 * rng(seed, 10).standard_normal((n_cycles, R, gamma))
+    c = (1.0 / (1.0 + np.exp(-z / tau[None, None, :]))).astype(np.float32)
+    u = rng(seed, 11).random((n_cycles, R, gamma), dtype=np.float32)
+    ok = u < c
+    n_full = np.where(ok.all(axis=2), gamma, np.argmin(ok, axis=2)).astype(np.int32)
+    sizes = np.asarray(w.get("capture_sizes", [64, 128, 256, 512, 1024]), np.int32)
+    return dict(c=c, n_full=n_full, capture_sizes=sizes, sps=sps_staircase(sizes),
                 K_cap=int(w.get("K_cap", R * (gamma + 1))))

@@ -150,7 +150,7 @@ def gpu_verify_markov(target, cu, d, g, cycle, temperature, max_rows=None):
     return dict(n_acc=host(n_acc), out_tokens=host(out), p_tok=host(p_tok), status=int(status.item()))
 
 
-def gpu_select(c, c_hist, sizes, sps, K_cap, mode):
+def gpu_select(c, c_hist, sizes, sps, K_cap, mode, conf_min=0.0):
     R, gamma = c.shape
     G = Guarded()
     a = G.out((R, gamma), torch.float32, float("nan"))
@@ -160,11 +160,28 @@ def gpu_select(c, c_hist, sizes, sps, K_cap, mode):
     status = G.out((1,), torch.int32, 0)
     t = lambda x: None if x is None else dev(x)
     try:
-        B.dspark_select_prefix(dev(c), t(c_hist), t(sizes), t(sps), K_cap, mode, a, l, cu, K, None, status)
+        B.dspark_select_prefix(dev(c), t(c_hist), t(sizes), t(sps), K_cap, mode, a, l, cu, K, None, status,
+                               conf_min=conf_min)
     finally:
         torch.cuda.synchronize()
         G.check()
     return dict(a=host(a), l=host(l), cu_seqlens=host(cu), K_used=int(K.item()), status=int(status.item()))
+
+
+def gpu_plan(c_seq, n_full, sizes, sps, K_cap, mode, conf_min=0.0, lag=2):
+    T, R, gamma = c_seq.shape
+    G = Guarded()
+    l = G.out((T, R), torch.int32, -7)
+    K = G.out((T,), torch.int32, -7)
+    stats = G.out((T, 4), torch.float64, float("nan"))
+    status = G.out((1,), torch.int32, 0)
+    B.dspark_plan_cycles(dev(c_seq), None if n_full is None else dev(n_full), dev(sizes), dev(sps), K_cap, mode,
+                         l, K, stats, conf_min=conf_min, lag=lag, dev_status=status)
+    torch.cuda.synchronize()
+    G.check()
+    st = host(stats)
+    return dict(l=host(l), K_used=host(K), theta_pred=st[:, 0], theta_real=st[:, 1],
+                accepted=st[:, 2].astype(np.int64), wasted=st[:, 3].astype(np.int64), status=int(status.item()))
 
 
 def gpu_commit(n_acc, l, gamma):

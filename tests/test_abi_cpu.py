@@ -90,15 +90,33 @@ def test_host_argument_checks(lib):
 
     s = lib.dspark_select_prefix
     s.restype = ctypes.c_int
-    s.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+    s.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
                   ctypes.c_int, vp, vp, vp, vp, vp, ctypes.c_size_t, vp, vp]
-    base = [fake, None, None, None, 0, 16, 0, 4, 3, fake, fake, fake, fake, None, 0, None, None]
+    base = [fake, None, None, None, 0, 16, 0, 0.0, 4, 3, fake, fake, fake, fake, None, 0, None, None]
     a = list(base); a[5] = 3
     assert s(*a) == -3          # K_cap < R
     a = list(base); a[6] = 1
     assert s(*a) == -1          # history mode without c_hist
-    a = list(base); a[7] = 4096; a[8] = 3; a[5] = 1 << 20
+    a = list(base); a[8] = 4096; a[9] = 3; a[5] = 1 << 20
     assert s(*a) == -2          # more candidates than one CTA sorts
+    a = list(base); a[6] = 6
+    assert s(*a) == -1          # no such mode
+    a = list(base); a[6] = 4; a[7] = float("nan")
+    assert s(*a) == -1          # NaN cutoff
+
+    pc = lib.dspark_plan_cycles
+    pc.restype = ctypes.c_int
+    pc.argtypes = [vp] * 4 + [ctypes.c_int] * 3 + [ctypes.c_float] + [ctypes.c_int] * 4 + [vp] * 5
+    # c_seq, n_full, sizes, sps, n_steps, K_cap, mode, conf_min, lag, n_cycles, R, gamma, l, K, stats, status, stream
+    base = [fake, None, fake, fake, 5, 1024, 1, 0.0, 2, 100, 512, 5, fake, fake, fake, None, None]
+    a = list(base); a[8] = 0
+    assert pc(*a) == -1         # lag < 1
+    a = list(base); a[4] = 0
+    assert pc(*a) == -1         # no capture sizes
+    a = list(base); a[5] = 100
+    assert pc(*a) == -3         # K_cap < R
+    a = list(base); a[9] = 0
+    assert pc(*a) == -1         # no cycles
 
     v = lib.dspark_verify
     v.restype = ctypes.c_int

@@ -394,6 +394,45 @@ def test_select_parity(B, orc, mode, R, gamma, seed):
             assert g["K_used"] == o["K_used"]
 
 
+@pytest.mark.parametrize("mode", [4, 5])
+@pytest.mark.parametrize("R,gamma,seed", [(512, 5, 0), (3, 3, 1), (97, 7, 2), (1000, 8, 3)])
+def test_select_cutoff_parity(B, orc, mode, R, gamma, seed):
+    """The static cutoffs (per-position confidence, survival), with room for
+    every eligible row and with less: bit-exact a, l, cu_seqlens and K."""
+    w = inputs.workload("confidence_scheduled", seed_offset=seed, R=R, gamma=gamma)
+    c = inputs.confidence_inputs(w)["c"]
+    for conf_min in (0.0, 0.3, 0.6, 0.95):
+        for K_cap in sorted({R, R + (R * gamma) // 3, R * (gamma + 1)}):
+            o = orc.select_prefix(c, None, None, None, K_cap, mode, conf_min)
+            g = H.gpu_select(c, None, None, None, K_cap, mode, conf_min)
+            assert o["status"] == 0 and g["status"] == 0
+            np.testing.assert_array_equal(g["a"].view(np.uint32), o["a"].view(np.uint32))
+            np.testing.assert_array_equal(g["l"], o["l"])
+            np.testing.assert_array_equal(g["cu_seqlens"], o["cu_seqlens"])
+            assert g["K_used"] == o["K_used"]
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4, 5])
+def test_plan_cycles_parity(B, orc, mode):
+    """A run of 64 cycles of the confidence-scheduled workload (R = 512,
+    gamma = 5, K_cap = 1024), one CTA per cycle: lengths, capacities, accepted
+    drafts and wasted rows bit-exact (cycles whose capacity choice is a
+    rounding-level Theta tie exempt), Theta to fp64 rounding."""
+    w = inputs.workload("confidence_scheduled")
+    seq = inputs.confidence_sequence(w, 64)
+    o = orc.plan_cycles(seq["c"], seq["n_full"], seq["capture_sizes"], seq["sps"], seq["K_cap"], mode, 0.6)
+    g = H.gpu_plan(seq["c"], seq["n_full"], seq["capture_sizes"], seq["sps"], seq["K_cap"], mode, 0.6)
+    assert o["status"] == 0 and g["status"] == 0
+    keep = o["theta_gap"] > 1e-9
+    assert keep.mean() > 0.99
+    np.testing.assert_array_equal(g["l"][keep], o["l"][keep])
+    np.testing.assert_array_equal(g["K_used"][keep], o["K_used"][keep])
+    np.testing.assert_array_equal(g["accepted"][keep], o["accepted"][keep])
+    np.testing.assert_array_equal(g["wasted"][keep], o["wasted"][keep])
+    np.testing.assert_allclose(g["theta_pred"][keep], o["theta_pred"][keep], rtol=1e-12)
+    np.testing.assert_allclose(g["theta_real"][keep], o["theta_real"][keep], rtol=1e-12)
+
+
 def test_select_ties_and_errors(B, orc):
     c = np.array([[1.0, 1.0], [1.0, 0.5], [0.7, 0.7]], np.float32)
     for K_cap in range(3, 10):

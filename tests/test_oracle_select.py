@@ -154,3 +154,103 @@ def test_commit_lengths(orc):
     assert list(out["discard"]) == [5, 2, 0, 3]
     bad = orc.commit_lengths(np.array([4], np.int32), np.array([3], np.int32), 5)
     assert bad["status"] == -6
+
+
+def _brute_best_within(a, n, cap):
+    """max over prefix-closed sets of size n with l[r] <= cap[r] of sum(a)."""
+    R, gamma = a.shape
+    best = -1.0
+    for ls in itertools.product(*[range(int(c) + 1) for c in cap]):
+        if sum(ls) != n:
+            continue
+        best = max(best, sum(float(a[r, :ls[r]].astype(np.float64).sum()) for r in range(R)))
+    return best
+
+
+@pytest.mark.parametrize("mode", [4, 5])
+def test_cutoff_modes(orc, mode):
+    """Static per-request cutoffs (the llama.cpp PR's conf_min confidence
+    pruning on the per-position confidence, mode 4; a fixed threshold on the
+    survival, mode 5).  With room for every eligible row, l counts the leading
+    positions that pass (computed here with numpy); with less room, the kept
+    set is the best prefix-closed one inside the eligible prefixes (brute force)."""
+    for seed in range(3):
+        ci = _conf(40, 6, seed)
+        c = ci["c"]
+        a = np.cumprod(c, axis=1, dtype=np.float32)
+        for conf_min in (0.0, 0.3, 0.6, 0.9, 1.01):
+            v = c if mode == 4 else a
+            passed = v >= np.float32(conf_min)
+            expect = np.where(passed.all(axis=1), c.shape[1], np.argmin(passed, axis=1))
+            out = orc.select_prefix(c, None, None, None, 40 * 7, mode, conf_min)
+            assert out["status"] == 0
+            np.testing.assert_array_equal(out["l"], expect)
+            assert out["K_used"] == 40 + expect.sum()
+    R, gamma = 3, 3
+    for seed in range(4):
+        ci = _conf(R, gamma, seed)
+        c, a = ci["c"], np.cumprod(ci["c"], axis=1, dtype=np.float32)
+        for conf_min in (0.2, 0.5):
+            v = c if mode == 4 else a
+            passed = v >= np.float32(conf_min)
+            cap = np.where(passed.all(axis=1), gamma, np.argmin(passed, axis=1))
+            for n in range(int(cap.sum()) + 1):
+                out = orc.select_prefix(c, None, None, None, R + n, mode, conf_min)
+                l = out["l"]
+                assert l.sum() == n and (l <= cap).all()
+                got = sum(float(a[r, :l[r]].astype(np.float64).sum()) for r in range(R))
+                assert got == pytest.approx(_brute_best_within(a, n, cap), rel=1e-12, abs=1e-15)
+
+
+def _seq(T, R, gamma, seed):
+    w = inputs.workload("confidence_scheduled", seed_offset=seed, R=R, gamma=gamma)
+    return inputs.confidence_sequence(w, T)
+
+
+def test_plan_cycles_accounting(orc):
+    """A run of cycles: every cycle's accepted and wasted rows split its verified
+    drafts (accepted + wasted = sum l, n_acc = min(n_full, l)); a drafter whose
+    every draft is accepted wastes nothing; one whose every draft is rejected
+    wastes every verified row and commits the guaranteed token alone."""
+    T, R, gamma = 12, 64, 5
+    seq = _seq(T, R, gamma, 0)
+    sizes, sps = seq["capture_sizes"], seq["sps"]
+    for mode in (0, 1, 2, 3, 4, 5):
+        out = orc.plan_cycles(seq["c"], seq["n_full"], sizes, sps, 256, mode, 0.5)
+        assert out["status"] == 0
+        nacc = np.minimum(seq["n_full"], out["l"])
+        np.testing.assert_array_equal(out["accepted"], nacc.sum(axis=1))
+        np.testing.assert_array_equal(out["accepted"] + out["wasted"], out["l"].sum(axis=1))
+        np.testing.assert_array_equal(out["K_used"], R + out["l"].sum(axis=1))
+        rate = np.array([sps[np.argmax(sizes >= K)] for K in out["K_used"]], np.float64)
+        np.testing.assert_allclose(out["theta_real"], rate * (R + out["accepted"]), rtol=1e-15)
+    full = orc.plan_cycles(seq["c"], np.full((T, R), gamma, np.int32), sizes, sps, 256, 0)
+    assert (full["wasted"] == 0).all() and (full["accepted"] == full["l"].sum(axis=1)).all()
+    none = orc.plan_cycles(seq["c"], np.zeros((T, R), np.int32), sizes, sps, 256, 0)
+    assert (none["accepted"] == 0).all() and (none["wasted"] == none["l"].sum(axis=1)).all()
+    assert (none["theta_real"] == np.array([sps[np.argmax(sizes >= K)] for K in none["K_used"]]) * R).all()
+
+
+def test_plan_cycles_history_is_causal(orc):
+    """HISTORY takes cycle t's capacity from cycle t - lag: the first lag cycles
+    use K_cap; later, the capacity is the one the single-cycle CURRENT mode
+    picks on the confidences of cycle t - lag, while the logical selection is
+    the top of cycle t's own survival; with every cycle's confidences equal
+    the two modes coincide."""
+    T, R, gamma = 10, 96, 5
+    seq = _seq(T, R, gamma, 1)
+    sizes, sps = seq["capture_sizes"], seq["sps"]
+    K_cap = 512
+    for lag in (1, 2, 3):
+        h = orc.plan_cycles(seq["c"], seq["n_full"], sizes, sps, K_cap, 1, lag=lag)
+        assert (h["K_used"][:lag] == min(K_cap, R * (gamma + 1))).all()
+        for t in range(lag, T):
+            cur = orc.select_prefix(seq["c"][t - lag], None, sizes, sps, K_cap, 2)
+            assert h["K_used"][t] == cur["K_used"]
+            top = orc.select_prefix(seq["c"][t], None, None, None, cur["K_used"], 0)
+            np.testing.assert_array_equal(h["l"][t], top["l"])
+    same = np.broadcast_to(seq["c"][0], seq["c"].shape).copy()
+    h = orc.plan_cycles(same, None, sizes, sps, K_cap, 1)
+    c = orc.plan_cycles(same, None, sizes, sps, K_cap, 2)
+    np.testing.assert_array_equal(h["l"][2:], c["l"][2:])
+    np.testing.assert_allclose(h["theta_pred"][2:], c["theta_pred"][2:], rtol=1e-15)
