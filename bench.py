@@ -504,6 +504,67 @@ def side_workload(name, args, peaks):
     return out
 
 
+PLAN_MODES = [("fixed", 0, 0.0), ("history", 1, 0.0), ("current", 2, 0.0), ("first_stop", 3, 0.0),
+              ("conf_cutoff_0.6", 4, 0.6), ("conf_cutoff_0.3", 4, 0.3), ("survival_cutoff_0.3", 5, 0.3)]
+
+
+def planner_study(n_cycles=1000, repeats=5):
+    """The planner on the workload as given (R = 512) and on two variants that
+    make the capacity choice matter: 384 request slots (between two capture
+    sizes), and the same with a wandering batch-wide confidence shift."""
+    return {"R512": planner_run(n_cycles, repeats),
+            "R384": planner_run(n_cycles, repeats, R=384),
+            "R384_drift": planner_run(n_cycles, repeats, R=384, drift=0.6)}
+
+
+def planner_run(n_cycles=1000, repeats=5, R=None, drift=0.0):
+    """The scheduler over a run of consecutive cycles of the confidence-scheduled
+    workload (R = 512, gamma = 5, K_cap = 1024, the synthetic SPS staircase),
+    one dspark_plan_cycles launch per policy: the capacity planned on the
+    confidences of two cycles back (HISTORY) against the non-causal CURRENT
+    mode, the paper's first-stop greedy, the fixed capacity and static
+    per-request cutoffs.  The target's verdicts are synthetic (each draft
+    survives with its calibrated confidence)."""
+    import torch
+    from speculative_decoding_dspark_gb300 import binding as B
+    w = inputs.workload("confidence_scheduled", **({} if R is None else {"R": R}))
+    seq = inputs.confidence_sequence(w, n_cycles, drift=drift)
+    R = w["R"]
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    c, nf = dev(seq["c"]), dev(seq["n_full"])
+    sizes, sps = dev(seq["capture_sizes"]), dev(seq["sps"])
+    l = torch.empty((n_cycles, R), dtype=torch.int32, device="cuda")
+    K = torch.empty(n_cycles, dtype=torch.int32, device="cuda")
+    st = torch.empty((n_cycles, 4), dtype=torch.float64, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = {"cycles": n_cycles, "R": R, "gamma": w["gamma"], "K_cap": seq["K_cap"], "lag": 2, "drift": drift,
+           "verdicts": "synthetic: draft k survives with probability c[t, r, k] given the ones before",
+           "policies": {}}
+    stream = torch.cuda.current_stream()
+    for name, mode, conf_min in PLAN_MODES:
+        run = lambda: B.dspark_plan_cycles(c, nf, sizes, sps, seq["K_cap"], mode, l, K, st, conf_min=conf_min,
+                                           lag=2, dev_status=status)
+        run()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(repeats):
+            run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        s_h = st.cpu().numpy()
+        k_h = K.cpu().numpy()
+        out["policies"][name] = {
+            "mode": mode, "conf_min": conf_min,
+            "theta_achieved_mean": float(s_h[:, 1].mean()), "theta_predicted_mean": float(s_h[:, 0].mean()),
+            "accepted_per_cycle": float(s_h[:, 2].mean()), "wasted_rows_per_cycle": float(s_h[:, 3].mean()),
+            "rows_per_cycle": float(k_h.mean()),
+            "launch_ms": e0.elapsed_time(e1) / repeats}
+    assert int(status.item()) == 0
+    out["unit_theta"] = "tokens/s of the synthetic engine: SPS(B) x (R + accepted drafts)"
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -603,6 +664,7 @@ def run_ours(args):
         torch.cuda.empty_cache()
         side = {name: side_workload(name, args, peaks)
                 for name in ("confidence_scheduled", "varlen_verify", "qwen3_8b_greedy")}
+        side["planner"] = planner_study()
 
     cpu = None
     if pool is not None:

@@ -183,16 +183,25 @@ def confidence_inputs(w: dict) -> dict:
                 K_cap=int(w.get("K_cap", R * (gamma + 1))), tau=tau)
 
 
-def confidence_sequence(w: dict, n_cycles: int) -> dict:
+def confidence_sequence(w: dict, n_cycles: int, drift: float = 0.0) -> dict:
     """Confidences of n_cycles consecutive cycles of the same R request slots
     ([n_cycles, R, gamma], each cycle drawn from the workload's law) and, as the
     synthetic stand-in for the target's verdicts, n_full [n_cycles, R]: how many
     leading drafts the target accepts, drawn so that draft k survives with
     probability c[t, r, k] given the ones before it (the confidences are
-    calibrated conditional acceptance rates)."""
+    calibrated conditional acceptance rates).  drift > 0 adds a batch-wide shift
+    of the confidence logits that wanders from cycle to cycle (a random walk of
+    step `drift` pulled back towards 0 by 10% a cycle: the batch's mix of easy and
+    hard text changing over time)."""
     R, gamma, seed = w["R"], w["gamma"], w["seed"]
     tau = confidence_inputs(w)["tau"]
     z = 1.0 + 1.5 * rng(seed, 10).standard_normal((n_cycles, R, gamma))
+    if drift > 0.0:
+        steps = drift * rng(seed, 12).standard_normal(n_cycles)
+        shift = np.zeros(n_cycles)
+        for t in range(1, n_cycles):
+            shift[t] = 0.9 * shift[t - 1] + steps[t]
+        z = z + shift[:, None, None]
     c = (1.0 / (1.0 + np.exp(-z / tau[None, None, :]))).astype(np.float32)
     u = rng(seed, 11).random((n_cycles, R, gamma), dtype=np.float32)
     ok = u < c
