@@ -565,6 +565,72 @@ def planner_run(n_cycles=1000, repeats=5, R=None, drift=0.0):
     return out
 
 
+def calibration_study(n_samples=512_000, repeats=5):
+    """dspark_fit_temperatures on labels drawn from the workload's per-position
+    temperatures: time per fit and the temperatures it recovers."""
+    import torch
+    from speculative_decoding_dspark_gb300 import binding as B
+    w = inputs.workload("confidence_scheduled")
+    cs = inputs.calibration_samples(w, n_samples)
+    gamma = w["gamma"]
+    z = torch.from_numpy(cs["z"]).cuda()
+    acc = torch.from_numpy(cs["accepted"]).cuda()
+    tau = torch.empty(gamma, device="cuda")
+    nll = torch.empty(gamma, dtype=torch.float64, device="cuda")
+    cnt = torch.empty(gamma, dtype=torch.int32, device="cuda")
+    ws = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_CALIBRATE, 0, gamma, 0))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    run = lambda: B.dspark_fit_temperatures(z, acc, tau, nll, cnt, ws, status)
+    run()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(repeats):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ms = e0.elapsed_time(e1) / repeats
+    bytes_read = n_samples * gamma * 5  # z and labels once; the Newton steps re-read them from L2
+    return {"samples": n_samples, "gamma": gamma, "ms": ms, "samples_per_s": n_samples / (ms / 1e3),
+            "tau_true": [float(x) for x in cs["tau_true"]], "tau_fit": [float(x) for x in tau.cpu()],
+            "samples_per_position": [int(x) for x in cnt.cpu()],
+            "note": f"latency-bound: {bytes_read / 1e6:.1f} MB of inputs, a few Newton steps each with a "
+                    "barrier of the position's CTAs"}
+
+
+R_SPARE = 512 * 24  # pages for 50 cycles of growth of 512 requests (at most 6 tokens a cycle each)
+
+
+def kv_study(cycles=50):
+    """dspark_kv_reserve + dspark_kv_commit per cycle on a 512-request paged KV
+    cache (page size 16): microseconds per cycle (one CTA each: latency-bound)."""
+    import torch
+    from speculative_decoding_dspark_gb300 import binding as B
+    w = inputs.workload("confidence_scheduled")
+    kv = inputs.kv_state(w, page_size=16, max_len=4096, spare_pages=R_SPARE)
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    g = np.random.default_rng(3)
+    R, gamma = w["R"], w["gamma"]
+    ls = [dev(g.integers(0, gamma + 1, size=R).astype(np.int32)) for _ in range(cycles)]
+    nas = [dev((g.random(R) * (ls[i].cpu().numpy() + 1)).astype(np.int32)) for i in range(cycles)]
+    d_len, d_bt = dev(kv["kv_len"]), dev(kv["block_table"])
+    d_free, d_top = dev(kv["free_pages"]), dev(np.array([kv["free_top"]], np.int32))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(cycles):
+        B.dspark_kv_reserve(d_len, ls[i], 16, d_bt, d_free, d_top, None, status)
+        B.dspark_kv_commit(d_len, ls[i], nas[i], 16, d_bt, d_free, d_top, status)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    # the first cycles may run out of pages as contexts grow: report the status
+    return {"R": R, "page_size": 16, "cycles": cycles, "us_per_cycle": 1000.0 * e0.elapsed_time(e1) / cycles,
+            "status": int(status.item()), "note": "reserve + commit, one CTA each (latency-bound)"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -665,6 +731,8 @@ def run_ours(args):
         side = {name: side_workload(name, args, peaks)
                 for name in ("confidence_scheduled", "varlen_verify", "qwen3_8b_greedy")}
         side["planner"] = planner_study()
+        side["calibration"] = calibration_study()
+        side["kv_bookkeeping"] = kv_study()
 
     cpu = None
     if pool is not None:

@@ -83,6 +83,7 @@ typedef struct CUstream_st* dspark_stream_t;
 #define DSPARK_OP_VERIFY 1
 #define DSPARK_OP_SELECT 2
 #define DSPARK_OP_VERIFY_MARKOV 3
+#define DSPARK_OP_CALIBRATE 4
 
 /* ---- dspark_markov_draft flags ---------------------------------------------- */
 #define DSPARK_DRAFT_FORCE_SIMT 1u   /* use the CUDA-core kernels even where the
@@ -109,7 +110,8 @@ typedef struct CUstream_st* dspark_stream_t;
 const char* dspark_status_string(int status);
 
 /* Library version, major * 10000 + minor * 100 + patch (1.1.0: cutoff modes,
- * conf_min in dspark_select_prefix, dspark_plan_cycles, the wait settings). */
+ * conf_min in dspark_select_prefix, dspark_plan_cycles, the wait settings,
+ * dspark_fit_temperatures, dspark_kv_reserve and dspark_kv_commit). */
 int dspark_version(void);
 
 /* Bytes of workspace one call of `op` needs for these sizes (0 on bad
@@ -371,6 +373,85 @@ int dspark_plan_cycles(const float* c_seq, const int32_t* n_full, const int32_t*
                        const float* sps, int n_steps, int K_cap, int mode, float conf_min, int lag,
                        int n_cycles, int R, int gamma, int32_t* l_seq, int32_t* K_seq, double* stats,
                        int32_t* dev_status, dspark_stream_t stream);
+
+/*
+ * dspark_fit_temperatures -- sequential temperature scaling of the confidence
+ * head (explainer section 8: the per-position confidences are calibrated left
+ * to right by a post-hoc temperature so that their products are calibrated
+ * survival probabilities; PR 25173 "Future work": the paper's Sequential
+ * Temperature Scaling).
+ *
+ * Position k is fitted on the samples that reached it (accepted[i][j] != 0 for
+ * every j < k), so that c_k = sigmoid(z_k / tau_k) estimates the conditional
+ * acceptance rate.  tau_k minimises the labels' negative log-likelihood
+ *   NLL(beta) = sum_i softplus(beta z_i[k]) - accepted_i[k] * beta z_i[k],
+ * beta = 1 / tau_k (convex in beta), by Newton's method from beta = 1 (halving
+ * beta when a step would leave (0, inf)) until the step is below 1e-12 of beta,
+ * then beta is clamped to [1e-3, 1e3].  A position no sample reached gets
+ * tau = 1 and count 0.
+ *
+ *   z        [N, gamma] fp32 raw confidence logits
+ *   accepted [N, gamma] uint8 labels (0 rejected; entries after a sample's first
+ *            rejection are ignored)
+ *   tau [gamma] fp32 out; nll [gamma] fp64 out (mean NLL at tau) or NULL;
+ *   count [gamma] int32 out (samples that reached the position) or NULL
+ *   ws, ws_bytes  dspark_workspace_size(DSPARK_OP_CALIBRATE, 0, gamma, 0, 0, 0, 0, 0)
+ * Limits: 1 <= gamma <= 16, N >= 1.  The CTAs of a position meet at bounded
+ * barriers between Newton steps (DSPARK_ERR_TIMEOUT if one runs out).
+ */
+int dspark_fit_temperatures(const float* z, const uint8_t* accepted, int N, int gamma, float* tau,
+                            double* nll, int32_t* count, void* ws, size_t ws_bytes, int32_t* dev_status,
+                            dspark_stream_t stream);
+
+/*
+ * dspark_kv_reserve / dspark_kv_commit -- the paged KV cache's bookkeeping
+ * around one verify (explainer section 11: verify writes its candidate rows
+ * into temporary pages; after the first rejection only the accepted prefix is
+ * promoted and every other candidate's state is released; section 15: leaked
+ * or double-freed temporary state is a failure class).
+ *
+ * State (device memory, owned by the caller):
+ *   kv_len      [R] int32    committed tokens of each request
+ *   block_table [R, max_blocks] int32  page ids; page b holds positions
+ *               [b * page_size, (b + 1) * page_size); a request's committed
+ *               pages are its leading ceil(kv_len / page_size) entries, the
+ *               rest are -1
+ *   free_pages  [pool_pages] int32 stack of free page ids, free_pages[0 .. *free_top)
+ *   free_top    [1] int32
+ *   pool_pages  the stack's capacity (every page of the pool); no call writes
+ *               past it (a state that would make it do so is rejected)
+ *
+ * dspark_kv_reserve: before the verify, request r needs
+ *   need[r] = ceil((kv_len + l + 1) / page_size) - ceil(kv_len / page_size)
+ * more pages for its l[r] + 1 verify rows (positions kv_len .. kv_len + l).
+ * The top T = sum of needs pages of the stack are handed out in request order
+ * (request r takes free_pages[*free_top - T + o_r + i], o_r = the needs of the
+ * requests before it) into its next block-table entries; *free_top -= T;
+ * reserved[r] = need[r] (reserved may be NULL).  All or nothing: when T >
+ * *free_top or a request would pass max_blocks, nothing changes and
+ * DSPARK_ERR_CAPACITY goes to *dev_status (DSPARK_ERR_DEVICE_INPUT for a
+ * negative length, whichever request comes first).
+ *
+ * dspark_kv_commit: after the verify (with the l of the reserve), request r
+ * keeps its committed prefix plus the rows of its accepted drafts:
+ *   kv_len[r] += n_accepted[r] + 1
+ * (the same count dspark_commit_lengths reports).  The pages past
+ * ceil(kv_len / page_size) held only rejected rows: they go back on the stack
+ * in request order (request r's at *free_top + o_r + i, o_r = the pages the
+ * requests before it release), their entries become -1 (an entry holding no
+ * page is skipped), and *free_top grows by the total.  A request with
+ * n_accepted outside [0, l] commits nothing, releases all its reserved pages
+ * and is reported (DSPARK_ERR_DEVICE_INPUT).  If the stack could not take the
+ * released pages (a state the reserve did not produce), nothing changes and
+ * DSPARK_ERR_DEVICE_INPUT is reported.
+ * Both calls run in one CTA; R >= 1, page_size >= 1, max_blocks >= 1.
+ */
+int dspark_kv_reserve(const int32_t* kv_len, const int32_t* l, int R, int page_size, int32_t* block_table,
+                      int max_blocks, int32_t* free_pages, int32_t* free_top, int pool_pages, int32_t* reserved,
+                      int32_t* dev_status, dspark_stream_t stream);
+int dspark_kv_commit(int32_t* kv_len, const int32_t* l, const int32_t* n_accepted, int R, int page_size,
+                     int32_t* block_table, int max_blocks, int32_t* free_pages, int32_t* free_top, int pool_pages,
+                     int32_t* dev_status, dspark_stream_t stream);
 
 /*
  * dspark_commit_lengths -- per-request commit and rollback counts

@@ -88,6 +88,12 @@ def lib():
             L.orc_plan_cycles.argtypes = [vp, vp, vp, vp, i32, i32, i32, f32, i32, i32, i32, i32,
                                           vp, vp, vp, vp]
             L.orc_plan_cycles.restype = i32
+            L.orc_fit_temperatures.argtypes = [vp, vp, i32, i32, vp, vp, vp]
+            L.orc_fit_temperatures.restype = i32
+            L.orc_kv_reserve.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp, i32, vp]
+            L.orc_kv_reserve.restype = i32
+            L.orc_kv_commit.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp, vp, i32]
+            L.orc_kv_commit.restype = i32
             L.orc_commit_lengths.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp]
             L.orc_commit_lengths.restype = i32
             _lib = L
@@ -247,6 +253,50 @@ def plan_cycles(c_seq, n_full, capture_sizes, sps, K_cap, mode, conf_min=0.0, la
                                T, R, gamma, _p(l_seq), _p(K_seq), _p(stats), _p(gap))
     return dict(status=st, l=l_seq, K_used=K_seq, theta_pred=stats[:, 0], theta_real=stats[:, 1],
                 accepted=stats[:, 2].astype(np.int64), wasted=stats[:, 3].astype(np.int64), theta_gap=gap)
+
+
+def fit_temperatures(z, accepted):
+    """Sequential temperature scaling: z [N, gamma] float32 confidence logits,
+    accepted [N, gamma] 0/1 labels -> tau, mean NLL and samples per position."""
+    z = _c(z, np.float32)
+    acc = _c(accepted, np.uint8)
+    N, gamma = z.shape
+    tau = np.zeros(gamma, np.float32)
+    nll = np.zeros(gamma, np.float64)
+    cnt = np.zeros(gamma, np.int32)
+    st = lib().orc_fit_temperatures(_p(z), _p(acc), N, gamma, _p(tau), _p(nll), _p(cnt))
+    return dict(status=st, tau=tau, nll=nll, count=cnt)
+
+
+class KvState:
+    """A paged KV cache's bookkeeping: committed lengths, block table, free stack."""
+
+    def __init__(self, kv_len, block_table, free_pages, free_top, page_size):
+        self.kv_len = _c(kv_len, np.int32).copy()
+        self.block_table = _c(block_table, np.int32).copy()
+        self.free_pages = _c(free_pages, np.int32).copy()
+        self.free_top = np.array([free_top], np.int32)
+        self.P = int(page_size)
+
+    def copy(self):
+        return KvState(self.kv_len, self.block_table, self.free_pages, int(self.free_top[0]), self.P)
+
+
+def kv_reserve(st: KvState, l):
+    l = _c(l, np.int32)
+    R, max_blocks = st.block_table.shape
+    reserved = np.zeros(R, np.int32)
+    rc = lib().orc_kv_reserve(_p(st.kv_len), _p(l), R, st.P, _p(st.block_table), max_blocks,
+                              _p(st.free_pages), _p(st.free_top), st.free_pages.size, _p(reserved))
+    return rc, reserved
+
+
+def kv_commit(st: KvState, l, n_acc):
+    l = _c(l, np.int32)
+    n_acc = _c(n_acc, np.int32)
+    R, max_blocks = st.block_table.shape
+    return lib().orc_kv_commit(_p(st.kv_len), _p(l), _p(n_acc), R, st.P, _p(st.block_table), max_blocks,
+                               _p(st.free_pages), _p(st.free_top), st.free_pages.size)
 
 
 def commit_lengths(n_acc, l, gamma):

@@ -611,6 +611,162 @@ int orc_plan_cycles(const float* c_seq, const int32_t* n_full, const int32_t* ca
     return status;
 }
 
+// Sequential temperature scaling of the confidence head ([EXPL] section 8:
+// the per-position confidences are calibrated left to right by a post-hoc
+// temperature so that their products are calibrated survival probabilities;
+// the llama.cpp PR's "Future work" names the paper's Sequential Temperature
+// Scaling calibration).  Position k is fitted on the samples that reached it
+// (every earlier draft accepted), so c_k = sigmoid(z_k / tau_k) estimates the
+// conditional acceptance rate the survival product multiplies.  With
+// beta = 1/tau the negative log-likelihood of the labels y,
+//   NLL(beta) = sum_i softplus(beta z_i) - y_i beta z_i,
+// is convex; Newton's method from beta = 1 takes steps g / h with
+//   g = sum_i (sigmoid(beta z_i) - y_i) z_i,  h = sum_i s_i (1 - s_i) z_i^2,
+// halving beta instead whenever a step would leave (0, inf), for a fixed
+// kFitIters iterations (the iterate has converged long before), and clamps
+// beta to [1e-3, 1e3].  A position no sample reached keeps tau = 1.
+// tau[k] = 1 / beta; nll[k] = NLL(beta) / count; count[k] = samples used.
+static const int kFitIters = 60;
+
+static double softplus(double x) { return x > 0.0 ? x + std::log1p(std::exp(-x)) : std::log1p(std::exp(x)); }
+static double sigmoid(double x) { return x >= 0.0 ? 1.0 / (1.0 + std::exp(-x)) : std::exp(x) / (1.0 + std::exp(x)); }
+
+int orc_fit_temperatures(const float* z, const uint8_t* accepted, int N, int gamma, float* tau,
+                         double* nll, int32_t* count) {
+    if (N <= 0 || gamma <= 0) return ORC_INVALID;
+    for (int k = 0; k < gamma; ++k) {
+        // the samples that reached position k
+        std::vector<int> use;
+        for (int i = 0; i < N; ++i) {
+            bool reached = true;
+            for (int j = 0; j < k; ++j)
+                if (!accepted[(size_t)i * gamma + j]) { reached = false; break; }
+            if (reached) use.push_back(i);
+        }
+        if (count) count[k] = (int32_t)use.size();
+        if (use.empty()) { tau[k] = 1.0f; if (nll) nll[k] = 0.0; continue; }
+        double beta = 1.0;
+        for (int it = 0; it < kFitIters; ++it) {
+            double g = 0.0, h = 0.0;
+            for (int i : use) {
+                const double zi = (double)z[(size_t)i * gamma + k];
+                const double yi = accepted[(size_t)i * gamma + k] ? 1.0 : 0.0;
+                const double si = sigmoid(beta * zi);
+                g += (si - yi) * zi;
+                h += si * (1.0 - si) * zi * zi;
+            }
+            if (!(h > 0.0)) break;
+            const double next = beta - g / h;
+            beta = (next > 0.0 && std::isfinite(next)) ? next : 0.5 * beta;
+        }
+        beta = std::min(1e3, std::max(1e-3, beta));
+        double f = 0.0;
+        for (int i : use) {
+            const double zi = (double)z[(size_t)i * gamma + k];
+            const double yi = accepted[(size_t)i * gamma + k] ? 1.0 : 0.0;
+            f += softplus(beta * zi) - yi * beta * zi;
+        }
+        tau[k] = (float)(1.0 / beta);
+        if (nll) nll[k] = f / (double)use.size();
+    }
+    return ORC_OK;
+}
+
+// Paged KV cache around one verify ([EXPL] section 11: the target's verify
+// writes its candidate rows into temporary pages or block-table entries; after
+// the first rejection only the accepted prefix is promoted to committed state
+// and everything else -- the rejected candidates' K/V and their metadata -- is
+// released or rolled back; section 15 lists leaked or double-freed temporary
+// state among the failure classes).
+//
+// State: per request r its committed length kv_len[r] (tokens) and a block
+// table of page ids (max_blocks per request; page b holds positions
+// [b P, (b + 1) P)); the committed pages are entries 0 .. ceil(kv_len/P) - 1,
+// the rest are -1.  Free pages form a stack free_pages[0 .. free_top).
+//
+// orc_kv_reserve: verify writes l[r] + 1 rows at positions kv_len .. kv_len + l,
+// so request r needs need[r] = ceil((kv_len + l + 1) / P) - ceil(kv_len / P)
+// more pages.  With T = sum need, the top T pages of the stack are handed out
+// in request order (request r takes free_pages[free_top - T + o_r + i], o_r =
+// need of the requests before it) into its next block-table entries, and
+// free_top -= T.  If T > free_top, or a request would pass max_blocks, nothing
+// changes and the call reports a capacity error.
+//
+// orc_kv_commit: request r keeps its committed prefix plus the accepted
+// drafts' rows: kv_len' = kv_len + n_acc + 1 (n_acc in [0, l]; otherwise the
+// request commits nothing, kv_len' = kv_len, and the call reports bad input).
+// Pages ceil(kv_len'/P) .. ceil((kv_len + l + 1)/P) - 1 held only rejected rows:
+// they go back on the stack in request order (request r's at free_top + o_r +
+// i, o_r = pages released by the requests before it), their entries become
+// -1, and free_top grows by the total.  Entries that hold no page (-1) are
+// skipped; if the stack (pool_pages entries) could not take the pages, nothing
+// changes and the call reports bad input.
+static int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+int orc_kv_reserve(const int32_t* kv_len, const int32_t* l, int R, int P, int32_t* block_table,
+                   int max_blocks, int32_t* free_pages, int32_t* free_top, int pool_pages, int32_t* reserved) {
+    if (R <= 0 || P <= 0 || max_blocks <= 0) return ORC_INVALID;
+    if (*free_top < 0 || *free_top > pool_pages) return ORC_DEVICE_INPUT;
+    std::vector<int> need(R);
+    long total = 0;
+    for (int r = 0; r < R; ++r) {
+        if (kv_len[r] < 0 || l[r] < 0) return ORC_DEVICE_INPUT;
+        const int have = ceil_div(kv_len[r], P), want = ceil_div(kv_len[r] + l[r] + 1, P);
+        if (want > max_blocks) return ORC_CAPACITY;
+        need[r] = want - have;
+        total += need[r];
+    }
+    if (total > *free_top) return ORC_CAPACITY;
+    const int base = *free_top - (int)total;
+    int o = 0;
+    for (int r = 0; r < R; ++r) {
+        const int have = ceil_div(kv_len[r], P);
+        for (int i = 0; i < need[r]; ++i)
+            block_table[(size_t)r * max_blocks + have + i] = free_pages[base + o + i];
+        if (reserved) reserved[r] = need[r];
+        o += need[r];
+    }
+    *free_top = base;
+    return ORC_OK;
+}
+
+int orc_kv_commit(int32_t* kv_len, const int32_t* l, const int32_t* n_acc, int R, int P,
+                  int32_t* block_table, int max_blocks, int32_t* free_pages, int32_t* free_top,
+                  int pool_pages) {
+    if (R <= 0 || P <= 0 || max_blocks <= 0) return ORC_INVALID;
+    int status = ORC_OK;
+    auto span = [&](int r, int& keep, int& held, int& new_len) {
+        if (kv_len[r] < 0 || l[r] < 0) { keep = held = 0; new_len = kv_len[r]; return; }  // unusable: untouched
+        held = std::min(max_blocks, ceil_div(kv_len[r] + l[r] + 1, P));
+        int committed = n_acc[r] + 1;
+        if (n_acc[r] < 0 || n_acc[r] > l[r]) committed = 0;
+        new_len = kv_len[r] + committed;
+        keep = ceil_div(new_len, P);
+    };
+    long pushes = 0;
+    for (int r = 0; r < R; ++r) {
+        int keep, held, new_len;
+        span(r, keep, held, new_len);
+        for (int b = keep; b < held; ++b)
+            if (block_table[(size_t)r * max_blocks + b] >= 0) ++pushes;
+    }
+    if (*free_top < 0 || *free_top + pushes > pool_pages) return ORC_DEVICE_INPUT;
+    int top = *free_top;
+    for (int r = 0; r < R; ++r) {
+        int keep, held, new_len;
+        span(r, keep, held, new_len);
+        if (n_acc[r] < 0 || n_acc[r] > l[r] || kv_len[r] < 0 || l[r] < 0) status = ORC_DEVICE_INPUT;
+        for (int b = keep; b < held; ++b) {
+            int32_t& e = block_table[(size_t)r * max_blocks + b];
+            if (e >= 0) free_pages[top++] = e;
+            e = -1;
+        }
+        kv_len[r] = new_len;
+    }
+    *free_top = top;
+    return status;
+}
+
 // Commit lengths ([EXPL] section 2: each cycle commits the accepted prefix
 // plus one target-correct token; section 11: everything verified beyond it is
 // rolled back).  commit_len = n_acc + 1, cu_commit = exclusive running sum,

@@ -27,7 +27,7 @@ DSPARK_ERR_DEVICE_INPUT = -6
 DSPARK_ERR_WORKSPACE = -7
 
 DSPARK_F32, DSPARK_BF16 = 0, 1
-DSPARK_OP_DRAFT, DSPARK_OP_VERIFY, DSPARK_OP_SELECT, DSPARK_OP_VERIFY_MARKOV = 0, 1, 2, 3
+DSPARK_OP_DRAFT, DSPARK_OP_VERIFY, DSPARK_OP_SELECT, DSPARK_OP_VERIFY_MARKOV, DSPARK_OP_CALIBRATE = 0, 1, 2, 3, 4
 DSPARK_DRAFT_FORCE_SIMT = 1
 DSPARK_SELECT_FIXED, DSPARK_SELECT_HISTORY, DSPARK_SELECT_CURRENT, DSPARK_SELECT_FIRST_STOP = 0, 1, 2, 3
 DSPARK_SELECT_CONF_CUTOFF, DSPARK_SELECT_SURVIVAL_CUTOFF = 4, 5
@@ -37,7 +37,7 @@ EXPORTED = ["dspark_status_string", "dspark_version", "dspark_workspace_size", "
             "dspark_markov_draft_uses_tensor_cores", "dspark_markov_draft", "dspark_verify",
             "dspark_select_prefix", "dspark_commit_lengths", "dspark_verify_static_scratch",
             "dspark_verify_markov", "dspark_set_wait_limit_ns", "dspark_set_fault_injection",
-            "dspark_plan_cycles"]
+            "dspark_plan_cycles", "dspark_fit_temperatures", "dspark_kv_reserve", "dspark_kv_commit"]
 
 
 class DSparkError(RuntimeError):
@@ -81,6 +81,12 @@ def _load():
     L.dspark_philox4x32_10.restype = i32
     L.dspark_commit_lengths.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, vp]
     L.dspark_commit_lengths.restype = i32
+    L.dspark_fit_temperatures.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, sz, vp, vp]
+    L.dspark_fit_temperatures.restype = i32
+    L.dspark_kv_reserve.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp, i32, vp, vp, vp]
+    L.dspark_kv_reserve.restype = i32
+    L.dspark_kv_commit.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp, vp, i32, vp, vp]
+    L.dspark_kv_commit.restype = i32
     L.dspark_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     L.dspark_set_wait_limit_ns.restype = ctypes.c_uint64
     L.dspark_set_fault_injection.argtypes = [ctypes.c_uint]
@@ -320,6 +326,52 @@ def dspark_plan_cycles(c_seq, n_full, capture_sizes, sps, K_cap, mode, l_seq, K_
                                int(K_cap), int(mode), float(conf_min), int(lag), T, R, gamma, _ptr(l_seq),
                                _ptr(K_seq), _ptr(stats), _ptr(dev_status), _stream(stream))
     _raise("dspark_plan_cycles", st)
+
+
+def dspark_fit_temperatures(z, accepted, tau, nll=None, count=None, ws=None, dev_status=None, stream=None):
+    N, gamma = z.shape
+    _check(z, "z", torch.float32)
+    _check(accepted, "accepted", torch.uint8, (N, gamma))
+    _check(tau, "tau", torch.float32, (gamma,))
+    _check(nll, "nll", torch.float64, (gamma,), allow_none=True)
+    _check(count, "count", torch.int32, (gamma,), allow_none=True)
+    _check(ws, "ws", torch.uint8)
+    _check(dev_status, "dev_status", torch.int32, allow_none=True)
+    st = _L.dspark_fit_temperatures(_ptr(z), _ptr(accepted), N, gamma, _ptr(tau), _ptr(nll), _ptr(count),
+                                    _ptr(ws), ws.numel(), _ptr(dev_status), _stream(stream))
+    _raise("dspark_fit_temperatures", st)
+
+
+def dspark_kv_reserve(kv_len, l, page_size, block_table, free_pages, free_top, reserved=None, dev_status=None,
+                      stream=None):
+    R, max_blocks = block_table.shape
+    _check(kv_len, "kv_len", torch.int32, (R,))
+    _check(l, "l", torch.int32, (R,))
+    _check(block_table, "block_table", torch.int32)
+    _check(free_pages, "free_pages", torch.int32)
+    _check(free_top, "free_top", torch.int32, (1,))
+    _check(reserved, "reserved", torch.int32, (R,), allow_none=True)
+    _check(dev_status, "dev_status", torch.int32, allow_none=True)
+    _raise("dspark_kv_reserve",
+           _L.dspark_kv_reserve(_ptr(kv_len), _ptr(l), R, int(page_size), _ptr(block_table), max_blocks,
+                                _ptr(free_pages), _ptr(free_top), free_pages.numel(), _ptr(reserved),
+                                _ptr(dev_status), _stream(stream)))
+
+
+def dspark_kv_commit(kv_len, l, n_accepted, page_size, block_table, free_pages, free_top, dev_status=None,
+                     stream=None):
+    R, max_blocks = block_table.shape
+    _check(kv_len, "kv_len", torch.int32, (R,))
+    _check(l, "l", torch.int32, (R,))
+    _check(n_accepted, "n_accepted", torch.int32, (R,))
+    _check(block_table, "block_table", torch.int32)
+    _check(free_pages, "free_pages", torch.int32)
+    _check(free_top, "free_top", torch.int32, (1,))
+    _check(dev_status, "dev_status", torch.int32, allow_none=True)
+    _raise("dspark_kv_commit",
+           _L.dspark_kv_commit(_ptr(kv_len), _ptr(l), _ptr(n_accepted), R, int(page_size), _ptr(block_table),
+                               max_blocks, _ptr(free_pages), _ptr(free_top), free_pages.numel(), _ptr(dev_status),
+                               _stream(stream)))
 
 
 def dspark_philox4x32_10(ctr, keys, out, stream=None):

@@ -131,6 +131,9 @@ size_t dspark_workspace_size(int op, int R, int gamma, int V, int rank, int max_
             return align_up(verify_layout(R, V).total) + residual_tc_workspace(R, rank);
         case DSPARK_OP_SELECT:
             return 0;
+        case DSPARK_OP_CALIBRATE:
+            if (gamma <= 0 || gamma > 16) return 0;
+            return calibrate_workspace(gamma);
         default:
             return 0;
     }
@@ -327,6 +330,35 @@ int dspark_plan_cycles(const float* c_seq, const int32_t* n_full, const int32_t*
     p.a = nullptr; p.l = l_seq; p.cu = nullptr; p.K_used = K_seq; p.dev_status = dev_status;
     p.lag = lag; p.n_full = n_full; p.stats = stats;
     return cuda_status(launch_plan(p, n_cycles, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dspark_fit_temperatures(const float* z, const uint8_t* accepted, int N, int gamma, float* tau,
+                            double* nll, int32_t* count, void* ws, size_t ws_bytes, int32_t* dev_status,
+                            dspark_stream_t stream) {
+    if (!z || !accepted || !tau) return DSPARK_ERR_INVALID_ARG;
+    if (N <= 0 || gamma <= 0 || gamma > 16) return DSPARK_ERR_INVALID_ARG;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return DSPARK_ERR_WORKSPACE;
+    if (ws_bytes < calibrate_workspace(gamma)) return DSPARK_ERR_WORKSPACE;
+    return cuda_status(launch_calibrate(z, accepted, N, gamma, tau, nll, count, dev_status, ws,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dspark_kv_reserve(const int32_t* kv_len, const int32_t* l, int R, int page_size, int32_t* block_table,
+                      int max_blocks, int32_t* free_pages, int32_t* free_top, int pool_pages, int32_t* reserved,
+                      int32_t* dev_status, dspark_stream_t stream) {
+    if (!kv_len || !l || !block_table || !free_pages || !free_top) return DSPARK_ERR_INVALID_ARG;
+    if (R <= 0 || page_size <= 0 || max_blocks <= 0 || pool_pages < 0) return DSPARK_ERR_INVALID_ARG;
+    return cuda_status(launch_kv_reserve(kv_len, l, R, page_size, block_table, max_blocks, free_pages, free_top,
+                                         pool_pages, reserved, dev_status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dspark_kv_commit(int32_t* kv_len, const int32_t* l, const int32_t* n_accepted, int R, int page_size,
+                     int32_t* block_table, int max_blocks, int32_t* free_pages, int32_t* free_top, int pool_pages,
+                     int32_t* dev_status, dspark_stream_t stream) {
+    if (!kv_len || !l || !n_accepted || !block_table || !free_pages || !free_top) return DSPARK_ERR_INVALID_ARG;
+    if (R <= 0 || page_size <= 0 || max_blocks <= 0 || pool_pages < 0) return DSPARK_ERR_INVALID_ARG;
+    return cuda_status(launch_kv_commit(kv_len, l, n_accepted, R, page_size, block_table, max_blocks, free_pages,
+                                        free_top, pool_pages, dev_status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int dspark_philox4x32_10(const uint32_t* ctr, const uint64_t* keys, int n, uint32_t* out,

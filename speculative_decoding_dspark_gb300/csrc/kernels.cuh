@@ -162,6 +162,24 @@ cudaError_t launch_philox_batch(const uint32_t* ctr, const uint64_t* keys, int n
 unsigned long long grid_wait_limit_ns();
 unsigned fault_injection_mask();
 
+// ----------------------------------------------------------------------------
+// Confidence calibration (sequential temperature scaling)
+// ----------------------------------------------------------------------------
+constexpr int kCalMaxCtas = 64;  // CTAs per position
+size_t calibrate_workspace(int gamma);
+cudaError_t launch_calibrate(const float* z, const uint8_t* accepted, int N, int gamma, float* tau, double* nll,
+                             int32_t* count, int32_t* dev_status, void* ws, cudaStream_t stream);
+
+// ----------------------------------------------------------------------------
+// Paged KV bookkeeping around a verify
+// ----------------------------------------------------------------------------
+cudaError_t launch_kv_reserve(const int32_t* kv_len, const int32_t* l, int R, int P, int32_t* bt, int max_blocks,
+                              const int32_t* free_pages, int32_t* free_top, int pool_pages, int32_t* reserved,
+                              int32_t* dev_status, cudaStream_t stream);
+cudaError_t launch_kv_commit(int32_t* kv_len, const int32_t* l, const int32_t* n_acc, int R, int P, int32_t* bt,
+                             int max_blocks, int32_t* free_pages, int32_t* free_top, int pool_pages,
+                             int32_t* dev_status, cudaStream_t stream);
+
 cudaError_t launch_commit(const int32_t* n_acc, const int32_t* l, int R, int gamma,
                           int32_t* commit_len, int32_t* cu_commit, int32_t* discard,
                           int32_t* total, int32_t* dev_status, cudaStream_t stream);

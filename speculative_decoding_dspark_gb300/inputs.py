@@ -209,3 +209,47 @@ def confidence_sequence(w: dict, n_cycles: int, drift: float = 0.0) -> dict:
     sizes = np.asarray(w.get("capture_sizes", [64, 128, 256, 512, 1024]), np.int32)
     return dict(c=c, n_full=n_full, capture_sizes=sizes, sps=sps_staircase(sizes),
                 K_cap=int(w.get("K_cap", R * (gamma + 1))))
+
+
+def calibration_samples(w: dict, n_samples: int, tau_true=None) -> dict:
+    """Labelled samples for the confidence calibration: the confidence head's raw
+    logits z [n_samples, gamma] (the workload's law, N(1, 1.5^2)) and 0/1
+    acceptance labels drawn left to right, position k accepted with
+    probability sigmoid(z_k / tau_true_k) when every earlier position was
+    (later positions of a rejected sample are labelled 0, as a verify that
+    stopped there would record).  tau_true defaults to the workload's
+    per-position temperatures."""
+    gamma, seed = w["gamma"], w["seed"]
+    tau = np.asarray(confidence_inputs(w)["tau"] if tau_true is None else tau_true, np.float64)
+    z = (1.0 + 1.5 * rng(seed, 13).standard_normal((n_samples, gamma))).astype(np.float32)
+    u = rng(seed, 14).random((n_samples, gamma))
+    p = 1.0 / (1.0 + np.exp(-z.astype(np.float64) / tau[None, :]))
+    ok = u < p
+    reached = np.cumprod(ok, axis=1).astype(bool)
+    return dict(z=z, accepted=reached.astype(np.uint8), tau_true=tau.astype(np.float32))
+
+
+def kv_state(w: dict, page_size: int = 16, max_len: int = 4096, spare_pages: int = 0) -> dict:
+    """A paged KV cache's bookkeeping before a cycle: committed lengths
+    kv_len [R] uniform in 0 .. max_len - (gamma + 1) * 2 tokens, a block table
+    [R, max_blocks] holding each request's committed pages (page ids a random
+    permutation, -1 past the committed ones), and a stack of free pages with
+    enough room for every request to verify gamma + 1 more rows (plus
+    spare_pages)."""
+    R, gamma, seed = w["R"], w["gamma"], w["seed"]
+    g = rng(seed, 15)
+    max_blocks = -(-max_len // page_size)
+    kv_len = g.integers(0, max_len - 2 * (gamma + 1), size=R, dtype=np.int64).astype(np.int32)
+    held = -(-kv_len.astype(np.int64) // page_size)
+    extra = -(-(kv_len.astype(np.int64) + gamma + 1) // page_size) - held
+    n_pages = int(held.sum() + extra.sum()) + spare_pages
+    perm = g.permutation(n_pages).astype(np.int32)
+    bt = np.full((R, max_blocks), -1, np.int32)
+    o = 0
+    for r in range(R):
+        bt[r, : held[r]] = perm[o: o + held[r]]
+        o += int(held[r])
+    free = np.zeros(n_pages, np.int32)
+    free[: n_pages - o] = perm[o:]
+    return dict(kv_len=kv_len, block_table=bt, free_pages=free, free_top=n_pages - o,
+                page_size=page_size, n_pages=n_pages)

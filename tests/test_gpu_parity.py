@@ -433,6 +433,89 @@ def test_plan_cycles_parity(B, orc, mode):
     np.testing.assert_allclose(g["theta_real"][keep], o["theta_real"][keep], rtol=1e-12)
 
 
+@pytest.mark.parametrize("N,gamma,tau,zero", [(200_000, 5, None, False), (1000, 3, [1.0, 2.0, 0.5], False),
+                                               (37, 4, None, False), (5000, 3, None, True)])
+def test_fit_temperatures_parity(B, orc, N, gamma, tau, zero):
+    """Sequential temperature scaling on the GPU against the oracle: the samples
+    per position exactly, the temperatures and mean NLL to fp64 rounding of two
+    Newton iterations converged to the same minimiser (relative 1e-6 and 1e-9);
+    with every label 0 the later positions keep tau = 1."""
+    w = inputs.workload("confidence_scheduled", gamma=gamma)
+    cs = inputs.calibration_samples(w, N, tau_true=tau)
+    if zero:
+        cs["accepted"][:] = 0
+    o = orc.fit_temperatures(cs["z"], cs["accepted"])
+    G = H.Guarded()
+    t = G.out((gamma,), torch.float32, float("nan"))
+    nll = G.out((gamma,), torch.float64, float("nan"))
+    cnt = G.out((gamma,), torch.int32, -7)
+    ws = G.workspace(B.dspark_workspace_size(B.DSPARK_OP_CALIBRATE, 0, gamma, 0))
+    status = G.out((1,), torch.int32, 0)
+    B.dspark_fit_temperatures(H.dev(cs["z"]), H.dev(cs["accepted"]), t, nll, cnt, ws, status)
+    torch.cuda.synchronize()
+    G.check()
+    assert int(status.item()) == 0 and o["status"] == 0
+    np.testing.assert_array_equal(H.host(cnt), o["count"])
+    np.testing.assert_allclose(H.host(t), o["tau"], rtol=1e-6)
+    np.testing.assert_allclose(H.host(nll), o["nll"], rtol=1e-9, atol=1e-12)
+    if zero:
+        assert (H.host(t)[1:] == 1.0).all()
+
+
+def test_kv_reserve_commit_parity(B, orc):
+    """Forty cycles of reserve -> verify outcome -> commit on a 512-request paged
+    KV cache (page size 16) against the oracle: lengths, block table, the whole
+    free stack and its top bit-exact after every call (the stack order is a
+    scan over the requests, so it is unique); then the two failure cases."""
+    w = inputs.workload("confidence_scheduled")
+    kv = inputs.kv_state(w, page_size=16, max_len=4096, spare_pages=3)
+    st = orc.KvState(kv["kv_len"], kv["block_table"], kv["free_pages"], kv["free_top"], kv["page_size"])
+    G = H.Guarded()
+    d_len = G.out((w["R"],), torch.int32, 0); d_len.copy_(H.dev(st.kv_len))
+    d_bt = G.out(st.block_table.shape, torch.int32, 0); d_bt.copy_(H.dev(st.block_table))
+    d_free = G.out(st.free_pages.shape, torch.int32, 0); d_free.copy_(H.dev(st.free_pages))
+    d_top = G.out((1,), torch.int32, 0); d_top.copy_(H.dev(st.free_top))
+    d_res = G.out((w["R"],), torch.int32, -7)
+    status = G.out((1,), torch.int32, 0)
+    g = np.random.default_rng(7)
+    P = kv["page_size"]
+
+    def same():
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(H.host(d_len), st.kv_len)
+        np.testing.assert_array_equal(H.host(d_bt), st.block_table)
+        np.testing.assert_array_equal(H.host(d_free), st.free_pages)
+        assert int(d_top.item()) == int(st.free_top[0])
+
+    for cycle in range(40):
+        l = g.integers(0, w["gamma"] + 1, size=w["R"]).astype(np.int32)
+        n_acc = (g.random(w["R"]) * (l + 1)).astype(np.int32)
+        rc, res = orc.kv_reserve(st, l)
+        assert rc == 0
+        B.dspark_kv_reserve(d_len, H.dev(l), P, d_bt, d_free, d_top, d_res, status)
+        same()
+        np.testing.assert_array_equal(H.host(d_res), res)
+        assert orc.kv_commit(st, l, n_acc) == 0
+        B.dspark_kv_commit(d_len, H.dev(l), H.dev(n_acc), P, d_bt, d_free, d_top, status)
+        same()
+        # requests past 3000 tokens finish: their pages go back (the same on both sides)
+        for r in np.nonzero(st.kv_len > 3000)[0]:
+            pages = st.block_table[r][st.block_table[r] >= 0]
+            st.free_pages[st.free_top[0]: st.free_top[0] + len(pages)] = pages
+            st.free_top[0] += len(pages)
+            st.block_table[r] = -1
+            st.kv_len[r] = 0
+        d_len.copy_(H.dev(st.kv_len)); d_bt.copy_(H.dev(st.block_table))
+        d_free.copy_(H.dev(st.free_pages)); d_top.copy_(H.dev(st.free_top))
+    assert int(status.item()) == 0
+    # too few free pages: nothing changes and the capacity error is reported
+    d_top.fill_(0); st.free_top[0] = 0
+    B.dspark_kv_reserve(d_len, H.dev(np.full(w["R"], w["gamma"], np.int32)), P, d_bt, d_free, d_top, None, status)
+    same()
+    assert int(status.item()) == B.DSPARK_ERR_CAPACITY
+    G.check()
+
+
 def test_select_ties_and_errors(B, orc):
     c = np.array([[1.0, 1.0], [1.0, 0.5], [0.7, 0.7]], np.float32)
     for K_cap in range(3, 10):

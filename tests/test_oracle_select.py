@@ -254,3 +254,49 @@ def test_plan_cycles_history_is_causal(orc):
     c = orc.plan_cycles(same, None, sizes, sps, K_cap, 2)
     np.testing.assert_array_equal(h["l"][2:], c["l"][2:])
     np.testing.assert_allclose(h["theta_pred"][2:], c["theta_pred"][2:], rtol=1e-15)
+
+
+def _nll(beta, z, y):
+    x = beta * z.astype(np.float64)
+    return float(np.sum(np.logaddexp(0.0, x) - y * x))
+
+
+def test_fit_temperatures_recovers_and_matches_library(orc):
+    """Sequential temperature scaling: on labels drawn from known per-position
+    temperatures the fit recovers them, and every position's temperature is the
+    minimiser of its conditioned NLL found by scipy's bounded scalar search on
+    the samples that reached the position."""
+    from scipy.optimize import minimize_scalar
+    w = inputs.workload("confidence_scheduled")
+    cs = inputs.calibration_samples(w, 200_000)
+    out = orc.fit_temperatures(cs["z"], cs["accepted"])
+    assert out["status"] == 0
+    np.testing.assert_allclose(out["tau"], cs["tau_true"], rtol=0.03)
+    acc = cs["accepted"].astype(np.float64)
+    for k in range(w["gamma"]):
+        reached = np.ones(len(acc), bool) if k == 0 else acc[:, :k].all(axis=1)
+        assert out["count"][k] == reached.sum()
+        zk, yk = cs["z"][reached, k], acc[reached, k]
+        res = minimize_scalar(lambda b: _nll(b, zk, yk), bounds=(1e-3, 1e3), method="bounded",
+                              options={"xatol": 1e-12})
+        assert 1.0 / out["tau"][k] == pytest.approx(res.x, rel=1e-5)
+        assert out["nll"][k] == pytest.approx(_nll(res.x, zk, yk) / reached.sum(), rel=1e-9)
+
+
+def test_fit_temperatures_conditions_on_reaching_the_position(orc):
+    """Labels after a rejection do not enter the fit (setting them all to 1
+    changes nothing), whereas fitting position 1 on every sample would give a
+    different temperature; a position no sample reaches keeps tau = 1."""
+    w = inputs.workload("confidence_scheduled", gamma=3)
+    cs = inputs.calibration_samples(w, 50_000, tau_true=[1.0, 2.0, 0.5])
+    base = orc.fit_temperatures(cs["z"], cs["accepted"])
+    noisy = cs["accepted"].copy()
+    reached = np.concatenate([np.ones((len(noisy), 1), bool),
+                              np.cumprod(noisy, axis=1)[:, :-1].astype(bool)], axis=1)
+    noisy[~reached] = 1
+    alt = orc.fit_temperatures(cs["z"], noisy)
+    np.testing.assert_array_equal(alt["tau"], base["tau"])
+    wrong = orc.fit_temperatures(cs["z"][:, 1:2], noisy[:, 1:2])  # position 1 on every sample
+    assert abs(wrong["tau"][0] - base["tau"][1]) > 0.05
+    none = orc.fit_temperatures(cs["z"], np.zeros_like(cs["accepted"]))
+    assert none["count"][1] == 0 and none["tau"][1] == 1.0 and none["tau"][2] == 1.0
