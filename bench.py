@@ -366,9 +366,9 @@ class Cycle:
                 self._draft(0, self.U, self.anchor, self.seeds)
         # launches of this library per step: tensor cores, every position and the
         # finalize in one launch; CUDA cores, counter reset then bias and sample
-        # kernels per position.  Verify: prologue, rounds (residual draw, finalize).
+        # kernels per position.  Verify: prologue, rounds (and the residual draw).
         draft_launches = 1 if self.uses_tc else 1 + 2 * gamma
-        verify_launches = 4 if self.T > 0 else 2
+        verify_launches = 3 if self.T > 0 else 2
         self.launches_per_step = (int(self.run_select) + draft_launches * int(self.run_draft) +
                                   verify_launches * int(self.run_verify) + int(self.run_commit))
 
@@ -609,7 +609,7 @@ def kv_study(cycles=50):
     import torch
     from speculative_decoding_dspark_gb300 import binding as B
     w = inputs.workload("confidence_scheduled")
-    kv = inputs.kv_state(w, page_size=16, max_len=4096, spare_pages=R_SPARE)
+    kv = inputs.kv_state(w, page_size=16, max_len=4096, spare_pages=R_SPARE, headroom=6 * cycles)
     dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
     g = np.random.default_rng(3)
     R, gamma = w["R"], w["gamma"]
@@ -775,7 +775,7 @@ def cyc_launches(args, w):
     R, V, gamma, rank = w["R"], w["V"], w["gamma"], w["rank"]
     uses_tc = B.dspark_markov_draft_uses_tensor_cores(B.DSPARK_BF16, B.DSPARK_BF16, R, V, rank)
     draft = (1 if uses_tc else 1 + 2 * gamma) * int(args.stage in ("cycle", "draft"))
-    verify = (4 if float(w["temperature"]) > 0 else 2) * int(args.stage in ("cycle", "verify"))
+    verify = (3 if float(w["temperature"]) > 0 else 2) * int(args.stage in ("cycle", "verify"))
     varlen = bool(w.get("varlen"))
     return int(args.stage == "cycle" and not varlen) + draft + verify + int(args.stage == "cycle")
 

@@ -117,6 +117,7 @@ int dspark_markov_draft_uses_tensor_cores(int u_dtype, int w_dtype, int R, int V
 
 size_t dspark_workspace_size(int op, int R, int gamma, int V, int rank, int max_rows,
                              int w_dtype, unsigned flags) {
+    if (op == DSPARK_OP_CALIBRATE) return (gamma <= 0 || gamma > 16) ? 0 : calibrate_workspace(gamma);
     if (R <= 0) return 0;
     switch (op) {
         case DSPARK_OP_DRAFT:
@@ -131,9 +132,6 @@ size_t dspark_workspace_size(int op, int R, int gamma, int V, int rank, int max_
             return align_up(verify_layout(R, V).total) + residual_tc_workspace(R, rank);
         case DSPARK_OP_SELECT:
             return 0;
-        case DSPARK_OP_CALIBRATE:
-            if (gamma <= 0 || gamma > 16) return 0;
-            return calibrate_workspace(gamma);
         default:
             return 0;
     }

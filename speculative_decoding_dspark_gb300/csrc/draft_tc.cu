@@ -18,7 +18,7 @@
 //             whole vocabulary, and recomputing one row per request costs one
 //             pass over W2 instead of keeping every drafted row in memory),
 //             then the extra token is drawn from max(0, p - q), or from p after
-//             full acceptance.
+//             full acceptance (the last CTA to finish writes the tokens).
 //
 // Persistent, one CTA per SM, 19 warps:
 //   A (M = 128 requests x K = rank) = rows W1[prev], copied by the epilogue
@@ -143,6 +143,7 @@ struct TcParams {
     float* q_tok;
     const float* target;
     const ResRow* rows;
+    int32_t* out_tokens;       // residual: [R][gamma + 1]
     // draft: the grid barriers between positions wait at most wait_ns; their
     // arrival count is the grid's plus phantom (1 only in the timeout test)
     unsigned long long wait_ns;
@@ -158,6 +159,8 @@ struct Bars {
     uint32_t tmem_slot;
     int abort_flag;
     int step_ok;               // the grid barrier after a step passed (read by every epilogue warp)
+    int fin_last, fin_nfb;     // residual tokens: this CTA is the last one done; requests drawn from p
+    unsigned long long fin_key;
     int a_tok[kM];             // the step's A rows' tokens: -1 zero row, -2 nothing to compute for the request
 };
 // Residual-only shared memory after the barriers: per request row and epilogue
@@ -331,6 +334,73 @@ __device__ __forceinline__ bool step_barrier(unsigned* done, int* abort_word, un
     return true;
 }
 
+
+// Residual launch, after every CTA has published its winner keys: the last
+// CTA to finish writes every request's extra token -- the race's winner, or,
+// when a rejected row's residual had no positive mass (p <= q everywhere, a
+// rounding-level event), a draw from p of the row with the same noise, made by
+// the whole CTA.  The dynamic shared memory is free by then and holds the list
+// of those requests.  keys[R] counts the CTAs that are done (zeroed with the
+// keys by the verify prologue).
+__device__ void residual_tokens_if_last(const TcParams& p, uint8_t* smem, Bars& bar) {
+    int& s_last = bar.fin_last;
+    int& s_nfb = bar.fin_nfb;
+    unsigned long long& s_key = bar.fin_key;
+    if (threadIdx.x == 0) {
+        __threadfence();  // this CTA's keys before its count
+        s_last = atomicAdd(p.keys + p.R, 1ull) == (unsigned long long)(gridDim.x - 1);
+        s_nfb = 0;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();  // every CTA's keys (their counts came first)
+    int* fb = reinterpret_cast<int*>(smem);
+    const int g1 = p.gamma + 1;
+    for (int r = threadIdx.x; r < p.R; r += blockDim.x) {  // one request per thread
+        const int mode = p.rows[r].mode, pos = p.rows[r].pos;
+        const unsigned long long key = __ldcg(p.keys + r);
+        if (mode == 0) continue;
+        if (key == 0 && mode == 1) {
+            fb[atomicAdd(&s_nfb, 1)] = r;
+            continue;
+        }
+        const int tok = key ? key_index(key) : -1;
+        if (tok < 0) report(p.dev_status, DSPARK_ERR_DEVICE_INPUT);  // no finite score (NaN logits)
+        p.out_tokens[(size_t)r * g1 + pos] = tok;
+    }
+    __syncthreads();
+    const float c2 = p.invT * kLog2eF;
+    for (int i = 0; i < s_nfb; ++i) {
+        const int r = fb[i];
+        const ResRow ri = p.rows[r];
+        if (threadIdx.x == 0) s_key = 0;
+        __syncthreads();
+        const float* trow = p.target + (size_t)ri.trow * p.V;
+        const uint64_t seed = p.seeds[r];
+        float bw = 0.0f, bE = 1.0f;
+        int bi = INT_MAX;
+        for (int v4 = threadIdx.x; 4 * v4 < p.V; v4 += blockDim.x) {
+            const uint4 x = philox4x32_10(make_uint4((uint32_t)v4, (uint32_t)ri.pos, (uint32_t)r, ri.w3),
+                                          (uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int v = 4 * v4 + e;
+                if (v >= p.V) break;
+                const float pv = ex2(fmaf(__ldg(trow + v), c2, -ri.lse2_p));
+                const float E = neg_log_uniform(word_of(x, e));
+                if (pv * bE > bw * E) { bw = pv; bE = E; bi = v; }
+            }
+        }
+        if (bi != INT_MAX) atomicMax(&s_key, winner_key(logf(bw) - logf(bE), bi));
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const int tok = s_key ? key_index(s_key) : -1;
+            if (tok < 0) report(p.dev_status, DSPARK_ERR_DEVICE_INPUT);
+            p.out_tokens[(size_t)r * g1 + ri.pos] = tok;
+        }
+        __syncthreads();
+    }
+}
 
 template <bool kRes>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -850,11 +920,16 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                                         cand &= cand - 1u;
                                         const float sc = pick<16>(sv, c);
                                         const float w = ex2(fmaf(sc, c2, nm));
-                                        const float E = neg_log_uniform(pick<16>(words, c));
-                                        if (w * bE > bw * E) {
-                                            bw = w; bE = E; part.idx = v0 + c; part.s_at = sc * c2;
-                                            rho = fminf(rho, race_bound(bE, bw));
-                                            rec = true;
+                                        const uint32_t wd = pick<16>(words, c);
+                                        // marked against the pass's first bound: test again against
+                                        // the record this pass may have raised before the logarithm
+                                        if (one_plus_complement(wd) < fmaf(w, rho, 1.0f)) {
+                                            const float E = neg_log_uniform(wd);
+                                            if (w * bE > bw * E) {
+                                                bw = w; bE = E; part.idx = v0 + c; part.s_at = sc * c2;
+                                                rho = fminf(rho, race_bound(bE, bw));
+                                                rec = true;
+                                            }
                                         }
                                     } while (cand);
                                 }
@@ -1113,50 +1188,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         tc::tmem_dealloc(tmem_base, kRes ? kTmemColsRes : kTmemCols);
     }
     if (*abort_flag && threadIdx.x == 0) report(p.dev_status, DSPARK_ERR_TIMEOUT);
-}
-
-// The extra token of every request, one CTA each: the race's winner (over
-// max(0, p - q) for a rejected row, over p for a bonus draw).  When a rejected
-// row's residual has no positive mass (p <= q everywhere), the CTA draws from
-// p of the row with the same noise.
-__global__ void __launch_bounds__(256) residual_finalize_kernel(const ResRow* rows, const unsigned long long* keys,
-                                                                const float* target, const uint64_t* seeds,
-                                                                float invT, int gamma, int V, int32_t* out_tokens,
-                                                                int32_t* dev_status) {
-    __shared__ unsigned long long s_key;
-    const int r = blockIdx.x;
-    const ResRow ri = rows[r];
-    if (ri.mode == 0) return;
-    unsigned long long key = keys[r];
-    if (key == 0 && ri.mode == 1) {
-        if (threadIdx.x == 0) s_key = 0;
-        __syncthreads();
-        const float c2 = invT * kLog2eF;
-        const float* trow = target + (size_t)ri.trow * V;
-        const uint64_t seed = seeds[r];
-        float bw = 0.0f, bE = 1.0f;
-        int bi = INT_MAX;
-        for (int v4 = threadIdx.x; 4 * v4 < V; v4 += blockDim.x) {
-            const uint4 x = philox4x32_10(make_uint4((uint32_t)v4, (uint32_t)ri.pos, (uint32_t)r, ri.w3),
-                                          (uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32));
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int v = 4 * v4 + e;
-                if (v >= V) break;
-                const float pv = ex2(fmaf(__ldg(trow + v), c2, -ri.lse2_p));
-                const float E = neg_log_uniform(word_of(x, e));
-                if (pv * bE > bw * E) { bw = pv; bE = E; bi = v; }
-            }
-        }
-        if (bi != INT_MAX) atomicMax(&s_key, winner_key(logf(bw) - logf(bE), bi));
-        __syncthreads();
-        key = s_key;
-    }
-    if (threadIdx.x == 0) {
-        const int tok = key ? key_index(key) : -1;
-        if (tok < 0) report(dev_status, DSPARK_ERR_DEVICE_INPUT);  // no finite score (NaN logits)
-        out_tokens[(size_t)r * (gamma + 1) + ri.pos] = tok;
-    }
+    if constexpr (kRes) residual_tokens_if_last(p, smem, bar);
 }
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -1178,16 +1210,17 @@ EncodeTiled encoder() {
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Workspace: winner keys, (draft) the step counters and the abort word of the
-// launch's grid barrier, zeroed with the keys, then (draft) the per-CTA
-// normaliser pieces or (residual) the per-request rows.
+// Workspace: winner keys (residual: and after them the count of CTAs done),
+// (draft) the step counters and the abort word of the launch's grid barrier,
+// zeroed with the keys, then (draft) the per-CTA normaliser pieces or
+// (residual) the per-request rows.
 struct TcLayout {
     size_t keys, n_keys, step_done, zero_bytes, parts, rows, total;
 };
 TcLayout tc_layout(int R, int gamma, bool residual) {
     TcLayout L;
     size_t off = 0;
-    L.n_keys = residual ? (size_t)R : (size_t)gamma * R;
+    L.n_keys = residual ? (size_t)R + 1 : (size_t)gamma * R;  // residual: + the count of CTAs done
     L.keys = off; off += sizeof(unsigned long long) * L.n_keys;
     L.step_done = off; off += residual ? 0 : sizeof(unsigned) * ((size_t)gamma + 1);
     L.zero_bytes = off;
@@ -1355,14 +1388,13 @@ int launch_residual_tc(const ResidualTcArgs& a, cudaStream_t stream) {
     p.greedy = 0;
     p.target = a.target;
     p.rows = rows;
+    p.out_tokens = a.out_tokens;
     p.wait_ns = kWaitNs;  // no grid barrier in the residual launch
     p.phantom = 0;
     if (cudaFuncSetAttribute(markov_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return DSPARK_ERR_CUDA;
     markov_tc_kernel<true><<<grid, kThreads, smem, stream>>>(tm_w2, tm_u, p);
-    residual_finalize_kernel<<<a.R, 256, 0, stream>>>(rows, p.keys, a.target, a.seeds, a.invT, a.gamma, a.V,
-                                                      a.out_tokens, a.dev_status);
     return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 

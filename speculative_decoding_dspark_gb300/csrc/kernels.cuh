@@ -73,7 +73,8 @@ struct VerifyParams {
     // dspark_verify_markov only (else NULL): the residual rows, written as the
     // requests are decided, and what they need
     ResRow* res_rows = nullptr;       // [R]
-    unsigned long long* res_keys = nullptr;  // [R] the residual draw's winner keys, zeroed by the prologue
+    unsigned long long* res_keys = nullptr;  // [R + 1] the residual draw's winner keys and its count of
+                                             // CTAs done, zeroed by the prologue
     const int32_t* anchor = nullptr;  // [R]
     const uint16_t* W1 = nullptr;     // [V, rank] bf16: each predecessor's row is requested into L2
     int rank = 0;

@@ -47,6 +47,7 @@ __global__ void __launch_bounds__(1024) verify_prologue_kernel(VerifyParams p) {
     if (threadIdx.x == 0) {
         p.ok[0] = ok;
         if (!ok) report(p.dev_status, DSPARK_ERR_DEVICE_INPUT);
+        if (p.res_keys) p.res_keys[p.R] = 0ull;  // the residual launch's count of CTAs done
     }
     for (int r = threadIdx.x; r < p.R; r += blockDim.x) {
         p.cnt1[r] = 0;

@@ -229,16 +229,17 @@ def calibration_samples(w: dict, n_samples: int, tau_true=None) -> dict:
     return dict(z=z, accepted=reached.astype(np.uint8), tau_true=tau.astype(np.float32))
 
 
-def kv_state(w: dict, page_size: int = 16, max_len: int = 4096, spare_pages: int = 0) -> dict:
+def kv_state(w: dict, page_size: int = 16, max_len: int = 4096, spare_pages: int = 0,
+             headroom: int = 0) -> dict:
     """A paged KV cache's bookkeeping before a cycle: committed lengths
     kv_len [R] uniform in 0 .. max_len - (gamma + 1) * 2 tokens, a block table
-    [R, max_blocks] holding each request's committed pages (page ids a random
-    permutation, -1 past the committed ones), and a stack of free pages with
-    enough room for every request to verify gamma + 1 more rows (plus
-    spare_pages)."""
+    [R, max_blocks] (room for max_len + headroom tokens) holding each request's
+    committed pages (page ids a random permutation, -1 past the committed
+    ones), and a stack of free pages with enough room for every request to
+    verify gamma + 1 more rows (plus spare_pages)."""
     R, gamma, seed = w["R"], w["gamma"], w["seed"]
     g = rng(seed, 15)
-    max_blocks = -(-max_len // page_size)
+    max_blocks = -(-(max_len + headroom) // page_size)
     kv_len = g.integers(0, max_len - 2 * (gamma + 1), size=R, dtype=np.int64).astype(np.int32)
     held = -(-kv_len.astype(np.int64) // page_size)
     extra = -(-(kv_len.astype(np.int64) + gamma + 1) // page_size) - held

@@ -63,6 +63,8 @@ def test_workspace_sizes(lib):
     d = ws(0, 4, 5, 64, 8, 0, 0, 1)
     assert d >= 4 * 64 * 4
     assert ws(0, 4, 0, 64, 8, 0, 0, 0) == 0
+    # calibration: partial sums per position, independent of the sample count
+    assert ws(4, 0, 5, 0, 0, 0, 0, 0) > 0 and ws(4, 0, 17, 0, 0, 0, 0, 0) == 0
 
 
 def test_host_argument_checks(lib):
