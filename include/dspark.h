@@ -85,6 +85,9 @@ typedef struct CUstream_st* dspark_stream_t;
 #define DSPARK_OP_VERIFY_MARKOV 3
 #define DSPARK_OP_CALIBRATE 4
 
+/* ---- dspark_workspace_size flags for DSPARK_OP_VERIFY_MARKOV --------------------- */
+#define DSPARK_VERIFY_HOST_TARGET 1u /* target_logits will be pinned host memory */
+
 /* ---- dspark_markov_draft flags ---------------------------------------------- */
 #define DSPARK_DRAFT_FORCE_SIMT 1u   /* use the CUDA-core kernels even where the
                                         tensor-core kernel applies (testing) */
@@ -234,6 +237,18 @@ int dspark_verify(const float* target_logits, const int32_t* cu_seqlens,
  * kernel does not take (use dspark_verify with q_logits there), and at
  * temperature > 0 when target_logits, U, W1 or W2 is not 16-byte aligned (the
  * residual kernel reads the rows in 16-byte pieces).
+ *
+ * Target rows in host memory.  target_logits may also point to pinned
+ * (page-locked) host memory that the device can read (cudaHostAlloc /
+ * cudaHostRegister; on a Grace-Blackwell node the link is NVLink-C2C): the
+ * kernels then read across the link only the rows they examine -- each
+ * request's rows up to its first rejection -- instead of the caller copying
+ * every presented row.  The decision pass keeps a device copy of each request's
+ * latest row for the residual draw, so at temperature > 0 the workspace must be
+ * dspark_workspace_size(DSPARK_OP_VERIFY_MARKOV, R, gamma, V, rank, max_rows,
+ * DSPARK_BF16, DSPARK_VERIFY_HOST_TARGET) bytes (R * V * 4 more).  Pageable host
+ * memory is refused (DSPARK_ERR_UNSUPPORTED), and so is any host memory in
+ * dspark_verify.
  */
 int dspark_verify_markov(const float* target_logits, const int32_t* cu_seqlens,
                          const int32_t* draft_tokens, const void* U, const void* W1,

@@ -29,6 +29,7 @@ DSPARK_ERR_WORKSPACE = -7
 DSPARK_F32, DSPARK_BF16 = 0, 1
 DSPARK_OP_DRAFT, DSPARK_OP_VERIFY, DSPARK_OP_SELECT, DSPARK_OP_VERIFY_MARKOV, DSPARK_OP_CALIBRATE = 0, 1, 2, 3, 4
 DSPARK_DRAFT_FORCE_SIMT = 1
+DSPARK_VERIFY_HOST_TARGET = 1
 DSPARK_SELECT_FIXED, DSPARK_SELECT_HISTORY, DSPARK_SELECT_CURRENT, DSPARK_SELECT_FIRST_STOP = 0, 1, 2, 3
 DSPARK_SELECT_CONF_CUTOFF, DSPARK_SELECT_SURVIVAL_CUTOFF = 4, 5
 DSPARK_INJECT_VERIFY_BARRIER, DSPARK_INJECT_DRAFT_BARRIER = 1, 2
@@ -131,13 +132,13 @@ def _dtype_code(t):
     raise TypeError(f"expected float32 or bfloat16, got {t.dtype}")
 
 
-def _check(t, name, dtype=None, shape=None, allow_none=False):
+def _check(t, name, dtype=None, shape=None, allow_none=False, allow_pinned=False):
     if t is None:
         if allow_none:
             return
         raise ValueError(f"{name} is required")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_cuda and not (allow_pinned and t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor" + (" or pinned host memory" if allow_pinned else ""))
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
@@ -231,7 +232,7 @@ def dspark_verify_markov(target_logits, cu_seqlens, draft_tokens, U, W1, W2, anc
     R, gamma = draft_tokens.shape
     V = target_logits.shape[1]
     rank = W1.shape[1]
-    _check(target_logits, "target_logits", torch.float32)
+    _check(target_logits, "target_logits", torch.float32, allow_pinned=True)
     _check(cu_seqlens, "cu_seqlens", torch.int32, (R + 1,))
     _check(draft_tokens, "draft_tokens", torch.int32)
     _check(U, "U", torch.bfloat16, (R, gamma, V))

@@ -71,6 +71,20 @@ bool tc_applies(int u_dtype, int w_dtype, int R, int V, int rank, unsigned flags
 
 bool valid_dtype(int d) { return d == DSPARK_F32 || d == DSPARK_BF16; }
 
+// Where a caller's pointer lives: device (or managed) memory, pinned host memory
+// the device can read, or memory the device cannot be trusted to read.
+enum class Residence { kDevice, kPinnedHost, kOther };
+Residence residence(const void* ptr) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free error of the query
+        return Residence::kOther;
+    }
+    if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return Residence::kDevice;
+    if (at.type == cudaMemoryTypeHost && at.devicePointer == ptr) return Residence::kPinnedHost;
+    return Residence::kOther;
+}
+
 // Process-wide settings of the grid-wide waits (see dspark_set_wait_limit_ns).
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
 std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
@@ -127,9 +141,12 @@ size_t dspark_workspace_size(int op, int R, int gamma, int V, int rank, int max_
         case DSPARK_OP_VERIFY:
             if (V <= 0 || max_rows < 0) return 0;
             return verify_layout(R, V).total;
-        case DSPARK_OP_VERIFY_MARKOV:
+        case DSPARK_OP_VERIFY_MARKOV: {
             if (V <= 0 || max_rows < 0 || rank <= 0) return 0;
-            return align_up(verify_layout(R, V).total) + residual_tc_workspace(R, rank);
+            const size_t base = align_up(verify_layout(R, V).total) + residual_tc_workspace(R, rank);
+            // a host-resident target keeps each request's latest row on the device
+            return (flags & DSPARK_VERIFY_HOST_TARGET) ? align_up(base) + align_up(sizeof(float) * (size_t)R * V) : base;
+        }
         case DSPARK_OP_SELECT:
             return 0;
         default:
@@ -203,6 +220,7 @@ int dspark_verify(const float* target_logits, const int32_t* cu_seqlens,
     if ((long long)max_rows * ((V + kStatChunk - 1) / kStatChunk) >= (1LL << 31) ||
         (long long)R * nchunk >= (1LL << 31))
         return DSPARK_ERR_UNSUPPORTED;
+    if (residence(target_logits) != Residence::kDevice) return DSPARK_ERR_UNSUPPORTED;
 
     VerifyParams p;
     p.target = target_logits; p.cu = cu_seqlens; p.y = draft_tokens; p.q_logits = q_logits;
@@ -243,9 +261,14 @@ int dspark_verify_markov(const float* target_logits, const int32_t* cu_seqlens,
     if (!greedy && (!aligned16(U) || !aligned16(W1) || !aligned16(W2) || !aligned16(target_logits)))
         return DSPARK_ERR_UNSUPPORTED;
     if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return DSPARK_ERR_WORKSPACE;
+    const Residence where = residence(target_logits);
+    if (where == Residence::kOther) return DSPARK_ERR_UNSUPPORTED;
+    const bool host_target = where == Residence::kPinnedHost && !greedy;
     const VerifyLayout L = verify_layout(R, V);
     const size_t res_off = align_up(L.total);
-    if (ws_bytes < res_off + residual_tc_workspace(R, rank)) return DSPARK_ERR_WORKSPACE;
+    const size_t copy_off = align_up(res_off + residual_tc_workspace(R, rank));
+    if (ws_bytes < (host_target ? copy_off + sizeof(float) * (size_t)R * V : res_off + residual_tc_workspace(R, rank)))
+        return DSPARK_ERR_WORKSPACE;
     const int nchunk = (V + kVerifyChunk - 1) / kVerifyChunk;
     if ((long long)max_rows * ((V + kStatChunk - 1) / kStatChunk) >= (1LL << 31)) return DSPARK_ERR_UNSUPPORTED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -272,6 +295,7 @@ int dspark_verify_markov(const float* target_logits, const int32_t* cu_seqlens,
         p.anchor = anchor;
         p.W1 = static_cast<const uint16_t*>(W1);
         p.rank = rank;
+        if (host_target) p.row_copy = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + copy_off);
     }
     const cudaError_t e = launch_verify_decide(p, s);
     if (e != cudaSuccess) return DSPARK_ERR_CUDA;
@@ -280,7 +304,7 @@ int dspark_verify_markov(const float* target_logits, const int32_t* cu_seqlens,
     ResidualTcArgs a;
     a.U = U; a.W1 = W1; a.W2 = W2; a.seeds = seeds;
     a.cycle = cycle; a.invT = p.invT; a.R = R; a.gamma = gamma; a.V = V; a.rank = rank;
-    a.target = target_logits;
+    a.target = host_target ? p.row_copy : target_logits;  // rows by request (host target) or packed
     a.out_tokens = out_tokens; a.dev_status = dev_status;
     a.ws = static_cast<unsigned char*>(ws) + res_off;
     return launch_residual_tc(a, s);

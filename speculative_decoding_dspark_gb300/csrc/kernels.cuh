@@ -78,6 +78,10 @@ struct VerifyParams {
     const int32_t* anchor = nullptr;  // [R]
     const uint16_t* W1 = nullptr;     // [V, rank] bf16: each predecessor's row is requested into L2
     int rank = 0;
+    // target rows in pinned host memory (dspark_verify_markov): every row the
+    // decision pass streams is also stored here, [R, V], so that the residual
+    // launch reads each request's last row from device memory
+    float* row_copy = nullptr;
     // the grid barriers between rounds: wait limit, and an arrival count one
     // above the grid's when the barrier-timeout test injection is on
     unsigned long long wait_ns = 2000000000ull;

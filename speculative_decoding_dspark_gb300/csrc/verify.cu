@@ -187,7 +187,7 @@ __device__ __forceinline__ DecideInputs decide_inputs(const VerifyParams& p, int
     if (d.valid && j < d.l) {
         d.y = p.y[(size_t)r * p.gamma + j];
         if (!kGreedy) {
-            d.t = __ldg(p.target + (size_t)(d.first + j) * p.V + d.y);
+            d.t = __ldcg(p.target + (size_t)(d.first + j) * p.V + d.y);  // (the target may be host memory)
             d.q = p.q_tok[(size_t)r * p.gamma + j];
             d.seed = p.seeds[r];
         }
@@ -283,7 +283,7 @@ __device__ __forceinline__ int decide_request(const VerifyParams& p, const RowSt
                 ResRow w;
                 w.mode = job.mode;
                 w.pos = n;
-                w.trow = job.row;
+                w.trow = p.row_copy ? r : job.row;  // the residual reads the device copy of the row
                 w.w3 = ctr_word3(p.cycle, job.mode == 1 ? kResidualGumbel : kBonusGumbel);
                 w.lse2_p = lse2;
                 w.q_lse2 = job.mode == 1 ? p.q_lse[(size_t)r * g + n] * kLog2e : 0.0f;
@@ -359,6 +359,14 @@ __global__ void __launch_bounds__(kRoundThreads, 1) verify_rounds_kernel(VerifyP
             }
             float m = -INFINITY, s = 0.0f, bm = -INFINITY;
             int bi = INT_MAX;
+            if (vec && p.row_copy) {  // host-resident target: keep the request's latest row on the device
+                float* dst = p.row_copy + (size_t)r * V;
+#pragma unroll
+                for (int i = 0; i < kStatVec; ++i) {
+                    const int v = v0 + 4 * (lane + 32 * i);
+                    if (v < V) *reinterpret_cast<float4*>(dst + v) = buf[i];
+                }
+            }
             if (vec) {
                 if (kGreedy) {
 #pragma unroll
@@ -385,7 +393,11 @@ __global__ void __launch_bounds__(kRoundThreads, 1) verify_rounds_kernel(VerifyP
             } else {
                 const int v1 = min(V, v0 + kStatChunk);
                 const float* base = p.target + (size_t)row * V;
-                for (int v = v0 + lane; v < v1; v += 32) stat_elem<kGreedy>(__ldg(base + v), v, c2, m, s, bm, bi);
+                for (int v = v0 + lane; v < v1; v += 32) {
+                    const float x = __ldcg(base + v);
+                    if (p.row_copy) p.row_copy[(size_t)r * V + v] = x;
+                    stat_elem<kGreedy>(x, v, c2, m, s, bm, bi);
+                }
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {

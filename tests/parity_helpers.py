@@ -124,8 +124,9 @@ def gpu_verify(target, cu, y, q_logits, q_lse, q_tok, seeds, cycle, temperature,
     return dict(n_acc=host(n_acc), out_tokens=host(out), p_tok=host(p_tok), status=int(status.item()))
 
 
-def gpu_verify_markov(target, cu, d, g, cycle, temperature, max_rows=None):
-    """dspark_verify_markov on the GPU draft g of inputs d (drafter logits recomputed)."""
+def gpu_verify_markov(target, cu, d, g, cycle, temperature, max_rows=None, host_target=False):
+    """dspark_verify_markov on the GPU draft g of inputs d (drafter logits recomputed);
+    host_target: target is a pinned host tensor read by the kernels across the link."""
     t = lambda a: a if isinstance(a, torch.Tensor) else dev(a)
     target_d, cu_d = t(target), t(cu)
     y_d = g["y_dev"]
@@ -138,7 +139,8 @@ def gpu_verify_markov(target, cu, d, g, cycle, temperature, max_rows=None):
     n_acc = G.out((R,), torch.int32, -7)
     out = G.out((R, gamma + 1), torch.int32, -7)
     p_tok = G.out((R, gamma), torch.float32, float("nan"))
-    ws = G.workspace(B.dspark_workspace_size(B.DSPARK_OP_VERIFY_MARKOV, R, gamma, V, rank, max_rows))
+    ws = G.workspace(B.dspark_workspace_size(B.DSPARK_OP_VERIFY_MARKOV, R, gamma, V, rank, max_rows, B.DSPARK_BF16,
+                                             B.DSPARK_VERIFY_HOST_TARGET if host_target else 0))
     status = G.out((1,), torch.int32, 0)
     samp = temperature > 0
     B.dspark_verify_markov(target_d, cu_d, y_d, dev(d["U"]), W1, dev(d["W2"]), dev(d["anchor"]),

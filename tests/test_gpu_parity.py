@@ -7,6 +7,8 @@ GPU and replay a sample of requests on the oracle (the draft and verify of a
 request depend only on that request's inputs and counters), while the
 selection is compared on every candidate.
 """
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -265,6 +267,77 @@ def test_verify_markov_parity(B, orc, name, over, T, cycles):
         clean = H.compare_draft(tally, g, o, T)
         H.compare_verify(tally, gm, ov, l, only=clean)
     tally.check()
+
+
+HOST_CASES = [
+    ("batched_sampling", dict(R=128, V=16392, gamma=3, rank=512, w_sigma=0.2), 0.7),
+    ("varlen_verify", dict(R=24, V=10008, gamma=5, rank=64, w_sigma=0.3), 1.0),
+    ("qwen3_8b_greedy", dict(R=9, V=16392, gamma=7, rank=64, w_sigma=0.3), 0.0),
+]
+
+
+@pytest.mark.parametrize("name,over,T", HOST_CASES)
+def test_verify_markov_host_target(B, orc, name, over, T):
+    """Target rows left in pinned host memory, read by the kernels across the host
+    link (only the rows up to each first rejection; the residual draw reads the
+    device copy the decision pass keeps): the same accepted counts, tokens and
+    p(y) as with the rows in device memory, bit for bit, and the same against the
+    oracle."""
+    w, d = H.cycle_inputs(name, **over)
+    full = inputs.target_full(w, d["U"])
+    l = inputs.verify_lengths(w)
+    cu = inputs.cu_from_lengths(l)
+    target = inputs.pack_rows(full, l)
+    tD, cuD = H.dev(target), H.dev(cu)
+    tH = torch.from_numpy(target).pin_memory()
+    tally = H.Tally()
+    for cycle in range(2):
+        g = H.gpu_draft(d, T, cycle)
+        on_dev = H.gpu_verify_markov(tD, cuD, d, g, cycle, T)
+        on_host = H.gpu_verify_markov(tH, cuD, d, g, cycle, T, host_target=True)
+        assert on_dev["status"] == 0 and on_host["status"] == 0
+        for k in ("n_acc", "out_tokens"):
+            np.testing.assert_array_equal(on_host[k], on_dev[k])
+        np.testing.assert_array_equal(np.isnan(on_host["p_tok"]), np.isnan(on_dev["p_tok"]))
+        ok = ~np.isnan(on_dev["p_tok"])
+        np.testing.assert_array_equal(on_host["p_tok"][ok], on_dev["p_tok"][ok])
+        o = orc.markov_draft(d["U"], d["W1"], d["W2"], d["anchor"], d["seeds"], cycle, T)
+        ov = orc.verify(target, cu, o["y"], o["q_logits"], d["seeds"], cycle, T)
+        clean = H.compare_draft(tally, g, o, T)
+        H.compare_verify(tally, on_host, ov, l, only=clean)
+    tally.check()
+
+
+def test_host_target_refusals(B):
+    """dspark_verify takes device rows only; pageable host memory is refused by
+    both verify calls (the device cannot be trusted to read it)."""
+    w, d = H.cycle_inputs("batched_sampling", R=4, V=1024, gamma=2, rank=64, w_sigma=0.2)
+    full = inputs.target_full(w, d["U"])
+    l = inputs.verify_lengths(w)
+    target = inputs.pack_rows(full, l)
+    g = H.gpu_draft(d, 0.7, 0)
+    cuD = H.dev(inputs.cu_from_lengths(l))
+    L = B.library()
+    vp = ctypes.c_void_p
+    n_acc = torch.empty(4, dtype=torch.int32, device="cuda")
+    out = torch.empty((4, 3), dtype=torch.int32, device="cuda")
+    pinned = torch.from_numpy(target).pin_memory()
+    ws1 = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_VERIFY, 4, 2, 1024, 0, 12))
+    st = L.dspark_verify(vp(pinned.data_ptr()), vp(cuD.data_ptr()), vp(g["y_dev"].data_ptr()),
+                         vp(g["q_logits_dev"].data_ptr()), vp(g["q_lse_dev"].data_ptr()),
+                         vp(g["q_tok_dev"].data_ptr()), vp(H.dev(d["seeds"]).data_ptr()), 0, 0.7, 4, 2, 1024, 12,
+                         vp(n_acc.data_ptr()), vp(out.data_ptr()), None, vp(ws1.data_ptr()), ws1.numel(), None, None)
+    assert st == B.DSPARK_ERR_UNSUPPORTED
+    pageable = np.ascontiguousarray(target)
+    ws = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_VERIFY_MARKOV, 4, 2, 1024, 64, 12, B.DSPARK_BF16,
+                                             B.DSPARK_VERIFY_HOST_TARGET))
+    U, W1, W2, anc = H.dev(d["U"]), H.dev(d["W1"]), H.dev(d["W2"]), H.dev(d["anchor"])
+    st = L.dspark_verify_markov(vp(pageable.ctypes.data), vp(cuD.data_ptr()), vp(g["y_dev"].data_ptr()),
+                                vp(U.data_ptr()), vp(W1.data_ptr()), vp(W2.data_ptr()), vp(anc.data_ptr()), 64,
+                                vp(g["q_lse_dev"].data_ptr()), vp(g["q_tok_dev"].data_ptr()),
+                                vp(H.dev(d["seeds"]).data_ptr()), 0, 0.7, 4, 2, 1024, 12, vp(n_acc.data_ptr()),
+                                vp(out.data_ptr()), None, vp(ws.data_ptr()), ws.numel(), None, None)
+    assert st == B.DSPARK_ERR_UNSUPPORTED
 
 
 def test_verify_tiny_many_cycles(B, orc):
