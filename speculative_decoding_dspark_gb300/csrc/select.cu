@@ -87,11 +87,23 @@ __device__ __forceinline__ double block_exclusive_scan_d(double x, double* tot, 
     return res;
 }
 
+constexpr int kTracks = 16;  // top-n sizes one radix selection finds at once
+
+// Shared memory of one selection: fixed fields, then the per-candidate arrays,
+// sized for the call's N = R * gamma candidates (select_smem_bytes) and carved
+// by select_carve.
 struct SelectSmem {
-    uint32_t key[2][kSelectMaxItems];  // float bits of a (non-negative: order-preserving); top bit: eligible
-    uint16_t id[2][kSelectMaxItems];   // candidate id = k * R + r
-    double prefix[kSelectMaxItems + 1];  // prefix[n] = sum of the n best a
-    int l[kSelectMaxItems];
+    uint32_t* key[2];  // [N] float bits of a (non-negative: order-preserving); top bit: eligible
+    uint16_t* id[2];   // [N] candidate id = k * R + r
+    double* prefix;    // [N + 1] sort path: prefix[n] = sum of the n best a
+    uint8_t* sel;      // [N] selection path: candidate chosen (shares prefix's space)
+    int* l;            // [R]
+    int bins[kTracks][256];
+    uint32_t tau[kTracks];   // per track: key of the n-th best candidate
+    int need[kTracks];       // per track: the wanted count, then how many keys equal to tau are taken
+    int track_n[kTracks];
+    double track_sum[kTracks];
+    int n_tracks;
     int cs[kSelectMaxSteps];
     float sp[kSelectMaxSteps];
     int warp_i[33];
@@ -100,6 +112,30 @@ struct SelectSmem {
     int n_sel;
     int n_elig;
 };
+
+__host__ __device__ constexpr size_t sel_align(size_t x) { return (x + 15) / 16 * 16; }
+
+__host__ __device__ inline size_t select_smem_bytes(int R, int N) {
+    return sel_align(sizeof(SelectSmem)) + 2 * sel_align(sizeof(uint32_t) * (size_t)N) +
+           2 * sel_align(sizeof(uint16_t) * (size_t)N) + sel_align(sizeof(double) * ((size_t)N + 1)) +
+           sel_align(sizeof(int) * (size_t)R);
+}
+
+// Thread 0 points the arrays into the dynamic shared memory after the fixed fields.
+__device__ SelectSmem& select_carve(unsigned char* base, int R, int N) {
+    SelectSmem& sm = *reinterpret_cast<SelectSmem*>(base);
+    if (threadIdx.x == 0) {
+        unsigned char* q = base + sel_align(sizeof(SelectSmem));
+        for (int b = 0; b < 2; ++b) { sm.key[b] = reinterpret_cast<uint32_t*>(q); q += sel_align(sizeof(uint32_t) * (size_t)N); }
+        for (int b = 0; b < 2; ++b) { sm.id[b] = reinterpret_cast<uint16_t*>(q); q += sel_align(sizeof(uint16_t) * (size_t)N); }
+        sm.prefix = reinterpret_cast<double*>(q);
+        sm.sel = q;
+        q += sel_align(sizeof(double) * ((size_t)N + 1));
+        sm.l = reinterpret_cast<int*>(q);
+    }
+    __syncthreads();
+    return sm;
+}
 
 constexpr uint32_t kEligible = 0x80000000u;
 
@@ -136,7 +172,8 @@ __device__ bool survival_sort_scan(SelectSmem& sm, const float* c, float* a_out,
             elig = elig && ((cutoff == DSPARK_SELECT_CONF_CUTOFF ? ck : run) >= conf_min);
             n_e += elig ? 1 : 0;
             const int idn = k * R + r;
-            sm.key[0][idn] = __float_as_uint(run) | (elig ? kEligible : 0u);
+            // -0 keys as +0 (a confidence of -0 is a survival of 0: it ties with +0)
+            sm.key[0][idn] = (__float_as_uint(run) & ~kEligible) | (elig ? kEligible : 0u);
             sm.id[0][idn] = (uint16_t)idn;
             if (a_out) a_out[(size_t)r * gamma + k] = run;
         }
@@ -190,6 +227,99 @@ __device__ bool survival_sort_scan(SelectSmem& sm, const float* c, float* a_out,
     return true;
 }
 
+// Radix selection without a sort: for every track t < sm.n_tracks, the key
+// tau[t] of the track_n[t]-th best candidate (1 <= track_n[t] < N) among the
+// keys sm.key[0][0 .. N) in candidate order, and need[t] = how many of the
+// candidates whose key equals tau[t] the best track_n[t] take (the earliest in
+// candidate order, which is position then request: the tie order).  Four
+// passes over 8-bit digits, most significant first; each pass counts the
+// candidates that agree with a track's digits so far into that track's 256
+// bins, and one warp per track walks its bins from the top.
+__device__ void radix_select(SelectSmem& sm, int N) {
+    const int nt = sm.n_tracks;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x < nt) { sm.tau[threadIdx.x] = 0u; sm.need[threadIdx.x] = sm.track_n[threadIdx.x]; }
+    const int ipt = (N + kNT - 1) / kNT;
+    const int lo = min(N, threadIdx.x * ipt), hi = min(N, lo + ipt);
+    for (int d = 0; d < 4; ++d) {
+        const int shift = 24 - 8 * d;
+        for (int b = threadIdx.x; b < nt * 256; b += kNT) (&sm.bins[0][0])[b] = 0;
+        __syncthreads();
+        for (int i = lo; i < hi; ++i) {
+            const uint32_t key = sm.key[0][i];
+            for (int t = 0; t < nt; ++t)
+                if (d == 0 || (key >> (shift + 8)) == (sm.tau[t] >> (shift + 8)))
+                    atomicAdd(&sm.bins[t][(key >> shift) & 255u], 1);
+        }
+        __syncthreads();
+        if (warp < nt) {
+            // lane L holds bins 255 - 8L - j (j = 0..7): the lanes in order walk the bins from the top
+            int c[8], sum = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) { c[j] = sm.bins[warp][255 - 8 * lane - j]; sum += c[j]; }
+            int incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            const int need = sm.need[warp];
+            const int before = incl - sum;
+            if (before < need && need <= incl) {  // exactly one lane
+                int acc = before, j = 0;
+                while (acc + c[j] < need) { acc += c[j]; ++j; }
+                sm.tau[warp] |= (uint32_t)(255 - 8 * lane - j) << shift;
+                sm.need[warp] = need - acc;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// Sum of the track_n[t] best survivals for every track (fixed-order fp64
+// reduction, the same on every call): those above tau plus need copies of tau.
+__device__ void track_sums(SelectSmem& sm, int N) {
+    const int nt = sm.n_tracks;
+    const int ipt = (N + kNT - 1) / kNT;
+    const int lo = min(N, threadIdx.x * ipt), hi = min(N, lo + ipt);
+    for (int t = 0; t < nt; ++t) {
+        const uint32_t tau = sm.tau[t];
+        double local = 0.0;
+        for (int i = lo; i < hi; ++i) {
+            const uint32_t key = sm.key[0][i];
+            if (key > tau) local += (double)__uint_as_float(key & ~kEligible);
+        }
+        double tot;
+        block_exclusive_scan_d(local, &tot, sm.warp_d);
+        if (threadIdx.x == 0)
+            sm.track_sum[t] = tot + (double)sm.need[t] * (double)__uint_as_float(tau & ~kEligible);
+        __syncthreads();
+    }
+}
+
+// Mark the n best candidates of the current keys in sm.sel (0 < n < N):
+// those above the n-th best key and the earliest ones equal to it.
+__device__ void mark_best(SelectSmem& sm, int N, int n) {
+    if (threadIdx.x == 0) { sm.n_tracks = 1; sm.track_n[0] = n; }
+    __syncthreads();
+    radix_select(sm, N);
+    const uint32_t tau = sm.tau[0];
+    const int take_eq = sm.need[0];
+    const int ipt = (N + kNT - 1) / kNT;
+    const int lo = min(N, threadIdx.x * ipt), hi = min(N, lo + ipt);
+    int eq = 0;
+    for (int i = lo; i < hi; ++i) eq += sm.key[0][i] == tau;
+    int tot;
+    int rank = block_exclusive_scan(eq, &tot, sm.warp_i);
+    for (int i = lo; i < hi; ++i) {
+        const uint32_t key = sm.key[0][i];
+        bool take = key > tau;
+        if (key == tau) take = rank++ < take_eq;
+        sm.sel[i] = take ? 1 : 0;
+    }
+    __syncthreads();
+}
+
 // Where one selection reads and writes: the current and the planning
 // confidences, the mode, and the outputs (a and cu may be NULL).
 struct SelectIo {
@@ -222,18 +352,44 @@ __device__ int select_body(SelectSmem& sm, const SelectParams& p, const SelectIo
 
     bool good = true;
     int n = 0;
-    if (mode == DSPARK_SELECT_HISTORY) {
-        good = survival_sort_scan(sm, io.c_hist, nullptr, R, gamma);
-    } else if (cutoff_mode(mode)) {
-        good = survival_sort_scan(sm, io.c, io.a, R, gamma, true, mode, p.conf_min);
-    } else {
-        const int n_fixed = min(p.K_cap - R, N);
-        const bool all_or_none = mode == DSPARK_SELECT_FIXED && (n_fixed == 0 || n_fixed == N);
-        good = survival_sort_scan(sm, io.c, io.a, R, gamma, !all_or_none);
-    }
-    if (good && cutoff_mode(mode)) {
-        n = min(sm.n_elig, p.K_cap - R);
-    } else if (good && (mode == DSPARK_SELECT_HISTORY || mode == DSPARK_SELECT_CURRENT)) {
+    // capacity from a survival plan (HISTORY: an earlier cycle's; CURRENT: this
+    // one's): the sums of the n_S best survivals for the capture sizes by radix
+    // selection, no sort (the sort path stays for the first-stop greedy, which
+    // needs the sum for every n, and for more distinct sizes than tracks)
+    auto plan_sizes = [&]() -> bool {  // false: too many distinct sizes for the tracks
+        if (threadIdx.x == 0) {
+            int nt = 0;
+            bool fits = true;
+            for (int i = 0; i < p.n_steps; ++i) {
+                const int S = sm.cs[i];
+                if (S < R) continue;
+                const int ni = min(min(S, p.K_cap) - R, N);
+                if (ni <= 0 || ni >= N) continue;
+                bool seen = false;
+                for (int t = 0; t < nt; ++t) seen = seen || sm.track_n[t] == ni;
+                if (seen) continue;
+                if (nt == kTracks) { fits = false; break; }
+                sm.track_n[nt++] = ni;
+            }
+            sm.n_tracks = fits ? nt : -1;
+        }
+        __syncthreads();
+        return sm.n_tracks >= 0;
+    };
+    auto choose_capacity = [&](bool sorted) {
+        // sorted: sums from sm.prefix; else from the tracks (and the total for n = N)
+        double total = 0.0;
+        if (!sorted) {
+            const int ipt = (N + kNT - 1) / kNT;
+            const int lo = min(N, threadIdx.x * ipt), hi = min(N, lo + ipt);
+            double local = 0.0;
+            for (int i = lo; i < hi; ++i) local += (double)__uint_as_float(sm.key[0][i] & ~kEligible);
+            block_exclusive_scan_d(local, &total, sm.warp_d);
+            if (sm.n_tracks > 0) {
+                radix_select(sm, N);
+                track_sums(sm, N);
+            }
+        }
         if (threadIdx.x == 0) {
             double best = -1.0;
             int best_S = -1, best_n = 0;
@@ -241,45 +397,70 @@ __device__ int select_body(SelectSmem& sm, const SelectParams& p, const SelectIo
                 const int S = sm.cs[i];
                 if (S < R) continue;
                 const int ni = min(min(S, p.K_cap) - R, N);
-                const double th = (double)sm.sp[i] * ((double)R + sm.prefix[ni]);
+                double top = 0.0;
+                if (sorted) {
+                    top = sm.prefix[ni];
+                } else if (ni >= N) {
+                    top = total;
+                } else if (ni > 0) {
+                    for (int t = 0; t < sm.n_tracks; ++t)
+                        if (sm.track_n[t] == ni) top = sm.track_sum[t];
+                }
+                const double th = (double)sm.sp[i] * ((double)R + top);
                 if (best_S < 0 || th > best) { best = th; best_S = S; best_n = ni; }
             }
             sm.n_sel = best_S < 0 ? 0 : best_n;
         }
         __syncthreads();
-        n = sm.n_sel;
-        if (mode == DSPARK_SELECT_HISTORY) good = survival_sort_scan(sm, io.c, io.a, R, gamma, n != 0 && n != N);
-    } else if (good && mode == DSPARK_SELECT_FIRST_STOP) {
-        // Theta(n) for every n in parallel; the answer is the first n whose
-        // successor is not strictly better (or infeasible).
-        if (threadIdx.x == 0) sm.n_sel = INT_MAX;
-        __syncthreads();
-        auto pad = [&](int B) {  // index of the smallest capture size >= B, or -1
-            int lo = 0, hi = p.n_steps;
-            while (lo < hi) { const int mid = (lo + hi) >> 1; if (sm.cs[mid] >= B) hi = mid; else lo = mid + 1; }
-            return lo < p.n_steps ? lo : -1;
-        };
-        const int p0 = pad(R);
-        if (p0 < 0) {
-            if (threadIdx.x == 0) sm.n_sel = 0;
-        } else {
-            for (int m = threadIdx.x; m < N; m += kNT) {
-                // may we go from m to m + 1 candidates?
-                const int B0 = R + m, B1 = R + m + 1;
-                const int i0 = pad(B0), i1 = pad(B1);
-                bool stop = (B1 > p.K_cap) || i1 < 0;
-                if (!stop) {
-                    const double th0 = (double)sm.sp[i0] * ((double)R + sm.prefix[m]);
-                    const double th1 = (double)sm.sp[i1] * ((double)R + sm.prefix[m + 1]);
-                    stop = !(th1 > th0);
-                }
-                if (stop) atomicMin(&sm.n_sel, m);
-            }
+        return sm.n_sel;
+    };
+    bool sorted = false;  // the selection reads the sorted candidate ids
+    if (mode == DSPARK_SELECT_HISTORY || mode == DSPARK_SELECT_CURRENT) {
+        const float* plan_c = mode == DSPARK_SELECT_HISTORY ? io.c_hist : io.c;
+        const bool fits = plan_sizes();
+        good = survival_sort_scan(sm, plan_c, mode == DSPARK_SELECT_CURRENT ? io.a : nullptr, R, gamma, !fits);
+        if (good) n = choose_capacity(!fits);
+        if (good && mode == DSPARK_SELECT_HISTORY) {
+            good = survival_sort_scan(sm, io.c, io.a, R, gamma, false);
+        } else if (good && !fits && n != 0 && n != N) {
+            sorted = true;  // CURRENT on the sort path: the ids are sorted already
         }
-        __syncthreads();
-        n = min(sm.n_sel, N);
-    } else if (good) {
-        n = min(p.K_cap - R, N);
+    } else if (mode == DSPARK_SELECT_FIRST_STOP) {
+        good = survival_sort_scan(sm, io.c, io.a, R, gamma, true);
+        sorted = true;
+        if (good) {
+            // Theta(n) for every n in parallel; the answer is the first n whose
+            // successor is not strictly better (or infeasible).
+            if (threadIdx.x == 0) sm.n_sel = INT_MAX;
+            __syncthreads();
+            auto pad = [&](int B) {  // index of the smallest capture size >= B, or -1
+                int lo = 0, hi = p.n_steps;
+                while (lo < hi) { const int mid = (lo + hi) >> 1; if (sm.cs[mid] >= B) hi = mid; else lo = mid + 1; }
+                return lo < p.n_steps ? lo : -1;
+            };
+            const int p0 = pad(R);
+            if (p0 < 0) {
+                if (threadIdx.x == 0) sm.n_sel = 0;
+            } else {
+                for (int m = threadIdx.x; m < N; m += kNT) {
+                    // may we go from m to m + 1 candidates?
+                    const int B0 = R + m, B1 = R + m + 1;
+                    const int i0 = pad(B0), i1 = pad(B1);
+                    bool stop = (B1 > p.K_cap) || i1 < 0;
+                    if (!stop) {
+                        const double th0 = (double)sm.sp[i0] * ((double)R + sm.prefix[m]);
+                        const double th1 = (double)sm.sp[i1] * ((double)R + sm.prefix[m + 1]);
+                        stop = !(th1 > th0);
+                    }
+                    if (stop) atomicMin(&sm.n_sel, m);
+                }
+            }
+            __syncthreads();
+            n = min(sm.n_sel, N);
+        }
+    } else {
+        good = survival_sort_scan(sm, io.c, io.a, R, gamma, false, cutoff_mode(mode) ? mode : 0, p.conf_min);
+        if (good) n = cutoff_mode(mode) ? min(sm.n_elig, p.K_cap - R) : min(p.K_cap - R, N);
     }
     __syncthreads();
     if (!good) {
@@ -289,9 +470,22 @@ __device__ int select_body(SelectSmem& sm, const SelectParams& p, const SelectIo
         if (threadIdx.x == 0) { io.K_used[0] = -1; report(p.dev_status, DSPARK_ERR_DEVICE_INPUT); }
         return -1;
     }
-    for (int r = threadIdx.x; r < R; r += kNT) sm.l[r] = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < n; i += kNT) atomicAdd(&sm.l[sm.id[0][i] % R], 1);
+    if (sorted) {
+        for (int r = threadIdx.x; r < R; r += kNT) sm.l[r] = 0;
+        __syncthreads();
+        for (int i = threadIdx.x; i < n; i += kNT) atomicAdd(&sm.l[sm.id[0][i] % R], 1);
+    } else {
+        // the n best current candidates (every one or none without a selection);
+        // the set is prefix-closed, so l[r] counts request r's chosen positions
+        if (n > 0 && n < N) mark_best(sm, N, n);
+        for (int r = threadIdx.x; r < R; r += kNT) {
+            int cnt = 0;
+            if (n >= N) cnt = gamma;
+            else if (n > 0)
+                for (int k = 0; k < gamma; ++k) cnt += sm.sel[k * R + r];
+            sm.l[r] = cnt;
+        }
+    }
     __syncthreads();
     // cu_seqlens: exclusive scan of l + 1 (blocked by thread)
     const int per = (R + kNT - 1) / kNT;
@@ -314,7 +508,7 @@ __device__ int select_body(SelectSmem& sm, const SelectParams& p, const SelectIo
 
 __global__ void __launch_bounds__(kNT) select_kernel(SelectParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    SelectSmem& sm = *reinterpret_cast<SelectSmem*>(smem_raw);
+    SelectSmem& sm = select_carve(smem_raw, p.R, p.R * p.gamma);
     SelectIo io;
     io.c = p.c; io.c_hist = p.c_hist; io.mode = p.mode;
     io.a = p.a; io.l = p.l; io.cu = p.cu; io.K_used = p.K_used;
@@ -327,7 +521,7 @@ __global__ void __launch_bounds__(kNT) select_kernel(SelectParams p) {
 // drafts and wasted verify rows.
 __global__ void __launch_bounds__(kNT) plan_kernel(SelectParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    SelectSmem& sm = *reinterpret_cast<SelectSmem*>(smem_raw);
+    SelectSmem& sm = select_carve(smem_raw, p.R, p.R * p.gamma);
     const int t = blockIdx.x;
     const int R = p.R, gamma = p.gamma;
     const size_t rg = (size_t)R * gamma;
@@ -432,7 +626,7 @@ __global__ void __launch_bounds__(1024) commit_kernel(const int32_t* n_acc, cons
 }  // namespace
 
 cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
-    const size_t smem = sizeof(SelectSmem);
+    const size_t smem = select_smem_bytes(p.R, p.R * p.gamma);
     cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
@@ -441,7 +635,7 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_plan(const SelectParams& p, int n_cycles, cudaStream_t stream) {
-    const size_t smem = sizeof(SelectSmem);
+    const size_t smem = select_smem_bytes(p.R, p.R * p.gamma);
     cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     plan_kernel<<<n_cycles, kNT, smem, stream>>>(p);
