@@ -108,6 +108,24 @@ double uniform_single(uint64_t seed, uint32_t cycle, int purpose, int req, int p
 // Standard Gumbel noise from a uniform: g = -log(-log u).
 double gumbel(double u) { return -std::log(-std::log(u)); }
 
+// The draft draw's two uniforms of vocabulary segment s (16 consecutive
+// entries, s = v / 16).  The segment is slot j = s % 8 of the 128-entry block
+// b = s / 8; slots j and j + 4 share the Philox counter (4 b + j % 4, position,
+// request, (cycle << 4) | purpose) and take words (0, 1) when j < 4, (2, 3)
+// otherwise: the first word is the race uniform u, the second the in-segment
+// uniform a.  (This library's layout; the pages fix none.)
+void segment_uniforms(uint64_t seed, uint32_t cycle, int purpose, int req, int pos,
+                      int seg, double* u, double* a) {
+    const uint32_t blk = (uint32_t)seg >> 3, slot = (uint32_t)seg & 7u;
+    const uint32_t ctr[4] = {4u * blk + (slot & 3u), (uint32_t)pos, (uint32_t)req,
+                             (cycle << 4) | (uint32_t)purpose};
+    uint32_t out[4];
+    philox4x32_10(ctr, (uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32), out);
+    const int w = (slot < 4u) ? 0 : 2;
+    *u = uniform_from_bits(out[w]);
+    *a = uniform_from_bits(out[w + 1]);
+}
+
 double bf16_to_double(uint16_t b) {
     const uint32_t bits = (uint32_t)b << 16;
     float f;
@@ -223,14 +241,30 @@ double orc_residual_weights(const double* p, const double* q, int n, double* res
 //   prev   = anchor[r] at k = 0, else y[r][k-1]   (anchor < 0: no bias at k=0)
 //   s_v    = (U[r][k][v] + b_v(prev)) * invT      (T > 0)
 //          =  U[r][k][v] + b_v(prev)              (T = 0, greedy)
-//   score  = s_v + Gumbel(u_v), u_v = Philox(purpose 0, position k)   (T > 0)
-//          = s_v                                                         (T = 0)
-//   y      = argmax score (lowest index on ties)
+//   y      = argmax_v s_v (lowest index on ties)                         (T = 0)
+//          = a draw from q = softmax(s) by Gumbel-max                    (T > 0)
 //   q_lse  = logsumexp_v s_v ;  q_tok = exp(s_y - q_lse)
+//
+// The Gumbel-max draw builds its noise top-down (Maddison, Tarlow, Minka,
+// "A* Sampling", NIPS 2014, section 3: for any partition of the entries, the
+// largest perturbed logit of a part is a Gumbel variable located at the log of
+// the part's total weight, and which entry attains it is independent of that
+// value and has probability w_v / W_part).  With parts = segments of 16
+// consecutive entries (the last one ragged) and (u_s, a_s) the segment's two
+// uniforms (segment_uniforms, purpose 0, position k):
+//   W_s    = sum_{v in s} exp(s_v)
+//   race   = log W_s - log(-log u_s)  ->  s* = argmax (lowest segment on ties)
+//   y      = the first v in s* whose running sum of exp(s_v') over s* up to
+//            and including v exceeds a_{s*} W_{s*}
+// so y is the argmax of a Gumbel-perturbed q, like one uniform per entry,
+// with two uniforms per 16 entries.
 // invT is the fp32 value 1.0f/T, shared with the library, widened to double.
 // req_ids maps the rows given here to the request indices the random
 // counters use (NULL: identity), so a subset of a batch can be replayed.
-// margin[r][k] receives the gap between the best and second-best score.
+// margin[r][k] receives how close the decision came to another token: greedy,
+// the gap between the two largest logits; sampling, the smaller of the gap
+// between the two best segment race values and the distance of a W from the
+// running sums on either side of y, in units of W.
 int orc_markov_draft(const void* U, int u_dtype, const void* W1, const void* W2,
                      int w_dtype, const int32_t* anchor, const uint64_t* seeds,
                      const int32_t* req_ids, uint32_t cycle, float temperature,
@@ -241,7 +275,7 @@ int orc_markov_draft(const void* U, int u_dtype, const void* W1, const void* W2,
         return ORC_INVALID;
     const bool greedy = temperature == 0.0f;
     const double invT = greedy ? 1.0 : (double)(1.0f / temperature);
-    std::vector<double> b(V), s(V), score(V);
+    std::vector<double> b(V), s(V);
     for (int r = 0; r < R; ++r) {
         const int rid = req_ids ? req_ids[r] : r;
         for (int k = 0; k < gamma; ++k) {
@@ -251,16 +285,39 @@ int orc_markov_draft(const void* U, int u_dtype, const void* W1, const void* W2,
             for (int v = 0; v < V; ++v) {
                 const double base = load_elem(U, u_dtype, ((size_t)r * gamma + k) * V + v);
                 s[v] = greedy ? (base + b[v]) : (base + b[v]) * invT;
-                if (greedy) {
-                    score[v] = s[v];
-                } else {
-                    const double u = uniform_vocab(seeds[r], cycle, kDraftGumbel, rid, k, v);
-                    score[v] = s[v] + gumbel(u);
-                }
             }
             double gap = 0.0;
-            const int tok = argmax_with_gap(score.data(), V, &gap);
+            int tok = 0;
             const double lse = logsumexp(s.data(), V);
+            if (greedy) {
+                tok = argmax_with_gap(s.data(), V, &gap);
+            } else {
+                // the segments' race values (weights relative to exp(lse))
+                const int n_seg = (V + 15) / 16;
+                std::vector<double> race(n_seg), a_of(n_seg), W(n_seg);
+                for (int g = 0; g < n_seg; ++g) {
+                    double u, a;
+                    segment_uniforms(seeds[r], cycle, kDraftGumbel, rid, k, g, &u, &a);
+                    double w_sum = 0.0;
+                    for (int v = 16 * g; v < std::min(V, 16 * g + 16); ++v) w_sum += std::exp(s[v] - lse);
+                    W[g] = w_sum;
+                    a_of[g] = a;
+                    race[g] = w_sum > 0.0 ? std::log(w_sum) - std::log(-std::log(u))
+                                          : -std::numeric_limits<double>::infinity();
+                }
+                const int win = argmax_with_gap(race.data(), n_seg, &gap);
+                if (n_seg == 1) gap = std::numeric_limits<double>::infinity();
+                // the entry of the winning segment by its running sum
+                const double target = a_of[win] * W[win];
+                double run = 0.0, before = 0.0;
+                tok = std::min(V, 16 * win + 16) - 1;
+                for (int v = 16 * win; v < std::min(V, 16 * win + 16); ++v) {
+                    before = run;
+                    run += std::exp(s[v] - lse);
+                    if (run > target) { tok = v; break; }
+                }
+                gap = std::min(gap, std::min(target - before, run - target) / W[win]);
+            }
             y[(size_t)r * gamma + k] = tok;
             if (q_lse) q_lse[(size_t)r * gamma + k] = lse;
             if (q_tok) q_tok[(size_t)r * gamma + k] = std::exp(s[tok] - lse);

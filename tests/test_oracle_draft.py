@@ -90,24 +90,75 @@ def test_draft_logits_and_stats(orc):
     np.testing.assert_allclose(out0["q_logits"][:, 0], U[:, 0] * invT, rtol=1e-13)
 
 
-def test_gumbel_max_draws_follow_softmax(orc):
-    """At T = 0.7 the drafted token's frequencies over 6000 cycles match
-    softmax(U * invT) (chi-square on 12 symbols); the draws change with the
-    cycle index and the request seed."""
-    V = 12
-    g = np.random.default_rng(11)
-    U = g.normal(0, 1.5, (1, 1, V)).astype(np.float32)
+@pytest.mark.parametrize("V,n,sigma", [(12, 6000, 1.5), (40, 12000, 1.0), (300, 30000, 0.4)])
+def test_gumbel_max_draws_follow_softmax(orc, V, n, sigma):
+    """At T = 0.7 the drafted token's frequencies over n cycles match
+    softmax(U * invT): chi-square over the entries and over the 16-entry
+    segments whose race decides the draw.  V = 12 is one segment (the draw is
+    the in-segment pick alone), V = 40 three (the last one ragged), V = 300 three
+    128-entry blocks (segments j and j + 4 of a block share a Philox counter).
+    A wrong word (race and pick from one word, or two segments from one word),
+    an off-by-one in the running sum or a sign error in the noise fails here."""
+    g = np.random.default_rng(11 + V)
+    U = g.normal(0, sigma, (1, 1, V)).astype(np.float32)
     W = np.zeros((V, 4), np.float32)
     T = 0.7
     invT = float(np.float32(1.0) / np.float32(T))
     ys = np.array([orc.markov_draft(U, W, W, [-1], [123], c, T, want_logits=False)["y"][0, 0]
-                   for c in range(6000)])
+                   for c in range(n)])
     counts = np.bincount(ys, minlength=V)
     p = orc.softmax(U[0, 0].astype(np.float64) * invT)
-    chi2 = ((counts - 6000 * p) ** 2 / (6000 * p)).sum()
+    chi2 = ((counts - n * p) ** 2 / (n * p)).sum()
     assert stats.chi2.sf(chi2, V - 1) > 1e-3, chi2
+    n_seg = (V + 15) // 16
+    if n_seg > 1:
+        seg_counts = np.add.reduceat(counts, np.arange(0, V, 16))
+        seg_p = np.add.reduceat(p, np.arange(0, V, 16))
+        chi2s = ((seg_counts - n * seg_p) ** 2 / (n * seg_p)).sum()
+        assert stats.chi2.sf(chi2s, n_seg - 1) > 1e-3, chi2s
     # a sign error in the noise (argmin-like sampling) would favour the least likely token
     assert counts[np.argmax(p)] > counts[np.argmin(p)]
+
+
+def test_draft_draw_is_argmax_of_its_segment_race(orc):
+    """Where one entry holds nearly all of the weight, every draw is that entry
+    (the race and the in-segment pick both follow the weight); where two
+    segments hold equal weight and the rest none, each wins about half the
+    time, independently of the block layout."""
+    V = 256
+    T = 1.0
+    W = np.zeros((V, 4), np.float32)
+    U = np.full((1, 1, V), -200.0, np.float32)
+    U[0, 0, 77] = 0.0
+    ys = [orc.markov_draft(U, W, W, [-1], [5], c, T, want_logits=False)["y"][0, 0] for c in range(200)]
+    assert set(ys) == {77}
+    for a, b in [(3, 200), (21, 85)]:  # slots of different blocks; slots j and j + 4 of one block
+        U = np.full((1, 1, V), -200.0, np.float32)
+        U[0, 0, a] = 0.0
+        U[0, 0, b] = 0.0
+        ys = np.array([orc.markov_draft(U, W, W, [-1], [9], c, T, want_logits=False)["y"][0, 0]
+                       for c in range(4000)])
+        assert set(np.unique(ys)) <= {a, b}
+        frac = float(np.mean(ys == a))
+        assert abs(frac - 0.5) < 4 * np.sqrt(0.25 / 4000), (a, b, frac)
+
+
+def test_draft_margin_reports_near_decisions(orc):
+    """The margin is the smaller of the race gap between the two best segments
+    and the distance of the pick from the running sums around the drawn token:
+    zero-margin cases cannot occur in general position, and an entry that
+    holds all the weight of a one-segment vocabulary leaves the pick a margin
+    equal to how far a W is from either end."""
+    V = 8
+    W = np.zeros((V, 4), np.float32)
+    U = np.full((1, 1, V), -400.0, np.float32)
+    U[0, 0, 5] = 0.0
+    for c in range(20):
+        out = orc.markov_draft(U, W, W, [-1], [3], c, 1.0, want_logits=False)
+        assert out["y"][0, 0] == 5
+        a = orc.philox4x32_10([0, 0, 0, (c << 4) | 0], 3)[1]
+        a = orc.uniform_from_bits(int(a))
+        assert out["margin"][0, 0] == pytest.approx(min(a, 1.0 - a), abs=1e-12)
 
 
 def test_request_subset_replays_batch(orc):
