@@ -9,9 +9,10 @@
 // are not multiples of 64, ...).  Per position k, two launches:
 //   draft_bias_simt    bias[r][v] = sum_j W2[v][j] * W1[prev_r][j], fp32, tiles
 //                      of 64 vocabulary rows x 16 requests staged in shared memory;
-//   draft_sample       one CTA per (request, 8192-entry chunk): logits, Gumbel
-//                      noise, running argmax and (max, sum of exp); the last CTA
-//                      of a request (counter, no spin) writes y, q_lse, q_tok.
+//   draft_sample       one CTA per (request, 8192-entry chunk): logits, the
+//                      segments' Gumbel race and picks, running argmax and (max,
+//                      sum of exp); the last CTA of a request (counter, no spin)
+//                      writes y, q_lse, q_tok.
 #include "kernels.cuh"
 
 namespace dspark {
@@ -136,27 +137,61 @@ __global__ void __launch_bounds__(kDraftThreads) draft_sample_kernel(DraftParams
 
     float score = -INFINITY, s_at = 0.0f, m = -INFINITY, sum = 0.0f;
     int idx = INT_MAX;
-    for (int v4 = (v0 >> 2) + threadIdx.x; 4 * v4 < v1; v4 += kDraftThreads) {
-        uint32_t words[4] = {0u, 0u, 0u, 0u};
-        if (!kGreedy) {
-            const uint4 wd = philox4x32_10(make_uint4((uint32_t)v4, (uint32_t)k, (uint32_t)r, w3), K);
-            words[0] = wd.x; words[1] = wd.y; words[2] = wd.z; words[3] = wd.w;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int v = 4 * v4 + i;
-            if (v >= v1) break;
-            const float base = load_elem(p.U, p.u_dtype, rk * V + v);
-            const float sum_b = base + brow[v];
-            const float s = kGreedy ? sum_b : sum_b * p.invT;
+    if (kGreedy) {
+        for (int v = v0 + threadIdx.x; v < v1; v += kDraftThreads) {
+            const float s = load_elem(p.U, p.u_dtype, rk * V + v) + brow[v];
             if (qrow) qrow[v] = s;
-            float sc = s;
-            if (!kGreedy) {
-                sc = s + gumbel_from_uniform(uniform_from_bits(words[i]));
-                if (s > m) { sum = sum * expf(m - s) + 1.0f; m = s; }
-                else sum += expf(s - m);
+            if (better(s, v, score, idx)) { score = s; idx = v; s_at = s; }
+        }
+    } else {
+        // Gumbel-max with its noise built per 16-entry segment: the segment's race
+        // value log W - log(-log u) and, for its pick, the first entry whose running
+        // weight passes a W (u, a: words 2 h, 2 h + 1 of the counter 4 (s / 8) + s % 4,
+        // h = (s / 4) % 2).  Each segment offers its pick with its race value; the
+        // best offer over the vocabulary is the draw.
+        for (int sg = (v0 >> 4) + (int)threadIdx.x; 16 * sg < v1; sg += kDraftThreads) {
+            const uint4 wd = philox4x32_10(
+                make_uint4((uint32_t)(4 * (sg >> 3) + (sg & 3)), (uint32_t)k, (uint32_t)r, w3), K);
+            const bool hi = (sg >> 2) & 1;
+            const float u = uniform_from_bits(hi ? wd.z : wd.x);
+            const float a = uniform_from_bits(hi ? wd.w : wd.y);
+            float sv[16];
+            float ms = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const int v = 16 * sg + c;
+                float s = -INFINITY;
+                if (v < v1) {
+                    s = (load_elem(p.U, p.u_dtype, rk * V + v) + brow[v]) * p.invT;
+                    if (qrow) qrow[v] = s;
+                }
+                sv[c] = s;
+                ms = fmaxf(ms, s);
             }
-            if (better(sc, v, score, idx)) { score = sc; idx = v; s_at = s; }
+            if (!(ms > -INFINITY)) continue;  // nothing finite in the segment
+            float w = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) w += expf(sv[c] - ms);
+            lse_merge(m, sum, ms, w);
+            const float race = ms + logf(w) + gumbel_from_uniform(u);
+            const float target = a * w;
+            float run = 0.0f;
+            int pick = -1, last = 0;
+            float s_pick = sv[0];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const float wc = expf(sv[c] - ms);
+                run += wc;
+                if (wc > 0.0f && pick < 0) last = c;
+                if (pick < 0 && run > target) { pick = c; s_pick = sv[c]; }
+            }
+            if (pick < 0) {
+                pick = last;
+#pragma unroll
+                for (int c = 0; c < 16; ++c)
+                    if (c == last) s_pick = sv[c];
+            }
+            if (better(race, 16 * sg + pick, score, idx)) { score = race; idx = 16 * sg + pick; s_at = s_pick; }
         }
     }
     draft_block_reduce(score, idx, s_at, m, sum);

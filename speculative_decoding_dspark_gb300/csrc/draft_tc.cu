@@ -21,14 +21,18 @@
 //             full acceptance (the last CTA to finish writes the tokens).
 //
 // Persistent, one CTA per SM, 19 warps:
-//   A (M = 128 requests x K = rank) = rows W1[prev], copied by the epilogue
-//     warps into 128-byte-swizzled shared memory at the start of each step
-//     (prev: the anchor at k = 0, else the step's predecessor decoded from the
-//     previous step's winner keys) and resident for the step;
+//   A (M = 128 requests x K = rank) = rows W1[prev] in tensor memory (columns
+//     256-511, two bf16 per column), written by the epilogue threads with
+//     tcgen05.st at the start of each step (prev: the anchor at k = 0, else the
+//     step's predecessor decoded from the previous step's winner keys; the
+//     residual: the rejected position's predecessor) and resident for the step,
+//     so that shared memory is left to the W2 ring;
 //   B (N = 128 vocabulary rows x K = rank) = W2 tiles streamed by TMA through a
-//     ring of 16 KB stages; the next tile's boxes are prefetched into L2 one
-//     tile ahead (two at a step's first tile, while the grid waits between
-//     steps) so the ring only has to cover L2 latency;
+//     ring of 16 KB stages (11 at rank 512 in the draft: 176 KB in flight per
+//     SM, which is what it takes to cover the loaded latency of a load, about
+//     2-3 us); the next tile's boxes are prefetched into L2 one tile ahead (two
+//     at a step's first tile); odd steps take a CTA's tiles in reverse order, so
+//     a step starts on tiles still in L2;
 //   D = A . B^T in fp32 tensor memory, two 128-column buffers so the epilogue
 //     of one vocabulary tile overlaps the MMAs of the next;
 //   U_k (draft) = the tile's base logits, by TMA into two 16 KB pass buffers
@@ -36,24 +40,26 @@
 //     epilogue, which adds them to the accumulator;
 //   epilogue (16 warps; thread = one request x 32 vocabulary columns of a
 //     tile, in two 16-column passes, pass h over columns 64 h .. 64 h + 63 of
-//     the tile across the four warps of a lane quadrant): Gumbel-max draws
-//     use the exponential-race form: with
-//     weight w > 0 and E = -log(u), the largest log(w) + Gumbel(u) is the
-//     largest w / E, so a candidate replaces the best when
-//     w * E_best > w_best * E.  Since E >= 1 - u, an entry with
-//     1 - u >= w * E_best / w_best cannot win; that test needs no logarithm
-//     (1 - u comes exactly from the random bits), and only the entries that
-//     pass it take the log (a short series in 1 - u near u = 1, the
-//     special-function log2 elsewhere; relative error about 2e-6) and the
-//     comparison, one candidate per lane at a time.  The four threads racing
-//     over a request row in a CTA (one per quarter) share their best records
-//     through shared memory, so each test uses the strongest of the four.
-//   The residual launch differs: its epilogue also needs each request's own
-//     target row and U row (128 scattered rows), so A lives in tensor memory
-//     (columns 256-511, written with tcgen05.st) and the shared memory it frees
-//     holds six staging buffers, each one 32-column pass of those rows, filled
-//     by the epilogue threads' own cp.async copies four passes ahead; the
-//     epilogue works in four 32-column passes per tile, 8 columns per thread.
+//     the tile across the four warps of a lane quadrant).  Draft draws are
+//     Gumbel-max with the noise built per 16-entry segment (one thread's pass
+//     is one segment): the segments race in the exponential-race form (with
+//     weight W = the segment's sum of exp and E = -log(u), the largest
+//     log W + Gumbel(u) is the largest W / E, so a segment replaces the record
+//     when W * E_best > W_best * E; since E >= 1 - u, a segment with
+//     1 - u >= W * E_best / W_best cannot win, a test that needs no logarithm),
+//     the record keeps its segment's logits in registers, and the entry is
+//     picked once per step, from the record, by its running sum against a
+//     second uniform times W.  The residual races entry by entry, with the
+//     same no-log test, only the entries that pass it taking the logarithm
+//     (a short series in 1 - u near u = 1, the special-function log2
+//     elsewhere; relative error about 2e-6).  The four threads racing over a
+//     request row in a CTA (one per quarter) share their best records through
+//     shared memory, so each test uses the strongest of the four.
+//   The residual launch also needs each request's own target row and U row
+//     (128 scattered rows): six staging buffers, each one 32-column pass of
+//     those rows, filled by the epilogue threads' own cp.async copies four
+//     passes ahead; the epilogue works in four 32-column passes per tile, 8
+//     columns per thread.
 //
 // Cross-CTA results need no merging pass: every CTA folds its winner into one
 // 64-bit key per request and step with atomicMax (order-preserving bits of
@@ -91,6 +97,7 @@ constexpr int kCtlWarps = 3;                  // W2 producer, MMA issuer, U prod
 constexpr int kThreads = kCtlWarps * 32 + kEpiThreads;
 constexpr int kPassCols = 16;                 // of which one pass handles
 constexpr int kUBufBytes = kM * 64 * 2;       // base logits of one pass: 128 requests x 64 columns
+constexpr int kUBufs = 2;                     // draft: pass buffers of base logits (one tile)
 // residual staging of one 32-column pass for the 128 requests: target logits
 // (fp32, 128-byte rows) and base logits (bf16, 64-byte rows), copied in
 // 16-byte pieces by the epilogue threads a few passes ahead
@@ -99,12 +106,16 @@ constexpr int kResTBytes = kM * kResCols * 4;  // 16 KB
 constexpr int kResUBytes = kM * kResCols * 2;  // 8 KB
 constexpr int kResBufs = 6;                    // staging buffers
 constexpr int kResAhead = kResBufs - 2;        // passes whose copies are issued ahead of the one computed
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;
 constexpr int kMaxP = 256;                    // CTAs per request block (pieces per request)
-constexpr uint32_t kTmemCols = 256;     // draft: two 128-column accumulators
-constexpr uint32_t kTmemColsRes = 512;  // residual: the accumulators, then the A rows (at most 256 columns)
-constexpr uint32_t kAcol = 256;         // residual: first tensor-memory column of A
+constexpr uint32_t kTmemCols = 512;     // two 128-column accumulators, then the A rows (at most 256 columns)
+constexpr uint32_t kAcol = 256;         // first tensor-memory column of A
 constexpr uint64_t kWaitNs = 2000000000ull;
+// W2 tiles pulled into L2 ahead of the ring: kPfAhead past the tile being
+// loaded, kPfStepAhead at a step's first tile (while the grid waits between
+// steps, HBM keeps streaming the step's later tiles)
+constexpr int kPfAhead = 1;
+constexpr int kPfStepAhead = 2;
 constexpr float kLog2eF = 1.4426950408889634f;
 constexpr float kLn2F = 0.6931471805599453f;
 // Relative slack of the no-log race test, far above the rounding of the
@@ -121,11 +132,14 @@ struct TcPartial {
     float m, sum;
     float pad[3];
 };
+// the draft's end-of-step exchange of the epilogue quarters ([3][kM]), whole KB
+constexpr int kExchBytes = (3 * kM * (int)sizeof(TcPartial) + 1023) / 1024 * 1024;
 
 
 struct TcParams {
     const uint16_t* U;
     const uint16_t* W1;
+    int w1_wide;               // W1 is 32-byte aligned: its rows are read 32 bytes a lane at a time
     unsigned long long* keys;  // draft [gamma][R]; residual [R]
     unsigned* step_done;       // draft [gamma]: CTAs done with step k; then one abort word
     float4* parts;             // draft [gamma][R][P]: (max, sum, winner logit, winner) per CTA
@@ -153,7 +167,7 @@ struct TcParams {
 struct Bars {
     uint64_t full[kMaxStages], empty[kMaxStages];
     uint64_t tfull[2], tempty[2];
-    uint64_t ufull[2], uempty[2];
+    uint64_t ufull[kUBufs], uempty[kUBufs];
     uint64_t sfull[kResBufs], sempty[kResBufs];  // residual staging buffers
     uint64_t afull, mma_done;  // afull: the step's A rows are in shared memory (one arrival per epilogue warp)
     uint32_t tmem_slot;
@@ -217,6 +231,15 @@ __device__ __forceinline__ unsigned long long winner_key(float score, int idx) {
 }
 
 __device__ __forceinline__ int key_index(unsigned long long key) { return (int)~(uint32_t)key; }
+
+// Vocabulary tile of a CTA's launch-global tile g (step g / n_local, the
+// step's i-th tile of the CTA's tiles cidx, cidx + P, ...).  Odd steps take the
+// CTA's tiles in reverse order, so that a step starts on the W2 tiles the
+// previous step ended with, which are still in L2.
+__device__ __forceinline__ int tile_at(int g, int n_local, int cidx, int P) {
+    const int k = g / n_local, i = g - k * n_local;
+    return cidx + ((k & 1) ? n_local - 1 - i : i) * P;
+}
 
 // 2^x on the special-function unit (relative error about 2^-22; the race
 // decisions and normalisers it feeds carry far larger margins).
@@ -283,6 +306,13 @@ __device__ __forceinline__ T pick(const T (&a)[N], int c) {
 
 __device__ __forceinline__ uint32_t word_of(const uint4& x, int j) {
     return j == 0 ? x.x : (j == 1 ? x.y : (j == 2 ? x.z : x.w));
+}
+
+// 32 bytes at p (32-byte aligned, read-only for the kernel's lifetime) in one load.
+__device__ __forceinline__ void ldg_nc_32b(const void* p, uint32_t (&w)[8]) {
+    asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "l"(p));
 }
 
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
@@ -407,22 +437,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_u, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    // draft: A rows | two U pass buffers | W2 ring; residual (A in tensor
-    // memory): target staging buffers | base-logit staging buffers | W2 ring
-    uint8_t* sA = smem;
-    uint8_t* sU = kRes ? smem : sA + p.nkb * kTileBytes;
+    // A lives in tensor memory.  Draft: quarter exchange | two U pass buffers |
+    // W2 ring; residual: target staging buffers | base-logit staging buffers |
+    // W2 ring
+    uint8_t* sX = smem;
+    uint8_t* sU = kRes ? smem : sX + kExchBytes;
     uint8_t* sRT = sU;
     uint8_t* sRU = sU + kResBufs * kResTBytes;
-    uint8_t* sB = sU + (kRes ? kResBufs * (kResTBytes + kResUBytes) : 2 * kUBufBytes);
+    uint8_t* sB = sU + (kRes ? kResBufs * (kResTBytes + kResUBytes) : kUBufs * kUBufBytes);
     Bars& bar = *reinterpret_cast<Bars*>(sB + p.n_stages * kTileBytes);
     ResShared& rsh = *reinterpret_cast<ResShared*>(&bar + 1);  // residual only
     DraftShared& dsh = *reinterpret_cast<DraftShared*>(&bar + 1);  // draft only
     float* g_share = &rsh.g_share[0][0];
-    // the quarters' exchange at the end of a step ([3][kM]): draft, the A rows'
-    // space (the step's MMAs have completed and the next step's rows are not
-    // written yet); residual, the W2 ring (drained when the last tile's
-    // accumulator has been seen)
-    TcPartial* scratch = reinterpret_cast<TcPartial*>(kRes ? sB : sA);
+    // the quarters' exchange at the end of a step ([3][kM]): draft, its own
+    // space (the ring and the U buffers stream on into the next step);
+    // residual, the W2 ring (drained when the last tile's accumulator has been
+    // seen)
+    TcPartial* scratch = reinterpret_cast<TcPartial*>(kRes ? sB : sX);
     volatile int* abort_flag = &bar.abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -437,7 +468,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) { tc::mbar_init(&bar.full[s], 1); tc::mbar_init(&bar.empty[s], 1); }
         for (int a = 0; a < 2; ++a) { tc::mbar_init(&bar.tfull[a], 1); tc::mbar_init(&bar.tempty[a], kEpiWarps); }
-        for (int a = 0; a < 2; ++a) { tc::mbar_init(&bar.ufull[a], 1); tc::mbar_init(&bar.uempty[a], kEpiWarps); }
+        for (int a = 0; a < kUBufs; ++a) { tc::mbar_init(&bar.ufull[a], 1); tc::mbar_init(&bar.uempty[a], kEpiWarps); }
         for (int a = 0; a < kResBufs; ++a) {
             tc::mbar_init(&bar.sfull[a], kEpiThreads);  // one cp.async arrival per epilogue thread
             tc::mbar_init(&bar.sempty[a], kEpiWarps);
@@ -448,7 +479,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         tc::fence_barrier_init();
     }
     if (warp == 1) {
-        tc::tmem_alloc(&bar.tmem_slot, kRes ? kTmemColsRes : kTmemCols);
+        tc::tmem_alloc(&bar.tmem_slot, kTmemCols);
         tc::tmem_relinquish();
     }
     if (warp == 0 && lane == 0) {
@@ -474,7 +505,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         if (lane == 0) {
             // L2 prefetch of global tile g (W2 boxes and, draft, the step's U passes)
             auto prefetch_tile = [&](int g) {
-                const int tn = cidx + (g % n_local) * p.P;
+                const int tn = tile_at(g, n_local, cidx, p.P);
                 for (int q = 0; q < p.nkb; ++q) tma_prefetch_l2_2d(&tm_w2, q * kKB, tn * kNV);
                 if (!kRes) {
                     tc::tma_prefetch_l2_3d(&tm_u, tn * kNV, g / n_local, row0);
@@ -485,7 +516,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
             // and two at a step's first tile, so that HBM keeps streaming the
             // step's next tiles while the grid waits between steps
             int pf_next = 0;
-            for (; pf_next < 2 && pf_next < n_tl; ++pf_next) prefetch_tile(pf_next);
+            for (; pf_next <= kPfStepAhead && pf_next < n_tl; ++pf_next) prefetch_tile(pf_next);
             const int n_loads = n_tl * p.nkb;  // W2 stage loads
             int issued = 0;
             bool ok = true;
@@ -495,12 +526,12 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                 const uint32_t ph = (uint32_t)((issued / S) & 1);
                 if (!tc::mbar_wait(&bar.empty[s], ph ^ 1u, abort_flag, kWaitNs)) { ok = false; break; }
                 const int g = issued / p.nkb, kb = issued - g * p.nkb;
-                const int t = cidx + (g % n_local) * p.P;
+                const int t = tile_at(g, n_local, cidx, p.P);
                 tc::mbar_arrive_expect_tx(&bar.full[s], kTileBytes);
                 tc::tma_load_2d(sB + s * kTileBytes, &tm_w2, &bar.full[s], kb * kKB, t * kNV);
                 // once a tile's first ring of loads is out, pull the next tile(s) into L2
                 if (kb == min(S, p.nkb) - 1) {
-                    const int horizon = min(n_tl - 1, g + (g % n_local == 0 ? 2 : 1));
+                    const int horizon = min(n_tl - 1, g + (g % n_local == 0 ? kPfStepAhead : kPfAhead));
                     for (; pf_next <= horizon; ++pf_next) prefetch_tile(pf_next);
                 }
             }
@@ -520,7 +551,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
             bool ok = true;
             int s = 0;
             uint32_t ph = 0;
-            const uint32_t a_base = tc::smem_u32(sA), b_base = tc::smem_u32(sB);
+            const uint32_t b_base = tc::smem_u32(sB);
             for (int k = 0; ok && k < n_steps; ++k) {
                 // the step's A rows, written by the epilogue warps
                 if (!tc::mbar_wait(&bar.afull, (uint32_t)(k & 1), abort_flag, kWaitNs)) { ok = false; break; }
@@ -535,17 +566,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                     for (int kb = 0; kb < p.nkb; ++kb) {
                         if (!tc::mbar_wait(&bar.full[s], ph, abort_flag, kWaitNs)) { ok = false; break; }
                         tc::tc_fence_after();
-                        const uint32_t aa = a_base + (uint32_t)(kb * kTileBytes);
                         const uint32_t bb = b_base + (uint32_t)(s * kTileBytes);
 #pragma unroll
-                        for (int j = 0; j < kKB / 16; ++j) {
-                            if constexpr (kRes)  // A in tensor memory: K elements 64 kb + 16 j .. at column 32 kb + 8 j
-                                tc::umma_bf16_ta(d, tmem_base + kAcol + (uint32_t)(32 * kb + 8 * j),
-                                                 tc::smem_desc_sw128(bb + 32u * j), idesc, (kb | j) != 0);
-                            else
-                                tc::umma_bf16(d, tc::smem_desc_sw128(aa + 32u * j), tc::smem_desc_sw128(bb + 32u * j),
-                                              idesc, (kb | j) != 0);
-                        }
+                        for (int j = 0; j < kKB / 16; ++j)  // A: K elements 64 kb + 16 j .. at column 32 kb + 8 j
+                            tc::umma_bf16_ta(d, tmem_base + kAcol + (uint32_t)(32 * kb + 8 * j),
+                                             tc::smem_desc_sw128(bb + 32u * j), idesc, (kb | j) != 0);
                         tc::umma_commit(&bar.empty[s]);
                         if (++s == S) { s = 0; ph ^= 1u; }
                     }
@@ -562,24 +587,25 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
     } else if (warp == 2) {
         // ------------------------------------------------------------ U producer
         // Draft: the base logits U_k of pass n (global tile n / 2, columns 64 (n % 2)
-        // .. + 63 of the tile, all 128 requests) into pass buffer n % 2, one pass
-        // ahead of the epilogue, across the steps of the launch.
+        // .. + 63 of the tile, all 128 requests) into pass buffer n % kUBufs, up to
+        // kUBufs passes ahead of the epilogue, across the steps of the launch
+        // (deeper buffering measured no faster: the W2 ring is what bounds a tile).
         if (!kRes && lane == 0) {
             const int n_pass = 2 * n_tl;
             int n = 0;
             for (; n < n_pass; ++n) {
-                const int b = n & 1, g = n >> 1;
-                const uint32_t use = (uint32_t)g;
+                const int b = n % kUBufs, g = n >> 1;
+                const uint32_t use = (uint32_t)(n / kUBufs);
                 if (!tc::mbar_wait(&bar.uempty[b], (use & 1u) ^ 1u, abort_flag, kWaitNs)) break;
                 tc::mbar_arrive_expect_tx(&bar.ufull[b], (uint32_t)kUBufBytes);
-                tc::tma_load_3d(sU + b * kUBufBytes, &tm_u, &bar.ufull[b], (cidx + (g % n_local) * p.P) * kNV + 64 * b,
-                                g / n_local, row0);
+                tc::tma_load_3d(sU + b * kUBufBytes, &tm_u, &bar.ufull[b],
+                                tile_at(g, n_local, cidx, p.P) * kNV + 64 * (n & 1), g / n_local, row0);
             }
             // the copies this thread issued must land before the CTA exits
             int dummy = 0;
             volatile int* no_abort = &dummy;
-            for (int l = max(0, n - 2); l < n; ++l)
-                tc::mbar_wait(&bar.ufull[l & 1], (uint32_t)((l >> 1) & 1), no_abort, kWaitNs);
+            for (int l = max(0, n - kUBufs); l < n; ++l)
+                tc::mbar_wait(&bar.ufull[l % kUBufs], (uint32_t)((l / kUBufs) & 1), no_abort, kWaitNs);
         }
         __syncwarp();
     } else {
@@ -711,22 +737,45 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                 epi_sync();
                 for (int n = 0; staged && n < kResAhead && n < n_res; ++n) staged = stage_issue(n);
             } else {
-                // warp ew copies rows 8 ew .. 8 ew + 7, every piece in flight at once
-#pragma unroll 1
-                for (int q = 0; q < 8; ++q) {
-                    const int j = 8 * ew + q;
-                    const int t = bar.a_tok[j];
-                    const uint4* src = reinterpret_cast<const uint4*>(p.W1 + (size_t)(t < 0 ? 0 : t) * p.rank);
+                // draft: thread (row m, quarter) moves row m's K elements rank/4 *
+                // quarter .. + rank/4 - 1 of W1[token] from global memory into tensor
+                // memory (zeros for a negative token), every piece in flight at once
+                const int n16 = cpr >> 2;  // 16-byte pieces of a quarter row (at most 16)
+                const int tk = bar.a_tok[m];
+                const uint4* src = reinterpret_cast<const uint4*>(p.W1 + (size_t)(tk < 0 ? 0 : tk) * p.rank) +
+                                   quarter * n16;
+                const uint32_t tq =
+                    tmem_base + ((uint32_t)(quad * 32) << 16) + kAcol + (uint32_t)(quarter * (n16 * 4));
+                if (p.w1_wide) {  // warp-uniform: 32 bytes a lane per load, half the requests
+                    uint32_t v[8][8];
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int c = lane + 32 * h;
-                        if (c < cpr)
-                            cp_async_16(sA + (c >> 3) * kTileBytes + j * 128 + (((c & 7) ^ (j & 7)) << 4), src + c, t >= 0);
+                    for (int c = 0; c < 8; ++c) {
+                        if (2 * c < n16 && tk >= 0) {
+                            ldg_nc_32b(src + 2 * c, v[c]);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) v[c][j] = 0u;
+                        }
+                    }
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        if (2 * c < n16) tc::tmem_st_32x32b_x8(tq + (uint32_t)(8 * c), v[c]);  // warp-uniform
+                } else {
+                    uint4 v[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        v[c] = (c < n16 && tk >= 0) ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                    for (int c = 0; c < 16; c += 2) {
+                        if (c < n16) {  // warp-uniform
+                            const uint32_t w[8] = {v[c].x, v[c].y, v[c].z, v[c].w,
+                                                   v[c + 1].x, v[c + 1].y, v[c + 1].z, v[c + 1].w};
+                            tc::tmem_st_32x32b_x8(tq + (uint32_t)(4 * c), w);
+                        }
                     }
                 }
-                cp_async_wait_all();
-                // the rows are read by the tensor cores (async proxy)
-                tc::fence_proxy_async_smem();
+                tc::tmem_st_wait();
+                tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&bar.afull);
             }
@@ -746,6 +795,14 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
             // draft's races gain too little from this to pay for the atomics.)
             float bw = 0.0f, bE = 1.0f;
             float rho = INFINITY;
+            // draft: the record segment's logits (before the temperature), its pick
+            // word and first entry; the tile's segment words
+            float seg[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) seg[c] = -INFINITY;
+            uint32_t seg_a = 0u;
+            int seg_v0 = 0;
+            uint4 seg_words = make_uint4(0u, 0u, 0u, 0u);
             float g_own = -INFINITY, g_pub = -INFINITY, g_glob = -INFINITY;
             unsigned long long gkey = 0;
             const bool share = kRes && row_ok;
@@ -755,8 +812,8 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
             // ---- draft: thread = request row m x 32 columns of a tile, two
             // 16-column passes (pass h covers columns 64 h + 16 quarter .. + 15)
             for (int i = 0; i < n_local; ++i) {
-                const int t = cidx + i * p.P;
                 const int g = k * n_local + i;  // global tile of the launch: TMEM buffer, U pass phases
+                const int t = tile_at(g, n_local, cidx, p.P);
                 const int a = g & 1;
                 const uint32_t use = (uint32_t)(g >> 1);
                 // warp-uniform wait: every lane waits (acquire), all leave together
@@ -773,14 +830,16 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                     __syncwarp();  // lanes that skipped the previous pass rejoin before the aligned load
                     tc::tmem_ld_32x32b_x16<0>(taddr + 64u * h, sv);
                     // this pass's base logits, then the buffer goes back to the U producer
-                    // pass buffer h is filled once per tile: its phase parity is g & 1
-                    if (!__all_sync(0xFFFFFFFFu,
-                                    tc::mbar_wait(&bar.ufull[h], (uint32_t)(g & 1), abort_flag, kWaitNs))) {
+                    // pass 2 g + h is in buffer (2 g + h) % kUBufs, filled for the
+                    // ((2 g + h) / kUBufs)-th time
+                    const int un = 2 * g + h, ub = un % kUBufs;
+                    if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.ufull[ub], (uint32_t)((un / kUBufs) & 1), abort_flag,
+                                                               kWaitNs))) {
                         tc::tmem_ld_wait();
                         break;
                     }
-                    const uint4 q0 = *reinterpret_cast<const uint4*>(sU + h * kUBufBytes + u_off0);
-                    const uint4 q1 = *reinterpret_cast<const uint4*>(sU + h * kUBufBytes + u_off1);
+                    const uint4 q0 = *reinterpret_cast<const uint4*>(sU + ub * kUBufBytes + u_off0);
+                    const uint4 q1 = *reinterpret_cast<const uint4*>(sU + ub * kUBufBytes + u_off1);
                     uw[0] = q0.x; uw[1] = q0.y; uw[2] = q0.z; uw[3] = q0.w;
                     uw[4] = q1.x; uw[5] = q1.y; uw[6] = q1.z; uw[7] = q1.w;
                     tc::tmem_ld_wait();
@@ -798,7 +857,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                     // the values are in registers: the async proxy may overwrite the buffer
                     tc::fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&bar.uempty[h]);
+                    if (lane == 0) tc::mbar_arrive(&bar.uempty[ub]);
                     if (row_ok && nvalid > 0) {
                         if (qrow) {  // scaled logits s = (U + B) / T
                             const float sc = sampling ? p.invT : 1.0f;
@@ -832,38 +891,25 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                                 for (int c = 1; c < 16; ++c) cm = fmaxf(cm, sv[c]);
                                 return cm * c2;
                             };
-                            uint4 x[4];
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                x[q] = make_uint4((uint32_t)((v0 >> 2) + q), (uint32_t)pos, (uint32_t)rr, w3);
-                            philox4x32_10_x4(x, key0, key1);
+                            // the tile's segment uniforms: pass h races with word 2 h and
+                            // picks with word 2 h + 1 of counter 4 t + quarter
+                            if (h == 0) {
+                                uint4 x1[1] = {make_uint4((uint32_t)(4 * t + quarter), (uint32_t)pos, (uint32_t)rr, w3)};
+                                philox4x32_10_xn<1>(x1, key0, key1);
+                                seg_words = x1[0];
+                            }
+                            const uint32_t wu = h ? seg_words.z : seg_words.x;
+                            const uint32_t wa = h ? seg_words.w : seg_words.y;
                             bool rec = false;  // this thread's record moved: publish it
                             if (part.m == -INFINITY) {
-                                // the step's first values: their largest is the reference and
-                                // seeds the race (a real entry, so the winner is unchanged; it
-                                // replaces nothing when it is tested again), which spares the
-                                // no-log test the empty record's unbounded rho
-                                int cb = -1;
-                                float sb = -INFINITY;
-                                uint32_t wb = 0;
-#pragma unroll
-                                for (int c = 0; c < 16; ++c)  // a NaN is never chosen
-                                    if (sv[c] > sb) { sb = sv[c]; cb = c; wb = word_of(x[c >> 2], c & 3); }
-                                part.m = sb * c2;
-                                if (cb >= 0 && part.m != -INFINITY) {
-                                    bw = ex2(fmaf(sb, c2, -part.m));
-                                    bE = neg_log_uniform(wb);
-                                    part.idx = v0 + cb;
-                                    part.s_at = sb * c2;
-                                    rec = true;
-                                } else {
-                                    part.m = -INFINITY;  // nothing finite yet
-                                }
+                                // the step's first values: their largest is the reference
+                                const float cm = pass_max2();
+                                if (cm > -INFINITY) part.m = cm;
                             }
-                            if (part.m != -INFINITY) {                     // else nothing finite yet
-                                // rho bounds E / w of the row's winner in this thread's units
-                                // (w = 2^(s c2 - m)): this thread's record, or the best
-                                // record G of the row's four quarters, E / w = 2^(m - G)
+                            if (part.m != -INFINITY) {  // else nothing finite yet
+                                // rho bounds E / W of the row's winning segment in this thread's
+                                // units (W = sum of 2^(s c2 - m)): this thread's record, or the
+                                // best record G of the row's four quarters, E / W = 2^(m - G)
                                 float gq;
                                 {
                                     const unsigned long long raw =
@@ -876,25 +922,16 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                                     gq = fmaxf(__low2float(gm), __high2float(gm));
                                 }
                                 rho = fminf(race_bound(bE, bw), ex2(part.m - gq) * kRaceSlack);
-                                // every weight into the normaliser; entries that may beat the
-                                // running winner marked for the exact test
-                                float ps;
-                                uint32_t cand;
+                                // the segment's weight, every entry of which goes into the normaliser
                                 auto weigh = [&]() {
                                     const float nm = -part.m;
                                     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                                    cand = 0;
 #pragma unroll
-                                    for (int c = 0; c < 16; ++c) {
-                                        const uint32_t wd = word_of(x[c >> 2], c & 3);
-                                        const float w = ex2(fmaf(sv[c], c2, nm));
-                                        acc[c & 3] += w;
-                                        cand |= (one_plus_complement(wd) < fmaf(w, rho, 1.0f)) ? (1u << c) : 0u;
-                                    }
-                                    ps = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                                    for (int c = 0; c < 16; ++c) acc[c & 3] += ex2(fmaf(sv[c], c2, nm));
+                                    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
                                 };
-                                weigh();
-                                if (!(ps <= 0x1p32f)) {
+                                float ws = weigh();
+                                if (!(ws <= 0x1p32f)) {
                                     // far above the reference (or a NaN): re-reference on this pass
                                     const float cm = pass_max2();
                                     if (cm > part.m) {
@@ -903,40 +940,28 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                                         bw *= sc;
                                         part.m = cm;
                                         rho = fminf(race_bound(bE, bw), ex2(part.m - gq) * kRaceSlack);
-                                        weigh();
+                                        ws = weigh();
                                     }
                                 }
-                                part.sum += ps;
-                                // this lane's candidates one at a time, lowest column first
-                                // (the warp runs as many rounds as its busiest lane needs,
-                                // instead of one branch per column any lane marked)
-                                if (cand) {
-                                    const float nm = -part.m;
-                                    uint32_t words[16];
+                                part.sum += ws;
+                                // the segment races with E = -ln u: it can replace the record only
+                                // if 1 - u < W rho (E >= 1 - u), which needs no logarithm
+                                if (one_plus_complement(wu) < fmaf(ws, rho, 1.0f)) {
+                                    const float E = neg_log_uniform(wu);
+                                    if (ws * bE > bw * E) {
+                                        bw = ws; bE = E;
 #pragma unroll
-                                    for (int c = 0; c < 16; ++c) words[c] = word_of(x[c >> 2], c & 3);
-                                    do {
-                                        const int c = __ffs(cand) - 1;
-                                        cand &= cand - 1u;
-                                        const float sc = pick<16>(sv, c);
-                                        const float w = ex2(fmaf(sc, c2, nm));
-                                        const uint32_t wd = pick<16>(words, c);
-                                        // marked against the pass's first bound: test again against
-                                        // the record this pass may have raised before the logarithm
-                                        if (one_plus_complement(wd) < fmaf(w, rho, 1.0f)) {
-                                            const float E = neg_log_uniform(wd);
-                                            if (w * bE > bw * E) {
-                                                bw = w; bE = E; part.idx = v0 + c; part.s_at = sc * c2;
-                                                rho = fminf(rho, race_bound(bE, bw));
-                                                rec = true;
-                                            }
-                                        }
-                                    } while (cand);
+                                        for (int c = 0; c < 16; ++c) seg[c] = sv[c];
+                                        seg_a = wa;
+                                        seg_v0 = v0;
+                                        rho = fminf(rho, race_bound(bE, bw));
+                                        rec = true;
+                                    }
                                 }
                             }
                             if (rec)
                                 *reinterpret_cast<volatile unsigned short*>(&dsh.g[m][quarter]) =
-                                    __half_as_ushort(__float2half_rd(part.s_at - lg2(bE)));
+                                    __half_as_ushort(__float2half_rd(part.m + lg2(bw) - lg2(bE)));
                         }
                     }
                 }
@@ -1078,10 +1103,46 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
             if (kRes) {
                 part.score = part.idx != INT_MAX ? logf(bw) - logf(bE) : -INFINITY;
             } else if (!p.greedy) {
+                if (bw > 0.0f) {
+                    // the entry of the record segment: the first whose running sum of
+                    // weights passes a times the segment's total (weights relative to
+                    // the segment's own largest value, so none underflows)
+                    float mx = seg[0];
+#pragma unroll
+                    for (int c = 1; c < 16; ++c) mx = fmaxf(mx, seg[c]);
+                    const float nm = -mx * c2;
+                    float wt[16];
+                    float tot = 0.0f;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        wt[c] = ex2(fmaf(seg[c], c2, nm));
+                        tot += wt[c];
+                    }
+                    const float target = uniform_from_bits(seg_a) * tot;
+                    // upward: the first c whose running sum passes the target; failing
+                    // that (rounding), the last entry with weight
+                    int pick_c = -1, last_c = 0;
+                    float run = 0.0f, s_pick = seg[0];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        run += wt[c];
+                        if (wt[c] > 0.0f && pick_c < 0) { last_c = c; }
+                        if (pick_c < 0 && run > target) { pick_c = c; s_pick = seg[c]; }
+                    }
+                    if (pick_c < 0) {
+                        pick_c = last_c;
+#pragma unroll
+                        for (int c = 0; c < 16; ++c)
+                            if (c == last_c) s_pick = seg[c];
+                    }
+                    part.idx = seg_v0 + pick_c;
+                    part.s_at = s_pick * c2;
+                    // the segment's race value log W - log E in natural units
+                    part.score = fmaf(part.m + lg2(bw), kLn2F, -logf(bE));
+                }
                 // back to natural units: the max and the winner's logit
                 part.m *= kLn2F;
                 part.s_at *= kLn2F;
-                if (part.idx != INT_MAX) part.score = part.s_at - logf(bE);
             }
 
             // ---- the CTA's result of the step: the row's four quarters merged by
@@ -1185,7 +1246,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
     __syncthreads();
     if (warp == 1) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tmem_base, kRes ? kTmemColsRes : kTmemCols);
+        tc::tmem_dealloc(tmem_base, kTmemCols);
     }
     if (*abort_flag && threadIdx.x == 0) report(p.dev_status, DSPARK_ERR_TIMEOUT);
     if constexpr (kRes) residual_tokens_if_last(p, smem, bar);
@@ -1251,14 +1312,13 @@ int prepare(EncodeTiled enc, const void* U, const void* W1, const void* W2, int 
     if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return DSPARK_ERR_CUDA;
     const int nkb = rank / kKB;
-    // residual: A lives in tensor memory, the staging buffers in shared memory
+    // A lives in tensor memory; shared memory holds the residual's staging
+    // buffers, or the draft's quarter exchange and U pass buffers, then the ring
     const size_t fixed =
         1024 + sizeof(Bars) +
         (residual ? kShareBytes + (size_t)kResBufs * (kResTBytes + kResUBytes)
-                  : sizeof(DraftShared) + (size_t)nkb * kTileBytes + 2 * (size_t)kUBufBytes);
-    // the end-of-step exchange of the epilogue quarters reuses the A rows' space
-    // (draft) or the drained W2 ring (residual, at least two stages)
-    if (!residual && (size_t)nkb * kTileBytes < 3 * kM * sizeof(TcPartial)) return DSPARK_ERR_UNSUPPORTED;
+                  : sizeof(DraftShared) + (size_t)kExchBytes + (size_t)kUBufs * kUBufBytes);
+    // the residual's end-of-step exchange reuses the drained W2 ring (at least two stages)
     static_assert(2 * kTileBytes >= 3 * kM * sizeof(TcPartial), "exchange larger than two ring stages");
     if ((size_t)max_smem < fixed + 2 * kTileBytes) return DSPARK_ERR_UNSUPPORTED;
     const int n_stages = (int)std::min<size_t>(kMaxStages, ((size_t)max_smem - fixed) / kTileBytes);
@@ -1280,6 +1340,7 @@ int prepare(EncodeTiled enc, const void* U, const void* W1, const void* W2, int 
     p = TcParams();
     p.U = static_cast<const uint16_t*>(U);
     p.W1 = static_cast<const uint16_t*>(W1);
+    p.w1_wide = (reinterpret_cast<uintptr_t>(W1) & 31u) == 0;
     p.R = R;
     p.gamma = gamma;
     p.V = V;
