@@ -28,11 +28,8 @@
 //     residual: the rejected position's predecessor) and resident for the step,
 //     so that shared memory is left to the W2 ring;
 //   B (N = 128 vocabulary rows x K = rank) = W2 tiles streamed by TMA through a
-//     ring of 16 KB stages (11 at rank 512 in the draft: 176 KB in flight per
-//     SM, which is what it takes to cover the loaded latency of a load, about
-//     2-3 us); the next tile's boxes are prefetched into L2 one tile ahead (two
-//     at a step's first tile); odd steps take a CTA's tiles in reverse order, so
-//     a step starts on tiles still in L2;
+//     ring of 16 KB stages (8, 128 KB in flight per SM; 6 to 12 measure alike,
+//     4 is slower; no L2 prefetch ahead of the ring, which only added traffic);
 //   D = A . B^T in fp32 tensor memory, two 128-column buffers so the epilogue
 //     of one vocabulary tile overlaps the MMAs of the next;
 //   U_k (draft) = the tile's base logits, by TMA into two 16 KB pass buffers
@@ -106,16 +103,11 @@ constexpr int kResTBytes = kM * kResCols * 4;  // 16 KB
 constexpr int kResUBytes = kM * kResCols * 2;  // 8 KB
 constexpr int kResBufs = 6;                    // staging buffers
 constexpr int kResAhead = kResBufs - 2;        // passes whose copies are issued ahead of the one computed
-constexpr int kMaxStages = 12;
+constexpr int kMaxStages = 8;
 constexpr int kMaxP = 256;                    // CTAs per request block (pieces per request)
 constexpr uint32_t kTmemCols = 512;     // two 128-column accumulators, then the A rows (at most 256 columns)
 constexpr uint32_t kAcol = 256;         // first tensor-memory column of A
 constexpr uint64_t kWaitNs = 2000000000ull;
-// W2 tiles pulled into L2 ahead of the ring: kPfAhead past the tile being
-// loaded, kPfStepAhead at a step's first tile (while the grid waits between
-// steps, HBM keeps streaming the step's later tiles)
-constexpr int kPfAhead = 1;
-constexpr int kPfStepAhead = 2;
 constexpr float kLog2eF = 1.4426950408889634f;
 constexpr float kLn2F = 0.6931471805599453f;
 // Relative slack of the no-log race test, far above the rounding of the
@@ -233,12 +225,10 @@ __device__ __forceinline__ unsigned long long winner_key(float score, int idx) {
 __device__ __forceinline__ int key_index(unsigned long long key) { return (int)~(uint32_t)key; }
 
 // Vocabulary tile of a CTA's launch-global tile g (step g / n_local, the
-// step's i-th tile of the CTA's tiles cidx, cidx + P, ...).  Odd steps take the
-// CTA's tiles in reverse order, so that a step starts on the W2 tiles the
-// previous step ended with, which are still in L2.
+// step's i-th tile of the CTA's tiles cidx, cidx + P, ...).  (Running odd steps
+// in reverse order, to start on tiles still in L2, measured slower.)
 __device__ __forceinline__ int tile_at(int g, int n_local, int cidx, int P) {
-    const int k = g / n_local, i = g - k * n_local;
-    return cidx + ((k & 1) ? n_local - 1 - i : i) * P;
+    return cidx + (g % n_local) * P;
 }
 
 // 2^x on the special-function unit (relative error about 2^-22; the race
@@ -314,15 +304,6 @@ __device__ __forceinline__ void ldg_nc_32b(const void* p, uint32_t (&w)[8]) {
                  : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
                  : "l"(p));
 }
-
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
-
 
 // 16 bytes global -> shared without registers; zeros when !valid (nothing read).
 __device__ __forceinline__ void cp_async_16(void* dst, const void* src, bool valid) {
@@ -501,22 +482,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         // ------------------------------------------------------------ producer
         // The W2 ring, tile-major over every step of the launch (the tiles are the
         // same at each step): nothing here depends on the draws, so the ring runs
-        // into the next step while the epilogue finishes the current one.
+        // into the next step while the epilogue finishes the current one.  (No L2
+        // prefetch ahead of the ring: the deep ring alone keeps HBM streaming, and
+        // prefetch requests measured as extra traffic that slowed it.)
         if (lane == 0) {
-            // L2 prefetch of global tile g (W2 boxes and, draft, the step's U passes)
-            auto prefetch_tile = [&](int g) {
-                const int tn = tile_at(g, n_local, cidx, p.P);
-                for (int q = 0; q < p.nkb; ++q) tma_prefetch_l2_2d(&tm_w2, q * kKB, tn * kNV);
-                if (!kRes) {
-                    tc::tma_prefetch_l2_3d(&tm_u, tn * kNV, g / n_local, row0);
-                    tc::tma_prefetch_l2_3d(&tm_u, tn * kNV + kKB, g / n_local, row0);
-                }
-            };
-            // prefetched up to (not including) global tile pf_next: one tile ahead,
-            // and two at a step's first tile, so that HBM keeps streaming the
-            // step's next tiles while the grid waits between steps
-            int pf_next = 0;
-            for (; pf_next <= kPfStepAhead && pf_next < n_tl; ++pf_next) prefetch_tile(pf_next);
             const int n_loads = n_tl * p.nkb;  // W2 stage loads
             int issued = 0;
             bool ok = true;
@@ -529,11 +498,6 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                 const int t = tile_at(g, n_local, cidx, p.P);
                 tc::mbar_arrive_expect_tx(&bar.full[s], kTileBytes);
                 tc::tma_load_2d(sB + s * kTileBytes, &tm_w2, &bar.full[s], kb * kKB, t * kNV);
-                // once a tile's first ring of loads is out, pull the next tile(s) into L2
-                if (kb == min(S, p.nkb) - 1) {
-                    const int horizon = min(n_tl - 1, g + (g % n_local == 0 ? kPfStepAhead : kPfAhead));
-                    for (; pf_next <= horizon; ++pf_next) prefetch_tile(pf_next);
-                }
             }
             // the copies this thread issued must land before the CTA exits
             if (!ok) {
