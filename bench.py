@@ -700,7 +700,8 @@ def run_ours(args):
     kname = "markov_tc_kernel<draft>" if cyc.uses_tc else "draft_bias_simt+draft_sample"
     digest = source_digest(["speculative_decoding_dspark_gb300/csrc/draft_tc.cu" if cyc.uses_tc else
                             "speculative_decoding_dspark_gb300/csrc/draft_simt.cu",
-                            "speculative_decoding_dspark_gb300/csrc/common.cuh"])
+                            "speculative_decoding_dspark_gb300/csrc/common.cuh",
+                            "speculative_decoding_dspark_gb300/csrc/tc_ptx.cuh"])
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
             "traffic": traffic_from_profile(kname, digest), "kernel": kname,
             "algorithmic_bytes_per_launch": launch_bytes, "steps_per_launch": steps_per_launch,

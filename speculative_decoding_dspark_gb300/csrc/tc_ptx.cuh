@@ -63,11 +63,14 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
     return ok != 0;
 }
 
-// Wait for the phase of parity `parity` to complete, at most limit_ns.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          uint64_t limit_ns) {
+// The bounded wait's slow path: sleep on the barrier until the phase completes,
+// another thread aborts, or limit_ns has passed (then abort).  Out of line, so
+// that the callers' hot loops stay free of its code: in the MMA issuer an
+// inlined copy made every tcgen05.mma cost ~117 cycles of issue against ~97
+// with this one out of line (64 with no wait at all).
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                            uint64_t limit_ns) {
     constexpr uint32_t kSleepNs = 20000;
-    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (;;) {
         if (mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
@@ -77,6 +80,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
             return false;
         }
     }
+}
+
+// Wait for the phase of parity `parity` to complete, at most limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t limit_ns) {
+    if (__builtin_expect(mbar_try_wait(bar, parity), 1)) return true;
+    return mbar_wait_slow(bar, parity, abort_flag, limit_ns);
 }
 
 // ---------------------------------------------------------------- proxies
