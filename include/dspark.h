@@ -69,6 +69,9 @@ typedef struct CUstream_st* dspark_stream_t;
 #define DSPARK_ERR_TIMEOUT (-5)      /* device side: a bounded wait gave up            */
 #define DSPARK_ERR_DEVICE_INPUT (-6) /* device side: bad token id / length / confidence */
 #define DSPARK_ERR_WORKSPACE (-7)    /* workspace NULL, misaligned or too small        */
+#define DSPARK_ERR_BOUNDS (-8)       /* DSPARK_DEBUG builds only: a device-side index
+                                        check failed; the access was skipped, so the
+                                        outputs of that call are invalid            */
 
 /* Largest R the verify calls accept (their per-round request list is kept in
  * shared memory). */

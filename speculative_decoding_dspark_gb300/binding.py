@@ -15,7 +15,8 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libdspark.so")
+# DSPARK_LIBRARY may name another build of the library (the DSPARK_DEBUG one)
+LIB_PATH = os.environ.get("DSPARK_LIBRARY") or os.path.join(_HERE, "libdspark.so")
 
 DSPARK_OK = 0
 DSPARK_ERR_INVALID_ARG = -1
@@ -25,6 +26,7 @@ DSPARK_ERR_CUDA = -4
 DSPARK_ERR_TIMEOUT = -5
 DSPARK_ERR_DEVICE_INPUT = -6
 DSPARK_ERR_WORKSPACE = -7
+DSPARK_ERR_BOUNDS = -8
 
 DSPARK_F32, DSPARK_BF16 = 0, 1
 DSPARK_OP_DRAFT, DSPARK_OP_VERIFY, DSPARK_OP_SELECT, DSPARK_OP_VERIFY_MARKOV, DSPARK_OP_CALIBRATE = 0, 1, 2, 3, 4

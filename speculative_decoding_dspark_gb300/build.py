@@ -4,6 +4,11 @@ Each .cu under csrc/ is compiled to an object in parallel, then linked into
 one shared library next to this file.  cudart is linked statically, so the
 library needs no CUDA driver to be loaded (the driver is resolved at run time
 through the runtime's entry-point query).
+
+build(debug=True) builds libdspark_debug.so instead, with -DDSPARK_DEBUG: the
+kernels then check the indices they compute (decoded tokens, packed-target
+rows, pages) and report DSPARK_ERR_BOUNDS instead of making the access.  The
+binding loads it when DSPARK_LIBRARY names it.
 """
 from __future__ import annotations
 
@@ -20,6 +25,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdspark.so")
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(HERE, "libdspark_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -30,8 +37,8 @@ def nvcc() -> str:
     return path
 
 
-def _flags(verbose_ptxas: bool):
-    f = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
+def _flags(verbose_ptxas: bool, debug: bool = False):
+    f = (["-DDSPARK_DEBUG"] if debug else []) + ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                 "-I" + INCLUDE, "-I" + CSRC, "--expt-relaxed-constexpr"]
     if verbose_ptxas:
         f += ["-Xptxas", "-v"]
@@ -46,22 +53,23 @@ def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + [os.path.join(INCLUDE, "dspark.h")]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None, debug: bool = False) -> str:
+    lib, bdir = (LIB_DEBUG, BUILD_DEBUG) if debug else (LIB, BUILD)
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
-    flags = _flags(verbose_ptxas)
+    flags = _flags(verbose_ptxas, debug)
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
         cmd = [cc, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -75,14 +83,14 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
         for _, log in results:
             sys.stderr.write(log)
     objs = [o for o, _ in results]
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv, debug="--debug" in sys.argv))

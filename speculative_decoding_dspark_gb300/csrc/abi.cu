@@ -118,6 +118,7 @@ const char* dspark_status_string(int status) {
         case DSPARK_ERR_TIMEOUT: return "device wait timed out";
         case DSPARK_ERR_DEVICE_INPUT: return "bad device-side input (token id, length or confidence)";
         case DSPARK_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case DSPARK_ERR_BOUNDS: return "device-side bounds check failed (debug build)";
         default: return "unknown status";
     }
 }

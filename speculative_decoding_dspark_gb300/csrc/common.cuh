@@ -112,6 +112,23 @@ __device__ __forceinline__ void report(int32_t* dev_status, int code) {
     if (dev_status) atomicCAS(dev_status, 0, code);
 }
 
+// Bounds checks of a DSPARK_DEBUG build: IN_BOUNDS(cond, status) is cond, and
+// reports DSPARK_ERR_BOUNDS when cond fails, so that the guarded access can be
+// skipped instead of faulting; in a normal build it is `true` and costs nothing.
+// The checks cover indices computed inside the kernels (decoded tokens, rows
+// of the packed target, statistics and workspace slots, pages); the inputs the
+// pages define (token ids < V, cu_seqlens monotone, l <= gamma) are checked in
+// every build.
+#ifdef DSPARK_DEBUG
+__device__ __forceinline__ bool in_bounds_check(bool cond, int32_t* dev_status) {
+    if (!cond) report(dev_status, DSPARK_ERR_BOUNDS);
+    return cond;
+}
+#define IN_BOUNDS(cond, dev_status) in_bounds_check((cond), (dev_status))
+#else
+#define IN_BOUNDS(cond, dev_status) true
+#endif
+
 // ---------------------------------------------------------------------------
 // Reductions.
 // ---------------------------------------------------------------------------

@@ -705,7 +705,8 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                 // quarter .. + rank/4 - 1 of W1[token] from global memory into tensor
                 // memory (zeros for a negative token), every piece in flight at once
                 const int n16 = cpr >> 2;  // 16-byte pieces of a quarter row (at most 16)
-                const int tk = bar.a_tok[m];
+                const int tk0 = bar.a_tok[m];
+                const int tk = (tk0 < 0 || IN_BOUNDS(tk0 < p.V, p.dev_status)) ? tk0 : -1;
                 const uint4* src = reinterpret_cast<const uint4*>(p.W1 + (size_t)(tk < 0 ? 0 : tk) * p.rank) +
                                    quarter * n16;
                 const uint32_t tq =
@@ -1122,7 +1123,8 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                     const size_t slot = (size_t)k * p.R + rr;
                     if (!p.greedy)
                         p.parts[slot * p.P + cidx] = make_float4(part.m, part.sum, part.s_at, __int_as_float(part.idx));
-                    if (part.idx != INT_MAX) atomicMax(p.keys + slot, winner_key(part.score, part.idx));
+                    if (part.idx != INT_MAX && IN_BOUNDS(part.idx >= 0 && part.idx < p.V, p.dev_status))
+                        atomicMax(p.keys + slot, winner_key(part.score, part.idx));
                 }
             }
             if (k + 1 < n_steps) {
@@ -1180,6 +1182,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                         continue;
                     }
                     const int idx = key_index(key);
+                    if (!IN_BOUNDS(idx >= 0 && idx < p.V, p.dev_status)) {
+                        if (lane == 0) p.y[rk] = -1;
+                        continue;
+                    }
                     if (p.greedy) {
                         if (lane == 0) p.y[rk] = idx;
                         continue;

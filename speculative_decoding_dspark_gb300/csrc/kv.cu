@@ -111,7 +111,11 @@ __global__ void __launch_bounds__(kKvThreads) kv_reserve_kernel(const int32_t* k
         int tot;
         const int o = carry + kv_scan(need, &tot, warp_sums);
         if (r < R) {
-            for (int i = 0; i < need; ++i) bt[(size_t)r * max_blocks + have + i] = free_pages[base_page + o + i];
+            for (int i = 0; i < need; ++i) {
+                const int32_t pg = free_pages[base_page + o + i];
+                // (a debug build: a page id outside the pool is reported and not handed out)
+                bt[(size_t)r * max_blocks + have + i] = IN_BOUNDS(pg >= 0 && pg < pool_pages, dev_status) ? pg : -1;
+            }
             if (reserved) reserved[r] = need;
         }
         carry += tot;
@@ -176,7 +180,7 @@ __global__ void __launch_bounds__(kKvThreads) kv_commit_kernel(int32_t* kv_len, 
         if (r < R) {
             for (int b = keep; b < held; ++b) {
                 int32_t* e = bt + (size_t)r * max_blocks + b;
-                if (*e >= 0) free_pages[o++] = *e;
+                if (*e >= 0 && IN_BOUNDS(*e < pool_pages, dev_status)) free_pages[o++] = *e;
                 *e = -1;
             }
             kv_len[r] = new_len;

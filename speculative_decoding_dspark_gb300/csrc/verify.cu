@@ -184,7 +184,7 @@ __device__ __forceinline__ DecideInputs decide_inputs(const VerifyParams& p, int
     d.valid = p.valid[r];
     d.first = p.cu[r];
     d.l = p.cu[r + 1] - d.first - 1;
-    if (d.valid && j < d.l) {
+    if (d.valid && j < d.l && IN_BOUNDS(d.first + j < p.max_rows, p.dev_status)) {
         d.y = p.y[(size_t)r * p.gamma + j];
         if (!kGreedy) {
             d.t = __ldcg(p.target + (size_t)(d.first + j) * p.V + d.y);  // (the target may be host memory)
@@ -338,7 +338,9 @@ __global__ void __launch_bounds__(kRoundThreads, 1) verify_rounds_kernel(VerifyP
             const int a = u / p.nsub;
             sub = u - a * p.nsub;
             r = act_at(a);
-            return __ldg(p.cu + r) + j;
+            const int row = __ldg(p.cu + r) + j;
+            // (a debug build: a row outside the packed target is read as row 0)
+            return IN_BOUNDS(row >= 0 && row < p.max_rows && r >= 0 && r < p.R, p.dev_status) ? row : 0;
         };
         float4 buf[kStatVec];
         if (vec && w0 < n_units) {
@@ -513,6 +515,7 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_correct_kernel(VerifyPa
     if (*reinterpret_cast<volatile int*>(p.lazy + kAbort)) return;
     const VerifyJob job = p.jobs[r];
     if (job.mode == 0) return;
+    if (!IN_BOUNDS(job.row >= 0 && job.row < p.max_rows && job.pos >= 0 && job.pos < p.gamma, p.dev_status)) return;
     const int V = p.V;
     const int v0 = chunk * kVerifyChunk;
     const int v1 = min(V, v0 + kVerifyChunk);

@@ -37,9 +37,24 @@ def test_exports_every_declared_symbol(lib):
     assert set(binding.EXPORTED) == set(names)
 
 
+def test_debug_build_exports_every_declared_symbol():
+    """The DSPARK_DEBUG build (device-side bounds checks) compiles and exports the
+    same functions."""
+    from speculative_decoding_dspark_gb300 import build
+    try:
+        build.nvcc()
+    except RuntimeError:
+        pytest.skip("nvcc not available")
+    dbg = ctypes.CDLL(build.build(debug=True))
+    for n in declared_functions():
+        assert hasattr(dbg, n), n
+    dbg.dspark_status_string.restype = ctypes.c_char_p
+    assert b"bounds" in dbg.dspark_status_string(-8)
+
+
 def test_status_strings_and_version(lib):
     lib.dspark_status_string.restype = ctypes.c_char_p
-    for code in range(0, -8, -1):
+    for code in range(0, -9, -1):
         s = lib.dspark_status_string(code).decode()
         assert s and s != "unknown status"
     assert lib.dspark_status_string(-99).decode() == "unknown status"

@@ -156,6 +156,40 @@ def test_draft_rank512_full_vocab_sampled(B, orc):
     tally.check()
 
 
+@pytest.mark.parametrize("rank", [64, 512])
+def test_draft_w1_alignment_fallback(B, orc, rank):
+    """W1 16 bytes past a 32-byte boundary: the tensor-core draft then reads the
+    A rows 16 bytes a lane instead of 32.  The outputs equal the aligned call's
+    bit for bit, and the oracle's."""
+    w, d = H.cycle_inputs("batched_sampling", R=130, V=17416, gamma=3, rank=rank, w_sigma=0.2)
+    assert B.dspark_markov_draft_uses_tensor_cores(B.DSPARK_BF16, B.DSPARK_BF16, 130, 17416, rank)
+    T = 0.7
+    ref = H.gpu_draft(d, T, 4, want_logits=False)
+    W1 = H.dev(d["W1"])
+    buf = torch.empty(W1.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    W1_off = buf[8:].view(W1.shape)
+    W1_off.copy_(W1)
+    assert W1_off.data_ptr() % 32 == 16
+    U, W2 = H.dev(d["U"]), H.dev(d["W2"])
+    R, gamma, V = U.shape
+    y = torch.full((R, gamma), -7, dtype=torch.int32, device="cuda")
+    q_lse = torch.full((R, gamma), float("nan"), device="cuda")
+    q_tok = torch.full((R, gamma), float("nan"), device="cuda")
+    ws = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_DRAFT, R, gamma, V, rank, 0, B.DSPARK_BF16, 0))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.dspark_markov_draft(U, W1_off, W2, H.dev(d["anchor"]), H.dev(d["seeds"]), 4, T, y, q_lse, q_tok, None, ws,
+                          status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    np.testing.assert_array_equal(H.host(y), ref["y"])
+    np.testing.assert_array_equal(H.host(q_lse), ref["q_lse"])
+    np.testing.assert_array_equal(H.host(q_tok), ref["q_tok"])
+    o = orc.markov_draft(d["U"], d["W1"], d["W2"], d["anchor"], d["seeds"], 4, T, want_logits=False)
+    tally = H.Tally()
+    H.compare_draft(tally, dict(y=H.host(y), q_lse=H.host(q_lse), q_tok=H.host(q_tok)), o, T)
+    tally.check()
+
+
 def test_draft_tiny_many_cycles(B, orc):
     """The V=64 workload: 2000 cycles at T=1 and 2000 greedy."""
     w, d = H.cycle_inputs("tiny_exhaustive")
