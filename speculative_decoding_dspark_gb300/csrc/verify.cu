@@ -515,7 +515,10 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_correct_kernel(VerifyPa
     if (*reinterpret_cast<volatile int*>(p.lazy + kAbort)) return;
     const VerifyJob job = p.jobs[r];
     if (job.mode == 0) return;
-    if (!IN_BOUNDS(job.row >= 0 && job.row < p.max_rows && job.pos >= 0 && job.pos < p.gamma, p.dev_status)) return;
+    if (!IN_BOUNDS(job.row >= 0 && job.row < p.max_rows && job.pos >= 0 &&
+                       (job.mode == 1 ? job.pos < p.gamma : job.pos <= p.gamma),  // a bonus draws at pos = l <= gamma
+                   p.dev_status))
+        return;
     const int V = p.V;
     const int v0 = chunk * kVerifyChunk;
     const int v1 = min(V, v0 + kVerifyChunk);

@@ -5,7 +5,8 @@ DSPARK_LIBRARY, so that this process keeps the normal library.  On valid
 inputs the debug build's outputs equal the normal build's bit for bit with
 status 0; a free-page stack holding a page id outside the pool (a value the
 normal build does not check) is reported as DSPARK_ERR_BOUNDS, and the page is
-not handed out.
+not handed out.  One verify case accepts every draft, so each bonus draw sits at
+position gamma, the largest position the checks must let through.
 """
 import json
 import os
@@ -50,6 +51,24 @@ CHILD = textwrap.dedent(r"""
         out[f"draft_{T}"] = [g["status"], g["y"].tolist(), g["q_lse"].tolist(), g["q_tok"].tolist()]
         out[f"markov_{T}"] = [gm["status"], gm["n_acc"].tolist(), gm["out_tokens"].tolist(), gm["p_tok"].tolist()]
         out[f"verify_{T}"] = [gv["status"], gv["n_acc"].tolist(), gv["out_tokens"].tolist(), gv["p_tok"].tolist()]
+    # stored-logits verify where every request accepts all gamma drafts, so the
+    # bonus draw sits at position gamma (the last row of each request)
+    R, V, gamma = 8, 1032, 3
+    rng = np.random.default_rng(5)
+    y = rng.integers(0, V, (R, gamma)).astype(np.int32)
+    ql = rng.standard_normal((R, gamma, V)).astype(np.float32)
+    m = ql.max(axis=2, keepdims=True)
+    q_lse = (m[..., 0] + np.log(np.exp(ql - m).sum(axis=2))).astype(np.float32)
+    q_tok = np.exp(np.take_along_axis(ql, y[..., None], 2)[..., 0] - q_lse).astype(np.float32)
+    target = np.zeros((R * (gamma + 1), V), np.float32)
+    for r in range(R):
+        for j in range(gamma):
+            target[r * (gamma + 1) + j, y[r, j]] = 60.0  # p(y) = 1: accepted
+        target[r * (gamma + 1) + gamma] = rng.standard_normal(V).astype(np.float32)
+    cu = inputs.cu_from_lengths(np.full(R, gamma, np.int32))
+    seeds = inputs.request_seeds(0x5EED0300, R)
+    gv = H.gpu_verify(target, cu, y, ql, q_lse, q_tok, seeds, 0, 1.0)
+    out["verify_bonus"] = [gv["status"], gv["n_acc"].tolist(), gv["out_tokens"].tolist(), gv["p_tok"].tolist()]
     # paged KV: a valid reserve and commit, then a stack with a page id outside the pool
     R, P, pool = 4, 16, 64
     kv_len = np.array([5, 16, 0, 31], np.int32)
@@ -106,6 +125,7 @@ def test_debug_build_matches_and_checks():
         assert debug[key] == normal[key], key
         if key.startswith(("draft", "markov", "verify")):
             assert normal[key][0] == 0, (key, normal[key][0])
+    assert normal["verify_bonus"][1] == [3] * 8  # every request took the bonus draw at position gamma
     assert normal["kv_False"][:2] == [0, 0]
     # the bad page id: handed out silently by the normal build, refused by the debug one
     B_ERR_BOUNDS = -8
