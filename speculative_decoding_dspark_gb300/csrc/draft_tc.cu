@@ -73,8 +73,11 @@
 //
 // Warp roles: warp 0 = W2 TMA producer, warp 1 = MMA issuer (and TMEM
 // owner), warp 2 = U TMA producer (draft), warps 3-18 = epilogue (and the A
-// rows).  Every mbarrier wait and the grid barrier are bounded (2 s); a timeout
-// aborts every CTA cleanly and reports DSPARK_ERR_TIMEOUT.
+// rows).  The three control warps each share a scheduler with four epilogue
+// warps that leave them few issue slots, so each runs its loop as a whole warp
+// (its state in uniform registers) and lets one elected lane issue the copies,
+// MMAs and commits.  Every mbarrier wait and the grid barrier are bounded
+// (2 s); a timeout aborts every CTA cleanly and reports DSPARK_ERR_TIMEOUT.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -104,6 +107,7 @@ constexpr int kResUBytes = kM * kResCols * 2;  // 8 KB
 constexpr int kResBufs = 6;                    // staging buffers
 constexpr int kResAhead = kResBufs - 2;        // passes whose copies are issued ahead of the one computed
 constexpr int kMaxStages = 8;
+constexpr int kMaxKb = 8;                   // k-blocks of a tile at rank 512, the largest
 constexpr int kMaxP = 256;                    // CTAs per request block (pieces per request)
 constexpr uint32_t kTmemCols = 512;     // two 128-column accumulators, then the A rows (at most 256 columns)
 constexpr uint32_t kAcol = 256;         // first tensor-memory column of A
@@ -484,69 +488,110 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         // same at each step): nothing here depends on the draws, so the ring runs
         // into the next step while the epilogue finishes the current one.  (No L2
         // prefetch ahead of the ring: the deep ring alone keeps HBM streaming, and
-        // prefetch requests measured as extra traffic that slowed it.)
-        if (lane == 0) {
-            const int n_loads = n_tl * p.nkb;  // W2 stage loads
-            int issued = 0;
-            bool ok = true;
+        // prefetch requests measured as extra traffic that slowed it.)  The whole
+        // warp runs the loop and one elected lane issues each load.  With several
+        // request blocks (their CTAs reread each tile from L2) the loads must go out
+        // as soon as stages free: the indices are counters, and this form took the
+        // R = 512 draft from 0.52 to 0.37 ms against a lane-0 loop that divides per
+        // load.  With one block (every tile streamed from HBM once) the dividing
+        // loop measured 2-4 % faster at R = 128 with sampling (and as much slower
+        // at R = 16 greedy); no load order or issue pacing that was tried explains
+        // it, and it is kept for that case.
+        const int n_loads = n_tl * p.nkb;  // W2 stage loads
+        int issued = 0;
+        bool ok = true;
+        if (p.nb == 1) {
             for (; issued < n_loads; ++issued) {
                 // load l goes to stage l % S, used for the (l / S)-th time
                 const int s = issued % S;
                 const uint32_t ph = (uint32_t)((issued / S) & 1);
-                if (!tc::mbar_wait(&bar.empty[s], ph ^ 1u, abort_flag, kWaitNs)) { ok = false; break; }
+                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.empty[s], ph ^ 1u, abort_flag, kWaitNs))) {
+                    ok = false;
+                    break;
+                }
                 const int g = issued / p.nkb, kb = issued - g * p.nkb;
                 const int t = tile_at(g, n_local, cidx, p.P);
-                tc::mbar_arrive_expect_tx(&bar.full[s], kTileBytes);
-                tc::tma_load_2d(sB + s * kTileBytes, &tm_w2, &bar.full[s], kb * kKB, t * kNV);
+                tc::tma_load_2d_elect(sB + s * kTileBytes, &tm_w2, &bar.full[s], kb * kKB, t * kNV, kTileBytes);
             }
-            // the copies this thread issued must land before the CTA exits
-            if (!ok) {
-                int dummy = 0;
-                volatile int* no_abort = &dummy;
-                for (int l = max(0, issued - S); l < issued; ++l)
-                    tc::mbar_wait(&bar.full[l % S], (uint32_t)((l / S) & 1), no_abort, kWaitNs);
+        } else {
+            int s = 0, kb = 0, i = 0, t = cidx;  // stage, k-block, local tile, tile
+            uint32_t ph = 0;
+            for (; issued < n_loads; ++issued) {
+                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.empty[s], ph ^ 1u, abort_flag, kWaitNs))) {
+                    ok = false;
+                    break;
+                }
+                tc::tma_load_2d_elect(sB + s * kTileBytes, &tm_w2, &bar.full[s], kb * kKB, t * kNV, kTileBytes);
+                if (++s == S) { s = 0; ph ^= 1u; }
+                if (++kb == p.nkb) {
+                    kb = 0;
+                    if (++i == n_local) { i = 0; t = cidx; } else { t += p.P; }
+                }
             }
+        }
+        // the copies this warp issued must land before the CTA exits
+        if (!ok && lane == 0) {
+            int dummy = 0;
+            volatile int* no_abort = &dummy;
+            for (int l = max(0, issued - S); l < issued; ++l)
+                tc::mbar_wait(&bar.full[l % S], (uint32_t)((l / S) & 1), no_abort, kWaitNs);
         }
         __syncwarp();  // the warp reconverges before the CTA-wide barrier below
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_bf16_f32(kM, kNV);
-            bool ok = true;
-            int s = 0;
-            uint32_t ph = 0;
-            const uint32_t b_base = tc::smem_u32(sB);
-            for (int k = 0; ok && k < n_steps; ++k) {
-                // the step's A rows, written by the epilogue warps
-                if (!tc::mbar_wait(&bar.afull, (uint32_t)(k & 1), abort_flag, kWaitNs)) { ok = false; break; }
+        // The whole warp runs the loop and waits; one elected lane issues the MMAs
+        // and commits (a lane-0 loop cost about 100 cycles of issue per MMA with
+        // the epilogue idle and ~180 beside a busy one, against 64 for the MMA).
+        // A tile's k-block kb reads A from column kAcol + 32 kb and B from ring
+        // stage s, whose descriptor is the ring base's plus s * 16 KB.
+        constexpr uint32_t idesc = tc::idesc_bf16_f32(kM, kNV);
+        bool ok = true;
+        int s = 0;
+        uint32_t ph = 0;
+        const uint64_t desc0 = tc::smem_desc_sw128(tc::smem_u32(sB));
+        const uint32_t a_base = tmem_base + kAcol;
+        for (int k = 0; ok && k < n_steps; ++k) {
+            // the step's A rows, written by the epilogue warps
+            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.afull, (uint32_t)(k & 1), abort_flag, kWaitNs))) {
+                ok = false;
+                break;
+            }
+            tc::tc_fence_after();
+            for (int i = 0; ok && i < n_local; ++i) {
+                const int g = k * n_local + i;
+                const int a = g & 1;
+                const uint32_t use = (uint32_t)(g >> 1);
+                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.tempty[a], (use & 1u) ^ 1u, abort_flag, kWaitNs))) {
+                    ok = false;
+                    break;
+                }
                 tc::tc_fence_after();
-                for (int i = 0; ok && i < n_local; ++i) {
-                    const int g = k * n_local + i;
-                    const int a = g & 1;
-                    const uint32_t use = (uint32_t)(g >> 1);
-                    if (!tc::mbar_wait(&bar.tempty[a], (use & 1u) ^ 1u, abort_flag, kWaitNs)) { ok = false; break; }
-                    tc::tc_fence_after();
-                    const uint32_t d = tmem_base + (uint32_t)(a * kNV);
-                    for (int kb = 0; kb < p.nkb; ++kb) {
-                        if (!tc::mbar_wait(&bar.full[s], ph, abort_flag, kWaitNs)) { ok = false; break; }
+                const uint32_t d = tmem_base + (uint32_t)(a * kNV);
+#pragma unroll
+                for (int kb = 0; kb < kMaxKb; ++kb) {
+                    if (kb < p.nkb) {  // warp-uniform
+                        if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.full[s], ph, abort_flag, kWaitNs))) {
+                            ok = false;
+                            break;
+                        }
                         tc::tc_fence_after();
-                        const uint32_t bb = b_base + (uint32_t)(s * kTileBytes);
+                        const uint64_t bd = desc0 + (uint64_t)(s * (kTileBytes >> 4));
 #pragma unroll
                         for (int j = 0; j < kKB / 16; ++j)  // A: K elements 64 kb + 16 j .. at column 32 kb + 8 j
-                            tc::umma_bf16_ta(d, tmem_base + kAcol + (uint32_t)(32 * kb + 8 * j),
-                                             tc::smem_desc_sw128(bb + 32u * j), idesc, (kb | j) != 0);
-                        tc::umma_commit(&bar.empty[s]);
+                            tc::umma_bf16_ta_elect(d, a_base + (uint32_t)(32 * kb + 8 * j), bd + (uint64_t)(2 * j),
+                                                   idesc, (kb | j) != 0);
+                        tc::umma_commit_elect(&bar.empty[s]);
                         if (++s == S) { s = 0; ph ^= 1u; }
                     }
-                    if (ok) tc::umma_commit(&bar.tfull[a]);
                 }
+                if (ok) tc::umma_commit_elect(&bar.tfull[a]);
             }
-            // every MMA issued has completed before anyone frees tensor memory
-            tc::umma_commit(&bar.mma_done);
-            int dummy = 0;
-            volatile int* no_abort = &dummy;
-            tc::mbar_wait(&bar.mma_done, 0, no_abort, kWaitNs);
         }
+        // every MMA issued has completed before anyone frees tensor memory
+        tc::umma_commit_elect(&bar.mma_done);
+        int dummy = 0;
+        volatile int* no_abort = &dummy;
+        tc::mbar_wait(&bar.mma_done, 0, no_abort, kWaitNs);
         __syncwarp();
     } else if (warp == 2) {
         // ------------------------------------------------------------ U producer
@@ -554,22 +599,28 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         // .. + 63 of the tile, all 128 requests) into pass buffer n % kUBufs, up to
         // kUBufs passes ahead of the epilogue, across the steps of the launch
         // (deeper buffering measured no faster: the W2 ring is what bounds a tile).
-        if (!kRes && lane == 0) {
+        if (!kRes) {
             const int n_pass = 2 * n_tl;
             int n = 0;
+            int b = 0, half = 0, i = 0, step = 0, t = cidx;  // buffer, pass of the tile, local tile, step, tile
+            uint32_t uph = 0;
             for (; n < n_pass; ++n) {
-                const int b = n % kUBufs, g = n >> 1;
-                const uint32_t use = (uint32_t)(n / kUBufs);
-                if (!tc::mbar_wait(&bar.uempty[b], (use & 1u) ^ 1u, abort_flag, kWaitNs)) break;
-                tc::mbar_arrive_expect_tx(&bar.ufull[b], (uint32_t)kUBufBytes);
-                tc::tma_load_3d(sU + b * kUBufBytes, &tm_u, &bar.ufull[b],
-                                tile_at(g, n_local, cidx, p.P) * kNV + 64 * (n & 1), g / n_local, row0);
+                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.uempty[b], uph ^ 1u, abort_flag, kWaitNs))) break;
+                tc::tma_load_3d_elect(sU + b * kUBufBytes, &tm_u, &bar.ufull[b], t * kNV + 64 * half, step, row0,
+                                      (uint32_t)kUBufBytes);
+                if (++b == kUBufs) { b = 0; uph ^= 1u; }
+                if (++half == 2) {
+                    half = 0;
+                    if (++i == n_local) { i = 0; t = cidx; ++step; } else { t += p.P; }
+                }
             }
-            // the copies this thread issued must land before the CTA exits
-            int dummy = 0;
-            volatile int* no_abort = &dummy;
-            for (int l = max(0, n - kUBufs); l < n; ++l)
-                tc::mbar_wait(&bar.ufull[l % kUBufs], (uint32_t)((l / kUBufs) & 1), no_abort, kWaitNs);
+            // the copies this warp issued must land before the CTA exits
+            if (lane == 0) {
+                int dummy = 0;
+                volatile int* no_abort = &dummy;
+                for (int l = max(0, n - kUBufs); l < n; ++l)
+                    tc::mbar_wait(&bar.ufull[l % kUBufs], (uint32_t)((l / kUBufs) & 1), no_abort, kWaitNs);
+            }
         }
         __syncwarp();
     } else {
