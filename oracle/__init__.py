@@ -1,7 +1,8 @@
 """CPU oracle for the DSpark decode-cycle hot path -- TEST INFRASTRUCTURE ONLY.
 
 A thin numpy/ctypes wrapper over ``dspark_oracle.cpp``, a plain single-threaded
-C++ restatement of the cycle in double precision (Markov-head draft, lossless
+C++ restatement of the cycle in double precision (Markov-head draft, from given
+base logits or from the drafter's hidden states and shared lm_head, lossless
 verify with residual and bonus, survival and prefix selection, commit
 lengths, and the Philox4x32-10 generator they draw from).
 
@@ -79,6 +80,9 @@ def lib():
             L.orc_markov_draft.argtypes = [vp, i32, vp, vp, i32, vp, vp, vp, u32, f32,
                                            i32, i32, i32, i32, vp, vp, vp, vp, vp]
             L.orc_markov_draft.restype = i32
+            L.orc_fused_draft.argtypes = [vp, vp, i32, i32, vp, vp, i32, vp, vp, vp, u32, f32,
+                                          i32, i32, i32, i32, vp, vp, vp, vp, vp]
+            L.orc_fused_draft.restype = i32
             L.orc_verify.argtypes = [vp, vp, vp, vp, vp, vp, u32, f32, i32, i32, i32,
                                      vp, vp, vp, vp, vp, vp]
             L.orc_verify.restype = i32
@@ -192,6 +196,34 @@ def markov_draft(U, W1, W2, anchor, seeds, cycle, temperature, req_ids=None,
     st = lib().orc_markov_draft(_p(U), _wdtype(U), _p(W1), _p(W2), _wdtype(W2), _p(anchor),
                                 _p(seeds), _p(rid), cycle, temperature, R, gamma, V, rank,
                                 _p(y), _p(q_lse), _p(q_tok), _p(q_logits), _p(margin))
+    return dict(status=st, y=y, q_lse=q_lse, q_tok=q_tok, q_logits=q_logits, margin=margin)
+
+
+def fused_draft(h, W_lm, W1, W2, anchor, seeds, cycle, temperature, req_ids=None,
+                want_logits=True):
+    """Draft gamma tokens per request with the base logits formed from the
+    drafter's hidden states and the shared lm_head: U[r,k,v] = <W_lm[v], h[r,k]>.
+    h: [R,gamma,d], W_lm: [V,d], both float32 or both bf16 bits."""
+    h = np.ascontiguousarray(h)
+    W_lm = np.ascontiguousarray(W_lm)
+    W1 = np.ascontiguousarray(W1)
+    W2 = np.ascontiguousarray(W2)
+    assert W1.dtype == W2.dtype and h.dtype == W_lm.dtype
+    R, gamma, d = h.shape
+    V = W_lm.shape[0]
+    assert W_lm.shape[1] == d and W2.shape[0] == V
+    rank = W2.shape[1]
+    anchor = _c(anchor, np.int32)
+    seeds = _c(seeds, np.uint64)
+    rid = None if req_ids is None else _c(req_ids, np.int32)
+    y = np.zeros((R, gamma), np.int32)
+    q_lse = np.zeros((R, gamma), np.float64)
+    q_tok = np.zeros((R, gamma), np.float64)
+    margin = np.zeros((R, gamma), np.float64)
+    q_logits = np.zeros((R, gamma, V), np.float64) if want_logits else None
+    st = lib().orc_fused_draft(_p(h), _p(W_lm), _wdtype(h), d, _p(W1), _p(W2), _wdtype(W2), _p(anchor),
+                               _p(seeds), _p(rid), cycle, temperature, R, gamma, V, rank,
+                               _p(y), _p(q_lse), _p(q_tok), _p(q_logits), _p(margin))
     return dict(status=st, y=y, q_lse=q_lse, q_tok=q_tok, q_logits=q_logits, margin=margin)
 
 

@@ -134,9 +134,11 @@ double bf16_to_double(uint16_t b) {
 }
 
 // Element read for the two storage types the library accepts: 0 = fp32,
-// 1 = bf16 (raw 16-bit patterns).
+// 1 = bf16 (raw 16-bit patterns); 2 = double, for base logits that the
+// oracle forms itself (orc_fused_draft).
 double load_elem(const void* base, int dtype, size_t idx) {
     if (dtype == 0) return (double)((const float*)base)[idx];
+    if (dtype == 2) return ((const double*)base)[idx];
     return bf16_to_double(((const uint16_t*)base)[idx]);
 }
 
@@ -327,6 +329,40 @@ int orc_markov_draft(const void* U, int u_dtype, const void* W1, const void* W2,
         }
     }
     return ORC_OK;
+}
+
+// Block draft from the drafter's hidden states, with the base logits formed
+// here instead of given ([EXPL] section 6: the parallel backbone produces
+// every block position's hidden state in one pass, and the base logits U_k
+// come from it; [PR] description: the drafter shares the target's lm_head).
+// Written out:
+//   U[r][k][v] = sum_i W_lm[v][i] * h[r][k][i]     (double, i = 0 .. d-1 in order)
+// and then every step of orc_markov_draft on those base logits, so that
+//   s_v = (U[r][k][v] + sum_j W2[v][j] * W1[prev][j]) * invT
+// is one contraction over the concatenated K = d + rank.
+//   h     [R, gamma, d]   x_dtype (0 fp32, 1 bf16): hidden state of request r at
+//                         block position k (rows of the requests given, like U)
+//   W_lm  [V, d]          x_dtype: the shared lm_head, one row per vocabulary entry
+// Everything else, outputs included, as orc_markov_draft.
+int orc_fused_draft(const void* h, const void* W_lm, int x_dtype, int d, const void* W1,
+                    const void* W2, int w_dtype, const int32_t* anchor, const uint64_t* seeds,
+                    const int32_t* req_ids, uint32_t cycle, float temperature,
+                    int R, int gamma, int V, int rank,
+                    int32_t* y, double* q_lse, double* q_tok, double* q_logits, double* margin) {
+    if (R <= 0 || gamma <= 0 || V <= 0 || d <= 0 || rank <= 0) return ORC_INVALID;
+    std::vector<double> U((size_t)R * gamma * V);
+    for (int r = 0; r < R; ++r)
+        for (int k = 0; k < gamma; ++k) {
+            const size_t hrow = ((size_t)r * gamma + k) * d;
+            for (int v = 0; v < V; ++v) {
+                double acc = 0.0;
+                for (int i = 0; i < d; ++i)
+                    acc += load_elem(W_lm, x_dtype, (size_t)v * d + i) * load_elem(h, x_dtype, hrow + i);
+                U[((size_t)r * gamma + k) * V + v] = acc;
+            }
+        }
+    return orc_markov_draft(U.data(), 2, W1, W2, w_dtype, anchor, seeds, req_ids, cycle, temperature,
+                            R, gamma, V, rank, y, q_lse, q_tok, q_logits, margin);
 }
 
 // Lossless verification of R drafted blocks ([EXPL] section 2: verify left

@@ -28,6 +28,12 @@ pages are not available, so every tensor is synthetic):
   confidences from an independent stream; capture sizes 64..1024 with the
   synthetic step-rate staircase SPS(S) = 1/(10 ms + 20 us * S); K_cap = 1024;
   T = 1.0.
+* ``fused_logits``  the batched-sampling shape (R=128, V=151936, gamma=7,
+  rank=512, T=0.7) with the base logits formed from the drafter's hidden
+  states instead of given: h[R, gamma, d] ~ N(0, 1) bf16 with d = 4096 (the
+  hidden size of Qwen3-8B, whose vocabulary V is) and a shared lm_head
+  W_lm[V, d] ~ N(0, (3 / sqrt(d))^2) bf16, so that U = W_lm . h keeps the
+  N(0, 3^2) law of the other workloads; Markov factors as there.
 """
 from __future__ import annotations
 
@@ -55,6 +61,9 @@ WORKLOADS = {
                                  confidence=True, K_cap=1024,
                                  tau=[1.0, 1.1, 1.2, 1.3, 1.4],
                                  capture_sizes=[64, 128, 256, 512, 1024]),
+    "fused_logits": dict(index=5, R=128, V=151936, gamma=7, rank=512, d=4096, w_dtype="bf16",
+                         w_sigma=0.02, u_dtype="bf16", u_sigma=3.0, t_u=0.6, t_z=0.8 * 3.0,
+                         bonus_law="z", temperature=0.7),
 }
 
 
@@ -120,6 +129,25 @@ def draft_inputs(w: dict) -> dict:
     U = _store(_normal(rng(seed, 3), (R, gamma, V), w["u_sigma"]), w["u_dtype"])
     anchor = rng(seed, 4).integers(0, V, size=R, dtype=np.int64).astype(np.int32)
     return dict(W1=W1, W2=W2, U=U, anchor=anchor, seeds=request_seeds(seed, R),
+                temperature=np.float32(w["temperature"]))
+
+
+def fused_inputs(w: dict) -> dict:
+    """Drafter hidden states h [R, gamma, d] ~ N(0, 1) and the shared lm_head
+    W_lm [V, d] ~ N(0, (u_sigma / sqrt(d))^2), both bf16, with the Markov factors,
+    anchors and seeds of draft_inputs (streams 1, 2, 4 as there; h and W_lm from
+    streams 13 and 14, so no U is drawn)."""
+    R, V, gamma, rank, d, seed = w["R"], w["V"], w["gamma"], w["rank"], w["d"], w["seed"]
+    W1 = _store(_normal(rng(seed, 1), (V, rank), w["w_sigma"]), w["w_dtype"])
+    W2 = _store(_normal(rng(seed, 2), (V, rank), w["w_sigma"]), w["w_dtype"])
+    h = bf16_bits(_normal(rng(seed, 13), (R, gamma, d), 1.0))
+    W_lm = np.empty((V, d), np.uint16)
+    g = rng(seed, 14)
+    sig = w["u_sigma"] / np.sqrt(d)
+    for v0 in range(0, V, 8192):  # in slices: the fp32 draw of a full lm_head would double the memory
+        W_lm[v0:v0 + 8192] = bf16_bits(_normal(g, (min(8192, V - v0), d), sig))
+    anchor = rng(seed, 4).integers(0, V, size=R, dtype=np.int64).astype(np.int32)
+    return dict(W1=W1, W2=W2, h=h, W_lm=W_lm, anchor=anchor, seeds=request_seeds(seed, R),
                 temperature=np.float32(w["temperature"]))
 
 

@@ -171,3 +171,74 @@ def test_request_subset_replays_batch(orc):
                             req_ids=sub)
     assert (part["y"] == full["y"][sub]).all()
     np.testing.assert_array_equal(part["q_lse"], full["q_lse"][sub])
+
+
+# ---------------------------------------------------------------------------
+# Fused drafter logits: the base logits come from the drafter's hidden states
+# and the shared lm_head (explainer section 6: the parallel backbone gives every
+# block position its hidden state in one pass; PR 25173 description: the drafter
+# shares the target's lm_head), U[r,k,v] = <W_lm[v], h[r,k]>.
+
+def _fused_case(V=520, d=64, R=3, gamma=4, rank=16, T=0.7, seed=0):
+    w = inputs.workload("fused_logits", seed_offset=seed, R=R, V=V, gamma=gamma, rank=rank, d=d,
+                        w_sigma=0.3, temperature=T)
+    return w, inputs.fused_inputs(w)
+
+
+@pytest.mark.parametrize("T", [0.7, 0.0])
+def test_fused_draft_reduces_to_markov_draft_with_one_hot_lm_head(orc, T):
+    """With W_lm[v] the unit vector e_{(3v+1) mod d}, U[r,k,v] = h[r,k,(3v+1) mod d] exactly:
+    the fused draft must equal the pinned Markov draft given those base logits, output
+    for output (a wrong position, a transposed lm_head or a dropped bias all break it)."""
+    w, f = _fused_case(T=T)
+    V, d = w["V"], w["d"]
+    one = np.uint16(0x3F80)  # 1.0 in bf16
+    col = (3 * np.arange(V) + 1) % d
+    W_lm = np.zeros((V, d), np.uint16)
+    W_lm[np.arange(V), col] = one
+    U = np.ascontiguousarray(f["h"][:, :, col])  # bf16 bits, exact
+    got = orc.fused_draft(f["h"], W_lm, f["W1"], f["W2"], f["anchor"], f["seeds"], 9, T)
+    ref = orc.markov_draft(U, f["W1"], f["W2"], f["anchor"], f["seeds"], 9, T)
+    assert got["status"] == 0 and ref["status"] == 0
+    np.testing.assert_array_equal(got["y"], ref["y"])
+    np.testing.assert_array_equal(got["q_logits"], ref["q_logits"])
+    np.testing.assert_array_equal(got["q_lse"], ref["q_lse"])
+    np.testing.assert_array_equal(got["margin"], ref["margin"])
+    # the h of another position gives other base logits
+    U_shift = np.ascontiguousarray(np.roll(f["h"], 1, axis=1)[:, :, col])
+    other = orc.markov_draft(U_shift, f["W1"], f["W2"], f["anchor"], f["seeds"], 9, T)
+    assert not np.array_equal(other["q_logits"], got["q_logits"])
+
+
+def test_fused_draft_logits_are_one_contraction(orc):
+    """q_logits[r,k] = ([W_lm | W2] @ [h[r,k]; W1[prev]]) * invT with prev the anchor or the
+    previous draft, against numpy in float64; with V == d the transposed lm_head reading
+    gives a different vector."""
+    w, f = _fused_case(V=256, d=256, rank=32)
+    T = float(w["temperature"])
+    invT = float(np.float32(1.0) / np.float32(T))
+    out = orc.fused_draft(f["h"], f["W_lm"], f["W1"], f["W2"], f["anchor"], f["seeds"], 4, T)
+    h, Wl = _bf16_decode(f["h"]), _bf16_decode(f["W_lm"])
+    W1, W2 = _bf16_decode(f["W1"]), _bf16_decode(f["W2"])
+    K = np.concatenate([Wl, W2], axis=1)
+    for r in range(w["R"]):
+        prev = int(f["anchor"][r])
+        for k in range(w["gamma"]):
+            x = np.concatenate([h[r, k], W1[prev]])
+            np.testing.assert_allclose(out["q_logits"][r, k], (K @ x) * invT, rtol=1e-12, atol=1e-12)
+            wrong = (np.concatenate([Wl.T, W2], axis=1) @ x) * invT
+            assert not np.allclose(out["q_logits"][r, k], wrong)
+            prev = int(out["y"][r, k])
+
+
+def test_fused_draft_subset_replays_requests(orc):
+    """Rows given with req_ids draw the same tokens as in the whole batch (the subset mode the
+    full-size GPU tests replay)."""
+    w, f = _fused_case(R=5)
+    T = float(w["temperature"])
+    full = orc.fused_draft(f["h"], f["W_lm"], f["W1"], f["W2"], f["anchor"], f["seeds"], 2, T)
+    ids = np.array([1, 4], np.int32)
+    sub = orc.fused_draft(f["h"][ids], f["W_lm"], f["W1"], f["W2"], f["anchor"][ids], f["seeds"][ids], 2, T,
+                          req_ids=ids)
+    np.testing.assert_array_equal(sub["y"], full["y"][ids])
+    np.testing.assert_array_equal(sub["q_logits"], full["q_logits"][ids])
