@@ -59,8 +59,9 @@ def parse(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--stage", choices=["cycle", "draft", "verify"], default="cycle",
-                    help="time the whole cycle (default) or one call of it (profiling)")
+    ap.add_argument("--stage", choices=["cycle", "draft", "verify", "fused_draft"], default="cycle",
+                    help="time the whole cycle (default) or one call of it (profiling); fused_draft: "
+                         "the fused drafter logits on the fused_logits workload alone")
     ap.add_argument("--gamma", type=int, default=None, help="override the workload's block size")
     ap.add_argument("--temperature", type=float, default=None, help="override the workload's T")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -505,6 +506,87 @@ def side_workload(name, args, peaks):
     return out
 
 
+def fused_study(args, peaks, unfused_route=True, **over):
+    """The fused drafter logits (dspark_markov_draft_fused, q_logits not kept) on the
+    fused_logits workload (or a variant): one draft call per step, timed in blocks
+    like the cycle.  Beside it, for context, the route it replaces: the lm_head GEMM
+    writing U (torch.matmul, i.e. cuBLAS, bf16 out) followed by dspark_markov_draft."""
+    import torch
+    from speculative_decoding_dspark_gb300 import binding as B
+    w = inputs.workload("fused_logits", **over)
+    f = inputs.fused_inputs(w)
+    R, V, gamma, rank, d = w["R"], w["V"], w["gamma"], w["rank"], w["d"]
+    T = float(w["temperature"])
+
+    def dev(x):
+        x = np.ascontiguousarray(x)
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+        if x.dtype == np.uint64:
+            return torch.from_numpy(x.view(np.int64)).cuda()
+        return torch.from_numpy(x).cuda()
+
+    t = {k: dev(f[k]) for k in ("h", "W_lm", "W1", "W2", "anchor", "seeds")}
+    del f
+    stream = torch.cuda.Stream()
+    y = torch.empty((R, gamma), dtype=torch.int32, device="cuda")
+    q_lse = torch.empty((R, gamma), device="cuda")
+    q_tok = torch.empty((R, gamma), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_DRAFT_FUSED, R, gamma, V, rank, 0, B.DSPARK_BF16, 0))
+    ws_u = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_DRAFT, R, gamma, V, rank, 0, B.DSPARK_BF16, 0))
+    U = torch.empty((R, gamma, V), dtype=torch.bfloat16, device="cuda")
+
+    def fused(c):
+        B.dspark_markov_draft_fused(t["h"], t["W_lm"], t["W1"], t["W2"], t["anchor"], t["seeds"], c, T, y,
+                                    q_lse, q_tok, None, ws, status, stream=stream)
+
+    def unfused(c):
+        torch.matmul(t["h"].view(R * gamma, d), t["W_lm"].t(), out=U.view(R * gamma, V))
+        B.dspark_markov_draft(U, t["W1"], t["W2"], t["anchor"], t["seeds"], c, T, y, q_lse, q_tok, None, ws_u,
+                              status, stream=stream)
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                fn(i)
+            torch.cuda.synchronize()
+            blocks, c = [], args.warmup
+            t_end = time.perf_counter() + SIDE_SECONDS
+            while (args.blocks is None and (not blocks or time.perf_counter() < t_end)) or \
+                    (args.blocks is not None and len(blocks) < args.blocks):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(args.steps):
+                    fn(c)
+                    c += 1
+                e1.record(stream)
+                torch.cuda.synchronize()
+                blocks.append(e0.elapsed_time(e1) / args.steps)
+        return statistics.median(blocks), len(blocks)
+
+    ms, nb = timed(fused)
+    assert int(status.item()) == 0, f"fused draft: device status {int(status.item())}"
+    ms_u = None
+    if unfused_route:
+        ms_u, _ = timed(unfused)
+        assert int(status.item()) == 0, f"unfused draft: device status {int(status.item())}"
+    hbm = peaks.get("hbm_gbs") or 6800.0
+    tens = peaks.get("bf16_tflops_sustained") or 1700.0
+    # algorithmic bytes: [W_lm | W2] once per position, h once
+    byts = gamma * V * (d + rank) * 2 + R * gamma * d * 2
+    fl = 2.0 * R * V * (d + rank) * gamma
+    del t, U
+    torch.cuda.empty_cache()
+    return {"R": R, "V": V, "gamma": gamma, "rank": rank, "d": d, "temperature": T, "blocks": nb,
+            "steps_per_block": args.steps, "metric": "fused draft calls/s", "value": 1000.0 / ms,
+            "draft_ms": ms, "algorithmic_bytes": byts, "achieved_gbs": byts / (ms / 1e3) / 1e9,
+            "frac_hbm": byts / (ms / 1e3) / 1e9 / hbm, "flops": fl, "achieved_tflops": fl / (ms / 1e3) / 1e12,
+            "frac_tensor": fl / (ms / 1e3) / 1e12 / tens, "tensor_peak": "bf16_tflops_sustained (measured)",
+            "unfused_route_ms": ms_u,
+            "unfused_route": "cuBLAS lm_head GEMM (torch.matmul, bf16 U written) + dspark_markov_draft"}
+
+
 PLAN_MODES = [("fixed", 0, 0.0), ("history", 1, 0.0), ("current", 2, 0.0), ("first_stop", 3, 0.0),
               ("conf_cutoff_0.6", 4, 0.6), ("conf_cutoff_0.3", 4, 0.3), ("survival_cutoff_0.3", 5, 0.3)]
 
@@ -733,6 +815,8 @@ def run_ours(args):
         torch.cuda.empty_cache()
         side = {name: side_workload(name, args, peaks)
                 for name in ("confidence_scheduled", "varlen_verify", "qwen3_8b_greedy")}
+        side["fused_logits"] = fused_study(args, peaks)
+        side["fused_logits_R512"] = fused_study(args, peaks, R=512, V=129280, gamma=5, temperature=1.0)
         side["planner"] = planner_study()
         side["calibration"] = calibration_study()
         side["kv_bookkeeping"] = kv_study()
@@ -891,7 +975,9 @@ def measure_e2e(cyc, args, world, host_target=True):
 
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.impl == "ours" and args.stage == "fused_draft":
+        print(json.dumps({"stage": "fused_draft", **fused_study(args, load_peaks(), unfused_route=False)}), flush=True)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -87,6 +87,10 @@ typedef struct CUstream_st* dspark_stream_t;
 #define DSPARK_OP_SELECT 2
 #define DSPARK_OP_VERIFY_MARKOV 3
 #define DSPARK_OP_CALIBRATE 4
+#define DSPARK_OP_DRAFT_FUSED 5
+
+/* Largest hidden size dspark_markov_draft_fused takes. */
+#define DSPARK_FUSED_MAX_D 16384
 
 /* ---- dspark_workspace_size flags for DSPARK_OP_VERIFY_MARKOV --------------------- */
 #define DSPARK_VERIFY_HOST_TARGET 1u /* target_logits will be pinned host memory */
@@ -117,7 +121,8 @@ const char* dspark_status_string(int status);
 
 /* Library version, major * 10000 + minor * 100 + patch (1.1.0: cutoff modes,
  * conf_min in dspark_select_prefix, dspark_plan_cycles, the wait settings,
- * dspark_fit_temperatures, dspark_kv_reserve and dspark_kv_commit). */
+ * dspark_fit_temperatures, dspark_kv_reserve and dspark_kv_commit; 1.2.0:
+ * dspark_markov_draft_fused). */
 int dspark_version(void);
 
 /* Bytes of workspace one call of `op` needs for these sizes (0 on bad
@@ -182,6 +187,39 @@ int dspark_markov_draft(const void* U, int u_dtype, const void* W1, const void* 
                         int rank, int32_t* draft_tokens, float* q_lse, float* q_tok,
                         float* q_logits, unsigned flags, void* ws, size_t ws_bytes,
                         int32_t* dev_status, dspark_stream_t stream);
+
+/*
+ * dspark_markov_draft_fused -- the block draft with the drafter's logits formed
+ * in one contraction from its hidden states (explainer section 6: the parallel
+ * backbone gives every block position's hidden state in one pass, the base
+ * logits come from it; PR 25173 description: the drafter shares the target's
+ * lm_head, bias(prev) = markov_w2 . markov_w1[prev]).
+ *
+ * Exactly dspark_markov_draft with
+ *   U[r][k][v] = sum_i W_lm[v][i] * h[r][k][i]
+ * except that U is never stored: per position the kernel contracts
+ * [W_lm | W2] (V x (d + rank)) with [h[r][k] ; W1[prev]] in one fp32
+ * accumulator, so U keeps fp32 precision instead of a bf16 rounding.  It reads
+ * W_lm once per position (gamma * V * d * 2 bytes), so it pays off against
+ * writing and reading U (R * gamma * V * 2 bytes twice, plus a separate lm_head
+ * GEMM) where the contraction is tensor-bound, i.e. at large R.
+ *
+ *   h          [R, gamma, d]  bf16: hidden state of request r at block position k
+ *   W_lm       [V, d]         bf16: the lm_head shared with the target
+ *   d          hidden size, a multiple of 64, <= DSPARK_FUSED_MAX_D
+ *   W1, W2     [V, rank]      bf16 Markov factors (rank % 64 == 0, rank <= 512)
+ *   everything else as dspark_markov_draft (V % 8 == 0; at most 128 requests
+ *   per SM of the current device; h, W_lm, W1, W2 16-byte aligned).
+ *   ws, ws_bytes  workspace of dspark_workspace_size(DSPARK_OP_DRAFT_FUSED, R,
+ *                 gamma, V, rank, 0, DSPARK_BF16, 0) bytes
+ * Tensor cores only: shapes outside these limits return DSPARK_ERR_UNSUPPORTED
+ * (there is no CUDA-core variant).
+ */
+int dspark_markov_draft_fused(const void* h, const void* W_lm, int d, const void* W1, const void* W2,
+                              const int32_t* anchor, const uint64_t* seeds, uint32_t cycle,
+                              float temperature, int R, int gamma, int V, int rank,
+                              int32_t* draft_tokens, float* q_lse, float* q_tok, float* q_logits,
+                              void* ws, size_t ws_bytes, int32_t* dev_status, dspark_stream_t stream);
 
 /*
  * dspark_verify -- lossless left-to-right verification (explainer sections

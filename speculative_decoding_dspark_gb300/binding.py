@@ -30,6 +30,8 @@ DSPARK_ERR_BOUNDS = -8
 
 DSPARK_F32, DSPARK_BF16 = 0, 1
 DSPARK_OP_DRAFT, DSPARK_OP_VERIFY, DSPARK_OP_SELECT, DSPARK_OP_VERIFY_MARKOV, DSPARK_OP_CALIBRATE = 0, 1, 2, 3, 4
+DSPARK_OP_DRAFT_FUSED = 5
+DSPARK_FUSED_MAX_D = 16384
 DSPARK_DRAFT_FORCE_SIMT = 1
 DSPARK_VERIFY_HOST_TARGET = 1
 DSPARK_SELECT_FIXED, DSPARK_SELECT_HISTORY, DSPARK_SELECT_CURRENT, DSPARK_SELECT_FIRST_STOP = 0, 1, 2, 3
@@ -40,7 +42,8 @@ EXPORTED = ["dspark_status_string", "dspark_version", "dspark_workspace_size", "
             "dspark_markov_draft_uses_tensor_cores", "dspark_markov_draft", "dspark_verify",
             "dspark_select_prefix", "dspark_commit_lengths", "dspark_verify_static_scratch",
             "dspark_verify_markov", "dspark_set_wait_limit_ns", "dspark_set_fault_injection",
-            "dspark_plan_cycles", "dspark_fit_temperatures", "dspark_kv_reserve", "dspark_kv_commit"]
+            "dspark_plan_cycles", "dspark_fit_temperatures", "dspark_kv_reserve", "dspark_kv_commit",
+            "dspark_markov_draft_fused"]
 
 
 class DSparkError(RuntimeError):
@@ -65,6 +68,9 @@ def _load():
     L.dspark_markov_draft.argtypes = [vp, i32, vp, vp, i32, vp, vp, u32, f32, i32, i32, i32, i32,
                                       vp, vp, vp, vp, ctypes.c_uint, vp, sz, vp, vp]
     L.dspark_markov_draft.restype = i32
+    L.dspark_markov_draft_fused.argtypes = [vp, vp, i32, vp, vp, vp, vp, u32, f32, i32, i32, i32, i32,
+                                            vp, vp, vp, vp, vp, sz, vp, vp]
+    L.dspark_markov_draft_fused.restype = i32
     L.dspark_verify.argtypes = [vp, vp, vp, vp, vp, vp, vp, u32, f32, i32, i32, i32, i32,
                                 vp, vp, vp, vp, sz, vp, vp]
     L.dspark_verify.restype = i32
@@ -200,6 +206,30 @@ def dspark_markov_draft(U, W1, W2, anchor, seeds, cycle, temperature, draft_toke
                                 _ptr(q_logits), int(flags), _ptr(ws), ws.numel(),
                                 _ptr(dev_status), _stream(stream))
     _raise("dspark_markov_draft", st)
+
+
+def dspark_markov_draft_fused(h, W_lm, W1, W2, anchor, seeds, cycle, temperature, draft_tokens, q_lse=None,
+                              q_tok=None, q_logits=None, ws=None, dev_status=None, stream=None):
+    R, gamma, d = h.shape
+    V = W_lm.shape[0]
+    rank = W1.shape[1]
+    _check(h, "h", torch.bfloat16, (R, gamma, d))
+    _check(W_lm, "W_lm", torch.bfloat16, (V, d))
+    _check(W1, "W1", torch.bfloat16, (V, rank))
+    _check(W2, "W2", torch.bfloat16, (V, rank))
+    _check(anchor, "anchor", torch.int32, (R,))
+    _check(seeds, "seeds", torch.int64, (R,), allow_none=True)
+    _check(draft_tokens, "draft_tokens", torch.int32, (R, gamma))
+    _check(q_lse, "q_lse", torch.float32, (R, gamma), allow_none=True)
+    _check(q_tok, "q_tok", torch.float32, (R, gamma), allow_none=True)
+    _check(q_logits, "q_logits", torch.float32, (R, gamma, V), allow_none=True)
+    _check(ws, "ws", torch.uint8)
+    _check(dev_status, "dev_status", torch.int32, allow_none=True)
+    st = _L.dspark_markov_draft_fused(_ptr(h), _ptr(W_lm), d, _ptr(W1), _ptr(W2), _ptr(anchor), _ptr(seeds),
+                                      int(cycle), float(temperature), R, gamma, V, rank, _ptr(draft_tokens),
+                                      _ptr(q_lse), _ptr(q_tok), _ptr(q_logits), _ptr(ws), ws.numel(),
+                                      _ptr(dev_status), _stream(stream))
+    _raise("dspark_markov_draft_fused", st)
 
 
 def dspark_verify(target_logits, cu_seqlens, draft_tokens, q_logits, q_lse, q_tok, seeds, cycle,

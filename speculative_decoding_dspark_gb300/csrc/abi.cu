@@ -123,7 +123,7 @@ const char* dspark_status_string(int status) {
     }
 }
 
-int dspark_version(void) { return 10100; }
+int dspark_version(void) { return 10200; }
 
 int dspark_markov_draft_uses_tensor_cores(int u_dtype, int w_dtype, int R, int V, int rank,
                                           unsigned flags) {
@@ -148,6 +148,9 @@ size_t dspark_workspace_size(int op, int R, int gamma, int V, int rank, int max_
             // a host-resident target keeps each request's latest row on the device
             return (flags & DSPARK_VERIFY_HOST_TARGET) ? align_up(base) + align_up(sizeof(float) * (size_t)R * V) : base;
         }
+        case DSPARK_OP_DRAFT_FUSED:
+            if (V <= 0 || rank <= 0 || gamma <= 0) return 0;
+            return draft_tc_workspace(R, gamma, rank);
         case DSPARK_OP_SELECT:
             return 0;
         default:
@@ -197,6 +200,34 @@ int dspark_markov_draft(const void* U, int u_dtype, const void* W1, const void* 
     p.parts = carve<DraftPartial>(ws, L.parts);
     p.bias = carve<float>(ws, L.bias);
     return cuda_status(launch_draft_simt(p, s));
+}
+
+int dspark_markov_draft_fused(const void* h, const void* W_lm, int d, const void* W1, const void* W2,
+                              const int32_t* anchor, const uint64_t* seeds, uint32_t cycle,
+                              float temperature, int R, int gamma, int V, int rank,
+                              int32_t* draft_tokens, float* q_lse, float* q_tok, float* q_logits,
+                              void* ws, size_t ws_bytes, int32_t* dev_status, dspark_stream_t stream) {
+    if (!h || !W_lm || !W1 || !W2 || !anchor || !draft_tokens) return DSPARK_ERR_INVALID_ARG;
+    if (R <= 0 || V <= 0 || rank <= 0 || d <= 0 || gamma <= 0 || gamma > 16) return DSPARK_ERR_INVALID_ARG;
+    if (!(temperature >= 0.0f) || temperature == INFINITY) return DSPARK_ERR_INVALID_ARG;
+    if (cycle >= (1u << 28)) return DSPARK_ERR_INVALID_ARG;
+    const bool greedy = temperature == 0.0f;
+    if (!greedy && (!seeds || !q_lse || !q_tok)) return DSPARK_ERR_INVALID_ARG;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return DSPARK_ERR_WORKSPACE;
+    // tensor cores only: the hidden size in whole 64-element k-blocks, the Markov
+    // factors as for the tensor-core draft
+    if (d % 64 != 0 || d > DSPARK_FUSED_MAX_D) return DSPARK_ERR_UNSUPPORTED;
+    if (!draft_tc_supported(DSPARK_BF16, DSPARK_BF16, R, V, rank) || !draft_tc_fits(R)) return DSPARK_ERR_UNSUPPORTED;
+    if (!aligned16(h) || !aligned16(W_lm) || !aligned16(W1) || !aligned16(W2)) return DSPARK_ERR_UNSUPPORTED;
+    if (ws_bytes < draft_tc_workspace(R, gamma, rank)) return DSPARK_ERR_WORKSPACE;
+    DraftTcArgs a;
+    a.U = nullptr; a.h = h; a.W_lm = W_lm; a.d = d;
+    a.W1 = W1; a.W2 = W2; a.anchor = anchor; a.seeds = seeds; a.cycle = cycle;
+    a.invT = greedy ? 1.0f : 1.0f / temperature; a.greedy = greedy;
+    a.R = R; a.gamma = gamma; a.V = V; a.rank = rank;
+    a.y = draft_tokens; a.q_lse = q_lse; a.q_tok = q_tok; a.q_logits = q_logits;
+    a.dev_status = dev_status; a.ws = ws;
+    return launch_draft_tc(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int dspark_verify(const float* target_logits, const int32_t* cu_seqlens,

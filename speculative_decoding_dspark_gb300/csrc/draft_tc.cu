@@ -58,6 +58,21 @@
 //     passes ahead; the epilogue works in four 32-column passes per tile, 8
 //     columns per thread.
 //
+// Fused drafter logits (a third instantiation of the draft): the base logits
+// are not given but formed in the same accumulator, U_k = W_lm . h_k with W_lm
+// the lm_head the drafter shares with the target and h_k the backbone's hidden
+// state at position k (explainer section 6; PR 25173 description), so one
+// contraction over K = d + rank gives the whole logit:
+//   s = [W_lm | W2] . [h_k ; W1[prev]].
+// Each vocabulary tile first runs d / 64 k-blocks whose ring stage (32 KB)
+// holds a W_lm block (B, TMA 2-D) and an h_k block (A, TMA 3-D, 128 requests
+// x 64 hidden elements, read from L2 after the first tile), both from shared
+// memory, then the rank / 64 W2 k-blocks with A = W1[prev] in tensor memory
+// as above.  No U is read or written: the U producer idles and the epilogue
+// takes the accumulator as the logit.  The MMA issuer waits for the step's A
+// rows only before its first W2 k-block, so the first tile's lm_head part
+// overlaps the hand-over between positions.
+//
 // Cross-CTA results need no merging pass: every CTA folds its winner into one
 // 64-bit key per request and step with atomicMax (order-preserving bits of
 // the score above the inverted index, so ties go to the lower index), and
@@ -146,6 +161,7 @@ struct TcParams {
     int greedy;
     int R, gamma, V, rank;
     int nb, P, n_tiles, n_stages, nkb;
+    int dkb;                   // fused drafter logits: 64-element k-blocks of the hidden size (else 0)
     const int32_t* anchor;
     float* q_logits;
     int32_t* y;                // draft outputs [R][gamma]
@@ -417,9 +433,14 @@ __device__ void residual_tokens_if_last(const TcParams& p, uint8_t* smem, Bars& 
     }
 }
 
-template <bool kRes>
+// tm_u: U [R, gamma, V] (draft), or for the fused draft the hidden states h
+// [R, gamma, d] (the same box: 64 elements x 1 position x 128 requests);
+// tm_wlm: the fused draft's lm_head [V, d] (unused otherwise).
+template <bool kRes, bool kFused = false>
 __global__ void __launch_bounds__(kThreads, 1)
-markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_u, const TcParams p) {
+markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_u,
+                 const __grid_constant__ CUtensorMap tm_wlm, const TcParams p) {
+    static_assert(!(kRes && kFused), "the residual recomputes from given base logits");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     // A lives in tensor memory.  Draft: quarter exchange | two U pass buffers |
@@ -429,8 +450,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
     uint8_t* sU = kRes ? smem : sX + kExchBytes;
     uint8_t* sRT = sU;
     uint8_t* sRU = sU + kResBufs * kResTBytes;
-    uint8_t* sB = sU + (kRes ? kResBufs * (kResTBytes + kResUBytes) : kUBufs * kUBufBytes);
-    Bars& bar = *reinterpret_cast<Bars*>(sB + p.n_stages * kTileBytes);
+    // fused: no U pass buffers; a ring stage holds B (W_lm or W2 block) then A (h block)
+    constexpr int kStage = kFused ? 2 * kTileBytes : kTileBytes;
+    uint8_t* sB = sU + (kRes ? kResBufs * (kResTBytes + kResUBytes) : (kFused ? 0 : kUBufs * kUBufBytes));
+    Bars& bar = *reinterpret_cast<Bars*>(sB + p.n_stages * kStage);
     ResShared& rsh = *reinterpret_cast<ResShared*>(&bar + 1);  // residual only
     DraftShared& dsh = *reinterpret_cast<DraftShared*>(&bar + 1);  // draft only
     float* g_share = &rsh.g_share[0][0];
@@ -470,6 +493,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
     if (warp == 0 && lane == 0) {
         tc::prefetch_tmap(&tm_w2);
         if (!kRes) tc::prefetch_tmap(&tm_u);
+        if (kFused) tc::prefetch_tmap(&tm_wlm);
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -497,10 +521,33 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         // loop measured 2-4 % faster at R = 128 with sampling (and as much slower
         // at R = 16 greedy); no load order or issue pacing that was tried explains
         // it, and it is kept for that case.
-        const int n_loads = n_tl * p.nkb;  // W2 stage loads
+        const int n_loads = n_tl * (p.dkb + p.nkb);  // stage loads
         int issued = 0;
         bool ok = true;
-        if (p.nb == 1) {
+        if constexpr (kFused) {
+            // per tile: d / 64 stages of (W_lm block, h block of the tile's step), then
+            // rank / 64 W2 stages; the same counters as below plus the step
+            const int nkt = p.dkb + p.nkb;
+            int s = 0, kb = 0, i = 0, t = cidx, step = 0;  // stage, k-block, local tile, tile, step
+            uint32_t ph = 0;
+            for (; issued < n_loads; ++issued) {
+                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.empty[s], ph ^ 1u, abort_flag, kWaitNs))) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* st = sB + s * kStage;
+                if (kb < p.dkb)
+                    tc::tma_load_2d_3d_elect(st, &tm_wlm, kb * kKB, t * kNV, st + kTileBytes, &tm_u, kb * kKB, step,
+                                             row0, &bar.full[s], 2u * kTileBytes);
+                else
+                    tc::tma_load_2d_elect(st, &tm_w2, &bar.full[s], (kb - p.dkb) * kKB, t * kNV, kTileBytes);
+                if (++s == S) { s = 0; ph ^= 1u; }
+                if (++kb == nkt) {
+                    kb = 0;
+                    if (++i == n_local) { i = 0; t = cidx; ++step; } else { t += p.P; }
+                }
+            }
+        } else if (p.nb == 1) {
             for (; issued < n_loads; ++issued) {
                 // load l goes to stage l % S, used for the (l / S)-th time
                 const int s = issued % S;
@@ -551,12 +598,15 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         const uint64_t desc0 = tc::smem_desc_sw128(tc::smem_u32(sB));
         const uint32_t a_base = tmem_base + kAcol;
         for (int k = 0; ok && k < n_steps; ++k) {
-            // the step's A rows, written by the epilogue warps
-            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.afull, (uint32_t)(k & 1), abort_flag, kWaitNs))) {
-                ok = false;
-                break;
+            // the step's A rows, written by the epilogue warps (fused: awaited before
+            // the first W2 k-block of the step, below)
+            if (!kFused) {
+                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.afull, (uint32_t)(k & 1), abort_flag, kWaitNs))) {
+                    ok = false;
+                    break;
+                }
+                tc::tc_fence_after();
             }
-            tc::tc_fence_after();
             for (int i = 0; ok && i < n_local; ++i) {
                 const int g = k * n_local + i;
                 const int a = g & 1;
@@ -567,6 +617,33 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                 }
                 tc::tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(a * kNV);
+                if constexpr (kFused) {
+                    // the lm_head part: A (h block) and B (W_lm block) both in the stage
+#pragma unroll 1
+                    for (int kb = 0; kb < p.dkb; ++kb) {
+                        if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.full[s], ph, abort_flag, kWaitNs))) {
+                            ok = false;
+                            break;
+                        }
+                        tc::tc_fence_after();
+                        const uint64_t bd = desc0 + (uint64_t)(s * (kStage >> 4));
+                        const uint64_t ad = bd + (uint64_t)(kTileBytes >> 4);
+#pragma unroll
+                        for (int j = 0; j < kKB / 16; ++j)
+                            tc::umma_bf16_elect(d, ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j), idesc, (kb | j) != 0);
+                        tc::umma_commit_elect(&bar.empty[s]);
+                        if (++s == S) { s = 0; ph ^= 1u; }
+                    }
+                    if (!ok) break;
+                    if (i == 0) {  // from here on the step's A rows are read
+                        if (!__all_sync(0xFFFFFFFFu,
+                                        tc::mbar_wait(&bar.afull, (uint32_t)(k & 1), abort_flag, kWaitNs))) {
+                            ok = false;
+                            break;
+                        }
+                        tc::tc_fence_after();
+                    }
+                }
 #pragma unroll
                 for (int kb = 0; kb < kMaxKb; ++kb) {
                     if (kb < p.nkb) {  // warp-uniform
@@ -575,11 +652,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                             break;
                         }
                         tc::tc_fence_after();
-                        const uint64_t bd = desc0 + (uint64_t)(s * (kTileBytes >> 4));
+                        const uint64_t bd = desc0 + (uint64_t)(s * (kStage >> 4));
 #pragma unroll
                         for (int j = 0; j < kKB / 16; ++j)  // A: K elements 64 kb + 16 j .. at column 32 kb + 8 j
                             tc::umma_bf16_ta_elect(d, a_base + (uint32_t)(32 * kb + 8 * j), bd + (uint64_t)(2 * j),
-                                                   idesc, (kb | j) != 0);
+                                                   idesc, kFused || (kb | j) != 0);
                         tc::umma_commit_elect(&bar.empty[s]);
                         if (++s == S) { s = 0; ph ^= 1u; }
                     }
@@ -599,7 +676,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         // .. + 63 of the tile, all 128 requests) into pass buffer n % kUBufs, up to
         // kUBufs passes ahead of the epilogue, across the steps of the launch
         // (deeper buffering measured no faster: the W2 ring is what bounds a tile).
-        if (!kRes) {
+        if (!kRes && !kFused) {
             const int n_pass = 2 * n_tl;
             int n = 0;
             int b = 0, half = 0, i = 0, step = 0, t = cidx;  // buffer, pass of the tile, local tile, step, tile
@@ -848,32 +925,37 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                     // this pass's base logits, then the buffer goes back to the U producer
                     // pass 2 g + h is in buffer (2 g + h) % kUBufs, filled for the
                     // ((2 g + h) / kUBufs)-th time
+                    // (fused: the accumulator already holds U + B)
                     const int un = 2 * g + h, ub = un % kUBufs;
-                    if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.ufull[ub], (uint32_t)((un / kUBufs) & 1), abort_flag,
-                                                               kWaitNs))) {
-                        tc::tmem_ld_wait();
-                        break;
+                    if constexpr (!kFused) {
+                        if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.ufull[ub], (uint32_t)((un / kUBufs) & 1),
+                                                                   abort_flag, kWaitNs))) {
+                            tc::tmem_ld_wait();
+                            break;
+                        }
+                        const uint4 q0 = *reinterpret_cast<const uint4*>(sU + ub * kUBufBytes + u_off0);
+                        const uint4 q1 = *reinterpret_cast<const uint4*>(sU + ub * kUBufBytes + u_off1);
+                        uw[0] = q0.x; uw[1] = q0.y; uw[2] = q0.z; uw[3] = q0.w;
+                        uw[4] = q1.x; uw[5] = q1.y; uw[6] = q1.z; uw[7] = q1.w;
                     }
-                    const uint4 q0 = *reinterpret_cast<const uint4*>(sU + ub * kUBufBytes + u_off0);
-                    const uint4 q1 = *reinterpret_cast<const uint4*>(sU + ub * kUBufBytes + u_off1);
-                    uw[0] = q0.x; uw[1] = q0.y; uw[2] = q0.z; uw[3] = q0.w;
-                    uw[4] = q1.x; uw[5] = q1.y; uw[6] = q1.z; uw[7] = q1.w;
                     tc::tmem_ld_wait();
                     if (h == 1) {  // both halves are in registers: hand the accumulator back
                         tc::tc_fence_before();
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&bar.tempty[a]);
                     }
+                    if constexpr (!kFused) {
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const uint32_t word = uw[c >> 1];
-                        const float u = __uint_as_float((c & 1) ? (word & 0xFFFF0000u) : (word << 16));
-                        sv[c] = u + sv[c];  // the logit before the temperature
+                        for (int c = 0; c < 16; ++c) {
+                            const uint32_t word = uw[c >> 1];
+                            const float u = __uint_as_float((c & 1) ? (word & 0xFFFF0000u) : (word << 16));
+                            sv[c] = u + sv[c];  // the logit before the temperature
+                        }
+                        // the values are in registers: the async proxy may overwrite the buffer
+                        tc::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&bar.uempty[ub]);
                     }
-                    // the values are in registers: the async proxy may overwrite the buffer
-                    tc::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&bar.uempty[ub]);
                     if (row_ok && nvalid > 0) {
                         if (qrow) {  // scaled logits s = (U + B) / T
                             const float sc = sampling ? p.invT : 1.0f;
@@ -1325,8 +1407,11 @@ bool encode_2d_bf16(EncodeTiled enc, CUtensorMap* m, const void* base, int inner
 
 // Shared launch setup of both modes: device limits, stage count, tensor maps,
 // the common parameter block.  Returns DSPARK_OK or an error status.
+// d > 0: the fused draft, with h [R, gamma, d] in place of U and the lm_head
+// W_lm [V, d] (tm_wlm; otherwise tm_wlm is a copy of tm_w2, unused).
 int prepare(EncodeTiled enc, const void* U, const void* W1, const void* W2, int R, int gamma, int V, int rank,
-            bool residual, TcParams& p, CUtensorMap& tm_w2, CUtensorMap& tm_u, int& grid, size_t& smem, int& n_sm) {
+            bool residual, const void* W_lm, int d, TcParams& p, CUtensorMap& tm_w2, CUtensorMap& tm_u,
+            CUtensorMap& tm_wlm, int& grid, size_t& smem, int& n_sm) {
     int dev = 0, max_smem = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DSPARK_ERR_CUDA;
@@ -1335,20 +1420,26 @@ int prepare(EncodeTiled enc, const void* U, const void* W1, const void* W2, int 
     const int nkb = rank / kKB;
     // A lives in tensor memory; shared memory holds the residual's staging
     // buffers, or the draft's quarter exchange and U pass buffers, then the ring
+    const bool fused = d > 0;
     const size_t fixed =
         1024 + sizeof(Bars) +
         (residual ? kShareBytes + (size_t)kResBufs * (kResTBytes + kResUBytes)
-                  : sizeof(DraftShared) + (size_t)kExchBytes + (size_t)kUBufs * kUBufBytes);
+                  : sizeof(DraftShared) + (size_t)kExchBytes + (fused ? 0 : (size_t)kUBufs * kUBufBytes));
     // the residual's end-of-step exchange reuses the drained W2 ring (at least two stages)
     static_assert(2 * kTileBytes >= 3 * kM * sizeof(TcPartial), "exchange larger than two ring stages");
-    if ((size_t)max_smem < fixed + 2 * kTileBytes) return DSPARK_ERR_UNSUPPORTED;
-    const int n_stages = (int)std::min<size_t>(kMaxStages, ((size_t)max_smem - fixed) / kTileBytes);
-    smem = fixed + (size_t)n_stages * kTileBytes;
+    const size_t stage = fused ? 2 * (size_t)kTileBytes : (size_t)kTileBytes;
+    if ((size_t)max_smem < fixed + 2 * stage) return DSPARK_ERR_UNSUPPORTED;
+    const int n_stages = (int)std::min<size_t>(kMaxStages, ((size_t)max_smem - fixed) / stage);
+    smem = fixed + (size_t)n_stages * stage;
 
     if (!encode_2d_bf16(enc, &tm_w2, W2, rank, V, kNV)) return DSPARK_ERR_CUDA;
+    tm_wlm = tm_w2;
+    if (fused && !encode_2d_bf16(enc, &tm_wlm, W_lm, d, V, kNV)) return DSPARK_ERR_CUDA;
     if (!residual) {
-        const cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)gamma, (cuuint64_t)R};
-        const cuuint64_t strides[2] = {(cuuint64_t)V * 2, (cuuint64_t)gamma * V * 2};
+        // U [R, gamma, V], or the fused draft's h [R, gamma, d]: boxes of 64 x 1 x 128
+        const int inner = fused ? d : V;
+        const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)gamma, (cuuint64_t)R};
+        const cuuint64_t strides[2] = {(cuuint64_t)inner * 2, (cuuint64_t)gamma * inner * 2};
         const cuuint32_t box[3] = {kKB, 1, kM};
         const cuuint32_t es[3] = {1, 1, 1};
         if (enc(&tm_u, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(U), dims, strides, box, es,
@@ -1371,6 +1462,7 @@ int prepare(EncodeTiled enc, const void* U, const void* W1, const void* W2, int 
     p.P = std::max(1, std::min(std::min(n_sm / p.nb, p.n_tiles), kMaxP));
     p.n_stages = n_stages;
     p.nkb = nkb;
+    p.dkb = fused ? d / kKB : 0;
     grid = p.P * p.nb;
     return DSPARK_OK;
 }
@@ -1408,10 +1500,12 @@ int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream) {
     const TcLayout L = tc_layout(a.R, a.gamma, false);
     unsigned char* w = static_cast<unsigned char*>(a.ws);
     TcParams p;
-    CUtensorMap tm_w2, tm_u;
+    CUtensorMap tm_w2, tm_u, tm_wlm;
     int grid = 0, n_sm = 0;
     size_t smem = 0;
-    const int st = prepare(enc, a.U, a.W1, a.W2, a.R, a.gamma, a.V, a.rank, false, p, tm_w2, tm_u, grid, smem, n_sm);
+    const bool fused = a.d > 0;
+    const int st = prepare(enc, fused ? a.h : a.U, a.W1, a.W2, a.R, a.gamma, a.V, a.rank, false, a.W_lm, a.d, p,
+                           tm_w2, tm_u, tm_wlm, grid, smem, n_sm);
     if (st != DSPARK_OK) return st;
     p.keys = reinterpret_cast<unsigned long long*>(w + L.keys);
     p.step_done = reinterpret_cast<unsigned*>(w + L.step_done);
@@ -1428,8 +1522,8 @@ int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream) {
     p.greedy = a.greedy;
     p.wait_ns = grid_wait_limit_ns();
     p.phantom = (fault_injection_mask() & DSPARK_INJECT_DRAFT_BARRIER) ? 1u : 0u;
-    if (cudaFuncSetAttribute(markov_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
+    auto kern = fused ? markov_tc_kernel<false, true> : markov_tc_kernel<false, false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DSPARK_ERR_CUDA;
     // keys, step counters and abort word in one piece
     if (cudaMemsetAsync(w, 0, L.zero_bytes, stream) != cudaSuccess) return DSPARK_ERR_CUDA;
@@ -1446,7 +1540,7 @@ int launch_draft_tc(const DraftTcArgs& a, cudaStream_t stream) {
     cfg.stream = stream;
     cfg.attrs = coop;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, markov_tc_kernel<false>, tm_w2, tm_u, p) != cudaSuccess) return DSPARK_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, tm_w2, tm_u, tm_wlm, p) != cudaSuccess) return DSPARK_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 
@@ -1456,10 +1550,11 @@ int launch_residual_tc(const ResidualTcArgs& a, cudaStream_t stream) {
     const TcLayout L = tc_layout(a.R, a.gamma, true);
     unsigned char* w = static_cast<unsigned char*>(a.ws);
     TcParams p;
-    CUtensorMap tm_w2, tm_u;
+    CUtensorMap tm_w2, tm_u, tm_wlm;
     int grid = 0, n_sm = 0;
     size_t smem = 0;
-    const int st = prepare(enc, a.U, a.W1, a.W2, a.R, a.gamma, a.V, a.rank, true, p, tm_w2, tm_u, grid, smem, n_sm);
+    const int st = prepare(enc, a.U, a.W1, a.W2, a.R, a.gamma, a.V, a.rank, true, nullptr, 0, p, tm_w2, tm_u, tm_wlm,
+                           grid, smem, n_sm);
     if (st != DSPARK_OK) return st;
     ResRow* rows = reinterpret_cast<ResRow*>(w + L.rows);
     p.keys = reinterpret_cast<unsigned long long*>(w + L.keys);  // zeroed by the verify prologue
@@ -1476,7 +1571,7 @@ int launch_residual_tc(const ResidualTcArgs& a, cudaStream_t stream) {
     if (cudaFuncSetAttribute(markov_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return DSPARK_ERR_CUDA;
-    markov_tc_kernel<true><<<grid, kThreads, smem, stream>>>(tm_w2, tm_u, p);
+    markov_tc_kernel<true><<<grid, kThreads, smem, stream>>>(tm_w2, tm_u, tm_wlm, p);
     return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 

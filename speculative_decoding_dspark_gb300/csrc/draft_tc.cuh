@@ -8,6 +8,11 @@ namespace dspark {
 
 struct DraftTcArgs {
     const void* U;
+    // fused drafter logits (d > 0): hidden states h [R, gamma, d] and the shared
+    // lm_head W_lm [V, d] (bf16) in place of U
+    const void* h = nullptr;
+    const void* W_lm = nullptr;
+    int d = 0;
     const void* W1;
     const void* W2;
     const int32_t* anchor;

@@ -151,6 +151,37 @@ __device__ __forceinline__ void tma_load_3d_elect(void* dst, const CUtensorMap* 
         : "memory");
 }
 
+// Arm `bar` for `bytes` and start two tile loads on it: a 2-D box of map_b into
+// dst_b and a 3-D box of map_a into dst_a (the two operands of one k-block).
+__device__ __forceinline__ void tma_load_2d_3d_elect(void* dst_b, const CUtensorMap* map_b, int xb, int yb,
+                                                     void* dst_a, const CUtensorMap* map_a, int xa, int ya, int za,
+                                                     uint64_t* bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%2], %10;\n\t"
+        "@e cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];\n\t"
+        "@e cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%5], [%6, {%7, %8, %9}], [%2];\n\t}" ::"r"(smem_u32(dst_b)),
+        "l"(reinterpret_cast<uint64_t>(map_b)), "r"(smem_u32(bar)), "r"(xb), "r"(yb), "r"(smem_u32(dst_a)),
+        "l"(reinterpret_cast<uint64_t>(map_a)), "r"(xa), "r"(ya), "r"(za), "r"(bytes)
+        : "memory");
+}
+
+// D (+)= A . B^T with both operands described in shared memory (as umma_bf16),
+// issued by the elected lane.
+__device__ __forceinline__ void umma_bf16_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // D (+)= A . B^T with A in tensor memory (as umma_bf16_ta), issued by the elected lane.
 __device__ __forceinline__ void umma_bf16_ta_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
                                                    uint32_t accumulate) {

@@ -104,6 +104,42 @@ def gpu_draft(d: dict, temperature: float, cycle: int, flags: int = 0, want_logi
     return out
 
 
+def gpu_fused_draft(f: dict, temperature: float, cycle: int, want_logits: bool = True, dev_inputs=None):
+    """dspark_markov_draft_fused on the inputs of inputs.fused_inputs (dev_inputs: the same
+    arrays already on the device, keyed alike)."""
+    t = dev_inputs or {k: dev(f[k]) for k in ("h", "W_lm", "W1", "W2", "anchor", "seeds")}
+    R, gamma, d = t["h"].shape
+    V = t["W_lm"].shape[0]
+    rank = t["W1"].shape[1]
+    G = Guarded()
+    y = G.out((R, gamma), torch.int32, -7)
+    q_lse = G.out((R, gamma), torch.float32, float("nan"))
+    q_tok = G.out((R, gamma), torch.float32, float("nan"))
+    q_logits = G.out((R, gamma, V), torch.float32, float("nan")) if want_logits else None
+    ws = G.workspace(B.dspark_workspace_size(B.DSPARK_OP_DRAFT_FUSED, R, gamma, V, rank, 0, B.DSPARK_BF16, 0))
+    status = G.out((1,), torch.int32, 0)
+    B.dspark_markov_draft_fused(t["h"], t["W_lm"], t["W1"], t["W2"], t["anchor"], t["seeds"], cycle, temperature,
+                                y, q_lse, q_tok, q_logits, ws, status)
+    torch.cuda.synchronize()
+    G.check()
+    out = dict(y=host(y), q_lse=host(q_lse), q_tok=host(q_tok), status=int(status.item()))
+    out["q_logits_dev"] = q_logits
+    return out
+
+
+def fused_logit_tol(x: np.ndarray, d: int, rank: int, sigma_s: float) -> np.ndarray:
+    """Elementwise bound on |GPU - oracle| for the fused draft's scaled logits x (the
+    oracle's, in double).  The contraction runs as (d + rank) / 16 tensor-core MMAs
+    of K = 16 adding into one fp32 accumulator; allowing each addition to lose one
+    unit in the last place (2^-23 relative, an accumulator that truncates) at a
+    partial-sum magnitude up to |x| + sigma_s (sigma_s: the scale of the logits'
+    law, the partial sums' typical excursion past the final value) gives
+    ((d + rank) / 16 + 2) * 2^-23 * (|x| + sigma_s).  A dropped or repeated 64-wide
+    k-block, or one wrong operand element, moves a logit by far more."""
+    n_mma = (d + rank) // 16
+    return (n_mma + 2) * 2.0 ** -23 * (np.abs(x) + sigma_s)
+
+
 def gpu_verify(target, cu, y, q_logits, q_lse, q_tok, seeds, cycle, temperature, max_rows=None):
     """All array arguments may be numpy (copied) or CUDA tensors (used as is)."""
     t = lambda a: None if a is None else (a if isinstance(a, torch.Tensor) else dev(a))
