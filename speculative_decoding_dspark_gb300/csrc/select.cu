@@ -515,6 +515,43 @@ __global__ void __launch_bounds__(kNT) select_kernel(SelectParams p) {
     select_body(sm, p, io, false);
 }
 
+// The fixed capacity when it admits every candidate (K_cap - R >= R * gamma):
+// no ranking is needed, every request verifies all gamma drafts.  The same
+// outputs as select_body for that case (survival a, l = gamma, cu_seqlens,
+// K_used = R + R * gamma, or -1 everywhere after a confidence outside [0, 1]),
+// from a kernel small enough that its code is fetched quickly.
+__global__ void __launch_bounds__(kNT) select_all_kernel(SelectParams p) {
+    __shared__ int bad;
+    if (threadIdx.x == 0) bad = 0;
+    __syncthreads();
+    const int R = p.R, gamma = p.gamma;
+    for (int r = threadIdx.x; r < R; r += kNT) {
+        float cv[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) cv[k] = k < gamma ? p.c[(size_t)r * gamma + k] : 1.0f;
+        float run = 1.0f;
+        bool ok = true;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            if (k >= gamma) break;
+            ok = ok && (cv[k] >= 0.0f && cv[k] <= 1.0f);
+            run = (k == 0) ? cv[k] : run * cv[k];
+            if (p.a) p.a[(size_t)r * gamma + k] = run;
+        }
+        if (!ok) bad = 1;
+    }
+    __syncthreads();
+    const bool good = !bad;
+    for (int r = threadIdx.x; r <= R; r += kNT) {
+        if (r < R) p.l[r] = good ? gamma : -1;
+        if (p.cu) p.cu[r] = good ? r * (gamma + 1) : -1;
+    }
+    if (threadIdx.x == 0) {
+        p.K_used[0] = good ? R + R * gamma : -1;
+        if (!good) report(p.dev_status, DSPARK_ERR_DEVICE_INPUT);
+    }
+}
+
 // One cycle of a planning run per CTA (blockIdx.x = cycle t): the selection
 // of c_seq[t] (capacity from c_seq[t - lag] in HISTORY mode; K_cap in the
 // first lag cycles), then the cycle's predicted and achieved Theta, accepted
@@ -626,6 +663,10 @@ __global__ void __launch_bounds__(1024) commit_kernel(const int32_t* n_acc, cons
 }  // namespace
 
 cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
+    if (p.mode == DSPARK_SELECT_FIXED && (long long)p.K_cap - p.R >= (long long)p.R * p.gamma) {
+        select_all_kernel<<<1, kNT, 0, stream>>>(p);
+        return cudaGetLastError();
+    }
     const size_t smem = select_smem_bytes(p.R, p.R * p.gamma);
     cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);

@@ -637,8 +637,10 @@ def test_select_ties_and_errors(B, orc):
         np.testing.assert_array_equal(g["l"], o["l"])
         np.testing.assert_array_equal(g["cu_seqlens"], o["cu_seqlens"])
     bad = c.copy(); bad[2, 1] = np.nan
-    g = H.gpu_select(bad, None, None, None, 6, 0)
-    assert g["status"] == -6 and (g["l"] == -1).all()
+    for K_cap in (6, 9):  # a ranked selection; a capacity that admits every candidate
+        g = H.gpu_select(bad, None, None, None, K_cap, 0)
+        assert g["status"] == -6 and (g["l"] == -1).all() and (g["cu_seqlens"] == -1).all()
+        assert g["K_used"] == -1
     with pytest.raises(B.DSparkError):
         H.gpu_select(c, None, None, None, 2, 0)
 
