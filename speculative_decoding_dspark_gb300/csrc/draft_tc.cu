@@ -30,6 +30,9 @@
 //   B (N = 128 vocabulary rows x K = rank) = W2 tiles streamed by TMA through a
 //     ring of 16 KB stages (8, 128 KB in flight per SM; 6 to 12 measure alike,
 //     4 is slower; no L2 prefetch ahead of the ring, which only added traffic);
+//     the draft's W2 loads carry an L2 policy that keeps a fixed 30 % of W2's
+//     lines resident from one position to the next (evict_last) and marks the
+//     rest evict_first, and the U loads evict_first;
 //   D = A . B^T in fp32 tensor memory, two 128-column buffers so the epilogue
 //     of one vocabulary tile overlaps the MMAs of the next;
 //   U_k (draft) = the tile's base logits, by TMA into two 16 KB pass buffers
@@ -127,6 +130,12 @@ constexpr int kMaxP = 256;                    // CTAs per request block (pieces 
 constexpr uint32_t kTmemCols = 512;     // two 128-column accumulators, then the A rows (at most 256 columns)
 constexpr uint32_t kAcol = 256;         // first tensor-memory column of A
 constexpr uint64_t kWaitNs = 2000000000ull;
+// The draft's W2 loads keep this fraction of W2's lines resident in L2 from one
+// position to the next (the same lines every time; the rest, and every U load,
+// are first to be evicted): W2 is larger than L2, so plain LRU keeps none of it.
+// At the R = 128 bench shape 0.2, 0.3 and 0.4 measured 261.4, 261.1 and 262.3 us
+// per draft call, 0.6 272 us, and no hints 273.3 us.
+constexpr float kW2KeepFraction = 0.3f;
 constexpr float kLog2eF = 1.4426950408889634f;
 constexpr float kLn2F = 0.6931471805599453f;
 // Relative slack of the no-log race test, far above the rounding of the
@@ -521,6 +530,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         // loop measured 2-4 % faster at R = 128 with sampling (and as much slower
         // at R = 16 greedy); no load order or issue pacing that was tried explains
         // it, and it is kept for that case.
+        const uint64_t pol_w2 = tc::policy_keep_fraction(kW2KeepFraction);  // the draft's W2 (see above)
         const int n_loads = n_tl * (p.dkb + p.nkb);  // stage loads
         int issued = 0;
         bool ok = true;
@@ -558,7 +568,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                 }
                 const int g = issued / p.nkb, kb = issued - g * p.nkb;
                 const int t = tile_at(g, n_local, cidx, p.P);
-                tc::tma_load_2d_elect(sB + s * kTileBytes, &tm_w2, &bar.full[s], kb * kKB, t * kNV, kTileBytes);
+                if (!kRes)
+                    tc::tma_load_2d_elect_hint(sB + s * kTileBytes, &tm_w2, &bar.full[s], kb * kKB, t * kNV, kTileBytes,
+                                               pol_w2);
+                else
+                    tc::tma_load_2d_elect(sB + s * kTileBytes, &tm_w2, &bar.full[s], kb * kKB, t * kNV, kTileBytes);
             }
         } else {
             int s = 0, kb = 0, i = 0, t = cidx;  // stage, k-block, local tile, tile
@@ -568,7 +582,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
                     ok = false;
                     break;
                 }
-                tc::tma_load_2d_elect(sB + s * kTileBytes, &tm_w2, &bar.full[s], kb * kKB, t * kNV, kTileBytes);
+                if (!kRes)
+                    tc::tma_load_2d_elect_hint(sB + s * kTileBytes, &tm_w2, &bar.full[s], kb * kKB, t * kNV, kTileBytes,
+                                               pol_w2);
+                else
+                    tc::tma_load_2d_elect(sB + s * kTileBytes, &tm_w2, &bar.full[s], kb * kKB, t * kNV, kTileBytes);
                 if (++s == S) { s = 0; ph ^= 1u; }
                 if (++kb == p.nkb) {
                     kb = 0;
@@ -678,13 +696,14 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constan
         // (deeper buffering measured no faster: the W2 ring is what bounds a tile).
         if (!kRes && !kFused) {
             const int n_pass = 2 * n_tl;
+            const uint64_t pol_u = tc::policy_evict_first();  // each U_k is read once
             int n = 0;
             int b = 0, half = 0, i = 0, step = 0, t = cidx;  // buffer, pass of the tile, local tile, step, tile
             uint32_t uph = 0;
             for (; n < n_pass; ++n) {
                 if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bar.uempty[b], uph ^ 1u, abort_flag, kWaitNs))) break;
-                tc::tma_load_3d_elect(sU + b * kUBufBytes, &tm_u, &bar.ufull[b], t * kNV + 64 * half, step, row0,
-                                      (uint32_t)kUBufBytes);
+                tc::tma_load_3d_elect_hint(sU + b * kUBufBytes, &tm_u, &bar.ufull[b], t * kNV + 64 * half, step, row0,
+                                           (uint32_t)kUBufBytes, pol_u);
                 if (++b == kUBufs) { b = 0; uph ^= 1u; }
                 if (++half == 2) {
                     half = 0;

@@ -138,6 +138,47 @@ __device__ __forceinline__ void tma_load_2d_elect(void* dst, const CUtensorMap* 
         : "memory");
 }
 
+// L2 cache policies (createpolicy) for the hinted loads below.  Every line of a
+// load with policy_evict_first() is a first candidate for eviction;
+// policy_keep_fraction(f) marks the fraction f of the lines of an address range
+// (the same lines every time) evict_last, the rest evict_first.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t policy_keep_fraction(float f) {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.L2::evict_first.b64 %0, %1;" : "=l"(pol) : "f"(f));
+    return pol;
+}
+
+// As tma_load_2d_elect, with an L2 cache policy for the loaded lines.
+__device__ __forceinline__ void tma_load_2d_elect_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                                       uint32_t bytes, uint64_t pol) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%2], %5;\n\t"
+        "@e cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %6;\n\t}" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(bytes), "l"(pol)
+        : "memory");
+}
+
+// As tma_load_3d_elect, with an L2 cache policy for the loaded lines.
+__device__ __forceinline__ void tma_load_3d_elect_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                                       int z, uint32_t bytes, uint64_t pol) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%2], %6;\n\t"
+        "@e cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %7;\n\t}" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(bytes), "l"(pol)
+        : "memory");
+}
+
 // Arm `bar` for `bytes` and start the 3-D tile load into dst.
 __device__ __forceinline__ void tma_load_3d_elect(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
                                                   int z, uint32_t bytes) {
