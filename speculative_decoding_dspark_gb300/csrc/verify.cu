@@ -18,7 +18,7 @@
 //                    a grid barrier one warp per such request merges its units
 //                    and decides draft j (or, at j = l, takes the bonus row);
 //                    accepted requests go on to round j + 1 (published by a
-//                    second grid barrier; when at most 24 requests are active,
+//                    second grid barrier; when at most 16 requests are active,
 //                    every CTA decides all of them itself instead and only the
 //                    owner of a request writes its outputs).  Rows after the
 //                    first rejection are never read: with a weak drafter a
@@ -165,7 +165,12 @@ __device__ __forceinline__ bool grid_barrier(const VerifyParams& p, int* st, uns
     return s_ok != 0;
 }
 
-constexpr int kRoundThreads = 768;  // one CTA per SM: 24 warps, a grid barrier of n_sm arrivals
+// One CTA per SM, a grid barrier of n_sm arrivals.  16 warps of up to 128
+// registers: with 24 warps the stream loop spilled at the 80-register cap and
+// the verify call took 118.9 us at the R = 128 bench shape against 110.7 us
+// here (20 warps: 114.0; 12: 112.1; 12 or 8 warps with two units in flight
+// per warp instead of one: 114.6 and 125.7).
+constexpr int kRoundThreads = 512;
 constexpr int kRoundWarps = kRoundThreads / 32;
 constexpr size_t kMaxListBytes = sizeof(int) * DSPARK_VERIFY_MAX_R;  // the round's request list in shared memory
 
