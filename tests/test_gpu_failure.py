@@ -96,6 +96,22 @@ def test_draft_barrier_timeout(B):
     np.testing.assert_array_equal(again["q_lse"], ref["q_lse"])
 
 
+def test_fused_draft_barrier_timeout(B):
+    """The fused drafter logits share the draft's grid barrier between positions."""
+    w = inputs.workload("fused_logits", R=24, V=8192, gamma=4, rank=64, d=256, w_sigma=0.2)
+    f = inputs.fused_inputs(w)
+    ref = H.gpu_fused_draft(f, 0.7, 2, want_logits=False)
+    assert ref["status"] == 0
+    with injected(B, B.DSPARK_INJECT_DRAFT_BARRIER):
+        bad = H.gpu_fused_draft(f, 0.7, 2, want_logits=False)
+    assert bad["status"] == B.DSPARK_ERR_TIMEOUT
+    assert (bad["y"] == -7).all() and np.isnan(bad["q_lse"]).all() and np.isnan(bad["q_tok"]).all()
+    again = H.gpu_fused_draft(f, 0.7, 2, want_logits=False)
+    assert again["status"] == 0
+    np.testing.assert_array_equal(again["y"], ref["y"])
+    np.testing.assert_array_equal(again["q_lse"], ref["q_lse"])
+
+
 def test_static_scratch_timeout_after_a_normal_call(B):
     """The shared static scratch keeps the previous call's per-request rows; a
     call whose decision pass gives up must not draw from them."""

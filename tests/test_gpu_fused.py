@@ -147,3 +147,25 @@ def test_fused_draft_refusals(B):
     assert L.dspark_markov_draft_fused(*args(256, 576, 4096)) == B.DSPARK_ERR_UNSUPPORTED  # rank > 512
     assert L.dspark_markov_draft_fused(*args(256, 64, 4100)) == B.DSPARK_ERR_UNSUPPORTED  # V % 8
     assert L.dspark_markov_draft_fused(*args(0, 64, 4096)) == B.DSPARK_ERR_INVALID_ARG
+
+
+def test_fused_draft_anchor_edge_cases(B, orc):
+    """anchor -1: no bias at position 0 (the other reading of the anchor-first block); an
+    anchor >= V: that request's tokens are -1 and DSPARK_ERR_DEVICE_INPUT is reported, while
+    every other request is drafted as the oracle drafts it."""
+    T = 0.7
+    w, f = _case(seed=2, R=12, V=2056, gamma=3, rank=64, d=128, w_sigma=0.2, temperature=T)
+    anchor = f["anchor"].copy()
+    anchor[1] = -1
+    anchor[5] = -1
+    anchor[7] = w["V"] + 3
+    g = H.gpu_fused_draft(dict(f, anchor=anchor), T, 0)
+    assert g["status"] == B.DSPARK_ERR_DEVICE_INPUT
+    assert (g["y"][7] == -1).all() and np.isnan(g["q_lse"][7]).all()
+    rows = [i for i in range(w["R"]) if i != 7]
+    o = orc.fused_draft(f["h"][rows], f["W_lm"], f["W1"], f["W2"], anchor[rows], f["seeds"][rows], 0, T,
+                        req_ids=rows)
+    tally = H.Tally()
+    clean = _compare(tally, g, o, T, w, rows=rows)
+    tally.check()
+    assert len(clean) >= len(rows) - 1
