@@ -80,6 +80,10 @@ def test_workspace_sizes(lib):
     assert ws(0, 4, 0, 64, 8, 0, 0, 0) == 0
     # calibration: partial sums per position, independent of the sample count
     assert ws(4, 0, 5, 0, 0, 0, 0, 0) > 0 and ws(4, 0, 17, 0, 0, 0, 0, 0) == 0
+    # fused drafter logits: the tensor-core draft's keys, step counters and pieces
+    f = ws(5, 128, 7, 151936, 512, 0, 1, 0)
+    assert f >= 7 * 128 * 8 and f % 256 == 0
+    assert ws(5, 128, 0, 151936, 512, 0, 1, 0) == 0 and ws(5, 0, 7, 151936, 512, 0, 1, 0) == 0
 
 
 def test_host_argument_checks(lib):
@@ -104,6 +108,29 @@ def test_host_argument_checks(lib):
     assert f(*a) == -7          # misaligned workspace
     a = list(args); a[19] = 16
     assert f(*a) == -7          # workspace too small
+
+    fd = lib.dspark_markov_draft_fused
+    fd.restype = ctypes.c_int
+    fd.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, vp, ctypes.c_uint32, ctypes.c_float,
+                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp,
+                   vp, ctypes.c_size_t, vp, vp]
+    # h, W_lm, d, W1, W2, anchor, seeds, cycle, T, R, gamma, V, rank, y, q_lse, q_tok, q_logits, ws, bytes, status, stream
+    fargs = [fake, fake, 256, fake, fake, fake, fake, 0, 0.7, 4, 5, 4096, 64, fake, fake, fake, None,
+             vp(256 * 64), 1 << 20, None, None]
+    a = list(fargs); a[1] = None
+    assert fd(*a) == -1         # NULL lm_head
+    a = list(fargs); a[2] = 0
+    assert fd(*a) == -1         # no hidden size
+    a = list(fargs); a[6] = None
+    assert fd(*a) == -1         # sampling without seeds
+    a = list(fargs); a[10] = 17
+    assert fd(*a) == -1         # gamma > 16
+    a = list(fargs); a[17] = vp(4100)
+    assert fd(*a) == -7         # misaligned workspace
+    a = list(fargs); a[2] = 100
+    assert fd(*a) == -2         # hidden size not a multiple of 64
+    a = list(fargs); a[2] = 16384 + 64
+    assert fd(*a) == -2         # hidden size above DSPARK_FUSED_MAX_D
 
     s = lib.dspark_select_prefix
     s.restype = ctypes.c_int
