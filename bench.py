@@ -49,6 +49,7 @@ UNIT = "cycles/s"
 DEFAULT_WORKLOAD = "batched_sampling"
 BLOCK_SECONDS = 1.0  # timed blocks of K steps are repeated until this much time has passed
 SIDE_SECONDS = 0.3   # the same for each side workload
+STAGE_BLOCKS = 3     # blocks with an event between the calls of each step (per-stage times)
 
 
 def parse(argv=None):
@@ -405,28 +406,39 @@ class Cycle:
                                          self.status)
         if ev is not None: ev[4].record(s)
 
-    def timed_blocks(self, steps, first_cycle, seconds, n_blocks=None):
+    def timed_blocks(self, steps, first_cycle, seconds, n_blocks=None, stage_blocks=STAGE_BLOCKS):
         """Blocks of exactly `steps` steps, each bracketed by CUDA events on the
-        launching stream, repeated until `seconds` have passed (or n_blocks).
-        Returns (per-block ms, per-stage mean ms, steps run)."""
+        launching stream, repeated until `seconds` have passed (or n_blocks); then
+        `stage_blocks` more blocks with an event between the calls of every step,
+        which give the per-stage times (the timed blocks carry no events inside,
+        so the markers do not add to the measured time).
+        Returns (per-block ms, per-stage mean ms, steps in the timed blocks,
+        median ms of the blocks with stage events)."""
         torch = self.torch
-        blocks, evs_all, cyc = [], [], first_cycle
-        t_end = time.perf_counter() + seconds
-        while (n_blocks is None and (not blocks or time.perf_counter() < t_end)) or \
-                (n_blocks is not None and len(blocks) < n_blocks):
-            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+        blocks, evs_all, staged, cyc = [], [], [], first_cycle
+
+        def block(evs):
+            nonlocal cyc
             b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             b0.record(self.stream)
             for i in range(steps):
-                self.step(cyc, evs[i])
+                self.step(cyc, evs[i] if evs else None)
                 cyc += 1
             b1.record(self.stream)
             torch.cuda.synchronize()
-            blocks.append(b0.elapsed_time(b1))
+            return b0.elapsed_time(b1)
+
+        t_end = time.perf_counter() + seconds
+        while (n_blocks is None and (not blocks or time.perf_counter() < t_end)) or \
+                (n_blocks is not None and len(blocks) < n_blocks):
+            blocks.append(block(None))
+        for _ in range(max(1, stage_blocks)):
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+            staged.append(block(evs))
             evs_all.extend(evs)
         per = {k: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs_all)
                for j, k in enumerate(["select", "draft", "verify", "commit"])}
-        return blocks, per, cyc - first_cycle
+        return blocks, per, len(blocks) * steps, statistics.median(staged)
 
     def rows_read(self):
         """Target rows the last verify read: up to each request's first rejection."""
@@ -472,7 +484,7 @@ def side_workload(name, args, peaks):
         cyc.step(i)
     torch.cuda.synchronize()
     assert int(cyc.status.item()) == 0, f"{name}: device status {int(cyc.status.item())}"
-    blocks, per, n = cyc.timed_blocks(args.steps, args.warmup, SIDE_SECONDS)
+    blocks, per, n, _ = cyc.timed_blocks(args.steps, args.warmup, SIDE_SECONDS)
     ms_block = statistics.median(blocks)
     hbm = peaks.get("hbm_gbs") or 6800.0
     tens = peaks.get("bf16_tflops_sustained") or 1700.0
@@ -752,7 +764,7 @@ def run_ours(args):
     clocks = ClockSampler(local)
     time.sleep(0.3)
     t0 = time.perf_counter()
-    blocks, per, n_timed = cyc.timed_blocks(args.steps, args.warmup, BLOCK_SECONDS, args.blocks)
+    blocks, per, n_timed, ms_staged = cyc.timed_blocks(args.steps, args.warmup, BLOCK_SECONDS, args.blocks)
     wall = time.perf_counter() - t0
     clk = clocks.stop()
     if world > 1:
@@ -840,6 +852,8 @@ def run_ours(args):
                 "config": workload_config(w, world),
                 "timing": {"blocks": len(blocks), "steps_per_block": args.steps,
                            "block_ms_min_median_max": [min(blocks), ms_block, max(blocks)],
+                           "stage_event_block_ms_median": ms_staged,
+                           "stage_ms_from": f"{max(1, STAGE_BLOCKS)} further blocks with an event between the calls",
                            "rule": "median of timed blocks of exactly K steps, repeated for about "
                                    f"{BLOCK_SECONDS:g} s"},
                 "roofline": roof, "verify_roofline": verify_roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
