@@ -411,7 +411,10 @@ class Cycle:
         launching stream, repeated until `seconds` have passed (or n_blocks); then
         `stage_blocks` more blocks with an event between the calls of every step,
         which give the per-stage times (the timed blocks carry no events inside,
-        so the markers do not add to the measured time).
+        so the markers do not add to the measured time).  The timed blocks replay
+        one CUDA graph of the block's `steps` steps (captured once: every replay
+        runs the same cycles' kernels again); if the capture fails they launch on
+        the stream and self.launch_mode says why.
         Returns (per-block ms, per-stage mean ms, steps in the timed blocks,
         median ms of the blocks with stage events)."""
         torch = self.torch
@@ -428,16 +431,45 @@ class Cycle:
             torch.cuda.synchronize()
             return b0.elapsed_time(b1)
 
+        graph = None
+        try:
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+                for i in range(steps):
+                    self.step(first_cycle + i)
+            graph.replay()
+            torch.cuda.synchronize()
+            self.launch_mode = "cuda_graph"
+        except Exception as exc:  # noqa: BLE001 -- any capture failure falls back to the stream
+            graph = None
+            torch.cuda.synchronize()
+            self.launch_mode = "stream (graph capture failed: %s)" % str(exc).splitlines()[0][:160]
+            try:  # a call that picks up the failed capture's error state
+                self.step(first_cycle)
+            except Exception:  # noqa: BLE001
+                pass
+            torch.cuda.synchronize()
+
+        def graph_block():
+            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b0.record(self.stream)
+            graph.replay()
+            b1.record(self.stream)
+            torch.cuda.synchronize()
+            return b0.elapsed_time(b1)
+
         t_end = time.perf_counter() + seconds
         while (n_blocks is None and (not blocks or time.perf_counter() < t_end)) or \
                 (n_blocks is not None and len(blocks) < n_blocks):
-            blocks.append(block(None))
+            blocks.append(graph_block() if graph is not None else block(None))
         for _ in range(max(1, stage_blocks)):
             evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
             staged.append(block(evs))
             evs_all.extend(evs)
         per = {k: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs_all)
                for j, k in enumerate(["select", "draft", "verify", "commit"])}
+        assert int(self.status.item()) == 0, f"device status {int(self.status.item())} after the timed blocks"
         return blocks, per, len(blocks) * steps, statistics.median(staged)
 
     def rows_read(self):
@@ -765,6 +797,7 @@ def run_ours(args):
     time.sleep(0.3)
     t0 = time.perf_counter()
     blocks, per, n_timed, ms_staged = cyc.timed_blocks(args.steps, args.warmup, BLOCK_SECONDS, args.blocks)
+    launch_mode = cyc.launch_mode
     wall = time.perf_counter() - t0
     clk = clocks.stop()
     if world > 1:
@@ -853,6 +886,7 @@ def run_ours(args):
                 "timing": {"blocks": len(blocks), "steps_per_block": args.steps,
                            "block_ms_min_median_max": [min(blocks), ms_block, max(blocks)],
                            "stage_event_block_ms_median": ms_staged,
+                           "launch": launch_mode,
                            "stage_ms_from": f"{max(1, STAGE_BLOCKS)} further blocks with an event between the calls",
                            "rule": "median of timed blocks of exactly K steps, repeated for about "
                                    f"{BLOCK_SECONDS:g} s"},
