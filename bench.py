@@ -550,6 +550,93 @@ def side_workload(name, args, peaks):
     return out
 
 
+def graph_timed(torch, step, steps, warmup, seconds):
+    """Median ms of blocks of `steps` calls of step(cycle), each block one replayed
+    CUDA graph captured once (stream launches if the capture fails), after `warmup`
+    plain steps.  Returns (median block ms, blocks, launch mode)."""
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    graph, mode = None, "cuda_graph"
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+            for i in range(steps):
+                step(warmup + i)
+        graph.replay()
+        torch.cuda.synchronize()
+    except Exception as exc:  # noqa: BLE001 -- any capture failure falls back to the stream
+        graph, mode = None, "stream (graph capture failed: %s)" % str(exc).splitlines()[0][:160]
+        torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    blocks, t_end = [], time.perf_counter() + seconds
+    while not blocks or time.perf_counter() < t_end:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            for i in range(steps):
+                step(warmup + i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        blocks.append(e0.elapsed_time(e1))
+    return statistics.median(blocks), len(blocks), mode
+
+
+def tiny_study(args):
+    """The tiny exhaustive workload (R = 1, V = 64, gamma = 5, rank 8, fp32 factors and
+    base logits): select, the CUDA-core draft keeping its logits, the verify on stored
+    logits and commit, at T = 1 and greedy.  Bound by launch latency: microseconds per
+    cycle, no roofline fraction."""
+    import torch
+    from speculative_decoding_dspark_gb300 import binding as B
+
+    def dev(x):
+        x = np.ascontiguousarray(x)
+        if x.dtype == np.uint64:
+            return torch.from_numpy(x.view(np.int64)).cuda()
+        return torch.from_numpy(x).cuda()
+
+    out = {}
+    for T in (1.0, 0.0):
+        w = inputs.workload("tiny_exhaustive", temperature=T)
+        d, ci = inputs.draft_inputs(w), inputs.confidence_inputs(w)
+        R, V, gamma, rank = w["R"], w["V"], w["gamma"], w["rank"]
+        rows = R * (gamma + 1)
+        target = dev(inputs.target_full(w, d["U"]).reshape(rows, V))
+        U, W1, W2, anc, seeds, c = (dev(d["U"]), dev(d["W1"]), dev(d["W2"]), dev(d["anchor"]), dev(d["seeds"]),
+                                    dev(ci["c"]))
+        f32 = dict(device="cuda")
+        i32 = dict(dtype=torch.int32, device="cuda")
+        y, q_lse, q_tok = torch.empty((R, gamma), **i32), torch.empty((R, gamma), **f32), torch.empty((R, gamma), **f32)
+        q_logits = torch.empty((R, gamma, V), **f32)
+        a, l, cu, K = torch.empty((R, gamma), **f32), torch.empty(R, **i32), torch.empty(R + 1, **i32), torch.empty(1, **i32)
+        n_acc, outt, p_tok = torch.empty(R, **i32), torch.empty((R, gamma + 1), **i32), torch.empty((R, gamma), **f32)
+        cl, cuc, disc, tot = torch.empty(R, **i32), torch.empty(R + 1, **i32), torch.empty(R, **i32), torch.empty(1, **i32)
+        status = torch.zeros(1, **i32)
+        ws_d = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_DRAFT, R, gamma, V, rank, 0, B.DSPARK_F32))
+        ws_v = B.workspace(B.dspark_workspace_size(B.DSPARK_OP_VERIFY, R, gamma, V, 0, rows))
+        samp = T > 0
+
+        def step(cycle):
+            B.dspark_select_prefix(c, None, None, None, rows, B.DSPARK_SELECT_FIXED, a, l, cu, K, None, status)
+            B.dspark_markov_draft(U, W1, W2, anc, seeds if samp else None, cycle, T, y, q_lse, q_tok, q_logits,
+                                  ws_d, status)
+            B.dspark_verify(target, cu, y, q_logits if samp else None, q_lse if samp else None,
+                            q_tok if samp else None, seeds if samp else None, cycle, T, rows, n_acc, outt, p_tok,
+                            ws_v, status)
+            B.dspark_commit_lengths(n_acc, l, gamma, cl, cuc, disc, tot, status)
+
+        ms, nb, mode = graph_timed(torch, step, args.steps, args.warmup, SIDE_SECONDS)
+        assert int(status.item()) == 0, f"tiny_exhaustive: device status {int(status.item())}"
+        out["T%g" % T] = {"us_per_cycle": 1000.0 * ms / args.steps, "cycles_per_s": 1000.0 * args.steps / ms,
+                          "blocks": nb, "steps_per_block": args.steps, "launch": mode,
+                          "draft_path": "simt (fp32 factors, rank 8)"}
+    out.update({"R": 1, "V": 64, "gamma": 5, "rank": 8, "bound": "launch latency"})
+    return out
+
+
 def fused_study(args, peaks, unfused_route=True, **over):
     """The fused drafter logits (dspark_markov_draft_fused, q_logits not kept) on the
     fused_logits workload (or a variant): one draft call per step, timed in blocks
@@ -860,6 +947,7 @@ def run_ours(args):
         torch.cuda.empty_cache()
         side = {name: side_workload(name, args, peaks)
                 for name in ("confidence_scheduled", "varlen_verify", "qwen3_8b_greedy")}
+        side["tiny_exhaustive"] = tiny_study(args)
         side["fused_logits"] = fused_study(args, peaks)
         side["fused_logits_R512"] = fused_study(args, peaks, R=512, V=129280, gamma=5, temperature=1.0)
         side["planner"] = planner_study()

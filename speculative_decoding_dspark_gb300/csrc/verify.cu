@@ -27,6 +27,8 @@
 //   verify_correct   (T > 0) one CTA per (request, chunk) of the row the extra
 //                    token comes from: Gumbel-max over log max(0, p - q) or
 //                    over p; the last CTA of the request writes the token.
+#include <algorithm>
+
 #include "kernels.cuh"
 
 namespace dspark {
@@ -607,8 +609,12 @@ cudaError_t launch_verify_decide(const VerifyParams& p, cudaStream_t stream) {
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kRoundThreads, sizeof(int) * p.R);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
-    // every CTA resident at once (cooperative launch): the rounds meet at grid barriers
-    const int grid = n_sm;
+    // every CTA resident at once (cooperative launch): the rounds meet at grid barriers.
+    // One CTA per SM, but no more CTAs than round 0 has units for one per warp: a
+    // small batch (R = 1, V = 64: one unit) meets at a barrier of one CTA instead of
+    // one per SM.
+    const long long units0 = (long long)p.R * p.nsub;
+    const int grid = (int)std::min<long long>(n_sm, std::max<long long>(1, (units0 + kRoundWarps - 1) / kRoundWarps));
     const size_t smem = sizeof(int) * (size_t)p.R;
     VerifyParams arg = p;
     arg.wait_ns = grid_wait_limit_ns();
