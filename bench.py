@@ -14,10 +14,15 @@ independent, no collective is needed), the time is the max over ranks and
 
 Timing: after W warm-up steps, blocks of exactly K steps are timed with CUDA
 events on the launching stream, one block after another until about a second
-has passed; `value` comes from the median block.  The line also carries the
-other workloads of the pages (`workloads`: the DeepSeek-style R=512, gamma=5,
-rank-512 confidence-scheduled cycle with its tensor-core fraction, the
-variable-length verify timed alone, the greedy Qwen3-8B-shaped cycle).
+has passed; `value` comes from the median block.  Each timed block replays one
+CUDA graph of its K steps, captured once from the same library calls (stream
+launches if the capture fails; `timing.launch` says which); the per-stage times
+come from further stream-launched blocks with an event between the calls.  The
+line also carries the other workloads of the pages (`workloads`: the tiny
+exhaustive cycle in microseconds, the DeepSeek-style R=512, gamma=5, rank-512
+confidence-scheduled cycle with its tensor-core fraction, the variable-length
+verify timed alone, the greedy Qwen3-8B-shaped cycle, and the fused drafter
+logits beside the unfused route).
 
 `--impl reference` times the CPU oracle (single-threaded C++, one request per
 task) over a pool of host processes, one per core: each timed step is one
