@@ -169,3 +169,20 @@ def test_fused_draft_anchor_edge_cases(B, orc):
     clean = _compare(tally, g, o, T, w, rows=rows)
     tally.check()
     assert len(clean) >= len(rows) - 1
+
+
+def test_fused_draft_four_request_blocks_sampled(B, orc):
+    """R = 512 (four request blocks over the same vocabulary tiles, the tensor-bound case the
+    bench times), V = 129280, gamma = 5, d = 4096, rank 512, T = 1: the whole batch on the
+    GPU, one request of every block replayed on the oracle."""
+    w, f = _case(seed=3, R=512, V=129280, gamma=5, temperature=1.0)
+    T = 1.0
+    g = H.gpu_fused_draft(f, T, 4, want_logits=False)
+    assert g["status"] == 0
+    assert (g["y"] >= 0).all() and (g["y"] < w["V"]).all()
+    rows = [1, 200, 300, 511]
+    o = orc.fused_draft(f["h"][rows], f["W_lm"], f["W1"], f["W2"], f["anchor"][rows], f["seeds"][rows], 4, T,
+                        req_ids=rows)
+    tally = H.Tally()
+    _compare(tally, g, o, T, w, rows=rows, want_logits=False)
+    tally.check()
